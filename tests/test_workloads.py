@@ -1,0 +1,42 @@
+"""The seeded input generators: determinism, shapes and the workload recipes (degree, graph
+structure, value scales)."""
+import numpy as np
+import pytest
+
+from clebsch_gordan_tensor_receiver_gb300 import workloads
+
+
+def test_tiny_recipe_and_determinism():
+    a = workloads.make_workload(0)
+    b = workloads.make_workload(0)
+    assert np.array_equal(a.src, b.src) and np.array_equal(a.x, b.x) and np.array_equal(a.Y, b.Y)
+    assert a.n_edges == 800 and a.x.shape == (100, 16, 4) and a.Y.shape == (800, 9)
+    assert a.x.dtype == np.float32 and a.Y.dtype == np.float32
+    assert np.all(np.diff(a.recv) >= 0)
+    for r in range(100):
+        s = a.src[a.recv == r]
+        assert s.size == 8 and np.all(np.diff(s) > 0) and not np.any(s == r)
+    w = workloads.make_weights(a.spec, a.n_edges, 9)
+    assert w.shape == (800, 9, 16)
+    assert np.std(w) == pytest.approx(1 / np.sqrt(8), rel=0.05)
+    g = workloads.make_cotangent(a.spec, 100, 29)
+    assert g.shape == (100, 16, 29)
+
+
+def test_periodic_graph_small():
+    rng = np.random.default_rng(1)
+    recv, src, vec, box = workloads.periodic_graph(3000, 0.056, 5.0, rng)
+    assert np.all(np.diff(recv) >= 0)
+    deg = np.bincount(recv, minlength=3000)
+    assert deg.mean() == pytest.approx(0.056 * 4 / 3 * np.pi * 125, rel=0.05)
+    pairs = set(zip(recv.tolist(), src.tolist()))
+    assert all((s, r) in pairs for r, s in list(pairs)[:500])  # symmetric neighbour list
+    assert not np.any(recv == src)
+    np.testing.assert_allclose(np.linalg.norm(vec, axis=1), 1.0, atol=1e-12)
+
+
+def test_unit_vector_sh_normalisation():
+    v = workloads.unit_vectors(100, np.random.default_rng(2))
+    Y = workloads.sh_inputs(v, 3)
+    for l in range(4):
+        np.testing.assert_allclose((Y[:, l * l:(l + 1) ** 2] ** 2).sum(1), 2 * l + 1, atol=1e-12)
