@@ -1,0 +1,428 @@
+#!/usr/bin/env python
+"""Benchmark of the channel-wise (UVU) CG tensor-product graph convolution on GB300.
+
+One step = one pass of the hot path over the workload: the forward (uvu_fwd) and the full VJP
+(uvu_bwd_edge for dw and dY, then dx).  The graph preparation (receiver CSR and its transpose)
+is done once before timing, as in "Receiver-streaming convolutions for channel-wise UVU tensor
+products" (opening post, benchmark paragraph: graph construction outside the timed region), and
+reported separately.
+
+Prints one JSON line.  `value` is whole-job fwd+VJP edges/s with inputs resident in HBM;
+`e2e` is the same metric through the C ABI with the inputs copied from pinned host memory and
+all outputs copied back inside the timed region.  The roofline object describes the kernel with
+the largest share of the step: algorithmic bytes per launch / its CUDA-event duration.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--dx-mode sender|atomic]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on bounded samples
+Under torchrun (N > 1) every rank runs an independent replica of the workload on its own GPU
+(the operation is not sharded); timings are max-reduced over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "edges/sec fwd & fwd+VJP UVU conv (5k nodes/280k edges); % of HBM roofline"
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="uvu", choices=["uvu", "reference"])
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--dx-mode", default="sender", choices=["sender", "atomic"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------- bytes and units
+
+def algorithmic_bytes(N, E, U, P, Dx, Dy, Do, s):
+    """Compulsory bytes per launch of each kernel (every tensor read or written once)."""
+    idx_r = 4 * (N + 1) + 4 * E          # recv_offsets + src
+    idx_s = 4 * (N + 1) + 8 * E          # send_offsets + send_eids + send_recv
+    x, Y, w, out = N * U * Dx * s, E * Dy * s, E * P * U * s, N * U * Do * s
+    return {
+        "uvu_fwd": x + Y + w + out + idx_r,
+        "uvu_bwd_edge": x + Y + w + out + idx_r + Y + w,        # reads x,Y,w,d_out; writes dY,dw
+        "uvu_bwd_edge+atomic_dx": x + Y + w + out + idx_r + Y + w + x,
+        "uvu_bwd_dx": Y + w + out + idx_s + x,                  # reads Y,w,d_out; writes dx
+        "fwd": x + Y + w + out + idx_r,
+        "vjp": (x + Y + w + out + idx_r + idx_s) + (x + Y + w),
+    }
+
+
+def describe(spec, info, E):
+    return (f"{spec.name}: {spec.n_nodes} nodes, {E} edges, x {spec.irreps_x}, "
+            f"SH {spec.irreps_sh}, l3<={spec.lmax_out} ({info.n_paths} paths), {spec.dtype}")
+
+
+# ------------------------------------------------------------------------- clocks sampling
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------- distributed
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over the process group (identity for one process)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_sample(wl, w, g, lay, n_recv, seed):
+    """Time the oracle's fwd + VJP on a sample of receivers (fwd, dw, dY over their edges) and
+    senders (dx).  Returns (edges/s, description, threads)."""
+    import numpy as np
+    from oracle import conv, graph
+    rng = np.random.default_rng(seed)
+    N = wl.n_nodes
+    off = graph.recv_offsets(wl.recv, N)
+    rs = np.sort(rng.choice(N, size=min(n_recv, N), replace=False))
+    ss = np.sort(rng.choice(N, size=min(n_recv, N), replace=False))
+    edges = np.concatenate([np.arange(off[r], off[r + 1]) for r in rs])
+    n_send_edges = int(np.isin(wl.src, ss).sum())
+    t0 = time.perf_counter()
+    conv.fwd(lay, off, wl.src, wl.x, wl.Y, w, receivers=rs)
+    t1 = time.perf_counter()
+    conv.bwd_edges(lay, off, wl.src, wl.x, wl.Y, w, g, edges=edges)
+    t2 = time.perf_counter()
+    conv.bwd_dx(lay, off, wl.src, wl.Y, w, g, N, senders=ss)
+    t3 = time.perf_counter()
+    per_edge = (t1 - t0) / edges.size + (t2 - t1) / edges.size + (t3 - t2) / max(n_send_edges, 1)
+    desc = (f"oracle fwd+VJP: fwd and dw/dY over {rs.size} receivers ({edges.size} edges), dx over "
+            f"{ss.size} senders ({n_send_edges} edges); {t3 - t0:.1f} s wall")
+    return 1.0 / per_edge, desc, conv.default_threads()
+
+
+def run_reference(args):
+    rank, local_rank, world = dist_env()
+    if world > 1 and rank != 0:
+        return 0
+    from clebsch_gordan_tensor_receiver_gb300 import workloads
+    from oracle import paths
+    spec = workloads.SPECS[args.config]
+    wl = workloads.make_workload(spec)
+    lay = paths.layout(spec.irreps_x, spec.irreps_sh, spec.lmax_out)
+    w = workloads.make_weights(spec, wl.n_edges, len(lay.paths))
+    g = workloads.make_cotangent(spec, wl.n_nodes, lay.dim_out)
+    n_recv = 40
+    for i in range(args.warmup):
+        oracle_sample(wl, w, g, lay, n_recv, 500 + i)
+    rates, descs = [], []
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        r, d, thr = oracle_sample(wl, w, g, lay, n_recv, 900 + i)
+        rates.append(r)
+        descs.append(d)
+    wall = time.perf_counter() - t0
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "edges/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * wall / max(args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(spec, type("I", (), {"n_paths": len(lay.paths)}), wl.n_edges),
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "edges/s", "cores": thr, "kind": "oracle",
+                         "sample": descs[0]},
+        "e2e": {"value": value, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------------- GPU leg
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import numpy as np
+    import torch
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+
+    from clebsch_gordan_tensor_receiver_gb300 import uvu, workloads
+    spec = workloads.SPECS[args.config]
+    wl = workloads.make_workload(spec)
+    plan = uvu.Plan(spec.irreps_x, spec.irreps_sh, spec.lmax_out, spec.dtype)
+    info = plan.info
+    N, E, U, P = wl.n_nodes, wl.n_edges, info.mul, info.n_paths
+    Dx, Dy, Do = info.dim_x, info.dim_sh, info.dim_out
+    w_h = workloads.make_weights(spec, E, P)
+    g_h = workloads.make_cotangent(spec, N, Do)
+    tdt = torch.float64 if spec.dtype == "float64" else torch.float32
+    s = 8 if spec.dtype == "float64" else 4
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    x, Y, w, g = to_dev(wl.x), to_dev(wl.Y), to_dev(w_h), to_dev(g_h)
+    recv, src = to_dev(wl.recv), to_dev(wl.src)
+    stream = torch.cuda.current_stream(dev)
+
+    # graph preparation (untimed in the metric; reported separately)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    G = uvu.Graph(N, recv, src)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    csr_ms = t0.elapsed_time(t1)
+
+    out = torch.empty(N, U, Do, dtype=tdt, device=dev)
+    dx = torch.empty(N, U, Dx, dtype=tdt, device=dev)
+    dY = torch.empty(E, Dy, dtype=tdt, device=dev)
+    dw = torch.empty(E, P, U, dtype=tdt, device=dev)
+
+    def step(mode, evs=None):
+        if evs:
+            evs[0].record(stream)
+        plan.fwd(N, x, Y, w, G.recv_offsets, src, out, stream)
+        if evs:
+            evs[1].record(stream)
+        plan.bwd_edge(N, x, Y, w, G.recv_offsets, src, g, dY=dY, dw=dw,
+                      dx_atomic=dx if mode == "atomic" else None, stream=stream)
+        if evs:
+            evs[2].record(stream)
+        if mode == "sender":
+            plan.bwd_dx(N, E, Y, w, G.send_offsets, G.send_eids, G.send_recv, g, dx, stream)
+        if evs:
+            evs[3].record(stream)
+
+    def timed(mode, K):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(K):
+            step(mode, evs[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        total = start.elapsed_time(end)
+        per = {"uvu_fwd": [], "uvu_bwd_edge": [], "uvu_bwd_dx": []}
+        for e in evs:
+            per["uvu_fwd"].append(e[0].elapsed_time(e[1]))
+            per["uvu_bwd_edge"].append(e[1].elapsed_time(e[2]))
+            if mode == "sender":
+                per["uvu_bwd_dx"].append(e[2].elapsed_time(e[3]))
+        return total, {k: statistics.mean(v) for k, v in per.items() if v}
+
+    other = "atomic" if args.dx_mode == "sender" else "sender"
+    for _ in range(max(args.warmup, 3)):
+        step(args.dx_mode)
+        step(other)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    total_ms, kern_ms = timed(args.dx_mode, args.steps)
+    total_o, kern_o = timed(other, args.steps)
+    clk = clocks.stop()
+
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_step = total_ms / args.steps
+    value = world * E / (ms_step / 1000.0)
+
+    B = algorithmic_bytes(N, E, U, P, Dx, Dy, Do, s)
+    fwd_ms = kern_ms["uvu_fwd"]
+    vjp_ms = kern_ms["uvu_bwd_edge"] + kern_ms.get("uvu_bwd_dx", 0.0)
+    vjp_o = kern_o["uvu_bwd_edge"] + kern_o.get("uvu_bwd_dx", 0.0)
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+    hbm_peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if hbm_peak else "fallback"
+    hbm_peak = hbm_peak or 6800.0
+
+    def frac(bytes_, ms):
+        gbs = bytes_ / (ms / 1000.0) / 1e9
+        return gbs, gbs / hbm_peak
+
+    kernels = {}
+    for k, ms in kern_ms.items():
+        key = k
+        if k == "uvu_bwd_edge" and args.dx_mode == "atomic":
+            key = "uvu_bwd_edge+atomic_dx"
+        gbs, fr = frac(B[key], ms)
+        kernels[k] = {"ms": ms, "bytes": B[key], "GB_s": gbs, "frac": fr}
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        import hashlib
+        tj = json.load(open(tpath))
+        h = hashlib.sha256(plan.source()[0].encode()).hexdigest()[:16]
+        ent = tj.get(f"{spec.name}:{dom}:{args.dx_mode}")
+        if ent and ent.get("source_sha") == h:
+            traffic = ent["dram_bytes_per_launch"]
+    fwd_gbs, fwd_fr = frac(B["fwd"], fwd_ms)
+    vjp_gbs, vjp_fr = frac(B["vjp"], vjp_ms)
+    vjpo_gbs, vjpo_fr = frac(B["vjp"], vjp_o)
+    line = {
+        "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64" if s == 8 else "f32", "data": "synthetic",
+        "config": {"workload": describe(spec, info, E), "n_nodes": N, "n_edges": E,
+                   "dx_mode": args.dx_mode, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (w alone is %.2f GB), no flush" % (E * P * U * s / 1e9)},
+        "fwd": {"edges_per_s": world * E / (fwd_ms / 1000), "ms": fwd_ms, "GB_s": fwd_gbs,
+                "hbm_frac": fwd_fr, "bytes": B["fwd"]},
+        "vjp": {"edges_per_s": world * E / (vjp_ms / 1000), "ms": vjp_ms, "GB_s": vjp_gbs,
+                "hbm_frac": vjp_fr, "bytes": B["vjp"], "dx_mode": args.dx_mode},
+        f"vjp_{other}": {"edges_per_s": world * E / (vjp_o / 1000), "ms": vjp_o, "GB_s": vjpo_gbs,
+                         "hbm_frac": vjpo_fr, "fwd_vjp_edges_per_s": world * E / (total_o / args.steps / 1000)},
+        "kernels": kernels,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["GB_s"],
+                     "peak": hbm_peak, "unit": "GB/s", "frac": kernels[dom]["frac"],
+                     "traffic": traffic, "peak_source": peak_src + " hbm_gbs (copy)"},
+        "csr_build_ms": csr_ms,
+        "clocks": clk,
+        "gpu_launches": args.steps * (3 if args.dx_mode == "sender" else 2),
+    }
+
+    # end-to-end through the C ABI from pinned host buffers
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()
+        hin = {"x": pin(x), "Y": pin(Y), "w": pin(w), "g": pin(g), "roff": pin(G.recv_offsets),
+               "src": pin(src), "soff": pin(G.send_offsets), "seid": pin(G.send_eids),
+               "srecv": pin(G.send_recv)}
+        dbuf = {k: torch.empty_like(v, device=dev) for k, v in hin.items()}
+        hout = {"out": pin(out), "dx": pin(dx), "dY": pin(dY), "dw": pin(dw)}
+        h2d = sum(v.numel() * v.element_size() for v in hin.values())
+        d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+        def e2e_step():
+            for k, v in hin.items():
+                dbuf[k].copy_(v, non_blocking=True)
+            b = dbuf
+            plan.fwd(N, b["x"], b["Y"], b["w"], b["roff"], b["src"], out, stream)
+            plan.bwd(N, b["x"], b["Y"], b["w"], b["roff"], b["src"], b["soff"], b["seid"],
+                     b["srecv"], b["g"], dx=dx, dY=dY, dw=dw,
+                     dx_mode=uvu.UVU_DX_SENDER if args.dx_mode == "sender" else uvu.UVU_DX_ATOMIC,
+                     stream=stream)
+            hout["out"].copy_(out, non_blocking=True)
+            hout["dx"].copy_(dx, non_blocking=True)
+            hout["dY"].copy_(dY, non_blocking=True)
+            hout["dw"].copy_(dw, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        tw = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks((time.perf_counter() - tw) * 1000 / args.e2e_steps, world, dev)
+        line["e2e"] = {"value": world * E / (e_ms / 1000), "unit": "edges/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import paths
+        lay = paths.layout(spec.irreps_x, spec.irreps_sh, spec.lmax_out)
+        rate, desc, thr = oracle_sample(wl, w_h, g_h, lay, 120, 7)
+        line["cpu_baseline"] = {"value": rate, "unit": "edges/s", "cores": thr, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

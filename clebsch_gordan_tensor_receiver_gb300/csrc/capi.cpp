@@ -1,0 +1,288 @@
+// The C ABI (include/uvu.h): argument checks on the host, then asynchronous launches on the
+// caller's stream.  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <exception>
+#include <limits>
+#include <memory>
+#include <string>
+
+#include "plan.h"
+
+struct uvu_plan_s {
+    uvu::Plan p;
+};
+
+namespace uvu {
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+uvu_status need(const void* p, const char* name) {
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, std::string(name) + " is NULL");
+    if (!aligned16(p)) return fail(UVU_ERR_INVALID_ARGUMENT, std::string(name) + " is not 16-byte aligned");
+    return UVU_OK;
+}
+
+uvu_status opt(const void* p, const char* name) {
+    if (p && !aligned16(p)) return fail(UVU_ERR_INVALID_ARGUMENT, std::string(name) + " is not 16-byte aligned");
+    return UVU_OK;
+}
+
+uvu_status check_sizes(int64_t N, int64_t E) {
+    if (N < 0 || E < 0) return fail(UVU_ERR_INVALID_ARGUMENT, "n_nodes and n_edges must be >= 0");
+    if (N >= std::numeric_limits<int32_t>::max() || E >= std::numeric_limits<int32_t>::max())
+        return fail(UVU_ERR_INVALID_ARGUMENT, "n_nodes and n_edges must be < 2^31 - 1 (int32 indices)");
+    return UVU_OK;
+}
+
+#define UVU_TRY(expr)                         \
+    do {                                      \
+        uvu_status _s = (expr);               \
+        if (_s != UVU_OK) return _s;          \
+    } while (0)
+
+uvu_status launch(cudaKernel_t k, int64_t owners, const KernelGeom& g, void** args, cudaStream_t st,
+                  const char* what) {
+    if (owners <= 0) return UVU_OK;
+    const int64_t blocks = (owners + g.owners_per_block - 1) / g.owners_per_block;
+    cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(unsigned(blocks)),
+                                     dim3(unsigned(g.threads)), args, g.smem, st);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return UVU_OK;
+}
+
+Plan* get(uvu_plan_t h) { return h ? &h->p : nullptr; }
+
+}  // namespace
+}  // namespace uvu
+
+using namespace uvu;
+
+extern "C" uvu_status uvu_plan_create(const char* irreps_x, const char* irreps_sh, int lmax_out,
+                                      uvu_dtype dtype, uvu_plan_t* plan_out) {
+    if (!plan_out) return fail(UVU_ERR_INVALID_ARGUMENT, "plan_out is NULL");
+    *plan_out = nullptr;
+    if (!irreps_x || !irreps_sh) return fail(UVU_ERR_INVALID_ARGUMENT, "irreps string is NULL");
+    if (dtype != UVU_F32 && dtype != UVU_F64) return fail(UVU_ERR_INVALID_ARGUMENT, "dtype must be UVU_F32 or UVU_F64");
+    try {
+        std::unique_ptr<uvu_plan_s> h(new uvu_plan_s);
+        Plan& p = h->p;
+        p.irreps_x = irreps_x;
+        p.irreps_sh = irreps_sh;
+        p.lmax_out = lmax_out;
+        p.dtype = dtype;
+        std::string err;
+        uvu_status s = build_paths(&p, &err);
+        if (s != UVU_OK) return fail(s, err);
+        p.source = emit_source(&p);
+        if (p.g_fwd.threads > 1024 || p.g_edge.threads > 1024 || p.g_dx.threads > 1024)
+            return fail(UVU_ERR_UNSUPPORTED, "multiplicity x register groups exceeds 1024 threads per owner");
+        s = compile_plan(&p, &err);
+        if (s != UVU_OK) return fail(s, err);
+        *plan_out = h.release();
+        return ok();
+    } catch (const std::exception& e) {
+        return fail(UVU_ERR_UNSUPPORTED, std::string("plan creation failed: ") + e.what());
+    }
+}
+
+extern "C" uvu_status uvu_plan_destroy(uvu_plan_t plan) {
+    if (!plan) return ok();
+    for (auto& kv : plan->p.modules) {
+        int cur = 0;
+        if (cudaGetDevice(&cur) == cudaSuccess && cur != kv.first) cudaSetDevice(kv.first);
+        cudaLibraryUnload(kv.second.lib);
+        if (cur != kv.first) cudaSetDevice(cur);
+    }
+    delete plan;
+    return ok();
+}
+
+extern "C" uvu_status uvu_plan_info(uvu_plan_t plan, int* mul_u, int* dim_x, int* dim_sh, int* dim_out,
+                                    int* n_paths, int* paths_l1l2l3) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    if (mul_u) *mul_u = p->U;
+    if (dim_x) *dim_x = p->Dx;
+    if (dim_sh) *dim_sh = p->Dy;
+    if (dim_out) *dim_out = p->Do;
+    if (n_paths) *n_paths = p->P;
+    if (paths_l1l2l3)
+        for (int i = 0; i < p->P; ++i) {
+            paths_l1l2l3[3 * i] = p->paths[i].l1;
+            paths_l1l2l3[3 * i + 1] = p->paths[i].l2;
+            paths_l1l2l3[3 * i + 2] = p->paths[i].l3;
+        }
+    return ok();
+}
+
+extern "C" uvu_status uvu_plan_cg(uvu_plan_t plan, int path, double* out) {
+    Plan* p = get(plan);
+    if (!p || !out) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or out is NULL");
+    if (path < 0 || path >= p->P) return fail(UVU_ERR_INVALID_ARGUMENT, "path index out of range");
+    std::memcpy(out, p->paths[path].cg.data(), p->paths[path].cg.size() * sizeof(double));
+    return ok();
+}
+
+extern "C" uvu_status uvu_plan_source(uvu_plan_t plan, const char** source, const char** log) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    if (source) *source = p->source.c_str();
+    if (log) *log = p->log.c_str();
+    return ok();
+}
+
+extern "C" uvu_status uvu_csr_from_sorted_recv(int64_t n_nodes, int64_t n_edges, const int32_t* recv,
+                                               int32_t* recv_offsets, uvu_stream_t stream) {
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    if (!recv_offsets) return fail(UVU_ERR_INVALID_ARGUMENT, "recv_offsets is NULL");
+    if (n_edges > 0 && !recv) return fail(UVU_ERR_INVALID_ARGUMENT, "recv is NULL");
+    cudaError_t e = launch_csr_offsets(n_nodes, n_edges, recv, recv_offsets, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "csr offsets launch");
+    return ok();
+}
+
+extern "C" uvu_status uvu_csr_transpose_workspace(int64_t n_nodes, int64_t n_edges, size_t* bytes) {
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    if (!bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    *bytes = transpose_workspace_bytes(n_nodes, n_edges);
+    return ok();
+}
+
+extern "C" uvu_status uvu_csr_transpose(int64_t n_nodes, int64_t n_edges, const int32_t* recv_offsets,
+                                        const int32_t* src, int32_t* send_offsets, int32_t* send_eids,
+                                        int32_t* send_recv, void* workspace, size_t workspace_bytes,
+                                        uvu_stream_t stream) {
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    if (!send_offsets || !workspace) return fail(UVU_ERR_INVALID_ARGUMENT, "send_offsets or workspace is NULL");
+    if (n_edges > 0 && (!recv_offsets || !src || !send_eids || !send_recv))
+        return fail(UVU_ERR_INVALID_ARGUMENT, "graph pointer is NULL");
+    if (!aligned16(workspace)) return fail(UVU_ERR_INVALID_ARGUMENT, "workspace is not 16-byte aligned");
+    if (workspace_bytes < transpose_workspace_bytes(n_nodes, n_edges))
+        return fail(UVU_ERR_INVALID_ARGUMENT, "workspace too small");
+    cudaError_t e = launch_csr_transpose(n_nodes, n_edges, recv_offsets, src, send_offsets, send_eids,
+                                         send_recv, workspace, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "csr transpose launch");
+    return ok();
+}
+
+extern "C" uvu_status uvu_graph_validate(int64_t n_nodes, int64_t n_edges, const int32_t* recv_offsets,
+                                         const int32_t* src, void* workspace, int64_t* n_bad,
+                                         uvu_stream_t stream) {
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    if (!recv_offsets || !workspace || !n_bad || (n_edges > 0 && !src))
+        return fail(UVU_ERR_INVALID_ARGUMENT, "NULL argument");
+    auto* bad = static_cast<unsigned long long*>(workspace);
+    cudaError_t e = launch_graph_validate(n_nodes, n_edges, recv_offsets, src, bad, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "validate launch");
+    unsigned long long h = 0;
+    e = cudaMemcpyAsync(&h, bad, sizeof h, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "validate readback");
+    *n_bad = int64_t(h);
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
+                                   const void* Y, const void* w, const int32_t* recv_offsets,
+                                   const int32_t* src, void* out, uvu_stream_t stream) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    if (n_nodes == 0) return ok();
+    UVU_TRY(need(out, "out"));
+    UVU_TRY(need(recv_offsets, "recv_offsets"));
+    if (n_edges > 0) {
+        UVU_TRY(need(x, "x"));
+        UVU_TRY(need(Y, "Y"));
+        UVU_TRY(need(w, "w"));
+        UVU_TRY(need(src, "src"));
+    }
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = module_for_current_device(p, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    long long N = n_nodes;
+    void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &out};
+    UVU_TRY(launch(m->fwd, n_nodes, p->g_fwd, args, stream, "uvu_fwd launch"));
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
+                                        const void* Y, const void* w, const int32_t* recv_offsets,
+                                        const int32_t* src, const void* d_out, void* dY, void* dw,
+                                        void* dx_atomic, uvu_stream_t stream) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    UVU_TRY(opt(dY, "dY"));
+    UVU_TRY(opt(dw, "dw"));
+    UVU_TRY(opt(dx_atomic, "dx"));
+    if (n_nodes == 0 || (!dY && !dw && !dx_atomic)) return ok();
+    UVU_TRY(need(recv_offsets, "recv_offsets"));
+    if (n_edges > 0) {
+        UVU_TRY(need(x, "x"));
+        UVU_TRY(need(Y, "Y"));
+        UVU_TRY(need(w, "w"));
+        UVU_TRY(need(src, "src"));
+        UVU_TRY(need(d_out, "d_out"));
+    }
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = module_for_current_device(p, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    if (dx_atomic) {
+        cudaError_t e = cudaMemsetAsync(dx_atomic, 0, size_t(n_nodes) * p->U * p->Dx * p->elem(), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "dx memset");
+    }
+    if (n_edges == 0) return ok();
+    long long N = n_nodes;
+    void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &d_out, &dY, &dw, &dx_atomic};
+    UVU_TRY(launch(m->bwd_edge, n_nodes, p->g_edge, args, stream, "uvu_bwd_edge launch"));
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_bwd_dx(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* Y,
+                                      const void* w, const int32_t* send_offsets, const int32_t* send_eids,
+                                      const int32_t* send_recv, const void* d_out, void* dx,
+                                      uvu_stream_t stream) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    if (n_nodes == 0) return ok();
+    UVU_TRY(need(dx, "dx"));
+    UVU_TRY(need(send_offsets, "send_offsets"));
+    if (n_edges > 0) {
+        UVU_TRY(need(Y, "Y"));
+        UVU_TRY(need(w, "w"));
+        UVU_TRY(need(send_eids, "send_eids"));
+        UVU_TRY(need(send_recv, "send_recv"));
+        UVU_TRY(need(d_out, "d_out"));
+    }
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = module_for_current_device(p, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    long long N = n_nodes;
+    void* args[] = {&N, &send_offsets, &send_eids, &send_recv, &Y, &w, &d_out, &dx};
+    UVU_TRY(launch(m->bwd_dx, n_nodes, p->g_dx, args, stream, "uvu_bwd_dx launch"));
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
+                                   const void* Y, const void* w, const int32_t* recv_offsets,
+                                   const int32_t* src, const int32_t* send_offsets, const int32_t* send_eids,
+                                   const int32_t* send_recv, const void* d_out, void* dx, void* dY, void* dw,
+                                   uvu_dx_mode dx_mode, uvu_stream_t stream) {
+    if (dx_mode != UVU_DX_SENDER && dx_mode != UVU_DX_ATOMIC)
+        return fail(UVU_ERR_INVALID_ARGUMENT, "dx_mode must be UVU_DX_SENDER or UVU_DX_ATOMIC");
+    if (dx_mode == UVU_DX_ATOMIC)
+        return uvu_conv_bwd_edge(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, d_out, dY, dw, dx, stream);
+    UVU_TRY(uvu_conv_bwd_edge(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, d_out, dY, dw, nullptr, stream));
+    if (dx)
+        UVU_TRY(uvu_conv_bwd_dx(plan, n_nodes, n_edges, Y, w, send_offsets, send_eids, send_recv, d_out, dx, stream));
+    return ok();
+}

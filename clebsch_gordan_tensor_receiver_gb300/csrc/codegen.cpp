@@ -1,0 +1,552 @@
+// CUDA C++ emission for a plan: three kernels, fully unrolled per path, CG non-zeros baked in
+// as immediates ("An Efficient Sparse Kernel Generator for O(3)-Equivariant Deep Networks",
+// abstract: static analysis at model compile time, sub-kernels whose operands live in
+// registers, long arithmetic instruction streams).
+//
+//   uvu_fwd       receiver-stationary streaming forward: one thread per (receiver, channel,
+//                 register group); the receiver's edges are scanned in CSR order and the output
+//                 row is reduced in registers ("Receiver-streaming convolutions for channel-wise
+//                 UVU tensor products", opening post, ownership paragraph).
+//   uvu_bwd_edge  edges of a receiver, channels in parallel: dw stored directly, dY reduced over
+//                 channels with warp shuffles and a fixed-order shared-memory sum, optional
+//                 atomic dx scatter (same post, backward paragraph).
+//   uvu_bwd_dx    sender-stationary dx over the transposed CSR, written once, no atomics
+//                 (same page, reply on source- vs destination-stationary convolutions).
+//
+// Per-edge arithmetic of one path p = (l1, l2, l3) for one channel, with q[a,b] = x[a] y[b]:
+//   forward   t[m3] = sum_nz c q[m1,m2];            acc[m3] += w_p t[m3]
+//   dw        dw_p  = sum_m3 g[m3] t[m3]
+//   dY, dx    h[m1,m2] += sum_nz c (w_p g[m3]);     dY[m2] += sum_m1 x[m1] h;  dx[m1] += sum_m2 y[m2] h
+// where h is accumulated over all paths sharing (l1, l2) before it is contracted.
+// Paths whose CG is a signed permutation with a scalar operand (l1 = 0 or l2 = 0) skip the
+// products: acc[m3] += (w_p x0) (+-y[m2]).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <map>
+#include <set>
+#include <sstream>
+#include <string>
+#include <vector>
+
+#include "plan.h"
+
+namespace uvu {
+namespace {
+
+struct Src {
+    std::ostringstream o;
+    int ind = 0;
+    Src& operator()(const std::string& s) {
+        for (int i = 0; i < ind; ++i) o << "  ";
+        o << s << "\n";
+        return *this;
+    }
+};
+
+std::string fmt(const char* f, ...) __attribute__((format(printf, 1, 2)));
+std::string fmt(const char* f, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, f);
+    vsnprintf(buf, sizeof buf, f, ap);
+    va_end(ap);
+    return buf;
+}
+
+struct Gen {
+    Plan* P;
+    bool f64;
+    std::string T;
+
+    std::string lit(double c) const {
+        char b[64];
+        if (f64) {
+            snprintf(b, sizeof b, "%.17e", c);
+            return b;
+        }
+        snprintf(b, sizeof b, "%.9ef", double(float(c)));
+        return b;
+    }
+    static bool is_one(double c) { return std::abs(std::abs(c) - 1.0) < 1e-14; }
+
+    // A path whose CG maps each m3 to exactly one (m1, m2) with coefficient +-1 and one operand
+    // of width 1: the identity couplings (0, l, l) and (l, 0, l).
+    bool is_identity(const PathInfo& p) const {
+        if (p.l1 != 0 && p.l2 != 0) return false;
+        std::vector<int> cnt(2 * p.l3 + 1, 0);
+        for (const Nz& z : p.nz) {
+            if (!is_one(z.c)) return false;
+            cnt[z.m3]++;
+        }
+        for (int c : cnt)
+            if (c != 1) return false;
+        return true;
+    }
+
+    std::set<int> x_needed(const std::vector<int>& paths) const {
+        std::set<int> s;
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            for (int m = 0; m < 2 * p.l1 + 1; ++m) s.insert(p.xoff + m);
+        }
+        return s;
+    }
+    std::set<int> y_needed(const std::vector<int>& paths) const {
+        std::set<int> s;
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            for (int m = 0; m < 2 * p.l2 + 1; ++m) s.insert(p.yoff + m);
+        }
+        return s;
+    }
+
+    // Emit loads "T pre_k = base[k]" for k in `need`, with 16-byte vector loads when the row
+    // stride keeps every row 16-byte aligned.
+    void emit_row_loads(Src& S, const std::string& pre, const std::string& base, int width,
+                        const std::set<int>& need) const {
+        const int esz = f64 ? 8 : 4;
+        const int V = 16 / esz;
+        if ((width * esz) % 16 == 0) {
+            const std::string VT = f64 ? "double2" : "float4";
+            std::set<int> chunks;
+            for (int k : need) chunks.insert(k / V);
+            S(fmt("const %s* %s_v = reinterpret_cast<const %s*>(%s);", VT.c_str(), pre.c_str(),
+                  VT.c_str(), base.c_str()));
+            for (int c : chunks) {
+                S(fmt("const %s %s_c%d = __ldg(%s_v + %d);", VT.c_str(), pre.c_str(), c, pre.c_str(), c));
+                static const char* comp[4] = {"x", "y", "z", "w"};
+                for (int i = 0; i < V; ++i) {
+                    const int k = c * V + i;
+                    if (need.count(k))
+                        S(fmt("const %s %s_%d = %s_c%d.%s;", T.c_str(), pre.c_str(), k, pre.c_str(), c, comp[i]));
+                }
+            }
+        } else {
+            for (int k : need) S(fmt("const %s %s_%d = __ldg(%s + %d);", T.c_str(), pre.c_str(), k, base.c_str(), k));
+        }
+    }
+
+    // Products q_a_b = xv_a * yv_b used by the non-identity paths in `paths`.
+    void emit_products(Src& S, const std::vector<int>& paths) const {
+        std::set<std::pair<int, int>> q;
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            if (is_identity(p)) continue;
+            for (const Nz& z : p.nz) q.insert({p.xoff + z.m1, p.yoff + z.m2});
+        }
+        for (auto& ab : q)
+            S(fmt("const %s q_%d_%d = xv_%d * yv_%d;", T.c_str(), ab.first, ab.second, ab.first, ab.second));
+    }
+
+    // t_<p>_<m3> = sum_nz c q   (general paths only)
+    void emit_t(Src& S, int pi) const {
+        const PathInfo& p = P->paths[pi];
+        for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3) {
+            bool first = true;
+            for (const Nz& z : p.nz) {
+                if (z.m3 != m3) continue;
+                const std::string q = fmt("q_%d_%d", p.xoff + z.m1, p.yoff + z.m2);
+                if (first) {
+                    if (is_one(z.c))
+                        S(fmt("%s t_%d_%d = %s%s;", T.c_str(), pi, m3, z.c < 0 ? "-" : "", q.c_str()));
+                    else
+                        S(fmt("%s t_%d_%d = %s * %s;", T.c_str(), pi, m3, lit(z.c).c_str(), q.c_str()));
+                    first = false;
+                } else {
+                    S(fmt("t_%d_%d = fma(%s, %s, t_%d_%d);", pi, m3, lit(z.c).c_str(), q.c_str(), pi, m3));
+                }
+            }
+            if (first) S(fmt("const %s t_%d_%d = 0;", T.c_str(), pi, m3));
+        }
+    }
+
+    // ------------------------------------------------------------------ forward
+    void emit_fwd_group(Src& S, int g) const {
+        const std::vector<int>& paths = P->groups[g];
+        S(fmt("__device__ __forceinline__ void fwd_group%d(int e0, int e1, int u, const int* __restrict__ src,", g));
+        S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, %s* __restrict__ orow) {",
+              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S.ind++;
+        std::vector<int> outs;
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            for (int m = 0; m < 2 * p.l3 + 1; ++m) outs.push_back(p.ooff + m);
+        }
+        for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
+        const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+        S("#pragma unroll 1");
+        S("for (int e = e0; e < e1; ++e) {");
+        S.ind++;
+        S("const int s = __ldg(src + e);");
+        emit_row_loads(S, "xv", fmt("x + ((size_t)s * UVU_U + u) * UVU_DX"), P->Dx, xn);
+        emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+        S("const " + T + "* __restrict__ we = w + (size_t)e * (UVU_P * UVU_U) + u;");
+        for (int pi : paths) S(fmt("const %s wv_%d = __ldg(we + %d * UVU_U);", T.c_str(), pi, pi));
+        emit_products(S, paths);
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            S(fmt("// path %d: (%d,%d,%d)", pi, p.l1, p.l2, p.l3));
+            if (is_identity(p)) {
+                const bool scal_x = (p.l1 == 0);
+                S(fmt("{ const %s sw = wv_%d * %s;", T.c_str(), pi,
+                      scal_x ? fmt("xv_%d", p.xoff).c_str() : fmt("yv_%d", p.yoff).c_str()));
+                for (const Nz& z : p.nz) {
+                    const std::string other = scal_x ? fmt("yv_%d", p.yoff + z.m2) : fmt("xv_%d", p.xoff + z.m1);
+                    S(fmt("  acc_%d = fma(%ssw, %s, acc_%d);", p.ooff + z.m3, z.c < 0 ? "-" : "", other.c_str(), p.ooff + z.m3));
+                }
+                S("}");
+            } else {
+                S("{");
+                S.ind++;
+                emit_t(S, pi);
+                for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3)
+                    S(fmt("acc_%d = fma(wv_%d, t_%d_%d, acc_%d);", p.ooff + m3, pi, pi, m3, p.ooff + m3));
+                S.ind--;
+                S("}");
+            }
+        }
+        S.ind--;
+        S("}");
+        for (int k : outs) S(fmt("orow[%d] = acc_%d;", k, k));
+        S.ind--;
+        S("}");
+    }
+
+    // ------------------------------------------------------------------ per-pair backward core
+    // Emits, for the paths of `paths` grouped by (ix, iy): optional dw stores, then the h
+    // accumulation and its contraction into dyp_* (if want_dy) and dxp_* (if want_dx).
+    // gval(k) names the d_out value of output index k.
+    template <class GV>
+    void emit_bwd_pairs(Src& S, const std::vector<int>& paths, bool want_dw, bool want_dy,
+                        bool want_dx, GV gval) const {
+        std::map<std::pair<int, int>, std::vector<int>> pairs;
+        for (int pi : paths) pairs[{P->paths[pi].ix, P->paths[pi].iy}].push_back(pi);
+        for (auto& kv : pairs) {
+            const std::vector<int>& pp = kv.second;
+            const PathInfo& p0 = P->paths[pp[0]];
+            const int d1 = 2 * p0.l1 + 1, d2 = 2 * p0.l2 + 1;
+            S("{");
+            S.ind++;
+            std::set<std::pair<int, int>> hdef;
+            for (int pi : pp) {
+                const PathInfo& p = P->paths[pi];
+                S(fmt("// path %d: (%d,%d,%d)", pi, p.l1, p.l2, p.l3));
+                if (want_dw) {
+                    if (is_identity(p)) {
+                        const bool scal_x = (p.l1 == 0);
+                        bool first = true;
+                        for (const Nz& z : p.nz) {
+                            const std::string other = scal_x ? fmt("yv_%d", p.yoff + z.m2) : fmt("xv_%d", p.xoff + z.m1);
+                            const std::string gv = gval(p.ooff + z.m3);
+                            if (first) {
+                                S(fmt("%s z_%d = %s%s * %s;", T.c_str(), pi, z.c < 0 ? "-" : "", gv.c_str(), other.c_str()));
+                                first = false;
+                            } else {
+                                S(fmt("z_%d = fma(%s%s, %s, z_%d);", pi, z.c < 0 ? "-" : "", gv.c_str(), other.c_str(), pi));
+                            }
+                        }
+                        S(fmt("dwe[%d * UVU_U] = z_%d * %s;", pi, pi,
+                              scal_x ? fmt("xv_%d", p.xoff).c_str() : fmt("yv_%d", p.yoff).c_str()));
+                    } else {
+                        S("{");
+                        S.ind++;
+                        emit_t(S, pi);
+                        for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3) {
+                            if (m3 == 0)
+                                S(fmt("%s z = %s * t_%d_0;", T.c_str(), gval(p.ooff).c_str(), pi));
+                            else
+                                S(fmt("z = fma(%s, t_%d_%d, z);", gval(p.ooff + m3).c_str(), pi, m3));
+                        }
+                        S(fmt("dwe[%d * UVU_U] = z;", pi));
+                        S.ind--;
+                        S("}");
+                    }
+                }
+                if (want_dy || want_dx) {
+                    for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3)
+                        S(fmt("const %s a_%d_%d = wv_%d * %s;", T.c_str(), pi, m3, pi, gval(p.ooff + m3).c_str()));
+                    for (const Nz& z : p.nz) {
+                        const int a = p.xoff + z.m1, b = p.yoff + z.m2;
+                        const std::string av = fmt("a_%d_%d", pi, z.m3);
+                        if (!hdef.count({a, b})) {
+                            hdef.insert({a, b});
+                            if (is_one(z.c))
+                                S(fmt("%s h_%d_%d = %s%s;", T.c_str(), a, b, z.c < 0 ? "-" : "", av.c_str()));
+                            else
+                                S(fmt("%s h_%d_%d = %s * %s;", T.c_str(), a, b, lit(z.c).c_str(), av.c_str()));
+                        } else {
+                            if (is_one(z.c))
+                                S(fmt("h_%d_%d %s= %s;", a, b, z.c < 0 ? "-" : "+", av.c_str()));
+                            else
+                                S(fmt("h_%d_%d = fma(%s, %s, h_%d_%d);", a, b, lit(z.c).c_str(), av.c_str(), a, b));
+                        }
+                    }
+                }
+            }
+            if (want_dy) {
+                for (int m2 = 0; m2 < d2; ++m2) {
+                    const int b = p0.yoff + m2;
+                    for (int m1 = 0; m1 < d1; ++m1) {
+                        const int a = p0.xoff + m1;
+                        if (hdef.count({a, b})) S(fmt("dyp_%d = fma(xv_%d, h_%d_%d, dyp_%d);", b, a, a, b, b));
+                    }
+                }
+            }
+            if (want_dx) {
+                for (int m1 = 0; m1 < d1; ++m1) {
+                    const int a = p0.xoff + m1;
+                    for (int m2 = 0; m2 < d2; ++m2) {
+                        const int b = p0.yoff + m2;
+                        if (hdef.count({a, b})) S(fmt("dxp_%d = fma(yv_%d, h_%d_%d, dxp_%d);", a, b, a, b, a));
+                    }
+                }
+            }
+            S.ind--;
+            S("}");
+        }
+    }
+
+    // ------------------------------------------------------------------ backward edge kernel
+    void emit_edge_group(Src& S, int g) const {
+        const std::vector<int>& paths = P->groups[g];
+        const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+        std::vector<int> outs;
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            for (int m = 0; m < 2 * p.l3 + 1; ++m) outs.push_back(p.ooff + m);
+        }
+        S(fmt("__device__ __forceinline__ void edge_group%d(int rl, int seg, int lane_in_seg, bool valid, int r_e0, int r_e1,", g));
+        S(fmt("    int nchunks, long long r, int u, const int* __restrict__ src, const %s* __restrict__ x,", T.c_str()));
+        S(fmt("    const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ gout,", T.c_str(), T.c_str(), T.c_str()));
+        S(fmt("    %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx, %s* sred, const int* s_e0, const int* s_e1) {",
+              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S.ind++;
+        S(fmt("const %s* __restrict__ grow = gout + ((size_t)(valid ? r : 0) * UVU_U + u) * UVU_DO;", T.c_str()));
+        for (int k : outs) S(fmt("const %s gv_%d = valid ? __ldg(grow + %d) : (%s)0;", T.c_str(), k, k, T.c_str()));
+        S("#pragma unroll 1");
+        S("for (int c = 0; c < nchunks; ++c) {");
+        S.ind++;
+        S("#pragma unroll 1");
+        S("for (int j = 0; j < UVU_CH; ++j) {");
+        S.ind++;
+        S("const int e = r_e0 + c * UVU_CH + j;");
+        S("const bool active = valid && e < r_e1;");
+        for (int k : yn) S(fmt("%s dyp_%d = 0;", T.c_str(), k));
+        S("if (active) {");
+        S.ind++;
+        S("const int s = __ldg(src + e);");
+        emit_row_loads(S, "xv", "x + ((size_t)s * UVU_U + u) * UVU_DX", P->Dx, xn);
+        emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+        S("const " + T + "* __restrict__ we = w + (size_t)e * (UVU_P * UVU_U) + u;");
+        S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
+        for (int pi : paths) S(fmt("const %s wv_%d = __ldg(we + %d * UVU_U);", T.c_str(), pi, pi));
+        for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
+        emit_products(S, paths);
+        auto gval = [](int k) { return fmt("gv_%d", k); };
+        S("if (dw) {");
+        S.ind++;
+        emit_bwd_pairs(S, paths, true, false, false, gval);
+        S.ind--;
+        S("}");
+        emit_bwd_pairs(S, paths, false, true, true, gval);
+        // atomic dx scatter
+        S("if (dx) {");
+        S.ind++;
+        S(T + "* __restrict__ dxr = dx + ((size_t)s * UVU_U + u) * UVU_DX;");
+        if (!f64 && P->Dx % 4 == 0) {
+            std::set<int> chunks;
+            for (int k : xn) chunks.insert(k / 4);
+            for (int c : chunks) {
+                std::string v[4];
+                for (int i = 0; i < 4; ++i) v[i] = xn.count(4 * c + i) ? fmt("dxp_%d", 4 * c + i) : "0.0f";
+                S(fmt("red_add_v4(dxr + %d, %s, %s, %s, %s);", 4 * c, v[0].c_str(), v[1].c_str(), v[2].c_str(), v[3].c_str()));
+            }
+        } else {
+            for (int k : xn) S(fmt("atomicAdd(dxr + %d, dxp_%d);", k, k));
+        }
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");  // active
+        // reduce the dY partials over the channels of this segment
+        S("if (dY) {");
+        S.ind++;
+        for (int k : yn) {
+            S(fmt("#pragma unroll"));
+            S(fmt("for (int o = UVU_SEGW / 2; o > 0; o >>= 1) dyp_%d += __shfl_xor_sync(0xffffffffu, dyp_%d, o);", k, k));
+        }
+        S("if (lane_in_seg == 0) {");
+        S.ind++;
+        S(T + "* sr = sred + ((size_t)(rl * UVU_SEGS + seg) * UVU_CH + j) * UVU_DY;");
+        for (int k = 0; k < P->Dy; ++k) {
+            if (yn.count(k)) S(fmt("sr[%d] = dyp_%d;", k, k));
+            else S(fmt("sr[%d] = 0;", k));
+        }
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");  // j
+        S("block_sync();");
+        S("if (dY) {");
+        S.ind++;
+        S("for (int it = threadIdx.x; it < UVU_RPB * UVU_CH * UVU_DY; it += UVU_TPB) {");
+        S.ind++;
+        S("const int k = it % UVU_DY, jj = (it / UVU_DY) % UVU_CH, r2 = it / (UVU_DY * UVU_CH);");
+        S("const int e = s_e0[r2] + c * UVU_CH + jj;");
+        S("if (e < s_e1[r2]) {");
+        S.ind++;
+        S(T + " acc = 0;");
+        S("#pragma unroll");
+        S("for (int sg = 0; sg < UVU_SEGS; ++sg) acc += sred[((size_t)(r2 * UVU_SEGS + sg) * UVU_CH + jj) * UVU_DY + k];");
+        S("dY[(size_t)e * UVU_DY + k] = acc;");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S("block_sync();");
+        S.ind--;
+        S("}");  // c
+        S.ind--;
+        S("}");
+    }
+
+    // ------------------------------------------------------------------ sender-stationary dx
+    void emit_dx_kernel(Src& S) const {
+        std::vector<int> all;
+        for (int p = 0; p < P->P; ++p) all.push_back(p);
+        const std::set<int> xn = x_needed(all), yn = y_needed(all);
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_DX_TPB) uvu_bwd_dx(long long N, const int* __restrict__ soff,"));
+        S(fmt("    const int* __restrict__ seid, const int* __restrict__ srecv, const %s* __restrict__ Y,", T.c_str()));
+        S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dx) {", T.c_str(), T.c_str(), T.c_str()));
+        S.ind++;
+        S("const int u = threadIdx.x % UVU_UP;");
+        S("const long long sn = (long long)blockIdx.x * UVU_SPB + threadIdx.x / UVU_UP;");
+        S("if (sn >= N || u >= UVU_U) return;");
+        S("const int k0 = __ldg(soff + sn), k1 = __ldg(soff + sn + 1);");
+        for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
+        S("#pragma unroll 1");
+        S("for (int kk = k0; kk < k1; ++kk) {");
+        S.ind++;
+        S("const int e = __ldg(seid + kk);");
+        S("const int r = __ldg(srecv + kk);");
+        emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+        S("const " + T + "* __restrict__ we = w + (size_t)e * (UVU_P * UVU_U) + u;");
+        S("const " + T + "* __restrict__ grow = gout + ((size_t)r * UVU_U + u) * UVU_DO;");
+        for (int pi : all) S(fmt("const %s wv_%d = __ldg(we + %d * UVU_U);", T.c_str(), pi, pi));
+        auto gval = [](int k) { return fmt("__ldg(grow + %d)", k); };
+        emit_bwd_pairs(S, all, false, false, true, gval);
+        S.ind--;
+        S("}");
+        S(T + "* __restrict__ dxr = dx + ((size_t)sn * UVU_U + u) * UVU_DX;");
+        for (int k = 0; k < P->Dx; ++k) S(fmt("dxr[%d] = %s;", k, xn.count(k) ? fmt("dxp_%d", k).c_str() : "0"));
+        S.ind--;
+        S("}");
+    }
+};
+
+}  // namespace
+
+std::string emit_source(Plan* plan) {
+    Gen G{plan, plan->dtype == UVU_F64, plan->dtype == UVU_F64 ? "double" : "float"};
+    const int U = plan->U, NG = int(plan->groups.size());
+    // Channel slots per owner: U rounded up to a whole number of warps (or, below 32, to a power
+    // of two dividing 32) so that no warp mixes two owners; padding lanes hold no channel.
+    int UP = 1;
+    if (U >= 32) UP = (U + 31) / 32 * 32;
+    else while (UP < U) UP *= 2;
+    plan->U_pad = UP;
+    const int owner_threads = UP * NG;
+    const int rpb = std::max(1, 128 / owner_threads);
+    const int segw = std::min(UP, 32);
+    const int segs = NG * ((UP + 31) / 32);
+    const int spb = std::max(1, 128 / UP);
+    const int ch = 16;
+    plan->g_fwd = {rpb * owner_threads, rpb, 0};
+    plan->edge_chunk = ch;
+    plan->g_edge = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem()};
+    plan->g_dx = {spb * UP, spb, 0};
+
+    Src S;
+    S("// Generated by the UVU planner. Channel-wise CG tensor-product graph convolution.");
+    S(fmt("// irreps_x=%s irreps_sh=%s lmax_out=%d dtype=%s", plan->irreps_x.c_str(),
+          plan->irreps_sh.c_str(), plan->lmax_out, G.f64 ? "fp64" : "fp32"));
+    for (int p = 0; p < plan->P; ++p) {
+        const PathInfo& pi = plan->paths[p];
+        S(fmt("// path %d: (%d,%d,%d) parity %+d xoff %d yoff %d ooff %d nnz %zu", p, pi.l1, pi.l2,
+              pi.l3, pi.parity, pi.xoff, pi.yoff, pi.ooff, pi.nz.size()));
+    }
+    S(fmt("#define UVU_U %d", U));
+    S(fmt("#define UVU_UP %d", UP));
+    S(fmt("#define UVU_P %d", plan->P));
+    S(fmt("#define UVU_DX %d", plan->Dx));
+    S(fmt("#define UVU_DY %d", plan->Dy));
+    S(fmt("#define UVU_DO %d", plan->Do));
+    S(fmt("#define UVU_G %d", NG));
+    S(fmt("#define UVU_RPB %d", rpb));
+    S(fmt("#define UVU_TPB %d", rpb * owner_threads));
+    S(fmt("#define UVU_SEGW %d", segw));
+    S(fmt("#define UVU_SEGS %d", segs));
+    S(fmt("#define UVU_CH %d", ch));
+    S(fmt("#define UVU_SPB %d", spb));
+    S(fmt("#define UVU_DX_TPB %d", spb * UP));
+    S("// Block-wide barrier usable from the per-group code paths: the non-aligned form may be");
+    S("// reached from different call sites, as long as every thread of the block arrives the same");
+    S("// number of times (each group runs the same uniform chunk loop).");
+    S("__device__ __forceinline__ void block_sync() { asm volatile(\"barrier.sync 0;\" ::: \"memory\"); }");
+    S("__device__ __forceinline__ void red_add_v4(float* a, float p, float q, float r, float s) {");
+    S("  asm volatile(\"red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\" :: \"l\"(a), \"f\"(p), \"f\"(q), \"f\"(r), \"f\"(s) : \"memory\");");
+    S("}");
+    for (int g = 0; g < NG; ++g) G.emit_fwd_group(S, g);
+    S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_TPB) uvu_fwd(long long N, const int* __restrict__ off,"));
+    S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", G.T.c_str(), G.T.c_str()));
+    S(fmt("    const %s* __restrict__ w, %s* __restrict__ out) {", G.T.c_str(), G.T.c_str()));
+    S("  const int u = threadIdx.x % UVU_UP;");
+    S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
+    S("  const long long r = (long long)blockIdx.x * UVU_RPB + threadIdx.x / (UVU_UP * UVU_G);");
+    S("  if (r >= N || u >= UVU_U) return;");
+    S("  const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+    S("  " + G.T + "* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
+    for (int g = 0; g < NG; ++g)
+        S(fmt("  %sif (g == %d) fwd_group%d(e0, e1, u, src, x, Y, w, orow);", g ? "else " : "", g, g));
+    S("}");
+
+    for (int g = 0; g < NG; ++g) G.emit_edge_group(S, g);
+    S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_TPB) uvu_bwd_edge(long long N, const int* __restrict__ off,"));
+    S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", G.T.c_str(), G.T.c_str()));
+    S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
+          G.T.c_str(), G.T.c_str(), G.T.c_str(), G.T.c_str()));
+    S(fmt("    %s* __restrict__ dx) {", G.T.c_str()));
+    S(fmt("  extern __shared__ __align__(16) unsigned char smem_raw[];"));
+    S(fmt("  %s* sred = reinterpret_cast<%s*>(smem_raw);", G.T.c_str(), G.T.c_str()));
+    S("  __shared__ int s_e0[UVU_RPB], s_e1[UVU_RPB], s_nch;");
+    S("  const int u = threadIdx.x % UVU_UP;");
+    S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
+    S("  const int rl = threadIdx.x / (UVU_UP * UVU_G);");
+    S("  const long long r = (long long)blockIdx.x * UVU_RPB + rl;");
+    S("  const bool rvalid = r < N;");
+    S("  const bool valid = rvalid && u < UVU_U;");
+    S("  if (threadIdx.x == 0) s_nch = 0;");
+    S("  __syncthreads();");
+    S("  if (threadIdx.x % (UVU_UP * UVU_G) == 0) {");
+    S("    const int a = rvalid ? __ldg(off + r) : 0, b = rvalid ? __ldg(off + r + 1) : 0;");
+    S("    s_e0[rl] = a; s_e1[rl] = b;");
+    S("    atomicMax(&s_nch, (b - a + UVU_CH - 1) / UVU_CH);");
+    S("  }");
+    S("  __syncthreads();");
+    S("  const int nchunks = s_nch;");
+    S("  const int seg = g * ((UVU_UP + 31) / 32) + u / 32;");
+    S("  const int lane_in_seg = u % UVU_SEGW;");
+    for (int g = 0; g < NG; ++g)
+        S(fmt("  %sif (g == %d) edge_group%d(rl, seg, lane_in_seg, valid, s_e0[rl], s_e1[rl], nchunks, r, u, src, x, Y, w, gout, dY, dw, dx, sred, s_e0, s_e1);",
+              g ? "else " : "", g, g));
+    S("}");
+    G.emit_dx_kernel(S);
+    return S.o.str();
+}
+
+}  // namespace uvu

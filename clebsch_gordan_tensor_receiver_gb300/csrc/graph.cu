@@ -1,0 +1,176 @@
+// Graph preparation kernels: receiver CSR from receiver-sorted edges, the transposed (sender)
+// CSR, and an on-device validity check.
+//
+// "Receiver-streaming convolutions for channel-wise UVU tensor products" (opening post,
+// benchmark paragraph) runs on prepared receiver-sorted edge lists and keeps graph construction
+// out of the timed region; these kernels are that preparation.  Every output word is written by
+// exactly one thread and the sender order is fixed (ascending edge id), so the result is
+// bit-exact regardless of scheduling.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "plan.h"
+
+namespace uvu {
+namespace {
+
+constexpr int kThreads = 256;
+
+int grid_for(int64_t n) {
+    int64_t b = (n + kThreads - 1) / kThreads;
+    if (b < 1) b = 1;
+    if (b > 152 * 32) b = 152 * 32;  // grid-stride loops cover the rest
+    return int(b);
+}
+
+// offsets[r] = #{e : recv[e] < r}.  The thread owning edge e writes every offset in
+// (recv[e-1], recv[e]]; the last edge also writes (recv[E-1], N].
+__global__ void csr_offsets_kernel(int64_t N, int64_t E, const int32_t* __restrict__ recv,
+                                   int32_t* __restrict__ off) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < E; e += stride) {
+        const int64_t r = recv[e];
+        const int64_t prev = e == 0 ? -1 : recv[e - 1];
+        for (int64_t k = prev + 1; k <= r; ++k) off[k] = int32_t(e);
+        if (e == E - 1)
+            for (int64_t k = r + 1; k <= N; ++k) off[k] = int32_t(E);
+    }
+}
+
+__global__ void fill_kernel(int32_t* __restrict__ p, int64_t n, int32_t v) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) p[i] = v;
+}
+
+__global__ void count_senders_kernel(int64_t E, const int32_t* __restrict__ src, int32_t* __restrict__ cnt) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < E; e += stride)
+        atomicAdd(cnt + src[e], 1);
+}
+
+// Exclusive scan of cnt[0..N) into off[0..N], one block: each thread scans a contiguous slice.
+__global__ void scan_kernel(int64_t N, const int32_t* __restrict__ cnt, int32_t* __restrict__ off) {
+    __shared__ int64_t part[1024];
+    const int t = threadIdx.x, T = blockDim.x;
+    const int64_t per = (N + T - 1) / T;
+    const int64_t b = int64_t(t) * per, e = (b + per < N) ? b + per : N;
+    int64_t s = 0;
+    for (int64_t i = b; i < e; ++i) s += cnt[i];
+    part[t] = s;
+    __syncthreads();
+    if (t == 0) {
+        int64_t run = 0;
+        for (int i = 0; i < T; ++i) {
+            const int64_t v = part[i];
+            part[i] = run;
+            run += v;
+        }
+        off[N] = int32_t(run);
+    }
+    __syncthreads();
+    int64_t run = part[t];
+    for (int64_t i = b; i < e; ++i) {
+        off[i] = int32_t(run);
+        run += cnt[i];
+    }
+}
+
+// Unordered scatter of edge ids into their sender segments (cursor starts at zero).
+__global__ void scatter_kernel(int64_t E, const int32_t* __restrict__ src, const int32_t* __restrict__ soff,
+                               int32_t* __restrict__ cursor, int32_t* __restrict__ tmp) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < E; e += stride) {
+        const int32_t s = src[e];
+        const int32_t pos = atomicAdd(cursor + s, 1);
+        tmp[soff[s] + pos] = int32_t(e);
+    }
+}
+
+__device__ __forceinline__ int32_t receiver_of(int64_t N, const int32_t* __restrict__ roff, int32_t e) {
+    // largest r with roff[r] <= e (the receiver whose segment holds e)
+    int64_t lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi + 1) >> 1;
+        if (roff[mid] <= e) lo = mid;
+        else hi = mid - 1;
+    }
+    return int32_t(lo);
+}
+
+// Place each unordered entry at its rank inside its sender segment (edge ids are distinct, so
+// the rank is unique): the result lists each sender's edges in ascending edge id.
+__global__ void rank_place_kernel(int64_t N, int64_t E, const int32_t* __restrict__ src,
+                                  const int32_t* __restrict__ soff, const int32_t* __restrict__ roff,
+                                  const int32_t* __restrict__ tmp, int32_t* __restrict__ eids,
+                                  int32_t* __restrict__ srecv) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < E; k += stride) {
+        const int32_t e = tmp[k];
+        const int32_t s = src[e];
+        const int32_t b = soff[s], t = soff[s + 1];
+        int32_t rank = 0;
+        for (int32_t j = b; j < t; ++j) rank += tmp[j] < e;
+        eids[b + rank] = e;
+        srecv[b + rank] = receiver_of(N, roff, e);
+    }
+}
+
+__global__ void validate_kernel(int64_t N, int64_t E, const int32_t* __restrict__ off,
+                                const int32_t* __restrict__ src, unsigned long long* bad) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    unsigned long long local = 0;
+    const int64_t n = N + 1 > E ? N + 1 : E;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        if (i <= N) {
+            if (i == 0 && off[0] != 0) ++local;
+            if (i == N && off[N] != E) ++local;
+            if (i < N && off[i + 1] < off[i]) ++local;
+        }
+        if (i < E && (src[i] < 0 || src[i] >= N)) ++local;
+    }
+    if (local) atomicAdd(bad, local);
+}
+
+}  // namespace
+
+size_t transpose_workspace_bytes(int64_t N, int64_t E) {
+    const size_t a = (size_t(N + 1) * 4 + 255) / 256 * 256;
+    const size_t b = (size_t(E > 0 ? E : 1) * 4 + 255) / 256 * 256;
+    return a + b;
+}
+
+cudaError_t launch_csr_offsets(int64_t N, int64_t E, const int32_t* recv, int32_t* off, cudaStream_t st) {
+    if (E == 0) {
+        fill_kernel<<<grid_for(N + 1), kThreads, 0, st>>>(off, N + 1, 0);
+    } else {
+        csr_offsets_kernel<<<grid_for(E), kThreads, 0, st>>>(N, E, recv, off);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_csr_transpose(int64_t N, int64_t E, const int32_t* roff, const int32_t* src,
+                                 int32_t* soff, int32_t* eids, int32_t* srecv, void* ws, cudaStream_t st) {
+    int32_t* cnt = static_cast<int32_t*>(ws);
+    int32_t* tmp = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + (size_t(N + 1) * 4 + 255) / 256 * 256);
+    fill_kernel<<<grid_for(N + 1), kThreads, 0, st>>>(cnt, N + 1, 0);
+    if (E > 0) count_senders_kernel<<<grid_for(E), kThreads, 0, st>>>(E, src, cnt);
+    scan_kernel<<<1, 1024, 0, st>>>(N, cnt, soff);
+    if (E > 0) {
+        fill_kernel<<<grid_for(N + 1), kThreads, 0, st>>>(cnt, N + 1, 0);
+        scatter_kernel<<<grid_for(E), kThreads, 0, st>>>(E, src, soff, cnt, tmp);
+        rank_place_kernel<<<grid_for(E), kThreads, 0, st>>>(N, E, src, soff, roff, tmp, eids, srecv);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_graph_validate(int64_t N, int64_t E, const int32_t* off, const int32_t* src,
+                                  unsigned long long* bad, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(bad, 0, sizeof(unsigned long long), st);
+    if (e != cudaSuccess) return e;
+    const int64_t n = N + 1 > E ? N + 1 : E;
+    validate_kernel<<<grid_for(n), kThreads, 0, st>>>(N, E, off, src, bad);
+    return cudaGetLastError();
+}
+
+}  // namespace uvu

@@ -1,0 +1,121 @@
+// NVRTC compilation of a plan's emitted source for sm_103a, and per-device module loading.
+//
+// The cubin is produced on the host at plan creation (no GPU needed) and loaded with
+// cudaLibraryLoadData on each device at its first launch there.  Compiled code is only loaded,
+// never inspected.  Identical sources share one compilation through a process-wide cache.
+#include <nvrtc.h>
+
+#include <functional>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "plan.h"
+
+namespace uvu {
+namespace {
+
+struct CacheEntry {
+    std::vector<char> cubin;
+    std::string log;
+};
+std::mutex g_cache_mu;
+std::map<std::string, CacheEntry> g_cache;  // keyed by the full source text
+
+uvu_status nvrtc_compile(const std::string& src, CacheEntry* out, std::string* err) {
+    nvrtcProgram prog;
+    nvrtcResult r = nvrtcCreateProgram(&prog, src.c_str(), "uvu_plan.cu", 0, nullptr, nullptr);
+    if (r != NVRTC_SUCCESS) {
+        *err = std::string("nvrtcCreateProgram: ") + nvrtcGetErrorString(r);
+        return UVU_ERR_COMPILE;
+    }
+    const char* opts[] = {"--gpu-architecture=sm_103a", "--std=c++17", "-lineinfo",
+                          "--ptxas-options=-v", "--fmad=true"};
+    r = nvrtcCompileProgram(prog, int(sizeof(opts) / sizeof(opts[0])), opts);
+    size_t log_size = 0;
+    nvrtcGetProgramLogSize(prog, &log_size);
+    std::string log(log_size, '\0');
+    if (log_size) nvrtcGetProgramLog(prog, &log[0]);
+    if (r != NVRTC_SUCCESS) {
+        *err = std::string("NVRTC compile failed: ") + nvrtcGetErrorString(r) + "\n" + log;
+        nvrtcDestroyProgram(&prog);
+        return UVU_ERR_COMPILE;
+    }
+    size_t n = 0;
+    nvrtcGetCUBINSize(prog, &n);
+    out->cubin.resize(n);
+    nvrtcGetCUBIN(prog, out->cubin.data());
+    out->log = log;
+    nvrtcDestroyProgram(&prog);
+    return UVU_OK;
+}
+
+}  // namespace
+
+uvu_status compile_plan(Plan* plan, std::string* err) {
+    {
+        std::lock_guard<std::mutex> g(g_cache_mu);
+        auto it = g_cache.find(plan->source);
+        if (it != g_cache.end()) {
+            plan->cubin = it->second.cubin;
+            plan->log = it->second.log;
+            return UVU_OK;
+        }
+    }
+    CacheEntry e;
+    uvu_status s = nvrtc_compile(plan->source, &e, err);
+    if (s != UVU_OK) return s;
+    plan->cubin = e.cubin;
+    plan->log = e.log;
+    std::lock_guard<std::mutex> g(g_cache_mu);
+    g_cache.emplace(plan->source, std::move(e));
+    return UVU_OK;
+}
+
+uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string* err) {
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) {
+        *err = std::string("cudaGetDevice: ") + cudaGetErrorString(ce);
+        return UVU_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> g(plan->mu);
+    auto it = plan->modules.find(dev);
+    if (it != plan->modules.end()) {
+        *out = &it->second;
+        return UVU_OK;
+    }
+    DeviceModule m;
+    ce = cudaLibraryLoadData(&m.lib, plan->cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0);
+    if (ce != cudaSuccess) {
+        *err = std::string("cudaLibraryLoadData: ") + cudaGetErrorString(ce);
+        return UVU_ERR_CUDA;
+    }
+    struct {
+        const char* name;
+        cudaKernel_t* k;
+    } ks[] = {{"uvu_fwd", &m.fwd}, {"uvu_bwd_edge", &m.bwd_edge}, {"uvu_bwd_dx", &m.bwd_dx}};
+    for (auto& k : ks) {
+        ce = cudaLibraryGetKernel(k.k, m.lib, k.name);
+        if (ce != cudaSuccess) {
+            *err = std::string("cudaLibraryGetKernel(") + k.name + "): " + cudaGetErrorString(ce);
+            cudaLibraryUnload(m.lib);
+            return UVU_ERR_CUDA;
+        }
+    }
+    if (plan->g_edge.smem > 48 * 1024) {
+        ce = cudaFuncSetAttribute(reinterpret_cast<const void*>(m.bwd_edge),
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(plan->g_edge.smem));
+        if (ce != cudaSuccess) {
+            *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(ce);
+            cudaLibraryUnload(m.lib);
+            return UVU_ERR_CUDA;
+        }
+    }
+    auto res = plan->modules.emplace(dev, m);
+    *out = &res.first->second;
+    return UVU_OK;
+}
+
+}  // namespace uvu

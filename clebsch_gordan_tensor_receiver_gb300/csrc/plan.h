@@ -1,0 +1,97 @@
+// Internal declarations of the UVU convolution library (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "uvu.h"
+
+namespace uvu {
+
+struct Irrep {
+    int mul;
+    int l;
+    int parity;  // +1 even, -1 odd
+};
+
+// One non-zero of a real CG tensor.
+struct Nz {
+    int m1, m2, m3;  // 0 .. 2l
+    double c;
+};
+
+struct PathInfo {
+    int l1, l2, l3, parity;
+    int ix, iy;              // index of the x irrep / SH irrep
+    int xoff, yoff, ooff;    // block offsets inside a channel's x row, an edge's Y row, a channel's out row
+    std::vector<double> cg;  // dense (2l1+1)(2l2+1)(2l3+1), row-major (m1, m2, m3)
+    std::vector<Nz> nz;      // non-zeros of cg
+};
+
+// Launch geometry of one generated kernel.
+struct KernelGeom {
+    int threads = 0;        // threads per block
+    int owners_per_block = 0;  // receivers (or senders) per block
+    size_t smem = 0;        // dynamic shared memory bytes
+};
+
+struct DeviceModule {
+    cudaLibrary_t lib = nullptr;
+    cudaKernel_t fwd = nullptr, bwd_edge = nullptr, bwd_dx = nullptr;
+};
+
+struct Plan {
+    std::string irreps_x, irreps_sh;
+    int lmax_out = 0;
+    uvu_dtype dtype = UVU_F32;
+    int U = 0, Dx = 0, Dy = 0, Do = 0, P = 0;
+    int U_pad = 0;  // channel slots per owner in the generated kernels
+    std::vector<Irrep> xs, ys;
+    std::vector<PathInfo> paths;
+    std::vector<std::vector<int>> groups;  // path ids per register group
+    KernelGeom g_fwd, g_edge, g_dx;
+    int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
+    std::string source, log;
+    std::vector<char> cubin;
+    std::mutex mu;
+    std::map<int, DeviceModule> modules;  // per device ordinal
+    size_t elem() const { return dtype == UVU_F64 ? 8 : 4; }
+};
+
+// cg.cpp
+std::vector<double> real_cg_dense(int l1, int l2, int l3);
+
+// irreps.cpp
+bool parse_irreps(const char* s, std::vector<Irrep>* out, std::string* err);
+uvu_status build_paths(Plan* plan, std::string* err);
+
+// codegen.cpp
+std::string emit_source(Plan* plan);
+
+// jit.cpp
+uvu_status compile_plan(Plan* plan, std::string* err);
+uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string* err);
+
+// status.cpp
+uvu_status fail(uvu_status s, const std::string& msg);
+uvu_status ok();
+uvu_status cuda_fail(cudaError_t e, const char* what);
+const char* g_last_message_cstr();
+
+}  // namespace uvu
+
+namespace uvu {
+// graph.cu
+size_t transpose_workspace_bytes(int64_t N, int64_t E);
+cudaError_t launch_csr_offsets(int64_t N, int64_t E, const int32_t* recv, int32_t* off, cudaStream_t st);
+cudaError_t launch_csr_transpose(int64_t N, int64_t E, const int32_t* roff, const int32_t* src,
+                                 int32_t* soff, int32_t* eids, int32_t* srecv, void* ws, cudaStream_t st);
+cudaError_t launch_graph_validate(int64_t N, int64_t E, const int32_t* off, const int32_t* src,
+                                  unsigned long long* bad, cudaStream_t st);
+}  // namespace uvu

@@ -1,0 +1,212 @@
+"""Python binding of libuvu.so (argument marshalling only).
+
+Every function named ``uvu_*`` here calls the C entry point of the same name in
+``include/uvu.h`` and raises ``UVUError`` when it returns a status other than UVU_OK.  All
+arithmetic runs in the library's CUDA kernels; there is no fallback path: if the library cannot
+be loaded, importing this module raises.
+
+``Plan`` is a small convenience wrapper that passes torch tensors' device pointers and the
+current CUDA stream; torch is used only for memory and streams.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libuvu.so")
+
+UVU_F32, UVU_F64 = 0, 1
+UVU_DX_SENDER, UVU_DX_ATOMIC = 0, 1
+STATUS = {0: "UVU_OK", 1: "UVU_ERR_INVALID_ARGUMENT", 2: "UVU_ERR_UNSUPPORTED",
+          3: "UVU_ERR_COMPILE", 4: "UVU_ERR_CUDA", 5: "UVU_ERR_OUT_OF_MEMORY"}
+
+# every symbol declared in include/uvu.h
+EXPORTS = (
+    "uvu_plan_create", "uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
+    "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
+    "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx", "uvu_conv_bwd",
+    "uvu_status_string", "uvu_last_error_message",
+)
+
+
+class UVUError(RuntimeError):
+    def __init__(self, status: int, fn: str, msg: str):
+        super().__init__(f"{fn}: {STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libuvu.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "uvu_plan_create": [ctypes.c_char_p, ctypes.c_char_p, I, I, ctypes.POINTER(P)],
+        "uvu_plan_destroy": [P],
+        "uvu_plan_info": [P, P, P, P, P, P, P],
+        "uvu_plan_cg": [P, I, P],
+        "uvu_plan_source": [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
+        "uvu_csr_from_sorted_recv": [I64, I64, P, P, P],
+        "uvu_csr_transpose_workspace": [I64, I64, ctypes.POINTER(SZ)],
+        "uvu_csr_transpose": [I64, I64, P, P, P, P, P, P, SZ, P],
+        "uvu_graph_validate": [I64, I64, P, P, P, ctypes.POINTER(I64), P],
+        "uvu_conv_fwd": [P, I64, I64, P, P, P, P, P, P, P],
+        "uvu_conv_bwd_edge": [P, I64, I64, P, P, P, P, P, P, P, P, P, P],
+        "uvu_conv_bwd_dx": [P, I64, I64, P, P, P, P, P, P, P, P],
+        "uvu_conv_bwd": [P, I64, I64, P, P, P, P, P, P, P, P, P, P, P, P, I, P],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.uvu_status_string.argtypes = [ctypes.c_int]
+    lib.uvu_status_string.restype = ctypes.c_char_p
+    lib.uvu_last_error_message.argtypes = []
+    lib.uvu_last_error_message.restype = ctypes.c_char_p
+    return lib
+
+
+lib = _load()
+
+
+def _check(st: int, fn: str):
+    if st != 0:
+        raise UVUError(st, fn, lib.uvu_last_error_message().decode())
+
+
+def _wrap(name):
+    f = getattr(lib, name)
+
+    def call(*args):
+        _check(f(*args), name)
+
+    call.__name__ = name
+    call.__doc__ = f"Calls {name} of include/uvu.h; raises UVUError on failure."
+    return call
+
+
+for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
+           "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
+           "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx",
+           "uvu_conv_bwd"):
+    globals()[_n] = _wrap(_n)
+
+
+def uvu_plan_create(irreps_x: str, irreps_sh: str, lmax_out: int, dtype: int) -> int:
+    h = ctypes.c_void_p()
+    _check(lib.uvu_plan_create(irreps_x.encode(), irreps_sh.encode(), lmax_out, dtype,
+                               ctypes.byref(h)), "uvu_plan_create")
+    return h.value
+
+
+def uvu_status_string(s: int) -> str:
+    return lib.uvu_status_string(s).decode()
+
+
+def uvu_last_error_message() -> str:
+    return lib.uvu_last_error_message().decode()
+
+
+# ----------------------------------------------------------------------- torch convenience
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+@dataclass
+class PlanInfo:
+    mul: int
+    dim_x: int
+    dim_sh: int
+    dim_out: int
+    n_paths: int
+    paths: list
+
+
+class Plan:
+    """Owns a uvu plan handle; methods take torch tensors already on the current device."""
+
+    def __init__(self, irreps_x: str, irreps_sh: str, lmax_out: int, dtype: str = "float32"):
+        self.dtype_name = dtype
+        self.handle = uvu_plan_create(irreps_x, irreps_sh, lmax_out,
+                                      UVU_F64 if dtype == "float64" else UVU_F32)
+        vals = [ctypes.c_int() for _ in range(5)]
+        uvu_plan_info(self.handle, *[ctypes.byref(v) for v in vals], None)
+        P = vals[4].value
+        arr = (ctypes.c_int * (3 * P))()
+        uvu_plan_info(self.handle, None, None, None, None, None, arr)
+        self.info = PlanInfo(vals[0].value, vals[1].value, vals[2].value, vals[3].value, P,
+                             [tuple(arr[3 * i:3 * i + 3]) for i in range(P)])
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            lib.uvu_plan_destroy(h)
+            self.handle = None
+
+    def cg(self, path: int):
+        import numpy as np
+        l1, l2, l3 = self.info.paths[path]
+        out = np.zeros((2 * l1 + 1, 2 * l2 + 1, 2 * l3 + 1))
+        uvu_plan_cg(self.handle, path, out.ctypes.data_as(ctypes.c_void_p))
+        return out
+
+    def source(self):
+        s, l = ctypes.c_char_p(), ctypes.c_char_p()
+        uvu_plan_source(self.handle, ctypes.byref(s), ctypes.byref(l))
+        return s.value.decode(), l.value.decode()
+
+    def fwd(self, n_nodes, x, Y, w, recv_offsets, src, out, stream=None):
+        uvu_conv_fwd(self.handle, n_nodes, src.numel() if src is not None else 0, _ptr(x), _ptr(Y),
+                     _ptr(w), _ptr(recv_offsets), _ptr(src), _ptr(out), _stream(stream))
+
+    def bwd_edge(self, n_nodes, x, Y, w, recv_offsets, src, d_out, dY=None, dw=None,
+                 dx_atomic=None, stream=None):
+        uvu_conv_bwd_edge(self.handle, n_nodes, src.numel(), _ptr(x), _ptr(Y), _ptr(w),
+                          _ptr(recv_offsets), _ptr(src), _ptr(d_out), _ptr(dY), _ptr(dw),
+                          _ptr(dx_atomic), _stream(stream))
+
+    def bwd_dx(self, n_nodes, n_edges, Y, w, send_offsets, send_eids, send_recv, d_out, dx,
+               stream=None):
+        uvu_conv_bwd_dx(self.handle, n_nodes, n_edges, _ptr(Y), _ptr(w), _ptr(send_offsets),
+                        _ptr(send_eids), _ptr(send_recv), _ptr(d_out), _ptr(dx), _stream(stream))
+
+    def bwd(self, n_nodes, x, Y, w, recv_offsets, src, send_offsets, send_eids, send_recv,
+            d_out, dx=None, dY=None, dw=None, dx_mode=UVU_DX_SENDER, stream=None):
+        uvu_conv_bwd(self.handle, n_nodes, src.numel(), _ptr(x), _ptr(Y), _ptr(w),
+                     _ptr(recv_offsets), _ptr(src), _ptr(send_offsets), _ptr(send_eids),
+                     _ptr(send_recv), _ptr(d_out), _ptr(dx), _ptr(dY), _ptr(dw), dx_mode,
+                     _stream(stream))
+
+
+class Graph:
+    """Receiver CSR and transposed CSR built on the device by the library's kernels."""
+
+    def __init__(self, n_nodes: int, recv, src, stream=None):
+        import torch
+        dev = src.device
+        self.n_nodes = n_nodes
+        self.n_edges = src.numel()
+        self.src = src
+        self.recv_offsets = torch.empty(n_nodes + 1, dtype=torch.int32, device=dev)
+        uvu_csr_from_sorted_recv(n_nodes, self.n_edges, _ptr(recv), _ptr(self.recv_offsets),
+                                 _stream(stream))
+        nb = ctypes.c_size_t()
+        uvu_csr_transpose_workspace(n_nodes, self.n_edges, ctypes.byref(nb))
+        ws = torch.empty(max(nb.value, 16), dtype=torch.uint8, device=dev)
+        self.send_offsets = torch.empty(n_nodes + 1, dtype=torch.int32, device=dev)
+        self.send_eids = torch.empty(max(self.n_edges, 1), dtype=torch.int32, device=dev)
+        self.send_recv = torch.empty(max(self.n_edges, 1), dtype=torch.int32, device=dev)
+        uvu_csr_transpose(n_nodes, self.n_edges, _ptr(self.recv_offsets), _ptr(src),
+                          _ptr(self.send_offsets), _ptr(self.send_eids), _ptr(self.send_recv),
+                          _ptr(ws), nb.value, _stream(stream))
+        self._ws = ws

@@ -1,0 +1,182 @@
+/*
+ * uvu.h -- C ABI of the GB300 (sm_103a) channel-wise (UVU) Clebsch-Gordan tensor-product graph
+ * convolution library (libuvu.so).
+ *
+ * The operation ("Receiver-streaming convolutions for channel-wise UVU tensor products",
+ * OpenEquivariance discussion #221, opening post; "An Efficient Sparse Kernel Generator for
+ * O(3)-Equivariant Deep Networks", abstract: CG tensor product fused with a graph convolution):
+ *
+ *   out[r,u,p,m3] = sum_{e : recv(e) = r} w[e,p,u] sum_{m1,m2} C^p[m1,m2,m3] x[src(e),u,l1,m1] Y[e,l2,m2]
+ *
+ * over the plan's paths p = (l1, l2, l3), and its vector-Jacobian product with respect to x, Y
+ * and w.  C^p is the real Clebsch-Gordan tensor (unitary per output component, canonical sign:
+ * the first non-zero entry in row-major (m1, m2, m3) order is positive; real basis with l = 1
+ * ordered (y, z, x)).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts (row-major, contiguous, one floating dtype per plan, indices int32):
+ *     x      [N][U][D_x]      l1 blocks in irreps_x order
+ *     Y      [E][D_Y]         l2 blocks in irreps_sh order (l*l + l + m for 0e+1o+2e+...)
+ *     w, dw  [E][P][U]
+ *     out, d_out [N][U][D_out]  path blocks in path order
+ *     recv_offsets [N+1]      receiver CSR: edges of receiver r are [recv_offsets[r], recv_offsets[r+1])
+ *     src    [E]              sender of each edge
+ *     send_offsets [N+1], send_eids [E], send_recv [E]   transposed (sender) CSR
+ * Path order: for each x irrep (string order), each SH irrep (string order), l3 ascending over
+ * |l1-l2| .. min(l1+l2, lmax_out); every triangle-allowed l3 is kept, with parity p1*p2.
+ *
+ * Memory: every tensor pointer is caller-owned DEVICE memory on the current device, 16-byte
+ * aligned.  No entry point allocates device memory; the transpose takes a caller workspace.
+ * Streams: work is enqueued on `stream` (0 = legacy default) and returns before it completes.
+ * Outputs are overwritten, never accumulated: receivers without edges get out = 0, senders
+ * without edges get dx = 0, n_edges == 0 writes zeros.
+ * Errors: argument errors are detected on the host before anything is enqueued and return
+ * UVU_ERR_INVALID_ARGUMENT; launch failures return UVU_ERR_CUDA; JIT failures return
+ * UVU_ERR_COMPILE.  uvu_last_error_message() gives a per-thread description of the last error.
+ * Graph contents (offsets monotone, indices in range) are trusted, not re-validated per call;
+ * uvu_graph_validate() checks them on the device when asked.  No kernel traps, asserts or
+ * waits on another kernel.
+ */
+#ifndef UVU_H_
+#define UVU_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct uvu_plan_s *uvu_plan_t;
+typedef struct CUstream_st *uvu_stream_t; /* same handle as cudaStream_t */
+
+typedef enum { UVU_F32 = 0, UVU_F64 = 1 } uvu_dtype;
+
+typedef enum {
+    UVU_OK = 0,
+    UVU_ERR_INVALID_ARGUMENT = 1,
+    UVU_ERR_UNSUPPORTED = 2,
+    UVU_ERR_COMPILE = 3,
+    UVU_ERR_CUDA = 4,
+    UVU_ERR_OUT_OF_MEMORY = 5
+} uvu_status;
+
+/* How dx is produced by uvu_conv_bwd. */
+typedef enum {
+    UVU_DX_SENDER = 0, /* sender-stationary over the transposed CSR: no atomics, deterministic */
+    UVU_DX_ATOMIC = 1  /* edge-parallel atomic scatter fused into the edge kernel (comparison) */
+} uvu_dx_mode;
+
+/* ---------------------------------------------------------------------------- planning ---- */
+
+/* Build a plan: parse the irreps, enumerate the paths, derive the real CG coefficients, emit
+ * fully unrolled CUDA C++ with the CG non-zeros as immediates and compile it with NVRTC for
+ * sm_103a.  Host only; the module is loaded on a device at its first launch there.
+ * ("An Efficient Sparse Kernel Generator for O(3)-Equivariant Deep Networks", abstract: static
+ * analysis at model compile time, long unrolled arithmetic instruction streams.)
+ *   irreps_x   e.g. "128x0e+128x1o"; every term must share one multiplicity U (UVU); each l at
+ *              most once; l <= 4.
+ *   irreps_sh  e.g. "1x0e+1x1o+1x2e+1x3o"; every term multiplicity 1; l <= 4.
+ *   lmax_out   0 <= lmax_out <= 8; bounds l3.
+ *   plan_out   receives an opaque handle owned by the caller (free with uvu_plan_destroy).
+ * Returns UVU_ERR_INVALID_ARGUMENT for a malformed string or a non-UVU multiplicity,
+ * UVU_ERR_UNSUPPORTED for l beyond the limits or an empty path set, UVU_ERR_COMPILE when NVRTC
+ * fails. */
+uvu_status uvu_plan_create(const char *irreps_x, const char *irreps_sh, int lmax_out,
+                           uvu_dtype dtype, uvu_plan_t *plan_out);
+
+/* Release a plan and the modules it loaded.  NULL is accepted. */
+uvu_status uvu_plan_destroy(uvu_plan_t plan);
+
+/* Shapes of a plan.  Any output pointer may be NULL.  paths_l1l2l3, if not NULL, receives
+ * 3*n_paths ints (l1, l2, l3 per path in path order). */
+uvu_status uvu_plan_info(uvu_plan_t plan, int *mul_u, int *dim_x, int *dim_sh, int *dim_out,
+                         int *n_paths, int *paths_l1l2l3);
+
+/* The plan's real CG tensor of one path as fp64, dense (2l1+1)(2l2+1)(2l3+1), row-major in
+ * (m1, m2, m3); `out` is caller-owned host memory of at least that many doubles. */
+uvu_status uvu_plan_cg(uvu_plan_t plan, int path, double *out);
+
+/* The emitted CUDA C++ source of the plan (valid until the plan is destroyed), and the NVRTC
+ * log (ptxas resource usage).  Either pointer may be NULL. */
+uvu_status uvu_plan_source(uvu_plan_t plan, const char **source, const char **compile_log);
+
+/* ------------------------------------------------------------------------- graph build ---- */
+
+/* Receiver CSR from receiver-sorted edges ("Receiver-streaming convolutions ...", opening post,
+ * benchmark paragraph: prepared, receiver-sorted edge lists; graph construction is not part of
+ * the timed convolution).  recv_offsets[r] = #{e : recv[e] < r}.
+ *   recv          device int32 [n_edges], non-decreasing, values in [0, n_nodes)
+ *   recv_offsets  device int32 [n_nodes + 1], written
+ * Bit-exact and deterministic. */
+uvu_status uvu_csr_from_sorted_recv(int64_t n_nodes, int64_t n_edges, const int32_t *recv,
+                                    int32_t *recv_offsets, uvu_stream_t stream);
+
+/* Bytes of device workspace uvu_csr_transpose needs for these sizes. */
+uvu_status uvu_csr_transpose_workspace(int64_t n_nodes, int64_t n_edges, size_t *bytes);
+
+/* Transposed (sender) CSR: send_offsets [N+1]; send_eids [E] lists, per sender, the ids of
+ * its edges in ascending edge-id order; send_recv[k] = receiver of edge send_eids[k].
+ * Deterministic and bit-exact (the ordering is unique).  `workspace` is caller-owned device
+ * memory of at least uvu_csr_transpose_workspace() bytes; its contents on entry do not matter. */
+uvu_status uvu_csr_transpose(int64_t n_nodes, int64_t n_edges, const int32_t *recv_offsets,
+                             const int32_t *src, int32_t *send_offsets, int32_t *send_eids,
+                             int32_t *send_recv, void *workspace, size_t workspace_bytes,
+                             uvu_stream_t stream);
+
+/* Check a receiver CSR and sender list on the device: offsets[0] == 0, non-decreasing,
+ * offsets[N] == E, 0 <= src < N.  Synchronises `stream`; *n_bad receives the number of
+ * violations (0 = valid).  `workspace` needs 8 bytes of device memory. */
+uvu_status uvu_graph_validate(int64_t n_nodes, int64_t n_edges, const int32_t *recv_offsets,
+                              const int32_t *src, void *workspace, int64_t *n_bad,
+                              uvu_stream_t stream);
+
+/* ------------------------------------------------------------------------ convolution ---- */
+
+/* Forward, receiver-stationary streaming: each (receiver, channel) owner scans its receiver's
+ * edges and reduces in registers; no per-edge intermediate touches global memory
+ * ("Receiver-streaming convolutions ...", opening post, ownership paragraph).  out is
+ * overwritten.  One kernel launch. */
+uvu_status uvu_conv_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
+                        const void *Y, const void *w, const int32_t *recv_offsets,
+                        const int32_t *src, void *out, uvu_stream_t stream);
+
+/* Backward edge kernel: per edge, channels in parallel; writes dw directly and reduces dY
+ * across channels inside the block, with no atomics ("Receiver-streaming convolutions ...",
+ * opening post, backward paragraph).  dY and dw are overwritten; either may be NULL (skipped).
+ * If dx_atomic is not NULL, dx is first zeroed and then accumulated by atomic adds from the
+ * same kernel (the atomic-scatter variant; its summation order is not deterministic).
+ * One kernel launch (plus a memset when dx_atomic is given). */
+uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
+                             const void *Y, const void *w, const int32_t *recv_offsets,
+                             const int32_t *src, const void *d_out, void *dY, void *dw,
+                             void *dx_atomic, uvu_stream_t stream);
+
+/* Backward dx, sender-stationary: each (sender, channel) owner walks the sender's edges through
+ * the transposed CSR and writes dx once, without atomics; deterministic (bitwise repeatable)
+ * ("Receiver-streaming convolutions ...", source- vs destination-stationary reply).
+ * One kernel launch. */
+uvu_status uvu_conv_bwd_dx(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *Y,
+                           const void *w, const int32_t *send_offsets, const int32_t *send_eids,
+                           const int32_t *send_recv, const void *d_out, void *dx,
+                           uvu_stream_t stream);
+
+/* Full VJP: dx, dY, dw (any may be NULL = not computed).  dx_mode selects the dx kernel; the
+ * transposed-CSR arguments may be NULL when dx_mode == UVU_DX_ATOMIC or dx == NULL. */
+uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
+                        const void *Y, const void *w, const int32_t *recv_offsets,
+                        const int32_t *src, const int32_t *send_offsets,
+                        const int32_t *send_eids, const int32_t *send_recv, const void *d_out,
+                        void *dx, void *dY, void *dw, uvu_dx_mode dx_mode, uvu_stream_t stream);
+
+/* ---------------------------------------------------------------------------- errors ---- */
+
+const char *uvu_status_string(uvu_status s);
+const char *uvu_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UVU_H_ */

@@ -1,0 +1,134 @@
+"""GPU parity of the convolution kernels against the fp64 oracle, through the C ABI.
+
+Small workloads are compared element by element over every output; the full-size workloads in
+the configuration the benchmark times are compared on sampled receivers, edges and senders
+(each sampled element computed by the oracle from its full definition) and by the adjoint
+identities, which hold at any size."""
+import numpy as np
+import pytest
+import torch
+
+from clebsch_gordan_tensor_receiver_gb300 import uvu, workloads
+from gpu_util import Problem, check, dev
+
+pytestmark = pytest.mark.gpu
+
+SH3 = "1x0e+1x1o+1x2e+1x3o"
+
+
+def _full_compare(P):
+    out = P.fwd().cpu().numpy()
+    check(out, P.ref_out(), P.f64, "out")
+    rdY, rdw = P.ref_edges()
+    rdx = P.ref_dx()
+    for mode in (uvu.UVU_DX_SENDER, uvu.UVU_DX_ATOMIC):
+        dx, dY, dw = (t.cpu().numpy() for t in P.bwd(mode))
+        check(dY, rdY, P.f64, "dY")
+        check(dw, rdw, P.f64, "dw")
+        check(dx, rdx, P.f64, f"dx mode {mode}")
+
+
+def test_tiny_workload_all_outputs():
+    _full_compare(Problem.from_spec(0))
+
+
+CUSTOM = [
+    # irreps_x, irreps_sh, lmax_out, dtype, N, max degree
+    ("48x0e+48x1o+48x2e", SH3, 3, "float32", 37, 12),     # channel padding, ragged degrees
+    ("96x0e+96x1o", SH3, 3, "float32", 21, 9),            # three warps per owner
+    ("32x0e", "1x0e", 0, "float32", 40, 7),               # scalar path only
+    ("8x1o+8x2e", "1x0e+1x1o+1x2e", 4, "float64", 19, 6),  # narrow fp64, pseudo-tensor outputs
+    ("64x0e+64x1o+64x2e", SH3, 3, "float64", 23, 8),      # fp64 with register groups
+    ("3x0e+3x1o", "1x0e+1x1o+1x2e", 2, "float32", 11, 5),  # three channels
+    ("128x0e+128x1o", SH3, 3, "float32", 300, 70),        # medium shapes, ragged, many chunks
+]
+
+
+@pytest.mark.parametrize("case", CUSTOM, ids=[c[0] + "-" + c[3] for c in CUSTOM])
+def test_custom_workloads_all_outputs(case):
+    irx, irs, lo, dt, N, dmax = case
+    spec = workloads.custom_spec(100 + CUSTOM.index(case), N, irx, irs, lo, dt)
+    rng = np.random.default_rng(CUSTOM.index(case))
+    deg = rng.integers(0, dmax + 1, size=N)
+    deg[[0, N // 2, N - 1]] = [0, dmax, 0]
+    recv, src = workloads.random_degree_graph(N, deg, rng)
+    vec = workloads.unit_vectors(src.size, rng)
+    lsh = int(irs.split("+")[-1].split("x")[1][:-1])
+    Y = workloads.sh_inputs(vec, lsh).astype(dt)
+    mul = int(irx.split("x")[0])
+    x = rng.standard_normal((N, mul, workloads.dim_of(irx))).astype(dt)
+    _full_compare(Problem(spec, recv, src, x, Y, N))
+
+
+def test_no_edges_writes_zeros():
+    spec = workloads.custom_spec(150, 9, "32x0e+32x1o", SH3, 3)
+    recv = np.zeros(0, np.int32)
+    src = np.zeros(0, np.int32)
+    x = np.ones((9, 32, 4), np.float32)
+    P = Problem(spec, recv, src, x, np.zeros((0, 16), np.float32), 9)
+    assert torch.all(P.fwd() == 0)
+    for mode in (uvu.UVU_DX_SENDER, uvu.UVU_DX_ATOMIC):
+        dx, dY, dw = P.bwd(mode)
+        assert torch.all(dx == 0) and dY.numel() == 0 and dw.numel() == 0
+
+
+def _sample(n, k, rng):
+    s = rng.choice(n, size=min(k, n), replace=False)
+    return np.unique(np.concatenate([s, [0, n - 1]]))
+
+
+@pytest.mark.parametrize("key", [1, 2, 3, 4])
+def test_full_size_sampled(key):
+    P = Problem.from_spec(key)
+    rng = np.random.default_rng(1000 + key)
+    rs = _sample(P.N, 48, rng)
+    es = _sample(P.E, 192, rng)
+    ss = _sample(P.N, 48, rng)
+    rs_t, es_t, ss_t = (torch.from_numpy(a).cuda() for a in (rs, es, ss))
+    out = P.fwd()
+    check(out[rs_t].cpu().numpy(), P.ref_out(rs), P.f64, "out")
+    rdY, rdw = P.ref_edges(es)
+    rdx = P.ref_dx(ss)
+    for mode in (uvu.UVU_DX_SENDER, uvu.UVU_DX_ATOMIC):
+        dx, dY, dw = P.bwd(mode)
+        check(dY[es_t].cpu().numpy(), rdY, P.f64, "dY")
+        check(dw[es_t].cpu().numpy(), rdw, P.f64, "dw")
+        check(dx[ss_t].cpu().numpy(), rdx, P.f64, f"dx mode {mode}")
+        assert not torch.isnan(dx).any() and not torch.isnan(dY).any() and not torch.isnan(dw).any()
+    assert not torch.isnan(out).any()
+    # adjoint identities over the whole problem: <d_out,out> = <dx,x> = <dY,Y> = <dw,w>
+    dx, dY, dw = P.bwd(uvu.UVU_DX_SENDER)
+    s = lambda a, b: float((a.double() * b.double()).sum())
+    ref = s(out, P.d["g"])
+    tol = 1e-10 if P.f64 else 2e-5
+    for a, b, name in ((dx, P.d["x"], "dx"), (dY, P.d["Y"], "dY"), (dw, P.d["w"], "dw")):
+        assert s(a, b) == pytest.approx(ref, rel=tol), name
+
+
+def test_deterministic_kernels_repeat_bitwise():
+    P = Problem.from_spec(1)
+    o1 = P.fwd()
+    a1 = P.bwd(uvu.UVU_DX_SENDER)
+    for _ in range(2):
+        assert torch.equal(P.fwd(), o1)
+        a2 = P.bwd(uvu.UVU_DX_SENDER)
+        for t1, t2 in zip(a1, a2):
+            assert torch.equal(t1, t2)
+
+
+def test_graph_validate():
+    P = Problem.from_spec(0)
+    ws = torch.zeros(2, dtype=torch.int64, device="cuda")
+    import ctypes
+    nbad = ctypes.c_int64(-1)
+    uvu.uvu_graph_validate(P.N, P.E, ctypes.c_void_p(P.G.recv_offsets.data_ptr()),
+                           ctypes.c_void_p(P.d["src"].data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                           ctypes.byref(nbad), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert nbad.value == 0
+    bad_src = P.d["src"].clone()
+    bad_src[5] = P.N + 3
+    bad_src[7] = -1
+    uvu.uvu_graph_validate(P.N, P.E, ctypes.c_void_p(P.G.recv_offsets.data_ptr()),
+                           ctypes.c_void_p(bad_src.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
+                           ctypes.byref(nbad), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert nbad.value == 2

