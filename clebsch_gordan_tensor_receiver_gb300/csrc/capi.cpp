@@ -2,6 +2,7 @@
 // caller's stream.  Nothing here allocates device memory.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <exception>
@@ -44,10 +45,16 @@ uvu_status check_sizes(int64_t N, int64_t E) {
         if (_s != UVU_OK) return _s;          \
     } while (0)
 
-uvu_status launch(cudaKernel_t k, int64_t owners, const KernelGeom& g, void** args, cudaStream_t st,
-                  const char* what) {
+uvu_status launch(cudaKernel_t k, int occ, int sm_count, int64_t owners, const KernelGeom& g, void** args,
+                  cudaStream_t st, const char* what) {
     if (owners <= 0) return UVU_OK;
-    const int64_t blocks = (owners + g.owners_per_block - 1) / g.owners_per_block;
+    int64_t blocks;
+    if (g.persistent) {
+        const int64_t items = owners * g.tiles;
+        blocks = std::min<int64_t>(items, int64_t(occ) * sm_count);
+    } else {
+        blocks = (owners + g.owners_per_block - 1) / g.owners_per_block;
+    }
     cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(unsigned(blocks)),
                                      dim3(unsigned(g.threads)), args, g.smem, st);
     if (e != cudaSuccess) return cuda_fail(e, what);
@@ -207,7 +214,7 @@ extern "C" uvu_status uvu_conv_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
     if (s != UVU_OK) return fail(s, err);
     long long N = n_nodes;
     void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &out};
-    UVU_TRY(launch(m->fwd, n_nodes, p->g_fwd, args, stream, "uvu_fwd launch"));
+    UVU_TRY(launch(m->fwd, m->occ_fwd, m->sm_count, n_nodes, p->g_fwd, args, stream, "uvu_fwd launch"));
     return ok();
 }
 
@@ -241,7 +248,7 @@ extern "C" uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_
     if (n_edges == 0) return ok();
     long long N = n_nodes;
     void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &d_out, &dY, &dw, &dx_atomic};
-    UVU_TRY(launch(m->bwd_edge, n_nodes, p->g_edge, args, stream, "uvu_bwd_edge launch"));
+    UVU_TRY(launch(m->bwd_edge, m->occ_edge, m->sm_count, n_nodes, p->g_edge, args, stream, "uvu_bwd_edge launch"));
     return ok();
 }
 
@@ -268,7 +275,7 @@ extern "C" uvu_status uvu_conv_bwd_dx(uvu_plan_t plan, int64_t n_nodes, int64_t 
     if (s != UVU_OK) return fail(s, err);
     long long N = n_nodes;
     void* args[] = {&N, &send_offsets, &send_eids, &send_recv, &Y, &w, &d_out, &dx};
-    UVU_TRY(launch(m->bwd_dx, n_nodes, p->g_dx, args, stream, "uvu_bwd_dx launch"));
+    UVU_TRY(launch(m->bwd_dx, m->occ_dx, m->sm_count, n_nodes, p->g_dx, args, stream, "uvu_bwd_dx launch"));
     return ok();
 }
 
@@ -284,5 +291,21 @@ extern "C" uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
     UVU_TRY(uvu_conv_bwd_edge(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, d_out, dY, dw, nullptr, stream));
     if (dx)
         UVU_TRY(uvu_conv_bwd_dx(plan, n_nodes, n_edges, Y, w, send_offsets, send_eids, send_recv, d_out, dx, stream));
+    return ok();
+}
+
+extern "C" uvu_status uvu_plan_device_status(uvu_plan_t plan, unsigned* word, int reset) {
+    Plan* p = get(plan);
+    if (!p || !word) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or word is NULL");
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = module_for_current_device(p, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    cudaError_t e = cudaMemcpy(word, m->status_word, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && reset) {
+        const unsigned zero = 0;
+        e = cudaMemcpy(m->status_word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "status word copy");
     return ok();
 }

@@ -104,7 +104,7 @@ struct Gen {
     // Emit loads "T pre_k = base[k]" for k in `need`, with 16-byte vector loads when the row
     // stride keeps every row 16-byte aligned.
     void emit_row_loads(Src& S, const std::string& pre, const std::string& base, int width,
-                        const std::set<int>& need) const {
+                        const std::set<int>& need, bool global = true) const {
         const int esz = f64 ? 8 : 4;
         const int V = 16 / esz;
         if ((width * esz) % 16 == 0) {
@@ -114,7 +114,10 @@ struct Gen {
             S(fmt("const %s* %s_v = reinterpret_cast<const %s*>(%s);", VT.c_str(), pre.c_str(),
                   VT.c_str(), base.c_str()));
             for (int c : chunks) {
-                S(fmt("const %s %s_c%d = __ldg(%s_v + %d);", VT.c_str(), pre.c_str(), c, pre.c_str(), c));
+                if (global)
+                    S(fmt("const %s %s_c%d = __ldg(%s_v + %d);", VT.c_str(), pre.c_str(), c, pre.c_str(), c));
+                else
+                    S(fmt("const %s %s_c%d = %s_v[%d];", VT.c_str(), pre.c_str(), c, pre.c_str(), c));
                 static const char* comp[4] = {"x", "y", "z", "w"};
                 for (int i = 0; i < V; ++i) {
                     const int k = c * V + i;
@@ -123,7 +126,12 @@ struct Gen {
                 }
             }
         } else {
-            for (int k : need) S(fmt("const %s %s_%d = __ldg(%s + %d);", T.c_str(), pre.c_str(), k, base.c_str(), k));
+            for (int k : need) {
+                if (global)
+                    S(fmt("const %s %s_%d = __ldg(%s + %d);", T.c_str(), pre.c_str(), k, base.c_str(), k));
+                else
+                    S(fmt("const %s %s_%d = (%s)[%d];", T.c_str(), pre.c_str(), k, base.c_str(), k));
+            }
         }
     }
 
@@ -162,27 +170,8 @@ struct Gen {
     }
 
     // ------------------------------------------------------------------ forward
-    void emit_fwd_group(Src& S, int g) const {
-        const std::vector<int>& paths = P->groups[g];
-        S(fmt("__device__ __forceinline__ void fwd_group%d(int e0, int e1, int u, const int* __restrict__ src,", g));
-        S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, %s* __restrict__ orow) {",
-              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
-        S.ind++;
-        std::vector<int> outs;
-        for (int pi : paths) {
-            const PathInfo& p = P->paths[pi];
-            for (int m = 0; m < 2 * p.l3 + 1; ++m) outs.push_back(p.ooff + m);
-        }
-        for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
-        const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
-        S("#pragma unroll 1");
-        S("for (int e = e0; e < e1; ++e) {");
-        S.ind++;
-        S("const int s = __ldg(src + e);");
-        emit_row_loads(S, "xv", fmt("x + ((size_t)s * UVU_U + u) * UVU_DX"), P->Dx, xn);
-        emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
-        S("const " + T + "* __restrict__ we = w + (size_t)e * (UVU_P * UVU_U) + u;");
-        for (int pi : paths) S(fmt("const %s wv_%d = __ldg(we + %d * UVU_U);", T.c_str(), pi, pi));
+    // acc_* += contribution of one edge, from xv_*, yv_*, wv_* already in registers.
+    void emit_fwd_edge(Src& S, const std::vector<int>& paths) const {
         emit_products(S, paths);
         for (int pi : paths) {
             const PathInfo& p = P->paths[pi];
@@ -206,6 +195,30 @@ struct Gen {
                 S("}");
             }
         }
+    }
+
+    void emit_fwd_group(Src& S, int g) const {
+        const std::vector<int>& paths = P->groups[g];
+        S(fmt("__device__ __forceinline__ void fwd_group%d(int e0, int e1, int u, const int* __restrict__ src,", g));
+        S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, %s* __restrict__ orow) {",
+              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S.ind++;
+        std::vector<int> outs;
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            for (int m = 0; m < 2 * p.l3 + 1; ++m) outs.push_back(p.ooff + m);
+        }
+        for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
+        const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+        S("#pragma unroll 1");
+        S("for (int e = e0; e < e1; ++e) {");
+        S.ind++;
+        S("const int s = __ldg(src + e);");
+        emit_row_loads(S, "xv", fmt("x + ((size_t)s * UVU_U + u) * UVU_DX"), P->Dx, xn);
+        emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+        S("const " + T + "* __restrict__ we = w + (size_t)e * (UVU_P * UVU_U) + u;");
+        for (int pi : paths) S(fmt("const %s wv_%d = __ldg(we + %d * UVU_U);", T.c_str(), pi, pi));
+        emit_fwd_edge(S, paths);
         S.ind--;
         S("}");
         for (int k : outs) S(fmt("orow[%d] = acc_%d;", k, k));
@@ -447,6 +460,608 @@ struct Gen {
         S.ind--;
         S("}");
     }
+
+    // ================================================================== pipelined kernels
+    // One producer warp streams the per-edge operands of each owner into a ring of NST shared
+    // memory stages with cp.async.bulk (completion counted on an mbarrier per stage); the
+    // consumer warps compute from shared memory and release the stage on a second mbarrier.
+    // Owners (receivers or senders) are assigned round-robin to persistent CTAs.
+    // Every wait is bounded (about two seconds on the global timer): on expiry the kernel sets
+    // a bit in uvu_status_word, skips the remaining work and returns.
+
+    // Per-edge operand sizes in bytes.
+    size_t wbytes() const { return size_t(P->P) * P->U * P->elem(); }
+    size_t xbytes() const { return size_t(P->U) * P->Dx * P->elem(); }
+    size_t ybytes() const { return size_t(P->Dy) * P->elem(); }
+
+    void emit_pipe_helpers(Src& S) const {
+        S(R"(__device__ unsigned int uvu_status_word;
+#define UVU_DEV_TIMEOUT 1u
+__device__ __forceinline__ unsigned smem_addr(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(unsigned b, unsigned n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(b), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned b, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(b), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(b) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(unsigned b, unsigned parity) {
+  unsigned ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+               : "=r"(ok) : "r"(b), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Slow path of a bounded wait: gives up after about two seconds and records the timeout.
+__device__ __noinline__ bool mbar_wait_slow(unsigned b, unsigned parity) {
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_test(b, parity)) return true;
+    if (global_ns() - t0 > 2000000000ull) {
+      atomicOr(&uvu_status_word, UVU_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait(unsigned b, unsigned parity) {
+  return mbar_test(b, parity) || mbar_wait_slow(b, parity);
+}
+__device__ __forceinline__ void bulk_g2s(unsigned dst, const void* src, unsigned bytes, unsigned bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+// Barrier among the consumer warps only (the producer warp never takes part).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" :: "r"(UVU_NCT) : "memory"); })");
+    }
+
+    // Stage layout of the receiver-ordered kernels (forward and edge backward).
+    struct RecvPipe {
+        int ch = 1, nst = 2;
+        bool xbulk = false, ybulk = false;
+        size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, total = 0;
+        size_t tx_per_edge = 0;
+    };
+    static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
+
+    RecvPipe recv_pipe(bool with_partials, int ncw) const {
+        RecvPipe R;
+        R.xbulk = xbytes() % 16 == 0;
+        R.ybulk = ybytes() % 16 == 0;
+        const size_t pe = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
+        R.ch = int(std::max<size_t>(1, std::min<size_t>(8, 32768 / pe)));
+        const size_t stage = a16(R.ch * wbytes()) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
+                             (R.ybulk ? a16(R.ch * ybytes()) : 0);
+        R.nst = int(std::max<size_t>(2, std::min<size_t>(6, (108 * 1024) / stage)));
+        R.w_off = 0;
+        R.x_off = a16(R.ch * wbytes());
+        R.y_off = R.x_off + (R.xbulk ? a16(R.ch * xbytes()) : 0);
+        R.stage = stage;
+        R.bar_off = R.nst * stage;
+        R.part_off = R.bar_off + 16 * R.nst;
+        R.total = R.part_off + (with_partials ? 2 * size_t(ncw) * R.ch * P->Dy * P->elem() : 0);
+        R.tx_per_edge = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
+        return R;
+    }
+
+    void emit_recv_pipe_defines(Src& S, const RecvPipe& R, const char* pre) const {
+        S(fmt("#define %s_CH %d", pre, R.ch));
+        S(fmt("#define %s_NST %d", pre, R.nst));
+        S(fmt("#define %s_STAGE %zu", pre, R.stage));
+        S(fmt("#define %s_XOFF %zu", pre, R.x_off));
+        S(fmt("#define %s_YOFF %zu", pre, R.y_off));
+        S(fmt("#define %s_BAR %zu", pre, R.bar_off));
+        S(fmt("#define %s_PART %zu", pre, R.part_off));
+        S(fmt("#define %s_TX %zu", pre, R.tx_per_edge));
+    }
+
+    // Producer for the receiver-ordered kernels: w block of the chunk (one copy, the receiver's
+    // edges are contiguous), Y block (one copy), x row of each edge's sender (one copy each).
+    void emit_recv_producer(Src& S, const RecvPipe& R, const char* pre, const char* name) const {
+        S(fmt("__device__ __noinline__ void %s(long long N, const int* __restrict__ off, const int* __restrict__ src,", name));
+        S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, unsigned sbase) {",
+              T.c_str(), T.c_str(), T.c_str()));
+        S.ind++;
+        S("unsigned c = 0;");
+        S("bool dead = false;");
+        S("for (long long r = blockIdx.x; r < N && !dead; r += gridDim.x) {");
+        S.ind++;
+        S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+        S(fmt("for (int eb = e0; eb < e1; eb += %s_CH, ++c) {", pre));
+        S.ind++;
+        S(fmt("const unsigned st = c %% %s_NST;", pre));
+        S(fmt("if (c >= %s_NST && !mbar_wait(sbase + %s_BAR + 8u * (%s_NST + st), ((c / %s_NST) - 1u) & 1u)) { dead = true; break; }",
+              pre, pre, pre, pre));
+        S(fmt("const int ne = min(%s_CH, e1 - eb);", pre));
+        S(fmt("const unsigned full = sbase + %s_BAR + 8u * st;", pre));
+        S(fmt("const unsigned stg = sbase + st * %s_STAGE;", pre));
+        S(fmt("mbar_expect_tx(full, (unsigned)ne * %s_TX);", pre));
+        S(fmt("bulk_g2s(stg, w + (size_t)eb * (UVU_P * UVU_U), (unsigned)ne * %zuu, full);", wbytes()));
+        if (R.ybulk) S(fmt("bulk_g2s(stg + %s_YOFF, Y + (size_t)eb * UVU_DY, (unsigned)ne * %zuu, full);", pre, ybytes()));
+        if (R.xbulk) {
+            S("for (int j = 0; j < ne; ++j) {");
+            S("  const int s = __ldg(src + eb + j);");
+            S(fmt("  bulk_g2s(stg + %s_XOFF + (unsigned)j * %zuu, x + (size_t)s * (UVU_U * UVU_DX), %zuu, full);", pre,
+                  xbytes(), xbytes()));
+            S("}");
+        }
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S("if (dead) {  // let the copies already issued land before the block exits");
+        S(fmt("  const unsigned n = c < %s_NST ? c : %s_NST;", pre, pre));
+        S(fmt("  for (unsigned k = c - n; k < c; ++k) mbar_wait(sbase + %s_BAR + 8u * (k %% %s_NST), (k / %s_NST) & 1u);", pre, pre, pre));
+        S("}");
+        S.ind--;
+        S("}");
+    }
+
+    // Operand loads of edge slot j of a stage for the receiver kernels.
+    void emit_stage_edge_loads(Src& S, const RecvPipe& R, const char* pre, const std::set<int>& xn,
+                               const std::set<int>& yn, const std::vector<int>& paths) const {
+        S("const int e = eb + j;");
+        if (R.xbulk) {
+            emit_row_loads(S, "xv", fmt("reinterpret_cast<const %s*>(stg + %s_XOFF) + (j * UVU_U + u) * UVU_DX", T.c_str(), pre),
+                           P->Dx, xn, false);
+        } else {
+            S("const int s = __ldg(src + e);");
+            emit_row_loads(S, "xv", "x + ((size_t)s * UVU_U + u) * UVU_DX", P->Dx, xn);
+        }
+        if (R.ybulk)
+            emit_row_loads(S, "yv", fmt("reinterpret_cast<const %s*>(stg + %s_YOFF) + j * UVU_DY", T.c_str(), pre), P->Dy, yn,
+                           false);
+        else
+            emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+        S(fmt("const %s* swr = reinterpret_cast<const %s*>(stg) + j * (UVU_P * UVU_U) + u;", T.c_str(), T.c_str()));
+        for (int pi : paths) S(fmt("const %s wv_%d = swr[%d * UVU_U];", T.c_str(), pi, pi));
+    }
+
+    void emit_fwd_v2(Src& S, const RecvPipe& R) const {
+        const int NG = int(P->groups.size());
+        emit_recv_producer(S, R, "FW", "fwd_producer");
+        for (int g = 0; g < NG; ++g) {
+            const std::vector<int>& paths = P->groups[g];
+            const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+            std::vector<int> outs;
+            for (int pi : paths)
+                for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
+            S(fmt("__device__ __forceinline__ void fwd_rcv%d(int e0, int e1, int u, bool uvalid, int lane, unsigned& c, bool& dead,", g));
+            S(fmt("    const unsigned char* smem, unsigned sbase, const int* __restrict__ src, const %s* __restrict__ x,", T.c_str()));
+            S(fmt("    const %s* __restrict__ Y, %s* __restrict__ orow) {", T.c_str(), T.c_str()));
+            S.ind++;
+            for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
+            S("for (int eb = e0; eb < e1; eb += FW_CH, ++c) {");
+            S.ind++;
+            S("const unsigned st = c % FW_NST;");
+            S("if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(sbase + FW_BAR + 8u * st, (c / FW_NST) & 1u));");
+            S("if (dead) continue;");
+            S("const int ne = min(FW_CH, e1 - eb);");
+            S("const unsigned char* stg = smem + st * FW_STAGE;");
+            S("if (uvalid) {");
+            S.ind++;
+            S("#pragma unroll");
+            S("for (int j = 0; j < FW_CH; ++j) {");
+            S.ind++;
+            S("if (j < ne) {");
+            S.ind++;
+            emit_stage_edge_loads(S, R, "FW", xn, yn, paths);
+            emit_fwd_edge(S, paths);
+            S.ind--;
+            S("}");
+            S.ind--;
+            S("}");
+            S.ind--;
+            S("}");
+            S("__syncwarp();");
+            S("if (lane == 0) mbar_arrive(sbase + FW_BAR + 8u * (FW_NST + st));");
+            S.ind--;
+            S("}");
+            S("if (uvalid) {");
+            for (int k : outs) S(fmt("  orow[%d] = acc_%d;", k, k));
+            S("}");
+            S.ind--;
+            S("}");
+        }
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32) uvu_fwd(long long N, const int* __restrict__ off,"));
+        S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
+        S(fmt("    const %s* __restrict__ w, %s* __restrict__ out) {", T.c_str(), T.c_str()));
+        S.ind++;
+        S("extern __shared__ __align__(128) unsigned char smem[];");
+        S("const unsigned sbase = smem_addr(smem);");
+        S("const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;");
+        S("if (tid == 0) {");
+        S("  for (int i = 0; i < FW_NST; ++i) { mbar_init(sbase + FW_BAR + 8u * i, 1u); mbar_init(sbase + FW_BAR + 8u * (FW_NST + i), UVU_NCW); }");
+        S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
+        S("}");
+        S("__syncthreads();");
+        S("if (warp == UVU_NCW) {");
+        S("  if (lane == 0) fwd_producer(N, off, src, x, Y, w, sbase);");
+        S("  return;");
+        S("}");
+        S("const int u = tid % UVU_UP, g = tid / UVU_UP;");
+        S("const bool uvalid = u < UVU_U;");
+        S("unsigned c = 0;");
+        S("bool dead = false;");
+        S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
+        S.ind++;
+        S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+        S(T + "* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
+        for (int g = 0; g < NG; ++g)
+            S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, Y, orow);", g ? "else " : "", g, g));
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+    }
+
+    // Warp transpose-reduction of the dY partials of one edge over the 32 channels of the warp,
+    // then one lane per component stores the warp sum into the stage's partial buffer.
+    // Values are halved level by level (each lane keeps one half and receives the other half of
+    // its xor partner), so D values over 32 lanes take about D shuffles instead of 5 D.
+    void emit_dy_warp_reduce(Src& S, const std::vector<int>& K) const {
+        const int D = int(K.size());
+        int P2 = 1;
+        while (P2 < D) P2 *= 2;
+        std::vector<std::string> v(P2);
+        for (int i = 0; i < P2; ++i) {
+            v[i] = fmt("rv_%d", i);
+            S(fmt("%s %s = %s;", T.c_str(), v[i].c_str(), i < D ? fmt("dyp_%d", K[i]).c_str() : "0"));
+        }
+        int len = P2;
+        int idx_terms_off[5], idx_terms_half[5], nsplit = 0, lowmask = 0;
+        for (int o = 16; o >= 1; o >>= 1) {
+            if (len > 1) {
+                const int h = len / 2;
+                S(fmt("{ const bool hi = (lane & %d) != 0;", o));
+                for (int i = 0; i < h; ++i) {
+                    S(fmt("  const %s snd_%d = hi ? %s : %s;", T.c_str(), i, v[i].c_str(), v[i + h].c_str()));
+                    S(fmt("  const %s kep_%d = hi ? %s : %s;", T.c_str(), i, v[i + h].c_str(), v[i].c_str()));
+                }
+                for (int i = 0; i < h; ++i)
+                    S(fmt("  %s = kep_%d + __shfl_xor_sync(0xffffffffu, snd_%d, %d);", v[i].c_str(), i, i, o));
+                S("}");
+                idx_terms_off[nsplit] = o;
+                idx_terms_half[nsplit] = h;
+                ++nsplit;
+                len = h;
+            } else {
+                S(fmt("%s += __shfl_xor_sync(0xffffffffu, %s, %d);", v[0].c_str(), v[0].c_str(), o));
+                lowmask |= o;
+            }
+        }
+        std::string idx = "0";
+        for (int i = 0; i < nsplit; ++i)
+            idx += fmt(" + ((lane & %d) ? %d : 0)", idx_terms_off[i], idx_terms_half[i]);
+        S(fmt("{ const int idx = %s;", idx.c_str()));
+        bool contiguous = true;
+        for (int i = 1; i < D; ++i) contiguous = contiguous && K[i] == K[0] + i;
+        std::string comp;
+        if (contiguous) {
+            comp = fmt("%d + idx", K[0]);
+        } else {
+            comp = "-1";
+            for (int i = D - 1; i >= 0; --i) comp = fmt("(idx == %d ? %d : %s)", i, K[i], comp.c_str());
+        }
+        S(fmt("  if ((lane & %d) == 0 && idx < %d) part[j * UVU_DY + (%s)] = %s; }", lowmask, D, comp.c_str(), v[0].c_str()));
+        std::set<int> ks(K.begin(), K.end());
+        for (int k = 0; k < P->Dy; ++k)
+            if (!ks.count(k)) S(fmt("if (lane == 0) part[j * UVU_DY + %d] = 0;", k));
+    }
+
+    void emit_edge_v2(Src& S, const RecvPipe& R) const {
+        const int NG = int(P->groups.size());
+        emit_recv_producer(S, R, "EG", "edge_producer");
+        for (int g = 0; g < NG; ++g) {
+            const std::vector<int>& paths = P->groups[g];
+            const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+            std::vector<int> outs;
+            for (int pi : paths)
+                for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
+            S(fmt("__device__ __forceinline__ void edge_rcv%d(long long r, int e0, int e1, int u, bool uvalid, int lane, int warp,", g));
+            S("    int tid, unsigned& c, bool& dead, int& buf, const unsigned char* smem, unsigned sbase,");
+            S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
+            S(fmt("    const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx) {",
+                  T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+            S.ind++;
+            S(fmt("const %s* __restrict__ grow = gout + ((size_t)r * UVU_U + (uvalid ? u : 0)) * UVU_DO;", T.c_str()));
+            for (int k : outs) S(fmt("const %s gv_%d = __ldg(grow + %d);", T.c_str(), k, k));
+            S(fmt("%s* partbase = reinterpret_cast<%s*>(const_cast<unsigned char*>(smem) + EG_PART);", T.c_str(), T.c_str()));
+            S("for (int eb = e0; eb < e1; eb += EG_CH, ++c) {");
+            S.ind++;
+            S("const unsigned st = c % EG_NST;");
+            S("if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(sbase + EG_BAR + 8u * st, (c / EG_NST) & 1u));");
+            S("const int ne = min(EG_CH, e1 - eb);");
+            S("const unsigned char* stg = smem + st * EG_STAGE;");
+            S(fmt("%s* part = partbase + (size_t)(buf * UVU_NCW + warp) * EG_CH * UVU_DY;", T.c_str()));
+            S("if (!dead) {");
+            S.ind++;
+            S("#pragma unroll");
+            S("for (int j = 0; j < EG_CH; ++j) {");
+            S.ind++;
+            S("if (j < ne) {");
+            S.ind++;
+            for (int k : yn) S(fmt("%s dyp_%d = 0;", T.c_str(), k));
+            S("if (uvalid) {");
+            S.ind++;
+            emit_stage_edge_loads(S, R, "EG", xn, yn, paths);
+            S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
+            for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
+            emit_products(S, paths);
+            auto gval = [](int k) { return fmt("gv_%d", k); };
+            S("if (dw) {");
+            S.ind++;
+            emit_bwd_pairs(S, paths, true, false, false, gval);
+            S.ind--;
+            S("}");
+            emit_bwd_pairs(S, paths, false, true, true, gval);
+            S("if (dx) {");
+            S.ind++;
+            if (!R.xbulk) {
+                S(T + "* __restrict__ dxr = dx + ((size_t)s * UVU_U + u) * UVU_DX;");
+            } else {
+                S("const int s = __ldg(src + e);");
+                S(T + "* __restrict__ dxr = dx + ((size_t)s * UVU_U + u) * UVU_DX;");
+            }
+            emit_dx_atomics(S, xn);
+            S.ind--;
+            S("}");
+            S.ind--;
+            S("}");  // uvalid
+            S("if (dY) {");
+            S.ind++;
+            std::vector<int> K(yn.begin(), yn.end());
+            emit_dy_warp_reduce(S, K);
+            S.ind--;
+            S("}");
+            S.ind--;
+            S("}");  // j < ne
+            S.ind--;
+            S("}");  // j
+            S("__syncwarp();");
+            S("if (lane == 0) mbar_arrive(sbase + EG_BAR + 8u * (EG_NST + st));");
+            S.ind--;
+            S("}");  // !dead
+            S("consumer_sync();");
+            S("if (!dead && dY) {");
+            S.ind++;
+            S("for (int t = tid; t < ne * UVU_DY; t += UVU_NCT) {");
+            S.ind++;
+            S("const int j = t / UVU_DY, k = t - j * UVU_DY;");
+            S(T + " acc = 0;");
+            S("#pragma unroll");
+            S("for (int wp = 0; wp < UVU_NCW; ++wp) acc += partbase[((size_t)(buf * UVU_NCW + wp) * EG_CH + j) * UVU_DY + k];");
+            S("dY[(size_t)(eb + j) * UVU_DY + k] = acc;");
+            S.ind--;
+            S("}");
+            S.ind--;
+            S("}");
+            S("buf ^= 1;");
+            S.ind--;
+            S("}");
+            S.ind--;
+            S("}");
+        }
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32) uvu_bwd_edge(long long N, const int* __restrict__ off,"));
+        S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
+        S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
+              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S(fmt("    %s* __restrict__ dx) {", T.c_str()));
+        S.ind++;
+        S("extern __shared__ __align__(128) unsigned char smem[];");
+        S("const unsigned sbase = smem_addr(smem);");
+        S("const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;");
+        S("if (tid == 0) {");
+        S("  for (int i = 0; i < EG_NST; ++i) { mbar_init(sbase + EG_BAR + 8u * i, 1u); mbar_init(sbase + EG_BAR + 8u * (EG_NST + i), UVU_NCW); }");
+        S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
+        S("}");
+        S("__syncthreads();");
+        S("if (warp == UVU_NCW) {");
+        S("  if (lane == 0) edge_producer(N, off, src, x, Y, w, sbase);");
+        S("  return;");
+        S("}");
+        S("const int u = tid % UVU_UP, g = tid / UVU_UP;");
+        S("const bool uvalid = u < UVU_U;");
+        S("unsigned c = 0;");
+        S("bool dead = false;");
+        S("int buf = 0;");
+        S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
+        S.ind++;
+        S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+        for (int g = 0; g < NG; ++g)
+            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, dead, buf, smem, sbase, src, x, Y, gout, dY, dw, dx);",
+                  g ? "else " : "", g, g));
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+    }
+
+    void emit_dx_atomics(Src& S, const std::set<int>& xn) const {
+        if (!f64 && P->Dx % 4 == 0) {
+            std::set<int> chunks;
+            for (int k : xn) chunks.insert(k / 4);
+            for (int c : chunks) {
+                std::string v[4];
+                for (int i = 0; i < 4; ++i) v[i] = xn.count(4 * c + i) ? fmt("dxp_%d", 4 * c + i) : "0.0f";
+                S(fmt("red_add_v4(dxr + %d, %s, %s, %s, %s);", 4 * c, v[0].c_str(), v[1].c_str(), v[2].c_str(), v[3].c_str()));
+            }
+        } else {
+            for (int k : xn) S(fmt("atomicAdd(dxr + %d, dxp_%d);", k, k));
+        }
+    }
+
+    // ------------------------------------------------------------------ sender-stationary dx
+    struct SendPipe {
+        int ut = 32, ntile = 1, ch = 1, nst = 2;
+        bool ybulk = false;
+        size_t wt = 0, gt = 0, w_off = 0, g_off = 0, y_off = 0, stage = 0, bar_off = 0, total = 0, tx = 0;
+    };
+
+    SendPipe send_pipe() const {
+        SendPipe D;
+        D.ut = std::min(P->U_pad, 128);
+        D.ntile = P->U_pad / D.ut;
+        D.ybulk = ybytes() % 16 == 0;
+        D.wt = size_t(P->P) * D.ut * P->elem();
+        D.gt = size_t(D.ut) * P->Do * P->elem();
+        const size_t pe = D.wt + D.gt + (D.ybulk ? ybytes() : 0);
+        D.ch = int(std::max<size_t>(1, std::min<size_t>(8, 32768 / pe)));
+        D.w_off = 0;
+        D.g_off = a16(D.ch * D.wt);
+        D.y_off = D.g_off + a16(D.ch * D.gt);
+        D.stage = D.y_off + (D.ybulk ? a16(D.ch * ybytes()) : 0);
+        D.nst = int(std::max<size_t>(2, std::min<size_t>(6, (108 * 1024) / D.stage)));
+        D.bar_off = D.nst * D.stage;
+        D.total = D.bar_off + 16 * D.nst;
+        D.tx = pe;
+        return D;
+    }
+
+    // Requirements of the tiled copies: channel tiles start and end on 16-byte boundaries.
+    bool send_pipe_ok(const SendPipe& D) const {
+        return P->U % D.ut == 0 && (size_t(D.ut) * P->elem()) % 16 == 0 && D.gt % 16 == 0 &&
+               (size_t(P->U) * P->Do * P->elem()) % 16 == 0;
+    }
+
+    void emit_dx_v2(Src& S, const SendPipe& D) const {
+        std::vector<int> all;
+        for (int p = 0; p < P->P; ++p) all.push_back(p);
+        const std::set<int> xn = x_needed(all), yn = y_needed(all);
+        S(fmt("#define DX_UT %d", D.ut));
+        S(fmt("#define DX_NT %d", D.ntile));
+        S(fmt("#define DX_CH %d", D.ch));
+        S(fmt("#define DX_NST %d", D.nst));
+        S(fmt("#define DX_STAGE %zu", D.stage));
+        S(fmt("#define DX_GOFF %zu", D.g_off));
+        S(fmt("#define DX_YOFF %zu", D.y_off));
+        S(fmt("#define DX_BAR %zu", D.bar_off));
+        S(fmt("#define DX_TX %zu", D.tx));
+        S(fmt("#define DX_NCW %d", D.ut / 32));
+        // producer
+        S(fmt("__device__ __noinline__ void dx_producer(long long N, const int* __restrict__ soff, const int* __restrict__ seid,"));
+        S(fmt("    const int* __restrict__ srecv, const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ gout,",
+              T.c_str(), T.c_str(), T.c_str()));
+        S("    unsigned sbase) {");
+        S.ind++;
+        S("unsigned c = 0;");
+        S("bool dead = false;");
+        S("for (long long it = blockIdx.x; it < N * DX_NT && !dead; it += gridDim.x) {");
+        S.ind++;
+        S("const long long sn = it / DX_NT;");
+        S("const int u0 = (int)(it - sn * DX_NT) * DX_UT;");
+        S("const int k0 = __ldg(soff + sn), k1 = __ldg(soff + sn + 1);");
+        S("for (int kb = k0; kb < k1; kb += DX_CH, ++c) {");
+        S.ind++;
+        S("const unsigned st = c % DX_NST;");
+        S("if (c >= DX_NST && !mbar_wait(sbase + DX_BAR + 8u * (DX_NST + st), ((c / DX_NST) - 1u) & 1u)) { dead = true; break; }");
+        S("const int ne = min(DX_CH, k1 - kb);");
+        S("const unsigned full = sbase + DX_BAR + 8u * st;");
+        S("const unsigned stg = sbase + st * DX_STAGE;");
+        S("mbar_expect_tx(full, (unsigned)ne * DX_TX);");
+        S("for (int j = 0; j < ne; ++j) {");
+        S.ind++;
+        S("const int e = __ldg(seid + kb + j), r = __ldg(srecv + kb + j);");
+        if (D.ut == P->U) {
+            S(fmt("bulk_g2s(stg + (unsigned)j * %zuu, w + (size_t)e * (UVU_P * UVU_U), %zuu, full);", D.wt, D.wt));
+        } else {
+            S("#pragma unroll 1");
+            S(fmt("for (int p = 0; p < UVU_P; ++p) bulk_g2s(stg + (unsigned)j * %zuu + (unsigned)p * %zuu, w + ((size_t)e * UVU_P + p) * UVU_U + u0, %zuu, full);",
+                  D.wt, size_t(D.ut) * P->elem(), size_t(D.ut) * P->elem()));
+        }
+        S(fmt("bulk_g2s(stg + DX_GOFF + (unsigned)j * %zuu, gout + ((size_t)r * UVU_U + u0) * UVU_DO, %zuu, full);", D.gt, D.gt));
+        if (D.ybulk) S(fmt("bulk_g2s(stg + DX_YOFF + (unsigned)j * %zuu, Y + (size_t)e * UVU_DY, %zuu, full);", ybytes(), ybytes()));
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S("if (dead) {");
+        S("  const unsigned n = c < DX_NST ? c : DX_NST;");
+        S("  for (unsigned k = c - n; k < c; ++k) mbar_wait(sbase + DX_BAR + 8u * (k % DX_NST), (k / DX_NST) & 1u);");
+        S("}");
+        S.ind--;
+        S("}");
+        // kernel
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(DX_UT + 32) uvu_bwd_dx(long long N, const int* __restrict__ soff,"));
+        S(fmt("    const int* __restrict__ seid, const int* __restrict__ srecv, const %s* __restrict__ Y,", T.c_str()));
+        S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dx) {", T.c_str(), T.c_str(), T.c_str()));
+        S.ind++;
+        S("extern __shared__ __align__(128) unsigned char smem[];");
+        S("const unsigned sbase = smem_addr(smem);");
+        S("const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;");
+        S("if (tid == 0) {");
+        S("  for (int i = 0; i < DX_NST; ++i) { mbar_init(sbase + DX_BAR + 8u * i, 1u); mbar_init(sbase + DX_BAR + 8u * (DX_NST + i), DX_NCW); }");
+        S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
+        S("}");
+        S("__syncthreads();");
+        S("if (warp == DX_NCW) {");
+        S("  if (lane == 0) dx_producer(N, soff, seid, srecv, Y, w, gout, sbase);");
+        S("  return;");
+        S("}");
+        S("const int ul = tid;");
+        S("unsigned c = 0;");
+        S("bool dead = false;");
+        S("for (long long it = blockIdx.x; it < N * DX_NT; it += gridDim.x) {");
+        S.ind++;
+        S("const long long sn = it / DX_NT;");
+        S("const int u = (int)(it - sn * DX_NT) * DX_UT + ul;");
+        S("const bool uvalid = u < UVU_U;");
+        S("const int k0 = __ldg(soff + sn), k1 = __ldg(soff + sn + 1);");
+        for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
+        S("for (int kb = k0; kb < k1; kb += DX_CH, ++c) {");
+        S.ind++;
+        S("const unsigned st = c % DX_NST;");
+        S("if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(sbase + DX_BAR + 8u * st, (c / DX_NST) & 1u));");
+        S("if (dead) continue;");
+        S("const int ne = min(DX_CH, k1 - kb);");
+        S("const unsigned char* stg = smem + st * DX_STAGE;");
+        S("if (uvalid) {");
+        S.ind++;
+        S("#pragma unroll");
+        S("for (int j = 0; j < DX_CH; ++j) {");
+        S.ind++;
+        S("if (j < ne) {");
+        S.ind++;
+        if (D.ybulk)
+            emit_row_loads(S, "yv", fmt("reinterpret_cast<const %s*>(stg + DX_YOFF) + j * UVU_DY", T.c_str()), P->Dy, yn, false);
+        else {
+            S("const int e = __ldg(seid + kb + j);");
+            emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+        }
+        S(fmt("const %s* swr = reinterpret_cast<const %s*>(stg) + j * (UVU_P * DX_UT) + ul;", T.c_str(), T.c_str()));
+        for (int pi : all) S(fmt("const %s wv_%d = swr[%d * DX_UT];", T.c_str(), pi, pi));
+        S(fmt("const %s* sgr = reinterpret_cast<const %s*>(stg + DX_GOFF) + (j * DX_UT + ul) * UVU_DO;", T.c_str(), T.c_str()));
+        auto gval = [](int k) { return fmt("sgr[%d]", k); };
+        emit_bwd_pairs(S, all, false, false, true, gval);
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S("__syncwarp();");
+        S("if (lane == 0) mbar_arrive(sbase + DX_BAR + 8u * (DX_NST + st));");
+        S.ind--;
+        S("}");
+        S("if (uvalid) {");
+        S.ind++;
+        S(T + "* __restrict__ dxr = dx + ((size_t)sn * UVU_U + u) * UVU_DX;");
+        for (int k = 0; k < P->Dx; ++k) S(fmt("dxr[%d] = %s;", k, xn.count(k) ? fmt("dxp_%d", k).c_str() : "0"));
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+    }
 };
 
 }  // namespace
@@ -466,10 +1081,28 @@ std::string emit_source(Plan* plan) {
     const int segs = NG * ((UP + 31) / 32);
     const int spb = std::max(1, 128 / UP);
     const int ch = 16;
-    plan->g_fwd = {rpb * owner_threads, rpb, 0};
-    plan->edge_chunk = ch;
-    plan->g_edge = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem()};
-    plan->g_dx = {spb * UP, spb, 0};
+    const int ncw = NG * UP / 32;
+
+    // Pipelined (bulk-copy) kernels need whole warps per owner and 16-byte multiples for the
+    // per-edge weight rows; otherwise the direct-load kernels are emitted.
+    const bool pipe_recv = U >= 32 && G.wbytes() % 16 == 0 && ncw * 32 + 32 <= 1024;
+    Gen::RecvPipe RF = G.recv_pipe(false, ncw), RE = G.recv_pipe(true, ncw);
+    Gen::SendPipe SD = G.send_pipe();
+    const bool pipe_dx = U >= 32 && G.send_pipe_ok(SD);
+    plan->pipelined_recv = pipe_recv;
+    plan->pipelined_dx = pipe_dx;
+    if (pipe_recv) {
+        plan->g_fwd = {ncw * 32 + 32, 1, RF.total, true};
+        plan->g_edge = {ncw * 32 + 32, 1, RE.total, true};
+    } else {
+        plan->g_fwd = {rpb * owner_threads, rpb, 0, false};
+        plan->g_edge = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem(), false};
+    }
+    plan->edge_chunk = pipe_recv ? RE.ch : ch;
+    if (pipe_dx)
+        plan->g_dx = {SD.ut + 32, 1, SD.total, true, SD.ntile};
+    else
+        plan->g_dx = {spb * UP, spb, 0, false};
 
     Src S;
     S("// Generated by the UVU planner. Channel-wise CG tensor-product graph convolution.");
@@ -494,6 +1127,8 @@ std::string emit_source(Plan* plan) {
     S(fmt("#define UVU_CH %d", ch));
     S(fmt("#define UVU_SPB %d", spb));
     S(fmt("#define UVU_DX_TPB %d", spb * UP));
+    S(fmt("#define UVU_NCW %d", ncw));
+    S(fmt("#define UVU_NCT %d", ncw * 32));
     S("// Block-wide barrier usable from the per-group code paths: the non-aligned form may be");
     S("// reached from different call sites, as long as every thread of the block arrives the same");
     S("// number of times (each group runs the same uniform chunk loop).");
@@ -501,51 +1136,62 @@ std::string emit_source(Plan* plan) {
     S("__device__ __forceinline__ void red_add_v4(float* a, float p, float q, float r, float s) {");
     S("  asm volatile(\"red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\" :: \"l\"(a), \"f\"(p), \"f\"(q), \"f\"(r), \"f\"(s) : \"memory\");");
     S("}");
-    for (int g = 0; g < NG; ++g) G.emit_fwd_group(S, g);
-    S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_TPB) uvu_fwd(long long N, const int* __restrict__ off,"));
-    S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", G.T.c_str(), G.T.c_str()));
-    S(fmt("    const %s* __restrict__ w, %s* __restrict__ out) {", G.T.c_str(), G.T.c_str()));
-    S("  const int u = threadIdx.x % UVU_UP;");
-    S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
-    S("  const long long r = (long long)blockIdx.x * UVU_RPB + threadIdx.x / (UVU_UP * UVU_G);");
-    S("  if (r >= N || u >= UVU_U) return;");
-    S("  const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
-    S("  " + G.T + "* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
-    for (int g = 0; g < NG; ++g)
-        S(fmt("  %sif (g == %d) fwd_group%d(e0, e1, u, src, x, Y, w, orow);", g ? "else " : "", g, g));
-    S("}");
+    G.emit_pipe_helpers(S);
+    if (pipe_recv) {
+        G.emit_recv_pipe_defines(S, RF, "FW");
+        G.emit_recv_pipe_defines(S, RE, "EG");
+        G.emit_fwd_v2(S, RF);
+        G.emit_edge_v2(S, RE);
+    } else {
+        for (int g = 0; g < NG; ++g) G.emit_fwd_group(S, g);
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_TPB) uvu_fwd(long long N, const int* __restrict__ off,"));
+        S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", G.T.c_str(), G.T.c_str()));
+        S(fmt("    const %s* __restrict__ w, %s* __restrict__ out) {", G.T.c_str(), G.T.c_str()));
+        S("  const int u = threadIdx.x % UVU_UP;");
+        S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
+        S("  const long long r = (long long)blockIdx.x * UVU_RPB + threadIdx.x / (UVU_UP * UVU_G);");
+        S("  if (r >= N || u >= UVU_U) return;");
+        S("  const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+        S("  " + G.T + "* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
+        for (int g = 0; g < NG; ++g)
+            S(fmt("  %sif (g == %d) fwd_group%d(e0, e1, u, src, x, Y, w, orow);", g ? "else " : "", g, g));
+        S("}");
 
-    for (int g = 0; g < NG; ++g) G.emit_edge_group(S, g);
-    S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_TPB) uvu_bwd_edge(long long N, const int* __restrict__ off,"));
-    S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", G.T.c_str(), G.T.c_str()));
-    S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
-          G.T.c_str(), G.T.c_str(), G.T.c_str(), G.T.c_str()));
-    S(fmt("    %s* __restrict__ dx) {", G.T.c_str()));
-    S(fmt("  extern __shared__ __align__(16) unsigned char smem_raw[];"));
-    S(fmt("  %s* sred = reinterpret_cast<%s*>(smem_raw);", G.T.c_str(), G.T.c_str()));
-    S("  __shared__ int s_e0[UVU_RPB], s_e1[UVU_RPB], s_nch;");
-    S("  const int u = threadIdx.x % UVU_UP;");
-    S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
-    S("  const int rl = threadIdx.x / (UVU_UP * UVU_G);");
-    S("  const long long r = (long long)blockIdx.x * UVU_RPB + rl;");
-    S("  const bool rvalid = r < N;");
-    S("  const bool valid = rvalid && u < UVU_U;");
-    S("  if (threadIdx.x == 0) s_nch = 0;");
-    S("  __syncthreads();");
-    S("  if (threadIdx.x % (UVU_UP * UVU_G) == 0) {");
-    S("    const int a = rvalid ? __ldg(off + r) : 0, b = rvalid ? __ldg(off + r + 1) : 0;");
-    S("    s_e0[rl] = a; s_e1[rl] = b;");
-    S("    atomicMax(&s_nch, (b - a + UVU_CH - 1) / UVU_CH);");
-    S("  }");
-    S("  __syncthreads();");
-    S("  const int nchunks = s_nch;");
-    S("  const int seg = g * ((UVU_UP + 31) / 32) + u / 32;");
-    S("  const int lane_in_seg = u % UVU_SEGW;");
-    for (int g = 0; g < NG; ++g)
-        S(fmt("  %sif (g == %d) edge_group%d(rl, seg, lane_in_seg, valid, s_e0[rl], s_e1[rl], nchunks, r, u, src, x, Y, w, gout, dY, dw, dx, sred, s_e0, s_e1);",
-              g ? "else " : "", g, g));
-    S("}");
-    G.emit_dx_kernel(S);
+        for (int g = 0; g < NG; ++g) G.emit_edge_group(S, g);
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_TPB) uvu_bwd_edge(long long N, const int* __restrict__ off,"));
+        S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", G.T.c_str(), G.T.c_str()));
+        S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
+              G.T.c_str(), G.T.c_str(), G.T.c_str(), G.T.c_str()));
+        S(fmt("    %s* __restrict__ dx) {", G.T.c_str()));
+        S(fmt("  extern __shared__ __align__(16) unsigned char smem_raw[];"));
+        S(fmt("  %s* sred = reinterpret_cast<%s*>(smem_raw);", G.T.c_str(), G.T.c_str()));
+        S("  __shared__ int s_e0[UVU_RPB], s_e1[UVU_RPB], s_nch;");
+        S("  const int u = threadIdx.x % UVU_UP;");
+        S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
+        S("  const int rl = threadIdx.x / (UVU_UP * UVU_G);");
+        S("  const long long r = (long long)blockIdx.x * UVU_RPB + rl;");
+        S("  const bool rvalid = r < N;");
+        S("  const bool valid = rvalid && u < UVU_U;");
+        S("  if (threadIdx.x == 0) s_nch = 0;");
+        S("  __syncthreads();");
+        S("  if (threadIdx.x % (UVU_UP * UVU_G) == 0) {");
+        S("    const int a = rvalid ? __ldg(off + r) : 0, b = rvalid ? __ldg(off + r + 1) : 0;");
+        S("    s_e0[rl] = a; s_e1[rl] = b;");
+        S("    atomicMax(&s_nch, (b - a + UVU_CH - 1) / UVU_CH);");
+        S("  }");
+        S("  __syncthreads();");
+        S("  const int nchunks = s_nch;");
+        S("  const int seg = g * ((UVU_UP + 31) / 32) + u / 32;");
+        S("  const int lane_in_seg = u % UVU_SEGW;");
+        for (int g = 0; g < NG; ++g)
+            S(fmt("  %sif (g == %d) edge_group%d(rl, seg, lane_in_seg, valid, s_e0[rl], s_e1[rl], nchunks, r, u, src, x, Y, w, gout, dY, dw, dx, sred, s_e0, s_e1);",
+                  g ? "else " : "", g, g));
+        S("}");
+    }
+    if (pipe_dx)
+        G.emit_dx_v2(S, SD);
+    else
+        G.emit_dx_kernel(S);
     return S.o.str();
 }
 

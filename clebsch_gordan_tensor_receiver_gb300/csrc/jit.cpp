@@ -104,14 +104,45 @@ uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string
             return UVU_ERR_CUDA;
         }
     }
-    if (plan->g_edge.smem > 48 * 1024) {
-        ce = cudaFuncSetAttribute(reinterpret_cast<const void*>(m.bwd_edge),
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize, int(plan->g_edge.smem));
-        if (ce != cudaSuccess) {
-            *err = std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(ce);
-            cudaLibraryUnload(m.lib);
-            return UVU_ERR_CUDA;
+    struct {
+        cudaKernel_t k;
+        const KernelGeom* g;
+        int* occ;
+        const char* name;
+    } kk[] = {{m.fwd, &plan->g_fwd, &m.occ_fwd, "uvu_fwd"},
+              {m.bwd_edge, &plan->g_edge, &m.occ_edge, "uvu_bwd_edge"},
+              {m.bwd_dx, &plan->g_dx, &m.occ_dx, "uvu_bwd_dx"}};
+    for (auto& k : kk) {
+        const void* f = reinterpret_cast<const void*>(k.k);
+        if (k.g->smem > 48 * 1024) {
+            ce = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(k.g->smem));
+            if (ce != cudaSuccess) {
+                *err = std::string("cudaFuncSetAttribute(") + k.name + "): " + cudaGetErrorString(ce);
+                cudaLibraryUnload(m.lib);
+                return UVU_ERR_CUDA;
+            }
         }
+        int occ = 0;
+        ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, k.g->threads, k.g->smem);
+        if (ce != cudaSuccess || occ < 1) {
+            *err = std::string("kernel ") + k.name + " cannot be resident (" +
+                   (ce != cudaSuccess ? cudaGetErrorString(ce) : "occupancy 0") + ")";
+            cudaLibraryUnload(m.lib);
+            return UVU_ERR_UNSUPPORTED;
+        }
+        *k.occ = occ;
+    }
+    ce = cudaDeviceGetAttribute(&m.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (ce == cudaSuccess) {
+        size_t bytes = 0;
+        void* ptr = nullptr;
+        ce = cudaLibraryGetGlobal(&ptr, &bytes, m.lib, "uvu_status_word");
+        m.status_word = static_cast<unsigned*>(ptr);
+    }
+    if (ce != cudaSuccess) {
+        *err = std::string("module set-up: ") + cudaGetErrorString(ce);
+        cudaLibraryUnload(m.lib);
+        return UVU_ERR_CUDA;
     }
     auto res = plan->modules.emplace(dev, m);
     *out = &res.first->second;

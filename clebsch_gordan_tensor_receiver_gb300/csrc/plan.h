@@ -36,14 +36,19 @@ struct PathInfo {
 
 // Launch geometry of one generated kernel.
 struct KernelGeom {
-    int threads = 0;        // threads per block
-    int owners_per_block = 0;  // receivers (or senders) per block
-    size_t smem = 0;        // dynamic shared memory bytes
+    int threads = 0;           // threads per block
+    int owners_per_block = 0;  // receivers (or senders) per block (non-persistent kernels)
+    size_t smem = 0;           // dynamic shared memory bytes
+    bool persistent = false;   // grid = resident blocks, owners assigned round-robin
+    int tiles = 1;             // work items per owner (channel tiles) for persistent kernels
 };
 
 struct DeviceModule {
     cudaLibrary_t lib = nullptr;
     cudaKernel_t fwd = nullptr, bwd_edge = nullptr, bwd_dx = nullptr;
+    int sm_count = 0;
+    int occ_fwd = 1, occ_edge = 1, occ_dx = 1;  // resident blocks per SM
+    unsigned* status_word = nullptr;            // device address of uvu_status_word
 };
 
 struct Plan {
@@ -57,6 +62,7 @@ struct Plan {
     std::vector<std::vector<int>> groups;  // path ids per register group
     KernelGeom g_fwd, g_edge, g_dx;
     int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
+    bool pipelined_recv = false, pipelined_dx = false;
     std::string source, log;
     std::vector<char> cubin;
     std::mutex mu;

@@ -26,6 +26,7 @@ STATUS = {0: "UVU_OK", 1: "UVU_ERR_INVALID_ARGUMENT", 2: "UVU_ERR_UNSUPPORTED",
 # every symbol declared in include/uvu.h
 EXPORTS = (
     "uvu_plan_create", "uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
+    "uvu_plan_device_status",
     "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
     "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx", "uvu_conv_bwd",
     "uvu_status_string", "uvu_last_error_message",
@@ -49,6 +50,7 @@ def _load():
         "uvu_plan_info": [P, P, P, P, P, P, P],
         "uvu_plan_cg": [P, I, P],
         "uvu_plan_source": [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
+        "uvu_plan_device_status": [P, ctypes.POINTER(ctypes.c_uint), I],
         "uvu_csr_from_sorted_recv": [I64, I64, P, P, P],
         "uvu_csr_transpose_workspace": [I64, I64, ctypes.POINTER(SZ)],
         "uvu_csr_transpose": [I64, I64, P, P, P, P, P, P, SZ, P],
@@ -89,6 +91,7 @@ def _wrap(name):
 
 
 for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
+           "uvu_plan_device_status",
            "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
            "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx",
            "uvu_conv_bwd"):
@@ -159,6 +162,12 @@ class Plan:
         out = np.zeros((2 * l1 + 1, 2 * l2 + 1, 2 * l3 + 1))
         uvu_plan_cg(self.handle, path, out.ctypes.data_as(ctypes.c_void_p))
         return out
+
+    def device_status(self, reset: bool = True) -> int:
+        """Status word of the plan's kernels on the current device (0 = no timeout)."""
+        w = ctypes.c_uint()
+        uvu_plan_device_status(self.handle, ctypes.byref(w), int(reset))
+        return w.value
 
     def source(self):
         s, l = ctypes.c_char_p(), ctypes.c_char_p()

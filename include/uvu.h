@@ -102,6 +102,14 @@ uvu_status uvu_plan_cg(uvu_plan_t plan, int path, double *out);
  * log (ptxas resource usage).  Either pointer may be NULL. */
 uvu_status uvu_plan_source(uvu_plan_t plan, const char **source, const char **compile_log);
 
+/* Device-side status of the plan's kernels on the current device: bit 0 (UVU_DEV_TIMEOUT) is set
+ * when a pipelined kernel gave up waiting for a shared-memory stage (about two seconds) and
+ * skipped the rest of its work, so its outputs are not valid.  Synchronous: waits for all work
+ * on the device, copies the word to *word and, if reset != 0, clears it.  Loads the plan's
+ * module on the current device if needed. */
+#define UVU_DEV_TIMEOUT 1u
+uvu_status uvu_plan_device_status(uvu_plan_t plan, unsigned *word, int reset);
+
 /* ------------------------------------------------------------------------- graph build ---- */
 
 /* Receiver CSR from receiver-sorted edges ("Receiver-streaming convolutions ...", opening post,

@@ -52,6 +52,10 @@ class Problem:
         dt = torch.float64 if self.f64 else torch.float32
         return torch.empty(*shape, dtype=dt, device="cuda")
 
+    def status_ok(self):
+        """No kernel of this plan reported a bounded-wait timeout on the device."""
+        return self.plan.device_status(reset=True) == 0
+
     def fwd(self):
         i = self.plan.info
         out = self.empty(self.N, i.mul, i.dim_out)

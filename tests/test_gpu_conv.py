@@ -26,6 +26,7 @@ def _full_compare(P):
         check(dY, rdY, P.f64, "dY")
         check(dw, rdw, P.f64, "dw")
         check(dx, rdx, P.f64, f"dx mode {mode}")
+    assert P.status_ok()
 
 
 def test_tiny_workload_all_outputs():
@@ -103,6 +104,7 @@ def test_full_size_sampled(key):
     tol = 1e-10 if P.f64 else 2e-5
     for a, b, name in ((dx, P.d["x"], "dx"), (dY, P.d["Y"], "dY"), (dw, P.d["w"], "dw")):
         assert s(a, b) == pytest.approx(ref, rel=tol), name
+    assert P.status_ok()
 
 
 def test_deterministic_kernels_repeat_bitwise():
@@ -114,6 +116,7 @@ def test_deterministic_kernels_repeat_bitwise():
         a2 = P.bwd(uvu.UVU_DX_SENDER)
         for t1, t2 in zip(a1, a2):
             assert torch.equal(t1, t2)
+    assert P.status_ok()
 
 
 def test_graph_validate():
