@@ -559,7 +559,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S(fmt("#define %s_BAR %zu", pre, R.bar_off));
         S(fmt("#define %s_PART %zu", pre, R.part_off));
         S(fmt("#define %s_TX %zu", pre, R.tx_per_edge));
+        S(fmt("#define %s_MINB %d", pre, std::min(minb(R.total), pre[0] == 'F' ? P->minb[0] : P->minb[1])));
     }
+    // Blocks per SM the shared-memory footprint allows (capped at 2): the register budget the
+    // compiler may use is sized so that this many blocks stay resident.
+    static int minb(size_t smem) { return int(std::max<size_t>(1, std::min<size_t>(2, (227 * 1024) / (smem + 1024)))); }
 
     // Producer for the receiver-ordered kernels: w block of the chunk (one copy, the receiver's
     // edges are contiguous), Y block (one copy), x row of each edge's sender (one copy each).
@@ -669,7 +673,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
             S.ind--;
             S("}");
         }
-        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32) uvu_fwd(long long N, const int* __restrict__ off,"));
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, FW_MINB) uvu_fwd(long long N, const int* __restrict__ off,"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
         S(fmt("    const %s* __restrict__ w, %s* __restrict__ out) {", T.c_str(), T.c_str()));
         S.ind++;
@@ -848,7 +852,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
             S.ind--;
             S("}");
         }
-        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32) uvu_bwd_edge(long long N, const int* __restrict__ off,"));
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, EG_MINB) uvu_bwd_edge(long long N, const int* __restrict__ off,"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
         S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
               T.c_str(), T.c_str(), T.c_str(), T.c_str()));
@@ -944,6 +948,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S(fmt("#define DX_BAR %zu", D.bar_off));
         S(fmt("#define DX_TX %zu", D.tx));
         S(fmt("#define DX_NCW %d", D.ut / 32));
+        S(fmt("#define DX_MINB %d", std::min(minb(D.total), P->minb[2])));
         // producer
         S(fmt("__device__ __noinline__ void dx_producer(long long N, const int* __restrict__ soff, const int* __restrict__ seid,"));
         S(fmt("    const int* __restrict__ srecv, const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ gout,",
@@ -990,7 +995,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S.ind--;
         S("}");
         // kernel
-        S(fmt("extern \"C\" __global__ void __launch_bounds__(DX_UT + 32) uvu_bwd_dx(long long N, const int* __restrict__ soff,"));
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(DX_UT + 32, DX_MINB) uvu_bwd_dx(long long N, const int* __restrict__ soff,"));
         S(fmt("    const int* __restrict__ seid, const int* __restrict__ srecv, const %s* __restrict__ Y,", T.c_str()));
         S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dx) {", T.c_str(), T.c_str(), T.c_str()));
         S.ind++;

@@ -5,6 +5,7 @@
 // never inspected.  Identical sources share one compilation through a process-wide cache.
 #include <nvrtc.h>
 
+#include <cstdlib>
 #include <functional>
 #include <map>
 #include <mutex>
@@ -52,6 +53,19 @@ uvu_status nvrtc_compile(const std::string& src, CacheEntry* out, std::string* e
 }
 
 }  // namespace
+
+// Spill store bytes ptxas reported for one entry function (0 if not found).
+size_t spill_bytes(const std::string& log, const char* kernel) {
+    const std::string key = std::string("Function properties for ") + kernel + "\n";
+    const size_t at = log.find(key);
+    if (at == std::string::npos) return 0;
+    const size_t eol = log.find('\n', at + key.size());
+    const std::string line = log.substr(at + key.size(), eol == std::string::npos ? std::string::npos : eol - at - key.size());
+    const size_t sp = line.find(" bytes spill stores");
+    if (sp == std::string::npos) return 0;
+    size_t b = line.rfind(' ', sp - 1);
+    return size_t(std::strtoull(line.c_str() + (b == std::string::npos ? 0 : b + 1), nullptr, 10));
+}
 
 uvu_status compile_plan(Plan* plan, std::string* err) {
     {

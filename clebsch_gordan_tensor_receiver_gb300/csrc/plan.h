@@ -63,6 +63,9 @@ struct Plan {
     KernelGeom g_fwd, g_edge, g_dx;
     int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
     bool pipelined_recv = false, pipelined_dx = false;
+    // Upper bound on resident blocks per SM that the register budget is sized for, per kernel
+    // (fwd, edge, dx); lowered to 1 for a kernel whose two-block budget makes ptxas spill.
+    int minb[3] = {2, 2, 2};
     std::string source, log;
     std::vector<char> cubin;
     std::mutex mu;
@@ -82,6 +85,7 @@ std::string emit_source(Plan* plan);
 
 // jit.cpp
 uvu_status compile_plan(Plan* plan, std::string* err);
+size_t spill_bytes(const std::string& log, const char* kernel);
 uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string* err);
 
 // status.cpp
