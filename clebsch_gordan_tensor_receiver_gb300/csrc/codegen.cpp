@@ -22,6 +22,7 @@
 // products: acc[m3] += (w_p x0) (+-y[m2]).
 #include <cmath>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <map>
 #include <set>
@@ -474,6 +475,31 @@ struct Gen {
     size_t xbytes() const { return size_t(P->U) * P->Dx * P->elem(); }
     size_t ybytes() const { return size_t(P->Dy) * P->elem(); }
 
+    // Release of a stage by the consumer warps.  The stage's shared memory was read through the
+    // generic proxy and the producer's next cp.async.bulk writes it through the async proxy, so
+    // every lane fences its reads (a CTA fence plus the generic->async proxy fence) before its
+    // warp's single arrival on the stage's "empty" barrier.  Without the fences the next copy
+    // was observed to overwrite data a warp had not finished reading.
+    // UVU_DBG_RELEASE (a debugging switch): 1 = per-thread arrival without fences,
+    // 3 = proxy fence only.
+    int release_mode() const {
+        const char* e = std::getenv("UVU_DBG_RELEASE");
+        return e ? std::atoi(e) : 0;
+    }
+    void emit_release(Src& S, const char* pre) const {
+        const int m = release_mode();
+        if (m == 1) {
+            S(fmt("mbar_arrive(sbase + %s_BAR + 8u * (%s_NST + st));", pre, pre));
+            return;
+        }
+        if (m != 3) S("__threadfence_block();");
+        S("asm volatile(\"fence.proxy.async.shared::cta;\" ::: \"memory\");");
+        S("__syncwarp();");
+        S(fmt("if (lane == 0) mbar_arrive(sbase + %s_BAR + 8u * (%s_NST + st));", pre, pre));
+    }
+    // Arrival count of a stage's "empty" barrier: one per consumer warp (or per consumer thread
+    // under the per-thread debugging release).
+    const char* empty_count(const char* ncw, const char* nct) const { return release_mode() == 1 ? nct : ncw; }
     void emit_pipe_helpers(Src& S) const {
         S(R"(__device__ unsigned int uvu_status_word;
 #define UVU_DEV_TIMEOUT 1u
@@ -536,9 +562,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         R.ybulk = ybytes() % 16 == 0;
         const size_t pe = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
         R.ch = int(std::max<size_t>(1, std::min<size_t>(8, 32768 / pe)));
+        if (const char* e = std::getenv("UVU_PIPE_CH")) R.ch = std::max(1, std::atoi(e));
         const size_t stage = a16(R.ch * wbytes()) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
                              (R.ybulk ? a16(R.ch * ybytes()) : 0);
         R.nst = int(std::max<size_t>(2, std::min<size_t>(6, (108 * 1024) / stage)));
+        if (const char* e = std::getenv("UVU_PIPE_NST")) R.nst = std::max(2, std::atoi(e));
         R.w_off = 0;
         R.x_off = a16(R.ch * wbytes());
         R.y_off = R.x_off + (R.xbulk ? a16(R.ch * xbytes()) : 0);
@@ -663,8 +691,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
             S("}");
             S.ind--;
             S("}");
-            S("__syncwarp();");
-            S("if (lane == 0) mbar_arrive(sbase + FW_BAR + 8u * (FW_NST + st));");
+            emit_release(S, "FW");
             S.ind--;
             S("}");
             S("if (uvalid) {");
@@ -681,7 +708,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S("const unsigned sbase = smem_addr(smem);");
         S("const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;");
         S("if (tid == 0) {");
-        S("  for (int i = 0; i < FW_NST; ++i) { mbar_init(sbase + FW_BAR + 8u * i, 1u); mbar_init(sbase + FW_BAR + 8u * (FW_NST + i), UVU_NCW); }");
+        S("  for (int i = 0; i < FW_NST; ++i) { mbar_init(sbase + FW_BAR + 8u * i, 1u); mbar_init(sbase + FW_BAR + 8u * (FW_NST + i), " + std::string(empty_count("UVU_NCW", "UVU_NCT")) + "); }");
         S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
         S("}");
         S("__syncthreads();");
@@ -828,8 +855,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
             S("}");  // j < ne
             S.ind--;
             S("}");  // j
-            S("__syncwarp();");
-            S("if (lane == 0) mbar_arrive(sbase + EG_BAR + 8u * (EG_NST + st));");
+            emit_release(S, "EG");
             S.ind--;
             S("}");  // !dead
             S("consumer_sync();");
@@ -862,7 +888,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S("const unsigned sbase = smem_addr(smem);");
         S("const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;");
         S("if (tid == 0) {");
-        S("  for (int i = 0; i < EG_NST; ++i) { mbar_init(sbase + EG_BAR + 8u * i, 1u); mbar_init(sbase + EG_BAR + 8u * (EG_NST + i), UVU_NCW); }");
+        S("  for (int i = 0; i < EG_NST; ++i) { mbar_init(sbase + EG_BAR + 8u * i, 1u); mbar_init(sbase + EG_BAR + 8u * (EG_NST + i), " + std::string(empty_count("UVU_NCW", "UVU_NCT")) + "); }");
         S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
         S("}");
         S("__syncthreads();");
@@ -1003,7 +1029,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S("const unsigned sbase = smem_addr(smem);");
         S("const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;");
         S("if (tid == 0) {");
-        S("  for (int i = 0; i < DX_NST; ++i) { mbar_init(sbase + DX_BAR + 8u * i, 1u); mbar_init(sbase + DX_BAR + 8u * (DX_NST + i), DX_NCW); }");
+        S("  for (int i = 0; i < DX_NST; ++i) { mbar_init(sbase + DX_BAR + 8u * i, 1u); mbar_init(sbase + DX_BAR + 8u * (DX_NST + i), " + std::string(empty_count("DX_NCW", "DX_UT")) + "); }");
         S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
         S("}");
         S("__syncthreads();");
@@ -1052,8 +1078,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S("}");
         S.ind--;
         S("}");
-        S("__syncwarp();");
-        S("if (lane == 0) mbar_arrive(sbase + DX_BAR + 8u * (DX_NST + st));");
+        emit_release(S, "DX");
         S.ind--;
         S("}");
         S("if (uvalid) {");
@@ -1090,10 +1115,12 @@ std::string emit_source(Plan* plan) {
 
     // Pipelined (bulk-copy) kernels need whole warps per owner and 16-byte multiples for the
     // per-edge weight rows; otherwise the direct-load kernels are emitted.
-    const bool pipe_recv = U >= 32 && G.wbytes() % 16 == 0 && ncw * 32 + 32 <= 1024;
+    // UVU_FORCE_DIRECT=1 (a debugging switch) selects the direct-load kernels everywhere.
+    const bool force_direct = std::getenv("UVU_FORCE_DIRECT") && std::atoi(std::getenv("UVU_FORCE_DIRECT")) != 0;
+    const bool pipe_recv = !force_direct && U >= 32 && G.wbytes() % 16 == 0 && ncw * 32 + 32 <= 1024;
     Gen::RecvPipe RF = G.recv_pipe(false, ncw), RE = G.recv_pipe(true, ncw);
     Gen::SendPipe SD = G.send_pipe();
-    const bool pipe_dx = U >= 32 && G.send_pipe_ok(SD);
+    const bool pipe_dx = !force_direct && U >= 32 && G.send_pipe_ok(SD);
     plan->pipelined_recv = pipe_recv;
     plan->pipelined_dx = pipe_dx;
     if (pipe_recv) {
