@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--single-mode", action="store_true",
+                    help="warm up and time only --dx-mode (profiling runs)")
     return ap.parse_args(argv)
 
 
@@ -302,13 +304,17 @@ def main(argv=None):
     other = "atomic" if args.dx_mode == "sender" else "sender"
     for _ in range(max(args.warmup, 3)):
         step(args.dx_mode)
-        step(other)
+        if not args.single_mode:
+            step(other)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local_rank)
     clocks.start()
     total_ms, kern_ms = timed(args.dx_mode, args.steps)
-    total_o, kern_o = timed(other, args.steps)
+    if args.single_mode:
+        total_o, kern_o = total_ms, kern_ms
+    else:
+        total_o, kern_o = timed(other, args.steps)
     clk = clocks.stop()
 
     total_ms = max_over_ranks(total_ms, world, dev)
