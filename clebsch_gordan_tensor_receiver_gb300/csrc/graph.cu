@@ -8,7 +8,11 @@
 // bit-exact regardless of scheduling.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <string>
 
 #include "plan.h"
 
@@ -174,3 +178,67 @@ cudaError_t launch_graph_validate(int64_t N, int64_t E, const int32_t* off, cons
 }
 
 }  // namespace uvu
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free transpose.  Some callers cannot hand this library a workspace: a plugin whose
+// host runtime owns every byte of device memory and only passes it input and output buffers, or
+// a latency-critical path that must not take an allocator lock or risk an out-of-memory failure
+// in the middle of a run.  For them the transpose's scratch (per-sender counters plus the
+// unordered edge list) lives in one fixed array compiled into the library.  The array exists on
+// every GPU that loads the library for as long as the process runs.  Each call re-initialises
+// what it reads (the counters are zeroed and the edge list is fully rewritten), so the contents
+// left by the previous call do not matter; calls whose work overlaps on the GPU share the array
+// and therefore race.
+namespace uvu {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char uvu_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+std::map<int, void*> g_noalloc_ptr;  // device ordinal -> device address of the array
+
+// The array's device address on the current device, looked up once per device.  In host code
+// `uvu_noalloc_scratch` names a host-side stand-in, so the address must come from the runtime.
+uvu_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> g(g_noalloc_mu);
+    auto it = g_noalloc_ptr.find(dev);
+    if (it == g_noalloc_ptr.end()) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, uvu_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(uvu_noalloc_scratch)");
+        it = g_noalloc_ptr.emplace(dev, p).first;
+    }
+    *out = it->second;
+    return UVU_OK;
+}
+
+}  // namespace
+}  // namespace uvu
+
+extern "C" uvu_status uvu_csr_transpose_noalloc(int64_t n_nodes, int64_t n_edges, const int32_t* recv_offsets,
+                                                const int32_t* src, int32_t* send_offsets, int32_t* send_eids,
+                                                int32_t* send_recv, uvu_stream_t stream) {
+    using namespace uvu;
+    if (n_nodes < 0 || n_edges < 0 || n_nodes >= INT32_MAX || n_edges >= INT32_MAX)
+        return fail(UVU_ERR_INVALID_ARGUMENT, "n_nodes and n_edges must be in [0, 2^31 - 1)");
+    if (!send_offsets) return fail(UVU_ERR_INVALID_ARGUMENT, "send_offsets is NULL");
+    if (n_edges > 0 && (!recv_offsets || !src || !send_eids || !send_recv))
+        return fail(UVU_ERR_INVALID_ARGUMENT, "graph pointer is NULL");
+    const size_t need = transpose_workspace_bytes(n_nodes, n_edges);
+    if (need > kNoAllocScratchBytes)
+        return fail(UVU_ERR_UNSUPPORTED,
+                    "graph needs " + std::to_string(need) + " bytes of transpose scratch; the built-in scratch holds " +
+                        std::to_string(kNoAllocScratchBytes) + " bytes (4(N+1) + 4E rounded up); use uvu_csr_transpose "
+                        "with a caller workspace");
+    void* ws = nullptr;
+    uvu_status s = noalloc_scratch(&ws);
+    if (s != UVU_OK) return s;
+    cudaError_t e = launch_csr_transpose(n_nodes, n_edges, recv_offsets, src, send_offsets, send_eids, send_recv,
+                                         ws, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "csr transpose launch");
+    return ok();
+}

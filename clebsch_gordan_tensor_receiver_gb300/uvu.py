@@ -28,7 +28,7 @@ EXPORTS = (
     "uvu_plan_create", "uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
     "uvu_plan_device_status",
     "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
-    "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx", "uvu_conv_bwd",
+    "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx", "uvu_conv_bwd",
     "uvu_status_string", "uvu_last_error_message",
 )
 
@@ -54,6 +54,7 @@ def _load():
         "uvu_csr_from_sorted_recv": [I64, I64, P, P, P],
         "uvu_csr_transpose_workspace": [I64, I64, ctypes.POINTER(SZ)],
         "uvu_csr_transpose": [I64, I64, P, P, P, P, P, P, SZ, P],
+        "uvu_csr_transpose_noalloc": [I64, I64, P, P, P, P, P, P],
         "uvu_graph_validate": [I64, I64, P, P, P, ctypes.POINTER(I64), P],
         "uvu_conv_fwd": [P, I64, I64, P, P, P, P, P, P, P],
         "uvu_conv_bwd_edge": [P, I64, I64, P, P, P, P, P, P, P, P, P, P],
@@ -93,7 +94,7 @@ def _wrap(name):
 for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
            "uvu_plan_device_status",
            "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
-           "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx",
+           "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx",
            "uvu_conv_bwd"):
     globals()[_n] = _wrap(_n)
 

@@ -133,6 +133,23 @@ uvu_status uvu_csr_transpose(int64_t n_nodes, int64_t n_edges, const int32_t *re
                              int32_t *send_recv, void *workspace, size_t workspace_bytes,
                              uvu_stream_t stream);
 
+/* Allocation-free variant of uvu_csr_transpose.  No counterpart in the paper: it exists for
+ * callers that cannot provide device memory of their own, such as a plugin whose host runtime
+ * owns the whole device memory pool and passes it only input and output buffers, or a
+ * latency-critical path that must not take an allocator lock or risk running out of memory in
+ * the middle of its work.  Same arguments and results as uvu_csr_transpose, without the
+ * workspace: the scratch is a fixed 16 MiB array compiled into the library, present on every
+ * GPU that loads it until the process exits.  Graphs needing more than that
+ * (uvu_csr_transpose_workspace() > 16 MiB, i.e. roughly 4(N+1) + 4E > 16 MiB) are rejected with
+ * UVU_ERR_UNSUPPORTED before anything is enqueued.  This function allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library call).  Its first call on a device looks up the
+ * array's device address there (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call re-initialises the scratch it reads, so the previous call's leftovers do
+ * not matter, but all calls share one array: calls whose work overlaps on the GPU race. */
+uvu_status uvu_csr_transpose_noalloc(int64_t n_nodes, int64_t n_edges, const int32_t *recv_offsets,
+                                     const int32_t *src, int32_t *send_offsets, int32_t *send_eids,
+                                     int32_t *send_recv, uvu_stream_t stream);
+
 /* Check a receiver CSR and sender list on the device: offsets[0] == 0, non-decreasing,
  * offsets[N] == E, 0 <= src < N.  Synchronises `stream`; *n_bad receives the number of
  * violations (0 = valid).  `workspace` needs 8 bytes of device memory. */
