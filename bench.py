@@ -42,7 +42,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="uvu", choices=["uvu", "reference"])
     ap.add_argument("--config", type=int, default=1)
-    ap.add_argument("--dx-mode", default="sender", choices=["sender", "atomic"])
+    ap.add_argument("--dx-mode", default="staged", choices=["staged", "sender", "atomic"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -63,6 +63,8 @@ def algorithmic_bytes(N, E, U, P, Dx, Dy, Do, s):
         "uvu_bwd_edge": x + Y + w + out + idx_r + Y + w,        # reads x,Y,w,d_out; writes dY,dw
         "uvu_bwd_edge+atomic_dx": x + Y + w + out + idx_r + Y + w + x,
         "uvu_bwd_dx": Y + w + out + idx_s + x,                  # reads Y,w,d_out; writes dx
+        "uvu_bwd_edge+dx_edge": x + Y + w + out + idx_r + Y + w + E * U * Dx * s,
+        "uvu_bwd_dx_reduce": E * U * Dx * s + 4 * (N + 1) + 4 * E + x,  # reads partials; writes dx
         "fwd": x + Y + w + out + idx_r,
         "vjp": (x + Y + w + out + idx_r + idx_s) + (x + Y + w),
     }
@@ -264,6 +266,13 @@ def main(argv=None):
     dx = torch.empty(N, U, Dx, dtype=tdt, device=dev)
     dY = torch.empty(E, Dy, dtype=tdt, device=dev)
     dw = torch.empty(E, P, U, dtype=tdt, device=dev)
+    modes = [args.dx_mode] + ([] if args.single_mode else
+                              [m for m in ("staged", "sender", "atomic") if m != args.dx_mode])
+    ws = None
+    if "staged" in modes:
+        ws = torch.empty(max(plan.workspace_bytes(N, E, uvu.UVU_DX_STAGED), 16), dtype=torch.uint8,
+                         device=dev)
+    dx_kernel = {"sender": "uvu_bwd_dx", "staged": "uvu_bwd_dx_reduce", "atomic": None}
 
     def step(mode, evs=None):
         if evs:
@@ -272,11 +281,14 @@ def main(argv=None):
         if evs:
             evs[1].record(stream)
         plan.bwd_edge(N, x, Y, w, G.recv_offsets, src, g, dY=dY, dw=dw,
-                      dx_atomic=dx if mode == "atomic" else None, stream=stream)
+                      dx_atomic=dx if mode == "atomic" else None,
+                      dx_edge=ws if mode == "staged" else None, stream=stream)
         if evs:
             evs[2].record(stream)
         if mode == "sender":
             plan.bwd_dx(N, E, Y, w, G.send_offsets, G.send_eids, G.send_recv, g, dx, stream)
+        elif mode == "staged":
+            plan.bwd_dx_reduce(N, E, G.send_offsets, G.send_eids, ws, dx, stream)
         if evs:
             evs[3].record(stream)
 
@@ -293,38 +305,33 @@ def main(argv=None):
         torch.cuda.synchronize()
         barrier(world)
         total = start.elapsed_time(end)
-        per = {"uvu_fwd": [], "uvu_bwd_edge": [], "uvu_bwd_dx": []}
+        per = {"uvu_fwd": [], "uvu_bwd_edge": []}
+        if dx_kernel[mode]:
+            per[dx_kernel[mode]] = []
         for e in evs:
             per["uvu_fwd"].append(e[0].elapsed_time(e[1]))
             per["uvu_bwd_edge"].append(e[1].elapsed_time(e[2]))
-            if mode == "sender":
-                per["uvu_bwd_dx"].append(e[2].elapsed_time(e[3]))
-        return total, {k: statistics.mean(v) for k, v in per.items() if v}
+            if dx_kernel[mode]:
+                per[dx_kernel[mode]].append(e[2].elapsed_time(e[3]))
+        return total, {k: statistics.mean(v) for k, v in per.items()}
 
-    other = "atomic" if args.dx_mode == "sender" else "sender"
     for _ in range(max(args.warmup, 3)):
-        step(args.dx_mode)
-        if not args.single_mode:
-            step(other)
+        for m in modes:
+            step(m)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local_rank)
     clocks.start()
-    total_ms, kern_ms = timed(args.dx_mode, args.steps)
-    if args.single_mode:
-        total_o, kern_o = total_ms, kern_ms
-    else:
-        total_o, kern_o = timed(other, args.steps)
+    results = {m: timed(m, args.steps) for m in modes}
     clk = clocks.stop()
+    assert plan.device_status() == 0, "a kernel reported a bounded-wait timeout"
 
+    total_ms, kern_ms = results[args.dx_mode]
     total_ms = max_over_ranks(total_ms, world, dev)
     ms_step = total_ms / args.steps
     value = world * E / (ms_step / 1000.0)
 
     B = algorithmic_bytes(N, E, U, P, Dx, Dy, Do, s)
-    fwd_ms = kern_ms["uvu_fwd"]
-    vjp_ms = kern_ms["uvu_bwd_edge"] + kern_ms.get("uvu_bwd_dx", 0.0)
-    vjp_o = kern_o["uvu_bwd_edge"] + kern_o.get("uvu_bwd_dx", 0.0)
     peaks = {}
     pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(pk_path):
@@ -337,11 +344,21 @@ def main(argv=None):
         gbs = bytes_ / (ms / 1000.0) / 1e9
         return gbs, gbs / hbm_peak
 
+    edge_key = {"atomic": "uvu_bwd_edge+atomic_dx", "staged": "uvu_bwd_edge+dx_edge",
+                "sender": "uvu_bwd_edge"}
+
+    def mode_summary(mode):
+        tot, km = results[mode]
+        vjp = sum(v for k, v in km.items() if k != "uvu_fwd")
+        gbs, fr = frac(B["vjp"], vjp)
+        return {"vjp_ms": vjp, "vjp_edges_per_s": world * E / (vjp / 1000), "vjp_GB_s": gbs,
+                "vjp_hbm_frac": fr, "fwd_vjp_edges_per_s": world * E / (tot / args.steps / 1000),
+                "deterministic": mode != "atomic",
+                "kernels_ms": km}
+
     kernels = {}
     for k, ms in kern_ms.items():
-        key = k
-        if k == "uvu_bwd_edge" and args.dx_mode == "atomic":
-            key = "uvu_bwd_edge+atomic_dx"
+        key = edge_key[args.dx_mode] if k == "uvu_bwd_edge" else k
         gbs, fr = frac(B[key], ms)
         kernels[k] = {"ms": ms, "bytes": B[key], "GB_s": gbs, "frac": fr}
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
@@ -354,9 +371,10 @@ def main(argv=None):
         ent = tj.get(f"{spec.name}:{dom}:{args.dx_mode}")
         if ent and ent.get("source_sha") == h:
             traffic = ent["dram_bytes_per_launch"]
+    fwd_ms = kern_ms["uvu_fwd"]
+    vjp_ms = sum(v for k, v in kern_ms.items() if k != "uvu_fwd")
     fwd_gbs, fwd_fr = frac(B["fwd"], fwd_ms)
     vjp_gbs, vjp_fr = frac(B["vjp"], vjp_ms)
-    vjpo_gbs, vjpo_fr = frac(B["vjp"], vjp_o)
     line = {
         "metric": METRIC, "value": value, "unit": "edges/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
@@ -369,15 +387,14 @@ def main(argv=None):
                 "hbm_frac": fwd_fr, "bytes": B["fwd"]},
         "vjp": {"edges_per_s": world * E / (vjp_ms / 1000), "ms": vjp_ms, "GB_s": vjp_gbs,
                 "hbm_frac": vjp_fr, "bytes": B["vjp"], "dx_mode": args.dx_mode},
-        f"vjp_{other}": {"edges_per_s": world * E / (vjp_o / 1000), "ms": vjp_o, "GB_s": vjpo_gbs,
-                         "hbm_frac": vjpo_fr, "fwd_vjp_edges_per_s": world * E / (total_o / args.steps / 1000)},
+        "dx_modes": {m: mode_summary(m) for m in modes},
         "kernels": kernels,
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["GB_s"],
                      "peak": hbm_peak, "unit": "GB/s", "frac": kernels[dom]["frac"],
                      "traffic": traffic, "peak_source": peak_src + " hbm_gbs (copy)"},
         "csr_build_ms": csr_ms,
         "clocks": clk,
-        "gpu_launches": args.steps * (3 if args.dx_mode == "sender" else 2),
+        "gpu_launches": args.steps * (2 if args.dx_mode == "atomic" else 3),
     }
 
     # end-to-end through the C ABI from pinned host buffers
@@ -390,6 +407,8 @@ def main(argv=None):
         hout = {"out": pin(out), "dx": pin(dx), "dY": pin(dY), "dw": pin(dw)}
         h2d = sum(v.numel() * v.element_size() for v in hin.values())
         d2h = sum(v.numel() * v.element_size() for v in hout.values())
+        mode_id = {"sender": uvu.UVU_DX_SENDER, "atomic": uvu.UVU_DX_ATOMIC,
+                   "staged": uvu.UVU_DX_STAGED}[args.dx_mode]
 
         def e2e_step():
             for k, v in hin.items():
@@ -397,8 +416,7 @@ def main(argv=None):
             b = dbuf
             plan.fwd(N, b["x"], b["Y"], b["w"], b["roff"], b["src"], out, stream)
             plan.bwd(N, b["x"], b["Y"], b["w"], b["roff"], b["src"], b["soff"], b["seid"],
-                     b["srecv"], b["g"], dx=dx, dY=dY, dw=dw,
-                     dx_mode=uvu.UVU_DX_SENDER if args.dx_mode == "sender" else uvu.UVU_DX_ATOMIC,
+                     b["srecv"], b["g"], dx=dx, dY=dY, dw=dw, dx_mode=mode_id, workspace=ws,
                      stream=stream)
             hout["out"].copy_(out, non_blocking=True)
             hout["dx"].copy_(dx, non_blocking=True)

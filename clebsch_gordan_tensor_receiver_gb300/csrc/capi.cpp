@@ -233,14 +233,17 @@ extern "C" uvu_status uvu_conv_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
 extern "C" uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
                                         const void* Y, const void* w, const int32_t* recv_offsets,
                                         const int32_t* src, const void* d_out, void* dY, void* dw,
-                                        void* dx_atomic, uvu_stream_t stream) {
+                                        void* dx_atomic, void* dx_edge, uvu_stream_t stream) {
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
     UVU_TRY(check_sizes(n_nodes, n_edges));
     UVU_TRY(opt(dY, "dY"));
     UVU_TRY(opt(dw, "dw"));
     UVU_TRY(opt(dx_atomic, "dx"));
-    if (n_nodes == 0 || (!dY && !dw && !dx_atomic)) return ok();
+    UVU_TRY(opt(dx_edge, "dx_edge"));
+    if (dx_edge && !p->staged_ok)
+        return fail(UVU_ERR_UNSUPPORTED, "per-edge dx partials need the pipelined kernels or a single register group");
+    if (n_nodes == 0 || (!dY && !dw && !dx_atomic && !dx_edge)) return ok();
     UVU_TRY(need(recv_offsets, "recv_offsets"));
     if (n_edges > 0) {
         UVU_TRY(need(x, "x"));
@@ -259,8 +262,42 @@ extern "C" uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_
     }
     if (n_edges == 0) return ok();
     long long N = n_nodes;
-    void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &d_out, &dY, &dw, &dx_atomic};
+    void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &d_out, &dY, &dw, &dx_atomic, &dx_edge};
     UVU_TRY(launch(m->bwd_edge, m->occ_edge, m->sm_count, n_nodes, p->g_edge, args, stream, "uvu_bwd_edge launch"));
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_bwd_dx_reduce(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges,
+                                             const int32_t* send_offsets, const int32_t* send_eids,
+                                             const void* dx_edge, void* dx, uvu_stream_t stream) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    if (n_nodes == 0) return ok();
+    UVU_TRY(need(dx, "dx"));
+    UVU_TRY(need(send_offsets, "send_offsets"));
+    if (n_edges > 0) {
+        UVU_TRY(need(send_eids, "send_eids"));
+        UVU_TRY(need(dx_edge, "dx_edge"));
+    }
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = module_for_current_device(p, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    long long N = n_nodes;
+    void* args[] = {&N, &send_offsets, &send_eids, &dx_edge, &dx};
+    const int64_t threads = n_nodes * p->U_pad;
+    const KernelGeom g{256, 256, 0, false, 1};
+    UVU_TRY(launch(m->bwd_dx_reduce, 1, m->sm_count, threads, g, args, stream, "uvu_bwd_dx_reduce launch"));
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_bwd_workspace(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges,
+                                             uvu_dx_mode dx_mode, size_t* bytes) {
+    Plan* p = get(plan);
+    if (!p || !bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or bytes is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    *bytes = dx_mode == UVU_DX_STAGED ? size_t(n_edges) * p->U * p->Dx * p->elem() : 0;
     return ok();
 }
 
@@ -295,12 +332,25 @@ extern "C" uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
                                    const void* Y, const void* w, const int32_t* recv_offsets,
                                    const int32_t* src, const int32_t* send_offsets, const int32_t* send_eids,
                                    const int32_t* send_recv, const void* d_out, void* dx, void* dY, void* dw,
-                                   uvu_dx_mode dx_mode, uvu_stream_t stream) {
-    if (dx_mode != UVU_DX_SENDER && dx_mode != UVU_DX_ATOMIC)
-        return fail(UVU_ERR_INVALID_ARGUMENT, "dx_mode must be UVU_DX_SENDER or UVU_DX_ATOMIC");
+                                   uvu_dx_mode dx_mode, void* workspace, size_t workspace_bytes,
+                                   uvu_stream_t stream) {
+    if (dx_mode != UVU_DX_SENDER && dx_mode != UVU_DX_ATOMIC && dx_mode != UVU_DX_STAGED)
+        return fail(UVU_ERR_INVALID_ARGUMENT, "dx_mode must be UVU_DX_SENDER, UVU_DX_ATOMIC or UVU_DX_STAGED");
     if (dx_mode == UVU_DX_ATOMIC)
-        return uvu_conv_bwd_edge(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, d_out, dY, dw, dx, stream);
-    UVU_TRY(uvu_conv_bwd_edge(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, d_out, dY, dw, nullptr, stream));
+        return uvu_conv_bwd_edge(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, d_out, dY, dw, dx, nullptr, stream);
+    if (dx_mode == UVU_DX_STAGED && dx) {
+        size_t need_bytes = 0;
+        UVU_TRY(uvu_conv_bwd_workspace(plan, n_nodes, n_edges, dx_mode, &need_bytes));
+        if (need_bytes && (!workspace || workspace_bytes < need_bytes))
+            return fail(UVU_ERR_INVALID_ARGUMENT, "UVU_DX_STAGED needs a workspace of uvu_conv_bwd_workspace() bytes");
+        UVU_TRY(opt(workspace, "workspace"));
+        UVU_TRY(uvu_conv_bwd_edge(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, d_out, dY, dw, nullptr,
+                                  need_bytes ? workspace : nullptr, stream));
+        UVU_TRY(uvu_conv_bwd_dx_reduce(plan, n_nodes, n_edges, send_offsets, send_eids, workspace, dx, stream));
+        return ok();
+    }
+    UVU_TRY(uvu_conv_bwd_edge(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, d_out, dY, dw, nullptr, nullptr,
+                              stream));
     if (dx)
         UVU_TRY(uvu_conv_bwd_dx(plan, n_nodes, n_edges, Y, w, send_offsets, send_eids, send_recv, d_out, dx, stream));
     return ok();

@@ -333,8 +333,9 @@ struct Gen {
         S(fmt("__device__ __forceinline__ void edge_group%d(int rl, int seg, int lane_in_seg, bool valid, int r_e0, int r_e1,", g));
         S(fmt("    int nchunks, long long r, int u, const int* __restrict__ src, const %s* __restrict__ x,", T.c_str()));
         S(fmt("    const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ gout,", T.c_str(), T.c_str(), T.c_str()));
-        S(fmt("    %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx, %s* sred, const int* s_e0, const int* s_e1) {",
+        S(fmt("    %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx, %s* sred, const int* s_e0, const int* s_e1,",
               T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S(fmt("    %s* __restrict__ dxe) {", T.c_str()));
         S.ind++;
         S(fmt("const %s* __restrict__ grow = gout + ((size_t)(valid ? r : 0) * UVU_U + u) * UVU_DO;", T.c_str()));
         for (int k : outs) S(fmt("const %s gv_%d = valid ? __ldg(grow + %d) : (%s)0;", T.c_str(), k, k, T.c_str()));
@@ -381,6 +382,7 @@ struct Gen {
         }
         S.ind--;
         S("}");
+        if (P->groups.size() == 1) emit_dx_edge_store(S, xn, 1);
         S.ind--;
         S("}");  // active
         // reduce the dY partials over the channels of this segment
@@ -551,7 +553,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
     struct RecvPipe {
         int ch = 1, nst = 2;
         bool xbulk = false, ybulk = false;
-        size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, total = 0;
+        size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, xpart_off = 0, total = 0;
         size_t tx_per_edge = 0;
     };
     static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
@@ -560,12 +562,17 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         RecvPipe R;
         R.xbulk = xbytes() % 16 == 0;
         R.ybulk = ybytes() % 16 == 0;
+        const int NG = int(P->groups.size());
         const size_t pe = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
         R.ch = int(std::max<size_t>(1, std::min<size_t>(8, 32768 / pe)));
         if (const char* e = std::getenv("UVU_PIPE_CH")) R.ch = std::max(1, std::atoi(e));
         const size_t stage = a16(R.ch * wbytes()) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
                              (R.ybulk ? a16(R.ch * ybytes()) : 0);
-        R.nst = int(std::max<size_t>(2, std::min<size_t>(6, (108 * 1024) / stage)));
+        // per-stage partial sums of the edge kernel: dY over warps, dx over register groups
+        const size_t dyp = with_partials ? a16(2 * size_t(ncw) * R.ch * P->Dy * P->elem()) : 0;
+        const size_t dxp = (with_partials && NG > 1) ? a16(2 * size_t(NG) * R.ch * P->U_pad * P->Dx * P->elem()) : 0;
+        const size_t room = 108 * 1024 > dyp + dxp + 2 * stage ? 108 * 1024 - dyp - dxp : 2 * stage;
+        R.nst = int(std::max<size_t>(2, std::min<size_t>(6, room / stage)));
         if (const char* e = std::getenv("UVU_PIPE_NST")) R.nst = std::max(2, std::atoi(e));
         R.w_off = 0;
         R.x_off = a16(R.ch * wbytes());
@@ -573,7 +580,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         R.stage = stage;
         R.bar_off = R.nst * stage;
         R.part_off = R.bar_off + 16 * R.nst;
-        R.total = R.part_off + (with_partials ? 2 * size_t(ncw) * R.ch * P->Dy * P->elem() : 0);
+        R.xpart_off = R.part_off + dyp;
+        R.total = R.xpart_off + dxp;
         R.tx_per_edge = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
         return R;
     }
@@ -586,6 +594,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S(fmt("#define %s_YOFF %zu", pre, R.y_off));
         S(fmt("#define %s_BAR %zu", pre, R.bar_off));
         S(fmt("#define %s_PART %zu", pre, R.part_off));
+        S(fmt("#define %s_XPART %zu", pre, R.xpart_off));
         S(fmt("#define %s_TX %zu", pre, R.tx_per_edge));
         S(fmt("#define %s_MINB %d", pre, std::min(minb(R.total), pre[0] == 'F' ? P->minb[0] : P->minb[1])));
     }
@@ -798,8 +807,9 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
             S(fmt("__device__ __forceinline__ void edge_rcv%d(long long r, int e0, int e1, int u, bool uvalid, int lane, int warp,", g));
             S("    int tid, unsigned& c, bool& dead, int& buf, const unsigned char* smem, unsigned sbase,");
             S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
-            S(fmt("    const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx) {",
+            S(fmt("    const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx,",
                   T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+            S(fmt("    %s* __restrict__ dxe, int g) {", T.c_str()));
             S.ind++;
             S(fmt("const %s* __restrict__ grow = gout + ((size_t)r * UVU_U + (uvalid ? u : 0)) * UVU_DO;", T.c_str()));
             for (int k : outs) S(fmt("const %s gv_%d = __ldg(grow + %d);", T.c_str(), k, k));
@@ -843,6 +853,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
             emit_dx_atomics(S, xn);
             S.ind--;
             S("}");
+            emit_dx_edge_store(S, xn, NG);
             S.ind--;
             S("}");  // uvalid
             S("if (dY) {");
@@ -859,6 +870,26 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
             S.ind--;
             S("}");  // !dead
             S("consumer_sync();");
+            if (NG > 1) {
+                S("if (!dead && dxe) {");
+                S.ind++;
+                S(fmt("const %s* xpb = reinterpret_cast<const %s*>(smem + EG_XPART) + (size_t)buf * (UVU_G * EG_CH * UVU_UP * UVU_DX);", T.c_str(), T.c_str()));
+                S("for (int t = tid; t < ne * UVU_UP * UVU_DX; t += UVU_NCT) {");
+                S.ind++;
+                S("const int k = t % UVU_DX, uu = (t / UVU_DX) % UVU_UP, j = t / (UVU_DX * UVU_UP);");
+                S("if (uu < UVU_U) {");
+                S.ind++;
+                S(T + " acc = 0;");
+                S("#pragma unroll");
+                S("for (int gg = 0; gg < UVU_G; ++gg) acc += xpb[((size_t)(gg * EG_CH + j) * UVU_UP + uu) * UVU_DX + k];");
+                S("dxe[((size_t)(eb + j) * UVU_U + uu) * UVU_DX + k] = acc;");
+                S.ind--;
+                S("}");
+                S.ind--;
+                S("}");
+                S.ind--;
+                S("}");
+            }
             S("if (!dead && dY) {");
             S.ind++;
             S("for (int t = tid; t < ne * UVU_DY; t += UVU_NCT) {");
@@ -882,7 +913,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
         S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
               T.c_str(), T.c_str(), T.c_str(), T.c_str()));
-        S(fmt("    %s* __restrict__ dx) {", T.c_str()));
+        S(fmt("    %s* __restrict__ dx, %s* __restrict__ dxe) {", T.c_str(), T.c_str()));
         S.ind++;
         S("extern __shared__ __align__(128) unsigned char smem[];");
         S("const unsigned sbase = smem_addr(smem);");
@@ -905,10 +936,38 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S.ind++;
         S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
         for (int g = 0; g < NG; ++g)
-            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, dead, buf, smem, sbase, src, x, Y, gout, dY, dw, dx);",
+            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, dead, buf, smem, sbase, src, x, Y, gout, dY, dw, dx, dxe, g);",
                   g ? "else " : "", g, g));
         S.ind--;
         S("}");
+        S.ind--;
+        S("}");
+    }
+
+    // Per-edge dx contribution of this thread's channel, for the deterministic (staged) dx:
+    // written straight to dxe[e][u][:] with one register group, otherwise into the stage's
+    // shared-memory partials [buf][g][j][u][:] that the consumers sum over groups after the
+    // stage barrier (fixed order).
+    void emit_dx_edge_store(Src& S, const std::set<int>& xn, int NG) const {
+        S("if (dxe) {");
+        S.ind++;
+        if (NG == 1) {
+            S(T + "* __restrict__ dxer = dxe + ((size_t)e * UVU_U + u) * UVU_DX;");
+            if (!f64 && P->Dx % 4 == 0) {
+                for (int c = 0; c < P->Dx / 4; ++c) {
+                    std::string v[4];
+                    for (int i = 0; i < 4; ++i) v[i] = xn.count(4 * c + i) ? fmt("dxp_%d", 4 * c + i) : "0.0f";
+                    S(fmt("reinterpret_cast<float4*>(dxer)[%d] = make_float4(%s, %s, %s, %s);", c, v[0].c_str(), v[1].c_str(),
+                          v[2].c_str(), v[3].c_str()));
+                }
+            } else {
+                for (int k = 0; k < P->Dx; ++k) S(fmt("dxer[%d] = %s;", k, xn.count(k) ? fmt("dxp_%d", k).c_str() : "0"));
+            }
+        } else {
+            S(fmt("%s* xp = reinterpret_cast<%s*>(const_cast<unsigned char*>(smem) + EG_XPART) + ((size_t)((buf * UVU_G + g) * EG_CH + j) * UVU_UP + u) * UVU_DX;",
+                  T.c_str(), T.c_str()));
+            for (int k = 0; k < P->Dx; ++k) S(fmt("xp[%d] = %s;", k, xn.count(k) ? fmt("dxp_%d", k).c_str() : "0"));
+        }
         S.ind--;
         S("}");
     }
@@ -925,6 +984,55 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         } else {
             for (int k : xn) S(fmt("atomicAdd(dxr + %d, dxp_%d);", k, k));
         }
+    }
+
+    // Sender-stationary sum of the per-edge dx partials over the transposed CSR: one thread per
+    // (sender, channel) adds its edges' rows in ascending edge-id order and writes dx once.
+    void emit_dx_reduce(Src& S) const {
+        const bool vec = !f64 && P->Dx % 4 == 0;
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(256) uvu_bwd_dx_reduce(long long N, const int* __restrict__ soff,"));
+        S(fmt("    const int* __restrict__ seid, const %s* __restrict__ dxe, %s* __restrict__ dx) {", T.c_str(), T.c_str()));
+        S.ind++;
+        S("const long long t = (long long)blockIdx.x * 256 + threadIdx.x;");
+        S("const long long sn = t / UVU_UP;");
+        S("const int u = (int)(t - sn * UVU_UP);");
+        S("if (sn >= N || u >= UVU_U) return;");
+        S("const int k0 = __ldg(soff + sn), k1 = __ldg(soff + sn + 1);");
+        for (int k = 0; k < P->Dx; ++k) S(fmt("%s a_%d = 0;", T.c_str(), k));
+        auto add_row = [&](const std::string& e) {
+            S(fmt("{ const %s* __restrict__ row = dxe + ((size_t)(%s) * UVU_U + u) * UVU_DX;", T.c_str(), e.c_str()));
+            if (vec) {
+                for (int c = 0; c < P->Dx / 4; ++c) {
+                    S(fmt("  const float4 v%d = __ldg(reinterpret_cast<const float4*>(row) + %d);", c, c));
+                    S(fmt("  a_%d += v%d.x; a_%d += v%d.y; a_%d += v%d.z; a_%d += v%d.w;", 4 * c, c, 4 * c + 1, c, 4 * c + 2, c,
+                          4 * c + 3, c));
+                }
+            } else {
+                for (int k = 0; k < P->Dx; ++k) S(fmt("  a_%d += __ldg(row + %d);", k, k));
+            }
+            S("}");
+        };
+        S("int k = k0;");
+        S("#pragma unroll 1");
+        S("for (; k + 4 <= k1; k += 4) {");
+        S.ind++;
+        S("const int e0 = __ldg(seid + k), e1 = __ldg(seid + k + 1), e2 = __ldg(seid + k + 2), e3 = __ldg(seid + k + 3);");
+        add_row("e0");
+        add_row("e1");
+        add_row("e2");
+        add_row("e3");
+        S.ind--;
+        S("}");
+        S("for (; k < k1; ++k) {");
+        S.ind++;
+        S("const int e0 = __ldg(seid + k);");
+        add_row("e0");
+        S.ind--;
+        S("}");
+        S(T + "* __restrict__ dxr = dx + ((size_t)sn * UVU_U + u) * UVU_DX;");
+        for (int k = 0; k < P->Dx; ++k) S(fmt("dxr[%d] = a_%d;", k, k));
+        S.ind--;
+        S("}");
     }
 
     // ------------------------------------------------------------------ sender-stationary dx
@@ -1096,6 +1204,26 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 
 }  // namespace
 
+// Split the paths into `ng` contiguous register groups of about equal per-edge cost (CG
+// non-zeros plus two operations per output component).
+void balance_groups(Plan* plan, int ng) {
+    std::vector<double> cost;
+    double total = 0;
+    for (const PathInfo& p : plan->paths) {
+        cost.push_back(double(p.nz.size()) + 2.0 * (2 * p.l3 + 1));
+        total += cost.back();
+    }
+    plan->groups.assign(1, {});
+    double acc = 0;
+    for (int p = 0; p < plan->P; ++p) {
+        const int g = int(plan->groups.size()) - 1;
+        if (!plan->groups.back().empty() && g + 1 < ng && acc + cost[p] / 2 > total * (g + 1) / ng)
+            plan->groups.emplace_back();
+        plan->groups.back().push_back(p);
+        acc += cost[p];
+    }
+}
+
 std::string emit_source(Plan* plan) {
     Gen G{plan, plan->dtype == UVU_F64, plan->dtype == UVU_F64 ? "double" : "float"};
     const int U = plan->U, NG = int(plan->groups.size());
@@ -1114,10 +1242,21 @@ std::string emit_source(Plan* plan) {
     const int ncw = NG * UP / 32;
 
     // Pipelined (bulk-copy) kernels need whole warps per owner and 16-byte multiples for the
-    // per-edge weight rows; otherwise the direct-load kernels are emitted.
+    // per-edge weight rows; otherwise the direct-load kernels are emitted.  For the pipelined
+    // kernels the paths are re-split into register groups of balanced per-edge cost so that an
+    // owner has at least 8 consumer warps (more warps to hide shared-memory and FMA latency).
     // UVU_FORCE_DIRECT=1 (a debugging switch) selects the direct-load kernels everywhere.
     const bool force_direct = std::getenv("UVU_FORCE_DIRECT") && std::atoi(std::getenv("UVU_FORCE_DIRECT")) != 0;
-    const bool pipe_recv = !force_direct && U >= 32 && G.wbytes() % 16 == 0 && ncw * 32 + 32 <= 1024;
+    bool pipe_recv = !force_direct && U >= 32 && G.wbytes() % 16 == 0 && ncw * 32 + 32 <= 1024;
+    if (pipe_recv) {
+        const int want = std::max(NG, std::min(plan->P, std::max(1, (8 * 32 + UP - 1) / UP)));
+        const int ng2 = std::min(want, std::max(1, 512 / UP));
+        if (ng2 != NG && !plan->rebalanced) {
+            balance_groups(plan, ng2);
+            plan->rebalanced = true;
+            return emit_source(plan);  // once more, with the new grouping
+        }
+    }
     Gen::RecvPipe RF = G.recv_pipe(false, ncw), RE = G.recv_pipe(true, ncw);
     Gen::SendPipe SD = G.send_pipe();
     const bool pipe_dx = !force_direct && U >= 32 && G.send_pipe_ok(SD);
@@ -1194,7 +1333,7 @@ std::string emit_source(Plan* plan) {
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", G.T.c_str(), G.T.c_str()));
         S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
               G.T.c_str(), G.T.c_str(), G.T.c_str(), G.T.c_str()));
-        S(fmt("    %s* __restrict__ dx) {", G.T.c_str()));
+        S(fmt("    %s* __restrict__ dx, %s* __restrict__ dxe) {", G.T.c_str(), G.T.c_str()));
         S(fmt("  extern __shared__ __align__(16) unsigned char smem_raw[];"));
         S(fmt("  %s* sred = reinterpret_cast<%s*>(smem_raw);", G.T.c_str(), G.T.c_str()));
         S("  __shared__ int s_e0[UVU_RPB], s_e1[UVU_RPB], s_nch;");
@@ -1216,7 +1355,7 @@ std::string emit_source(Plan* plan) {
         S("  const int seg = g * ((UVU_UP + 31) / 32) + u / 32;");
         S("  const int lane_in_seg = u % UVU_SEGW;");
         for (int g = 0; g < NG; ++g)
-            S(fmt("  %sif (g == %d) edge_group%d(rl, seg, lane_in_seg, valid, s_e0[rl], s_e1[rl], nchunks, r, u, src, x, Y, w, gout, dY, dw, dx, sred, s_e0, s_e1);",
+            S(fmt("  %sif (g == %d) edge_group%d(rl, seg, lane_in_seg, valid, s_e0[rl], s_e1[rl], nchunks, r, u, src, x, Y, w, gout, dY, dw, dx, sred, s_e0, s_e1, dxe);",
                   g ? "else " : "", g, g));
         S("}");
     }
@@ -1224,6 +1363,8 @@ std::string emit_source(Plan* plan) {
         G.emit_dx_v2(S, SD);
     else
         G.emit_dx_kernel(S);
+    G.emit_dx_reduce(S);
+    plan->staged_ok = pipe_recv || NG == 1;
     return S.o.str();
 }
 

@@ -45,7 +45,7 @@ struct KernelGeom {
 
 struct DeviceModule {
     cudaLibrary_t lib = nullptr;
-    cudaKernel_t fwd = nullptr, bwd_edge = nullptr, bwd_dx = nullptr;
+    cudaKernel_t fwd = nullptr, bwd_edge = nullptr, bwd_dx = nullptr, bwd_dx_reduce = nullptr;
     int sm_count = 0;
     int occ_fwd = 1, occ_edge = 1, occ_dx = 1;  // resident blocks per SM
     unsigned* status_word = nullptr;            // device address of uvu_status_word
@@ -63,6 +63,8 @@ struct Plan {
     KernelGeom g_fwd, g_edge, g_dx;
     int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
     bool pipelined_recv = false, pipelined_dx = false;
+    bool staged_ok = false;
+    bool rebalanced = false;  // register groups re-split for the pipelined kernels  // the edge kernel can write per-edge dx partials (staged dx)
     // Upper bound on resident blocks per SM that the register budget is sized for, per kernel
     // (fwd, edge, dx); lowered to 1 for a kernel whose two-block budget makes ptxas spill.
     int minb[3] = {2, 2, 2};
@@ -82,6 +84,7 @@ uvu_status build_paths(Plan* plan, std::string* err);
 
 // codegen.cpp
 std::string emit_source(Plan* plan);
+void balance_groups(Plan* plan, int ng);
 
 // jit.cpp
 uvu_status compile_plan(Plan* plan, std::string* err);

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libuvu.so")
 
 UVU_F32, UVU_F64 = 0, 1
-UVU_DX_SENDER, UVU_DX_ATOMIC = 0, 1
+UVU_DX_SENDER, UVU_DX_ATOMIC, UVU_DX_STAGED = 0, 1, 2
 STATUS = {0: "UVU_OK", 1: "UVU_ERR_INVALID_ARGUMENT", 2: "UVU_ERR_UNSUPPORTED",
           3: "UVU_ERR_COMPILE", 4: "UVU_ERR_CUDA", 5: "UVU_ERR_OUT_OF_MEMORY"}
 
@@ -28,7 +28,8 @@ EXPORTS = (
     "uvu_plan_create", "uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
     "uvu_plan_device_status",
     "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
-    "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx", "uvu_conv_bwd",
+    "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
+    "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
     "uvu_status_string", "uvu_last_error_message",
 )
 
@@ -57,9 +58,11 @@ def _load():
         "uvu_csr_transpose_noalloc": [I64, I64, P, P, P, P, P, P],
         "uvu_graph_validate": [I64, I64, P, P, P, ctypes.POINTER(I64), P],
         "uvu_conv_fwd": [P, I64, I64, P, P, P, P, P, P, P],
-        "uvu_conv_bwd_edge": [P, I64, I64, P, P, P, P, P, P, P, P, P, P],
+        "uvu_conv_bwd_edge": [P, I64, I64, P, P, P, P, P, P, P, P, P, P, P],
         "uvu_conv_bwd_dx": [P, I64, I64, P, P, P, P, P, P, P, P],
-        "uvu_conv_bwd": [P, I64, I64, P, P, P, P, P, P, P, P, P, P, P, P, I, P],
+        "uvu_conv_bwd_dx_reduce": [P, I64, I64, P, P, P, P, P],
+        "uvu_conv_bwd_workspace": [P, I64, I64, I, ctypes.POINTER(SZ)],
+        "uvu_conv_bwd": [P, I64, I64, P, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -94,8 +97,8 @@ def _wrap(name):
 for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
            "uvu_plan_device_status",
            "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
-           "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge", "uvu_conv_bwd_dx",
-           "uvu_conv_bwd"):
+           "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
+           "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd"):
     globals()[_n] = _wrap(_n)
 
 
@@ -180,22 +183,42 @@ class Plan:
                      _ptr(w), _ptr(recv_offsets), _ptr(src), _ptr(out), _stream(stream))
 
     def bwd_edge(self, n_nodes, x, Y, w, recv_offsets, src, d_out, dY=None, dw=None,
-                 dx_atomic=None, stream=None):
+                 dx_atomic=None, dx_edge=None, stream=None):
         uvu_conv_bwd_edge(self.handle, n_nodes, src.numel(), _ptr(x), _ptr(Y), _ptr(w),
                           _ptr(recv_offsets), _ptr(src), _ptr(d_out), _ptr(dY), _ptr(dw),
-                          _ptr(dx_atomic), _stream(stream))
+                          _ptr(dx_atomic), _ptr(dx_edge), _stream(stream))
 
     def bwd_dx(self, n_nodes, n_edges, Y, w, send_offsets, send_eids, send_recv, d_out, dx,
                stream=None):
         uvu_conv_bwd_dx(self.handle, n_nodes, n_edges, _ptr(Y), _ptr(w), _ptr(send_offsets),
                         _ptr(send_eids), _ptr(send_recv), _ptr(d_out), _ptr(dx), _stream(stream))
 
+    def bwd_dx_reduce(self, n_nodes, n_edges, send_offsets, send_eids, dx_edge, dx, stream=None):
+        uvu_conv_bwd_dx_reduce(self.handle, n_nodes, n_edges, _ptr(send_offsets), _ptr(send_eids),
+                               _ptr(dx_edge), _ptr(dx), _stream(stream))
+
+    def workspace_bytes(self, n_nodes, n_edges, dx_mode) -> int:
+        b = ctypes.c_size_t()
+        uvu_conv_bwd_workspace(self.handle, n_nodes, n_edges, dx_mode, ctypes.byref(b))
+        return b.value
+
     def bwd(self, n_nodes, x, Y, w, recv_offsets, src, send_offsets, send_eids, send_recv,
-            d_out, dx=None, dY=None, dw=None, dx_mode=UVU_DX_SENDER, stream=None):
-        uvu_conv_bwd(self.handle, n_nodes, src.numel(), _ptr(x), _ptr(Y), _ptr(w),
+            d_out, dx=None, dY=None, dw=None, dx_mode=UVU_DX_SENDER, workspace=None,
+            stream=None):
+        """Full VJP.  UVU_DX_STAGED needs `workspace` (a uint8 device tensor of at least
+        workspace_bytes() bytes); pass None to let this wrapper allocate it with torch."""
+        n_edges = src.numel()
+        ws_ptr, ws_bytes = None, 0
+        if dx_mode == UVU_DX_STAGED and dx is not None:
+            need = self.workspace_bytes(n_nodes, n_edges, dx_mode)
+            if workspace is None:
+                import torch
+                workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=src.device)
+            ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+        uvu_conv_bwd(self.handle, n_nodes, n_edges, _ptr(x), _ptr(Y), _ptr(w),
                      _ptr(recv_offsets), _ptr(src), _ptr(send_offsets), _ptr(send_eids),
                      _ptr(send_recv), _ptr(d_out), _ptr(dx), _ptr(dY), _ptr(dw), dx_mode,
-                     _stream(stream))
+                     ws_ptr, ws_bytes, _stream(stream))
 
 
 class Graph:

@@ -64,8 +64,15 @@ typedef enum {
 
 /* How dx is produced by uvu_conv_bwd. */
 typedef enum {
-    UVU_DX_SENDER = 0, /* sender-stationary over the transposed CSR: no atomics, deterministic */
-    UVU_DX_ATOMIC = 1  /* edge-parallel atomic scatter fused into the edge kernel (comparison) */
+    UVU_DX_SENDER = 0, /* sender-stationary over the transposed CSR, recomputing each edge's
+                          contribution from w, Y and the gathered d_out row: no atomics,
+                          deterministic, no workspace */
+    UVU_DX_ATOMIC = 1, /* edge-parallel atomic scatter fused into the edge kernel (comparison);
+                          summation order not deterministic */
+    UVU_DX_STAGED = 2  /* the edge kernel writes each edge's dx contribution to a workspace, then a
+                          sender-stationary kernel sums them over the transposed CSR in ascending
+                          edge order: no atomics, deterministic, E*U*D_x*sizeof(dtype) bytes of
+                          workspace */
 } uvu_dx_mode;
 
 /* ---------------------------------------------------------------------------- planning ---- */
@@ -172,11 +179,27 @@ uvu_status uvu_conv_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const
  * opening post, backward paragraph).  dY and dw are overwritten; either may be NULL (skipped).
  * If dx_atomic is not NULL, dx is first zeroed and then accumulated by atomic adds from the
  * same kernel (the atomic-scatter variant; its summation order is not deterministic).
+ * If dx_edge is not NULL (device [E][U][D_x]), each edge's dx contribution
+ * sum_p w[e,p,u] sum_{m2,m3} C Y[e] d_out[recv(e)] is written there, to be summed per sender by
+ * uvu_conv_bwd_dx_reduce (UVU_ERR_UNSUPPORTED for a plan whose kernels cannot produce it).
  * One kernel launch (plus a memset when dx_atomic is given). */
 uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
                              const void *Y, const void *w, const int32_t *recv_offsets,
                              const int32_t *src, const void *d_out, void *dY, void *dw,
-                             void *dx_atomic, uvu_stream_t stream);
+                             void *dx_atomic, void *dx_edge, uvu_stream_t stream);
+
+/* Sender-stationary reduction of per-edge dx contributions: dx[s,u,:] = sum over the sender's
+ * edges (transposed CSR, ascending edge id) of dx_edge[e,u,:].  Written once per sender, no
+ * atomics, bitwise deterministic ("Receiver-streaming convolutions ...", reply on source- vs
+ * destination-stationary convolutions: the dx side owned by the source node).
+ * One kernel launch. */
+uvu_status uvu_conv_bwd_dx_reduce(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges,
+                                  const int32_t *send_offsets, const int32_t *send_eids,
+                                  const void *dx_edge, void *dx, uvu_stream_t stream);
+
+/* Bytes of device workspace uvu_conv_bwd needs in dx_mode (0 except for UVU_DX_STAGED). */
+uvu_status uvu_conv_bwd_workspace(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges,
+                                  uvu_dx_mode dx_mode, size_t *bytes);
 
 /* Backward dx, sender-stationary: each (sender, channel) owner walks the sender's edges through
  * the transposed CSR and writes dx once, without atomics; deterministic (bitwise repeatable)
@@ -187,13 +210,17 @@ uvu_status uvu_conv_bwd_dx(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, co
                            const int32_t *send_recv, const void *d_out, void *dx,
                            uvu_stream_t stream);
 
-/* Full VJP: dx, dY, dw (any may be NULL = not computed).  dx_mode selects the dx kernel; the
- * transposed-CSR arguments may be NULL when dx_mode == UVU_DX_ATOMIC or dx == NULL. */
+/* Full VJP: dx, dY, dw (any may be NULL = not computed).  dx_mode selects how dx is formed; the
+ * transposed-CSR arguments may be NULL when dx_mode == UVU_DX_ATOMIC or dx == NULL, and
+ * send_recv may be NULL for UVU_DX_STAGED.  `workspace` (caller-owned device memory of at least
+ * uvu_conv_bwd_workspace() bytes, 16-byte aligned) is needed by UVU_DX_STAGED only.
+ * Launches: SENDER 2 kernels, ATOMIC 1 kernel + 1 memset, STAGED 2 kernels. */
 uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
                         const void *Y, const void *w, const int32_t *recv_offsets,
                         const int32_t *src, const int32_t *send_offsets,
                         const int32_t *send_eids, const int32_t *send_recv, const void *d_out,
-                        void *dx, void *dY, void *dw, uvu_dx_mode dx_mode, uvu_stream_t stream);
+                        void *dx, void *dY, void *dw, uvu_dx_mode dx_mode, void *workspace,
+                        size_t workspace_bytes, uvu_stream_t stream);
 
 /* ---------------------------------------------------------------------------- errors ---- */
 

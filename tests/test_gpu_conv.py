@@ -14,6 +14,7 @@ from gpu_util import Problem, check, dev
 pytestmark = pytest.mark.gpu
 
 SH3 = "1x0e+1x1o+1x2e+1x3o"
+MODES = (uvu.UVU_DX_SENDER, uvu.UVU_DX_ATOMIC, uvu.UVU_DX_STAGED)
 
 
 def _full_compare(P):
@@ -21,7 +22,7 @@ def _full_compare(P):
     check(out, P.ref_out(), P.f64, "out")
     rdY, rdw = P.ref_edges()
     rdx = P.ref_dx()
-    for mode in (uvu.UVU_DX_SENDER, uvu.UVU_DX_ATOMIC):
+    for mode in MODES:
         dx, dY, dw = (t.cpu().numpy() for t in P.bwd(mode))
         check(dY, rdY, P.f64, "dY")
         check(dw, rdw, P.f64, "dw")
@@ -68,7 +69,7 @@ def test_no_edges_writes_zeros():
     x = np.ones((9, 32, 4), np.float32)
     P = Problem(spec, recv, src, x, np.zeros((0, 16), np.float32), 9)
     assert torch.all(P.fwd() == 0)
-    for mode in (uvu.UVU_DX_SENDER, uvu.UVU_DX_ATOMIC):
+    for mode in MODES:
         dx, dY, dw = P.bwd(mode)
         assert torch.all(dx == 0) and dY.numel() == 0 and dw.numel() == 0
 
@@ -90,7 +91,7 @@ def test_full_size_sampled(key):
     check(out[rs_t].cpu().numpy(), P.ref_out(rs), P.f64, "out")
     rdY, rdw = P.ref_edges(es)
     rdx = P.ref_dx(ss)
-    for mode in (uvu.UVU_DX_SENDER, uvu.UVU_DX_ATOMIC):
+    for mode in MODES:
         dx, dY, dw = P.bwd(mode)
         check(dY[es_t].cpu().numpy(), rdY, P.f64, "dY")
         check(dw[es_t].cpu().numpy(), rdw, P.f64, "dw")
@@ -107,13 +108,14 @@ def test_full_size_sampled(key):
     assert P.status_ok()
 
 
-def test_deterministic_kernels_repeat_bitwise():
+@pytest.mark.parametrize("mode", [uvu.UVU_DX_SENDER, uvu.UVU_DX_STAGED])
+def test_deterministic_kernels_repeat_bitwise(mode):
     P = Problem.from_spec(1)
     o1 = P.fwd()
-    a1 = P.bwd(uvu.UVU_DX_SENDER)
+    a1 = P.bwd(mode)
     for _ in range(2):
         assert torch.equal(P.fwd(), o1)
-        a2 = P.bwd(uvu.UVU_DX_SENDER)
+        a2 = P.bwd(mode)
         for t1, t2 in zip(a1, a2):
             assert torch.equal(t1, t2)
     assert P.status_ok()

@@ -23,7 +23,8 @@ def _run(P, env):
         spec = P.spec
         P.plan = uvu.Plan(spec.irreps_x, spec.irreps_sh, spec.lmax_out, spec.dtype)
         out = P.fwd()
-        res = [out] + list(P.bwd(uvu.UVU_DX_SENDER)) + [P.bwd(uvu.UVU_DX_ATOMIC)[0]]
+        res = [out] + list(P.bwd(uvu.UVU_DX_SENDER)) + [P.bwd(uvu.UVU_DX_ATOMIC)[0],
+                                                        P.bwd(uvu.UVU_DX_STAGED)[0]]
         torch.cuda.synchronize()
         assert P.status_ok()
         return res
@@ -37,7 +38,7 @@ def _run(P, env):
 def test_pipelined_matches_direct_full_size(key):
     P = Problem.from_spec(key)
     ref = _run(P, {"UVU_FORCE_DIRECT": "1"})
-    names = ("out", "dx", "dY", "dw", "dx_atomic")
+    names = ("out", "dx", "dY", "dw", "dx_atomic", "dx_staged")
     for env in ({}, {"UVU_PIPE_CH": "1"}, {"UVU_PIPE_CH": "1", "UVU_PIPE_NST": "2"}):
         got = _run(P, env)
         for n, a, b in zip(names, got, ref):

@@ -72,10 +72,16 @@ def test_host_argument_errors_before_any_launch():
     assert L.uvu_conv_fwd(p.handle, 4, 4, None, None, None, None, None, None, None) == 1
     assert L.uvu_conv_fwd(p.handle, 4, 4, bad, bad, bad, bad, bad, bad, None) == 1
     assert "aligned" in uvu.uvu_last_error_message()
-    assert L.uvu_conv_bwd(p.handle, 4, 4, *[None] * 12, 7, None) == 1  # bad dx_mode
+    assert L.uvu_conv_bwd(p.handle, 4, 4, *[None] * 12, 7, None, 0, None) == 1  # bad dx_mode
     assert L.uvu_conv_bwd_dx(p.handle, 4, 4, None, None, None, None, None, None, None, None) == 1
     assert L.uvu_conv_bwd_edge(p.handle, 4, 4, None, None, None, None, None, None, bad, None,
-                               None, None) == 1
+                               None, None, None) == 1
+    assert L.uvu_conv_bwd_dx_reduce(p.handle, 4, 4, None, None, None, None, None) == 1
+    nbw = ctypes.c_size_t()
+    assert L.uvu_conv_bwd_workspace(p.handle, 10, 20, uvu.UVU_DX_STAGED, ctypes.byref(nbw)) == 0
+    assert nbw.value == 20 * 16 * 4 * 4
+    assert L.uvu_conv_bwd_workspace(p.handle, 10, 20, uvu.UVU_DX_SENDER, ctypes.byref(nbw)) == 0
+    assert nbw.value == 0
     nb = ctypes.c_size_t()
     assert L.uvu_csr_transpose_workspace(10, 20, ctypes.byref(nb)) == 0 and nb.value >= 120
     assert L.uvu_csr_transpose(10, 20, None, None, None, None, None, None, 0, None) == 1
