@@ -84,9 +84,10 @@ extern "C" uvu_status uvu_plan_create(const char* irreps_x, const char* irreps_s
         std::string err;
         uvu_status s = build_paths(&p, &err);
         if (s != UVU_OK) return fail(s, err);
-        // Compile with a register budget sized for two resident blocks per SM; a kernel that
-        // spills more than a call-site save under that budget is recompiled with it lifted.
-        for (int attempt = 0; attempt < 2; ++attempt) {
+        // Compile with a register budget sized for as many resident blocks per SM as the shared
+        // memory allows (up to 4); a kernel that spills more than a call-site save under that
+        // budget is recompiled for one block fewer.
+        for (int attempt = 0; attempt < 4; ++attempt) {
             p.source = emit_source(&p);
             if (p.g_fwd.threads > 1024 || p.g_edge.threads > 1024 || p.g_dx.threads > 1024)
                 return fail(UVU_ERR_UNSUPPORTED, "multiplicity x register groups exceeds 1024 threads per owner");
@@ -95,8 +96,8 @@ extern "C" uvu_status uvu_plan_create(const char* irreps_x, const char* irreps_s
             const char* names[3] = {"uvu_fwd", "uvu_bwd_edge", "uvu_bwd_dx"};
             bool again = false;
             for (int k = 0; k < 3; ++k)
-                if (p.minb[k] > 1 && spill_bytes(p.log, names[k]) > 32) {
-                    p.minb[k] = 1;
+                if (p.minb_eff[k] > 1 && spill_bytes(p.log, names[k]) > 32) {
+                    p.minb[k] = p.minb_eff[k] - 1;
                     again = true;
                 }
             if (!again) break;

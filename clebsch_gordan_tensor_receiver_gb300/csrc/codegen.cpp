@@ -571,8 +571,9 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         // per-stage partial sums of the edge kernel: dY over warps, dx over register groups
         const size_t dyp = with_partials ? a16(2 * size_t(ncw) * R.ch * P->Dy * P->elem()) : 0;
         const size_t dxp = (with_partials && NG > 1) ? a16(2 * size_t(NG) * R.ch * P->U_pad * P->Dx * P->elem()) : 0;
-        const size_t room = 108 * 1024 > dyp + dxp + 2 * stage ? 108 * 1024 - dyp - dxp : 2 * stage;
-        R.nst = int(std::max<size_t>(2, std::min<size_t>(6, room / stage)));
+        // Two stages: with several blocks resident per SM, one stage of look-ahead per block keeps
+        // enough bytes in flight, and the smaller footprint lets more blocks (warps) reside.
+        R.nst = 2;
         if (const char* e = std::getenv("UVU_PIPE_NST")) R.nst = std::max(2, std::atoi(e));
         R.w_off = 0;
         R.x_off = a16(R.ch * wbytes());
@@ -596,11 +597,17 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S(fmt("#define %s_PART %zu", pre, R.part_off));
         S(fmt("#define %s_XPART %zu", pre, R.xpart_off));
         S(fmt("#define %s_TX %zu", pre, R.tx_per_edge));
-        S(fmt("#define %s_MINB %d", pre, std::min(minb(R.total), pre[0] == 'F' ? P->minb[0] : P->minb[1])));
+        const int mb = std::min(minb(R.total), pre[0] == 'F' ? P->minb[0] : P->minb[1]);
+        P->minb_eff[pre[0] == 'F' ? 0 : 1] = mb;
+        S(fmt("#define %s_MINB %d", pre, mb));
     }
-    // Blocks per SM the shared-memory footprint allows (capped at 2): the register budget the
-    // compiler may use is sized so that this many blocks stay resident.
-    static int minb(size_t smem) { return int(std::max<size_t>(1, std::min<size_t>(2, (227 * 1024) / (smem + 1024)))); }
+    // Blocks per SM the shared-memory footprint allows (capped at 4); UVU_PIPE_MINB (a tuning
+    // switch) lowers the cap.
+    static int minb(size_t smem) {
+        size_t cap = 4;
+        if (const char* e = std::getenv("UVU_PIPE_MINB")) cap = size_t(std::max(1, std::atoi(e)));
+        return int(std::max<size_t>(1, std::min<size_t>(cap, (227 * 1024) / (smem + 1024))));
+    }
 
     // Producer for the receiver-ordered kernels: w block of the chunk (one copy, the receiver's
     // edges are contiguous), Y block (one copy), x row of each edge's sender (one copy each).
@@ -1055,7 +1062,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         D.g_off = a16(D.ch * D.wt);
         D.y_off = D.g_off + a16(D.ch * D.gt);
         D.stage = D.y_off + (D.ybulk ? a16(D.ch * ybytes()) : 0);
-        D.nst = int(std::max<size_t>(2, std::min<size_t>(6, (108 * 1024) / D.stage)));
+        D.nst = 2;
         D.bar_off = D.nst * D.stage;
         D.total = D.bar_off + 16 * D.nst;
         D.tx = pe;
@@ -1082,7 +1089,9 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S(fmt("#define DX_BAR %zu", D.bar_off));
         S(fmt("#define DX_TX %zu", D.tx));
         S(fmt("#define DX_NCW %d", D.ut / 32));
-        S(fmt("#define DX_MINB %d", std::min(minb(D.total), P->minb[2])));
+        const int mb = std::min(minb(D.total), P->minb[2]);
+        P->minb_eff[2] = mb;
+        S(fmt("#define DX_MINB %d", mb));
         // producer
         S(fmt("__device__ __noinline__ void dx_producer(long long N, const int* __restrict__ soff, const int* __restrict__ seid,"));
         S(fmt("    const int* __restrict__ srecv, const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ gout,",
@@ -1248,10 +1257,12 @@ std::string emit_source(Plan* plan) {
     // UVU_FORCE_DIRECT=1 (a debugging switch) selects the direct-load kernels everywhere.
     const bool force_direct = std::getenv("UVU_FORCE_DIRECT") && std::atoi(std::getenv("UVU_FORCE_DIRECT")) != 0;
     bool pipe_recv = !force_direct && U >= 32 && G.wbytes() % 16 == 0 && ncw * 32 + 32 <= 1024;
-    if (pipe_recv) {
-        const int want = std::max(NG, std::min(plan->P, std::max(1, (8 * 32 + UP - 1) / UP)));
-        const int ng2 = std::min(want, std::max(1, 512 / UP));
-        if (ng2 != NG && !plan->rebalanced) {
+    // UVU_PIPE_GROUPS=n (a tuning switch) re-splits the paths into n register groups of
+    // balanced per-edge cost for the pipelined kernels; by default the register-budget groups
+    // stand (more groups add a barrier-coupled imbalance between warps that measured slower).
+    if (pipe_recv && std::getenv("UVU_PIPE_GROUPS") && !plan->rebalanced) {
+        const int ng2 = std::max(1, std::min(std::min(plan->P, std::atoi(std::getenv("UVU_PIPE_GROUPS"))), std::max(1, 512 / UP)));
+        if (ng2 != NG) {
             balance_groups(plan, ng2);
             plan->rebalanced = true;
             return emit_source(plan);  // once more, with the new grouping

@@ -66,8 +66,9 @@ struct Plan {
     bool staged_ok = false;
     bool rebalanced = false;  // register groups re-split for the pipelined kernels  // the edge kernel can write per-edge dx partials (staged dx)
     // Upper bound on resident blocks per SM that the register budget is sized for, per kernel
-    // (fwd, edge, dx); lowered to 1 for a kernel whose two-block budget makes ptxas spill.
-    int minb[3] = {2, 2, 2};
+    // (fwd, edge, dx); lowered one block at a time for a kernel whose budget makes ptxas spill.
+    int minb[3] = {4, 4, 4};
+    int minb_eff[3] = {1, 1, 1};  // value used by the last emission
     std::string source, log;
     std::vector<char> cubin;
     std::mutex mu;
