@@ -46,6 +46,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
     ap.add_argument("--single-mode", action="store_true",
                     help="warm up and time only --dx-mode (profiling runs)")
     return ap.parse_args(argv)
@@ -313,6 +314,8 @@ def main(argv=None):
             per["uvu_bwd_edge"].append(e[1].elapsed_time(e[2]))
             if dx_kernel[mode]:
                 per[dx_kernel[mode]].append(e[2].elapsed_time(e[3]))
+        spread[mode] = {k: {"median": statistics.median(v), "min": min(v), "max": max(v)}
+                        for k, v in per.items()}
         return total, {k: statistics.mean(v) for k, v in per.items()}
 
     for _ in range(max(args.warmup, 3)):
@@ -320,8 +323,10 @@ def main(argv=None):
             step(m)
     torch.cuda.synchronize()
 
+    spread = {}
     clocks = ClockSampler(local_rank)
-    clocks.start()
+    if not args.no_clocks:
+        clocks.start()
     results = {m: timed(m, args.steps) for m in modes}
     clk = clocks.stop()
     assert plan.device_status() == 0, "a kernel reported a bounded-wait timeout"
@@ -392,6 +397,7 @@ def main(argv=None):
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["GB_s"],
                      "peak": hbm_peak, "unit": "GB/s", "frac": kernels[dom]["frac"],
                      "traffic": traffic, "peak_source": peak_src + " hbm_gbs (copy)"},
+        "kernel_ms_spread": spread,
         "csr_build_ms": csr_ms,
         "clocks": clk,
         "gpu_launches": args.steps * (2 if args.dx_mode == "atomic" else 3),

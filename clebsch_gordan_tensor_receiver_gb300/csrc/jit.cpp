@@ -5,6 +5,7 @@
 // never inspected.  Identical sources share one compilation through a process-wide cache.
 #include <nvrtc.h>
 
+#include <cstdio>
 #include <cstdlib>
 #include <functional>
 #include <map>
@@ -31,8 +32,13 @@ uvu_status nvrtc_compile(const std::string& src, CacheEntry* out, std::string* e
         *err = std::string("nvrtcCreateProgram: ") + nvrtcGetErrorString(r);
         return UVU_ERR_COMPILE;
     }
+    // --no-cache: NVRTC's cross-process compile cache returns the cubin without running ptxas
+    // on a hit, so the log would lack the register/spill report the planner's register-budget
+    // choice reads (a later process then kept a spilling four-block budget: edge kernel 1.35 ms
+    // instead of 0.87 ms on MACE-medium).  Plans compile once per process and in-process copies
+    // share the result through the cache below.
     const char* opts[] = {"--gpu-architecture=sm_103a", "--std=c++17", "-lineinfo",
-                          "--ptxas-options=-v", "--fmad=true"};
+                          "--ptxas-options=-v", "--fmad=true", "--no-cache"};
     r = nvrtcCompileProgram(prog, int(sizeof(opts) / sizeof(opts[0])), opts);
     size_t log_size = 0;
     nvrtcGetProgramLogSize(prog, &log_size);
@@ -137,6 +143,20 @@ uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string
                 return UVU_ERR_CUDA;
             }
         }
+        if (k.g->persistent) {
+            // The persistent grid is sized for the resident blocks the occupancy calculation
+            // reports, which assumes the largest shared-memory carveout.  Without this
+            // preference the driver sometimes kept a smaller L1/shared split, fewer blocks fit,
+            // and the grid ran as 1.5 waves (the edge kernel measured 1.35 ms instead of 0.87 ms
+            // in some processes).
+            ce = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      int(cudaSharedmemCarveoutMaxShared));
+            if (ce != cudaSuccess) {
+                *err = std::string("cudaFuncSetAttribute(carveout, ") + k.name + "): " + cudaGetErrorString(ce);
+                cudaLibraryUnload(m.lib);
+                return UVU_ERR_CUDA;
+            }
+        }
         int occ = 0;
         ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, f, k.g->threads, k.g->smem);
         if (ce != cudaSuccess || occ < 1) {
@@ -158,6 +178,21 @@ uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string
         *err = std::string("module set-up: ") + cudaGetErrorString(ce);
         cudaLibraryUnload(m.lib);
         return UVU_ERR_CUDA;
+    }
+    if (std::getenv("UVU_DEBUG")) {  // diagnostics of the loaded module (a debugging switch)
+        std::fprintf(stderr, "[uvu] device %d sms %d occupancy fwd %d edge %d dx %d minb %d/%d/%d spills %zu/%zu/%zu\n", dev,
+                     m.sm_count, m.occ_fwd, m.occ_edge, m.occ_dx, plan->minb_eff[0], plan->minb_eff[1],
+                     plan->minb_eff[2], spill_bytes(plan->log, "uvu_fwd"), spill_bytes(plan->log, "uvu_bwd_edge"),
+                     spill_bytes(plan->log, "uvu_bwd_dx"));
+        for (const char* k : {"uvu_fwd", "uvu_bwd_edge", "uvu_bwd_dx"}) {
+            const std::string key = std::string("Function properties for ") + k + "\n";
+            const size_t at = plan->log.find(key);
+            if (at != std::string::npos) {
+                const size_t u = plan->log.find("Used ", at);
+                const size_t e = plan->log.find('\n', u);
+                std::fprintf(stderr, "[uvu]   %s: %s\n", k, plan->log.substr(u, e - u).c_str());
+            }
+        }
     }
     auto res = plan->modules.emplace(dev, m);
     *out = &res.first->second;

@@ -45,3 +45,17 @@ def test_cg_immediates_present_in_source():
     src, _ = p.source()
     # the (1,1,1) coupling is the cross product / sqrt(2): 0.707106781 appears as an immediate
     assert "7.071067" in src
+
+
+def test_plan_is_identical_across_processes():
+    # The planner's register-budget choice reads ptxas's report; it must see a full report in
+    # every process (no cross-process compile cache short-circuiting it), so two processes emit
+    # the same source.
+    import subprocess
+    import sys
+    code = ("import hashlib; from clebsch_gordan_tensor_receiver_gb300 import uvu, workloads; "
+            "s = workloads.SPECS[1]; p = uvu.Plan(s.irreps_x, s.irreps_sh, s.lmax_out, s.dtype); "
+            "src, log = p.source(); print(hashlib.sha256(src.encode()).hexdigest(), 'Used' in log)")
+    outs = [subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, check=True,
+                           cwd=__import__("conftest").ROOT).stdout.split() for _ in range(2)]
+    assert outs[0] == outs[1] and outs[0][1] == "True"
