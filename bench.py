@@ -44,6 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--dx-mode", default="staged", choices=["staged", "sender", "atomic"])
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunks", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
@@ -403,7 +404,11 @@ def main(argv=None):
         "gpu_launches": args.steps * (2 if args.dx_mode == "atomic" else 3),
     }
 
-    # end-to-end through the C ABI from pinned host buffers
+    # end-to-end through the C ABI from pinned host buffers: every step copies its inputs (x, Y,
+    # w, d_out and the graph arrays) in and its results (out, dx, dY, dw) out.  The receivers are
+    # split into chunks whose copies and kernels are pipelined over three streams (copy in,
+    # compute, copy out), using receiver sub-ranges of the same entry points (offsets are absolute
+    # edge indices, so recv_offsets + r0 with n_nodes = r1 - r0 is a valid CSR for the chunk).
     if not args.no_e2e:
         pin = lambda t: t.cpu().pin_memory()
         hin = {"x": pin(x), "Y": pin(Y), "w": pin(w), "g": pin(g), "roff": pin(G.recv_offsets),
@@ -413,32 +418,80 @@ def main(argv=None):
         hout = {"out": pin(out), "dx": pin(dx), "dY": pin(dY), "dw": pin(dw)}
         h2d = sum(v.numel() * v.element_size() for v in hin.values())
         d2h = sum(v.numel() * v.element_size() for v in hout.values())
-        mode_id = {"sender": uvu.UVU_DX_SENDER, "atomic": uvu.UVU_DX_ATOMIC,
-                   "staged": uvu.UVU_DX_STAGED}[args.dx_mode]
+        roff_h = hin["roff"].numpy()
+        # atomic dx is zeroed by the edge-kernel call, so that mode runs as one chunk
+        K = 1 if args.dx_mode == "atomic" else max(1, min(args.e2e_chunks, N))
+        cuts = [0]
+        for i in range(1, K):  # equal edge counts per chunk
+            cuts.append(int(np.searchsorted(roff_h, i * E / K)))
+        cuts.append(N)
+        cuts = sorted(set(cuts))
+        s_in, s_cmp, s_out = torch.cuda.Stream(dev), stream, torch.cuda.Stream(dev)
+        mode_e2e = args.dx_mode
 
         def e2e_step():
-            for k, v in hin.items():
-                dbuf[k].copy_(v, non_blocking=True)
-            b = dbuf
-            plan.fwd(N, b["x"], b["Y"], b["w"], b["roff"], b["src"], out, stream)
-            plan.bwd(N, b["x"], b["Y"], b["w"], b["roff"], b["src"], b["soff"], b["seid"],
-                     b["srecv"], b["g"], dx=dx, dY=dY, dw=dw, dx_mode=mode_id, workspace=ws,
-                     stream=stream)
-            hout["out"].copy_(out, non_blocking=True)
-            hout["dx"].copy_(dx, non_blocking=True)
-            hout["dY"].copy_(dY, non_blocking=True)
-            hout["dw"].copy_(dw, non_blocking=True)
+            ev_in, ev_cmp = [], []
+            with torch.cuda.stream(s_in):
+                s_in.wait_stream(s_out)  # previous step's results are out before buffers are reused
+                for k in ("x", "roff", "src", "soff", "seid", "srecv"):
+                    dbuf[k].copy_(hin[k], non_blocking=True)
+                for a, b in zip(cuts[:-1], cuts[1:]):
+                    e0, e1 = int(roff_h[a]), int(roff_h[b])
+                    dbuf["Y"][e0:e1].copy_(hin["Y"][e0:e1], non_blocking=True)
+                    dbuf["w"][e0:e1].copy_(hin["w"][e0:e1], non_blocking=True)
+                    dbuf["g"][a:b].copy_(hin["g"][a:b], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(s_in)
+                    ev_in.append(ev)
+            d = dbuf
+            for i, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+                s_cmp.wait_event(ev_in[i])
+                n = b - a
+                ro = d["roff"][a:]
+                plan.fwd(n, d["x"], d["Y"], d["w"], ro, d["src"], out[a:], s_cmp)
+                plan.bwd_edge(n, d["x"], d["Y"], d["w"], ro, d["src"], d["g"][a:], dY=dY, dw=dw,
+                              dx_atomic=dx if mode_e2e == "atomic" else None,
+                              dx_edge=ws if mode_e2e == "staged" else None, stream=s_cmp)
+                ev = torch.cuda.Event()
+                ev.record(s_cmp)
+                ev_cmp.append(ev)
+            if mode_e2e == "staged":
+                plan.bwd_dx_reduce(N, E, d["soff"], d["seid"], ws, dx, s_cmp)
+            elif mode_e2e == "sender":
+                plan.bwd_dx(N, E, d["Y"], d["w"], d["soff"], d["seid"], d["srecv"], d["g"], dx, s_cmp)
+            ev_dx = torch.cuda.Event()
+            ev_dx.record(s_cmp)
+            with torch.cuda.stream(s_out):
+                for i, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+                    s_out.wait_event(ev_cmp[i])
+                    e0, e1 = int(roff_h[a]), int(roff_h[b])
+                    hout["out"][a:b].copy_(out[a:b], non_blocking=True)
+                    hout["dY"][e0:e1].copy_(dY[e0:e1], non_blocking=True)
+                    hout["dw"][e0:e1].copy_(dw[e0:e1], non_blocking=True)
+                s_out.wait_event(ev_dx)
+                hout["dx"].copy_(dx, non_blocking=True)
 
-        e2e_step()
+        # device-resident results of one ordinary step, to check the chunked host path against
+        step(args.dx_mode)
         torch.cuda.synchronize()
+        ref = {k: v.clone() for k, v in dict(out=out, dx=dx, dY=dY, dw=dw).items()}
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        same = all(torch.equal(hout[k], ref[k].cpu()) for k in ref) if args.dx_mode != "atomic" else None
+        del ref
         barrier(world)
         tw = time.perf_counter()
         for _ in range(args.e2e_steps):
             e2e_step()
         torch.cuda.synchronize()
         e_ms = max_over_ranks((time.perf_counter() - tw) * 1000 / args.e2e_steps, world, dev)
+        # the results that came back are the full outputs of the step
         line["e2e"] = {"value": world * E / (e_ms / 1000), "unit": "edges/s",
-                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+                       "chunks": len(cuts) - 1, "dx_mode": mode_e2e, "bitwise_equal_to_resident": same,
+                       "h2d_GB_s": h2d / (e_ms / 1000) / 1e9, "d2h_GB_s": d2h / (e_ms / 1000) / 1e9}
+        assert plan.device_status() == 0
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import paths

@@ -27,6 +27,14 @@ uvu_status need(const void* p, const char* name) {
     return UVU_OK;
 }
 
+// Index arrays (int32) are read with scalar loads: 4-byte alignment is enough, which lets a
+// caller pass a receiver sub-range (recv_offsets + r0) of a larger CSR.
+uvu_status need_idx(const void* p, const char* name) {
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, std::string(name) + " is NULL");
+    if (reinterpret_cast<uintptr_t>(p) & 3u) return fail(UVU_ERR_INVALID_ARGUMENT, std::string(name) + " is not 4-byte aligned");
+    return UVU_OK;
+}
+
 uvu_status opt(const void* p, const char* name) {
     if (p && !aligned16(p)) return fail(UVU_ERR_INVALID_ARGUMENT, std::string(name) + " is not 16-byte aligned");
     return UVU_OK;
@@ -214,12 +222,12 @@ extern "C" uvu_status uvu_conv_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
     UVU_TRY(check_sizes(n_nodes, n_edges));
     if (n_nodes == 0) return ok();
     UVU_TRY(need(out, "out"));
-    UVU_TRY(need(recv_offsets, "recv_offsets"));
+    UVU_TRY(need_idx(recv_offsets, "recv_offsets"));
     if (n_edges > 0) {
         UVU_TRY(need(x, "x"));
         UVU_TRY(need(Y, "Y"));
         UVU_TRY(need(w, "w"));
-        UVU_TRY(need(src, "src"));
+        UVU_TRY(need_idx(src, "src"));
     }
     DeviceModule* m = nullptr;
     std::string err;
@@ -245,12 +253,12 @@ extern "C" uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_
     if (dx_edge && !p->staged_ok)
         return fail(UVU_ERR_UNSUPPORTED, "per-edge dx partials need the pipelined kernels or a single register group");
     if (n_nodes == 0 || (!dY && !dw && !dx_atomic && !dx_edge)) return ok();
-    UVU_TRY(need(recv_offsets, "recv_offsets"));
+    UVU_TRY(need_idx(recv_offsets, "recv_offsets"));
     if (n_edges > 0) {
         UVU_TRY(need(x, "x"));
         UVU_TRY(need(Y, "Y"));
         UVU_TRY(need(w, "w"));
-        UVU_TRY(need(src, "src"));
+        UVU_TRY(need_idx(src, "src"));
         UVU_TRY(need(d_out, "d_out"));
     }
     DeviceModule* m = nullptr;
@@ -276,9 +284,9 @@ extern "C" uvu_status uvu_conv_bwd_dx_reduce(uvu_plan_t plan, int64_t n_nodes, i
     UVU_TRY(check_sizes(n_nodes, n_edges));
     if (n_nodes == 0) return ok();
     UVU_TRY(need(dx, "dx"));
-    UVU_TRY(need(send_offsets, "send_offsets"));
+    UVU_TRY(need_idx(send_offsets, "send_offsets"));
     if (n_edges > 0) {
-        UVU_TRY(need(send_eids, "send_eids"));
+        UVU_TRY(need_idx(send_eids, "send_eids"));
         UVU_TRY(need(dx_edge, "dx_edge"));
     }
     DeviceModule* m = nullptr;
@@ -311,12 +319,12 @@ extern "C" uvu_status uvu_conv_bwd_dx(uvu_plan_t plan, int64_t n_nodes, int64_t 
     UVU_TRY(check_sizes(n_nodes, n_edges));
     if (n_nodes == 0) return ok();
     UVU_TRY(need(dx, "dx"));
-    UVU_TRY(need(send_offsets, "send_offsets"));
+    UVU_TRY(need_idx(send_offsets, "send_offsets"));
     if (n_edges > 0) {
         UVU_TRY(need(Y, "Y"));
         UVU_TRY(need(w, "w"));
-        UVU_TRY(need(send_eids, "send_eids"));
-        UVU_TRY(need(send_recv, "send_recv"));
+        UVU_TRY(need_idx(send_eids, "send_eids"));
+        UVU_TRY(need_idx(send_recv, "send_recv"));
         UVU_TRY(need(d_out, "d_out"));
     }
     DeviceModule* m = nullptr;

@@ -26,8 +26,11 @@
  * Path order: for each x irrep (string order), each SH irrep (string order), l3 ascending over
  * |l1-l2| .. min(l1+l2, lmax_out); every triangle-allowed l3 is kept, with parity p1*p2.
  *
- * Memory: every tensor pointer is caller-owned DEVICE memory on the current device, 16-byte
- * aligned.  No entry point allocates device memory; the transpose takes a caller workspace.
+ * Memory: every pointer is caller-owned DEVICE memory on the current device; floating-point
+ * tensors are 16-byte aligned, int32 index arrays 4-byte aligned.  Because offsets are absolute
+ * edge indices, a receiver sub-range [r0, r1) of a CSR is itself valid input: pass
+ * recv_offsets + r0 with n_nodes = r1 - r0 and the matching rows of out / d_out (the edge-indexed
+ * tensors keep their base pointers).  No entry point allocates device memory; the transpose takes a caller workspace.
  * Streams: work is enqueued on `stream` (0 = legacy default) and returns before it completes.
  * Outputs are overwritten, never accumulated: receivers without edges get out = 0, senders
  * without edges get dx = 0, n_edges == 0 writes zeros.

@@ -137,3 +137,26 @@ def test_graph_validate():
                            ctypes.c_void_p(bad_src.data_ptr()), ctypes.c_void_p(ws.data_ptr()),
                            ctypes.byref(nbad), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert nbad.value == 2
+
+
+def test_receiver_subranges_match_whole_graph():
+    # offsets are absolute edge indices, so recv_offsets + r0 with n_nodes = r1 - r0 computes the
+    # receivers [r0, r1) exactly as a whole-graph call does (the chunked host pipeline relies on it)
+    P = Problem.from_spec(workloads.custom_spec(160, 333, "64x0e+64x1o+64x2e", SH3, 3, degree=9))
+    i = P.plan.info
+    out_ref = P.fwd()
+    dxe_ref = torch.empty(P.E, i.mul, i.dim_x, device="cuda")
+    dY_ref = torch.empty(P.E, i.dim_sh, device="cuda")
+    dw_ref = torch.empty(P.E, i.n_paths, i.mul, device="cuda")
+    P.plan.bwd_edge(P.N, P.d["x"], P.d["Y"], P.d["w"], P.G.recv_offsets, P.d["src"], P.d["g"],
+                    dY=dY_ref, dw=dw_ref, dx_edge=dxe_ref)
+    out = torch.full_like(out_ref, float("nan"))
+    dxe, dY, dw = (torch.full_like(t, float("nan")) for t in (dxe_ref, dY_ref, dw_ref))
+    for a, b in ((0, 17), (17, 200), (200, 333)):
+        ro = P.G.recv_offsets[a:]
+        P.plan.fwd(b - a, P.d["x"], P.d["Y"], P.d["w"], ro, P.d["src"], out[a:])
+        P.plan.bwd_edge(b - a, P.d["x"], P.d["Y"], P.d["w"], ro, P.d["src"], P.d["g"][a:],
+                        dY=dY, dw=dw, dx_edge=dxe)
+    for got, want in ((out, out_ref), (dxe, dxe_ref), (dY, dY_ref), (dw, dw_ref)):
+        assert torch.equal(got, want)
+    assert P.status_ok()
