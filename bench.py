@@ -44,7 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--dx-mode", default="staged", choices=["staged", "sender", "atomic"])
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--e2e-chunks", type=int, default=8)
+    ap.add_argument("--e2e-chunks", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
