@@ -33,4 +33,4 @@ a dense brute force).  The pages print no worked numerical example of this opera
 golden value comes from them; ``tests/golden/`` holds closed-form values derived by hand.
 """
 
-from . import cg, sh, paths, graph, conv, wigner  # noqa: F401
+from . import cg, sh, paths, graph, conv, wigner, hvp  # noqa: F401
