@@ -123,6 +123,7 @@ extern "C" uvu_status uvu_plan_destroy(uvu_plan_t plan) {
         int cur = 0;
         if (cudaGetDevice(&cur) == cudaSuccess && cur != kv.first) cudaSetDevice(kv.first);
         cudaLibraryUnload(kv.second.lib);
+        if (kv.second.hvp_lib) cudaLibraryUnload(kv.second.hvp_lib);
         if (cur != kv.first) cudaSetDevice(cur);
     }
     delete plan;
@@ -378,5 +379,74 @@ extern "C" uvu_status uvu_plan_device_status(uvu_plan_t plan, unsigned* word, in
         e = cudaMemcpy(m->status_word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
     }
     if (e != cudaSuccess) return cuda_fail(e, "status word copy");
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_hvp_workspace(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, size_t* bytes) {
+    Plan* p = get(plan);
+    if (!p || !bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or bytes is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    *bytes = p->groups.size() == 1 ? size_t(n_edges) * p->U * p->Dx * p->elem() : 0;
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
+                                   const void* Y, const void* w, const int32_t* recv_offsets,
+                                   const int32_t* src, const int32_t* send_offsets, const int32_t* send_eids,
+                                   const void* d_out, const void* ax, const void* aY, const void* aw,
+                                   void* grad_d_out, void* grad_x, void* grad_Y, void* grad_w, void* workspace,
+                                   size_t workspace_bytes, uvu_stream_t stream) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    for (auto& kv : {std::make_pair(ax, "ax"), std::make_pair(aY, "aY"), std::make_pair(aw, "aw"),
+                     std::make_pair(static_cast<const void*>(grad_d_out), "grad_d_out"),
+                     std::make_pair(static_cast<const void*>(grad_x), "grad_x"),
+                     std::make_pair(static_cast<const void*>(grad_Y), "grad_Y"),
+                     std::make_pair(static_cast<const void*>(grad_w), "grad_w")})
+        UVU_TRY(opt(kv.first, kv.second));
+    if (n_nodes == 0 || (!grad_d_out && !grad_x && !grad_Y && !grad_w)) return ok();
+    UVU_TRY(need_idx(recv_offsets, "recv_offsets"));
+    const bool need_edge = grad_x || grad_Y || grad_w;
+    if (n_edges > 0) {
+        UVU_TRY(need(x, "x"));
+        UVU_TRY(need(Y, "Y"));
+        UVU_TRY(need(w, "w"));
+        UVU_TRY(need_idx(src, "src"));
+        if (need_edge) UVU_TRY(need(d_out, "d_out"));
+    }
+    size_t ws_need = 0;
+    UVU_TRY(uvu_conv_hvp_workspace(plan, n_nodes, n_edges, &ws_need));
+    const bool staged = grad_x && ws_need > 0;
+    if (grad_x) {
+        UVU_TRY(need_idx(send_offsets, "send_offsets"));
+        if (n_edges > 0 && staged) UVU_TRY(need_idx(send_eids, "send_eids"));
+        if (staged && (!workspace || workspace_bytes < ws_need))
+            return fail(UVU_ERR_INVALID_ARGUMENT, "grad_x needs a workspace of uvu_conv_hvp_workspace() bytes");
+        UVU_TRY(opt(workspace, "workspace"));
+    }
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = hvp_module_for_current_device(p, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    const int hm = (ax ? 1 : 0) | (aY ? 2 : 0) | (aw ? 4 : 0);
+    long long N = n_nodes;
+    if (grad_d_out) {
+        void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &ax, &aY, &aw, const_cast<int*>(&hm), &grad_d_out};
+        UVU_TRY(launch(m->hvp_fwd, 1, m->sm_count, n_nodes, p->g_hvp_fwd, args, stream, "uvu_hvp_fwd launch"));
+    }
+    if (!need_edge) return ok();
+    void* dx_atomic = (grad_x && !staged) ? grad_x : nullptr;
+    void* dx_edge = staged ? workspace : nullptr;
+    if (dx_atomic) {
+        cudaError_t e = cudaMemsetAsync(dx_atomic, 0, size_t(n_nodes) * p->U * p->Dx * p->elem(), stream);
+        if (e != cudaSuccess) return cuda_fail(e, "grad_x memset");
+    }
+    if (n_edges > 0) {
+        void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &d_out, &ax, &aY, &aw, const_cast<int*>(&hm),
+                        &grad_Y, &grad_w, &dx_atomic, &dx_edge};
+        UVU_TRY(launch(m->hvp_edge, 1, m->sm_count, n_nodes, p->g_hvp_edge, args, stream, "uvu_hvp_edge launch"));
+    }
+    if (staged) UVU_TRY(uvu_conv_bwd_dx_reduce(plan, n_nodes, n_edges, send_offsets, send_eids, workspace, grad_x, stream));
     return ok();
 }

@@ -73,7 +73,12 @@ struct Gen {
 
     // A path whose CG maps each m3 to exactly one (m1, m2) with coefficient +-1 and one operand
     // of width 1: the identity couplings (0, l, l) and (l, 0, l).
+    // Set while emitting the double-backward kernels, whose operands are sums of products and
+    // therefore always take the generic path.
+    mutable bool no_identity = false;
+
     bool is_identity(const PathInfo& p) const {
+        if (no_identity) return false;
         if (p.l1 != 0 && p.l2 != 0) return false;
         std::vector<int> cnt(2 * p.l3 + 1, 0);
         for (const Nz& z : p.nz) {
@@ -148,25 +153,25 @@ struct Gen {
             S(fmt("const %s q_%d_%d = xv_%d * yv_%d;", T.c_str(), ab.first, ab.second, ab.first, ab.second));
     }
 
-    // t_<p>_<m3> = sum_nz c q   (general paths only)
-    void emit_t(Src& S, int pi) const {
+    // <tpre>_<p>_<m3> = sum_nz c <qpre>_<a>_<b>   (general paths only)
+    void emit_t(Src& S, int pi, const char* qpre = "q", const char* tpre = "t") const {
         const PathInfo& p = P->paths[pi];
         for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3) {
             bool first = true;
             for (const Nz& z : p.nz) {
                 if (z.m3 != m3) continue;
-                const std::string q = fmt("q_%d_%d", p.xoff + z.m1, p.yoff + z.m2);
+                const std::string q = fmt("%s_%d_%d", qpre, p.xoff + z.m1, p.yoff + z.m2);
                 if (first) {
                     if (is_one(z.c))
-                        S(fmt("%s t_%d_%d = %s%s;", T.c_str(), pi, m3, z.c < 0 ? "-" : "", q.c_str()));
+                        S(fmt("%s %s_%d_%d = %s%s;", T.c_str(), tpre, pi, m3, z.c < 0 ? "-" : "", q.c_str()));
                     else
-                        S(fmt("%s t_%d_%d = %s * %s;", T.c_str(), pi, m3, lit(z.c).c_str(), q.c_str()));
+                        S(fmt("%s %s_%d_%d = %s * %s;", T.c_str(), tpre, pi, m3, lit(z.c).c_str(), q.c_str()));
                     first = false;
                 } else {
-                    S(fmt("t_%d_%d = fma(%s, %s, t_%d_%d);", pi, m3, lit(z.c).c_str(), q.c_str(), pi, m3));
+                    S(fmt("%s_%d_%d = fma(%s, %s, %s_%d_%d);", tpre, pi, m3, lit(z.c).c_str(), q.c_str(), tpre, pi, m3));
                 }
             }
-            if (first) S(fmt("const %s t_%d_%d = 0;", T.c_str(), pi, m3));
+            if (first) S(fmt("const %s %s_%d_%d = 0;", T.c_str(), tpre, pi, m3));
         }
     }
 
@@ -233,7 +238,8 @@ struct Gen {
     // gval(k) names the d_out value of output index k.
     template <class GV>
     void emit_bwd_pairs(Src& S, const std::vector<int>& paths, bool want_dw, bool want_dy,
-                        bool want_dx, GV gval) const {
+                        bool want_dx, GV gval, const char* xname = "xv", const char* yname = "yv",
+                        const char* wname = "wv") const {
         std::map<std::pair<int, int>, std::vector<int>> pairs;
         for (int pi : paths) pairs[{P->paths[pi].ix, P->paths[pi].iy}].push_back(pi);
         for (auto& kv : pairs) {
@@ -279,7 +285,7 @@ struct Gen {
                 }
                 if (want_dy || want_dx) {
                     for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3)
-                        S(fmt("const %s a_%d_%d = wv_%d * %s;", T.c_str(), pi, m3, pi, gval(p.ooff + m3).c_str()));
+                        S(fmt("const %s a_%d_%d = %s_%d * %s;", T.c_str(), pi, m3, wname, pi, gval(p.ooff + m3).c_str()));
                     for (const Nz& z : p.nz) {
                         const int a = p.xoff + z.m1, b = p.yoff + z.m2;
                         const std::string av = fmt("a_%d_%d", pi, z.m3);
@@ -303,7 +309,7 @@ struct Gen {
                     const int b = p0.yoff + m2;
                     for (int m1 = 0; m1 < d1; ++m1) {
                         const int a = p0.xoff + m1;
-                        if (hdef.count({a, b})) S(fmt("dyp_%d = fma(xv_%d, h_%d_%d, dyp_%d);", b, a, a, b, b));
+                        if (hdef.count({a, b})) S(fmt("dyp_%d = fma(%s_%d, h_%d_%d, dyp_%d);", b, xname, a, a, b, b));
                     }
                 }
             }
@@ -312,7 +318,7 @@ struct Gen {
                     const int a = p0.xoff + m1;
                     for (int m2 = 0; m2 < d2; ++m2) {
                         const int b = p0.yoff + m2;
-                        if (hdef.count({a, b})) S(fmt("dxp_%d = fma(yv_%d, h_%d_%d, dxp_%d);", a, b, a, b, a));
+                        if (hdef.count({a, b})) S(fmt("dxp_%d = fma(%s_%d, h_%d_%d, dxp_%d);", a, yname, b, a, b, a));
                     }
                 }
             }
@@ -428,6 +434,235 @@ struct Gen {
         S.ind--;
         S("}");  // c
         S.ind--;
+        S("}");
+    }
+
+    // ================================================================== double backward (HVP)
+    // With T = <g, F(x, Y, w)> multilinear, the gradients of L2 = <ax,dx> + <aY,dY> + <aw,dw>
+    // are forward / VJP contractions with one argument substituted ("Receiver-streaming
+    // convolutions ...", results table, HVP column; "An Efficient Sparse Kernel Generator ...",
+    // abstract, higher partial derivatives):
+    //   dL2/dg = F(ax,Y,w) + F(x,aY,w) + F(x,Y,aw)          -> uvu_hvp_fwd (receiver-stationary)
+    //   dL2/dw = dw(x<-ax) + dw(Y<-aY)                       -> uvu_hvp_edge
+    //   dL2/dY = dY(x<-ax) + dY(w<-aw)                       -> uvu_hvp_edge
+    //   dL2/dx = dx(Y<-aY) + dx(w<-aw)  per edge, then the sender-stationary reduction
+    // Absent cotangents are marked in the bit mask hm (1 = ax, 2 = aY, 4 = aw) and read as zero.
+
+    // Declares pre_k = 0 for k in `need`, then loads them from `base` when `cond` holds.
+    void emit_row_loads_masked(Src& S, const std::string& pre, const std::string& base, int width,
+                               const std::set<int>& need, const std::string& cond) const {
+        for (int k : need) S(fmt("%s %s_%d = 0;", T.c_str(), pre.c_str(), k));
+        S("if (" + cond + ") {");
+        S.ind++;
+        emit_row_loads(S, pre + "l", base, width, need);
+        for (int k : need) S(fmt("%s_%d = %sl_%d;", pre.c_str(), k, pre.c_str(), k));
+        S.ind--;
+        S("}");
+    }
+
+    // q_a_b = ax_a y_b + x_a ay_b  (the mixed products of the substituted forward terms)
+    void emit_mixed_products(Src& S, const std::vector<int>& paths, const char* name) const {
+        std::set<std::pair<int, int>> q;
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            for (const Nz& z : p.nz) q.insert({p.xoff + z.m1, p.yoff + z.m2});
+        }
+        for (auto& ab : q)
+            S(fmt("const %s %s_%d_%d = fma(axv_%d, yv_%d, xv_%d * ayv_%d);", T.c_str(), name, ab.first, ab.second,
+                  ab.first, ab.second, ab.first, ab.second));
+    }
+
+    void emit_hvp_edge_loads(Src& S, const std::vector<int>& paths) const {
+        const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+        S("const int s = __ldg(src + e);");
+        emit_row_loads(S, "xv", "x + ((size_t)s * UVU_U + u) * UVU_DX", P->Dx, xn);
+        emit_row_loads_masked(S, "axv", "ax + ((size_t)s * UVU_U + u) * UVU_DX", P->Dx, xn, "hm & 1");
+        emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+        emit_row_loads_masked(S, "ayv", "aY + (size_t)e * UVU_DY", P->Dy, yn, "hm & 2");
+        S("const " + T + "* __restrict__ we = w + (size_t)e * (UVU_P * UVU_U) + u;");
+        for (int pi : paths) S(fmt("const %s wv_%d = __ldg(we + %d * UVU_U);", T.c_str(), pi, pi));
+        for (int pi : paths) S(fmt("%s awv_%d = 0;", T.c_str(), pi));
+        S("if (hm & 4) {");
+        S("  const " + T + "* __restrict__ awe = aw + (size_t)e * (UVU_P * UVU_U) + u;");
+        for (int pi : paths) S(fmt("  awv_%d = __ldg(awe + %d * UVU_U);", pi, pi));
+        S("}");
+    }
+
+    void emit_hvp_fwd_group(Src& S, int g) const {
+        const std::vector<int>& paths = P->groups[g];
+        std::vector<int> outs;
+        for (int pi : paths)
+            for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
+        S(fmt("__device__ __forceinline__ void hvp_fwd_group%d(int e0, int e1, int u, int hm, const int* __restrict__ src,", g));
+        S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ ax,",
+              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S(fmt("    const %s* __restrict__ aY, const %s* __restrict__ aw, %s* __restrict__ orow) {", T.c_str(), T.c_str(), T.c_str()));
+        S.ind++;
+        for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
+        S("#pragma unroll 1");
+        S("for (int e = e0; e < e1; ++e) {");
+        S.ind++;
+        emit_hvp_edge_loads(S, paths);
+        emit_mixed_products(S, paths, "qm");
+        emit_products(S, paths);
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            S("{");
+            S.ind++;
+            emit_t(S, pi, "qm", "tm");
+            emit_t(S, pi, "q", "t");
+            for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3)
+                S(fmt("acc_%d = fma(wv_%d, tm_%d_%d, fma(awv_%d, t_%d_%d, acc_%d));", p.ooff + m3, pi, pi, m3, pi, pi, m3,
+                      p.ooff + m3));
+            S.ind--;
+            S("}");
+        }
+        S.ind--;
+        S("}");
+        for (int k : outs) S(fmt("orow[%d] = acc_%d;", k, k));
+        S.ind--;
+        S("}");
+    }
+
+    void emit_hvp_edge_group(Src& S, int g) const {
+        const std::vector<int>& paths = P->groups[g];
+        const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+        std::vector<int> outs;
+        for (int pi : paths)
+            for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
+        S(fmt("__device__ __forceinline__ void hvp_edge_group%d(int rl, int seg, int lane_in_seg, bool valid, int r_e0, int r_e1,", g));
+        S(fmt("    int nchunks, long long r, int u, int hm, const int* __restrict__ src, const %s* __restrict__ x,", T.c_str()));
+        S(fmt("    const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ gout,", T.c_str(), T.c_str(), T.c_str()));
+        S(fmt("    const %s* __restrict__ ax, const %s* __restrict__ aY, const %s* __restrict__ aw,", T.c_str(), T.c_str(), T.c_str()));
+        S(fmt("    %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx, %s* __restrict__ dxe, %s* sred,",
+              T.c_str(), T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S("    const int* s_e0, const int* s_e1) {");
+        S.ind++;
+        S(fmt("const %s* __restrict__ grow = gout + ((size_t)(valid ? r : 0) * UVU_U + u) * UVU_DO;", T.c_str()));
+        for (int k : outs) S(fmt("const %s gv_%d = valid ? __ldg(grow + %d) : (%s)0;", T.c_str(), k, k, T.c_str()));
+        S("#pragma unroll 1");
+        S("for (int c = 0; c < nchunks; ++c) {");
+        S.ind++;
+        S("#pragma unroll 1");
+        S("for (int j = 0; j < UVU_CH; ++j) {");
+        S.ind++;
+        S("const int e = r_e0 + c * UVU_CH + j;");
+        S("const bool active = valid && e < r_e1;");
+        for (int k : yn) S(fmt("%s dyp_%d = 0;", T.c_str(), k));
+        S("if (active) {");
+        S.ind++;
+        emit_hvp_edge_loads(S, paths);
+        S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
+        for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
+        auto gval = [](int k) { return fmt("gv_%d", k); };
+        S("if (dw) {");
+        S.ind++;
+        emit_mixed_products(S, paths, "q");
+        emit_bwd_pairs(S, paths, true, false, false, gval);
+        S.ind--;
+        S("}");
+        emit_bwd_pairs(S, paths, false, true, true, gval, "axv", "ayv", "wv");
+        emit_bwd_pairs(S, paths, false, true, true, gval, "xv", "yv", "awv");
+        S("if (dx) {");
+        S.ind++;
+        S(T + "* __restrict__ dxr = dx + ((size_t)s * UVU_U + u) * UVU_DX;");
+        emit_dx_atomics(S, xn);
+        S.ind--;
+        S("}");
+        if (P->groups.size() == 1) emit_dx_edge_store(S, xn, 1);
+        S.ind--;
+        S("}");  // active
+        S("if (dY) {");
+        S.ind++;
+        for (int k : yn) {
+            S("#pragma unroll");
+            S(fmt("for (int o = UVU_SEGW / 2; o > 0; o >>= 1) dyp_%d += __shfl_xor_sync(0xffffffffu, dyp_%d, o);", k, k));
+        }
+        S("if (lane_in_seg == 0) {");
+        S.ind++;
+        S(T + "* sr = sred + ((size_t)(rl * UVU_SEGS + seg) * UVU_CH + j) * UVU_DY;");
+        for (int k = 0; k < P->Dy; ++k) {
+            if (yn.count(k)) S(fmt("sr[%d] = dyp_%d;", k, k));
+            else S(fmt("sr[%d] = 0;", k));
+        }
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");  // j
+        S("block_sync();");
+        S("if (dY) {");
+        S.ind++;
+        S("for (int it = threadIdx.x; it < UVU_RPB * UVU_CH * UVU_DY; it += UVU_TPB) {");
+        S.ind++;
+        S("const int k = it % UVU_DY, jj = (it / UVU_DY) % UVU_CH, r2 = it / (UVU_DY * UVU_CH);");
+        S("const int e = s_e0[r2] + c * UVU_CH + jj;");
+        S("if (e < s_e1[r2]) {");
+        S.ind++;
+        S(T + " acc = 0;");
+        S("#pragma unroll");
+        S("for (int sg = 0; sg < UVU_SEGS; ++sg) acc += sred[((size_t)(r2 * UVU_SEGS + sg) * UVU_CH + jj) * UVU_DY + k];");
+        S("dY[(size_t)e * UVU_DY + k] = acc;");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+        S("block_sync();");
+        S.ind--;
+        S("}");  // c
+        S.ind--;
+        S("}");
+    }
+
+    void emit_hvp_kernels(Src& S) const {
+        const int NG = int(P->groups.size());
+        no_identity = true;
+        for (int g = 0; g < NG; ++g) emit_hvp_fwd_group(S, g);
+        for (int g = 0; g < NG; ++g) emit_hvp_edge_group(S, g);
+        no_identity = false;
+        const char* t = T.c_str();
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_TPB) uvu_hvp_fwd(long long N, const int* __restrict__ off,"));
+        S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w,", t, t, t));
+        S(fmt("    const %s* __restrict__ ax, const %s* __restrict__ aY, const %s* __restrict__ aw, int hm, %s* __restrict__ out) {", t, t, t, t));
+        S("  const int u = threadIdx.x % UVU_UP;");
+        S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
+        S("  const long long r = (long long)blockIdx.x * UVU_RPB + threadIdx.x / (UVU_UP * UVU_G);");
+        S("  if (r >= N || u >= UVU_U) return;");
+        S("  const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+        S(fmt("  %s* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;", t));
+        for (int g = 0; g < NG; ++g)
+            S(fmt("  %sif (g == %d) hvp_fwd_group%d(e0, e1, u, hm, src, x, Y, w, ax, aY, aw, orow);", g ? "else " : "", g, g));
+        S("}");
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_TPB) uvu_hvp_edge(long long N, const int* __restrict__ off,"));
+        S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w,", t, t, t));
+        S(fmt("    const %s* __restrict__ gout, const %s* __restrict__ ax, const %s* __restrict__ aY, const %s* __restrict__ aw,", t, t, t, t));
+        S(fmt("    int hm, %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx, %s* __restrict__ dxe) {", t, t, t, t));
+        S("  extern __shared__ __align__(16) unsigned char smem_raw[];");
+        S(fmt("  %s* sred = reinterpret_cast<%s*>(smem_raw);", t, t));
+        S("  __shared__ int s_e0[UVU_RPB], s_e1[UVU_RPB], s_nch;");
+        S("  const int u = threadIdx.x % UVU_UP;");
+        S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
+        S("  const int rl = threadIdx.x / (UVU_UP * UVU_G);");
+        S("  const long long r = (long long)blockIdx.x * UVU_RPB + rl;");
+        S("  const bool rvalid = r < N;");
+        S("  const bool valid = rvalid && u < UVU_U;");
+        S("  if (threadIdx.x == 0) s_nch = 0;");
+        S("  __syncthreads();");
+        S("  if (threadIdx.x % (UVU_UP * UVU_G) == 0) {");
+        S("    const int a = rvalid ? __ldg(off + r) : 0, b = rvalid ? __ldg(off + r + 1) : 0;");
+        S("    s_e0[rl] = a; s_e1[rl] = b;");
+        S("    atomicMax(&s_nch, (b - a + UVU_CH - 1) / UVU_CH);");
+        S("  }");
+        S("  __syncthreads();");
+        S("  const int nchunks = s_nch;");
+        S("  const int seg = g * ((UVU_UP + 31) / 32) + u / 32;");
+        S("  const int lane_in_seg = u % UVU_SEGW;");
+        for (int g = 0; g < NG; ++g)
+            S(fmt("  %sif (g == %d) hvp_edge_group%d(rl, seg, lane_in_seg, valid, s_e0[rl], s_e1[rl], nchunks, r, u, hm, src, x, Y, w, gout, ax, aY, aw, dY, dw, dx, dxe, sred, s_e0, s_e1);",
+                  g ? "else " : "", g, g));
         S("}");
     }
 
@@ -1376,6 +1611,47 @@ std::string emit_source(Plan* plan) {
         G.emit_dx_kernel(S);
     G.emit_dx_reduce(S);
     plan->staged_ok = pipe_recv || NG == 1;
+    return S.o.str();
+}
+
+}  // namespace uvu
+
+namespace uvu {
+
+// Source of the plan's second module: the double-backward (HVP) kernels, compiled on the first
+// HVP call so that plans used only for the forward and the VJP do not pay for them.  They use
+// the direct-load structure and the plan's register groups.
+std::string emit_hvp_source(Plan* plan) {
+    Gen G{plan, plan->dtype == UVU_F64, plan->dtype == UVU_F64 ? "double" : "float"};
+    const int U = plan->U, NG = int(plan->groups.size()), UP = plan->U_pad;
+    const int owner_threads = UP * NG;
+    const int rpb = std::max(1, 128 / owner_threads);
+    const int segw = std::min(UP, 32);
+    const int segs = NG * ((UP + 31) / 32);
+    const int ch = 16;
+    plan->g_hvp_fwd = {rpb * owner_threads, rpb, 0, false};
+    plan->g_hvp_edge = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem(), false};
+    Src S;
+    S("// Generated by the UVU planner: double backward (HVP) of the channel-wise CG convolution.");
+    S(fmt("// irreps_x=%s irreps_sh=%s lmax_out=%d dtype=%s", plan->irreps_x.c_str(), plan->irreps_sh.c_str(),
+          plan->lmax_out, G.f64 ? "fp64" : "fp32"));
+    S(fmt("#define UVU_U %d", U));
+    S(fmt("#define UVU_UP %d", UP));
+    S(fmt("#define UVU_P %d", plan->P));
+    S(fmt("#define UVU_DX %d", plan->Dx));
+    S(fmt("#define UVU_DY %d", plan->Dy));
+    S(fmt("#define UVU_DO %d", plan->Do));
+    S(fmt("#define UVU_G %d", NG));
+    S(fmt("#define UVU_RPB %d", rpb));
+    S(fmt("#define UVU_TPB %d", rpb * owner_threads));
+    S(fmt("#define UVU_SEGW %d", segw));
+    S(fmt("#define UVU_SEGS %d", segs));
+    S(fmt("#define UVU_CH %d", ch));
+    S("__device__ __forceinline__ void block_sync() { asm volatile(\"barrier.sync 0;\" ::: \"memory\"); }");
+    S("__device__ __forceinline__ void red_add_v4(float* a, float p, float q, float r, float s) {");
+    S("  asm volatile(\"red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\" :: \"l\"(a), \"f\"(p), \"f\"(q), \"f\"(r), \"f\"(s) : \"memory\");");
+    S("}");
+    G.emit_hvp_kernels(S);
     return S.o.str();
 }
 

@@ -199,4 +199,37 @@ uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string
     return UVU_OK;
 }
 
+// The double-backward module: emitted and compiled on the first HVP call of the plan (host),
+// then loaded once per device.
+uvu_status hvp_module_for_current_device(Plan* plan, DeviceModule** out, std::string* err) {
+    DeviceModule* m = nullptr;
+    uvu_status s = module_for_current_device(plan, &m, err);
+    if (s != UVU_OK) return s;
+    std::lock_guard<std::mutex> g(plan->mu);
+    if (plan->hvp_cubin.empty()) {
+        plan->hvp_source = emit_hvp_source(plan);
+        CacheEntry e;
+        s = nvrtc_compile(plan->hvp_source, &e, err);
+        if (s != UVU_OK) return s;
+        plan->hvp_cubin = std::move(e.cubin);
+        plan->hvp_log = std::move(e.log);
+    }
+    if (!m->hvp_lib) {
+        cudaError_t ce = cudaLibraryLoadData(&m->hvp_lib, plan->hvp_cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0);
+        if (ce == cudaSuccess) ce = cudaLibraryGetKernel(&m->hvp_fwd, m->hvp_lib, "uvu_hvp_fwd");
+        if (ce == cudaSuccess) ce = cudaLibraryGetKernel(&m->hvp_edge, m->hvp_lib, "uvu_hvp_edge");
+        if (ce == cudaSuccess && plan->g_hvp_edge.smem > 48 * 1024)
+            ce = cudaFuncSetAttribute(reinterpret_cast<const void*>(m->hvp_edge),
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(plan->g_hvp_edge.smem));
+        if (ce != cudaSuccess) {
+            *err = std::string("loading the HVP module: ") + cudaGetErrorString(ce);
+            if (m->hvp_lib) cudaLibraryUnload(m->hvp_lib);
+            m->hvp_lib = nullptr;
+            return UVU_ERR_CUDA;
+        }
+    }
+    *out = m;
+    return UVU_OK;
+}
+
 }  // namespace uvu

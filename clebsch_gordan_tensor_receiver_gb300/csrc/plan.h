@@ -46,6 +46,8 @@ struct KernelGeom {
 struct DeviceModule {
     cudaLibrary_t lib = nullptr;
     cudaKernel_t fwd = nullptr, bwd_edge = nullptr, bwd_dx = nullptr, bwd_dx_reduce = nullptr;
+    cudaLibrary_t hvp_lib = nullptr;  // second module (double backward), loaded on first use
+    cudaKernel_t hvp_fwd = nullptr, hvp_edge = nullptr;
     int sm_count = 0;
     int occ_fwd = 1, occ_edge = 1, occ_dx = 1;  // resident blocks per SM
     unsigned* status_word = nullptr;            // device address of uvu_status_word
@@ -60,7 +62,7 @@ struct Plan {
     std::vector<Irrep> xs, ys;
     std::vector<PathInfo> paths;
     std::vector<std::vector<int>> groups;  // path ids per register group
-    KernelGeom g_fwd, g_edge, g_dx;
+    KernelGeom g_fwd, g_edge, g_dx, g_hvp_fwd, g_hvp_edge;
     int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
     bool pipelined_recv = false, pipelined_dx = false;
     bool staged_ok = false;
@@ -71,6 +73,8 @@ struct Plan {
     int minb_eff[3] = {1, 1, 1};  // value used by the last emission
     std::string source, log;
     std::vector<char> cubin;
+    std::string hvp_source, hvp_log;  // double-backward module, compiled on the first HVP call
+    std::vector<char> hvp_cubin;
     std::mutex mu;
     std::map<int, DeviceModule> modules;  // per device ordinal
     size_t elem() const { return dtype == UVU_F64 ? 8 : 4; }
@@ -85,12 +89,14 @@ uvu_status build_paths(Plan* plan, std::string* err);
 
 // codegen.cpp
 std::string emit_source(Plan* plan);
+std::string emit_hvp_source(Plan* plan);
 void balance_groups(Plan* plan, int ng);
 
 // jit.cpp
 uvu_status compile_plan(Plan* plan, std::string* err);
 size_t spill_bytes(const std::string& log, const char* kernel);
 uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string* err);
+uvu_status hvp_module_for_current_device(Plan* plan, DeviceModule** out, std::string* err);
 
 // status.cpp
 uvu_status fail(uvu_status s, const std::string& msg);

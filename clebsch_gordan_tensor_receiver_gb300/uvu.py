@@ -30,7 +30,7 @@ EXPORTS = (
     "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
     "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
     "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
-    "uvu_status_string", "uvu_last_error_message",
+    "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_status_string", "uvu_last_error_message",
 )
 
 
@@ -63,6 +63,8 @@ def _load():
         "uvu_conv_bwd_dx_reduce": [P, I64, I64, P, P, P, P, P],
         "uvu_conv_bwd_workspace": [P, I64, I64, I, ctypes.POINTER(SZ)],
         "uvu_conv_bwd": [P, I64, I64, P, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P],
+        "uvu_conv_hvp": [P, I64, I64] + [P] * 16 + [SZ, P],
+        "uvu_conv_hvp_workspace": [P, I64, I64, ctypes.POINTER(SZ)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -98,7 +100,8 @@ for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source"
            "uvu_plan_device_status",
            "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
            "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
-           "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd"):
+           "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
+           "uvu_conv_hvp", "uvu_conv_hvp_workspace"):
     globals()[_n] = _wrap(_n)
 
 
@@ -219,6 +222,29 @@ class Plan:
                      _ptr(recv_offsets), _ptr(src), _ptr(send_offsets), _ptr(send_eids),
                      _ptr(send_recv), _ptr(d_out), _ptr(dx), _ptr(dY), _ptr(dw), dx_mode,
                      ws_ptr, ws_bytes, _stream(stream))
+
+
+def _hvp_method(self, n_nodes, x, Y, w, recv_offsets, src, send_offsets, send_eids, d_out,
+                ax=None, aY=None, aw=None, grad_d_out=None, grad_x=None, grad_Y=None, grad_w=None,
+                workspace=None, stream=None):
+    """Double backward: gradients of <ax,dx> + <aY,dY> + <aw,dw> (see uvu_conv_hvp)."""
+    n_edges = src.numel()
+    ws_ptr, ws_bytes = None, 0
+    if grad_x is not None:
+        b = ctypes.c_size_t()
+        uvu_conv_hvp_workspace(self.handle, n_nodes, n_edges, ctypes.byref(b))
+        if b.value:
+            if workspace is None:
+                import torch
+                workspace = torch.empty(b.value, dtype=torch.uint8, device=src.device)
+            ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    uvu_conv_hvp(self.handle, n_nodes, n_edges, _ptr(x), _ptr(Y), _ptr(w), _ptr(recv_offsets),
+                 _ptr(src), _ptr(send_offsets), _ptr(send_eids), _ptr(d_out), _ptr(ax), _ptr(aY),
+                 _ptr(aw), _ptr(grad_d_out), _ptr(grad_x), _ptr(grad_Y), _ptr(grad_w), ws_ptr,
+                 ws_bytes, _stream(stream))
+
+
+Plan.hvp = _hvp_method
 
 
 class Graph:

@@ -225,6 +225,35 @@ uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const
                         void *dx, void *dY, void *dw, uvu_dx_mode dx_mode, void *workspace,
                         size_t workspace_bytes, uvu_stream_t stream);
 
+/* Double backward (Hessian-vector product) of the convolution, for force training
+ * ("Receiver-streaming convolutions ...", results table: HVP column; "An Efficient Sparse Kernel
+ * Generator ...", abstract: higher partial derivatives for interatomic forces).  Given the
+ * cotangents ax [N][U][D_x], aY [E][D_Y], aw [E][P][U] of the VJP outputs (dx, dY, dw) for the
+ * cotangent d_out, it returns the gradients of
+ *     L2 = <ax, dx> + <aY, dY> + <aw, dw>
+ * with respect to d_out, x, Y and w.  Because the output is linear in each of x, Y, w, these
+ * are forward and VJP contractions with one argument substituted:
+ *     grad_d_out = F(ax,Y,w) + F(x,aY,w) + F(x,Y,aw)      [N][U][D_out]
+ *     grad_x     = dx(Y<-aY) + dx(w<-aw)                  [N][U][D_x]
+ *     grad_Y     = dY(x<-ax) + dY(w<-aw)                  [E][D_Y]
+ *     grad_w     = dw(x<-ax) + dw(Y<-aY)                  [E][P][U]
+ * A NULL cotangent counts as zero; a NULL output is not computed.  grad_x is formed from
+ * per-edge contributions summed per sender over the transposed CSR (deterministic) when
+ * uvu_conv_hvp_workspace() reports a non-zero size, which needs that much caller workspace;
+ * otherwise (plans with several register groups) by atomic adds into a zeroed grad_x.
+ * The plan's HVP kernels are compiled on its first HVP call (host, NVRTC) and loaded once per
+ * device.  Launches: uvu_hvp_fwd (if grad_d_out), uvu_hvp_edge (if grad_x, grad_Y or grad_w),
+ * and the sender-stationary reduction for grad_x. */
+uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
+                        const void *Y, const void *w, const int32_t *recv_offsets,
+                        const int32_t *src, const int32_t *send_offsets, const int32_t *send_eids,
+                        const void *d_out, const void *ax, const void *aY, const void *aw,
+                        void *grad_d_out, void *grad_x, void *grad_Y, void *grad_w,
+                        void *workspace, size_t workspace_bytes, uvu_stream_t stream);
+
+/* Bytes of device workspace uvu_conv_hvp needs for grad_x (0 when it uses atomic adds). */
+uvu_status uvu_conv_hvp_workspace(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, size_t *bytes);
+
 /* ---------------------------------------------------------------------------- errors ---- */
 
 const char *uvu_status_string(uvu_status s);
