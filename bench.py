@@ -47,6 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-chunks", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-hvp", action="store_true", help="skip the double-backward measurement")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
     ap.add_argument("--single-mode", action="store_true",
                     help="warm up and time only --dx-mode (profiling runs)")
@@ -403,6 +404,48 @@ def main(argv=None):
         "clocks": clk,
         "gpu_launches": args.steps * (2 if args.dx_mode == "atomic" else 3),
     }
+
+    # double backward (HVP): gradients of <ax,dx> + <aY,dY> + <aw,dw>, timed on the same workload
+    if not args.no_hvp and world == 1:
+        gen = torch.Generator(device=dev).manual_seed(2026)
+        ax = torch.randn(x.shape, generator=gen, device=dev, dtype=tdt)
+        aY = torch.randn(Y.shape, generator=gen, device=dev, dtype=tdt)
+        aw = torch.randn(w.shape, generator=gen, device=dev, dtype=tdt)
+        hg, hx = torch.empty_like(out), torch.empty_like(dx)
+        hY, hw = torch.empty_like(dY), torch.empty_like(dw)
+        hws = torch.empty(max(1, plan.workspace_bytes(N, E, uvu.UVU_DX_STAGED)), dtype=torch.uint8, device=dev)
+
+        def hvp_call(**outs):
+            plan.hvp(N, x, Y, w, G.recv_offsets, src, G.send_offsets, G.send_eids, g, ax=ax, aY=aY,
+                     aw=aw, workspace=hws, stream=stream, **outs)
+
+        def ev_time(fn, reps):
+            for _ in range(2):
+                fn()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+        reps = max(3, args.steps // 2)
+        t_all = ev_time(lambda: hvp_call(grad_d_out=hg, grad_x=hx, grad_Y=hY, grad_w=hw), reps)
+        t_fwd = ev_time(lambda: hvp_call(grad_d_out=hg), reps)
+        t_edge = ev_time(lambda: hvp_call(grad_Y=hY, grad_w=hw), reps)
+        xb, Yb, wb, ob = N * U * Dx * s, E * Dy * s, E * P * U * s, N * U * Do * s
+        hvp_bytes = (2 * xb + 2 * Yb + 2 * wb + ob + 4 * (N + 1) * 2 + 8 * E) + (ob + xb + Yb + wb)
+        gbs, fr = frac(hvp_bytes, t_all)
+        line["hvp"] = {"ms": t_all, "edges_per_s": E / (t_all / 1000), "GB_s": gbs, "hbm_frac": fr,
+                       "bytes": hvp_bytes, "kernels_ms": {"uvu_hvp_fwd": t_fwd, "uvu_hvp_edge": t_edge,
+                                                          "uvu_bwd_dx_reduce": max(0.0, t_all - t_fwd - t_edge)},
+                       "note": "gradients of <ax,dx>+<aY,dY>+<aw,dw> w.r.t. d_out, x, Y, w; compulsory "
+                               "bytes: reads x,ax,Y,aY,w,aw,d_out,CSRs; writes the four gradients"}
+        assert plan.device_status() == 0
+        del ax, aY, aw, hg, hx, hY, hw, hws
 
     # end-to-end through the C ABI from pinned host buffers: every step copies its inputs (x, Y,
     # w, d_out and the graph arrays) in and its results (out, dx, dY, dw) out.  The receivers are

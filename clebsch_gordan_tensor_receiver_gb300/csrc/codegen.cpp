@@ -780,26 +780,35 @@ __device__ __forceinline__ void bulk_g2s(unsigned dst, const void* src, unsigned
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+// Asks the memory system to bring [src, src + bytes) into L2 ahead of its use (no completion
+// to wait for; the later bulk copy to shared memory then hits in L2).
+__device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
 // Barrier among the consumer warps only (the producer warp never takes part).
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" :: "r"(UVU_NCT) : "memory"); })");
+__device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, %0;" :: "r"(UVU_NCT) : "memory"); })");
     }
 
     // Stage layout of the receiver-ordered kernels (forward and edge backward).
     struct RecvPipe {
         int ch = 1, nst = 2;
+        int pf = 0;  // L2 prefetch distance in chunks (0 = none; prefetching measured slower)
         bool xbulk = false, ybulk = false;
-        size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, xpart_off = 0, total = 0;
+        int odp = 0;  // row stride (elements) of the staged output block, 0 = not staged
+        bool ovec = false;  // staged block copied out with 16-byte vectors
+        size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, xpart_off = 0, out_off = 0, total = 0;
         size_t tx_per_edge = 0;
     };
     static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
 
-    RecvPipe recv_pipe(bool with_partials, int ncw) const {
+    RecvPipe recv_pipe(bool with_partials, int ncw, bool stage_out = false, int ch = 0) const {
         RecvPipe R;
         R.xbulk = xbytes() % 16 == 0;
         R.ybulk = ybytes() % 16 == 0;
         const int NG = int(P->groups.size());
         const size_t pe = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
-        R.ch = int(std::max<size_t>(1, std::min<size_t>(8, 32768 / pe)));
+        const bool chosen = ch > 0 || std::getenv("UVU_PIPE_CH");
+        R.ch = ch > 0 ? ch : int(std::max<size_t>(1, std::min<size_t>(8, 32768 / pe)));
         if (const char* e = std::getenv("UVU_PIPE_CH")) R.ch = std::max(1, std::atoi(e));
         const size_t stage = a16(R.ch * wbytes()) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
                              (R.ybulk ? a16(R.ch * ybytes()) : 0);
@@ -810,6 +819,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         // enough bytes in flight, and the smaller footprint lets more blocks (warps) reside.
         R.nst = 2;
         if (const char* e = std::getenv("UVU_PIPE_NST")) R.nst = std::max(2, std::atoi(e));
+        if (const char* e = std::getenv("UVU_PIPE_PF")) R.pf = std::max(0, std::atoi(e));
         R.w_off = 0;
         R.x_off = a16(R.ch * wbytes());
         R.y_off = R.x_off + (R.xbulk ? a16(R.ch * xbytes()) : 0);
@@ -817,8 +827,21 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         R.bar_off = R.nst * stage;
         R.part_off = R.bar_off + 16 * R.nst;
         R.xpart_off = R.part_off + dyp;
-        R.total = R.xpart_off + dxp;
+        R.out_off = R.xpart_off + dxp;
+        // The receiver's output block out[r] (U x D_out, contiguous in global memory) is staged in
+        // shared memory so that it leaves the block as coalesced row writes instead of one
+        // D_out-strided store per thread and output component.  Rows are padded to an odd stride
+        // so that the per-thread row writes fall in distinct banks.
+        if (stage_out) {
+            R.odp = P->Do % 2 ? P->Do : P->Do + 1;
+            R.ovec = R.odp == P->Do && (size_t(P->U) * P->Do * P->elem()) % 16 == 0;
+        }
+        R.total = R.out_off + (stage_out ? a16(size_t(P->U) * R.odp * P->elem()) : 0);
         R.tx_per_edge = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
+        // With the output block staged, shorter stages keep three blocks resident per SM where
+        // the default chunk would leave fewer (more warps beat a longer look-ahead per block).
+        if (stage_out && !chosen && R.ch > 1 && minb(R.total) < 3)
+            return recv_pipe(with_partials, ncw, stage_out, R.ch - 1);
         return R;
     }
 
@@ -832,6 +855,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S(fmt("#define %s_PART %zu", pre, R.part_off));
         S(fmt("#define %s_XPART %zu", pre, R.xpart_off));
         S(fmt("#define %s_TX %zu", pre, R.tx_per_edge));
+        S(fmt("#define %s_OBUF %zu", pre, R.out_off));
+        S(fmt("#define %s_ODP %d", pre, R.odp));
         const int mb = std::min(minb(R.total), pre[0] == 'F' ? P->minb[0] : P->minb[1]);
         P->minb_eff[pre[0] == 'F' ? 0 : 1] = mb;
         S(fmt("#define %s_MINB %d", pre, mb));
@@ -846,36 +871,65 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
 
     // Producer for the receiver-ordered kernels: w block of the chunk (one copy, the receiver's
     // edges are contiguous), Y block (one copy), x row of each edge's sender (one copy each).
+    // The sender ids of the next chunk and the offsets of the next receiver are loaded one step
+    // ahead, before the current chunk's copies are issued: the copies are asm statements with a
+    // memory clobber, so a load placed after one of them would wait its full latency in line.
     void emit_recv_producer(Src& S, const RecvPipe& R, const char* pre, const char* name) const {
+        const int CH = R.ch;
         S(fmt("__device__ __noinline__ void %s(long long N, const int* __restrict__ off, const int* __restrict__ src,", name));
         S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, unsigned sbase) {",
               T.c_str(), T.c_str(), T.c_str()));
         S.ind++;
         S("unsigned c = 0;");
         S("bool dead = false;");
-        S("for (long long r = blockIdx.x; r < N && !dead; r += gridDim.x) {");
+        S("const long long G = gridDim.x;");
+        S("long long r = blockIdx.x;");
+        S("int eb = 0, e1 = 0, nb = 0, n1 = 0;");
+        S("if (r < N) { eb = __ldg(off + r); e1 = __ldg(off + r + 1); }");
+        S("if (r + G < N) { nb = __ldg(off + r + G); n1 = __ldg(off + r + G + 1); }");
+        for (int j = 0; j < CH; ++j) S(fmt("int sv%d = (%d < e1 - eb) ? __ldg(src + eb + %d) : 0;", j, j, j));
+        S("while (r < N && !dead) {");
         S.ind++;
-        S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
-        S(fmt("for (int eb = e0; eb < e1; eb += %s_CH, ++c) {", pre));
+        S("if (eb >= e1) {  // receiver done (or empty): move to the next one");
         S.ind++;
+        S("r += G;");
+        S("if (r >= N) break;");
+        S("eb = nb; e1 = n1;");
+        S("if (r + G < N) { nb = __ldg(off + r + G); n1 = __ldg(off + r + G + 1); }");
+        for (int j = 0; j < CH; ++j) S(fmt("sv%d = (%d < e1 - eb) ? __ldg(src + eb + %d) : 0;", j, j, j));
+        S("continue;");
+        S.ind--;
+        S("}");
+        S(fmt("const int ne = min(%s_CH, e1 - eb);", pre));
+        S(fmt("const int ebn = eb + %s_CH;", pre));
+        for (int j = 0; j < CH; ++j) S(fmt("const int svn%d = (ebn + %d < e1) ? __ldg(src + ebn + %d) : 0;", j, j, j));
+        if (R.pf > 0) {
+            // L2 prefetch of the w (and Y) rows R.pf chunks ahead, in this receiver or the next
+            S(fmt("{ int pa = eb + %d, pb; bool ok = true;", R.pf * CH));
+            S(fmt("  if (pa < e1) { pb = min(pa + %s_CH, e1); }", pre));
+            S(fmt("  else if (r + G < N) { pa = nb + (pa - e1); pb = min(pa + %s_CH, n1); ok = pa < n1; }", pre));
+            S("  else { ok = false; pb = pa; }");
+            S(fmt("  if (ok) { prefetch_l2(w + (size_t)pa * (UVU_P * UVU_U), (unsigned)(pb - pa) * %zuu);", wbytes()));
+            if (R.ybulk) S(fmt("             prefetch_l2(Y + (size_t)pa * UVU_DY, (unsigned)(pb - pa) * %zuu); }", ybytes()));
+            else S("  }");
+            S("}");
+        }
         S(fmt("const unsigned st = c %% %s_NST;", pre));
         S(fmt("if (c >= %s_NST && !mbar_wait(sbase + %s_BAR + 8u * (%s_NST + st), ((c / %s_NST) - 1u) & 1u)) { dead = true; break; }",
               pre, pre, pre, pre));
-        S(fmt("const int ne = min(%s_CH, e1 - eb);", pre));
         S(fmt("const unsigned full = sbase + %s_BAR + 8u * st;", pre));
         S(fmt("const unsigned stg = sbase + st * %s_STAGE;", pre));
         S(fmt("mbar_expect_tx(full, (unsigned)ne * %s_TX);", pre));
         S(fmt("bulk_g2s(stg, w + (size_t)eb * (UVU_P * UVU_U), (unsigned)ne * %zuu, full);", wbytes()));
         if (R.ybulk) S(fmt("bulk_g2s(stg + %s_YOFF, Y + (size_t)eb * UVU_DY, (unsigned)ne * %zuu, full);", pre, ybytes()));
         if (R.xbulk) {
-            S("for (int j = 0; j < ne; ++j) {");
-            S("  const int s = __ldg(src + eb + j);");
-            S(fmt("  bulk_g2s(stg + %s_XOFF + (unsigned)j * %zuu, x + (size_t)s * (UVU_U * UVU_DX), %zuu, full);", pre,
-                  xbytes(), xbytes()));
-            S("}");
+            for (int j = 0; j < CH; ++j)
+                S(fmt("if (%d < ne) bulk_g2s(stg + %s_XOFF + %zuu, x + (size_t)sv%d * (UVU_U * UVU_DX), %zuu, full);", j, pre,
+                      size_t(j) * xbytes(), j, xbytes()));
         }
-        S.ind--;
-        S("}");
+        for (int j = 0; j < CH; ++j) S(fmt("sv%d = svn%d;", j, j));
+        S("eb = ebn;");
+        S("++c;");
         S.ind--;
         S("}");
         S("if (dead) {  // let the copies already issued land before the block exits");
@@ -971,12 +1025,45 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S("const bool uvalid = u < UVU_U;");
         S("unsigned c = 0;");
         S("bool dead = false;");
+        if (R.odp == 0) {
+            S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
+            S.ind++;
+            S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+            S(T + "* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
+            for (int g = 0; g < NG; ++g)
+                S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, Y, orow);", g ? "else " : "", g, g));
+            S.ind--;
+            S("}");
+            S.ind--;
+            S("}");
+            return;
+        }
+        S(fmt("%s* const sout = reinterpret_cast<%s*>(smem + FW_OBUF);", T.c_str(), T.c_str()));
+        S(fmt("%s* const orow = sout + u * FW_ODP;", T.c_str()));
+        if (R.ovec) S("const bool ovec = (reinterpret_cast<size_t>(out) & 15) == 0;");
         S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
         S.ind++;
         S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
-        S(T + "* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
+        S("consumer_sync();  // the previous receiver's block has been copied out of sout");
         for (int g = 0; g < NG; ++g)
             S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, Y, orow);", g ? "else " : "", g, g));
+        S("consumer_sync();");
+        S(fmt("%s* const og = out + (size_t)r * (UVU_U * UVU_DO);", T.c_str()));
+        if (R.ovec) {
+            const int nv = int(size_t(P->U) * P->Do * P->elem() / 16);
+            S("if (ovec) {");
+            S(fmt("  for (int i = tid; i < %d; i += UVU_NCT) reinterpret_cast<float4*>(og)[i] = reinterpret_cast<const float4*>(sout)[i];", nv));
+            S("} else {");
+            S("  for (int i = tid; i < UVU_U * UVU_DO; i += UVU_NCT) og[i] = sout[i];");
+            S("}");
+        } else if (R.odp == P->Do) {
+            S("for (int i = tid; i < UVU_U * UVU_DO; i += UVU_NCT) og[i] = sout[i];");
+        } else {
+            S("for (int i = tid; i < UVU_U * UVU_DO; i += UVU_NCT) {");
+            S("  const int uu = i / UVU_DO;");
+            S("  og[i] = sout[uu * FW_ODP + (i - uu * UVU_DO)];");
+            S("}");
+        }
         S.ind--;
         S("}");
         S.ind--;
@@ -1335,33 +1422,45 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;"
         S.ind++;
         S("unsigned c = 0;");
         S("bool dead = false;");
+        // The edge ids and receivers of the next chunk are loaded before the current chunk's
+        // copies are issued (the copies are asm statements with a memory clobber).
         S("for (long long it = blockIdx.x; it < N * DX_NT && !dead; it += gridDim.x) {");
         S.ind++;
         S("const long long sn = it / DX_NT;");
         S("const int u0 = (int)(it - sn * DX_NT) * DX_UT;");
         S("const int k0 = __ldg(soff + sn), k1 = __ldg(soff + sn + 1);");
+        for (int j = 0; j < D.ch; ++j)
+            S(fmt("int ev%d = 0, rv%d = 0; if (k0 + %d < k1) { ev%d = __ldg(seid + k0 + %d); rv%d = __ldg(srecv + k0 + %d); }", j, j,
+                  j, j, j, j, j));
         S("for (int kb = k0; kb < k1; kb += DX_CH, ++c) {");
         S.ind++;
+        S("const int kn = kb + DX_CH;");
+        for (int j = 0; j < D.ch; ++j)
+            S(fmt("int evn%d = 0, rvn%d = 0; if (kn + %d < k1) { evn%d = __ldg(seid + kn + %d); rvn%d = __ldg(srecv + kn + %d); }", j,
+                  j, j, j, j, j, j));
         S("const unsigned st = c % DX_NST;");
         S("if (c >= DX_NST && !mbar_wait(sbase + DX_BAR + 8u * (DX_NST + st), ((c / DX_NST) - 1u) & 1u)) { dead = true; break; }");
         S("const int ne = min(DX_CH, k1 - kb);");
         S("const unsigned full = sbase + DX_BAR + 8u * st;");
         S("const unsigned stg = sbase + st * DX_STAGE;");
         S("mbar_expect_tx(full, (unsigned)ne * DX_TX);");
-        S("for (int j = 0; j < ne; ++j) {");
-        S.ind++;
-        S("const int e = __ldg(seid + kb + j), r = __ldg(srecv + kb + j);");
-        if (D.ut == P->U) {
-            S(fmt("bulk_g2s(stg + (unsigned)j * %zuu, w + (size_t)e * (UVU_P * UVU_U), %zuu, full);", D.wt, D.wt));
-        } else {
-            S("#pragma unroll 1");
-            S(fmt("for (int p = 0; p < UVU_P; ++p) bulk_g2s(stg + (unsigned)j * %zuu + (unsigned)p * %zuu, w + ((size_t)e * UVU_P + p) * UVU_U + u0, %zuu, full);",
-                  D.wt, size_t(D.ut) * P->elem(), size_t(D.ut) * P->elem()));
+        for (int j = 0; j < D.ch; ++j) {
+            S(fmt("if (%d < ne) {", j));
+            S.ind++;
+            S(fmt("const int e = ev%d, r = rv%d;", j, j));
+            if (D.ut == P->U) {
+                S(fmt("bulk_g2s(stg + %zuu, w + (size_t)e * (UVU_P * UVU_U), %zuu, full);", size_t(j) * D.wt, D.wt));
+            } else {
+                S("#pragma unroll 1");
+                S(fmt("for (int p = 0; p < UVU_P; ++p) bulk_g2s(stg + %zuu + (unsigned)p * %zuu, w + ((size_t)e * UVU_P + p) * UVU_U + u0, %zuu, full);",
+                      size_t(j) * D.wt, size_t(D.ut) * P->elem(), size_t(D.ut) * P->elem()));
+            }
+            S(fmt("bulk_g2s(stg + DX_GOFF + %zuu, gout + ((size_t)r * UVU_U + u0) * UVU_DO, %zuu, full);", size_t(j) * D.gt, D.gt));
+            if (D.ybulk) S(fmt("bulk_g2s(stg + DX_YOFF + %zuu, Y + (size_t)e * UVU_DY, %zuu, full);", size_t(j) * ybytes(), ybytes()));
+            S.ind--;
+            S("}");
         }
-        S(fmt("bulk_g2s(stg + DX_GOFF + (unsigned)j * %zuu, gout + ((size_t)r * UVU_U + u0) * UVU_DO, %zuu, full);", D.gt, D.gt));
-        if (D.ybulk) S(fmt("bulk_g2s(stg + DX_YOFF + (unsigned)j * %zuu, Y + (size_t)e * UVU_DY, %zuu, full);", ybytes(), ybytes()));
-        S.ind--;
-        S("}");
+        for (int j = 0; j < D.ch; ++j) S(fmt("ev%d = evn%d; rv%d = rvn%d;", j, j, j, j));
         S.ind--;
         S("}");
         S.ind--;
@@ -1503,7 +1602,9 @@ std::string emit_source(Plan* plan) {
             return emit_source(plan);  // once more, with the new grouping
         }
     }
-    Gen::RecvPipe RF = G.recv_pipe(false, ncw), RE = G.recv_pipe(true, ncw);
+    // UVU_PIPE_OSTAGE=0 (a tuning switch) writes the forward output straight from registers.
+    const bool ostage = !(std::getenv("UVU_PIPE_OSTAGE") && std::atoi(std::getenv("UVU_PIPE_OSTAGE")) == 0);
+    Gen::RecvPipe RF = G.recv_pipe(false, ncw, ostage), RE = G.recv_pipe(true, ncw);
     Gen::SendPipe SD = G.send_pipe();
     const bool pipe_dx = !force_direct && U >= 32 && G.send_pipe_ok(SD);
     plan->pipelined_recv = pipe_recv;
