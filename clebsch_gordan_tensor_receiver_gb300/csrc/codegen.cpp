@@ -796,12 +796,14 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         bool xbulk = false, ybulk = false;
         int odp = 0;  // row stride (elements) of the staged output block, 0 = not staged
         bool ovec = false;  // staged block copied out with 16-byte vectors
+        bool gst = false;  // the receiver's d_out block is bulk-copied into shared memory
         size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, xpart_off = 0, out_off = 0, total = 0;
+        size_t g_off = 0, gbytes = 0;
         size_t tx_per_edge = 0;
     };
     static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
 
-    RecvPipe recv_pipe(bool with_partials, int ncw, bool stage_out = false, int ch = 0) const {
+    RecvPipe recv_pipe(bool with_partials, int ncw, bool stage_out = false, int ch = 0, bool stage_g = false) const {
         RecvPipe R;
         R.xbulk = xbytes() % 16 == 0;
         R.ybulk = ybytes() % 16 == 0;
@@ -825,7 +827,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         R.y_off = R.x_off + (R.xbulk ? a16(R.ch * xbytes()) : 0);
         R.stage = stage;
         R.bar_off = R.nst * stage;
-        R.part_off = R.bar_off + 16 * R.nst;
+        // The edge kernel's d_out block (U x D_out, contiguous) arrives by one bulk copy per
+        // receiver into a buffer of its own, with a full/empty barrier pair after the stages'.
+        R.gbytes = size_t(P->U) * P->Do * P->elem();
+        R.gst = stage_g && R.gbytes % 16 == 0;
+        R.part_off = R.bar_off + 16 * R.nst + (R.gst ? 16 : 0);
         R.xpart_off = R.part_off + dyp;
         R.out_off = R.xpart_off + dxp;
         // The receiver's output block out[r] (U x D_out, contiguous in global memory) is staged in
@@ -837,11 +843,16 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             R.ovec = R.odp == P->Do && (size_t(P->U) * P->Do * P->elem()) % 16 == 0;
         }
         R.total = R.out_off + (stage_out ? a16(size_t(P->U) * R.odp * P->elem()) : 0);
+        R.g_off = R.total;
+        if (R.gst) R.total += a16(R.gbytes);
         R.tx_per_edge = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
-        // With the output block staged, shorter stages keep three blocks resident per SM where
+        // With a receiver block staged, shorter stages keep three blocks resident per SM where
         // the default chunk would leave fewer (more warps beat a longer look-ahead per block).
-        if (stage_out && !chosen && R.ch > 1 && minb(R.total) < 3)
-            return recv_pipe(with_partials, ncw, stage_out, R.ch - 1);
+        if ((stage_out || R.gst) && !chosen && R.ch > 1 && minb(R.total) < 3)
+            return recv_pipe(with_partials, ncw, stage_out, R.ch - 1, stage_g);
+        // a staged block that does not fit next to the stages is not staged
+        if (R.total > 227 * 1024 && R.gst) return recv_pipe(with_partials, ncw, stage_out, ch, false);
+        if (R.total > 227 * 1024 && stage_out) return recv_pipe(with_partials, ncw, false, ch, stage_g);
         return R;
     }
 
@@ -856,6 +867,9 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S(fmt("#define %s_XPART %zu", pre, R.xpart_off));
         S(fmt("#define %s_TX %zu", pre, R.tx_per_edge));
         S(fmt("#define %s_OBUF %zu", pre, R.out_off));
+        S(fmt("#define %s_GBUF %zu", pre, R.g_off));
+        S(fmt("#define %s_GBAR %zu", pre, R.bar_off + 16 * R.nst));
+        S(fmt("#define %s_GBYTES %zu", pre, R.gbytes));
         S(fmt("#define %s_ODP %d", pre, R.odp));
         const int mb = std::min(minb(R.total), pre[0] == 'F' ? P->minb[0] : P->minb[1]);
         P->minb_eff[pre[0] == 'F' ? 0 : 1] = mb;
@@ -877,10 +891,13 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     void emit_recv_producer(Src& S, const RecvPipe& R, const char* pre, const char* name) const {
         const int CH = R.ch;
         S(fmt("__device__ __noinline__ void %s(long long N, const int* __restrict__ off, const int* __restrict__ src,", name));
-        S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, unsigned sbase) {",
-              T.c_str(), T.c_str(), T.c_str()));
+        S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ gout,",
+              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S("    unsigned sbase) {");
         S.ind++;
         S("unsigned c = 0;");
+        if (R.gst) S("unsigned kg = 0;  // d_out blocks issued");
+        if (R.gst) S("bool fresh = true;  // no chunk of receiver r issued yet");
         S("bool dead = false;");
         S("const long long G = gridDim.x;");
         S("long long r = blockIdx.x;");
@@ -895,6 +912,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("r += G;");
         S("if (r >= N) break;");
         S("eb = nb; e1 = n1;");
+        if (R.gst) S("fresh = true;");
         S("if (r + G < N) { nb = __ldg(off + r + G); n1 = __ldg(off + r + G + 1); }");
         for (int j = 0; j < CH; ++j) S(fmt("sv%d = (%d < e1 - eb) ? __ldg(src + eb + %d) : 0;", j, j, j));
         S("continue;");
@@ -912,6 +930,17 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S(fmt("  if (ok) { prefetch_l2(w + (size_t)pa * (UVU_P * UVU_U), (unsigned)(pb - pa) * %zuu);", wbytes()));
             if (R.ybulk) S(fmt("             prefetch_l2(Y + (size_t)pa * UVU_DY, (unsigned)(pb - pa) * %zuu); }", ybytes()));
             else S("  }");
+            S("}");
+        }
+        if (R.gst) {
+            // first chunk of a receiver: its d_out block goes into the (single) block buffer once
+            // the consumers have taken the previous receiver's block into registers
+            S("if (fresh) {");
+            S(fmt("  if (kg >= 1u && !mbar_wait(sbase + %s_GBAR + 8u, (kg - 1u) & 1u)) { dead = true; break; }", pre));
+            S(fmt("  mbar_expect_tx(sbase + %s_GBAR, %zuu);", pre, R.gbytes));
+            S(fmt("  bulk_g2s(sbase + %s_GBUF, gout + (size_t)r * (UVU_U * UVU_DO), %zuu, sbase + %s_GBAR);", pre, R.gbytes, pre));
+            S("  ++kg;");
+            S("  fresh = false;");
             S("}");
         }
         S(fmt("const unsigned st = c %% %s_NST;", pre));
@@ -935,6 +964,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("if (dead) {  // let the copies already issued land before the block exits");
         S(fmt("  const unsigned n = c < %s_NST ? c : %s_NST;", pre, pre));
         S(fmt("  for (unsigned k = c - n; k < c; ++k) mbar_wait(sbase + %s_BAR + 8u * (k %% %s_NST), (k / %s_NST) & 1u);", pre, pre, pre));
+        if (R.gst) S(fmt("  if (kg >= 1u) mbar_wait(sbase + %s_GBAR, (kg - 1u) & 1u);", pre));
         S("}");
         S.ind--;
         S("}");
@@ -1018,7 +1048,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("}");
         S("__syncthreads();");
         S("if (warp == UVU_NCW) {");
-        S("  if (lane == 0) fwd_producer(N, off, src, x, Y, w, sbase);");
+        S("  if (lane == 0) fwd_producer(N, off, src, x, Y, w, nullptr, sbase);");
         S("  return;");
         S("}");
         S("const int u = tid % UVU_UP, g = tid / UVU_UP;");
@@ -1134,14 +1164,36 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             for (int pi : paths)
                 for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
             S(fmt("__device__ __forceinline__ void edge_rcv%d(long long r, int e0, int e1, int u, bool uvalid, int lane, int warp,", g));
-            S("    int tid, unsigned& c, bool& dead, int& buf, const unsigned char* smem, unsigned sbase,");
+            S("    int tid, unsigned& c, unsigned& kg, bool& dead, int& buf, const unsigned char* smem, unsigned sbase,");
             S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
             S(fmt("    const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx,",
                   T.c_str(), T.c_str(), T.c_str(), T.c_str()));
             S(fmt("    %s* __restrict__ dxe, int g) {", T.c_str()));
             S.ind++;
-            S(fmt("const %s* __restrict__ grow = gout + ((size_t)r * UVU_U + (uvalid ? u : 0)) * UVU_DO;", T.c_str()));
-            for (int k : outs) S(fmt("const %s gv_%d = __ldg(grow + %d);", T.c_str(), k, k));
+            if (R.gst) {
+                // d_out row of this channel from the receiver's staged block; the block buffer
+                // is handed back to the producer as soon as the row is in registers
+                for (int k : outs) S(fmt("%s gv_%d = 0;", T.c_str(), k));
+                S("if (e1 > e0) {");
+                S.ind++;
+                S("if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(sbase + EG_GBAR, kg & 1u));");
+                S(fmt("const %s* grow = reinterpret_cast<const %s*>(smem + EG_GBUF) + (uvalid ? u : 0) * UVU_DO;", T.c_str(), T.c_str()));
+                for (int k : outs) S(fmt("gv_%d = grow[%d];", k, k));
+                S("if (!dead) {");
+                S.ind++;
+                if (release_mode() != 3) S("__threadfence_block();");
+                S("asm volatile(\"fence.proxy.async.shared::cta;\" ::: \"memory\");");
+                S("__syncwarp();");
+                S(std::string("if (") + (release_mode() == 1 ? "true" : "lane == 0") + ") mbar_arrive(sbase + EG_GBAR + 8u);");
+                S.ind--;
+                S("}");
+                S("++kg;");
+                S.ind--;
+                S("}");
+            } else {
+                S(fmt("const %s* __restrict__ grow = gout + ((size_t)r * UVU_U + (uvalid ? u : 0)) * UVU_DO;", T.c_str()));
+                for (int k : outs) S(fmt("const %s gv_%d = __ldg(grow + %d);", T.c_str(), k, k));
+            }
             S(fmt("%s* partbase = reinterpret_cast<%s*>(const_cast<unsigned char*>(smem) + EG_PART);", T.c_str(), T.c_str()));
             S("for (int eb = e0; eb < e1; eb += EG_CH, ++c) {");
             S.ind++;
@@ -1249,23 +1301,24 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;");
         S("if (tid == 0) {");
         S("  for (int i = 0; i < EG_NST; ++i) { mbar_init(sbase + EG_BAR + 8u * i, 1u); mbar_init(sbase + EG_BAR + 8u * (EG_NST + i), " + std::string(empty_count("UVU_NCW", "UVU_NCT")) + "); }");
+        if (R.gst) S("  mbar_init(sbase + EG_GBAR, 1u); mbar_init(sbase + EG_GBAR + 8u, " + std::string(empty_count("UVU_NCW", "UVU_NCT")) + ");");
         S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
         S("}");
         S("__syncthreads();");
         S("if (warp == UVU_NCW) {");
-        S("  if (lane == 0) edge_producer(N, off, src, x, Y, w, sbase);");
+        S("  if (lane == 0) edge_producer(N, off, src, x, Y, w, gout, sbase);");
         S("  return;");
         S("}");
         S("const int u = tid % UVU_UP, g = tid / UVU_UP;");
         S("const bool uvalid = u < UVU_U;");
-        S("unsigned c = 0;");
+        S("unsigned c = 0, kg = 0;");
         S("bool dead = false;");
         S("int buf = 0;");
         S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
         S.ind++;
         S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
         for (int g = 0; g < NG; ++g)
-            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, dead, buf, smem, sbase, src, x, Y, gout, dY, dw, dx, dxe, g);",
+            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, kg, dead, buf, smem, sbase, src, x, Y, gout, dY, dw, dx, dxe, g);",
                   g ? "else " : "", g, g));
         S.ind--;
         S("}");
@@ -1604,7 +1657,9 @@ std::string emit_source(Plan* plan) {
     }
     // UVU_PIPE_OSTAGE=0 (a tuning switch) writes the forward output straight from registers.
     const bool ostage = !(std::getenv("UVU_PIPE_OSTAGE") && std::atoi(std::getenv("UVU_PIPE_OSTAGE")) == 0);
-    Gen::RecvPipe RF = G.recv_pipe(false, ncw, ostage), RE = G.recv_pipe(true, ncw);
+    // UVU_PIPE_GSTAGE=0 (a tuning switch) reads the edge kernel's d_out rows straight from global memory.
+    const bool gstage = !(std::getenv("UVU_PIPE_GSTAGE") && std::atoi(std::getenv("UVU_PIPE_GSTAGE")) == 0);
+    Gen::RecvPipe RF = G.recv_pipe(false, ncw, ostage), RE = G.recv_pipe(true, ncw, false, 0, gstage);
     Gen::SendPipe SD = G.send_pipe();
     const bool pipe_dx = !force_direct && U >= 32 && G.send_pipe_ok(SD);
     plan->pipelined_recv = pipe_recv;
