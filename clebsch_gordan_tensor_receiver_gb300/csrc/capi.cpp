@@ -164,6 +164,17 @@ extern "C" uvu_status uvu_plan_source(uvu_plan_t plan, const char** source, cons
     return ok();
 }
 
+extern "C" uvu_status uvu_plan_hvp_source(uvu_plan_t plan, const char** source, const char** log) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    std::string err;
+    uvu_status s = compile_hvp(p, &err);
+    if (s != UVU_OK) return fail(s, err);
+    if (source) *source = p->hvp_source.c_str();
+    if (log) *log = p->hvp_log.c_str();
+    return ok();
+}
+
 extern "C" uvu_status uvu_csr_from_sorted_recv(int64_t n_nodes, int64_t n_edges, const int32_t* recv,
                                                int32_t* recv_offsets, uvu_stream_t stream) {
     UVU_TRY(check_sizes(n_nodes, n_edges));
@@ -374,9 +385,16 @@ extern "C" uvu_status uvu_plan_device_status(uvu_plan_t plan, unsigned* word, in
     uvu_status s = module_for_current_device(p, &m, &err);
     if (s != UVU_OK) return fail(s, err);
     cudaError_t e = cudaMemcpy(word, m->status_word, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && m->hvp_status_word) {  // the double-backward module's own word
+        unsigned w2 = 0;
+        e = cudaMemcpy(&w2, m->hvp_status_word, sizeof(unsigned), cudaMemcpyDeviceToHost);
+        *word |= w2;
+    }
     if (e == cudaSuccess && reset) {
         const unsigned zero = 0;
         e = cudaMemcpy(m->status_word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
+        if (e == cudaSuccess && m->hvp_status_word)
+            e = cudaMemcpy(m->hvp_status_word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
     }
     if (e != cudaSuccess) return cuda_fail(e, "status word copy");
     return ok();
@@ -386,7 +404,9 @@ extern "C" uvu_status uvu_conv_hvp_workspace(uvu_plan_t plan, int64_t n_nodes, i
     Plan* p = get(plan);
     if (!p || !bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or bytes is NULL");
     UVU_TRY(check_sizes(n_nodes, n_edges));
-    *bytes = p->groups.size() == 1 ? size_t(n_edges) * p->U * p->Dx * p->elem() : 0;
+    // per-edge grad_x partials: written by the pipelined kernels for any register grouping and by
+    // the direct-load kernels with one group; otherwise grad_x is accumulated with atomics
+    *bytes = (p->pipelined_recv || p->groups.size() == 1) ? size_t(n_edges) * p->U * p->Dx * p->elem() : 0;
     return ok();
 }
 
@@ -433,7 +453,7 @@ extern "C" uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
     long long N = n_nodes;
     if (grad_d_out) {
         void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &ax, &aY, &aw, const_cast<int*>(&hm), &grad_d_out};
-        UVU_TRY(launch(m->hvp_fwd, 1, m->sm_count, n_nodes, p->g_hvp_fwd, args, stream, "uvu_hvp_fwd launch"));
+        UVU_TRY(launch(m->hvp_fwd, m->occ_hvp_fwd, m->sm_count, n_nodes, p->g_hvp_fwd, args, stream, "uvu_hvp_fwd launch"));
     }
     if (!need_edge) return ok();
     void* dx_atomic = (grad_x && !staged) ? grad_x : nullptr;
@@ -445,7 +465,7 @@ extern "C" uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
     if (n_edges > 0) {
         void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &d_out, &ax, &aY, &aw, const_cast<int*>(&hm),
                         &grad_Y, &grad_w, &dx_atomic, &dx_edge};
-        UVU_TRY(launch(m->hvp_edge, 1, m->sm_count, n_nodes, p->g_hvp_edge, args, stream, "uvu_hvp_edge launch"));
+        UVU_TRY(launch(m->hvp_edge, m->occ_hvp_edge, m->sm_count, n_nodes, p->g_hvp_edge, args, stream, "uvu_hvp_edge launch"));
     }
     if (staged) UVU_TRY(uvu_conv_bwd_dx_reduce(plan, n_nodes, n_edges, send_offsets, send_eids, workspace, grad_x, stream));
     return ok();

@@ -450,11 +450,11 @@ struct Gen {
 
     // Declares pre_k = 0 for k in `need`, then loads them from `base` when `cond` holds.
     void emit_row_loads_masked(Src& S, const std::string& pre, const std::string& base, int width,
-                               const std::set<int>& need, const std::string& cond) const {
+                               const std::set<int>& need, const std::string& cond, bool global = true) const {
         for (int k : need) S(fmt("%s %s_%d = 0;", T.c_str(), pre.c_str(), k));
         S("if (" + cond + ") {");
         S.ind++;
-        emit_row_loads(S, pre + "l", base, width, need);
+        emit_row_loads(S, pre + "l", base, width, need, global);
         for (int k : need) S(fmt("%s_%d = %sl_%d;", pre.c_str(), k, pre.c_str(), k));
         S.ind--;
         S("}");
@@ -488,6 +488,24 @@ struct Gen {
         S("}");
     }
 
+    // Per-edge part of dL2/dg: F(ax,Y,w) + F(x,aY,w) through the mixed products, plus F(x,Y,aw).
+    void emit_hvp_fwd_edge(Src& S, const std::vector<int>& paths) const {
+        emit_mixed_products(S, paths, "qm");
+        emit_products(S, paths);
+        for (int pi : paths) {
+            const PathInfo& p = P->paths[pi];
+            S("{");
+            S.ind++;
+            emit_t(S, pi, "qm", "tm");
+            emit_t(S, pi, "q", "t");
+            for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3)
+                S(fmt("acc_%d = fma(wv_%d, tm_%d_%d, fma(awv_%d, t_%d_%d, acc_%d));", p.ooff + m3, pi, pi, m3, pi, pi, m3,
+                      p.ooff + m3));
+            S.ind--;
+            S("}");
+        }
+    }
+
     void emit_hvp_fwd_group(Src& S, int g) const {
         const std::vector<int>& paths = P->groups[g];
         std::vector<int> outs;
@@ -503,20 +521,7 @@ struct Gen {
         S("for (int e = e0; e < e1; ++e) {");
         S.ind++;
         emit_hvp_edge_loads(S, paths);
-        emit_mixed_products(S, paths, "qm");
-        emit_products(S, paths);
-        for (int pi : paths) {
-            const PathInfo& p = P->paths[pi];
-            S("{");
-            S.ind++;
-            emit_t(S, pi, "qm", "tm");
-            emit_t(S, pi, "q", "t");
-            for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3)
-                S(fmt("acc_%d = fma(wv_%d, tm_%d_%d, fma(awv_%d, t_%d_%d, acc_%d));", p.ooff + m3, pi, pi, m3, pi, pi, m3,
-                      p.ooff + m3));
-            S.ind--;
-            S("}");
-        }
+        emit_hvp_fwd_edge(S, paths);
         S.ind--;
         S("}");
         for (int k : outs) S(fmt("orow[%d] = acc_%d;", k, k));
@@ -797,23 +802,27 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         int odp = 0;  // row stride (elements) of the staged output block, 0 = not staged
         bool ovec = false;  // staged block copied out with 16-byte vectors
         bool gst = false;  // the receiver's d_out block is bulk-copied into shared memory
+        bool dual = false;  // double backward: the stage also holds the cotangent rows aw, ax, aY
+        size_t aw_off = 0, ax_off = 0, ay_off = 0;
         size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, xpart_off = 0, out_off = 0, total = 0;
         size_t g_off = 0, gbytes = 0;
         size_t tx_per_edge = 0;
     };
     static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
 
-    RecvPipe recv_pipe(bool with_partials, int ncw, bool stage_out = false, int ch = 0, bool stage_g = false) const {
+    RecvPipe recv_pipe(bool with_partials, int ncw, bool stage_out = false, int ch = 0, bool stage_g = false,
+                       bool dual = false) const {
         RecvPipe R;
+        R.dual = dual;
         R.xbulk = xbytes() % 16 == 0;
         R.ybulk = ybytes() % 16 == 0;
         const int NG = int(P->groups.size());
-        const size_t pe = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
+        const size_t pe = (wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0)) * (dual ? 2 : 1);
         const bool chosen = ch > 0 || std::getenv("UVU_PIPE_CH");
         R.ch = ch > 0 ? ch : int(std::max<size_t>(1, std::min<size_t>(8, 32768 / pe)));
         if (const char* e = std::getenv("UVU_PIPE_CH")) R.ch = std::max(1, std::atoi(e));
-        const size_t stage = a16(R.ch * wbytes()) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
-                             (R.ybulk ? a16(R.ch * ybytes()) : 0);
+        const size_t stage = (a16(R.ch * wbytes()) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
+                              (R.ybulk ? a16(R.ch * ybytes()) : 0)) * (dual ? 2 : 1);
         // per-stage partial sums of the edge kernel: dY over warps, dx over register groups
         const size_t dyp = with_partials ? a16(2 * size_t(ncw) * R.ch * P->Dy * P->elem()) : 0;
         const size_t dxp = (with_partials && NG > 1) ? a16(2 * size_t(NG) * R.ch * P->U_pad * P->Dx * P->elem()) : 0;
@@ -823,8 +832,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         if (const char* e = std::getenv("UVU_PIPE_NST")) R.nst = std::max(2, std::atoi(e));
         if (const char* e = std::getenv("UVU_PIPE_PF")) R.pf = std::max(0, std::atoi(e));
         R.w_off = 0;
-        R.x_off = a16(R.ch * wbytes());
-        R.y_off = R.x_off + (R.xbulk ? a16(R.ch * xbytes()) : 0);
+        R.aw_off = dual ? a16(R.ch * wbytes()) : 0;
+        R.x_off = (dual ? 2 : 1) * a16(R.ch * wbytes());
+        R.ax_off = R.x_off + ((dual && R.xbulk) ? a16(R.ch * xbytes()) : 0);
+        R.y_off = R.x_off + (R.xbulk ? (dual ? 2 : 1) * a16(R.ch * xbytes()) : 0);
+        R.ay_off = R.y_off + ((dual && R.ybulk) ? a16(R.ch * ybytes()) : 0);
         R.stage = stage;
         R.bar_off = R.nst * stage;
         // The edge kernel's d_out block (U x D_out, contiguous) arrives by one bulk copy per
@@ -849,14 +861,15 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         // With a receiver block staged, shorter stages keep three blocks resident per SM where
         // the default chunk would leave fewer (more warps beat a longer look-ahead per block).
         if ((stage_out || R.gst) && !chosen && R.ch > 1 && minb(R.total) < 3)
-            return recv_pipe(with_partials, ncw, stage_out, R.ch - 1, stage_g);
+            return recv_pipe(with_partials, ncw, stage_out, R.ch - 1, stage_g, dual);
         // a staged block that does not fit next to the stages is not staged
-        if (R.total > 227 * 1024 && R.gst) return recv_pipe(with_partials, ncw, stage_out, ch, false);
-        if (R.total > 227 * 1024 && stage_out) return recv_pipe(with_partials, ncw, false, ch, stage_g);
+        if (R.total > 227 * 1024 && R.gst) return recv_pipe(with_partials, ncw, stage_out, ch, false, dual);
+        if (R.total > 227 * 1024 && stage_out) return recv_pipe(with_partials, ncw, false, ch, stage_g, dual);
         return R;
     }
 
-    void emit_recv_pipe_defines(Src& S, const RecvPipe& R, const char* pre) const {
+    // slot: the kernel's entry in the plan's register-budget tables (0 fwd, 1 edge, 3 hvp_fwd, 4 hvp_edge)
+    void emit_recv_pipe_defines(Src& S, const RecvPipe& R, const char* pre, int slot) const {
         S(fmt("#define %s_CH %d", pre, R.ch));
         S(fmt("#define %s_NST %d", pre, R.nst));
         S(fmt("#define %s_STAGE %zu", pre, R.stage));
@@ -870,9 +883,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S(fmt("#define %s_GBUF %zu", pre, R.g_off));
         S(fmt("#define %s_GBAR %zu", pre, R.bar_off + 16 * R.nst));
         S(fmt("#define %s_GBYTES %zu", pre, R.gbytes));
+        S(fmt("#define %s_AWOFF %zu", pre, R.aw_off));
+        S(fmt("#define %s_AXOFF %zu", pre, R.ax_off));
+        S(fmt("#define %s_AYOFF %zu", pre, R.ay_off));
         S(fmt("#define %s_ODP %d", pre, R.odp));
-        const int mb = std::min(minb(R.total), pre[0] == 'F' ? P->minb[0] : P->minb[1]);
-        P->minb_eff[pre[0] == 'F' ? 0 : 1] = mb;
+        const int mb = std::min(minb(R.total), P->minb[slot]);
+        P->minb_eff[slot] = mb;
         S(fmt("#define %s_MINB %d", pre, mb));
     }
     // Blocks per SM the shared-memory footprint allows (capped at 4); UVU_PIPE_MINB (a tuning
@@ -893,8 +909,14 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S(fmt("__device__ __noinline__ void %s(long long N, const int* __restrict__ off, const int* __restrict__ src,", name));
         S(fmt("    const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ w, const %s* __restrict__ gout,",
               T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        if (R.dual)
+            S(fmt("    const %s* __restrict__ ax, const %s* __restrict__ aY, const %s* __restrict__ aw, int hm,", T.c_str(), T.c_str(),
+                  T.c_str()));
         S("    unsigned sbase) {");
         S.ind++;
+        if (R.dual)  // bytes per edge with the cotangent rows that are present (mask hm: 1 = ax, 2 = aY, 4 = aw)
+            S(fmt("const unsigned txe = %s_TX + ((hm & 4) ? %zuu : 0u) + ((hm & 2) ? %zuu : 0u) + ((hm & 1) ? %zuu : 0u);", pre,
+                  wbytes(), R.ybulk ? ybytes() : size_t(0), R.xbulk ? xbytes() : size_t(0)));
         S("unsigned c = 0;");
         if (R.gst) S("unsigned kg = 0;  // d_out blocks issued");
         if (R.gst) S("bool fresh = true;  // no chunk of receiver r issued yet");
@@ -948,13 +970,20 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
               pre, pre, pre, pre));
         S(fmt("const unsigned full = sbase + %s_BAR + 8u * st;", pre));
         S(fmt("const unsigned stg = sbase + st * %s_STAGE;", pre));
-        S(fmt("mbar_expect_tx(full, (unsigned)ne * %s_TX);", pre));
+        if (R.dual) S("mbar_expect_tx(full, (unsigned)ne * txe);");
+        else S(fmt("mbar_expect_tx(full, (unsigned)ne * %s_TX);", pre));
         S(fmt("bulk_g2s(stg, w + (size_t)eb * (UVU_P * UVU_U), (unsigned)ne * %zuu, full);", wbytes()));
+        if (R.dual) S(fmt("if (hm & 4) bulk_g2s(stg + %s_AWOFF, aw + (size_t)eb * (UVU_P * UVU_U), (unsigned)ne * %zuu, full);", pre, wbytes()));
         if (R.ybulk) S(fmt("bulk_g2s(stg + %s_YOFF, Y + (size_t)eb * UVU_DY, (unsigned)ne * %zuu, full);", pre, ybytes()));
+        if (R.ybulk && R.dual) S(fmt("if (hm & 2) bulk_g2s(stg + %s_AYOFF, aY + (size_t)eb * UVU_DY, (unsigned)ne * %zuu, full);", pre, ybytes()));
         if (R.xbulk) {
             for (int j = 0; j < CH; ++j)
                 S(fmt("if (%d < ne) bulk_g2s(stg + %s_XOFF + %zuu, x + (size_t)sv%d * (UVU_U * UVU_DX), %zuu, full);", j, pre,
                       size_t(j) * xbytes(), j, xbytes()));
+            if (R.dual)
+                for (int j = 0; j < CH; ++j)
+                    S(fmt("if ((hm & 1) && %d < ne) bulk_g2s(stg + %s_AXOFF + %zuu, ax + (size_t)sv%d * (UVU_U * UVU_DX), %zuu, full);",
+                          j, pre, size_t(j) * xbytes(), j, xbytes()));
         }
         for (int j = 0; j < CH; ++j) S(fmt("sv%d = svn%d;", j, j));
         S("eb = ebn;");
@@ -988,6 +1017,24 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
         S(fmt("const %s* swr = reinterpret_cast<const %s*>(stg) + j * (UVU_P * UVU_U) + u;", T.c_str(), T.c_str()));
         for (int pi : paths) S(fmt("const %s wv_%d = swr[%d * UVU_U];", T.c_str(), pi, pi));
+        if (!R.dual) return;
+        // cotangent rows of the double backward; absent ones (mask hm) read as zero
+        if (R.xbulk) {
+            emit_row_loads_masked(S, "axv", fmt("reinterpret_cast<const %s*>(stg + %s_AXOFF) + (j * UVU_U + u) * UVU_DX", T.c_str(), pre),
+                                  P->Dx, xn, "hm & 1", false);
+        } else {
+            emit_row_loads_masked(S, "axv", "ax + ((size_t)s * UVU_U + u) * UVU_DX", P->Dx, xn, "hm & 1");
+        }
+        if (R.ybulk)
+            emit_row_loads_masked(S, "ayv", fmt("reinterpret_cast<const %s*>(stg + %s_AYOFF) + j * UVU_DY", T.c_str(), pre), P->Dy, yn,
+                                  "hm & 2", false);
+        else
+            emit_row_loads_masked(S, "ayv", "aY + (size_t)e * UVU_DY", P->Dy, yn, "hm & 2");
+        for (int pi : paths) S(fmt("%s awv_%d = 0;", T.c_str(), pi));
+        S("if (hm & 4) {");
+        S(fmt("  const %s* swa = reinterpret_cast<const %s*>(stg + %s_AWOFF) + j * (UVU_P * UVU_U) + u;", T.c_str(), T.c_str(), pre));
+        for (int pi : paths) S(fmt("  awv_%d = swa[%d * UVU_U];", pi, pi));
+        S("}");
     }
 
     void emit_fwd_v2(Src& S, const RecvPipe& R) const {
@@ -1001,6 +1048,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
             S(fmt("__device__ __forceinline__ void fwd_rcv%d(int e0, int e1, int u, bool uvalid, int lane, unsigned& c, bool& dead,", g));
             S(fmt("    const unsigned char* smem, unsigned sbase, const int* __restrict__ src, const %s* __restrict__ x,", T.c_str()));
+            if (R.dual) S(fmt("    const %s* __restrict__ ax, const %s* __restrict__ aY, int hm,", T.c_str(), T.c_str()));
             S(fmt("    const %s* __restrict__ Y, %s* __restrict__ orow) {", T.c_str(), T.c_str()));
             S.ind++;
             for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
@@ -1019,7 +1067,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("if (j < ne) {");
             S.ind++;
             emit_stage_edge_loads(S, R, "FW", xn, yn, paths);
-            emit_fwd_edge(S, paths);
+            if (R.dual) emit_hvp_fwd_edge(S, paths);
+            else emit_fwd_edge(S, paths);
             S.ind--;
             S("}");
             S.ind--;
@@ -1035,9 +1084,15 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S.ind--;
             S("}");
         }
-        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, FW_MINB) uvu_fwd(long long N, const int* __restrict__ off,"));
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, FW_MINB) %s(long long N, const int* __restrict__ off,",
+              R.dual ? "uvu_hvp_fwd" : "uvu_fwd"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
-        S(fmt("    const %s* __restrict__ w, %s* __restrict__ out) {", T.c_str(), T.c_str()));
+        if (R.dual)
+            S(fmt("    const %s* __restrict__ w, const %s* __restrict__ ax, const %s* __restrict__ aY, const %s* __restrict__ aw, int hm,",
+                  T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        else
+            S(fmt("    const %s* __restrict__ w,", T.c_str()));
+        S(fmt("    %s* __restrict__ out) {", T.c_str()));
         S.ind++;
         S("extern __shared__ __align__(128) unsigned char smem[];");
         S("const unsigned sbase = smem_addr(smem);");
@@ -1048,7 +1103,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("}");
         S("__syncthreads();");
         S("if (warp == UVU_NCW) {");
-        S("  if (lane == 0) fwd_producer(N, off, src, x, Y, w, nullptr, sbase);");
+        if (R.dual) S("  if (lane == 0) fwd_producer(N, off, src, x, Y, w, nullptr, ax, aY, aw, hm, sbase);");
+        else S("  if (lane == 0) fwd_producer(N, off, src, x, Y, w, nullptr, sbase);");
         S("  return;");
         S("}");
         S("const int u = tid % UVU_UP, g = tid / UVU_UP;");
@@ -1061,7 +1117,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
             S(T + "* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
             for (int g = 0; g < NG; ++g)
-                S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, Y, orow);", g ? "else " : "", g, g));
+                S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, %sY, orow);", g ? "else " : "", g, g,
+                      R.dual ? "ax, aY, hm, " : ""));
             S.ind--;
             S("}");
             S.ind--;
@@ -1076,7 +1133,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
         S("consumer_sync();  // the previous receiver's block has been copied out of sout");
         for (int g = 0; g < NG; ++g)
-            S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, Y, orow);", g ? "else " : "", g, g));
+            S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, %sY, orow);", g ? "else " : "", g, g,
+                  R.dual ? "ax, aY, hm, " : ""));
         S("consumer_sync();");
         S(fmt("%s* const og = out + (size_t)r * (UVU_U * UVU_DO);", T.c_str()));
         if (R.ovec) {
@@ -1166,6 +1224,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S(fmt("__device__ __forceinline__ void edge_rcv%d(long long r, int e0, int e1, int u, bool uvalid, int lane, int warp,", g));
             S("    int tid, unsigned& c, unsigned& kg, bool& dead, int& buf, const unsigned char* smem, unsigned sbase,");
             S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
+            if (R.dual) S(fmt("    const %s* __restrict__ ax, const %s* __restrict__ aY, int hm,", T.c_str(), T.c_str()));
             S(fmt("    const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx,",
                   T.c_str(), T.c_str(), T.c_str(), T.c_str()));
             S(fmt("    %s* __restrict__ dxe, int g) {", T.c_str()));
@@ -1215,14 +1274,27 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             emit_stage_edge_loads(S, R, "EG", xn, yn, paths);
             S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
             for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
-            emit_products(S, paths);
             auto gval = [](int k) { return fmt("gv_%d", k); };
-            S("if (dw) {");
-            S.ind++;
-            emit_bwd_pairs(S, paths, true, false, false, gval);
-            S.ind--;
-            S("}");
-            emit_bwd_pairs(S, paths, false, true, true, gval);
+            if (R.dual) {
+                // dw(x<-ax) + dw(Y<-aY) through the mixed products; dY(x<-ax) and dx(Y<-aY) with
+                // w; dY and dx with w<-aw
+                S("if (dw) {");
+                S.ind++;
+                emit_mixed_products(S, paths, "q");
+                emit_bwd_pairs(S, paths, true, false, false, gval);
+                S.ind--;
+                S("}");
+                emit_bwd_pairs(S, paths, false, true, true, gval, "axv", "ayv", "wv");
+                emit_bwd_pairs(S, paths, false, true, true, gval, "xv", "yv", "awv");
+            } else {
+                emit_products(S, paths);
+                S("if (dw) {");
+                S.ind++;
+                emit_bwd_pairs(S, paths, true, false, false, gval);
+                S.ind--;
+                S("}");
+                emit_bwd_pairs(S, paths, false, true, true, gval);
+            }
             S("if (dx) {");
             S.ind++;
             if (!R.xbulk) {
@@ -1290,10 +1362,16 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S.ind--;
             S("}");
         }
-        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, EG_MINB) uvu_bwd_edge(long long N, const int* __restrict__ off,"));
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, EG_MINB) %s(long long N, const int* __restrict__ off,",
+              R.dual ? "uvu_hvp_edge" : "uvu_bwd_edge"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
-        S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
-              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        if (R.dual)
+            S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, const %s* __restrict__ ax, const %s* __restrict__ aY,\n"
+                  "    const %s* __restrict__ aw, int hm, %s* __restrict__ dY, %s* __restrict__ dw,",
+                  T.c_str(), T.c_str(), T.c_str(), T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        else
+            S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw,",
+                  T.c_str(), T.c_str(), T.c_str(), T.c_str()));
         S(fmt("    %s* __restrict__ dx, %s* __restrict__ dxe) {", T.c_str(), T.c_str()));
         S.ind++;
         S("extern __shared__ __align__(128) unsigned char smem[];");
@@ -1306,7 +1384,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("}");
         S("__syncthreads();");
         S("if (warp == UVU_NCW) {");
-        S("  if (lane == 0) edge_producer(N, off, src, x, Y, w, gout, sbase);");
+        if (R.dual) S("  if (lane == 0) edge_producer(N, off, src, x, Y, w, gout, ax, aY, aw, hm, sbase);");
+        else S("  if (lane == 0) edge_producer(N, off, src, x, Y, w, gout, sbase);");
         S("  return;");
         S("}");
         S("const int u = tid % UVU_UP, g = tid / UVU_UP;");
@@ -1318,8 +1397,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S.ind++;
         S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
         for (int g = 0; g < NG; ++g)
-            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, kg, dead, buf, smem, sbase, src, x, Y, gout, dY, dw, dx, dxe, g);",
-                  g ? "else " : "", g, g));
+            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, kg, dead, buf, smem, sbase, src, x, Y, %sgout, dY, dw, dx, dxe, g);",
+                  g ? "else " : "", g, g, R.dual ? "ax, aY, hm, " : ""));
         S.ind--;
         S("}");
         S.ind--;
@@ -1711,8 +1790,8 @@ std::string emit_source(Plan* plan) {
     S("}");
     G.emit_pipe_helpers(S);
     if (pipe_recv) {
-        G.emit_recv_pipe_defines(S, RF, "FW");
-        G.emit_recv_pipe_defines(S, RE, "EG");
+        G.emit_recv_pipe_defines(S, RF, "FW", 0);
+        G.emit_recv_pipe_defines(S, RE, "EG", 1);
         G.emit_fwd_v2(S, RF);
         G.emit_edge_v2(S, RE);
     } else {
@@ -1785,8 +1864,22 @@ std::string emit_hvp_source(Plan* plan) {
     const int segw = std::min(UP, 32);
     const int segs = NG * ((UP + 31) / 32);
     const int ch = 16;
-    plan->g_hvp_fwd = {rpb * owner_threads, rpb, 0, false};
-    plan->g_hvp_edge = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem(), false};
+    const int ncw = NG * UP / 32;
+    // Same kernels as the pipelined forward and edge backward, with stages that also carry the
+    // cotangent rows (aw, aY, ax); otherwise the direct-load kernels.
+    const bool pipe = plan->pipelined_recv;
+    const bool ostage = !(std::getenv("UVU_PIPE_OSTAGE") && std::atoi(std::getenv("UVU_PIPE_OSTAGE")) == 0);
+    const bool gstage = !(std::getenv("UVU_PIPE_GSTAGE") && std::atoi(std::getenv("UVU_PIPE_GSTAGE")) == 0);
+    Gen::RecvPipe RF, RE;
+    if (pipe) {
+        RF = G.recv_pipe(false, ncw, ostage, 0, false, true);
+        RE = G.recv_pipe(true, ncw, false, 0, gstage, true);
+        plan->g_hvp_fwd = {ncw * 32 + 32, 1, RF.total, true};
+        plan->g_hvp_edge = {ncw * 32 + 32, 1, RE.total, true};
+    } else {
+        plan->g_hvp_fwd = {rpb * owner_threads, rpb, 0, false};
+        plan->g_hvp_edge = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem(), false};
+    }
     Src S;
     S("// Generated by the UVU planner: double backward (HVP) of the channel-wise CG convolution.");
     S(fmt("// irreps_x=%s irreps_sh=%s lmax_out=%d dtype=%s", plan->irreps_x.c_str(), plan->irreps_sh.c_str(),
@@ -1803,11 +1896,23 @@ std::string emit_hvp_source(Plan* plan) {
     S(fmt("#define UVU_SEGW %d", segw));
     S(fmt("#define UVU_SEGS %d", segs));
     S(fmt("#define UVU_CH %d", ch));
+    S(fmt("#define UVU_NCW %d", ncw));
+    S(fmt("#define UVU_NCT %d", ncw * 32));
     S("__device__ __forceinline__ void block_sync() { asm volatile(\"barrier.sync 0;\" ::: \"memory\"); }");
     S("__device__ __forceinline__ void red_add_v4(float* a, float p, float q, float r, float s) {");
     S("  asm volatile(\"red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\" :: \"l\"(a), \"f\"(p), \"f\"(q), \"f\"(r), \"f\"(s) : \"memory\");");
     S("}");
-    G.emit_hvp_kernels(S);
+    if (pipe) {
+        G.emit_pipe_helpers(S);
+        G.emit_recv_pipe_defines(S, RF, "FW", 3);
+        G.emit_recv_pipe_defines(S, RE, "EG", 4);
+        G.no_identity = true;
+        G.emit_fwd_v2(S, RF);
+        G.emit_edge_v2(S, RE);
+        G.no_identity = false;
+    } else {
+        G.emit_hvp_kernels(S);
+    }
     return S.o.str();
 }
 

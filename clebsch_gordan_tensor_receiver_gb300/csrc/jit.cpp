@@ -200,31 +200,74 @@ uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string
 }
 
 // The double-backward module: emitted and compiled on the first HVP call of the plan (host),
-// then loaded once per device.
+// then loaded once per device.  Its pipelined kernels get the same register-budget retry and
+// launch set-up (shared-memory size, carveout, occupancy, status word) as the plan's own.
+// Same register-budget retry as the plan's own kernels (see uvu_plan_create): a pipelined HVP
+// kernel that spills under its budget is rebuilt for one resident block fewer.
+static uvu_status compile_hvp_locked(Plan* plan, std::string* err) {
+    if (!plan->hvp_cubin.empty()) return UVU_OK;
+    const char* names[2] = {"uvu_hvp_fwd", "uvu_hvp_edge"};
+    for (int attempt = 0;; ++attempt) {
+        plan->hvp_source = emit_hvp_source(plan);
+        CacheEntry e;
+        uvu_status s = nvrtc_compile(plan->hvp_source, &e, err);
+        if (s != UVU_OK) return s;
+        bool again = false;
+        for (int k = 0; k < 2 && attempt < 3; ++k)
+            if (plan->pipelined_recv && plan->minb_eff[3 + k] > 1 && spill_bytes(e.log, names[k]) > 32) {
+                plan->minb[3 + k] = plan->minb_eff[3 + k] - 1;
+                again = true;
+            }
+        if (!again) {
+            plan->hvp_cubin = std::move(e.cubin);
+            plan->hvp_log = std::move(e.log);
+            return UVU_OK;
+        }
+    }
+}
+
+uvu_status compile_hvp(Plan* plan, std::string* err) {
+    std::lock_guard<std::mutex> g(plan->mu);
+    return compile_hvp_locked(plan, err);
+}
+
 uvu_status hvp_module_for_current_device(Plan* plan, DeviceModule** out, std::string* err) {
     DeviceModule* m = nullptr;
     uvu_status s = module_for_current_device(plan, &m, err);
     if (s != UVU_OK) return s;
     std::lock_guard<std::mutex> g(plan->mu);
-    if (plan->hvp_cubin.empty()) {
-        plan->hvp_source = emit_hvp_source(plan);
-        CacheEntry e;
-        s = nvrtc_compile(plan->hvp_source, &e, err);
-        if (s != UVU_OK) return s;
-        plan->hvp_cubin = std::move(e.cubin);
-        plan->hvp_log = std::move(e.log);
-    }
+    const char* names[2] = {"uvu_hvp_fwd", "uvu_hvp_edge"};
+    s = compile_hvp_locked(plan, err);
+    if (s != UVU_OK) return s;
     if (!m->hvp_lib) {
         cudaError_t ce = cudaLibraryLoadData(&m->hvp_lib, plan->hvp_cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0);
-        if (ce == cudaSuccess) ce = cudaLibraryGetKernel(&m->hvp_fwd, m->hvp_lib, "uvu_hvp_fwd");
-        if (ce == cudaSuccess) ce = cudaLibraryGetKernel(&m->hvp_edge, m->hvp_lib, "uvu_hvp_edge");
-        if (ce == cudaSuccess && plan->g_hvp_edge.smem > 48 * 1024)
-            ce = cudaFuncSetAttribute(reinterpret_cast<const void*>(m->hvp_edge),
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(plan->g_hvp_edge.smem));
+        if (ce == cudaSuccess) ce = cudaLibraryGetKernel(&m->hvp_fwd, m->hvp_lib, names[0]);
+        if (ce == cudaSuccess) ce = cudaLibraryGetKernel(&m->hvp_edge, m->hvp_lib, names[1]);
+        struct {
+            cudaKernel_t k;
+            const KernelGeom* g;
+            int* occ;
+        } kk[] = {{m->hvp_fwd, &plan->g_hvp_fwd, &m->occ_hvp_fwd}, {m->hvp_edge, &plan->g_hvp_edge, &m->occ_hvp_edge}};
+        for (auto& k : kk) {
+            if (ce != cudaSuccess) break;
+            const void* f = reinterpret_cast<const void*>(k.k);
+            if (k.g->smem > 48 * 1024) ce = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(k.g->smem));
+            if (ce == cudaSuccess && k.g->persistent)
+                ce = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, int(cudaSharedmemCarveoutMaxShared));
+            if (ce == cudaSuccess) ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(k.occ, f, k.g->threads, k.g->smem);
+            if (ce == cudaSuccess && *k.occ < 1) ce = cudaErrorInvalidConfiguration;
+        }
+        if (ce == cudaSuccess && plan->pipelined_recv) {
+            size_t bytes = 0;
+            void* ptr = nullptr;
+            ce = cudaLibraryGetGlobal(&ptr, &bytes, m->hvp_lib, "uvu_status_word");
+            m->hvp_status_word = static_cast<unsigned*>(ptr);
+        }
         if (ce != cudaSuccess) {
             *err = std::string("loading the HVP module: ") + cudaGetErrorString(ce);
             if (m->hvp_lib) cudaLibraryUnload(m->hvp_lib);
             m->hvp_lib = nullptr;
+            m->hvp_status_word = nullptr;
             return UVU_ERR_CUDA;
         }
     }

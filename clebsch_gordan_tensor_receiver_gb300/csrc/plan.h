@@ -50,7 +50,9 @@ struct DeviceModule {
     cudaKernel_t hvp_fwd = nullptr, hvp_edge = nullptr;
     int sm_count = 0;
     int occ_fwd = 1, occ_edge = 1, occ_dx = 1;  // resident blocks per SM
+    int occ_hvp_fwd = 1, occ_hvp_edge = 1;
     unsigned* status_word = nullptr;            // device address of uvu_status_word
+    unsigned* hvp_status_word = nullptr;        // the same word of the double-backward module
 };
 
 struct Plan {
@@ -65,12 +67,13 @@ struct Plan {
     KernelGeom g_fwd, g_edge, g_dx, g_hvp_fwd, g_hvp_edge;
     int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
     bool pipelined_recv = false, pipelined_dx = false;
-    bool staged_ok = false;
-    bool rebalanced = false;  // register groups re-split for the pipelined kernels  // the edge kernel can write per-edge dx partials (staged dx)
+    bool staged_ok = false;   // the edge kernel can write per-edge dx partials (staged dx)
+    bool rebalanced = false;  // register groups re-split for the pipelined kernels
     // Upper bound on resident blocks per SM that the register budget is sized for, per kernel
-    // (fwd, edge, dx); lowered one block at a time for a kernel whose budget makes ptxas spill.
-    int minb[3] = {4, 4, 4};
-    int minb_eff[3] = {1, 1, 1};  // value used by the last emission
+    // (fwd, edge, dx, hvp_fwd, hvp_edge); lowered one block at a time for a kernel whose budget
+    // makes ptxas spill.
+    int minb[5] = {4, 4, 4, 4, 4};
+    int minb_eff[5] = {1, 1, 1, 1, 1};  // value used by the last emission
     std::string source, log;
     std::vector<char> cubin;
     std::string hvp_source, hvp_log;  // double-backward module, compiled on the first HVP call
@@ -96,6 +99,7 @@ void balance_groups(Plan* plan, int ng);
 uvu_status compile_plan(Plan* plan, std::string* err);
 size_t spill_bytes(const std::string& log, const char* kernel);
 uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string* err);
+uvu_status compile_hvp(Plan* plan, std::string* err);  // host only
 uvu_status hvp_module_for_current_device(Plan* plan, DeviceModule** out, std::string* err);
 
 // status.cpp

@@ -26,7 +26,7 @@ STATUS = {0: "UVU_OK", 1: "UVU_ERR_INVALID_ARGUMENT", 2: "UVU_ERR_UNSUPPORTED",
 # every symbol declared in include/uvu.h
 EXPORTS = (
     "uvu_plan_create", "uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
-    "uvu_plan_device_status",
+    "uvu_plan_hvp_source", "uvu_plan_device_status",
     "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
     "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
     "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
@@ -51,6 +51,7 @@ def _load():
         "uvu_plan_info": [P, P, P, P, P, P, P],
         "uvu_plan_cg": [P, I, P],
         "uvu_plan_source": [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
+        "uvu_plan_hvp_source": [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
         "uvu_plan_device_status": [P, ctypes.POINTER(ctypes.c_uint), I],
         "uvu_csr_from_sorted_recv": [I64, I64, P, P, P],
         "uvu_csr_transpose_workspace": [I64, I64, ctypes.POINTER(SZ)],
@@ -96,7 +97,7 @@ def _wrap(name):
     return call
 
 
-for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
+for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source", "uvu_plan_hvp_source",
            "uvu_plan_device_status",
            "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
            "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
@@ -179,6 +180,12 @@ class Plan:
     def source(self):
         s, l = ctypes.c_char_p(), ctypes.c_char_p()
         uvu_plan_source(self.handle, ctypes.byref(s), ctypes.byref(l))
+        return s.value.decode(), l.value.decode()
+
+    def hvp_source(self):
+        """(source, NVRTC log) of the double-backward kernels; compiles them on the host if needed."""
+        s, l = ctypes.c_char_p(), ctypes.c_char_p()
+        uvu_plan_hvp_source(self.handle, ctypes.byref(s), ctypes.byref(l))
         return s.value.decode(), l.value.decode()
 
     def fwd(self, n_nodes, x, Y, w, recv_offsets, src, out, stream=None):

@@ -112,6 +112,11 @@ uvu_status uvu_plan_cg(uvu_plan_t plan, int path, double *out);
  * log (ptxas resource usage).  Either pointer may be NULL. */
 uvu_status uvu_plan_source(uvu_plan_t plan, const char **source, const char **compile_log);
 
+/* The emitted source and NVRTC log of the plan's double-backward (HVP) kernels.  Compiles them
+ * on the host if no HVP call has done so yet (no device needed); UVU_ERR_COMPILE if NVRTC fails.
+ * The strings stay valid until the plan is destroyed.  Either pointer may be NULL. */
+uvu_status uvu_plan_hvp_source(uvu_plan_t plan, const char **source, const char **compile_log);
+
 /* Device-side status of the plan's kernels on the current device: bit 0 (UVU_DEV_TIMEOUT) is set
  * when a pipelined kernel gave up waiting for a shared-memory stage (about two seconds) and
  * skipped the rest of its work, so its outputs are not valid.  Synchronous: waits for all work
@@ -240,10 +245,13 @@ uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const
  * A NULL cotangent counts as zero; a NULL output is not computed.  grad_x is formed from
  * per-edge contributions summed per sender over the transposed CSR (deterministic) when
  * uvu_conv_hvp_workspace() reports a non-zero size, which needs that much caller workspace;
- * otherwise (plans with several register groups) by atomic adds into a zeroed grad_x.
- * The plan's HVP kernels are compiled on its first HVP call (host, NVRTC) and loaded once per
- * device.  Launches: uvu_hvp_fwd (if grad_d_out), uvu_hvp_edge (if grad_x, grad_Y or grad_w),
- * and the sender-stationary reduction for grad_x. */
+ * otherwise (direct-load plans, U < 32, with several register groups) by atomic adds into a
+ * zeroed grad_x.  The plan's HVP kernels are compiled on its first HVP call (host, NVRTC) and
+ * loaded once per device; for U >= 32 they are the bulk-copy pipelined kernels of the forward
+ * and edge backward with the cotangent rows in the same stages, and their bounded waits report
+ * through uvu_plan_device_status like the plan's other kernels.
+ * Launches: uvu_hvp_fwd (if grad_d_out), uvu_hvp_edge (if grad_x, grad_Y or grad_w), and the
+ * sender-stationary reduction for grad_x. */
 uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
                         const void *Y, const void *w, const int32_t *recv_offsets,
                         const int32_t *src, const int32_t *send_offsets, const int32_t *send_eids,

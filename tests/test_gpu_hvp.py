@@ -2,8 +2,9 @@
 
 The oracle's double backward (oracle.hvp) is pinned by finite differences of its VJP; here the
 CUDA kernels are compared with it element by element on small workloads (including absent
-cotangents and a plan with several register groups, whose grad_x uses atomics) and on sampled
-outputs of the full MACE-medium workload."""
+cotangents, a plan with several register groups whose pipelined edge kernel sums the per-edge
+grad_x partials across groups in shared memory, and a direct-load plan with U < 32) and on
+sampled outputs of the full MACE-medium workload."""
 import numpy as np
 import pytest
 import torch
@@ -56,7 +57,7 @@ def test_tiny_workload_all_outputs():
 
 CUSTOM = [
     ("48x0e+48x1o+48x2e", SH3, 3, "float32", 29, 9),
-    ("64x0e+64x1o+64x2e", SH3, 3, "float64", 17, 6),   # several register groups: atomic grad_x
+    ("64x0e+64x1o+64x2e", SH3, 3, "float64", 17, 6),   # several register groups
     ("8x1o+8x2e", "1x0e+1x1o+1x2e", 4, "float32", 13, 5),
 ]
 

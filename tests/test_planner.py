@@ -61,3 +61,19 @@ def test_plan_is_identical_across_processes():
     outs = [subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, check=True,
                            cwd=__import__("conftest").ROOT).stdout.split() for _ in range(2)]
     assert outs[0] == outs[1] and outs[0][1] == "True"
+
+
+@pytest.mark.parametrize("key", sorted(workloads.SPECS))
+def test_hvp_kernels_build_on_the_host(key):
+    """The double-backward module compiles without a device; plans with U >= 32 get the
+    bulk-copy pipelined kernels (stages carrying the cotangent rows too), smaller ones the
+    direct-load kernels."""
+    spec = workloads.SPECS[key]
+    p = uvu.Plan(spec.irreps_x, spec.irreps_sh, spec.lmax_out, spec.dtype)
+    src, log = p.hvp_source()
+    for k in ("uvu_hvp_fwd", "uvu_hvp_edge"):
+        assert f"Function properties for {k}" in log
+    assert ("cp.async.bulk" in src) == (p.info.mul >= 32)
+    if p.info.mul >= 32:
+        assert "if (hm & 4) bulk_g2s" in src  # aw rows staged only when present
+    assert p.hvp_source()[0] == src  # compiled once per plan
