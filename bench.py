@@ -42,6 +42,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="uvu", choices=["uvu", "reference"])
     ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--nodes", type=int, default=None,
+                    help="node count of the workload (default: the config's); smaller graphs of the "
+                         "same plan serve ncu captures, which must stay a few GB on the device")
     ap.add_argument("--dx-mode", default="staged", choices=["staged", "sender", "atomic"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-chunks", type=int, default=16)
@@ -73,8 +76,8 @@ def algorithmic_bytes(N, E, U, P, Dx, Dy, Do, s):
     }
 
 
-def describe(spec, info, E):
-    return (f"{spec.name}: {spec.n_nodes} nodes, {E} edges, x {spec.irreps_x}, "
+def describe(spec, info, E, N=None):
+    return (f"{spec.name}: {N or spec.n_nodes} nodes, {E} edges, x {spec.irreps_x}, "
             f"SH {spec.irreps_sh}, l3<={spec.lmax_out} ({info.n_paths} paths), {spec.dtype}")
 
 
@@ -238,7 +241,7 @@ def main(argv=None):
 
     from clebsch_gordan_tensor_receiver_gb300 import uvu, workloads
     spec = workloads.SPECS[args.config]
-    wl = workloads.make_workload(spec)
+    wl = workloads.make_workload(spec, args.nodes)
     plan = uvu.Plan(spec.irreps_x, spec.irreps_sh, spec.lmax_out, spec.dtype)
     info = plan.info
     N, E, U, P = wl.n_nodes, wl.n_edges, info.mul, info.n_paths
@@ -387,7 +390,7 @@ def main(argv=None):
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64" if s == 8 else "f32", "data": "synthetic",
-        "config": {"workload": describe(spec, info, E), "n_nodes": N, "n_edges": E,
+        "config": {"workload": describe(spec, info, E, N), "n_nodes": N, "n_edges": E,
                    "dx_mode": args.dx_mode, "parallelism": "replicas" if world > 1 else "single",
                    "l2": "inputs larger than L2 (w alone is %.2f GB), no flush" % (E * P * U * s / 1e9)},
         "fwd": {"edges_per_s": world * E / (fwd_ms / 1000), "ms": fwd_ms, "GB_s": fwd_gbs,
