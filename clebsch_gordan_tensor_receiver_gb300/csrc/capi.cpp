@@ -53,16 +53,17 @@ uvu_status check_sizes(int64_t N, int64_t E) {
         if (_s != UVU_OK) return _s;          \
     } while (0)
 
+// Grid of a launch: persistent kernels get the resident blocks (at most max_blocks), the others
+// one block per owners_per_block owners.
+int64_t grid_blocks(int occ, int sm_count, int64_t owners, const KernelGeom& g, int64_t max_blocks) {
+    if (g.persistent) return std::min(std::min<int64_t>(owners * g.tiles, int64_t(occ) * sm_count), max_blocks);
+    return (owners + g.owners_per_block - 1) / g.owners_per_block;
+}
+
 uvu_status launch(cudaKernel_t k, int occ, int sm_count, int64_t owners, const KernelGeom& g, void** args,
-                  cudaStream_t st, const char* what) {
+                  cudaStream_t st, const char* what, int64_t max_blocks = INT64_MAX) {
     if (owners <= 0) return UVU_OK;
-    int64_t blocks;
-    if (g.persistent) {
-        const int64_t items = owners * g.tiles;
-        blocks = std::min<int64_t>(items, int64_t(occ) * sm_count);
-    } else {
-        blocks = (owners + g.owners_per_block - 1) / g.owners_per_block;
-    }
+    const int64_t blocks = grid_blocks(occ, sm_count, owners, g, max_blocks);
     cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(k), dim3(unsigned(blocks)),
                                      dim3(unsigned(g.threads)), args, g.smem, st);
     if (e != cudaSuccess) return cuda_fail(e, what);
@@ -123,7 +124,8 @@ extern "C" uvu_status uvu_plan_destroy(uvu_plan_t plan) {
         int cur = 0;
         if (cudaGetDevice(&cur) == cudaSuccess && cur != kv.first) cudaSetDevice(kv.first);
         cudaLibraryUnload(kv.second.lib);
-        if (kv.second.hvp_lib) cudaLibraryUnload(kv.second.hvp_lib);
+        for (auto& a : kv.second.aux)
+            if (a.lib) cudaLibraryUnload(a.lib);
         if (cur != kv.first) cudaSetDevice(cur);
     }
     delete plan;
@@ -164,14 +166,18 @@ extern "C" uvu_status uvu_plan_source(uvu_plan_t plan, const char** source, cons
     return ok();
 }
 
-extern "C" uvu_status uvu_plan_hvp_source(uvu_plan_t plan, const char** source, const char** log) {
+extern "C" uvu_status uvu_plan_module_source(uvu_plan_t plan, uvu_module module, const char** source, const char** log) {
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    if (module == UVU_MODULE_CONV) return uvu_plan_source(plan, source, log);
+    const int kind = module == UVU_MODULE_HVP ? AUX_HVP : module == UVU_MODULE_TP ? AUX_TP
+                   : module == UVU_MODULE_TP_SHARED ? AUX_TP_SHARED : -1;
+    if (kind < 0) return fail(UVU_ERR_INVALID_ARGUMENT, "unknown module");
     std::string err;
-    uvu_status s = compile_hvp(p, &err);
+    uvu_status s = compile_aux(p, kind, &err);
     if (s != UVU_OK) return fail(s, err);
-    if (source) *source = p->hvp_source.c_str();
-    if (log) *log = p->hvp_log.c_str();
+    if (source) *source = p->aux[kind].source.c_str();
+    if (log) *log = p->aux[kind].log.c_str();
     return ok();
 }
 
@@ -385,16 +391,17 @@ extern "C" uvu_status uvu_plan_device_status(uvu_plan_t plan, unsigned* word, in
     uvu_status s = module_for_current_device(p, &m, &err);
     if (s != UVU_OK) return fail(s, err);
     cudaError_t e = cudaMemcpy(word, m->status_word, sizeof(unsigned), cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess && m->hvp_status_word) {  // the double-backward module's own word
+    for (auto& a : m->aux) {  // the auxiliary modules' own words
+        if (e != cudaSuccess || !a.status_word) continue;
         unsigned w2 = 0;
-        e = cudaMemcpy(&w2, m->hvp_status_word, sizeof(unsigned), cudaMemcpyDeviceToHost);
+        e = cudaMemcpy(&w2, a.status_word, sizeof(unsigned), cudaMemcpyDeviceToHost);
         *word |= w2;
     }
     if (e == cudaSuccess && reset) {
         const unsigned zero = 0;
         e = cudaMemcpy(m->status_word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
-        if (e == cudaSuccess && m->hvp_status_word)
-            e = cudaMemcpy(m->hvp_status_word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
+        for (auto& a : m->aux)
+            if (e == cudaSuccess && a.status_word) e = cudaMemcpy(a.status_word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
     }
     if (e != cudaSuccess) return cuda_fail(e, "status word copy");
     return ok();
@@ -447,13 +454,15 @@ extern "C" uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
     }
     DeviceModule* m = nullptr;
     std::string err;
-    uvu_status s = hvp_module_for_current_device(p, &m, &err);
+    uvu_status s = aux_module_for_current_device(p, AUX_HVP, &m, &err);
     if (s != UVU_OK) return fail(s, err);
+    const AuxLoaded& L = m->aux[AUX_HVP];
+    const AuxBuild& A = p->aux[AUX_HVP];
     const int hm = (ax ? 1 : 0) | (aY ? 2 : 0) | (aw ? 4 : 0);
     long long N = n_nodes;
     if (grad_d_out) {
         void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &ax, &aY, &aw, const_cast<int*>(&hm), &grad_d_out};
-        UVU_TRY(launch(m->hvp_fwd, m->occ_hvp_fwd, m->sm_count, n_nodes, p->g_hvp_fwd, args, stream, "uvu_hvp_fwd launch"));
+        UVU_TRY(launch(L.k[0], L.occ[0], m->sm_count, n_nodes, A.g[0], args, stream, "uvu_hvp_fwd launch"));
     }
     if (!need_edge) return ok();
     void* dx_atomic = (grad_x && !staged) ? grad_x : nullptr;
@@ -465,8 +474,104 @@ extern "C" uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
     if (n_edges > 0) {
         void* args[] = {&N, &recv_offsets, &src, &x, &Y, &w, &d_out, &ax, &aY, &aw, const_cast<int*>(&hm),
                         &grad_Y, &grad_w, &dx_atomic, &dx_edge};
-        UVU_TRY(launch(m->hvp_edge, m->occ_hvp_edge, m->sm_count, n_nodes, p->g_hvp_edge, args, stream, "uvu_hvp_edge launch"));
+        UVU_TRY(launch(L.k[1], L.occ[1], m->sm_count, n_nodes, A.g[1], args, stream, "uvu_hvp_edge launch"));
     }
     if (staged) UVU_TRY(uvu_conv_bwd_dx_reduce(plan, n_nodes, n_edges, send_offsets, send_eids, workspace, grad_x, stream));
+    return ok();
+}
+
+// ------------------------------------------------------------- batched tensor product (no graph)
+
+namespace uvu {
+namespace {
+// Grid cap of the batch-shared-weight edge kernel: bounds the rows of its partial-dw workspace.
+constexpr int64_t kTpMaxBlocks = 2048;
+
+uvu_status tp_check(Plan* p, int64_t batch) {
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    if (batch < 0 || batch > INT32_MAX - 1) return fail(UVU_ERR_INVALID_ARGUMENT, "batch must be in [0, 2^31 - 1)");
+    if (!p->pipelined_recv)
+        return fail(UVU_ERR_UNSUPPORTED, "the batched tensor product needs a plan whose kernels are pipelined (U >= 32)");
+    return UVU_OK;
+}
+}  // namespace
+}  // namespace uvu
+
+extern "C" uvu_status uvu_tp_bwd_workspace(uvu_plan_t plan, int64_t batch, int w_shared, size_t* bytes) {
+    Plan* p = get(plan);
+    if (!bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    UVU_TRY(tp_check(p, batch));
+    *bytes = w_shared ? size_t(std::min<int64_t>(batch, kTpMaxBlocks)) * p->P * p->U * sizeof(double) : 0;
+    return ok();
+}
+
+extern "C" uvu_status uvu_tp_fwd(uvu_plan_t plan, int64_t batch, const void* x, const void* y, const void* w,
+                                 int w_shared, void* out, uvu_stream_t stream) {
+    Plan* p = get(plan);
+    UVU_TRY(tp_check(p, batch));
+    if (batch == 0) return ok();
+    UVU_TRY(need(out, "out"));
+    UVU_TRY(need(x, "x"));
+    UVU_TRY(need(y, "y"));
+    UVU_TRY(need(w, "w"));
+    const int kind = w_shared ? AUX_TP_SHARED : AUX_TP;
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = aux_module_for_current_device(p, kind, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    long long N = batch;
+    const int32_t* none = nullptr;
+    void* args[] = {&N, &none, &none, &x, &y, &w, &out};
+    return launch(m->aux[kind].k[0], m->aux[kind].occ[0], m->sm_count, batch, p->aux[kind].g[0], args, stream,
+                  "uvu_tp_fwd launch");
+}
+
+extern "C" uvu_status uvu_tp_bwd(uvu_plan_t plan, int64_t batch, const void* x, const void* y, const void* w,
+                                 int w_shared, const void* d_out, void* dx, void* dy, void* dw, void* workspace,
+                                 size_t workspace_bytes, uvu_stream_t stream) {
+    Plan* p = get(plan);
+    UVU_TRY(tp_check(p, batch));
+    UVU_TRY(opt(dx, "dx"));
+    UVU_TRY(opt(dy, "dy"));
+    UVU_TRY(opt(dw, "dw"));
+    if (!dx && !dy && !dw) return ok();
+    const size_t wsz = size_t(p->P) * p->U * p->elem();
+    if (batch == 0) {  // a shared dw over an empty batch is zero
+        if (dw && w_shared) {
+            cudaError_t e = cudaMemsetAsync(dw, 0, wsz, stream);
+            if (e != cudaSuccess) return cuda_fail(e, "dw memset");
+        }
+        return ok();
+    }
+    UVU_TRY(need(x, "x"));
+    UVU_TRY(need(y, "y"));
+    UVU_TRY(need(w, "w"));
+    UVU_TRY(need(d_out, "d_out"));
+    size_t ws_need = 0;
+    UVU_TRY(uvu_tp_bwd_workspace(plan, batch, w_shared, &ws_need));
+    const bool partials = w_shared && dw;
+    if (partials) {
+        if (!workspace || workspace_bytes < ws_need)
+            return fail(UVU_ERR_INVALID_ARGUMENT, "a shared-weight dw needs a workspace of uvu_tp_bwd_workspace() bytes");
+        UVU_TRY(need(workspace, "workspace"));
+    }
+    const int kind = w_shared ? AUX_TP_SHARED : AUX_TP;
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = aux_module_for_current_device(p, kind, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    const AuxLoaded& L = m->aux[kind];
+    const AuxBuild& A = p->aux[kind];
+    long long N = batch;
+    const int32_t* none = nullptr;
+    void* dw_arg = partials ? workspace : dw;
+    void* dx_atomic = nullptr;
+    void* args[] = {&N, &none, &none, &x, &y, &w, &d_out, &dy, &dw_arg, &dx_atomic, &dx};
+    UVU_TRY(launch(L.k[1], L.occ[1], m->sm_count, batch, A.g[1], args, stream, "uvu_tp_edge launch", kTpMaxBlocks));
+    if (partials) {
+        const int64_t rows = grid_blocks(L.occ[1], m->sm_count, batch, A.g[1], kTpMaxBlocks);
+        cudaError_t e = launch_column_sum(workspace, rows, int64_t(p->P) * p->U, dw, p->dtype == UVU_F64, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "dw column sum launch");
+    }
     return ok();
 }

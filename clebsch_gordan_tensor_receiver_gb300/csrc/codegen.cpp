@@ -47,12 +47,15 @@ struct Src {
 
 std::string fmt(const char* f, ...) __attribute__((format(printf, 1, 2)));
 std::string fmt(const char* f, ...) {
-    char buf[512];
-    va_list ap;
+    va_list ap, ap2;
     va_start(ap, f);
-    vsnprintf(buf, sizeof buf, f, ap);
+    va_copy(ap2, ap);
+    const int n = vsnprintf(nullptr, 0, f, ap);
     va_end(ap);
-    return buf;
+    std::string out(n > 0 ? size_t(n) : 0, '\0');
+    if (n > 0) vsnprintf(&out[0], size_t(n) + 1, f, ap2);  // writes the terminator into the spare byte
+    va_end(ap2);
+    return out;
 }
 
 struct Gen {
@@ -76,6 +79,13 @@ struct Gen {
     // Set while emitting the double-backward kernels, whose operands are sums of products and
     // therefore always take the generic path.
     mutable bool no_identity = false;
+    // dw of a path: stored per edge (dwe[p * U]) or, for weights shared by a whole batch,
+    // accumulated in fp64 in the thread's registers (dwa_p) over the samples it processes (a sum
+    // over many samples: fp32 accumulation lost digits where the terms cancel)
+    mutable bool dw_accum = false;
+    std::string dw_store(int pi, const std::string& v) const {
+        return dw_accum ? fmt("dwa_%d += (double)(%s);", pi, v.c_str()) : fmt("dwe[%d * UVU_U] = %s;", pi, v.c_str());
+    }
 
     bool is_identity(const PathInfo& p) const {
         if (no_identity) return false;
@@ -266,8 +276,7 @@ struct Gen {
                                 S(fmt("z_%d = fma(%s%s, %s, z_%d);", pi, z.c < 0 ? "-" : "", gv.c_str(), other.c_str(), pi));
                             }
                         }
-                        S(fmt("dwe[%d * UVU_U] = z_%d * %s;", pi, pi,
-                              scal_x ? fmt("xv_%d", p.xoff).c_str() : fmt("yv_%d", p.yoff).c_str()));
+                        S(dw_store(pi, fmt("z_%d * %s", pi, scal_x ? fmt("xv_%d", p.xoff).c_str() : fmt("yv_%d", p.yoff).c_str())));
                     } else {
                         S("{");
                         S.ind++;
@@ -278,7 +287,7 @@ struct Gen {
                             else
                                 S(fmt("z = fma(%s, t_%d_%d, z);", gval(p.ooff + m3).c_str(), pi, m3));
                         }
-                        S(fmt("dwe[%d * UVU_U] = z;", pi));
+                        S(dw_store(pi, "z"));
                         S.ind--;
                         S("}");
                     }
@@ -803,6 +812,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         bool ovec = false;  // staged block copied out with 16-byte vectors
         bool gst = false;  // the receiver's d_out block is bulk-copied into shared memory
         bool dual = false;  // double backward: the stage also holds the cotangent rows aw, ax, aY
+        bool tp = false;    // batched tensor product: sample b is receiver b with the one edge b, sender b
+        bool wsh = false;   // weights [P][U] shared by the batch: not staged, read once per sample
         size_t aw_off = 0, ax_off = 0, ay_off = 0;
         size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, xpart_off = 0, out_off = 0, total = 0;
         size_t g_off = 0, gbytes = 0;
@@ -811,18 +822,22 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
 
     RecvPipe recv_pipe(bool with_partials, int ncw, bool stage_out = false, int ch = 0, bool stage_g = false,
-                       bool dual = false) const {
+                       bool dual = false, bool tp = false, bool wsh = false) const {
         RecvPipe R;
         R.dual = dual;
+        R.tp = tp;
+        R.wsh = wsh;
         R.xbulk = xbytes() % 16 == 0;
         R.ybulk = ybytes() % 16 == 0;
         const int NG = int(P->groups.size());
-        const size_t pe = (wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0)) * (dual ? 2 : 1);
-        const bool chosen = ch > 0 || std::getenv("UVU_PIPE_CH");
+        const size_t wb = wsh ? 0 : wbytes();  // staged weight bytes per edge
+        const size_t pe = std::max<size_t>(16, (wb + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0)) * (dual ? 2 : 1));
+        const bool chosen = ch > 0 || std::getenv("UVU_PIPE_CH") || tp;
         R.ch = ch > 0 ? ch : int(std::max<size_t>(1, std::min<size_t>(8, 32768 / pe)));
         if (const char* e = std::getenv("UVU_PIPE_CH")) R.ch = std::max(1, std::atoi(e));
-        const size_t stage = (a16(R.ch * wbytes()) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
-                              (R.ybulk ? a16(R.ch * ybytes()) : 0)) * (dual ? 2 : 1);
+        if (tp) R.ch = 1;  // one edge per receiver
+        const size_t stage = std::max<size_t>(16, (a16(R.ch * wb) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
+                                                   (R.ybulk ? a16(R.ch * ybytes()) : 0)) * (dual ? 2 : 1));
         // per-stage partial sums of the edge kernel: dY over warps, dx over register groups
         const size_t dyp = with_partials ? a16(2 * size_t(ncw) * R.ch * P->Dy * P->elem()) : 0;
         const size_t dxp = (with_partials && NG > 1) ? a16(2 * size_t(NG) * R.ch * P->U_pad * P->Dx * P->elem()) : 0;
@@ -833,7 +848,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         if (const char* e = std::getenv("UVU_PIPE_PF")) R.pf = std::max(0, std::atoi(e));
         R.w_off = 0;
         R.aw_off = dual ? a16(R.ch * wbytes()) : 0;
-        R.x_off = (dual ? 2 : 1) * a16(R.ch * wbytes());
+        R.x_off = (dual ? 2 : 1) * a16(R.ch * wb);
         R.ax_off = R.x_off + ((dual && R.xbulk) ? a16(R.ch * xbytes()) : 0);
         R.y_off = R.x_off + (R.xbulk ? (dual ? 2 : 1) * a16(R.ch * xbytes()) : 0);
         R.ay_off = R.y_off + ((dual && R.ybulk) ? a16(R.ch * ybytes()) : 0);
@@ -857,19 +872,19 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         R.total = R.out_off + (stage_out ? a16(size_t(P->U) * R.odp * P->elem()) : 0);
         R.g_off = R.total;
         if (R.gst) R.total += a16(R.gbytes);
-        R.tx_per_edge = wbytes() + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
+        R.tx_per_edge = wb + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
         // With a receiver block staged, shorter stages keep three blocks resident per SM where
         // the default chunk would leave fewer (more warps beat a longer look-ahead per block).
         if ((stage_out || R.gst) && !chosen && R.ch > 1 && minb(R.total) < 3)
-            return recv_pipe(with_partials, ncw, stage_out, R.ch - 1, stage_g, dual);
+            return recv_pipe(with_partials, ncw, stage_out, R.ch - 1, stage_g, dual, tp, wsh);
         // a staged block that does not fit next to the stages is not staged
-        if (R.total > 227 * 1024 && R.gst) return recv_pipe(with_partials, ncw, stage_out, ch, false, dual);
-        if (R.total > 227 * 1024 && stage_out) return recv_pipe(with_partials, ncw, false, ch, stage_g, dual);
+        if (R.total > 227 * 1024 && R.gst) return recv_pipe(with_partials, ncw, stage_out, ch, false, dual, tp, wsh);
+        if (R.total > 227 * 1024 && stage_out) return recv_pipe(with_partials, ncw, false, ch, stage_g, dual, tp, wsh);
         return R;
     }
 
-    // slot: the kernel's entry in the plan's register-budget tables (0 fwd, 1 edge, 3 hvp_fwd, 4 hvp_edge)
-    void emit_recv_pipe_defines(Src& S, const RecvPipe& R, const char* pre, int slot) const {
+    // cap / eff: the kernel's entries in its register-budget tables (blocks per SM allowed, used)
+    void emit_recv_pipe_defines(Src& S, const RecvPipe& R, const char* pre, int& cap, int& eff) const {
         S(fmt("#define %s_CH %d", pre, R.ch));
         S(fmt("#define %s_NST %d", pre, R.nst));
         S(fmt("#define %s_STAGE %zu", pre, R.stage));
@@ -887,8 +902,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S(fmt("#define %s_AXOFF %zu", pre, R.ax_off));
         S(fmt("#define %s_AYOFF %zu", pre, R.ay_off));
         S(fmt("#define %s_ODP %d", pre, R.odp));
-        const int mb = std::min(minb(R.total), P->minb[slot]);
-        P->minb_eff[slot] = mb;
+        const int mb = std::min(minb(R.total), cap);
+        eff = mb;
         S(fmt("#define %s_MINB %d", pre, mb));
     }
     // Blocks per SM the shared-memory footprint allows (capped at 4); UVU_PIPE_MINB (a tuning
@@ -904,6 +919,15 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     // The sender ids of the next chunk and the offsets of the next receiver are loaded one step
     // ahead, before the current chunk's copies are issued: the copies are asm statements with a
     // memory clobber, so a load placed after one of them would wait its full latency in line.
+    // Receiver offsets and sender ids: from the CSR, or the identity for the batched tensor
+    // product (sample b = receiver b with the single edge b from sender b).
+    static std::string off_at(const RecvPipe& R, const std::string& r) {
+        return R.tp ? "(int)(" + r + ")" : "__ldg(off + " + r + ")";
+    }
+    static std::string src_at(const RecvPipe& R, const std::string& e) {
+        return R.tp ? "(" + e + ")" : "__ldg(src + " + e + ")";
+    }
+
     void emit_recv_producer(Src& S, const RecvPipe& R, const char* pre, const char* name) const {
         const int CH = R.ch;
         S(fmt("__device__ __noinline__ void %s(long long N, const int* __restrict__ off, const int* __restrict__ src,", name));
@@ -924,9 +948,9 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("const long long G = gridDim.x;");
         S("long long r = blockIdx.x;");
         S("int eb = 0, e1 = 0, nb = 0, n1 = 0;");
-        S("if (r < N) { eb = __ldg(off + r); e1 = __ldg(off + r + 1); }");
-        S("if (r + G < N) { nb = __ldg(off + r + G); n1 = __ldg(off + r + G + 1); }");
-        for (int j = 0; j < CH; ++j) S(fmt("int sv%d = (%d < e1 - eb) ? __ldg(src + eb + %d) : 0;", j, j, j));
+        S("if (r < N) { eb = " + off_at(R, "r") + "; e1 = " + off_at(R, "r + 1") + "; }");
+        S("if (r + G < N) { nb = " + off_at(R, "r + G") + "; n1 = " + off_at(R, "r + G + 1") + "; }");
+        for (int j = 0; j < CH; ++j) S(fmt("int sv%d = (%d < e1 - eb) ? %s : 0;", j, j, src_at(R, fmt("eb + %d", j)).c_str()));
         S("while (r < N && !dead) {");
         S.ind++;
         S("if (eb >= e1) {  // receiver done (or empty): move to the next one");
@@ -935,14 +959,15 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("if (r >= N) break;");
         S("eb = nb; e1 = n1;");
         if (R.gst) S("fresh = true;");
-        S("if (r + G < N) { nb = __ldg(off + r + G); n1 = __ldg(off + r + G + 1); }");
-        for (int j = 0; j < CH; ++j) S(fmt("sv%d = (%d < e1 - eb) ? __ldg(src + eb + %d) : 0;", j, j, j));
+        S("if (r + G < N) { nb = " + off_at(R, "r + G") + "; n1 = " + off_at(R, "r + G + 1") + "; }");
+        for (int j = 0; j < CH; ++j) S(fmt("sv%d = (%d < e1 - eb) ? %s : 0;", j, j, src_at(R, fmt("eb + %d", j)).c_str()));
         S("continue;");
         S.ind--;
         S("}");
         S(fmt("const int ne = min(%s_CH, e1 - eb);", pre));
         S(fmt("const int ebn = eb + %s_CH;", pre));
-        for (int j = 0; j < CH; ++j) S(fmt("const int svn%d = (ebn + %d < e1) ? __ldg(src + ebn + %d) : 0;", j, j, j));
+        for (int j = 0; j < CH; ++j)
+            S(fmt("const int svn%d = (ebn + %d < e1) ? %s : 0;", j, j, src_at(R, fmt("ebn + %d", j)).c_str()));
         if (R.pf > 0) {
             // L2 prefetch of the w (and Y) rows R.pf chunks ahead, in this receiver or the next
             S(fmt("{ int pa = eb + %d, pb; bool ok = true;", R.pf * CH));
@@ -972,7 +997,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S(fmt("const unsigned stg = sbase + st * %s_STAGE;", pre));
         if (R.dual) S("mbar_expect_tx(full, (unsigned)ne * txe);");
         else S(fmt("mbar_expect_tx(full, (unsigned)ne * %s_TX);", pre));
-        S(fmt("bulk_g2s(stg, w + (size_t)eb * (UVU_P * UVU_U), (unsigned)ne * %zuu, full);", wbytes()));
+        if (!R.wsh) S(fmt("bulk_g2s(stg, w + (size_t)eb * (UVU_P * UVU_U), (unsigned)ne * %zuu, full);", wbytes()));
         if (R.dual) S(fmt("if (hm & 4) bulk_g2s(stg + %s_AWOFF, aw + (size_t)eb * (UVU_P * UVU_U), (unsigned)ne * %zuu, full);", pre, wbytes()));
         if (R.ybulk) S(fmt("bulk_g2s(stg + %s_YOFF, Y + (size_t)eb * UVU_DY, (unsigned)ne * %zuu, full);", pre, ybytes()));
         if (R.ybulk && R.dual) S(fmt("if (hm & 2) bulk_g2s(stg + %s_AYOFF, aY + (size_t)eb * UVU_DY, (unsigned)ne * %zuu, full);", pre, ybytes()));
@@ -1007,7 +1032,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             emit_row_loads(S, "xv", fmt("reinterpret_cast<const %s*>(stg + %s_XOFF) + (j * UVU_U + u) * UVU_DX", T.c_str(), pre),
                            P->Dx, xn, false);
         } else {
-            S("const int s = __ldg(src + e);");
+            S("const int s = " + src_at(R, "e") + ";");
             emit_row_loads(S, "xv", "x + ((size_t)s * UVU_U + u) * UVU_DX", P->Dx, xn);
         }
         if (R.ybulk)
@@ -1015,8 +1040,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                            false);
         else
             emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
-        S(fmt("const %s* swr = reinterpret_cast<const %s*>(stg) + j * (UVU_P * UVU_U) + u;", T.c_str(), T.c_str()));
-        for (int pi : paths) S(fmt("const %s wv_%d = swr[%d * UVU_U];", T.c_str(), pi, pi));
+        if (R.wsh) {  // batch-shared weights: the channel's row, cached by L1 across samples
+            for (int pi : paths) S(fmt("const %s wv_%d = __ldg(w + %d * UVU_U + u);", T.c_str(), pi, pi));
+        } else {
+            S(fmt("const %s* swr = reinterpret_cast<const %s*>(stg) + j * (UVU_P * UVU_U) + u;", T.c_str(), T.c_str()));
+            for (int pi : paths) S(fmt("const %s wv_%d = swr[%d * UVU_U];", T.c_str(), pi, pi));
+        }
         if (!R.dual) return;
         // cotangent rows of the double backward; absent ones (mask hm) read as zero
         if (R.xbulk) {
@@ -1049,7 +1078,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S(fmt("__device__ __forceinline__ void fwd_rcv%d(int e0, int e1, int u, bool uvalid, int lane, unsigned& c, bool& dead,", g));
             S(fmt("    const unsigned char* smem, unsigned sbase, const int* __restrict__ src, const %s* __restrict__ x,", T.c_str()));
             if (R.dual) S(fmt("    const %s* __restrict__ ax, const %s* __restrict__ aY, int hm,", T.c_str(), T.c_str()));
-            S(fmt("    const %s* __restrict__ Y, %s* __restrict__ orow) {", T.c_str(), T.c_str()));
+            S(fmt("    const %s* __restrict__ Y, const %s* __restrict__ w, %s* __restrict__ orow) {", T.c_str(), T.c_str(), T.c_str()));
             S.ind++;
             for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
             S("for (int eb = e0; eb < e1; eb += FW_CH, ++c) {");
@@ -1085,7 +1114,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("}");
         }
         S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, FW_MINB) %s(long long N, const int* __restrict__ off,",
-              R.dual ? "uvu_hvp_fwd" : "uvu_fwd"));
+              R.dual ? "uvu_hvp_fwd" : R.tp ? (R.wsh ? "uvu_tp_fwd_sh" : "uvu_tp_fwd") : "uvu_fwd"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
         if (R.dual)
             S(fmt("    const %s* __restrict__ w, const %s* __restrict__ ax, const %s* __restrict__ aY, const %s* __restrict__ aw, int hm,",
@@ -1114,10 +1143,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         if (R.odp == 0) {
             S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
             S.ind++;
-            S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+            S("const int e0 = " + off_at(R, "r") + ", e1 = " + off_at(R, "r + 1") + ";");
             S(T + "* orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
             for (int g = 0; g < NG; ++g)
-                S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, %sY, orow);", g ? "else " : "", g, g,
+                S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, %sY, w, orow);", g ? "else " : "", g, g,
                       R.dual ? "ax, aY, hm, " : ""));
             S.ind--;
             S("}");
@@ -1130,10 +1159,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         if (R.ovec) S("const bool ovec = (reinterpret_cast<size_t>(out) & 15) == 0;");
         S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
         S.ind++;
-        S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+        S("const int e0 = " + off_at(R, "r") + ", e1 = " + off_at(R, "r + 1") + ";");
         S("consumer_sync();  // the previous receiver's block has been copied out of sout");
         for (int g = 0; g < NG; ++g)
-            S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, %sY, orow);", g ? "else " : "", g, g,
+            S(fmt("%sif (g == %d) fwd_rcv%d(e0, e1, u, uvalid, lane, c, dead, smem, sbase, src, x, %sY, w, orow);", g ? "else " : "", g, g,
                   R.dual ? "ax, aY, hm, " : ""));
         S("consumer_sync();");
         S(fmt("%s* const og = out + (size_t)r * (UVU_U * UVU_DO);", T.c_str()));
@@ -1214,6 +1243,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
 
     void emit_edge_v2(Src& S, const RecvPipe& R) const {
         const int NG = int(P->groups.size());
+        dw_accum = R.wsh;
         emit_recv_producer(S, R, "EG", "edge_producer");
         for (int g = 0; g < NG; ++g) {
             const std::vector<int>& paths = P->groups[g];
@@ -1227,7 +1257,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             if (R.dual) S(fmt("    const %s* __restrict__ ax, const %s* __restrict__ aY, int hm,", T.c_str(), T.c_str()));
             S(fmt("    const %s* __restrict__ gout, %s* __restrict__ dY, %s* __restrict__ dw, %s* __restrict__ dx,",
                   T.c_str(), T.c_str(), T.c_str(), T.c_str()));
-            S(fmt("    %s* __restrict__ dxe, int g) {", T.c_str()));
+            std::string dwa;
+            if (R.wsh)
+                for (int pi : paths) dwa += fmt(", double& dwa_%d", pi);
+            S(fmt("    %s* __restrict__ dxe, int g, const %s* __restrict__ w%s) {", T.c_str(), T.c_str(), dwa.c_str()));
             S.ind++;
             if (R.gst) {
                 // d_out row of this channel from the receiver's staged block; the block buffer
@@ -1272,7 +1305,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("if (uvalid) {");
             S.ind++;
             emit_stage_edge_loads(S, R, "EG", xn, yn, paths);
-            S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
+            if (!R.wsh) S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
             for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
             auto gval = [](int k) { return fmt("gv_%d", k); };
             if (R.dual) {
@@ -1300,7 +1333,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             if (!R.xbulk) {
                 S(T + "* __restrict__ dxr = dx + ((size_t)s * UVU_U + u) * UVU_DX;");
             } else {
-                S("const int s = __ldg(src + e);");
+                S("const int s = " + src_at(R, "e") + ";");
                 S(T + "* __restrict__ dxr = dx + ((size_t)s * UVU_U + u) * UVU_DX;");
             }
             emit_dx_atomics(S, xn);
@@ -1363,7 +1396,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("}");
         }
         S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, EG_MINB) %s(long long N, const int* __restrict__ off,",
-              R.dual ? "uvu_hvp_edge" : "uvu_bwd_edge"));
+              R.dual ? "uvu_hvp_edge" : R.tp ? (R.wsh ? "uvu_tp_edge_sh" : "uvu_tp_edge") : "uvu_bwd_edge"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
         if (R.dual)
             S(fmt("    const %s* __restrict__ w, const %s* __restrict__ gout, const %s* __restrict__ ax, const %s* __restrict__ aY,\n"
@@ -1393,16 +1426,33 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("unsigned c = 0, kg = 0;");
         S("bool dead = false;");
         S("int buf = 0;");
+        if (R.wsh)  // dw of batch-shared weights: this block's sum over its samples, per thread
+            for (int pi = 0; pi < P->P; ++pi) S(fmt("double dwa_%d = 0;", pi));
         S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
         S.ind++;
-        S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
-        for (int g = 0; g < NG; ++g)
-            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, kg, dead, buf, smem, sbase, src, x, Y, %sgout, dY, dw, dx, dxe, g);",
-                  g ? "else " : "", g, g, R.dual ? "ax, aY, hm, " : ""));
+        S("const int e0 = " + off_at(R, "r") + ", e1 = " + off_at(R, "r + 1") + ";");
+        for (int g = 0; g < NG; ++g) {
+            std::string dwa;
+            if (R.wsh)
+                for (int pi : P->groups[g]) dwa += fmt(", dwa_%d", pi);
+            S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, kg, dead, buf, smem, sbase, src, x, Y, %sgout, dY, dw, dx, dxe, g, w%s);",
+                  g ? "else " : "", g, g, R.dual ? "ax, aY, hm, " : "", dwa.c_str()));
+        }
         S.ind--;
         S("}");
+        if (R.wsh) {  // the block's partial dw [P][U] in fp64 (row blockIdx.x of the caller's workspace)
+            S("if (dw && uvalid) {");
+            S("  double* __restrict__ pr = reinterpret_cast<double*>(dw) + (size_t)blockIdx.x * (UVU_P * UVU_U) + u;");
+            for (int g = 0; g < NG; ++g) {
+                std::string st;
+                for (int pi : P->groups[g]) st += fmt(" pr[%d * UVU_U] = dwa_%d;", pi, pi);
+                S(fmt("  %sif (g == %d) {%s }", g ? "else " : "", g, st.c_str()));
+            }
+            S("}");
+        }
         S.ind--;
         S("}");
+        dw_accum = false;
     }
 
     // Per-edge dx contribution of this thread's channel, for the deterministic (staged) dx:
@@ -1790,8 +1840,8 @@ std::string emit_source(Plan* plan) {
     S("}");
     G.emit_pipe_helpers(S);
     if (pipe_recv) {
-        G.emit_recv_pipe_defines(S, RF, "FW", 0);
-        G.emit_recv_pipe_defines(S, RE, "EG", 1);
+        G.emit_recv_pipe_defines(S, RF, "FW", plan->minb[0], plan->minb_eff[0]);
+        G.emit_recv_pipe_defines(S, RE, "EG", plan->minb[1], plan->minb_eff[1]);
         G.emit_fwd_v2(S, RF);
         G.emit_edge_v2(S, RE);
     } else {
@@ -1856,8 +1906,17 @@ namespace uvu {
 // Source of the plan's second module: the double-backward (HVP) kernels, compiled on the first
 // HVP call so that plans used only for the forward and the VJP do not pay for them.  They use
 // the direct-load structure and the plan's register groups.
-std::string emit_hvp_source(Plan* plan) {
+const char* const kAuxKernelNames[AUX_COUNT][2] = {
+    {"uvu_hvp_fwd", "uvu_hvp_edge"}, {"uvu_tp_fwd", "uvu_tp_edge"}, {"uvu_tp_fwd_sh", "uvu_tp_edge_sh"}};
+
+// Source of an auxiliary module: the double backward (AUX_HVP) or the batched tensor product
+// with per-sample (AUX_TP) or batch-shared (AUX_TP_SHARED) weights.  For U >= 32 these are the
+// pipelined receiver kernels in their dual-operand / single-edge-receiver variants; the double
+// backward of smaller plans uses the direct-load kernels, and the batched tensor product needs
+// the pipelined plan (the C ABI refuses it otherwise).
+std::string emit_aux_source(Plan* plan, int kind) {
     Gen G{plan, plan->dtype == UVU_F64, plan->dtype == UVU_F64 ? "double" : "float"};
+    AuxBuild& A = plan->aux[kind];
     const int U = plan->U, NG = int(plan->groups.size()), UP = plan->U_pad;
     const int owner_threads = UP * NG;
     const int rpb = std::max(1, 128 / owner_threads);
@@ -1865,23 +1924,23 @@ std::string emit_hvp_source(Plan* plan) {
     const int segs = NG * ((UP + 31) / 32);
     const int ch = 16;
     const int ncw = NG * UP / 32;
-    // Same kernels as the pipelined forward and edge backward, with stages that also carry the
-    // cotangent rows (aw, aY, ax); otherwise the direct-load kernels.
     const bool pipe = plan->pipelined_recv;
     const bool ostage = !(std::getenv("UVU_PIPE_OSTAGE") && std::atoi(std::getenv("UVU_PIPE_OSTAGE")) == 0);
     const bool gstage = !(std::getenv("UVU_PIPE_GSTAGE") && std::atoi(std::getenv("UVU_PIPE_GSTAGE")) == 0);
+    const bool hvp = kind == AUX_HVP, tp = !hvp, wsh = kind == AUX_TP_SHARED;
     Gen::RecvPipe RF, RE;
     if (pipe) {
-        RF = G.recv_pipe(false, ncw, ostage, 0, false, true);
-        RE = G.recv_pipe(true, ncw, false, 0, gstage, true);
-        plan->g_hvp_fwd = {ncw * 32 + 32, 1, RF.total, true};
-        plan->g_hvp_edge = {ncw * 32 + 32, 1, RE.total, true};
+        RF = G.recv_pipe(false, ncw, ostage, 0, false, hvp, tp, wsh);
+        RE = G.recv_pipe(true, ncw, false, 0, gstage, hvp, tp, wsh);
+        A.g[0] = {ncw * 32 + 32, 1, RF.total, true};
+        A.g[1] = {ncw * 32 + 32, 1, RE.total, true};
     } else {
-        plan->g_hvp_fwd = {rpb * owner_threads, rpb, 0, false};
-        plan->g_hvp_edge = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem(), false};
+        A.g[0] = {rpb * owner_threads, rpb, 0, false};
+        A.g[1] = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem(), false};
     }
     Src S;
-    S("// Generated by the UVU planner: double backward (HVP) of the channel-wise CG convolution.");
+    S(fmt("// Generated by the UVU planner: %s of the channel-wise CG tensor product.",
+          hvp ? "double backward (HVP) of the convolution" : wsh ? "batched product, batch-shared weights" : "batched product, per-sample weights"));
     S(fmt("// irreps_x=%s irreps_sh=%s lmax_out=%d dtype=%s", plan->irreps_x.c_str(), plan->irreps_sh.c_str(),
           plan->lmax_out, G.f64 ? "fp64" : "fp32"));
     S(fmt("#define UVU_U %d", U));
@@ -1904,13 +1963,13 @@ std::string emit_hvp_source(Plan* plan) {
     S("}");
     if (pipe) {
         G.emit_pipe_helpers(S);
-        G.emit_recv_pipe_defines(S, RF, "FW", 3);
-        G.emit_recv_pipe_defines(S, RE, "EG", 4);
-        G.no_identity = true;
+        G.emit_recv_pipe_defines(S, RF, "FW", A.minb[0], A.minb_eff[0]);
+        G.emit_recv_pipe_defines(S, RE, "EG", A.minb[1], A.minb_eff[1]);
+        G.no_identity = hvp;
         G.emit_fwd_v2(S, RF);
         G.emit_edge_v2(S, RE);
         G.no_identity = false;
-    } else {
+    } else if (hvp) {
         G.emit_hvp_kernels(S);
     }
     return S.o.str();

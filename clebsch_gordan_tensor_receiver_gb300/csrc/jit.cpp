@@ -199,75 +199,69 @@ uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string
     return UVU_OK;
 }
 
-// The double-backward module: emitted and compiled on the first HVP call of the plan (host),
-// then loaded once per device.  Its pipelined kernels get the same register-budget retry and
-// launch set-up (shared-memory size, carveout, occupancy, status word) as the plan's own.
-// Same register-budget retry as the plan's own kernels (see uvu_plan_create): a pipelined HVP
-// kernel that spills under its budget is rebuilt for one resident block fewer.
-static uvu_status compile_hvp_locked(Plan* plan, std::string* err) {
-    if (!plan->hvp_cubin.empty()) return UVU_OK;
-    const char* names[2] = {"uvu_hvp_fwd", "uvu_hvp_edge"};
+// Auxiliary modules (double backward, batched tensor product): emitted and compiled on the
+// host on first use, then loaded once per device with the same launch set-up as the plan's own
+// kernels (shared-memory size, carveout, occupancy, status word).  The register-budget retry of
+// uvu_plan_create applies too: a pipelined kernel that spills under its budget is rebuilt for
+// one resident block fewer.
+static uvu_status compile_aux_locked(Plan* plan, int kind, std::string* err) {
+    AuxBuild& A = plan->aux[kind];
+    if (!A.cubin.empty()) return UVU_OK;
     for (int attempt = 0;; ++attempt) {
-        plan->hvp_source = emit_hvp_source(plan);
+        A.source = emit_aux_source(plan, kind);
         CacheEntry e;
-        uvu_status s = nvrtc_compile(plan->hvp_source, &e, err);
+        uvu_status s = nvrtc_compile(A.source, &e, err);
         if (s != UVU_OK) return s;
         bool again = false;
         for (int k = 0; k < 2 && attempt < 3; ++k)
-            if (plan->pipelined_recv && plan->minb_eff[3 + k] > 1 && spill_bytes(e.log, names[k]) > 32) {
-                plan->minb[3 + k] = plan->minb_eff[3 + k] - 1;
+            if (plan->pipelined_recv && A.minb_eff[k] > 1 && spill_bytes(e.log, kAuxKernelNames[kind][k]) > 32) {
+                A.minb[k] = A.minb_eff[k] - 1;
                 again = true;
             }
         if (!again) {
-            plan->hvp_cubin = std::move(e.cubin);
-            plan->hvp_log = std::move(e.log);
+            A.cubin = std::move(e.cubin);
+            A.log = std::move(e.log);
             return UVU_OK;
         }
     }
 }
 
-uvu_status compile_hvp(Plan* plan, std::string* err) {
+uvu_status compile_aux(Plan* plan, int kind, std::string* err) {
     std::lock_guard<std::mutex> g(plan->mu);
-    return compile_hvp_locked(plan, err);
+    return compile_aux_locked(plan, kind, err);
 }
 
-uvu_status hvp_module_for_current_device(Plan* plan, DeviceModule** out, std::string* err) {
+uvu_status aux_module_for_current_device(Plan* plan, int kind, DeviceModule** out, std::string* err) {
     DeviceModule* m = nullptr;
     uvu_status s = module_for_current_device(plan, &m, err);
     if (s != UVU_OK) return s;
     std::lock_guard<std::mutex> g(plan->mu);
-    const char* names[2] = {"uvu_hvp_fwd", "uvu_hvp_edge"};
-    s = compile_hvp_locked(plan, err);
+    s = compile_aux_locked(plan, kind, err);
     if (s != UVU_OK) return s;
-    if (!m->hvp_lib) {
-        cudaError_t ce = cudaLibraryLoadData(&m->hvp_lib, plan->hvp_cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0);
-        if (ce == cudaSuccess) ce = cudaLibraryGetKernel(&m->hvp_fwd, m->hvp_lib, names[0]);
-        if (ce == cudaSuccess) ce = cudaLibraryGetKernel(&m->hvp_edge, m->hvp_lib, names[1]);
-        struct {
-            cudaKernel_t k;
-            const KernelGeom* g;
-            int* occ;
-        } kk[] = {{m->hvp_fwd, &plan->g_hvp_fwd, &m->occ_hvp_fwd}, {m->hvp_edge, &plan->g_hvp_edge, &m->occ_hvp_edge}};
-        for (auto& k : kk) {
-            if (ce != cudaSuccess) break;
-            const void* f = reinterpret_cast<const void*>(k.k);
-            if (k.g->smem > 48 * 1024) ce = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(k.g->smem));
-            if (ce == cudaSuccess && k.g->persistent)
+    AuxBuild& A = plan->aux[kind];
+    AuxLoaded& L = m->aux[kind];
+    if (!L.lib) {
+        cudaError_t ce = cudaLibraryLoadData(&L.lib, A.cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0);
+        for (int k = 0; k < 2 && ce == cudaSuccess; ++k) {
+            ce = cudaLibraryGetKernel(&L.k[k], L.lib, kAuxKernelNames[kind][k]);
+            const void* f = reinterpret_cast<const void*>(L.k[k]);
+            if (ce == cudaSuccess && A.g[k].smem > 48 * 1024)
+                ce = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, int(A.g[k].smem));
+            if (ce == cudaSuccess && A.g[k].persistent)
                 ce = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, int(cudaSharedmemCarveoutMaxShared));
-            if (ce == cudaSuccess) ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(k.occ, f, k.g->threads, k.g->smem);
-            if (ce == cudaSuccess && *k.occ < 1) ce = cudaErrorInvalidConfiguration;
+            if (ce == cudaSuccess) ce = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&L.occ[k], f, A.g[k].threads, A.g[k].smem);
+            if (ce == cudaSuccess && L.occ[k] < 1) ce = cudaErrorInvalidConfiguration;
         }
         if (ce == cudaSuccess && plan->pipelined_recv) {
             size_t bytes = 0;
             void* ptr = nullptr;
-            ce = cudaLibraryGetGlobal(&ptr, &bytes, m->hvp_lib, "uvu_status_word");
-            m->hvp_status_word = static_cast<unsigned*>(ptr);
+            ce = cudaLibraryGetGlobal(&ptr, &bytes, L.lib, "uvu_status_word");
+            L.status_word = static_cast<unsigned*>(ptr);
         }
         if (ce != cudaSuccess) {
-            *err = std::string("loading the HVP module: ") + cudaGetErrorString(ce);
-            if (m->hvp_lib) cudaLibraryUnload(m->hvp_lib);
-            m->hvp_lib = nullptr;
-            m->hvp_status_word = nullptr;
+            *err = std::string("loading the ") + kAuxKernelNames[kind][0] + " module: " + cudaGetErrorString(ce);
+            if (L.lib) cudaLibraryUnload(L.lib);
+            L = AuxLoaded{};
             return UVU_ERR_CUDA;
         }
     }

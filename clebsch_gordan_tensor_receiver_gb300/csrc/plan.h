@@ -43,16 +43,34 @@ struct KernelGeom {
     int tiles = 1;             // work items per owner (channel tiles) for persistent kernels
 };
 
+// Auxiliary modules of a plan, emitted and compiled on their first use, each with a
+// receiver-ordered "forward" kernel and an "edge" kernel: the double backward, and the batched
+// (non-convolution) tensor product with per-sample or batch-shared weights.
+enum AuxKind { AUX_HVP = 0, AUX_TP = 1, AUX_TP_SHARED = 2, AUX_COUNT = 3 };
+extern const char* const kAuxKernelNames[AUX_COUNT][2];
+
+struct AuxBuild {  // host side, per plan
+    std::string source, log;
+    std::vector<char> cubin;
+    KernelGeom g[2];
+    int minb[2] = {4, 4};      // register-budget caps (blocks per SM), lowered on spills
+    int minb_eff[2] = {1, 1};  // value used by the last emission
+};
+
+struct AuxLoaded {  // per device
+    cudaLibrary_t lib = nullptr;
+    cudaKernel_t k[2] = {nullptr, nullptr};
+    int occ[2] = {1, 1};
+    unsigned* status_word = nullptr;  // the module's own uvu_status_word (pipelined kernels only)
+};
+
 struct DeviceModule {
     cudaLibrary_t lib = nullptr;
     cudaKernel_t fwd = nullptr, bwd_edge = nullptr, bwd_dx = nullptr, bwd_dx_reduce = nullptr;
-    cudaLibrary_t hvp_lib = nullptr;  // second module (double backward), loaded on first use
-    cudaKernel_t hvp_fwd = nullptr, hvp_edge = nullptr;
     int sm_count = 0;
     int occ_fwd = 1, occ_edge = 1, occ_dx = 1;  // resident blocks per SM
-    int occ_hvp_fwd = 1, occ_hvp_edge = 1;
     unsigned* status_word = nullptr;            // device address of uvu_status_word
-    unsigned* hvp_status_word = nullptr;        // the same word of the double-backward module
+    AuxLoaded aux[AUX_COUNT];
 };
 
 struct Plan {
@@ -64,20 +82,18 @@ struct Plan {
     std::vector<Irrep> xs, ys;
     std::vector<PathInfo> paths;
     std::vector<std::vector<int>> groups;  // path ids per register group
-    KernelGeom g_fwd, g_edge, g_dx, g_hvp_fwd, g_hvp_edge;
+    KernelGeom g_fwd, g_edge, g_dx;
     int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
     bool pipelined_recv = false, pipelined_dx = false;
     bool staged_ok = false;   // the edge kernel can write per-edge dx partials (staged dx)
     bool rebalanced = false;  // register groups re-split for the pipelined kernels
     // Upper bound on resident blocks per SM that the register budget is sized for, per kernel
-    // (fwd, edge, dx, hvp_fwd, hvp_edge); lowered one block at a time for a kernel whose budget
-    // makes ptxas spill.
-    int minb[5] = {4, 4, 4, 4, 4};
-    int minb_eff[5] = {1, 1, 1, 1, 1};  // value used by the last emission
+    // (fwd, edge, dx); lowered one block at a time for a kernel whose budget makes ptxas spill.
+    int minb[3] = {4, 4, 4};
+    int minb_eff[3] = {1, 1, 1};  // value used by the last emission
     std::string source, log;
     std::vector<char> cubin;
-    std::string hvp_source, hvp_log;  // double-backward module, compiled on the first HVP call
-    std::vector<char> hvp_cubin;
+    AuxBuild aux[AUX_COUNT];
     std::mutex mu;
     std::map<int, DeviceModule> modules;  // per device ordinal
     size_t elem() const { return dtype == UVU_F64 ? 8 : 4; }
@@ -92,15 +108,15 @@ uvu_status build_paths(Plan* plan, std::string* err);
 
 // codegen.cpp
 std::string emit_source(Plan* plan);
-std::string emit_hvp_source(Plan* plan);
+std::string emit_aux_source(Plan* plan, int kind);
 void balance_groups(Plan* plan, int ng);
 
 // jit.cpp
 uvu_status compile_plan(Plan* plan, std::string* err);
 size_t spill_bytes(const std::string& log, const char* kernel);
 uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string* err);
-uvu_status compile_hvp(Plan* plan, std::string* err);  // host only
-uvu_status hvp_module_for_current_device(Plan* plan, DeviceModule** out, std::string* err);
+uvu_status compile_aux(Plan* plan, int kind, std::string* err);  // host only
+uvu_status aux_module_for_current_device(Plan* plan, int kind, DeviceModule** out, std::string* err);
 
 // status.cpp
 uvu_status fail(uvu_status s, const std::string& msg);
@@ -118,4 +134,6 @@ cudaError_t launch_csr_transpose(int64_t N, int64_t E, const int32_t* roff, cons
                                  int32_t* soff, int32_t* eids, int32_t* srecv, void* ws, cudaStream_t st);
 cudaError_t launch_graph_validate(int64_t N, int64_t E, const int32_t* off, const int32_t* src,
                                   unsigned long long* bad, cudaStream_t st);
+// tp.cu
+cudaError_t launch_column_sum(const void* part, int64_t rows, int64_t cols, void* out, bool f64, cudaStream_t st);
 }  // namespace uvu

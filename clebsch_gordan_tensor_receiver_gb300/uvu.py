@@ -20,17 +20,19 @@ LIB_PATH = os.path.join(_HERE, "_build", "libuvu.so")
 
 UVU_F32, UVU_F64 = 0, 1
 UVU_DX_SENDER, UVU_DX_ATOMIC, UVU_DX_STAGED = 0, 1, 2
+UVU_MODULE_CONV, UVU_MODULE_HVP, UVU_MODULE_TP, UVU_MODULE_TP_SHARED = 0, 1, 2, 3
 STATUS = {0: "UVU_OK", 1: "UVU_ERR_INVALID_ARGUMENT", 2: "UVU_ERR_UNSUPPORTED",
           3: "UVU_ERR_COMPILE", 4: "UVU_ERR_CUDA", 5: "UVU_ERR_OUT_OF_MEMORY"}
 
 # every symbol declared in include/uvu.h
 EXPORTS = (
     "uvu_plan_create", "uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source",
-    "uvu_plan_hvp_source", "uvu_plan_device_status",
+    "uvu_plan_module_source", "uvu_plan_device_status",
     "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
     "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
     "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
-    "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_status_string", "uvu_last_error_message",
+    "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
+    "uvu_status_string", "uvu_last_error_message",
 )
 
 
@@ -51,7 +53,7 @@ def _load():
         "uvu_plan_info": [P, P, P, P, P, P, P],
         "uvu_plan_cg": [P, I, P],
         "uvu_plan_source": [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
-        "uvu_plan_hvp_source": [P, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
+        "uvu_plan_module_source": [P, I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
         "uvu_plan_device_status": [P, ctypes.POINTER(ctypes.c_uint), I],
         "uvu_csr_from_sorted_recv": [I64, I64, P, P, P],
         "uvu_csr_transpose_workspace": [I64, I64, ctypes.POINTER(SZ)],
@@ -66,6 +68,9 @@ def _load():
         "uvu_conv_bwd": [P, I64, I64, P, P, P, P, P, P, P, P, P, P, P, P, I, P, SZ, P],
         "uvu_conv_hvp": [P, I64, I64] + [P] * 16 + [SZ, P],
         "uvu_conv_hvp_workspace": [P, I64, I64, ctypes.POINTER(SZ)],
+        "uvu_tp_fwd": [P, I64, P, P, P, I, P, P],
+        "uvu_tp_bwd": [P, I64, P, P, P, I, P, P, P, P, P, SZ, P],
+        "uvu_tp_bwd_workspace": [P, I64, I, ctypes.POINTER(SZ)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -97,12 +102,12 @@ def _wrap(name):
     return call
 
 
-for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source", "uvu_plan_hvp_source",
+for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source", "uvu_plan_module_source",
            "uvu_plan_device_status",
            "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
            "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
            "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
-           "uvu_conv_hvp", "uvu_conv_hvp_workspace"):
+           "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace"):
     globals()[_n] = _wrap(_n)
 
 
@@ -182,11 +187,39 @@ class Plan:
         uvu_plan_source(self.handle, ctypes.byref(s), ctypes.byref(l))
         return s.value.decode(), l.value.decode()
 
-    def hvp_source(self):
-        """(source, NVRTC log) of the double-backward kernels; compiles them on the host if needed."""
+    def module_source(self, module: int):
+        """(source, NVRTC log) of one of the plan's modules (UVU_MODULE_*); compiles it on the host
+        if needed."""
         s, l = ctypes.c_char_p(), ctypes.c_char_p()
-        uvu_plan_hvp_source(self.handle, ctypes.byref(s), ctypes.byref(l))
+        uvu_plan_module_source(self.handle, module, ctypes.byref(s), ctypes.byref(l))
         return s.value.decode(), l.value.decode()
+
+    def hvp_source(self):
+        return self.module_source(UVU_MODULE_HVP)
+
+    def tp_fwd(self, batch, x, y, w, out, w_shared=False, stream=None):
+        """Batched tensor product (see uvu_tp_fwd)."""
+        uvu_tp_fwd(self.handle, batch, _ptr(x), _ptr(y), _ptr(w), int(bool(w_shared)), _ptr(out),
+                   _stream(stream))
+
+    def tp_workspace_bytes(self, batch, w_shared) -> int:
+        b = ctypes.c_size_t()
+        uvu_tp_bwd_workspace(self.handle, batch, int(bool(w_shared)), ctypes.byref(b))
+        return b.value
+
+    def tp_bwd(self, batch, x, y, w, d_out, dx=None, dy=None, dw=None, w_shared=False,
+               workspace=None, stream=None):
+        """VJP of the batched tensor product (see uvu_tp_bwd); a shared dw needs `workspace`
+        (a uint8 device tensor of tp_workspace_bytes() bytes), allocated here with torch if None."""
+        ws_ptr, ws_bytes = None, 0
+        need = self.tp_workspace_bytes(batch, w_shared) if dw is not None else 0
+        if need:
+            if workspace is None:
+                import torch
+                workspace = torch.empty(need, dtype=torch.uint8, device=d_out.device)
+            ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+        uvu_tp_bwd(self.handle, batch, _ptr(x), _ptr(y), _ptr(w), int(bool(w_shared)), _ptr(d_out),
+                   _ptr(dx), _ptr(dy), _ptr(dw), ws_ptr, ws_bytes, _stream(stream))
 
     def fwd(self, n_nodes, x, Y, w, recv_offsets, src, out, stream=None):
         uvu_conv_fwd(self.handle, n_nodes, src.numel() if src is not None else 0, _ptr(x), _ptr(Y),

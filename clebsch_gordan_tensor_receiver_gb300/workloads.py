@@ -238,3 +238,16 @@ def custom_spec(key: int, n_nodes: int, irreps_x: str, irreps_sh: str, lmax_out:
     """A small uniform-degree workload for tests (keys >= 100 keep their own seed streams)."""
     return WorkloadSpec(key, f"custom{key}", n_nodes, irreps_x, irreps_sh, lmax_out, dtype,
                         "uniform", degree=degree, w_scale_degree=max(degree, 1))
+
+
+def tp_inputs(spec: WorkloadSpec, batch: int, n_paths: int, dim_out: int, shared: bool, seed: int = 0):
+    """Inputs of the batched (non-convolution) tensor product on the irreps of `spec`:
+    x [B][U][D_x] ~ N(0,1); y [B][D_Y] = SH of normalised N(0, I3) vectors; w ~ N(0,1), per sample
+    [B][P][U] or shared [P][U]; d_out [B][U][D_out] ~ N(0,1).  Seeded by (spec key, seed)."""
+    rng = np.random.default_rng(np.random.SeedSequence([SEED_BASE + spec.key, 7, seed]))
+    dtype = np.dtype(spec.dtype).type
+    x = _normal(rng, (batch, spec.mul, dim_of(spec.irreps_x)), dtype)
+    y = sh_inputs(unit_vectors(batch, rng), spec.sh_lmax).astype(dtype)
+    w = _normal(rng, (n_paths, spec.mul) if shared else (batch, n_paths, spec.mul), dtype)
+    g = _normal(rng, (batch, spec.mul, dim_out), dtype)
+    return np.ascontiguousarray(x), np.ascontiguousarray(y), np.ascontiguousarray(w), np.ascontiguousarray(g)

@@ -112,10 +112,22 @@ uvu_status uvu_plan_cg(uvu_plan_t plan, int path, double *out);
  * log (ptxas resource usage).  Either pointer may be NULL. */
 uvu_status uvu_plan_source(uvu_plan_t plan, const char **source, const char **compile_log);
 
-/* The emitted source and NVRTC log of the plan's double-backward (HVP) kernels.  Compiles them
- * on the host if no HVP call has done so yet (no device needed); UVU_ERR_COMPILE if NVRTC fails.
- * The strings stay valid until the plan is destroyed.  Either pointer may be NULL. */
-uvu_status uvu_plan_hvp_source(uvu_plan_t plan, const char **source, const char **compile_log);
+/* A plan's generated modules: the convolution (forward, VJP; built by uvu_plan_create), and the
+ * modules built on their first use: the double backward and the batched tensor product with
+ * per-sample or batch-shared weights. */
+typedef enum {
+  UVU_MODULE_CONV = 0,
+  UVU_MODULE_HVP = 1,
+  UVU_MODULE_TP = 2,
+  UVU_MODULE_TP_SHARED = 3
+} uvu_module;
+
+/* The emitted source and NVRTC log of one of the plan's modules.  Compiles it on the host if no
+ * call has done so yet (no device needed); UVU_ERR_COMPILE if NVRTC fails,
+ * UVU_ERR_INVALID_ARGUMENT for an unknown module.  The strings stay valid until the plan is
+ * destroyed.  Either pointer may be NULL. */
+uvu_status uvu_plan_module_source(uvu_plan_t plan, uvu_module module, const char **source,
+                                  const char **compile_log);
 
 /* Device-side status of the plan's kernels on the current device: bit 0 (UVU_DEV_TIMEOUT) is set
  * when a pipelined kernel gave up waiting for a shared-memory stage (about two seconds) and
@@ -261,6 +273,37 @@ uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const
 
 /* Bytes of device workspace uvu_conv_hvp needs for grad_x (0 when it uses atomic adds). */
 uvu_status uvu_conv_hvp_workspace(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, size_t *bytes);
+
+/* ------------------------------------------------------- batched tensor product (no graph) ---- */
+
+/* The channel-wise CG tensor product on its own, over a batch of B independent samples ("An
+ * Efficient Sparse Kernel Generator for O(3)-Equivariant Deep Networks", abstract: two dense
+ * feature vectors contracted with a structured sparse tensor, before its fusion with a graph
+ * convolution), with the plan's paths and coefficients:
+ *     out[b,u,ooff(p)+m3] = w[.,p,u] * sum_{m1,m2} C^p[m1,m2,m3] x[b,u,xoff(p)+m1] y[b,yoff(p)+m2]
+ * x [B][U][D_x], y [B][D_Y], out [B][U][D_out] in the convolution's layouts.  w is per sample,
+ * [B][P][U] (w_shared = 0), or shared by the batch, [P][U] (w_shared != 0).  Every tensor is
+ * caller-owned device memory, 16-byte aligned; out is overwritten (B = 0 writes nothing).
+ * It runs the plan's pipelined receiver kernels with sample b as receiver b holding the one edge
+ * b from sender b, so it needs a plan with U >= 32 (UVU_ERR_UNSUPPORTED otherwise).  The kernels
+ * are compiled on the first call for each weight mode (host, NVRTC) and loaded once per device.
+ * Launches: 1 kernel. */
+uvu_status uvu_tp_fwd(uvu_plan_t plan, int64_t batch, const void *x, const void *y, const void *w,
+                      int w_shared, void *out, uvu_stream_t stream);
+
+/* VJP of uvu_tp_fwd for the cotangent d_out [B][U][D_out]: dx [B][U][D_x], dy [B][D_Y] and dw
+ * ([B][P][U] per sample, or [P][U] summed over the batch when w_shared); any may be NULL = not
+ * computed.  A shared dw is formed deterministically and in fp64: each block of the edge kernel
+ * sums its samples in order into one fp64 row of `workspace` (at least uvu_tp_bwd_workspace()
+ * bytes), then the rows are added in block order and rounded once to the plan's type.  For
+ * B = 0 a shared dw is set to zero.
+ * Launches: 1 kernel, plus the row sum for a shared dw. */
+uvu_status uvu_tp_bwd(uvu_plan_t plan, int64_t batch, const void *x, const void *y, const void *w,
+                      int w_shared, const void *d_out, void *dx, void *dy, void *dw, void *workspace,
+                      size_t workspace_bytes, uvu_stream_t stream);
+
+/* Bytes of device workspace uvu_tp_bwd needs (0 unless w_shared): min(B, 2048) * P * U * 8. */
+uvu_status uvu_tp_bwd_workspace(uvu_plan_t plan, int64_t batch, int w_shared, size_t *bytes);
 
 /* ---------------------------------------------------------------------------- errors ---- */
 

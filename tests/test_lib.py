@@ -98,3 +98,21 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
         uvu._load()
     assert "clebsch_gordan_tensor_receiver_gb300.uvu" in sys.modules
     importlib.invalidate_caches()
+
+
+def test_batched_tensor_product_host_checks():
+    """Argument checks of the batched tensor product that run before any device work: plans with
+    U < 32 are refused, negative batches are refused, and the shared-dw workspace size."""
+    import pytest
+    from clebsch_gordan_tensor_receiver_gb300 import uvu
+    small = uvu.Plan("16x0e+16x1o", "1x0e+1x1o+1x2e", 2)
+    with pytest.raises(uvu.UVUError) as ei:
+        small.tp_workspace_bytes(10, True)
+    assert ei.value.status == 2  # UVU_ERR_UNSUPPORTED
+    p = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3)
+    i = p.info
+    assert p.tp_workspace_bytes(10, False) == 0
+    assert p.tp_workspace_bytes(10, True) == 10 * i.n_paths * i.mul * 8  # fp64 partial rows
+    assert p.tp_workspace_bytes(10 ** 6, True) == 2048 * i.n_paths * i.mul * 8
+    with pytest.raises(uvu.UVUError):
+        p.tp_workspace_bytes(-1, True)
