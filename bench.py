@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-hvp", action="store_true", help="skip the double-backward measurement")
+    ap.add_argument("--no-tp", action="store_true", help="skip the batched tensor-product measurement")
+    ap.add_argument("--tp-batch", type=int, default=100000, help="samples of the batched tensor product")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
     ap.add_argument("--single-mode", action="store_true",
                     help="warm up and time only --dx-mode (profiling runs)")
@@ -407,6 +409,53 @@ def main(argv=None):
         "clocks": clk,
         "gpu_launches": args.steps * (2 if args.dx_mode == "atomic" else 3),
     }
+
+    # batched (non-convolution) tensor product on the same irreps: B samples, per-sample and
+    # batch-shared weights, forward and VJP (dx, dy, dw); inputs drawn on the device (seeded)
+    if not args.no_tp and world == 1 and info.mul >= 32:
+        Bt = args.tp_batch
+        gen = torch.Generator(device=dev).manual_seed(4242)
+        tx = torch.randn((Bt, U, Dx), generator=gen, device=dev, dtype=tdt)
+        ty = torch.randn((Bt, Dy), generator=gen, device=dev, dtype=tdt)
+        tg = torch.randn((Bt, U, Do), generator=gen, device=dev, dtype=tdt)
+        tout, tdx, tdy = torch.empty_like(tg), torch.empty_like(tx), torch.empty_like(ty)
+
+        def ev_ms(fn, reps):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+        xs_, ys_, os_ = Bt * U * Dx * s, Bt * Dy * s, Bt * U * Do * s
+        tp_line = {"batch": Bt, "note": "x [B][U][D_x], y [B][D_Y], d_out ~ N(0,1) drawn on the device; "
+                   "compulsory bytes: fwd reads x, y, w and writes out; VJP reads x, y, w, d_out and "
+                   "writes dx, dy, dw"}
+        reps = max(5, args.steps // 2)
+        for mode, shared in (("per_sample", False), ("shared", True)):
+            tw = torch.randn((P, U) if shared else (Bt, P, U), generator=gen, device=dev, dtype=tdt)
+            tdw = torch.empty_like(tw)
+            tws = torch.empty(max(16, plan.tp_workspace_bytes(Bt, shared)), dtype=torch.uint8, device=dev)
+            wb = tw.numel() * s
+            f_ms = ev_ms(lambda: plan.tp_fwd(Bt, tx, ty, tw, tout, w_shared=shared, stream=stream), reps)
+            b_ms = ev_ms(lambda: plan.tp_bwd(Bt, tx, ty, tw, tg, dx=tdx, dy=tdy, dw=tdw, w_shared=shared,
+                                             workspace=tws, stream=stream), reps)
+            fb, bb = xs_ + ys_ + wb + os_, xs_ + ys_ + wb + os_ + xs_ + ys_ + wb
+            f_gbs, f_fr = frac(fb, f_ms)
+            b_gbs, b_fr = frac(bb, b_ms)
+            tp_line[mode] = {"fwd_ms": f_ms, "fwd_samples_per_s": Bt / (f_ms / 1000), "fwd_GB_s": f_gbs,
+                             "fwd_hbm_frac": f_fr, "vjp_ms": b_ms, "vjp_samples_per_s": Bt / (b_ms / 1000),
+                             "vjp_GB_s": b_gbs, "vjp_hbm_frac": b_fr, "fwd_bytes": fb, "vjp_bytes": bb}
+            del tw, tdw, tws
+        assert plan.device_status() == 0
+        line["tp"] = tp_line
+        del tx, ty, tg, tout, tdx, tdy
 
     # double backward (HVP): gradients of <ax,dx> + <aY,dY> + <aw,dw>, timed on the same workload
     if not args.no_hvp and world == 1:

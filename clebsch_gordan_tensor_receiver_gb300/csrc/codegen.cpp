@@ -80,11 +80,10 @@ struct Gen {
     // therefore always take the generic path.
     mutable bool no_identity = false;
     // dw of a path: stored per edge (dwe[p * U]) or, for weights shared by a whole batch,
-    // accumulated in fp64 in the thread's registers (dwa_p) over the samples it processes (a sum
-    // over many samples: fp32 accumulation lost digits where the terms cancel)
+    // accumulated in the thread's registers (dwa_p) over the samples it processes
     mutable bool dw_accum = false;
     std::string dw_store(int pi, const std::string& v) const {
-        return dw_accum ? fmt("dwa_%d += (double)(%s);", pi, v.c_str()) : fmt("dwe[%d * UVU_U] = %s;", pi, v.c_str());
+        return dw_accum ? fmt("dwa_%d += %s;", pi, v.c_str()) : fmt("dwe[%d * UVU_U] = %s;", pi, v.c_str());
     }
 
     bool is_identity(const PathInfo& p) const {
@@ -817,6 +816,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         size_t aw_off = 0, ax_off = 0, ay_off = 0;
         size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, xpart_off = 0, out_off = 0, total = 0;
         size_t g_off = 0, gbytes = 0;
+        size_t dacc_off = 0;  // fp64 dw accumulators [P][U_pad] of the batch-shared-weight edge kernel
         size_t tx_per_edge = 0;
     };
     static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
@@ -872,6 +872,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         R.total = R.out_off + (stage_out ? a16(size_t(P->U) * R.odp * P->elem()) : 0);
         R.g_off = R.total;
         if (R.gst) R.total += a16(R.gbytes);
+        R.dacc_off = R.total;
+        if (wsh && with_partials && !f64) R.total += a16(size_t(P->P) * P->U_pad * 8);
         R.tx_per_edge = wb + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
         // With a receiver block staged, shorter stages keep three blocks resident per SM where
         // the default chunk would leave fewer (more warps beat a longer look-ahead per block).
@@ -898,6 +900,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S(fmt("#define %s_GBUF %zu", pre, R.g_off));
         S(fmt("#define %s_GBAR %zu", pre, R.bar_off + 16 * R.nst));
         S(fmt("#define %s_GBYTES %zu", pre, R.gbytes));
+        S(fmt("#define %s_DACC %zu", pre, R.dacc_off));
         S(fmt("#define %s_AWOFF %zu", pre, R.aw_off));
         S(fmt("#define %s_AXOFF %zu", pre, R.ax_off));
         S(fmt("#define %s_AYOFF %zu", pre, R.ay_off));
@@ -1259,7 +1262,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                   T.c_str(), T.c_str(), T.c_str(), T.c_str()));
             std::string dwa;
             if (R.wsh)
-                for (int pi : paths) dwa += fmt(", double& dwa_%d", pi);
+                for (int pi : paths) dwa += fmt(", %s& dwa_%d", T.c_str(), pi);
             S(fmt("    %s* __restrict__ dxe, int g, const %s* __restrict__ w%s) {", T.c_str(), T.c_str(), dwa.c_str()));
             S.ind++;
             if (R.gst) {
@@ -1426,8 +1429,32 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("unsigned c = 0, kg = 0;");
         S("bool dead = false;");
         S("int buf = 0;");
-        if (R.wsh)  // dw of batch-shared weights: this block's sum over its samples, per thread
-            for (int pi = 0; pi < P->P; ++pi) S(fmt("double dwa_%d = 0;", pi));
+        // dw of batch-shared weights: this block's sum over its samples, per thread.  An fp32 plan
+        // sums 16 samples in registers and adds each such chunk into the thread's own fp64 slots
+        // in shared memory (a sum over many samples lost digits in fp32 where the terms cancel;
+        // fp64 registers cost a resident block); an fp64 plan sums in registers.
+        const bool dacc = R.wsh && !f64;
+        if (R.wsh) {
+            for (int pi = 0; pi < P->P; ++pi) S(fmt("%s dwa_%d = 0;", T.c_str(), pi));
+            if (dacc) {
+                S("double* const sacc = reinterpret_cast<double*>(smem + EG_DACC) + u;");
+                S("int nacc = 0;");
+                for (int g = 0; g < NG; ++g) {
+                    std::string st;
+                    for (int pi : P->groups[g]) st += fmt(" sacc[%d * UVU_UP] = 0.0;", pi);
+                    S(fmt("%sif (g == %d) {%s }", g ? "else " : "", g, st.c_str()));
+                }
+            }
+        }
+        auto flush = [&](const char* cond) {
+            S(std::string("if (") + cond + ") {");
+            for (int g = 0; g < NG; ++g) {
+                std::string st;
+                for (int pi : P->groups[g]) st += fmt(" sacc[%d * UVU_UP] += (double)dwa_%d; dwa_%d = 0;", pi, pi, pi);
+                S(fmt("  %sif (g == %d) {%s }", g ? "else " : "", g, st.c_str()));
+            }
+            S("}");
+        };
         S("for (long long r = blockIdx.x; r < N; r += gridDim.x) {");
         S.ind++;
         S("const int e0 = " + off_at(R, "r") + ", e1 = " + off_at(R, "r + 1") + ";");
@@ -1438,14 +1465,17 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S(fmt("%sif (g == %d) edge_rcv%d(r, e0, e1, u, uvalid, lane, warp, tid, c, kg, dead, buf, smem, sbase, src, x, Y, %sgout, dY, dw, dx, dxe, g, w%s);",
                   g ? "else " : "", g, g, R.dual ? "ax, aY, hm, " : "", dwa.c_str()));
         }
+        if (dacc) flush("++nacc == 16 && (nacc = 0, true)");
         S.ind--;
         S("}");
+        if (dacc) flush("true");
         if (R.wsh) {  // the block's partial dw [P][U] in fp64 (row blockIdx.x of the caller's workspace)
             S("if (dw && uvalid) {");
             S("  double* __restrict__ pr = reinterpret_cast<double*>(dw) + (size_t)blockIdx.x * (UVU_P * UVU_U) + u;");
             for (int g = 0; g < NG; ++g) {
                 std::string st;
-                for (int pi : P->groups[g]) st += fmt(" pr[%d * UVU_U] = dwa_%d;", pi, pi);
+                for (int pi : P->groups[g]) st += dacc ? fmt(" pr[%d * UVU_U] = sacc[%d * UVU_UP];", pi, pi)
+                                                       : fmt(" pr[%d * UVU_U] = dwa_%d;", pi, pi);
                 S(fmt("  %sif (g == %d) {%s }", g ? "else " : "", g, st.c_str()));
             }
             S("}");
