@@ -410,6 +410,35 @@ def main(argv=None):
         "gpu_launches": args.steps * (2 if args.dx_mode == "atomic" else 3),
     }
 
+    # receiver- vs sender-stationary forward: the data-movement model's bytes and choice, and both
+    # forwards timed on this workload
+    if world == 1 and not args.single_mode:
+        choice, br, bs = plan.fwd_model(N, E)
+        fs_out = torch.empty_like(out)
+
+        def ev_med(fn, reps=5):
+            for _ in range(2):
+                fn()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+        r_ms = ev_med(lambda: plan.fwd(N, x, Y, w, G.recv_offsets, src, fs_out, stream=stream))
+        s_ms = ev_med(lambda: plan.fwd_sender(N, E, x, Y, w, G.send_offsets, G.send_eids, G.send_recv,
+                                              fs_out, stream=stream))
+        line["fwd_modes"] = {"model_choice": {uvu.UVU_FWD_RECEIVER: "receiver", uvu.UVU_FWD_SENDER: "sender"}[choice],
+                             "model_bytes": {"receiver": br, "sender": bs},
+                             "measured_ms": {"receiver": r_ms, "sender": s_ms},
+                             "measured_choice": "receiver" if r_ms <= s_ms else "sender"}
+        assert plan.device_status() == 0
+        del fs_out
+
     # batched (non-convolution) tensor product on the same irreps: B samples, per-sample and
     # batch-shared weights, forward and VJP (dx, dy, dw); inputs drawn on the device (seeded)
     if not args.no_tp and world == 1 and info.mul >= 32:

@@ -480,6 +480,74 @@ extern "C" uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
     return ok();
 }
 
+// ------------------------------------------------- receiver- vs sender-stationary forward
+
+namespace uvu {
+namespace {
+// Bytes each forward moves through the memory system per launch (the data-movement model):
+// receiver-stationary gathers an x row per edge and writes each out row once; sender-stationary
+// reads each x row once, zero-fills out and read-modify-writes an out row per edge.
+void fwd_model(const Plan* p, int64_t N, int64_t E, double* br, double* bs) {
+    const double s = double(p->elem()), U = p->U;
+    const double wY = double(E) * (p->P * U + p->Dy) * s;
+    *br = wY + double(E) * U * p->Dx * s + double(N) * U * p->Do * s + 4.0 * (N + 1) + 4.0 * E;
+    *bs = wY + double(N) * U * p->Dx * s + double(N) * U * p->Do * s + 2.0 * double(E) * U * p->Do * s +
+          4.0 * (N + 1) + 8.0 * E;
+}
+}  // namespace
+}  // namespace uvu
+
+extern "C" uvu_status uvu_conv_fwd_model(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, uvu_fwd_mode* choice,
+                                         double* bytes_receiver, double* bytes_sender) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    double br = 0, bs = 0;
+    fwd_model(p, n_nodes, n_edges, &br, &bs);
+    if (choice) *choice = bs < br ? UVU_FWD_SENDER : UVU_FWD_RECEIVER;
+    if (bytes_receiver) *bytes_receiver = br;
+    if (bytes_sender) *bytes_sender = bs;
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_fwd_sender(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
+                                          const void* Y, const void* w, const int32_t* send_offsets,
+                                          const int32_t* send_eids, const int32_t* send_recv, void* out,
+                                          uvu_stream_t stream) {
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    if (n_nodes == 0) return ok();
+    UVU_TRY(need(out, "out"));
+    cudaError_t e = cudaMemsetAsync(out, 0, size_t(n_nodes) * p->U * p->Do * p->elem(), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "out memset");
+    if (n_edges == 0) return ok();
+    UVU_TRY(need(x, "x"));
+    UVU_TRY(need(Y, "Y"));
+    UVU_TRY(need(w, "w"));
+    UVU_TRY(need_idx(send_offsets, "send_offsets"));
+    UVU_TRY(need_idx(send_eids, "send_eids"));
+    UVU_TRY(need_idx(send_recv, "send_recv"));
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = module_for_current_device(p, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    long long N = n_nodes;
+    void* args[] = {&N, &send_offsets, &send_eids, &send_recv, &x, &Y, &w, &out};
+    return launch(m->fwd_sender, 1, m->sm_count, n_nodes, p->g_fwd_sender, args, stream, "uvu_fwd_sender launch");
+}
+
+extern "C" uvu_status uvu_conv_fwd_mode(uvu_plan_t plan, uvu_fwd_mode mode, int64_t n_nodes, int64_t n_edges,
+                                        const void* x, const void* Y, const void* w, const int32_t* recv_offsets,
+                                        const int32_t* src, const int32_t* send_offsets, const int32_t* send_eids,
+                                        const int32_t* send_recv, void* out, uvu_stream_t stream) {
+    if (mode == UVU_FWD_AUTO) UVU_TRY(uvu_conv_fwd_model(plan, n_nodes, n_edges, &mode, nullptr, nullptr));
+    if (mode == UVU_FWD_RECEIVER) return uvu_conv_fwd(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, out, stream);
+    if (mode == UVU_FWD_SENDER)
+        return uvu_conv_fwd_sender(plan, n_nodes, n_edges, x, Y, w, send_offsets, send_eids, send_recv, out, stream);
+    return fail(UVU_ERR_INVALID_ARGUMENT, "unknown forward mode");
+}
+
 // ------------------------------------------------------------- batched tensor product (no graph)
 
 namespace uvu {

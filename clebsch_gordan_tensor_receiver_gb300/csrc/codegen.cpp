@@ -186,6 +186,56 @@ struct Gen {
 
     // ------------------------------------------------------------------ forward
     // acc_* += contribution of one edge, from xv_*, yv_*, wv_* already in registers.
+    // Sender-stationary forward (source-stationary convolution): one thread per (sender, register
+    // group, channel) keeps its x row in registers, walks the sender's out-edges over the
+    // transposed CSR and adds each edge's contribution to out[recv] with reduction atomics (out
+    // zeroed first).  The alternative to the receiver-stationary forward when x rows are wider
+    // than out rows ("Receiver-streaming convolutions ...", replies: source- and destination-
+    // stationary convolutions, the one that moves less data chosen at init time).
+    void emit_fwd_sender_group(Src& S, int g) const {
+        const std::vector<int>& paths = P->groups[g];
+        const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+        std::vector<int> outs;
+        for (int pi : paths)
+            for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
+        S(fmt("__device__ __forceinline__ void fsend_group%d(int k0, int k1, int u, const int* __restrict__ seid,", g));
+        S(fmt("    const int* __restrict__ srecv, const %s* __restrict__ xrow, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
+        S(fmt("    const %s* __restrict__ w, %s* __restrict__ out) {", T.c_str(), T.c_str()));
+        S.ind++;
+        emit_row_loads(S, "xv", "xrow", P->Dx, xn);
+        S("#pragma unroll 1");
+        S("for (int k = k0; k < k1; ++k) {");
+        S.ind++;
+        S("const int e = __ldg(seid + k), r = __ldg(srecv + k);");
+        emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+        S("const " + T + "* __restrict__ we = w + (size_t)e * (UVU_P * UVU_U) + u;");
+        for (int pi : paths) S(fmt("const %s wv_%d = __ldg(we + %d * UVU_U);", T.c_str(), pi, pi));
+        for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
+        emit_fwd_edge(S, paths);
+        S(T + "* __restrict__ orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
+        for (int k : outs) S(fmt("atomicAdd(orow + %d, acc_%d);", k, k));
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+    }
+    void emit_fwd_sender_kernel(Src& S) const {
+        const int NG = int(P->groups.size());
+        for (int g = 0; g < NG; ++g) emit_fwd_sender_group(S, g);
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_FS_TPB) uvu_fwd_sender(long long N, const int* __restrict__ soff,"));
+        S(fmt("    const int* __restrict__ seid, const int* __restrict__ srecv, const %s* __restrict__ x,", T.c_str()));
+        S(fmt("    const %s* __restrict__ Y, const %s* __restrict__ w, %s* __restrict__ out) {", T.c_str(), T.c_str(), T.c_str()));
+        S("  const int u = threadIdx.x % UVU_UP;");
+        S("  const int g = (threadIdx.x / UVU_UP) % UVU_G;");
+        S("  const long long sn = (long long)blockIdx.x * UVU_FS_SPB + threadIdx.x / (UVU_UP * UVU_G);");
+        S("  if (sn >= N || u >= UVU_U) return;");
+        S("  const int k0 = __ldg(soff + sn), k1 = __ldg(soff + sn + 1);");
+        S(fmt("  const %s* xrow = x + ((size_t)sn * UVU_U + u) * UVU_DX;", T.c_str()));
+        for (int g = 0; g < NG; ++g)
+            S(fmt("  %sif (g == %d) fsend_group%d(k0, k1, u, seid, srecv, xrow, Y, w, out);", g ? "else " : "", g, g));
+        S("}");
+    }
+
     void emit_fwd_edge(Src& S, const std::vector<int>& paths) const {
         emit_products(S, paths);
         for (int pi : paths) {
@@ -1831,6 +1881,8 @@ std::string emit_source(Plan* plan) {
         plan->g_edge = {rpb * owner_threads, rpb, size_t(rpb) * segs * ch * plan->Dy * plan->elem(), false};
     }
     plan->edge_chunk = pipe_recv ? RE.ch : ch;
+    const int fs_spb = std::max(1, 128 / owner_threads);
+    plan->g_fwd_sender = {fs_spb * owner_threads, fs_spb, 0, false};
     if (pipe_dx)
         plan->g_dx = {SD.ut + 32, 1, SD.total, true, SD.ntile};
     else
@@ -1861,6 +1913,8 @@ std::string emit_source(Plan* plan) {
     S(fmt("#define UVU_DX_TPB %d", spb * UP));
     S(fmt("#define UVU_NCW %d", ncw));
     S(fmt("#define UVU_NCT %d", ncw * 32));
+    S(fmt("#define UVU_FS_SPB %d", fs_spb));
+    S(fmt("#define UVU_FS_TPB %d", fs_spb * owner_threads));
     S("// Block-wide barrier usable from the per-group code paths: the non-aligned form may be");
     S("// reached from different call sites, as long as every thread of the block arrives the same");
     S("// number of times (each group runs the same uniform chunk loop).");
@@ -1925,6 +1979,7 @@ std::string emit_source(Plan* plan) {
     else
         G.emit_dx_kernel(S);
     G.emit_dx_reduce(S);
+    G.emit_fwd_sender_kernel(S);
     plan->staged_ok = pipe_recv || NG == 1;
     return S.o.str();
 }

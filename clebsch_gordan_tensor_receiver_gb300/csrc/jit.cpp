@@ -116,7 +116,7 @@ uvu_status module_for_current_device(Plan* plan, DeviceModule** out, std::string
         const char* name;
         cudaKernel_t* k;
     } ks[] = {{"uvu_fwd", &m.fwd}, {"uvu_bwd_edge", &m.bwd_edge}, {"uvu_bwd_dx", &m.bwd_dx},
-              {"uvu_bwd_dx_reduce", &m.bwd_dx_reduce}};
+              {"uvu_bwd_dx_reduce", &m.bwd_dx_reduce}, {"uvu_fwd_sender", &m.fwd_sender}};
     for (auto& k : ks) {
         ce = cudaLibraryGetKernel(k.k, m.lib, k.name);
         if (ce != cudaSuccess) {

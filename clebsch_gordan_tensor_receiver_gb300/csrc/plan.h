@@ -66,7 +66,7 @@ struct AuxLoaded {  // per device
 
 struct DeviceModule {
     cudaLibrary_t lib = nullptr;
-    cudaKernel_t fwd = nullptr, bwd_edge = nullptr, bwd_dx = nullptr, bwd_dx_reduce = nullptr;
+    cudaKernel_t fwd = nullptr, bwd_edge = nullptr, bwd_dx = nullptr, bwd_dx_reduce = nullptr, fwd_sender = nullptr;
     int sm_count = 0;
     int occ_fwd = 1, occ_edge = 1, occ_dx = 1;  // resident blocks per SM
     unsigned* status_word = nullptr;            // device address of uvu_status_word
@@ -82,7 +82,7 @@ struct Plan {
     std::vector<Irrep> xs, ys;
     std::vector<PathInfo> paths;
     std::vector<std::vector<int>> groups;  // path ids per register group
-    KernelGeom g_fwd, g_edge, g_dx;
+    KernelGeom g_fwd, g_edge, g_dx, g_fwd_sender;
     int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
     bool pipelined_recv = false, pipelined_dx = false;
     bool staged_ok = false;   // the edge kernel can write per-edge dx partials (staged dx)

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libuvu.so")
 UVU_F32, UVU_F64 = 0, 1
 UVU_DX_SENDER, UVU_DX_ATOMIC, UVU_DX_STAGED = 0, 1, 2
 UVU_MODULE_CONV, UVU_MODULE_HVP, UVU_MODULE_TP, UVU_MODULE_TP_SHARED = 0, 1, 2, 3
+UVU_FWD_AUTO, UVU_FWD_RECEIVER, UVU_FWD_SENDER = 0, 1, 2
 STATUS = {0: "UVU_OK", 1: "UVU_ERR_INVALID_ARGUMENT", 2: "UVU_ERR_UNSUPPORTED",
           3: "UVU_ERR_COMPILE", 4: "UVU_ERR_CUDA", 5: "UVU_ERR_OUT_OF_MEMORY"}
 
@@ -32,6 +33,7 @@ EXPORTS = (
     "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
     "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
     "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
+    "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
     "uvu_status_string", "uvu_last_error_message",
 )
 
@@ -71,6 +73,10 @@ def _load():
         "uvu_tp_fwd": [P, I64, P, P, P, I, P, P],
         "uvu_tp_bwd": [P, I64, P, P, P, I, P, P, P, P, P, SZ, P],
         "uvu_tp_bwd_workspace": [P, I64, I, ctypes.POINTER(SZ)],
+        "uvu_conv_fwd_model": [P, I64, I64, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_double),
+                               ctypes.POINTER(ctypes.c_double)],
+        "uvu_conv_fwd_sender": [P, I64, I64, P, P, P, P, P, P, P, P],
+        "uvu_conv_fwd_mode": [P, I, I64, I64, P, P, P, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -107,7 +113,8 @@ for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source"
            "uvu_csr_from_sorted_recv", "uvu_csr_transpose_workspace", "uvu_csr_transpose",
            "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
            "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
-           "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace"):
+           "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
+           "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode"):
     globals()[_n] = _wrap(_n)
 
 
@@ -224,6 +231,22 @@ class Plan:
     def fwd(self, n_nodes, x, Y, w, recv_offsets, src, out, stream=None):
         uvu_conv_fwd(self.handle, n_nodes, src.numel() if src is not None else 0, _ptr(x), _ptr(Y),
                      _ptr(w), _ptr(recv_offsets), _ptr(src), _ptr(out), _stream(stream))
+
+    def fwd_model(self, n_nodes, n_edges):
+        """(chosen UVU_FWD_* mode, bytes of the receiver forward, bytes of the sender forward)."""
+        c, br, bs = ctypes.c_int(), ctypes.c_double(), ctypes.c_double()
+        uvu_conv_fwd_model(self.handle, n_nodes, n_edges, ctypes.byref(c), ctypes.byref(br), ctypes.byref(bs))
+        return c.value, br.value, bs.value
+
+    def fwd_sender(self, n_nodes, n_edges, x, Y, w, send_offsets, send_eids, send_recv, out, stream=None):
+        uvu_conv_fwd_sender(self.handle, n_nodes, n_edges, _ptr(x), _ptr(Y), _ptr(w), _ptr(send_offsets),
+                            _ptr(send_eids), _ptr(send_recv), _ptr(out), _stream(stream))
+
+    def fwd_mode(self, mode, n_nodes, n_edges, x, Y, w, graph, out, stream=None):
+        """Forward by mode (UVU_FWD_*) over a Graph holding both CSRs."""
+        uvu_conv_fwd_mode(self.handle, mode, n_nodes, n_edges, _ptr(x), _ptr(Y), _ptr(w),
+                          _ptr(graph.recv_offsets), _ptr(graph.src), _ptr(graph.send_offsets),
+                          _ptr(graph.send_eids), _ptr(graph.send_recv), _ptr(out), _stream(stream))
 
     def bwd_edge(self, n_nodes, x, Y, w, recv_offsets, src, d_out, dY=None, dw=None,
                  dx_atomic=None, dx_edge=None, stream=None):

@@ -274,6 +274,41 @@ uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const
 /* Bytes of device workspace uvu_conv_hvp needs for grad_x (0 when it uses atomic adds). */
 uvu_status uvu_conv_hvp_workspace(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, size_t *bytes);
 
+/* ------------------------------------------- receiver- vs sender-stationary forward ---- */
+
+/* The two ownerships of the convolution's forward ("Receiver-streaming convolutions ...",
+ * replies: a source-stationary and a destination-stationary convolution behind one interface,
+ * the one that moves less data determined from the irreps at init time; opening post: a mode
+ * argument selects an implementation, the auto mode picks one). */
+typedef enum { UVU_FWD_AUTO = 0, UVU_FWD_RECEIVER = 1, UVU_FWD_SENDER = 2 } uvu_fwd_mode;
+
+/* Data-movement model of the two forwards for a graph of this size: bytes moved per launch by
+ * the receiver-stationary forward (w, Y, one gathered x row per edge, one out row per receiver,
+ * CSR) and by the sender-stationary one (w, Y, one x row per sender, out zero-filled plus one
+ * out-row read-modify-write per edge, transposed CSR).  *choice = the smaller (receiver on a
+ * tie).  Host only.  Any output pointer may be NULL. */
+uvu_status uvu_conv_fwd_model(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, uvu_fwd_mode *choice,
+                              double *bytes_receiver, double *bytes_sender);
+
+/* Sender-stationary forward: the same out as uvu_conv_fwd, formed by one thread per (sender,
+ * channel) that keeps its x row in registers, walks the sender's out-edges over the transposed
+ * CSR (send_offsets, send_eids, send_recv of uvu_csr_transpose) and adds each edge's
+ * contribution to out[recv] with reduction atomics after zero-filling out.  The summation order
+ * varies between runs (fp32 results differ in the last bits; within the same tolerance).
+ * Launches: 1 memset + 1 kernel. */
+uvu_status uvu_conv_fwd_sender(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
+                               const void *Y, const void *w, const int32_t *send_offsets,
+                               const int32_t *send_eids, const int32_t *send_recv, void *out,
+                               uvu_stream_t stream);
+
+/* Forward by mode: UVU_FWD_RECEIVER = uvu_conv_fwd (needs recv_offsets, src), UVU_FWD_SENDER =
+ * uvu_conv_fwd_sender (needs the transposed CSR), UVU_FWD_AUTO = the one uvu_conv_fwd_model
+ * chooses (the arrays of the other mode may be NULL). */
+uvu_status uvu_conv_fwd_mode(uvu_plan_t plan, uvu_fwd_mode mode, int64_t n_nodes, int64_t n_edges,
+                             const void *x, const void *Y, const void *w, const int32_t *recv_offsets,
+                             const int32_t *src, const int32_t *send_offsets, const int32_t *send_eids,
+                             const int32_t *send_recv, void *out, uvu_stream_t stream);
+
 /* ------------------------------------------------------- batched tensor product (no graph) ---- */
 
 /* The channel-wise CG tensor product on its own, over a batch of B independent samples ("An

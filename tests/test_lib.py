@@ -116,3 +116,21 @@ def test_batched_tensor_product_host_checks():
     assert p.tp_workspace_bytes(10 ** 6, True) == 2048 * i.n_paths * i.mul * 8
     with pytest.raises(uvu.UVUError):
         p.tp_workspace_bytes(-1, True)
+
+
+def test_forward_data_movement_model():
+    """uvu_conv_fwd_model: the byte counts of the two forwards and the choice between them.
+    MACE-medium (D_x = 4, D_out = 55) gathers little x per edge but has wide out rows, so the
+    receiver-stationary forward moves less; an invariant readout of wide x (D_x = 25, D_out = 1)
+    is the opposite."""
+    from clebsch_gordan_tensor_receiver_gb300 import uvu
+    N, E = 5000, 280000
+    p = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3)
+    choice, br, bs = p.fwd_model(N, E)
+    U, P, Dx, Dy, Do, s = 128, 13, 4, 16, 55, 4
+    wY = E * (P * U + Dy) * s
+    assert br == wY + E * U * Dx * s + N * U * Do * s + 4 * (N + 1) + 4 * E
+    assert bs == wY + N * U * Dx * s + N * U * Do * s + 2 * E * U * Do * s + 4 * (N + 1) + 8 * E
+    assert choice == uvu.UVU_FWD_RECEIVER
+    q = uvu.Plan("32x0e+32x1e+32x2e+32x3e+32x4e", "1x0e", 0)
+    assert q.fwd_model(N, E)[0] == uvu.UVU_FWD_SENDER
