@@ -548,6 +548,78 @@ extern "C" uvu_status uvu_conv_fwd_mode(uvu_plan_t plan, uvu_fwd_mode mode, int6
     return fail(UVU_ERR_INVALID_ARGUMENT, "unknown forward mode");
 }
 
+// ------------------------------------------ channel mixing (factorised UVW -> UVU convolution)
+
+namespace uvu {
+namespace {
+uvu_status mix_check(Plan* p, int64_t N, int W) {
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    if (N < 0) return fail(UVU_ERR_INVALID_ARGUMENT, "n_nodes < 0");
+    if (W < 1 || W > 4096) return fail(UVU_ERR_INVALID_ARGUMENT, "w_out must be in [1, 4096]");
+    if (p->P > mix_max_paths()) return fail(UVU_ERR_UNSUPPORTED, "too many paths for the mixing kernels");
+    return UVU_OK;
+}
+}  // namespace
+}  // namespace uvu
+
+extern "C" uvu_status uvu_mix_bwd_workspace(uvu_plan_t plan, int64_t n_nodes, int w_out, size_t* bytes) {
+    Plan* p = get(plan);
+    if (!bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "bytes is NULL");
+    UVU_TRY(mix_check(p, n_nodes, w_out));
+    *bytes = mix_dM_chunks(n_nodes) * size_t(p->P) * p->U * size_t(w_out) * sizeof(double);
+    return ok();
+}
+
+extern "C" uvu_status uvu_mix_fwd(uvu_plan_t plan, int64_t n_nodes, int w_out, const void* in, const void* M,
+                                  void* out, uvu_stream_t stream) {
+    Plan* p = get(plan);
+    UVU_TRY(mix_check(p, n_nodes, w_out));
+    if (n_nodes == 0) return ok();
+    UVU_TRY(need(in, "in"));
+    UVU_TRY(need(M, "M"));
+    UVU_TRY(need(out, "out"));
+    cudaError_t e = launch_mix_fwd(*p, n_nodes, w_out, in, M, out, stream);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "uvu_mix_fwd launch");
+}
+
+extern "C" uvu_status uvu_mix_bwd(uvu_plan_t plan, int64_t n_nodes, int w_out, const void* in, const void* M,
+                                  const void* d_out, void* d_in, void* dM, void* workspace, size_t workspace_bytes,
+                                  uvu_stream_t stream) {
+    Plan* p = get(plan);
+    UVU_TRY(mix_check(p, n_nodes, w_out));
+    UVU_TRY(opt(d_in, "d_in"));
+    UVU_TRY(opt(dM, "dM"));
+    if (!d_in && !dM) return ok();
+    if (n_nodes > 0) UVU_TRY(need(d_out, "d_out"));
+    if (d_in && n_nodes > 0) {
+        UVU_TRY(need(M, "M"));
+        cudaError_t e = launch_mix_bwd_in(*p, n_nodes, w_out, d_out, M, d_in, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "uvu_mix_bwd d_in launch");
+    }
+    if (dM) {
+        size_t need_ws = 0;
+        UVU_TRY(uvu_mix_bwd_workspace(plan, n_nodes, w_out, &need_ws));
+        if (n_nodes > 0) {
+            UVU_TRY(need(in, "in"));
+            if (!workspace || workspace_bytes < need_ws)
+                return fail(UVU_ERR_INVALID_ARGUMENT, "dM needs a workspace of uvu_mix_bwd_workspace() bytes");
+            UVU_TRY(need(workspace, "workspace"));
+        }
+        cudaError_t e = launch_mix_bwd_M(*p, n_nodes, w_out, in, d_out, workspace, dM, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "uvu_mix_bwd dM launch");
+    }
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_uvw_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
+                                       const void* Y, const void* w, const int32_t* recv_offsets,
+                                       const int32_t* src, const void* M, int w_out, void* uvu_out, void* out,
+                                       uvu_stream_t stream) {
+    UVU_TRY(mix_check(get(plan), n_nodes, w_out));
+    UVU_TRY(uvu_conv_fwd(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, uvu_out, stream));
+    return uvu_mix_fwd(plan, n_nodes, w_out, uvu_out, M, out, stream);
+}
+
 // ------------------------------------------------------------- batched tensor product (no graph)
 
 namespace uvu {

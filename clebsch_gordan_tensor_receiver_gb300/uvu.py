@@ -34,6 +34,7 @@ EXPORTS = (
     "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
     "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
     "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
+    "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_bwd_workspace", "uvu_conv_uvw_fwd",
     "uvu_status_string", "uvu_last_error_message",
 )
 
@@ -77,6 +78,10 @@ def _load():
                                ctypes.POINTER(ctypes.c_double)],
         "uvu_conv_fwd_sender": [P, I64, I64, P, P, P, P, P, P, P, P],
         "uvu_conv_fwd_mode": [P, I, I64, I64, P, P, P, P, P, P, P, P, P, P],
+        "uvu_mix_fwd": [P, I64, I, P, P, P, P],
+        "uvu_mix_bwd": [P, I64, I, P, P, P, P, P, P, SZ, P],
+        "uvu_mix_bwd_workspace": [P, I64, I, ctypes.POINTER(SZ)],
+        "uvu_conv_uvw_fwd": [P, I64, I64, P, P, P, P, P, P, I, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -114,7 +119,8 @@ for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source"
            "uvu_csr_transpose_noalloc", "uvu_graph_validate", "uvu_conv_fwd", "uvu_conv_bwd_edge",
            "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
            "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
-           "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode"):
+           "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
+           "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_bwd_workspace", "uvu_conv_uvw_fwd"):
     globals()[_n] = _wrap(_n)
 
 
@@ -247,6 +253,32 @@ class Plan:
         uvu_conv_fwd_mode(self.handle, mode, n_nodes, n_edges, _ptr(x), _ptr(Y), _ptr(w),
                           _ptr(graph.recv_offsets), _ptr(graph.src), _ptr(graph.send_offsets),
                           _ptr(graph.send_eids), _ptr(graph.send_recv), _ptr(out), _stream(stream))
+
+    def mix_fwd(self, n_nodes, w_out, inp, M, out, stream=None):
+        """Per-path channel mixing of a UVU output (see uvu_mix_fwd)."""
+        uvu_mix_fwd(self.handle, n_nodes, w_out, _ptr(inp), _ptr(M), _ptr(out), _stream(stream))
+
+    def mix_workspace_bytes(self, n_nodes, w_out) -> int:
+        b = ctypes.c_size_t()
+        uvu_mix_bwd_workspace(self.handle, n_nodes, w_out, ctypes.byref(b))
+        return b.value
+
+    def mix_bwd(self, n_nodes, w_out, inp, M, d_out, d_in=None, dM=None, workspace=None, stream=None):
+        """VJP of mix_fwd; dM needs `workspace` (uint8, mix_workspace_bytes()), allocated here if None."""
+        ws_ptr, ws_bytes = None, 0
+        if dM is not None:
+            need = self.mix_workspace_bytes(n_nodes, w_out)
+            if workspace is None:
+                import torch
+                workspace = torch.empty(need, dtype=torch.uint8, device=dM.device)
+            ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+        uvu_mix_bwd(self.handle, n_nodes, w_out, _ptr(inp), _ptr(M), _ptr(d_out), _ptr(d_in), _ptr(dM),
+                    ws_ptr, ws_bytes, _stream(stream))
+
+    def uvw_fwd(self, n_nodes, x, Y, w, recv_offsets, src, M, w_out, uvu_out, out, stream=None):
+        """Factorised UVW convolution (see uvu_conv_uvw_fwd)."""
+        uvu_conv_uvw_fwd(self.handle, n_nodes, src.numel(), _ptr(x), _ptr(Y), _ptr(w), _ptr(recv_offsets),
+                         _ptr(src), _ptr(M), w_out, _ptr(uvu_out), _ptr(out), _stream(stream))
 
     def bwd_edge(self, n_nodes, x, Y, w, recv_offsets, src, d_out, dY=None, dw=None,
                  dx_atomic=None, dx_edge=None, stream=None):

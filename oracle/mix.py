@@ -14,8 +14,9 @@ receiver's edges:
 
     out_uvw[r,w,ooff(p)+m3] = sum_u M[p,u,w] * out_uvu[r,u,ooff(p)+m3].
 
-``fwd`` and ``vjp`` are that per-path contraction and its gradients, written with
-``numpy.einsum``; ``uvw_conv_brute`` is the UVW convolution with the factorised weights summed
+``fwd`` and ``vjp`` are that per-path contraction and its gradients, each one ``numpy.einsum``
+call (a matrix product over the channel index, left to numpy's contraction routine);
+``uvw_conv_brute`` is the UVW convolution with the factorised weights summed
 edge by edge (no reduction), which pins the reading.
 """
 
@@ -35,7 +36,7 @@ def fwd(lay, inp, M):
     inp, M = np.asarray(inp, dtype=np.float64), np.asarray(M, dtype=np.float64)
     out = np.zeros((inp.shape[0], M.shape[2], lay.dim_out))
     for i, p in enumerate(lay.paths):
-        out[:, :, _so(p)] = np.einsum("nuk,uw->nwk", inp[:, :, _so(p)], M[i])
+        out[:, :, _so(p)] = np.einsum("nuk,uw->nwk", inp[:, :, _so(p)], M[i], optimize=True)
     return out
 
 
@@ -44,8 +45,8 @@ def vjp(lay, inp, M, g):
     inp, M, g = (np.asarray(a, dtype=np.float64) for a in (inp, M, g))
     d_inp, dM = np.zeros_like(inp), np.zeros_like(M)
     for i, p in enumerate(lay.paths):
-        d_inp[:, :, _so(p)] = np.einsum("nwk,uw->nuk", g[:, :, _so(p)], M[i])
-        dM[i] = np.einsum("nuk,nwk->uw", inp[:, :, _so(p)], g[:, :, _so(p)])
+        d_inp[:, :, _so(p)] = np.einsum("nwk,uw->nuk", g[:, :, _so(p)], M[i], optimize=True)
+        dM[i] = np.einsum("nuk,nwk->uw", inp[:, :, _so(p)], g[:, :, _so(p)], optimize=True)
     return d_inp, dM
 
 

@@ -134,3 +134,14 @@ def test_forward_data_movement_model():
     assert choice == uvu.UVU_FWD_RECEIVER
     q = uvu.Plan("32x0e+32x1e+32x2e+32x3e+32x4e", "1x0e", 0)
     assert q.fwd_model(N, E)[0] == uvu.UVU_FWD_SENDER
+
+
+def test_mixing_host_checks():
+    from clebsch_gordan_tensor_receiver_gb300 import uvu
+    import pytest
+    p = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3)
+    assert p.mix_workspace_bytes(5000, 64) == 32 * 13 * 128 * 64 * 8
+    assert p.mix_workspace_bytes(3, 64) == 3 * 13 * 128 * 64 * 8
+    for bad in (0, 5000):
+        with pytest.raises(uvu.UVUError):
+            p.mix_workspace_bytes(10, bad)
