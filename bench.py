@@ -439,6 +439,47 @@ def main(argv=None):
         assert plan.device_status() == 0
         del fs_out
 
+    # channel mixing of the UVU output (the factorised UVW convolution's second step), W = U:
+    # a dense contraction over the channel index, bound by the FP32 FMA pipe (its bytes are the
+    # UVU output in and the mixed output out)
+    if world == 1 and not args.single_mode:
+        Wm = U
+        mgen = torch.Generator(device=dev).manual_seed(77)
+        Mm = torch.randn((P, U, Wm), generator=mgen, device=dev, dtype=tdt) / (U ** 0.5)
+        mo = torch.empty((N, Wm, Do), device=dev, dtype=tdt)
+        mg = torch.randn((N, Wm, Do), generator=mgen, device=dev, dtype=tdt)
+        md_in, mdM = torch.empty_like(out), torch.empty_like(Mm)
+        mws = torch.empty(plan.mix_workspace_bytes(N, Wm), dtype=torch.uint8, device=dev)
+
+        def ev_mix(fn, reps=10):
+            for _ in range(3):
+                fn()
+            ts = []
+            for _ in range(reps):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                ts.append((a, b))
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+        mf = ev_mix(lambda: plan.mix_fwd(N, Wm, out, Mm, mo, stream=stream))
+        mi = ev_mix(lambda: plan.mix_bwd(N, Wm, out, Mm, mg, d_in=md_in, stream=stream))
+        mM = ev_mix(lambda: plan.mix_bwd(N, Wm, out, Mm, mg, dM=mdM, workspace=mws, stream=stream))
+        flops = 2.0 * N * U * Wm * Do
+        # FP32 peak from the unit counts and clocks: 128 FMA lanes per SM x 2 flop x SMs x max SM clock
+        sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = 128 * 2 * sm_count * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        line["mix"] = {"w_out": Wm, "flops_per_launch": flops,
+                       "fwd_ms": mf, "bwd_d_in_ms": mi, "bwd_dM_ms": mM,
+                       "fwd_tflops": flops / (mf / 1000) / 1e12, "bwd_d_in_tflops": flops / (mi / 1000) / 1e12,
+                       "bwd_dM_tflops": flops / (mM / 1000) / 1e12,
+                       "alu_peak_tflops": alu_peak, "fwd_alu_frac": flops / (mf / 1000) / 1e12 / alu_peak,
+                       "note": "bound alu: fp32 FMA peak = 128 lanes x 2 flop x SMs x max SM clock"}
+        assert plan.device_status() == 0
+        del Mm, mo, mg, md_in, mdM, mws
+
     # batched (non-convolution) tensor product on the same irreps: B samples, per-sample and
     # batch-shared weights, forward and VJP (dx, dy, dw); inputs drawn on the device (seeded)
     if not args.no_tp and world == 1 and info.mul >= 32:

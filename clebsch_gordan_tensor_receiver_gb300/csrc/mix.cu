@@ -3,7 +3,7 @@
 // that can be reduced to UVU).  With per-edge weights W_e[p,u,w] = w[e,p,u] M[p,u,w], the
 // mixing M is the same on every edge and commutes with the sum over a receiver's edges:
 //     out[r,w,ooff(p)+m3] = sum_u M[p,u,w] in[r,u,ooff(p)+m3]        in = the UVU output.
-// Three kernels: the mixing, its input gradient (the same contraction with M transposed) and
+// Two kernels: the mixing and its input gradient (one tiled product kernel, M or M transposed) and
 // dM[p,u,w] = sum_r sum_m3 in[r,u,ooff+m3] g[r,w,ooff+m3], the last one over fixed receiver
 // chunks into fp64 partial rows that are then added in chunk order (deterministic).
 #include "plan.h"
@@ -12,7 +12,6 @@ namespace uvu {
 namespace {
 
 constexpr int kMaxD3 = 9;   // 2 l3 + 1 for l3 <= 4
-constexpr int kMT = 128;    // threads per block of the row kernels
 constexpr int kMaxPaths = 128;
 
 struct PathTab {
@@ -21,54 +20,110 @@ struct PathTab {
     int d3[kMaxPaths];
 };
 
-// out[r, c0 + t, :] for RB receivers per block, channels c0 .. c0 + kMT - 1 of the output side:
-//   out[r, c, ooff+m] = sum_k A(p, k, c) in[r, k, ooff+m],  A(p, k, c) = M[(p K + k) ldk + c] when
-// k runs over the input channels (forward: K = U, C = W, A = M), or M[(p C + c) ldk + k] for the
-// input gradient (K = W, C = U, A = M transposed).
-template <typename T, int RB, bool TRANS>
-__global__ void __launch_bounds__(kMT) mix_rows(int64_t N, int K, int C, int Do, PathTab tab,
+// The mixing and its input gradient are, per path p, a dense product
+//   out_p[q, c] = sum_k in_p[q, k] B_p[k, c],   q = (r, m) over N x (2 l3 + 1) rows,
+// with in_p[q, k] = in[r, k, ooff + m] and B_p = M[p] (forward: K = U, C = W) or M[p]^T (input
+// gradient: K = W, C = U).  One block computes a 64-row x 128-column tile of one path with 256
+// threads, each owning a 4 x 8 register tile; k advances in chunks of 32 staged in shared memory
+// (rows of `in` gathered as (r, m) pairs, M read along its contiguous index).
+constexpr int kRows = 64, kCols = 128, kK = 32;
+
+struct TileTab {
+    int n;
+    int ooff[kMaxPaths];
+    int d3[kMaxPaths];
+    int tile0[kMaxPaths + 1];  // first row-tile index of each path (prefix over paths)
+};
+
+template <typename T, bool TRANS>
+__global__ void __launch_bounds__(256) mix_gemm(int64_t N, int K, int C, int Do, TileTab tab,
                                                 const T* __restrict__ in, const T* __restrict__ M,
                                                 T* __restrict__ out) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    T* s_in = reinterpret_cast<T*>(smem_raw);            // [RB][K][Do]
-    T* s_out = s_in + size_t(RB) * K * Do;               // [RB][kMT][Do]
-    const int64_t r0 = int64_t(blockIdx.x) * RB;
-    const int c0 = blockIdx.y * kMT, tc = threadIdx.x, c = c0 + tc;
-    const int nr = int(N - r0 < RB ? N - r0 : int64_t(RB));
-    const int nc = min(kMT, C - c0);
-    for (int64_t i = threadIdx.x; i < int64_t(nr) * K * Do; i += kMT) s_in[i] = in[r0 * K * Do + i];
-    __syncthreads();
-    if (c < C) {
-        for (int pi = 0; pi < tab.n; ++pi) {
-            const int o = tab.ooff[pi], d = tab.d3[pi];
-            T acc[RB][kMaxD3];
+    __shared__ __align__(16) T sA[kK][kRows];   // A transposed: [k][q]
+    __shared__ __align__(16) T sB[kK][kCols];   // [k][c]
+    int pi = 0;
+    while (pi + 1 < tab.n && int(blockIdx.x) >= tab.tile0[pi + 1]) ++pi;
+    const int o = tab.ooff[pi], d = tab.d3[pi];
+    const int64_t nq = N * d;
+    const int64_t q0 = int64_t(int(blockIdx.x) - tab.tile0[pi]) * kRows;
+    const int c0 = blockIdx.y * kCols;
+    const int tr = threadIdx.x / 16, tc = threadIdx.x % 16;
+    T acc[4][8];
 #pragma unroll
-            for (int rb = 0; rb < RB; ++rb)
+    for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int m = 0; m < kMaxD3; ++m) acc[rb][m] = 0;
-            for (int k = 0; k < K; ++k) {
-                const T a = TRANS ? __ldg(M + (size_t(pi) * C + c) * K + k) : __ldg(M + (size_t(pi) * K + k) * C + c);
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0;
+    // The next k-chunk's elements are loaded into registers while the current one is computed
+    // (8 of A and 16 of B per thread).  Both tiles are staged with the row / column index
+    // fastest across threads (conflict-free shared-memory writes); M is small and L2-resident.
+    T ra[kRows * kK / 256], rb[kK * kCols / 256];
+    auto load = [&](int k0) {
 #pragma unroll
-                for (int rb = 0; rb < RB; ++rb) {
-                    const T* row = s_in + (size_t(rb) * K + k) * Do + o;
-#pragma unroll
-                    for (int m = 0; m < kMaxD3; ++m)
-                        if (m < d) acc[rb][m] = fma(a, row[m], acc[rb][m]);
-                }
+        for (int t = 0; t < kRows * kK / 256; ++t) {
+            const int e = threadIdx.x + t * 256;
+            const int qi = e % kRows, ki = e / kRows;
+            const int64_t q = q0 + qi;
+            const int k = k0 + ki;
+            T v = 0;
+            if (q < nq && k < K) {
+                const int64_t r = q / d;
+                const int m = int(q - r * d);
+                v = in[(r * K + k) * Do + o + m];
             }
-#pragma unroll
-            for (int rb = 0; rb < RB; ++rb)
-#pragma unroll
-                for (int m = 0; m < kMaxD3; ++m)
-                    if (m < d) s_out[(size_t(rb) * kMT + tc) * Do + o + m] = acc[rb][m];
+            ra[t] = v;
         }
+#pragma unroll
+        for (int t = 0; t < kK * kCols / 256; ++t) {
+            const int e = threadIdx.x + t * 256;
+            const int ci = e % kCols, ki = e / kCols;
+            const int k = k0 + ki, c = c0 + ci;
+            T v = 0;
+            if (k < K && c < C) v = TRANS ? M[(size_t(pi) * C + c) * K + k] : M[(size_t(pi) * K + k) * C + c];
+            rb[t] = v;
+        }
+    };
+    auto store = [&]() {
+#pragma unroll
+        for (int t = 0; t < kRows * kK / 256; ++t) {
+            const int e = threadIdx.x + t * 256;
+            sA[e / kRows][e % kRows] = ra[t];
+        }
+#pragma unroll
+        for (int t = 0; t < kK * kCols / 256; ++t) {
+            const int e = threadIdx.x + t * 256;
+            sB[e / kCols][e % kCols] = rb[t];
+        }
+    };
+    load(0);
+    for (int k0 = 0; k0 < K; k0 += kK) {
+        store();
+        __syncthreads();
+        if (k0 + kK < K) load(k0 + kK);
+#pragma unroll 8
+        for (int ki = 0; ki < kK; ++ki) {
+            T a[4], b[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = sA[ki][tr * 4 + i];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) b[j] = sB[ki][tc * 8 + j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[i][j] = fma(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    // the block's output rows [r][c0 .. c0 + nc)[0 .. Do) are contiguous: coalesced copy-out
-    for (int rb = 0; rb < nr; ++rb) {
-        T* dst = out + ((r0 + rb) * C + c0) * Do;
-        const T* srcp = s_out + size_t(rb) * kMT * Do;
-        for (int i = threadIdx.x; i < nc * Do; i += kMT) dst[i] = srcp[i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int64_t q = q0 + tr * 4 + i;
+        if (q >= nq) continue;
+        const int64_t r = q / d;
+        const int m = int(q - r * d);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = c0 + tc * 8 + j;
+            if (c < C) out[(r * C + c) * Do + o + m] = acc[i][j];
+        }
     }
 }
 
@@ -146,29 +201,21 @@ PathTab make_tab(const Plan& p) {
 
 template <typename T, bool TRANS>
 cudaError_t rows_launch(const Plan& p, int64_t N, int K, int C, const void* in, const void* M, void* out, cudaStream_t st) {
-    const PathTab tab = make_tab(p);
-    const int Do = p.Do;
-    // two receivers per block when their rows fit in shared memory, else one
-    const size_t per = (size_t(K) + kMT) * Do * sizeof(T);
-    const bool two = 2 * per <= 200 * 1024;
-    const size_t smem = (two ? 2 : 1) * per;
-    if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
-    const int rb = two ? 2 : 1;
-    dim3 grid(unsigned((N + rb - 1) / rb), unsigned((C + kMT - 1) / kMT));
-    const T* a = static_cast<const T*>(in);
-    const T* m = static_cast<const T*>(M);
-    T* o = static_cast<T*>(out);
-    cudaError_t e;
-    if (two) {
-        auto k = mix_rows<T, 2, TRANS>;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e == cudaSuccess) k<<<grid, kMT, smem, st>>>(N, K, C, Do, tab, a, m, o);
-    } else {
-        auto k = mix_rows<T, 1, TRANS>;
-        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e == cudaSuccess) k<<<grid, kMT, smem, st>>>(N, K, C, Do, tab, a, m, o);
+    TileTab tab{};
+    tab.n = p.P;
+    int64_t tiles = 0;
+    for (int i = 0; i < p.P && i < kMaxPaths; ++i) {
+        tab.ooff[i] = p.paths[i].ooff;
+        tab.d3[i] = 2 * p.paths[i].l3 + 1;
+        tab.tile0[i] = int(tiles);
+        tiles += (N * tab.d3[i] + kRows - 1) / kRows;
     }
-    return e != cudaSuccess ? e : cudaGetLastError();
+    tab.tile0[p.P] = int(tiles);
+    if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
+    dim3 grid(unsigned(tiles), unsigned((C + kCols - 1) / kCols));
+    mix_gemm<T, TRANS><<<grid, 256, 0, st>>>(N, K, C, p.Do, tab, static_cast<const T*>(in), static_cast<const T*>(M),
+                                             static_cast<T*>(out));
+    return cudaGetLastError();
 }
 
 }  // namespace
