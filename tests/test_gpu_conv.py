@@ -43,6 +43,8 @@ CUSTOM = [
     ("64x0e+64x1o+64x2e", SH3, 3, "float64", 23, 8),      # fp64 with register groups
     ("3x0e+3x1o", "1x0e+1x1o+1x2e", 2, "float32", 11, 5),  # three channels
     ("128x0e+128x1o", SH3, 3, "float32", 300, 70),        # medium shapes, ragged, many chunks
+    ("33x0e+33x1o+33x2e", SH3, 3, "float32", 29, 9),      # pipelined, x rows not 16-byte multiples (no bulk x)
+    ("40x1o", "1x0e+1x1o+1x2e", 2, "float64", 17, 7),     # pipelined, Y rows not bulk, even D_out (padded stride)
 ]
 
 

@@ -59,6 +59,8 @@ CUSTOM = [
     ("48x0e+48x1o+48x2e", SH3, 3, "float32", 29, 9),
     ("64x0e+64x1o+64x2e", SH3, 3, "float64", 17, 6),   # several register groups
     ("8x1o+8x2e", "1x0e+1x1o+1x2e", 4, "float32", 13, 5),
+    ("33x0e+33x1o+33x2e", SH3, 3, "float32", 15, 6),      # pipelined, x and ax rows read directly
+    ("40x1o", "1x0e+1x1o+1x2e", 2, "float64", 11, 5),     # pipelined, Y and aY rows read directly
 ]
 
 

@@ -36,6 +36,8 @@ CASES = [
     ("48x0e+48x1o+48x2e", SH3, 3, "float32", 40),
     ("128x0e+128x1o", SH3, 3, "float32", 300),
     ("64x0e+64x1o+64x2e", SH3, 3, "float64", 25),   # several register groups
+    ("33x0e+33x1o+33x2e", SH3, 3, "float32", 13),   # x rows read directly (not 16-byte multiples)
+    ("40x1o", "1x0e+1x1o+1x2e", 2, "float64", 9),   # y rows read directly, even D_out
 ]
 
 
