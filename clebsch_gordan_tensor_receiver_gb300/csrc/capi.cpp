@@ -10,6 +10,8 @@
 #include <memory>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "plan.h"
 
 struct uvu_plan_s {
@@ -18,6 +20,16 @@ struct uvu_plan_s {
 
 namespace uvu {
 namespace {
+
+// An NVTX range around each C-ABI call, named after the entry point (visible in Nsight traces;
+// a no-op without a profiler attached).
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+};
+#define UVU_RANGE(name) ::uvu::Range uvu_nvtx_range_(name)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -79,6 +91,7 @@ using namespace uvu;
 
 extern "C" uvu_status uvu_plan_create(const char* irreps_x, const char* irreps_sh, int lmax_out,
                                       uvu_dtype dtype, uvu_plan_t* plan_out) {
+    UVU_RANGE("uvu_plan_create");
     if (!plan_out) return fail(UVU_ERR_INVALID_ARGUMENT, "plan_out is NULL");
     *plan_out = nullptr;
     if (!irreps_x || !irreps_sh) return fail(UVU_ERR_INVALID_ARGUMENT, "irreps string is NULL");
@@ -119,6 +132,7 @@ extern "C" uvu_status uvu_plan_create(const char* irreps_x, const char* irreps_s
 }
 
 extern "C" uvu_status uvu_plan_destroy(uvu_plan_t plan) {
+    UVU_RANGE("uvu_plan_destroy");
     if (!plan) return ok();
     for (auto& kv : plan->p.modules) {
         int cur = 0;
@@ -167,6 +181,7 @@ extern "C" uvu_status uvu_plan_source(uvu_plan_t plan, const char** source, cons
 }
 
 extern "C" uvu_status uvu_plan_module_source(uvu_plan_t plan, uvu_module module, const char** source, const char** log) {
+    UVU_RANGE("uvu_plan_module_source");
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
     if (module == UVU_MODULE_CONV) return uvu_plan_source(plan, source, log);
@@ -183,6 +198,7 @@ extern "C" uvu_status uvu_plan_module_source(uvu_plan_t plan, uvu_module module,
 
 extern "C" uvu_status uvu_csr_from_sorted_recv(int64_t n_nodes, int64_t n_edges, const int32_t* recv,
                                                int32_t* recv_offsets, uvu_stream_t stream) {
+    UVU_RANGE("uvu_csr_from_sorted_recv");
     UVU_TRY(check_sizes(n_nodes, n_edges));
     if (!recv_offsets) return fail(UVU_ERR_INVALID_ARGUMENT, "recv_offsets is NULL");
     if (n_edges > 0 && !recv) return fail(UVU_ERR_INVALID_ARGUMENT, "recv is NULL");
@@ -202,6 +218,7 @@ extern "C" uvu_status uvu_csr_transpose(int64_t n_nodes, int64_t n_edges, const 
                                         const int32_t* src, int32_t* send_offsets, int32_t* send_eids,
                                         int32_t* send_recv, void* workspace, size_t workspace_bytes,
                                         uvu_stream_t stream) {
+    UVU_RANGE("uvu_csr_transpose");
     UVU_TRY(check_sizes(n_nodes, n_edges));
     if (!send_offsets || !workspace) return fail(UVU_ERR_INVALID_ARGUMENT, "send_offsets or workspace is NULL");
     if (n_edges > 0 && (!recv_offsets || !src || !send_eids || !send_recv))
@@ -218,6 +235,7 @@ extern "C" uvu_status uvu_csr_transpose(int64_t n_nodes, int64_t n_edges, const 
 extern "C" uvu_status uvu_graph_validate(int64_t n_nodes, int64_t n_edges, const int32_t* recv_offsets,
                                          const int32_t* src, void* workspace, int64_t* n_bad,
                                          uvu_stream_t stream) {
+    UVU_RANGE("uvu_graph_validate");
     UVU_TRY(check_sizes(n_nodes, n_edges));
     if (!recv_offsets || !workspace || !n_bad || (n_edges > 0 && !src))
         return fail(UVU_ERR_INVALID_ARGUMENT, "NULL argument");
@@ -235,6 +253,7 @@ extern "C" uvu_status uvu_graph_validate(int64_t n_nodes, int64_t n_edges, const
 extern "C" uvu_status uvu_conv_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
                                    const void* Y, const void* w, const int32_t* recv_offsets,
                                    const int32_t* src, void* out, uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_fwd");
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
     UVU_TRY(check_sizes(n_nodes, n_edges));
@@ -261,6 +280,7 @@ extern "C" uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_
                                         const void* Y, const void* w, const int32_t* recv_offsets,
                                         const int32_t* src, const void* d_out, void* dY, void* dw,
                                         void* dx_atomic, void* dx_edge, uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_bwd_edge");
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
     UVU_TRY(check_sizes(n_nodes, n_edges));
@@ -297,6 +317,7 @@ extern "C" uvu_status uvu_conv_bwd_edge(uvu_plan_t plan, int64_t n_nodes, int64_
 extern "C" uvu_status uvu_conv_bwd_dx_reduce(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges,
                                              const int32_t* send_offsets, const int32_t* send_eids,
                                              const void* dx_edge, void* dx, uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_bwd_dx_reduce");
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
     UVU_TRY(check_sizes(n_nodes, n_edges));
@@ -332,6 +353,7 @@ extern "C" uvu_status uvu_conv_bwd_dx(uvu_plan_t plan, int64_t n_nodes, int64_t 
                                       const void* w, const int32_t* send_offsets, const int32_t* send_eids,
                                       const int32_t* send_recv, const void* d_out, void* dx,
                                       uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_bwd_dx");
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
     UVU_TRY(check_sizes(n_nodes, n_edges));
@@ -361,6 +383,7 @@ extern "C" uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
                                    const int32_t* send_recv, const void* d_out, void* dx, void* dY, void* dw,
                                    uvu_dx_mode dx_mode, void* workspace, size_t workspace_bytes,
                                    uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_bwd");
     if (dx_mode != UVU_DX_SENDER && dx_mode != UVU_DX_ATOMIC && dx_mode != UVU_DX_STAGED)
         return fail(UVU_ERR_INVALID_ARGUMENT, "dx_mode must be UVU_DX_SENDER, UVU_DX_ATOMIC or UVU_DX_STAGED");
     if (dx_mode == UVU_DX_ATOMIC)
@@ -384,6 +407,7 @@ extern "C" uvu_status uvu_conv_bwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
 }
 
 extern "C" uvu_status uvu_plan_device_status(uvu_plan_t plan, unsigned* word, int reset) {
+    UVU_RANGE("uvu_plan_device_status");
     Plan* p = get(plan);
     if (!p || !word) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or word is NULL");
     DeviceModule* m = nullptr;
@@ -423,6 +447,7 @@ extern "C" uvu_status uvu_conv_hvp(uvu_plan_t plan, int64_t n_nodes, int64_t n_e
                                    const void* d_out, const void* ax, const void* aY, const void* aw,
                                    void* grad_d_out, void* grad_x, void* grad_Y, void* grad_w, void* workspace,
                                    size_t workspace_bytes, uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_hvp");
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
     UVU_TRY(check_sizes(n_nodes, n_edges));
@@ -514,6 +539,7 @@ extern "C" uvu_status uvu_conv_fwd_sender(uvu_plan_t plan, int64_t n_nodes, int6
                                           const void* Y, const void* w, const int32_t* send_offsets,
                                           const int32_t* send_eids, const int32_t* send_recv, void* out,
                                           uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_fwd_sender");
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
     UVU_TRY(check_sizes(n_nodes, n_edges));
@@ -541,6 +567,7 @@ extern "C" uvu_status uvu_conv_fwd_mode(uvu_plan_t plan, uvu_fwd_mode mode, int6
                                         const void* x, const void* Y, const void* w, const int32_t* recv_offsets,
                                         const int32_t* src, const int32_t* send_offsets, const int32_t* send_eids,
                                         const int32_t* send_recv, void* out, uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_fwd_mode");
     if (mode == UVU_FWD_AUTO) UVU_TRY(uvu_conv_fwd_model(plan, n_nodes, n_edges, &mode, nullptr, nullptr));
     if (mode == UVU_FWD_RECEIVER) return uvu_conv_fwd(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, out, stream);
     if (mode == UVU_FWD_SENDER)
@@ -572,6 +599,7 @@ extern "C" uvu_status uvu_mix_bwd_workspace(uvu_plan_t plan, int64_t n_nodes, in
 
 extern "C" uvu_status uvu_mix_fwd(uvu_plan_t plan, int64_t n_nodes, int w_out, const void* in, const void* M,
                                   void* out, uvu_stream_t stream) {
+    UVU_RANGE("uvu_mix_fwd");
     Plan* p = get(plan);
     UVU_TRY(mix_check(p, n_nodes, w_out));
     if (n_nodes == 0) return ok();
@@ -585,6 +613,7 @@ extern "C" uvu_status uvu_mix_fwd(uvu_plan_t plan, int64_t n_nodes, int w_out, c
 extern "C" uvu_status uvu_mix_bwd(uvu_plan_t plan, int64_t n_nodes, int w_out, const void* in, const void* M,
                                   const void* d_out, void* d_in, void* dM, void* workspace, size_t workspace_bytes,
                                   uvu_stream_t stream) {
+    UVU_RANGE("uvu_mix_bwd");
     Plan* p = get(plan);
     UVU_TRY(mix_check(p, n_nodes, w_out));
     UVU_TRY(opt(d_in, "d_in"));
@@ -615,6 +644,7 @@ extern "C" uvu_status uvu_conv_uvw_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t
                                        const void* Y, const void* w, const int32_t* recv_offsets,
                                        const int32_t* src, const void* M, int w_out, void* uvu_out, void* out,
                                        uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_uvw_fwd");
     UVU_TRY(mix_check(get(plan), n_nodes, w_out));
     UVU_TRY(uvu_conv_fwd(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, uvu_out, stream));
     return uvu_mix_fwd(plan, n_nodes, w_out, uvu_out, M, out, stream);
@@ -647,6 +677,7 @@ extern "C" uvu_status uvu_tp_bwd_workspace(uvu_plan_t plan, int64_t batch, int w
 
 extern "C" uvu_status uvu_tp_fwd(uvu_plan_t plan, int64_t batch, const void* x, const void* y, const void* w,
                                  int w_shared, void* out, uvu_stream_t stream) {
+    UVU_RANGE("uvu_tp_fwd");
     Plan* p = get(plan);
     UVU_TRY(tp_check(p, batch));
     if (batch == 0) return ok();
@@ -669,6 +700,7 @@ extern "C" uvu_status uvu_tp_fwd(uvu_plan_t plan, int64_t batch, const void* x, 
 extern "C" uvu_status uvu_tp_bwd(uvu_plan_t plan, int64_t batch, const void* x, const void* y, const void* w,
                                  int w_shared, const void* d_out, void* dx, void* dy, void* dw, void* workspace,
                                  size_t workspace_bytes, uvu_stream_t stream) {
+    UVU_RANGE("uvu_tp_bwd");
     Plan* p = get(plan);
     UVU_TRY(tp_check(p, batch));
     UVU_TRY(opt(dx, "dx"));

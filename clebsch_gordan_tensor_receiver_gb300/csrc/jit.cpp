@@ -5,8 +5,10 @@
 // never inspected.  Identical sources share one compilation through a process-wide cache.
 #include <nvrtc.h>
 
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <fstream>
 #include <functional>
 #include <map>
 #include <mutex>
@@ -25,7 +27,83 @@ struct CacheEntry {
 std::mutex g_cache_mu;
 std::map<std::string, CacheEntry> g_cache;  // keyed by the full source text
 
+// 64-bit FNV-1a of the text (names cache and dump files; the cache also stores the full source
+// and compares it, so a collision cannot return the wrong module).
+std::string text_hash(const std::string& t) {
+    uint64_t h = 1469598103934665603ull;
+    for (unsigned char c : t) h = (h ^ c) * 1099511628211ull;
+    char buf[17];
+    std::snprintf(buf, sizeof buf, "%016llx", (unsigned long long)h);
+    return buf;
+}
+
+const char* env_dir(const char* name) {
+    const char* d = std::getenv(name);
+    return (d && *d) ? d : nullptr;
+}
+
+// Disk cache (UVU_CACHE_DIR): one file per source, holding the source, the cubin and the NVRTC
+// log (the log carries the register/spill report the planner reads).  Written to a temporary
+// name and renamed, so concurrent processes never read a partial file.
+bool cache_read(const std::string& path, const std::string& src, CacheEntry* out) {
+    std::ifstream f(path, std::ios::binary);
+    if (!f) return false;
+    uint64_t n[3];
+    char magic[8];
+    if (!f.read(magic, 8) || std::string(magic, 8) != "UVUCUBN1" || !f.read(reinterpret_cast<char*>(n), sizeof n)) return false;
+    if (n[0] != src.size() || n[1] > (1ull << 30) || n[2] > (1ull << 30)) return false;
+    std::string s(n[0], '\0');
+    out->cubin.resize(n[1]);
+    out->log.assign(n[2], '\0');
+    if (!f.read(&s[0], std::streamsize(n[0])) || s != src) return false;
+    if (!f.read(out->cubin.data(), std::streamsize(n[1])) || !f.read(&out->log[0], std::streamsize(n[2]))) return false;
+    return true;
+}
+
+void cache_write(const std::string& path, const std::string& src, const CacheEntry& e) {
+    const std::string tmp = path + ".tmp" + std::to_string(uint64_t(reinterpret_cast<uintptr_t>(&e)));
+    {
+        std::ofstream f(tmp, std::ios::binary);
+        if (!f) return;
+        const uint64_t n[3] = {src.size(), e.cubin.size(), e.log.size()};
+        f.write("UVUCUBN1", 8);
+        f.write(reinterpret_cast<const char*>(n), sizeof n);
+        f.write(src.data(), std::streamsize(src.size()));
+        f.write(e.cubin.data(), std::streamsize(e.cubin.size()));
+        f.write(e.log.data(), std::streamsize(e.log.size()));
+        if (!f) {
+            std::remove(tmp.c_str());
+            return;
+        }
+    }
+    std::rename(tmp.c_str(), path.c_str());
+}
+
+uvu_status nvrtc_compile_uncached(const std::string& src, CacheEntry* out, std::string* err);
+
+// UVU_FAIL_COMPILE=1 makes every compilation fail (host-side fault injection for the error
+// path); UVU_DUMP_SOURCE=<dir> writes each emitted source there for review.
 uvu_status nvrtc_compile(const std::string& src, CacheEntry* out, std::string* err) {
+    if (const char* f = std::getenv("UVU_FAIL_COMPILE"); f && std::atoi(f) != 0) {
+        *err = "NVRTC compile failed: failure injected by UVU_FAIL_COMPILE";
+        return UVU_ERR_COMPILE;
+    }
+    int ver_major = 0, ver_minor = 0;
+    nvrtcVersion(&ver_major, &ver_minor);
+    const std::string key = text_hash(src + "|nvrtc " + std::to_string(ver_major) + "." + std::to_string(ver_minor));
+    if (const char* d = env_dir("UVU_DUMP_SOURCE")) {
+        std::ofstream f(std::string(d) + "/uvu_" + key + ".cu");
+        f << src;
+    }
+    const char* cdir = env_dir("UVU_CACHE_DIR");
+    const std::string cpath = cdir ? std::string(cdir) + "/uvu_" + key + ".bin" : std::string();
+    if (cdir && cache_read(cpath, src, out)) return UVU_OK;
+    uvu_status s = nvrtc_compile_uncached(src, out, err);
+    if (s == UVU_OK && cdir) cache_write(cpath, src, *out);
+    return s;
+}
+
+uvu_status nvrtc_compile_uncached(const std::string& src, CacheEntry* out, std::string* err) {
     nvrtcProgram prog;
     nvrtcResult r = nvrtcCreateProgram(&prog, src.c_str(), "uvu_plan.cu", 0, nullptr, nullptr);
     if (r != NVRTC_SUCCESS) {

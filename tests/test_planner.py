@@ -77,3 +77,49 @@ def test_hvp_kernels_build_on_the_host(key):
     if p.info.mul >= 32:
         assert "if (hm & 4) bulk_g2s" in src  # aw rows staged only when present
     assert p.hvp_source()[0] == src  # compiled once per plan
+
+
+def _run_child(code, env):
+    import os, subprocess, sys
+    e = dict(os.environ)
+    e.update(env)
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    return subprocess.run([sys.executable, "-c", code], cwd=root, env=e, capture_output=True, text=True, timeout=300)
+
+
+_CHILD = """
+from clebsch_gordan_tensor_receiver_gb300 import uvu
+try:
+    p = uvu.Plan("48x0e+48x1o", "1x0e+1x1o+1x2e", 2)
+    src, log = p.source()
+    print("OK", len(src), "Function properties for uvu_fwd" in log)
+except uvu.UVUError as e:
+    print("ERR", e.status, str(e))
+"""
+
+
+def test_compile_failure_injection():
+    """UVU_FAIL_COMPILE=1 (host-side fault injection): plan creation reports UVU_ERR_COMPILE with
+    the injected message and nothing crashes."""
+    r = _run_child(_CHILD, {"UVU_FAIL_COMPILE": "1"})
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.startswith("ERR 3") and "injected" in r.stdout, r.stdout
+
+
+def test_disk_cache_and_source_dump(tmp_path):
+    """UVU_CACHE_DIR keeps one file per emitted source with the cubin and the NVRTC log (the
+    register/spill report survives a cache hit); UVU_DUMP_SOURCE writes the emitted CUDA C++."""
+    cache, dump = tmp_path / "cache", tmp_path / "dump"
+    cache.mkdir()
+    dump.mkdir()
+    env = {"UVU_CACHE_DIR": str(cache), "UVU_DUMP_SOURCE": str(dump)}
+    first = _run_child(_CHILD, env)
+    assert first.stdout.startswith("OK") and first.stdout.strip().endswith("True"), first.stdout + first.stderr
+    files = sorted(f.name for f in cache.iterdir())
+    assert files and all(f.startswith("uvu_") and f.endswith(".bin") for f in files)
+    stamp = {f.name: f.stat().st_mtime_ns for f in cache.iterdir()}
+    second = _run_child(_CHILD, env)
+    assert second.stdout == first.stdout
+    assert {f.name: f.stat().st_mtime_ns for f in cache.iterdir()} == stamp  # served from the cache
+    dumped = list(dump.glob("uvu_*.cu"))
+    assert dumped and "uvu_fwd" in dumped[0].read_text()
