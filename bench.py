@@ -449,7 +449,7 @@ def main(argv=None):
         mo = torch.empty((N, Wm, Do), device=dev, dtype=tdt)
         mg = torch.randn((N, Wm, Do), generator=mgen, device=dev, dtype=tdt)
         md_in, mdM = torch.empty_like(out), torch.empty_like(Mm)
-        mws = torch.empty(plan.mix_workspace_bytes(N, Wm), dtype=torch.uint8, device=dev)
+        mws = torch.empty(max(plan.mix_workspace_bytes(N, Wm)), dtype=torch.uint8, device=dev)
 
         def ev_mix(fn, reps=10):
             for _ in range(3):
@@ -464,8 +464,8 @@ def main(argv=None):
             torch.cuda.synchronize()
             return statistics.median(a.elapsed_time(b) for a, b in ts)
 
-        mf = ev_mix(lambda: plan.mix_fwd(N, Wm, out, Mm, mo, stream=stream))
-        mi = ev_mix(lambda: plan.mix_bwd(N, Wm, out, Mm, mg, d_in=md_in, stream=stream))
+        mf = ev_mix(lambda: plan.mix_fwd(N, Wm, out, Mm, mo, workspace=mws, stream=stream))
+        mi = ev_mix(lambda: plan.mix_bwd(N, Wm, out, Mm, mg, d_in=md_in, workspace=mws, stream=stream))
         mM = ev_mix(lambda: plan.mix_bwd(N, Wm, out, Mm, mg, dM=mdM, workspace=mws, stream=stream))
         flops = 2.0 * N * U * Wm * Do
         # FP32 peak from the unit counts and clocks: 128 FMA lanes per SM x 2 flop x SMs x max SM clock

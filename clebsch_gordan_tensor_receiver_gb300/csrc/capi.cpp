@@ -589,16 +589,17 @@ uvu_status mix_check(Plan* p, int64_t N, int W) {
 }  // namespace
 }  // namespace uvu
 
-extern "C" uvu_status uvu_mix_bwd_workspace(uvu_plan_t plan, int64_t n_nodes, int w_out, size_t* bytes) {
+extern "C" uvu_status uvu_mix_workspace(uvu_plan_t plan, int64_t n_nodes, int w_out, size_t* fwd_bytes,
+                                        size_t* bwd_bytes) {
     Plan* p = get(plan);
-    if (!bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "bytes is NULL");
     UVU_TRY(mix_check(p, n_nodes, w_out));
-    *bytes = mix_dM_chunks(n_nodes) * size_t(p->P) * p->U * size_t(w_out) * sizeof(double);
+    if (fwd_bytes) *fwd_bytes = mix_workspace_bytes(*p, n_nodes, w_out, false);
+    if (bwd_bytes) *bwd_bytes = mix_workspace_bytes(*p, n_nodes, w_out, true);
     return ok();
 }
 
 extern "C" uvu_status uvu_mix_fwd(uvu_plan_t plan, int64_t n_nodes, int w_out, const void* in, const void* M,
-                                  void* out, uvu_stream_t stream) {
+                                  void* out, void* workspace, size_t workspace_bytes, uvu_stream_t stream) {
     UVU_RANGE("uvu_mix_fwd");
     Plan* p = get(plan);
     UVU_TRY(mix_check(p, n_nodes, w_out));
@@ -606,7 +607,10 @@ extern "C" uvu_status uvu_mix_fwd(uvu_plan_t plan, int64_t n_nodes, int w_out, c
     UVU_TRY(need(in, "in"));
     UVU_TRY(need(M, "M"));
     UVU_TRY(need(out, "out"));
-    cudaError_t e = launch_mix_fwd(*p, n_nodes, w_out, in, M, out, stream);
+    UVU_TRY(need(workspace, "workspace"));
+    if (workspace_bytes < mix_workspace_bytes(*p, n_nodes, w_out, false))
+        return fail(UVU_ERR_INVALID_ARGUMENT, "workspace smaller than uvu_mix_workspace() reports for the forward");
+    cudaError_t e = launch_mix_fwd(*p, n_nodes, w_out, in, M, out, workspace, stream);
     return e == cudaSuccess ? ok() : cuda_fail(e, "uvu_mix_fwd launch");
 }
 
@@ -619,35 +623,26 @@ extern "C" uvu_status uvu_mix_bwd(uvu_plan_t plan, int64_t n_nodes, int w_out, c
     UVU_TRY(opt(d_in, "d_in"));
     UVU_TRY(opt(dM, "dM"));
     if (!d_in && !dM) return ok();
-    if (n_nodes > 0) UVU_TRY(need(d_out, "d_out"));
-    if (d_in && n_nodes > 0) {
-        UVU_TRY(need(M, "M"));
-        cudaError_t e = launch_mix_bwd_in(*p, n_nodes, w_out, d_out, M, d_in, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "uvu_mix_bwd d_in launch");
+    if (n_nodes > 0) {
+        UVU_TRY(need(d_out, "d_out"));
+        if (d_in) UVU_TRY(need(M, "M"));
+        if (dM) UVU_TRY(need(in, "in"));
+        UVU_TRY(need(workspace, "workspace"));
+        if (workspace_bytes < mix_workspace_bytes(*p, n_nodes, w_out, true))
+            return fail(UVU_ERR_INVALID_ARGUMENT, "workspace smaller than uvu_mix_workspace() reports for the backward");
     }
-    if (dM) {
-        size_t need_ws = 0;
-        UVU_TRY(uvu_mix_bwd_workspace(plan, n_nodes, w_out, &need_ws));
-        if (n_nodes > 0) {
-            UVU_TRY(need(in, "in"));
-            if (!workspace || workspace_bytes < need_ws)
-                return fail(UVU_ERR_INVALID_ARGUMENT, "dM needs a workspace of uvu_mix_bwd_workspace() bytes");
-            UVU_TRY(need(workspace, "workspace"));
-        }
-        cudaError_t e = launch_mix_bwd_M(*p, n_nodes, w_out, in, d_out, workspace, dM, stream);
-        if (e != cudaSuccess) return cuda_fail(e, "uvu_mix_bwd dM launch");
-    }
-    return ok();
+    cudaError_t e = launch_mix_bwd(*p, n_nodes, w_out, in, M, d_out, d_in, dM, workspace, stream);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "uvu_mix_bwd launch");
 }
 
 extern "C" uvu_status uvu_conv_uvw_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
                                        const void* Y, const void* w, const int32_t* recv_offsets,
                                        const int32_t* src, const void* M, int w_out, void* uvu_out, void* out,
-                                       uvu_stream_t stream) {
+                                       void* workspace, size_t workspace_bytes, uvu_stream_t stream) {
     UVU_RANGE("uvu_conv_uvw_fwd");
     UVU_TRY(mix_check(get(plan), n_nodes, w_out));
     UVU_TRY(uvu_conv_fwd(plan, n_nodes, n_edges, x, Y, w, recv_offsets, src, uvu_out, stream));
-    return uvu_mix_fwd(plan, n_nodes, w_out, uvu_out, M, out, stream);
+    return uvu_mix_fwd(plan, n_nodes, w_out, uvu_out, M, out, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------- batched tensor product (no graph)

@@ -3,259 +3,366 @@
 // that can be reduced to UVU).  With per-edge weights W_e[p,u,w] = w[e,p,u] M[p,u,w], the
 // mixing M is the same on every edge and commutes with the sum over a receiver's edges:
 //     out[r,w,ooff(p)+m3] = sum_u M[p,u,w] in[r,u,ooff(p)+m3]        in = the UVU output.
-// Two kernels: the mixing and its input gradient (one tiled product kernel, M or M transposed) and
-// dM[p,u,w] = sum_r sum_m3 in[r,u,ooff+m3] g[r,w,ooff+m3], the last one over fixed receiver
-// chunks into fp64 partial rows that are then added in chunk order (deterministic).
+//
+// In the convolution's layout [N][U][D_out] a path's components are a few values inside each
+// 55-106-wide row, so a direct product gathers D_out-strided values.  The kernels here first copy
+// the operand to a component-major layout [D_out][N][U] (one pass, coalesced both ways through a
+// shared-memory tile); a path p is then the contiguous matrix of rows (ooff(p)+m, r), and the
+// mixing is one dense product per path, A_p [d3*N x U] times M[p] [U x W], written component-major
+// and copied back.  The input gradient is the same product with M[p] transposed (copied once per
+// call), and dM[p] = A_p^T G_p is a product over the rows, split into fixed row chunks summed in
+// fp64 (fp32 within 16 rows) and added in chunk order (deterministic).
 #include "plan.h"
 
 namespace uvu {
 namespace {
 
-constexpr int kMaxD3 = 9;   // 2 l3 + 1 for l3 <= 4
 constexpr int kMaxPaths = 128;
 
-struct PathTab {
+// ----------------------------------------------------------------------------- layout copies
+
+// out[b][n][a] = in[n][a][b]  (to component-major: a = channel, b = component), or the inverse
+// out[n][a][b] = in[b][n][a] when INV.  Block = (n, 32 consecutive a); the tile [32][B] passes
+// through shared memory with an odd row pitch.
+template <typename T, bool INV>
+__global__ void __launch_bounds__(256) relayout(int64_t N, int A, int B, const T* __restrict__ in, T* __restrict__ out) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    T* s = reinterpret_cast<T*>(smem_raw);
+    const int pitch = B | 1;
+    const int64_t n = blockIdx.x;
+    const int a0 = blockIdx.y * 32;
+    const int na = min(32, A - a0);
+    if (!INV) {
+        for (int e = threadIdx.x; e < na * B; e += 256) s[(e / B) * pitch + e % B] = in[(n * A + a0) * B + e];
+        __syncthreads();
+        for (int e = threadIdx.x; e < B * 32; e += 256) {
+            const int b = e / 32, al = e % 32;
+            if (al < na) out[(int64_t(b) * N + n) * A + a0 + al] = s[al * pitch + b];
+        }
+    } else {
+        for (int e = threadIdx.x; e < B * 32; e += 256) {
+            const int b = e / 32, al = e % 32;
+            if (al < na) s[al * pitch + b] = in[(int64_t(b) * N + n) * A + a0 + al];
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < na * B; e += 256) out[(n * A + a0) * B + e] = s[(e / B) * pitch + e % B];
+    }
+}
+
+// Mt[p][w][u] = M[p][u][w]
+template <typename T>
+__global__ void transpose_M(int P, int U, int W, const T* __restrict__ M, T* __restrict__ Mt) {
+    const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= int64_t(P) * U * W) return;
+    const int64_t p = i / (int64_t(U) * W), rem = i % (int64_t(U) * W);
+    const int u = int(rem / W), w = int(rem % W);
+    Mt[(p * W + w) * U + u] = M[i];
+}
+
+// ------------------------------------------------------------------- per-path dense products
+
+struct SegTab {
     int n;
-    int ooff[kMaxPaths];
-    int d3[kMaxPaths];
+    int64_t row0[kMaxPaths];   // first row of the path in the component-major operand (ooff * N)
+    int64_t rows[kMaxPaths];   // d3 * N
+    int tile0[kMaxPaths + 1];  // prefix of row tiles
 };
 
-// The mixing and its input gradient are, per path p, a dense product
-//   out_p[q, c] = sum_k in_p[q, k] B_p[k, c],   q = (r, m) over N x (2 l3 + 1) rows,
-// with in_p[q, k] = in[r, k, ooff + m] and B_p = M[p] (forward: K = U, C = W) or M[p]^T (input
-// gradient: K = W, C = U).  One block computes a 64-row x 128-column tile of one path with 256
-// threads, each owning a 4 x 8 register tile; k advances in chunks of 32 staged in shared memory
-// (rows of `in` gathered as (r, m) pairs, M read along its contiguous index).
-constexpr int kRows = 64, kCols = 128, kK = 32;
+constexpr int kTM = 128, kTN = 128, kTK = 8;
 
-struct TileTab {
-    int n;
-    int ooff[kMaxPaths];
-    int d3[kMaxPaths];
-    int tile0[kMaxPaths + 1];  // first row-tile index of each path (prefix over paths)
-};
-
-template <typename T, bool TRANS>
-__global__ void __launch_bounds__(256) mix_gemm(int64_t N, int K, int C, int Do, TileTab tab,
-                                                const T* __restrict__ in, const T* __restrict__ M,
-                                                T* __restrict__ out) {
-    __shared__ __align__(16) T sA[kK][kRows];   // A transposed: [k][q]
-    __shared__ __align__(16) T sB[kK][kCols];   // [k][c]
+// C[row][c] = sum_k A[row][k] Bp[k][c] for the rows of each path (Bp = Bmat + p K Nc), A and C
+// row-major, row = component-major row index.  256 threads with 8 x 8 outputs each (rows
+// tr*4 + {0..3} and 64 + tr*4 + {0..3}, columns likewise: conflict-free shared-memory reads);
+// k advances in chunks of 8, the next chunk loaded into registers during the current one.
+template <typename T>
+__global__ void __launch_bounds__(256) seg_gemm(int K, int Nc, SegTab tab, const T* __restrict__ A,
+                                                const T* __restrict__ Bmat, T* __restrict__ C) {
+    __shared__ __align__(16) T sA[2][kTK][kTM];
+    __shared__ __align__(16) T sB[2][kTK][kTN];
     int pi = 0;
     while (pi + 1 < tab.n && int(blockIdx.x) >= tab.tile0[pi + 1]) ++pi;
-    const int o = tab.ooff[pi], d = tab.d3[pi];
-    const int64_t nq = N * d;
-    const int64_t q0 = int64_t(int(blockIdx.x) - tab.tile0[pi]) * kRows;
-    const int c0 = blockIdx.y * kCols;
-    const int tr = threadIdx.x / 16, tc = threadIdx.x % 16;
-    T acc[4][8];
+    const int64_t rbeg = tab.row0[pi] + int64_t(int(blockIdx.x) - tab.tile0[pi]) * kTM;
+    const int64_t rend = tab.row0[pi] + tab.rows[pi];
+    const int c0 = blockIdx.y * kTN;
+    const T* Bp = Bmat + size_t(pi) * K * Nc;
+    const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
+    // loader roles: A row (tid / 2) with k half (tid % 2) * 4; B k row (tid / 32) with columns (tid % 32) * 4
+    const int la_r = tid / 2, la_k = (tid % 2) * 4;
+    const int lb_k = tid / 32, lb_c = (tid % 32) * 4;
+    T ra[4], rb[4];
+    auto load = [&](int k0) {
+        const int64_t row = rbeg + la_r;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i) {
+            const int k = k0 + la_k + i;
+            ra[i] = (row < rend && k < K) ? A[row * K + k] : T(0);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = k0 + lb_k, c = c0 + lb_c + i;
+            rb[i] = (k < K && c < Nc) ? Bp[size_t(k) * Nc + c] : T(0);
+        }
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sA[buf][la_k + i][la_r] = ra[i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sB[buf][lb_k][lb_c + i] = rb[i];
+    };
+    T acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0;
-    // The next k-chunk's elements are loaded into registers while the current one is computed
-    // (8 of A and 16 of B per thread).  Both tiles are staged with the row / column index
-    // fastest across threads (conflict-free shared-memory writes); M is small and L2-resident.
-    T ra[kRows * kK / 256], rb[kK * kCols / 256];
-    auto load = [&](int k0) {
-#pragma unroll
-        for (int t = 0; t < kRows * kK / 256; ++t) {
-            const int e = threadIdx.x + t * 256;
-            const int qi = e % kRows, ki = e / kRows;
-            const int64_t q = q0 + qi;
-            const int k = k0 + ki;
-            T v = 0;
-            if (q < nq && k < K) {
-                const int64_t r = q / d;
-                const int m = int(q - r * d);
-                v = in[(r * K + k) * Do + o + m];
-            }
-            ra[t] = v;
-        }
-#pragma unroll
-        for (int t = 0; t < kK * kCols / 256; ++t) {
-            const int e = threadIdx.x + t * 256;
-            const int ci = e % kCols, ki = e / kCols;
-            const int k = k0 + ki, c = c0 + ci;
-            T v = 0;
-            if (k < K && c < C) v = TRANS ? M[(size_t(pi) * C + c) * K + k] : M[(size_t(pi) * K + k) * C + c];
-            rb[t] = v;
-        }
-    };
-    auto store = [&]() {
-#pragma unroll
-        for (int t = 0; t < kRows * kK / 256; ++t) {
-            const int e = threadIdx.x + t * 256;
-            sA[e / kRows][e % kRows] = ra[t];
-        }
-#pragma unroll
-        for (int t = 0; t < kK * kCols / 256; ++t) {
-            const int e = threadIdx.x + t * 256;
-            sB[e / kCols][e % kCols] = rb[t];
-        }
-    };
     load(0);
-    for (int k0 = 0; k0 < K; k0 += kK) {
-        store();
-        __syncthreads();
-        if (k0 + kK < K) load(k0 + kK);
-#pragma unroll 8
-        for (int ki = 0; ki < kK; ++ki) {
-            T a[4], b[8];
+    store(0);
+    __syncthreads();
+    int buf = 0;
+    for (int k0 = 0; k0 < K; k0 += kTK) {
+        const bool more = k0 + kTK < K;
+        if (more) load(k0 + kTK);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = sA[ki][tr * 4 + i];
+        for (int k = 0; k < kTK; ++k) {
+            T a[8], b[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) b[j] = sB[ki][tc * 8 + j];
+            for (int i = 0; i < 4; ++i) {
+                a[i] = sA[buf][k][tr * 4 + i];
+                a[4 + i] = sA[buf][k][64 + tr * 4 + i];
+                b[i] = sB[buf][k][tc * 4 + i];
+                b[4 + i] = sB[buf][k][64 + tc * 4 + i];
+            }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) acc[i][j] = fma(a[i], b[j], acc[i][j]);
         }
-        __syncthreads();
+        if (more) {
+            store(buf ^ 1);
+            __syncthreads();
+            buf ^= 1;
+        }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t q = q0 + tr * 4 + i;
-        if (q >= nq) continue;
-        const int64_t r = q / d;
-        const int m = int(q - r * d);
+    for (int i = 0; i < 8; ++i) {
+        const int64_t row = rbeg + (i < 4 ? tr * 4 + i : 64 + tr * 4 + i - 4);
+        if (row >= rend) continue;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int c = c0 + tc * 8 + j;
-            if (c < C) out[(r * C + c) * Do + o + m] = acc[i][j];
+            const int c = c0 + (j < 4 ? tc * 4 + j : 64 + tc * 4 + j - 4);
+            if (c < Nc) C[row * Nc + c] = acc[i][j];
         }
     }
 }
 
-// dM partials: block (u-tile, w-tile) x path x receiver chunk; 16 x 16 threads, each owning a
-// 4 x 4 (u, w) register tile; rows of in and g for the tile staged in shared memory per receiver.
-constexpr int kTile = 64;
+// dM partials: part[ch][p][u][w] = sum over the rows of chunk ch of path p of A[row][u] G[row][w].
+// Block tile 64 u x 64 w, 256 threads with 4 x 4 outputs each.  Rows go in steps of 16 summed in
+// the plan's type; the step sums are added with Kahan compensation, and into fp64 registers every
+// 16 steps.  A plain fp32 sum of a chunk lost digits where the terms cancel, and an fp64 add after
+// every step cost more than the products (FP64 runs at a small fraction of FP32 here).  Stored as
+// fp64; chunks past a path's rows store zero.
+constexpr int kRowChunk = 1024, kDT = 64, kDR = 16;
 template <typename T>
-__global__ void __launch_bounds__(256) mix_dM(int64_t N, int U, int W, int Do, PathTab tab, int64_t chunk,
-                                              const T* __restrict__ in, const T* __restrict__ g,
+__global__ void __launch_bounds__(256) seg_dM(int U, int W, SegTab tab, const T* __restrict__ A, const T* __restrict__ G,
                                               double* __restrict__ part) {
-    __shared__ T s_a[kTile][kMaxD3 + 1];
-    __shared__ T s_b[kTile][kMaxD3 + 1];
-    const int nwt = (W + kTile - 1) / kTile;
-    const int u0 = (blockIdx.x / nwt) * kTile, w0 = (blockIdx.x % nwt) * kTile;
-    const int pi = blockIdx.y;
-    const int64_t ck = blockIdx.z;
-    const int o = tab.ooff[pi], d = tab.d3[pi];
-    const int ty = threadIdx.x / 16, tx = threadIdx.x % 16;
-    // sums over up to 16 receivers in the plan's type, added into fp64 (FP64 FMAs are slow on
-    // this part; a long fp32 sum loses digits where the terms cancel)
+    __shared__ __align__(16) T sA[kDR][kDT];
+    __shared__ __align__(16) T sG[kDR][kDT];
+    const int ntw = (W + kDT - 1) / kDT;
+    const int u0 = (blockIdx.x / ntw) * kDT, w0 = (blockIdx.x % ntw) * kDT;
+    const int pi = blockIdx.y, ch = blockIdx.z;
+    const int64_t rbeg = tab.row0[pi] + int64_t(ch) * kRowChunk;
+    const int64_t rend = min(tab.row0[pi] + tab.rows[pi], rbeg + kRowChunk);
+    const int tid = threadIdx.x, tr = tid / 16, tc = tid % 16;
     double acc[4][4] = {};
-    T acc_c[4][4] = {};
-    int nacc = 0;
-    const int64_t r_end = min(N, (ck + 1) * chunk);
-    for (int64_t r = ck * chunk; r < r_end; ++r) {
-        for (int i = threadIdx.x; i < kTile * d; i += 256) {
-            const int row = i / d, m = i - row * d;
-            const int u = u0 + row, w = w0 + row;
-            s_a[row][m] = u < U ? in[(r * U + u) * Do + o + m] : T(0);
-            s_b[row][m] = w < W ? g[(r * W + w) * Do + o + m] : T(0);
+    T ksum[4][4] = {}, kcomp[4][4] = {};
+    int nstep = 0;
+    for (int64_t r0 = rbeg; r0 < rend; r0 += kDR) {
+        // 16 rows x 64 columns of each operand: 4 consecutive columns per thread
+        {
+            const int lr = tid / 16, lc = (tid % 16) * 4;
+            const int64_t row = r0 + lr;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int u = u0 + lc + i, w = w0 + lc + i;
+                sA[lr][lc + i] = (row < rend && u < U) ? A[row * U + u] : T(0);
+                sG[lr][lc + i] = (row < rend && w < W) ? G[row * W + w] : T(0);
+            }
         }
         __syncthreads();
-        for (int m = 0; m < d; ++m) {
+        T part_acc[4][4] = {};
+#pragma unroll
+        for (int k = 0; k < kDR; ++k) {
             T a[4], b[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = s_a[ty * 4 + i][m];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = s_b[tx * 4 + j][m];
+            for (int i = 0; i < 4; ++i) {
+                a[i] = sA[k][tr + 16 * i];
+                b[i] = sG[k][tc + 16 * i];
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc_c[i][j] = fma(a[i], b[j], acc_c[i][j]);
+                for (int j = 0; j < 4; ++j) part_acc[i][j] = fma(a[i], b[j], part_acc[i][j]);
         }
-        __syncthreads();
-        if (++nacc == 16 || r + 1 == r_end) {
-            nacc = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const T y = part_acc[i][j] - kcomp[i][j];
+                const T t = ksum[i][j] + y;
+                kcomp[i][j] = (t - ksum[i][j]) - y;
+                ksum[i][j] = t;
+            }
+        if (++nstep == 16 || r0 + kDR >= rend) {
+            nstep = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    acc[i][j] += double(acc_c[i][j]);
-                    acc_c[i][j] = T(0);
+                    acc[i][j] += double(ksum[i][j]) - double(kcomp[i][j]);
+                    ksum[i][j] = T(0);
+                    kcomp[i][j] = T(0);
                 }
         }
+        __syncthreads();
     }
-    double* pr = part + (size_t(ck) * tab.n + pi) * size_t(U) * W;
+    double* pr = part + (size_t(ch) * tab.n + pi) * size_t(U) * W;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 4; ++i) {
+        const int u = u0 + tr + 16 * i;
+        if (u >= U) continue;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int u = u0 + ty * 4 + i, w = w0 + tx * 4 + j;
-            if (u < U && w < W) pr[size_t(u) * W + w] = acc[i][j];
+            const int w = w0 + tc + 16 * j;
+            if (w < W) pr[size_t(u) * W + w] = acc[i][j];
         }
+    }
 }
 
-PathTab make_tab(const Plan& p) {
-    PathTab t{};
+// ----------------------------------------------------------------------------------- host side
+
+SegTab make_seg(const Plan& p, int64_t N, int64_t* tiles) {
+    SegTab t{};
     t.n = p.P;
+    int64_t tl = 0;
     for (int i = 0; i < p.P && i < kMaxPaths; ++i) {
-        t.ooff[i] = p.paths[i].ooff;
-        t.d3[i] = 2 * p.paths[i].l3 + 1;
+        t.row0[i] = int64_t(p.paths[i].ooff) * N;
+        t.rows[i] = int64_t(2 * p.paths[i].l3 + 1) * N;
+        t.tile0[i] = int(tl);
+        tl += (t.rows[i] + kTM - 1) / kTM;
     }
+    t.tile0[p.P] = int(tl);
+    if (tiles) *tiles = tl;
     return t;
 }
 
-template <typename T, bool TRANS>
-cudaError_t rows_launch(const Plan& p, int64_t N, int K, int C, const void* in, const void* M, void* out, cudaStream_t st) {
-    TileTab tab{};
-    tab.n = p.P;
-    int64_t tiles = 0;
-    for (int i = 0; i < p.P && i < kMaxPaths; ++i) {
-        tab.ooff[i] = p.paths[i].ooff;
-        tab.d3[i] = 2 * p.paths[i].l3 + 1;
-        tab.tile0[i] = int(tiles);
-        tiles += (N * tab.d3[i] + kRows - 1) / kRows;
+int64_t max_chunks(const Plan& p, int64_t N) {
+    int64_t m = 1;
+    for (int i = 0; i < p.P; ++i) m = std::max<int64_t>(m, (int64_t(2 * p.paths[i].l3 + 1) * N + kRowChunk - 1) / kRowChunk);
+    return m;
+}
+
+template <typename T>
+cudaError_t relayout_launch(int64_t N, int A, int B, bool inv, const void* in, void* out, cudaStream_t st) {
+    const size_t smem = size_t(32) * (B | 1) * sizeof(T);
+    dim3 grid(unsigned(N), unsigned((A + 31) / 32));
+    cudaError_t e;
+    if (inv) {
+        auto k = relayout<T, true>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e == cudaSuccess) k<<<grid, 256, smem, st>>>(N, A, B, static_cast<const T*>(in), static_cast<T*>(out));
+    } else {
+        auto k = relayout<T, false>;
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e == cudaSuccess) k<<<grid, 256, smem, st>>>(N, A, B, static_cast<const T*>(in), static_cast<T*>(out));
     }
-    tab.tile0[p.P] = int(tiles);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// in [N][K][Do] -> out [N][Nc][Do] through component-major copies in ws: [Do N K] then [Do N Nc]
+template <typename T>
+cudaError_t mix_product(const Plan& p, int64_t N, int K, int Nc, const void* in, const void* Bmat, void* out,
+                        void* ws, cudaStream_t st) {
+    T* inT = static_cast<T*>(ws);
+    T* outT = reinterpret_cast<T*>(static_cast<char*>(ws) + (size_t(N) * p.Do * K * sizeof(T) + 255) / 256 * 256);
+    cudaError_t e = relayout_launch<T>(N, K, p.Do, false, in, inT, st);
+    if (e != cudaSuccess) return e;
+    int64_t tiles = 0;
+    const SegTab tab = make_seg(p, N, &tiles);
     if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
-    dim3 grid(unsigned(tiles), unsigned((C + kCols - 1) / kCols));
-    mix_gemm<T, TRANS><<<grid, 256, 0, st>>>(N, K, C, p.Do, tab, static_cast<const T*>(in), static_cast<const T*>(M),
-                                             static_cast<T*>(out));
-    return cudaGetLastError();
+    seg_gemm<T><<<dim3(unsigned(tiles), unsigned((Nc + kTN - 1) / kTN)), 256, 0, st>>>(
+        K, Nc, tab, inT, static_cast<const T*>(Bmat), outT);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return relayout_launch<T>(N, Nc, p.Do, true, outT, out, st);
 }
 
 }  // namespace
 
 int mix_max_paths() { return kMaxPaths; }
-int mix_max_d3() { return kMaxD3; }
 
-size_t mix_dM_chunks(int64_t N) { return size_t(std::min<int64_t>(std::max<int64_t>(N, 1), 32)); }
+namespace {
+size_t r256(size_t b) { return (b + 255) / 256 * 256; }
+}  // namespace
 
-cudaError_t launch_mix_fwd(const Plan& p, int64_t N, int W, const void* in, const void* M, void* out, cudaStream_t st) {
-    if (N == 0) return cudaSuccess;
-    return p.dtype == UVU_F64 ? rows_launch<double, false>(p, N, p.U, W, in, M, out, st)
-                              : rows_launch<float, false>(p, N, p.U, W, in, M, out, st);
+// Workspace regions (each starting on a 256-byte boundary).  Forward: [in | out] component-major.
+// Backward: [g | d_in] component-major (the input-gradient product; g alone for dM), in
+// component-major, M transposed, fp64 dM partials.
+size_t mix_workspace_bytes(const Plan& p, int64_t N, int W, bool bwd) {
+    const size_t s = p.elem(), ND = size_t(N) * p.Do;
+    const size_t U = size_t(p.U);
+    if (!bwd) return r256(ND * U * s) + r256(ND * W * s);
+    return r256(ND * W * s) + r256(ND * U * s) + r256(ND * U * s) + r256(size_t(p.P) * U * W * s) +
+           r256(size_t(max_chunks(p, N)) * p.P * U * W * sizeof(double));
 }
 
-cudaError_t launch_mix_bwd_in(const Plan& p, int64_t N, int W, const void* g, const void* M, void* d_in, cudaStream_t st) {
+cudaError_t launch_mix_fwd(const Plan& p, int64_t N, int W, const void* in, const void* M, void* out, void* ws,
+                           cudaStream_t st) {
     if (N == 0) return cudaSuccess;
-    return p.dtype == UVU_F64 ? rows_launch<double, true>(p, N, W, p.U, g, M, d_in, st)
-                              : rows_launch<float, true>(p, N, W, p.U, g, M, d_in, st);
+    return p.dtype == UVU_F64 ? mix_product<double>(p, N, p.U, W, in, M, out, ws, st)
+                              : mix_product<float>(p, N, p.U, W, in, M, out, ws, st);
 }
 
-cudaError_t launch_mix_bwd_M(const Plan& p, int64_t N, int W, const void* in, const void* g, void* part, void* dM,
-                             cudaStream_t st) {
-    const int64_t cols = int64_t(p.P) * p.U * W;
-    if (N == 0) return cudaMemsetAsync(dM, 0, size_t(cols) * p.elem(), st);
-    const PathTab tab = make_tab(p);
-    const int64_t C = int64_t(mix_dM_chunks(N));
-    const int64_t chunk = (N + C - 1) / C;
-    const unsigned tiles = unsigned(((p.U + kTile - 1) / kTile) * ((W + kTile - 1) / kTile));
-    dim3 grid(tiles, unsigned(p.P), unsigned(C));
-    double* pr = static_cast<double*>(part);
-    if (p.dtype == UVU_F64)
-        mix_dM<double><<<grid, 256, 0, st>>>(N, p.U, W, p.Do, tab, chunk, static_cast<const double*>(in),
-                                              static_cast<const double*>(g), pr);
-    else
-        mix_dM<float><<<grid, 256, 0, st>>>(N, p.U, W, p.Do, tab, chunk, static_cast<const float*>(in),
-                                             static_cast<const float*>(g), pr);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_column_sum(part, C, cols, dM, p.dtype == UVU_F64, st);
+cudaError_t launch_mix_bwd(const Plan& p, int64_t N, int W, const void* in, const void* M, const void* g, void* d_in,
+                           void* dM, void* ws, cudaStream_t st) {
+    const size_t s = p.elem(), ND = size_t(N) * p.Do;
+    const size_t PUW = size_t(p.P) * p.U * W;
+    if (N == 0) return dM ? cudaMemsetAsync(dM, 0, PUW * s, st) : cudaSuccess;
+    char* base = static_cast<char*>(ws);
+    void* prod_ws = base;                                // [gT | d_inT], then gT alone for dM
+    void* inT = base + r256(ND * W * s) + r256(ND * p.U * s);
+    void* Mt = static_cast<char*>(inT) + r256(ND * p.U * s);
+    void* part = static_cast<char*>(Mt) + r256(PUW * s);
+    const bool f64 = p.dtype == UVU_F64;
+    cudaError_t e = cudaSuccess;
+    if (d_in) {
+        const unsigned nb = unsigned((PUW + 255) / 256);
+        if (f64) transpose_M<double><<<nb, 256, 0, st>>>(p.P, p.U, W, static_cast<const double*>(M), static_cast<double*>(Mt));
+        else transpose_M<float><<<nb, 256, 0, st>>>(p.P, p.U, W, static_cast<const float*>(M), static_cast<float*>(Mt));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = f64 ? mix_product<double>(p, N, W, p.U, g, Mt, d_in, prod_ws, st)
+                : mix_product<float>(p, N, W, p.U, g, Mt, d_in, prod_ws, st);
+        if (e != cudaSuccess) return e;
+    }
+    if (dM) {
+        void* gT = prod_ws;
+        e = f64 ? relayout_launch<double>(N, p.U, p.Do, false, in, inT, st)
+                : relayout_launch<float>(N, p.U, p.Do, false, in, inT, st);
+        if (e != cudaSuccess) return e;
+        e = f64 ? relayout_launch<double>(N, W, p.Do, false, g, gT, st)
+                : relayout_launch<float>(N, W, p.Do, false, g, gT, st);
+        if (e != cudaSuccess) return e;
+        const SegTab tab = make_seg(p, N, nullptr);
+        const int64_t C = max_chunks(p, N);
+        const unsigned tiles = unsigned(((p.U + kDT - 1) / kDT) * ((W + kDT - 1) / kDT));
+        dim3 grid(tiles, unsigned(p.P), unsigned(C));
+        if (f64)
+            seg_dM<double><<<grid, 256, 0, st>>>(p.U, W, tab, static_cast<const double*>(inT),
+                                                  static_cast<const double*>(gT), static_cast<double*>(part));
+        else
+            seg_dM<float><<<grid, 256, 0, st>>>(p.U, W, tab, static_cast<const float*>(inT),
+                                                 static_cast<const float*>(gT), static_cast<double*>(part));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_column_sum(part, C, int64_t(PUW), dM, f64, st);
+    }
+    return e;
 }
 
 }  // namespace uvu

@@ -138,10 +138,9 @@ cudaError_t launch_graph_validate(int64_t N, int64_t E, const int32_t* off, cons
 cudaError_t launch_column_sum(const void* part, int64_t rows, int64_t cols, void* out, bool f64, cudaStream_t st);
 // mix.cu
 int mix_max_paths();
-int mix_max_d3();
-size_t mix_dM_chunks(int64_t N);
-cudaError_t launch_mix_fwd(const Plan& p, int64_t N, int W, const void* in, const void* M, void* out, cudaStream_t st);
-cudaError_t launch_mix_bwd_in(const Plan& p, int64_t N, int W, const void* g, const void* M, void* d_in, cudaStream_t st);
-cudaError_t launch_mix_bwd_M(const Plan& p, int64_t N, int W, const void* in, const void* g, void* part, void* dM,
-                             cudaStream_t st);
+size_t mix_workspace_bytes(const Plan& p, int64_t N, int W, bool bwd);
+cudaError_t launch_mix_fwd(const Plan& p, int64_t N, int W, const void* in, const void* M, void* out, void* ws,
+                           cudaStream_t st);
+cudaError_t launch_mix_bwd(const Plan& p, int64_t N, int W, const void* in, const void* M, const void* g, void* d_in,
+                           void* dM, void* ws, cudaStream_t st);
 }  // namespace uvu

@@ -34,7 +34,7 @@ EXPORTS = (
     "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
     "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
     "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
-    "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_bwd_workspace", "uvu_conv_uvw_fwd",
+    "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
     "uvu_status_string", "uvu_last_error_message",
 )
 
@@ -78,10 +78,10 @@ def _load():
                                ctypes.POINTER(ctypes.c_double)],
         "uvu_conv_fwd_sender": [P, I64, I64, P, P, P, P, P, P, P, P],
         "uvu_conv_fwd_mode": [P, I, I64, I64, P, P, P, P, P, P, P, P, P, P],
-        "uvu_mix_fwd": [P, I64, I, P, P, P, P],
+        "uvu_mix_fwd": [P, I64, I, P, P, P, P, SZ, P],
         "uvu_mix_bwd": [P, I64, I, P, P, P, P, P, P, SZ, P],
-        "uvu_mix_bwd_workspace": [P, I64, I, ctypes.POINTER(SZ)],
-        "uvu_conv_uvw_fwd": [P, I64, I64, P, P, P, P, P, P, I, P, P, P],
+        "uvu_mix_workspace": [P, I64, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
+        "uvu_conv_uvw_fwd": [P, I64, I64, P, P, P, P, P, P, I, P, P, P, SZ, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -120,7 +120,7 @@ for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source"
            "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
            "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
            "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
-           "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_bwd_workspace", "uvu_conv_uvw_fwd"):
+           "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd"):
     globals()[_n] = _wrap(_n)
 
 
@@ -254,31 +254,36 @@ class Plan:
                           _ptr(graph.recv_offsets), _ptr(graph.src), _ptr(graph.send_offsets),
                           _ptr(graph.send_eids), _ptr(graph.send_recv), _ptr(out), _stream(stream))
 
-    def mix_fwd(self, n_nodes, w_out, inp, M, out, stream=None):
-        """Per-path channel mixing of a UVU output (see uvu_mix_fwd)."""
-        uvu_mix_fwd(self.handle, n_nodes, w_out, _ptr(inp), _ptr(M), _ptr(out), _stream(stream))
+    def mix_workspace_bytes(self, n_nodes, w_out):
+        """(forward bytes, backward bytes) of device workspace for the channel mixing."""
+        f, b = ctypes.c_size_t(), ctypes.c_size_t()
+        uvu_mix_workspace(self.handle, n_nodes, w_out, ctypes.byref(f), ctypes.byref(b))
+        return f.value, b.value
 
-    def mix_workspace_bytes(self, n_nodes, w_out) -> int:
-        b = ctypes.c_size_t()
-        uvu_mix_bwd_workspace(self.handle, n_nodes, w_out, ctypes.byref(b))
-        return b.value
+    def _mix_ws(self, n_nodes, w_out, bwd, workspace, device):
+        need = self.mix_workspace_bytes(n_nodes, w_out)[1 if bwd else 0]
+        if workspace is None:
+            import torch
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+    def mix_fwd(self, n_nodes, w_out, inp, M, out, workspace=None, stream=None):
+        """Per-path channel mixing of a UVU output (see uvu_mix_fwd); `workspace` (uint8) is
+        allocated here with torch if None."""
+        ws, nb = self._mix_ws(n_nodes, w_out, False, workspace, out.device)
+        uvu_mix_fwd(self.handle, n_nodes, w_out, _ptr(inp), _ptr(M), _ptr(out), ws, nb, _stream(stream))
 
     def mix_bwd(self, n_nodes, w_out, inp, M, d_out, d_in=None, dM=None, workspace=None, stream=None):
-        """VJP of mix_fwd; dM needs `workspace` (uint8, mix_workspace_bytes()), allocated here if None."""
-        ws_ptr, ws_bytes = None, 0
-        if dM is not None:
-            need = self.mix_workspace_bytes(n_nodes, w_out)
-            if workspace is None:
-                import torch
-                workspace = torch.empty(need, dtype=torch.uint8, device=dM.device)
-            ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+        """VJP of mix_fwd (see uvu_mix_bwd)."""
+        ws, nb = self._mix_ws(n_nodes, w_out, True, workspace, d_out.device)
         uvu_mix_bwd(self.handle, n_nodes, w_out, _ptr(inp), _ptr(M), _ptr(d_out), _ptr(d_in), _ptr(dM),
-                    ws_ptr, ws_bytes, _stream(stream))
+                    ws, nb, _stream(stream))
 
-    def uvw_fwd(self, n_nodes, x, Y, w, recv_offsets, src, M, w_out, uvu_out, out, stream=None):
+    def uvw_fwd(self, n_nodes, x, Y, w, recv_offsets, src, M, w_out, uvu_out, out, workspace=None, stream=None):
         """Factorised UVW convolution (see uvu_conv_uvw_fwd)."""
+        ws, nb = self._mix_ws(n_nodes, w_out, False, workspace, out.device)
         uvu_conv_uvw_fwd(self.handle, n_nodes, src.numel(), _ptr(x), _ptr(Y), _ptr(w), _ptr(recv_offsets),
-                         _ptr(src), _ptr(M), w_out, _ptr(uvu_out), _ptr(out), _stream(stream))
+                         _ptr(src), _ptr(M), w_out, _ptr(uvu_out), _ptr(out), ws, nb, _stream(stream))
 
     def bwd_edge(self, n_nodes, x, Y, w, recv_offsets, src, d_out, dY=None, dw=None,
                  dx_atomic=None, dx_edge=None, stream=None):

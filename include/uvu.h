@@ -317,30 +317,34 @@ uvu_status uvu_conv_fwd_mode(uvu_plan_t plan, uvu_fwd_mode mode, int64_t n_nodes
  * ("Receiver-streaming convolutions ...", replies: UVW cases that can be reduced to UVU; which
  * cases is not stated there, this factorisation is the reading taken):
  *     out[r,w,ooff(p)+m3] = sum_u M[p,u,w] in[r,u,ooff(p)+m3]
- * in [N][U][D_out] (a UVU output), out [N][W][D_out], W = w_out in [1, 4096].  Caller-owned device
- * memory, 16-byte aligned; out is overwritten.  Launches: 1 kernel. */
+ * in [N][U][D_out] (a UVU output), out [N][W][D_out], W = w_out in [1, 4096].  The kernels copy
+ * the operand to a component-major layout in `workspace` (at least the forward size
+ * uvu_mix_workspace() reports), run one dense product per path, and copy the result back.
+ * Caller-owned device memory, 16-byte aligned; out is overwritten.  Launches: 3 kernels. */
 uvu_status uvu_mix_fwd(uvu_plan_t plan, int64_t n_nodes, int w_out, const void *in, const void *M,
-                       void *out, uvu_stream_t stream);
+                       void *out, void *workspace, size_t workspace_bytes, uvu_stream_t stream);
 
 /* VJP of uvu_mix_fwd for the cotangent d_out [N][W][D_out]: d_in [N][U][D_out] and
- * dM [P][U][W] = sum_r sum_m3 in[r,u,ooff+m3] d_out[r,w,ooff+m3]; either may be NULL.  dM is
- * summed over fixed receiver chunks into fp64 rows of `workspace` (uvu_mix_bwd_workspace()
- * bytes), which are added in chunk order: deterministic.  For N = 0, dM is set to zero.
- * Launches: 1 kernel for d_in; 2 for dM. */
+ * dM [P][U][W] = sum_r sum_m3 in[r,u,ooff+m3] d_out[r,w,ooff+m3]; either may be NULL.  dM is a
+ * product over fixed row chunks (fp32 within 16 rows, fp64 across) added in chunk
+ * order: deterministic.  `workspace` holds at least the backward size of uvu_mix_workspace().
+ * For N = 0, dM is set to zero.  Launches: 4 kernels for d_in, 4 for dM. */
 uvu_status uvu_mix_bwd(uvu_plan_t plan, int64_t n_nodes, int w_out, const void *in, const void *M,
                        const void *d_out, void *d_in, void *dM, void *workspace, size_t workspace_bytes,
                        uvu_stream_t stream);
 
-/* Bytes of device workspace uvu_mix_bwd needs for dM: min(max(N,1), 32) * P * U * W * 8. */
-uvu_status uvu_mix_bwd_workspace(uvu_plan_t plan, int64_t n_nodes, int w_out, size_t *bytes);
+/* Device workspace bytes of uvu_mix_fwd and uvu_mix_bwd (either pointer may be NULL). */
+uvu_status uvu_mix_workspace(uvu_plan_t plan, int64_t n_nodes, int w_out, size_t *fwd_bytes,
+                             size_t *bwd_bytes);
 
 /* The factorised UVW convolution: uvu_conv_fwd into uvu_out [N][U][D_out] (caller-owned), then
- * uvu_mix_fwd into out [N][W][D_out].  Its VJP composes uvu_mix_bwd (d_in is the convolution's
- * d_out) with uvu_conv_bwd.  Launches: 2 kernels. */
+ * uvu_mix_fwd into out [N][W][D_out] with `workspace` (the forward size of uvu_mix_workspace()).
+ * Its VJP composes uvu_mix_bwd (d_in is the convolution's d_out) with uvu_conv_bwd.
+ * Launches: 4 kernels. */
 uvu_status uvu_conv_uvw_fwd(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
                             const void *Y, const void *w, const int32_t *recv_offsets,
                             const int32_t *src, const void *M, int w_out, void *uvu_out, void *out,
-                            uvu_stream_t stream);
+                            void *workspace, size_t workspace_bytes, uvu_stream_t stream);
 
 /* ------------------------------------------------------- batched tensor product (no graph) ---- */
 

@@ -140,8 +140,12 @@ def test_mixing_host_checks():
     from clebsch_gordan_tensor_receiver_gb300 import uvu
     import pytest
     p = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3)
-    assert p.mix_workspace_bytes(5000, 64) == 32 * 13 * 128 * 64 * 8
-    assert p.mix_workspace_bytes(3, 64) == 3 * 13 * 128 * 64 * 8
+    r = lambda b: (b + 255) // 256 * 256
+    N, W, U, Do, P = 5000, 64, 128, 55, 13
+    fwd, bwd = p.mix_workspace_bytes(N, W)
+    assert fwd == r(N * Do * U * 4) + r(N * Do * W * 4)
+    chunks = (7 * N + 1023) // 1024  # widest path (l3 = 3) over 1024-row chunks
+    assert bwd == r(N * Do * W * 4) + 2 * r(N * Do * U * 4) + r(P * U * W * 4) + r(chunks * P * U * W * 8)
     for bad in (0, 5000):
         with pytest.raises(uvu.UVUError):
             p.mix_workspace_bytes(10, bad)
