@@ -656,6 +656,36 @@ def main(argv=None):
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                        "chunks": len(cuts) - 1, "dx_mode": mode_e2e, "bitwise_equal_to_resident": same,
                        "h2d_GB_s": h2d / (e_ms / 1000) / 1e9, "d2h_GB_s": d2h / (e_ms / 1000) / 1e9}
+
+        # this machine's host link, measured the same way (pinned buffers, one large copy each way,
+        # alone and concurrently): the ceiling the end-to-end step is bound by
+        def link(fn, reps=3):
+            fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                fn()
+            torch.cuda.synchronize()
+            return (time.perf_counter() - t0) / reps
+
+        wb = hin["w"].numel() * hin["w"].element_size()
+
+        def h2d_only():
+            with torch.cuda.stream(s_in):
+                dbuf["w"].copy_(hin["w"], non_blocking=True)
+
+        def d2h_only():
+            with torch.cuda.stream(s_out):
+                hout["dw"].copy_(dw, non_blocking=True)
+
+        def both():
+            h2d_only()
+            d2h_only()
+
+        t_h, t_d, t_b = link(h2d_only), link(d2h_only), link(both)
+        line["e2e"]["link"] = {"h2d_GB_s": wb / t_h / 1e9, "d2h_GB_s": wb / t_d / 1e9,
+                               "concurrent_each_way_GB_s": wb / t_b / 1e9, "bytes_per_copy": wb}
+        line["e2e"]["frac_of_concurrent_link"] = ((h2d + d2h) / 2 / (e_ms / 1000)) / (wb / t_b)
         assert plan.device_status() == 0
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
