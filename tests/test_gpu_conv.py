@@ -162,3 +162,23 @@ def test_receiver_subranges_match_whole_graph():
     for got, want in ((out, out_ref), (dxe, dxe_ref), (dY, dY_ref), (dw, dw_ref)):
         assert torch.equal(got, want)
     assert P.status_ok()
+
+
+def test_one_plan_over_changing_graphs():
+    """One plan serves graphs of any size in sequence (the plan depends on the irreps only):
+    growing, shrinking and empty graphs, each checked against the oracle."""
+    spec0 = workloads.custom_spec(170, 10, "32x0e+32x1o", SH3, 3)
+    plan = None
+    rng = np.random.default_rng(17)
+    for N, dmax in ((10, 4), (57, 20), (3, 0), (31, 9), (1, 2)):
+        spec = workloads.custom_spec(170, N, "32x0e+32x1o", SH3, 3)
+        deg = rng.integers(0, dmax + 1, size=N)
+        recv, src = workloads.random_degree_graph(N, deg, rng)
+        Y = workloads.sh_inputs(workloads.unit_vectors(src.size, rng), 3).astype(np.float32)
+        x = rng.standard_normal((N, 32, 4)).astype(np.float32)
+        P = Problem(spec, recv, src, x, Y, N)
+        if plan is None:
+            plan = P.plan
+        P.plan = plan  # the same plan object for every graph
+        _full_compare(P)
+    assert spec0.n_nodes == 10

@@ -123,3 +123,12 @@ def test_disk_cache_and_source_dump(tmp_path):
     assert {f.name: f.stat().st_mtime_ns for f in cache.iterdir()} == stamp  # served from the cache
     dumped = list(dump.glob("uvu_*.cu"))
     assert dumped and "uvu_fwd" in dumped[0].read_text()
+
+
+def test_unwritable_cache_dir_is_harmless(tmp_path):
+    """A cache directory that cannot be written (here: a path under a regular file) does not fail
+    plan creation; the plan compiles and runs from memory."""
+    blocker = tmp_path / "file"
+    blocker.write_text("x")
+    r = _run_child(_CHILD, {"UVU_CACHE_DIR": str(blocker / "sub")})
+    assert r.returncode == 0 and r.stdout.startswith("OK"), r.stdout + r.stderr
