@@ -81,6 +81,13 @@ void cache_write(const std::string& path, const std::string& src, const CacheEnt
 
 uvu_status nvrtc_compile_uncached(const std::string& src, CacheEntry* out, std::string* err);
 
+// --no-cache: NVRTC's cross-process compile cache returns the cubin without running ptxas on a
+// hit, so the log would lack the register/spill report the planner's register-budget choice
+// reads (a later process then kept a spilling four-block budget: edge kernel 1.35 ms instead of
+// 0.87 ms on MACE-medium).  Modules are cached by this library instead (UVU_CACHE_DIR), log included.
+const char* const kNvrtcOpts[] = {"--gpu-architecture=sm_103a", "--std=c++17", "-lineinfo",
+                                  "--ptxas-options=-v", "--fmad=true", "--no-cache"};
+
 // UVU_FAIL_COMPILE=1 makes every compilation fail (host-side fault injection for the error
 // path); UVU_DUMP_SOURCE=<dir> writes each emitted source there for review.
 uvu_status nvrtc_compile(const std::string& src, CacheEntry* out, std::string* err) {
@@ -90,7 +97,9 @@ uvu_status nvrtc_compile(const std::string& src, CacheEntry* out, std::string* e
     }
     int ver_major = 0, ver_minor = 0;
     nvrtcVersion(&ver_major, &ver_minor);
-    const std::string key = text_hash(src + "|nvrtc " + std::to_string(ver_major) + "." + std::to_string(ver_minor));
+    std::string salt = "|nvrtc " + std::to_string(ver_major) + "." + std::to_string(ver_minor);
+    for (const char* o : kNvrtcOpts) salt += std::string("|") + o;
+    const std::string key = text_hash(src + salt);
     if (const char* d = env_dir("UVU_DUMP_SOURCE")) {
         std::ofstream f(std::string(d) + "/uvu_" + key + ".cu");
         f << src;
@@ -110,14 +119,7 @@ uvu_status nvrtc_compile_uncached(const std::string& src, CacheEntry* out, std::
         *err = std::string("nvrtcCreateProgram: ") + nvrtcGetErrorString(r);
         return UVU_ERR_COMPILE;
     }
-    // --no-cache: NVRTC's cross-process compile cache returns the cubin without running ptxas
-    // on a hit, so the log would lack the register/spill report the planner's register-budget
-    // choice reads (a later process then kept a spilling four-block budget: edge kernel 1.35 ms
-    // instead of 0.87 ms on MACE-medium).  Plans compile once per process and in-process copies
-    // share the result through the cache below.
-    const char* opts[] = {"--gpu-architecture=sm_103a", "--std=c++17", "-lineinfo",
-                          "--ptxas-options=-v", "--fmad=true", "--no-cache"};
-    r = nvrtcCompileProgram(prog, int(sizeof(opts) / sizeof(opts[0])), opts);
+    r = nvrtcCompileProgram(prog, int(sizeof(kNvrtcOpts) / sizeof(kNvrtcOpts[0])), kNvrtcOpts);
     size_t log_size = 0;
     nvrtcGetProgramLogSize(prog, &log_size);
     std::string log(log_size, '\0');
