@@ -867,6 +867,14 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         size_t w_off = 0, x_off = 0, y_off = 0, stage = 0, bar_off = 0, part_off = 0, xpart_off = 0, out_off = 0, total = 0;
         size_t g_off = 0, gbytes = 0;
         size_t dacc_off = 0;  // fp64 dw accumulators [P][U_pad] of the batch-shared-weight edge kernel
+        // edge kernel, one register group, UVU_PIPE_LASTWARP=1 (a tuning switch): the per-stage dY
+        // partials are summed by the last warp to finish the stage (an arrival counter per buffer,
+        // three buffers) instead of after a barrier of all consumer warps.  Off by default: it
+        // measured slower (MACE-medium edge kernel 0.897 vs 0.862 ms); the barrier keeps the warps
+        // in step over the shared stages.
+        bool lastwarp = false;
+        int nbuf = 2;
+        size_t cnt_off = 0;
         size_t tx_per_edge = 0;
     };
     static size_t a16(size_t v) { return (v + 15) / 16 * 16; }
@@ -889,7 +897,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         const size_t stage = std::max<size_t>(16, (a16(R.ch * wb) + (R.xbulk ? a16(R.ch * xbytes()) : 0) +
                                                    (R.ybulk ? a16(R.ch * ybytes()) : 0)) * (dual ? 2 : 1));
         // per-stage partial sums of the edge kernel: dY over warps, dx over register groups
-        const size_t dyp = with_partials ? a16(2 * size_t(ncw) * R.ch * P->Dy * P->elem()) : 0;
+        R.lastwarp = with_partials && NG == 1 && std::getenv("UVU_PIPE_LASTWARP") &&
+                     std::atoi(std::getenv("UVU_PIPE_LASTWARP")) != 0;
+        R.nbuf = R.lastwarp ? 3 : 2;
+        const size_t dyp = with_partials ? a16(size_t(R.nbuf) * ncw * R.ch * P->Dy * P->elem()) + (R.lastwarp ? 16 : 0) : 0;
         const size_t dxp = (with_partials && NG > 1) ? a16(2 * size_t(NG) * R.ch * P->U_pad * P->Dx * P->elem()) : 0;
         // Two stages: with several blocks resident per SM, one stage of look-ahead per block keeps
         // enough bytes in flight, and the smaller footprint lets more blocks (warps) reside.
@@ -910,6 +921,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         R.gst = stage_g && R.gbytes % 16 == 0;
         R.part_off = R.bar_off + 16 * R.nst + (R.gst ? 16 : 0);
         R.xpart_off = R.part_off + dyp;
+        R.cnt_off = R.part_off + dyp - (R.lastwarp ? 16 : 0);
         R.out_off = R.xpart_off + dxp;
         // The receiver's output block out[r] (U x D_out, contiguous in global memory) is staged in
         // shared memory so that it leaves the block as coalesced row writes instead of one
@@ -951,6 +963,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S(fmt("#define %s_GBAR %zu", pre, R.bar_off + 16 * R.nst));
         S(fmt("#define %s_GBYTES %zu", pre, R.gbytes));
         S(fmt("#define %s_DACC %zu", pre, R.dacc_off));
+        if (R.lastwarp) {
+            S(fmt("#define %s_CNT %zu", pre, R.cnt_off));
+            S(fmt("#define %s_NBUF %d", pre, R.nbuf));
+        }
         S(fmt("#define %s_AWOFF %zu", pre, R.aw_off));
         S(fmt("#define %s_AXOFF %zu", pre, R.ax_off));
         S(fmt("#define %s_AYOFF %zu", pre, R.ay_off));
@@ -1408,6 +1424,39 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             emit_release(S, "EG");
             S.ind--;
             S("}");  // !dead
+            if (R.lastwarp) {
+                // the last warp to finish the stage sums the warps' dY partials; the others go on
+                S("if (!dead && dY) {");
+                S.ind++;
+                S("unsigned* const cnt = reinterpret_cast<unsigned*>(const_cast<unsigned char*>(smem) + EG_CNT);");
+                S("__syncwarp();");
+                S("unsigned last = 0;");
+                S("if (lane == 0) { __threadfence_block(); last = atomicAdd(cnt + buf, 1u) == UVU_NCW - 1; }");
+                S("last = __shfl_sync(0xffffffffu, last, 0);");
+                S("if (last) {");
+                S.ind++;
+                S("__threadfence_block();");
+                S("for (int t = lane; t < ne * UVU_DY; t += 32) {");
+                S.ind++;
+                S("const int j = t / UVU_DY, k = t - j * UVU_DY;");
+                S(T + " acc = 0;");
+                S("#pragma unroll");
+                S("for (int wp = 0; wp < UVU_NCW; ++wp) acc += partbase[((size_t)(buf * UVU_NCW + wp) * EG_CH + j) * UVU_DY + k];");
+                S("dY[(size_t)(eb + j) * UVU_DY + k] = acc;");
+                S.ind--;
+                S("}");
+                S("__syncwarp();");
+                S("if (lane == 0) cnt[buf] = 0u;");
+                S.ind--;
+                S("}");
+                S.ind--;
+                S("}");
+                S("buf = buf == EG_NBUF - 1 ? 0 : buf + 1;");
+                S.ind--;
+                S("}");
+                S.ind--;
+                S("}");
+            } else {
             S("consumer_sync();");
             if (NG > 1) {
                 S("if (!dead && dxe) {");
@@ -1447,6 +1496,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("}");
             S.ind--;
             S("}");
+            }
         }
         S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, EG_MINB) %s(long long N, const int* __restrict__ off,",
               R.dual ? "uvu_hvp_edge" : R.tp ? (R.wsh ? "uvu_tp_edge_sh" : "uvu_tp_edge") : "uvu_bwd_edge"));
@@ -1466,6 +1516,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("if (tid == 0) {");
         S("  for (int i = 0; i < EG_NST; ++i) { mbar_init(sbase + EG_BAR + 8u * i, 1u); mbar_init(sbase + EG_BAR + 8u * (EG_NST + i), " + std::string(empty_count("UVU_NCW", "UVU_NCT")) + "); }");
         if (R.gst) S("  mbar_init(sbase + EG_GBAR, 1u); mbar_init(sbase + EG_GBAR + 8u, " + std::string(empty_count("UVU_NCW", "UVU_NCT")) + ");");
+        if (R.lastwarp) S("  for (int i = 0; i < EG_NBUF; ++i) reinterpret_cast<unsigned*>(smem + EG_CNT)[i] = 0u;");
         S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
         S("}");
         S("__syncthreads();");

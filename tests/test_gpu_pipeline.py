@@ -13,7 +13,7 @@ from gpu_util import Problem
 
 pytestmark = pytest.mark.gpu
 
-KNOBS = ("UVU_FORCE_DIRECT", "UVU_PIPE_CH", "UVU_PIPE_NST")
+KNOBS = ("UVU_FORCE_DIRECT", "UVU_PIPE_CH", "UVU_PIPE_NST", "UVU_PIPE_LASTWARP")
 
 
 def _run(P, env):
@@ -45,3 +45,18 @@ def test_pipelined_matches_direct_full_size(key):
             tol = 1e-5 * (1 + b.abs())
             bad = ((a - b).abs() > tol)
             assert not bad.any(), f"{env} {n}: {int(bad.sum())} elements differ, max {float((a - b).abs().max()):.3e}"
+
+
+def test_last_warp_dy_sum_is_bitwise_identical():
+    """The opt-in last-warp dY sum (UVU_PIPE_LASTWARP=1) adds the warps' partials in the same
+    fixed order as the default barrier version, so every output is bitwise identical."""
+    P = Problem.from_spec(1)
+    ref = _run(P, {})
+    got = _run(P, {"UVU_PIPE_LASTWARP": "1"})
+    # outputs: out, sender-mode dx, dY, dw, atomic-mode dx, staged-mode dx; the atomic dx sums in
+    # a run-dependent order, so it is compared within rounding instead
+    for i, (a, b) in enumerate(zip(ref, got)):
+        if i == 4:
+            assert torch.allclose(a, b, rtol=1e-5, atol=1e-5)
+        else:
+            assert torch.equal(a, b), i
