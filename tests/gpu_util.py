@@ -37,6 +37,9 @@ class Problem:
         self.N = n_nodes
         self.E = int(src.size)
         self.recv, self.src, self.x, self.Y = recv, src, x, Y
+        i = self.plan.info
+        assert Y.shape == (self.E, i.dim_sh) and x.shape == (n_nodes, i.mul, i.dim_x), \
+            ("inputs do not match the plan's layout", Y.shape, x.shape)
         self.w = workloads.make_weights(spec, self.E, self.plan.info.n_paths)
         self.g = workloads.make_cotangent(spec, n_nodes, self.plan.info.dim_out)
         self.off_host = graph.recv_offsets(recv, n_nodes)

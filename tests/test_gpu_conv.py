@@ -45,6 +45,7 @@ CUSTOM = [
     ("128x0e+128x1o", SH3, 3, "float32", 300, 70),        # medium shapes, ragged, many chunks
     ("33x0e+33x1o+33x2e", SH3, 3, "float32", 29, 9),      # pipelined, x rows not 16-byte multiples (no bulk x)
     ("40x1o", "1x0e+1x1o+1x2e", 2, "float64", 17, 7),     # pipelined, Y rows not bulk, even D_out (padded stride)
+    ("32x1o+32x4e", "1x0e+1x1o+1x2e+1x3o+1x4e", 4, "float32", 13, 6),  # l = 4 everywhere: 27 paths, D_out 159
 ]
 
 
@@ -58,7 +59,8 @@ def test_custom_workloads_all_outputs(case):
     recv, src = workloads.random_degree_graph(N, deg, rng)
     vec = workloads.unit_vectors(src.size, rng)
     lsh = int(irs.split("+")[-1].split("x")[1][:-1])
-    Y = workloads.sh_inputs(vec, lsh).astype(dt)
+    # Y is an input of the convolution: SH values up to l = 3, plain normal values beyond
+    Y = (workloads.sh_inputs(vec, lsh) if lsh <= 3 else rng.standard_normal((src.size, workloads.dim_of(irs)))).astype(dt)
     mul = int(irx.split("x")[0])
     x = rng.standard_normal((N, mul, workloads.dim_of(irx))).astype(dt)
     _full_compare(Problem(spec, recv, src, x, Y, N))

@@ -61,6 +61,7 @@ CUSTOM = [
     ("8x1o+8x2e", "1x0e+1x1o+1x2e", 4, "float32", 13, 5),
     ("33x0e+33x1o+33x2e", SH3, 3, "float32", 15, 6),      # pipelined, x and ax rows read directly
     ("40x1o", "1x0e+1x1o+1x2e", 2, "float64", 11, 5),     # pipelined, Y and aY rows read directly
+    ("32x2e+32x4e", "1x0e+1x2e+1x4e", 4, "float32", 9, 4),  # l = 4 paths
 ]
 
 
@@ -73,7 +74,9 @@ def test_custom_workloads(case):
     deg[0] = 0
     recv, src = workloads.random_degree_graph(N, deg, rng)
     lsh = int(irs.split("+")[-1].split("x")[1][:-1])
-    Y = workloads.sh_inputs(workloads.unit_vectors(src.size, rng), lsh).astype(dt)
+    # Y is an input of the convolution: SH values up to l = 3, plain normal values beyond
+    Y = (workloads.sh_inputs(workloads.unit_vectors(src.size, rng), lsh) if lsh <= 3
+         else rng.standard_normal((src.size, workloads.dim_of(irs)))).astype(dt)
     x = rng.standard_normal((N, int(irx.split("x")[0]), workloads.dim_of(irx))).astype(dt)
     _full_compare(Problem(spec, recv, src, x, Y, N), 7)
 
