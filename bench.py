@@ -93,7 +93,11 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu = gpu_index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        # raw nvidia-smi samples (the JSON line carries their summary); UVU_BENCH_CLOCKS_DIR
+        # chooses where they are kept
+        import tempfile
+        d = os.environ.get("UVU_BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"uvu_bench_clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
