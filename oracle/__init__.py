@@ -28,6 +28,8 @@ wigner   real Wigner-D matrices fitted from SH samples (used only by equivarianc
 hvp      double backward (Hessian-vector product) through substituted forward / VJP calls.
 tp       batched (non-convolution) tensor product and its VJP, per-sample or shared weights.
 mix      per-path channel mixing that reduces a factorised UVW convolution to the UVU one.
+radial   radial weights from edge lengths (Bessel basis, polynomial envelope, SiLU network) and
+         the convolution that uses them.
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against properties
 that the mathematics fixes (orthogonality, completeness, closed forms for l <= 1, intertwining
@@ -36,4 +38,4 @@ a dense brute force).  The pages print no worked numerical example of this opera
 golden value comes from them; ``tests/golden/`` holds closed-form values derived by hand.
 """
 
-from . import cg, sh, paths, graph, conv, wigner, hvp, tp, mix  # noqa: F401
+from . import cg, sh, paths, graph, conv, wigner, hvp, tp, mix, radial  # noqa: F401
