@@ -52,6 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-hvp", action="store_true", help="skip the double-backward measurement")
     ap.add_argument("--no-tp", action="store_true", help="skip the batched tensor-product measurement")
+    ap.add_argument("--no-radial", action="store_true", help="skip the fused-radial-weight measurement")
     ap.add_argument("--tp-batch", type=int, default=100000, help="samples of the batched tensor product")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
     ap.add_argument("--single-mode", action="store_true",
@@ -483,6 +484,58 @@ def main(argv=None):
                        "note": "bound alu: fp32 FMA peak = 128 lanes x 2 flop x SMs x max SM clock"}
         assert plan.device_status() == 0
         del Mm, mo, mg, md_in, mdM, mws
+
+    # convolution with fused radial weights: the radial network (edge lengths -> hidden features
+    # h, enveloped Bessel basis of 8 functions, three SiLU layers of 64) and the forward that forms
+    # w = h W_last per (edge, channel) in registers.  Beside them the materialised alternative on
+    # the same h: the last layer as one cuBLAS GEMM writing w [E][P][U] (FP32, and TF32 tensor
+    # cores), then uvu_fwd reading it.  Inputs drawn on the device (seeded).
+    if not args.no_radial and world == 1 and not args.single_mode:
+        Hr, widths = 64, [8, 64, 64, 64]
+        rgen = torch.Generator(device=dev).manual_seed(515)
+        a3 = (0.75 / 5.0) ** 3
+        rr = 5.0 * (a3 + (1 - a3) * torch.rand(E, generator=rgen, device=dev, dtype=torch.float64)) ** (1.0 / 3.0)
+        rr = rr.to(tdt)
+        Wn = torch.cat([(torch.randn((widths[i], widths[i + 1]), generator=rgen, device=dev, dtype=tdt)
+                         / widths[i] ** 0.5).reshape(-1) for i in range(3)])
+        Wlast = torch.randn((Hr, P, U), generator=rgen, device=dev, dtype=tdt) / Hr ** 0.5 / spec.w_scale_degree ** 0.5
+        hbuf = torch.empty((E, Hr), device=dev, dtype=tdt)
+        rout = torch.empty_like(out)
+        reps = max(5, args.steps // 2)
+        hid_ms = ev_mix(lambda: plan.radial_hidden(rr, 5.0, 5, widths, Wn, hbuf, stream=stream), reps)
+        fus_ms = ev_mix(lambda: plan.fwd_radial(N, x, Y, hbuf, Wlast, G.recv_offsets, src, rout, stream=stream), reps)
+        wmat = torch.empty((E, P * U), device=dev, dtype=tdt)
+        tf32_prev = torch.backends.cuda.matmul.allow_tf32
+        gemm = {}
+        for name, tf in (("fp32", False), ("tf32", True)):
+            torch.backends.cuda.matmul.allow_tf32 = tf
+            gemm[name] = ev_mix(lambda: torch.matmul(hbuf, Wlast.view(Hr, P * U), out=wmat), reps)
+        torch.backends.cuda.matmul.allow_tf32 = False
+        torch.matmul(hbuf, Wlast.view(Hr, P * U), out=wmat)
+        torch.backends.cuda.matmul.allow_tf32 = tf32_prev
+        conv_ms = ev_mix(lambda: plan.fwd(N, x, Y, wmat.view(E, P, U), G.recv_offsets, src, out, stream), reps)
+        torch.cuda.synchronize()
+        rel = float(torch.linalg.vector_norm((rout - out).double()) / torch.linalg.vector_norm(out.double()))
+        flops_last = 2.0 * E * U * P * Hr
+        hid_flops = 2.0 * E * sum(widths[i] * widths[i + 1] for i in range(3))
+        fused_bytes = E * U * Dx * s + E * Dy * s + E * Hr * s + N * U * Do * s + 4 * (N + 1) + 4 * E
+        line["radial"] = {
+            "hidden": widths, "r_cut": 5.0, "p_env": 5,
+            "hidden_ms": hid_ms, "hidden_tflops": hid_flops / (hid_ms / 1000) / 1e12,
+            "fused_fwd_ms": fus_ms, "fused_edges_per_s": E / (fus_ms / 1000),
+            "fused_last_layer_tflops": flops_last / (fus_ms / 1000) / 1e12,
+            "fused_last_layer_alu_frac": flops_last / (fus_ms / 1000) / 1e12 / alu_peak,
+            "fused_bytes": fused_bytes, "fused_GB_s": fused_bytes / (fus_ms / 1000) / 1e9,
+            "materialised": {"gemm_fp32_ms": gemm["fp32"], "gemm_tf32_ms": gemm["tf32"], "uvu_fwd_ms": conv_ms,
+                             "w_bytes": E * P * U * s,
+                             "total_fp32_ms": hid_ms + gemm["fp32"] + conv_ms,
+                             "total_tf32_ms": hid_ms + gemm["tf32"] + conv_ms},
+            "fused_total_ms": hid_ms + fus_ms,
+            "rel_frobenius_vs_materialised_fp32": rel,
+            "note": "alu bound: last-layer FMAs (2 E U P H flop) over the fp32 peak from unit counts; "
+                    "the materialised GEMMs are cuBLAS (library), shown for comparison only"}
+        assert plan.device_status() == 0
+        del rr, Wn, Wlast, hbuf, rout, wmat
 
     # batched (non-convolution) tensor product on the same irreps: B samples, per-sample and
     # batch-shared weights, forward and VJP (dx, dy, dw); inputs drawn on the device (seeded)

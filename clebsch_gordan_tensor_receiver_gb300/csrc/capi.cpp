@@ -3,7 +3,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <exception>
 #include <limits>
@@ -740,5 +742,112 @@ extern "C" uvu_status uvu_tp_bwd(uvu_plan_t plan, int64_t batch, const void* x, 
         cudaError_t e = launch_column_sum(workspace, rows, int64_t(p->P) * p->U, dw, p->dtype == UVU_F64, stream);
         if (e != cudaSuccess) return cuda_fail(e, "dw column sum launch");
     }
+    return ok();
+}
+
+// ------------------------------------------------------------------ fused radial weights
+namespace uvu {
+namespace {
+// Fixes (or checks) the plan's hidden width for the fused radial forward.
+uvu_status radial_prepare(Plan* p, int hidden) {
+    if (hidden < 4 || hidden > 256 || hidden % 4)
+        return fail(UVU_ERR_INVALID_ARGUMENT, "hidden must be a multiple of 4 in [4, 256]");
+    std::lock_guard<std::mutex> g(p->mu);
+    AuxBuild& A = p->aux[AUX_RADIAL];
+    if (A.radial_h == 0) {
+        A.radial_h = hidden;
+        // UVU_RAD_NE (a tuning switch): edges whose weights a thread forms together
+        if (const char* e = std::getenv("UVU_RAD_NE")) A.radial_ne = std::max(1, std::min(8, std::atoi(e)));
+    } else if (A.radial_h != hidden) {
+        return fail(UVU_ERR_UNSUPPORTED, "this plan's fused radial forward was built for hidden width " +
+                                             std::to_string(A.radial_h));
+    }
+    return UVU_OK;
+}
+}  // namespace
+}  // namespace uvu
+
+extern "C" uvu_status uvu_radial_hidden(uvu_plan_t plan, int64_t n_edges, const void* r, double r_cut, int p_env,
+                                        int n_layers, const int* widths, const void* weights, void* h,
+                                        uvu_stream_t stream) {
+    UVU_RANGE("uvu_radial_hidden");
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(0, n_edges));
+    if (!(r_cut > 0) || !std::isfinite(r_cut)) return fail(UVU_ERR_INVALID_ARGUMENT, "r_cut must be positive and finite");
+    if (p_env < 1 || p_env > 16) return fail(UVU_ERR_INVALID_ARGUMENT, "p_env must be in [1, 16]");
+    if (n_layers < 1 || n_layers > kRadialMaxLayers) return fail(UVU_ERR_INVALID_ARGUMENT, "n_layers must be in [1, 4]");
+    if (!widths) return fail(UVU_ERR_INVALID_ARGUMENT, "widths is NULL");
+    RadialNet net;
+    net.n_layers = n_layers;
+    if (widths[0] < 1 || widths[0] > 64) return fail(UVU_ERR_INVALID_ARGUMENT, "widths[0] (n_basis) must be in [1, 64]");
+    for (int i = 0; i <= n_layers; ++i) {
+        if (i > 0 && (widths[i] < 4 || widths[i] > 128 || widths[i] % 4))
+            return fail(UVU_ERR_INVALID_ARGUMENT, "hidden widths must be multiples of 4 in [4, 128]");
+        net.widths[i] = widths[i];
+        net.max_width = std::max(net.max_width, widths[i]);
+    }
+    if (n_edges == 0) return ok();
+    UVU_TRY(need(r, "r"));
+    UVU_TRY(need(weights, "weights"));
+    UVU_TRY(need(h, "h"));
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "device query");
+    e = launch_radial_hidden(n_edges, r, r_cut, p_env, net, weights, h, p->dtype == UVU_F64, sms,
+                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "radial network launch");
+    return ok();
+}
+
+extern "C" uvu_status uvu_radial_module_source(uvu_plan_t plan, int hidden, const char** source, const char** log) {
+    UVU_RANGE("uvu_radial_module_source");
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(radial_prepare(p, hidden));
+    std::string err;
+    uvu_status s = compile_aux(p, AUX_RADIAL, &err);
+    if (s != UVU_OK) return fail(s, err);
+    if (source) *source = p->aux[AUX_RADIAL].source.c_str();
+    if (log) *log = p->aux[AUX_RADIAL].log.c_str();
+    return ok();
+}
+
+extern "C" uvu_status uvu_conv_fwd_radial(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void* x,
+                                          const void* Y, const void* h, int hidden, const void* w_last,
+                                          const int32_t* recv_offsets, const int32_t* src, void* out,
+                                          uvu_stream_t stream) {
+    UVU_RANGE("uvu_conv_fwd_radial");
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(n_nodes, n_edges));
+    UVU_TRY(radial_prepare(p, hidden));
+    if (n_nodes == 0) return ok();
+    UVU_TRY(need(out, "out"));
+    UVU_TRY(need_idx(recv_offsets, "recv_offsets"));
+    UVU_TRY(need(w_last, "w_last"));
+    if (n_edges > 0) {
+        UVU_TRY(need(x, "x"));
+        UVU_TRY(need(Y, "Y"));
+        UVU_TRY(need(h, "h"));
+        UVU_TRY(need_idx(src, "src"));
+    }
+    DeviceModule* m = nullptr;
+    std::string err;
+    uvu_status s = aux_module_for_current_device(p, AUX_RADIAL, &m, &err);
+    if (s != UVU_OK) return fail(s, err);
+    const AuxLoaded& L = m->aux[AUX_RADIAL];
+    const AuxBuild& A = p->aux[AUX_RADIAL];
+    // grid: whole channel slices, each with the resident blocks' share (at most one block per
+    // A.radial_rpb receivers)
+    const int64_t nsl = A.radial_nsl;
+    const int64_t want = (n_nodes + A.radial_rpb - 1) / A.radial_rpb;
+    const int64_t per_slice = std::max<int64_t>(1, std::min<int64_t>(want, int64_t(L.occ[0]) * m->sm_count / nsl));
+    long long N = n_nodes;
+    void* args[] = {&N, &recv_offsets, &src, &x, &Y, &h, &w_last, &out};
+    cudaError_t e = cudaLaunchKernel(reinterpret_cast<const void*>(L.k[0]), dim3(unsigned(nsl * per_slice)),
+                                     dim3(unsigned(A.g[0].threads)), args, A.g[0].smem, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "uvu_fwd_radial launch");
     return ok();
 }

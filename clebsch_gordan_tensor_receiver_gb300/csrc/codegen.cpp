@@ -20,6 +20,7 @@
 // where h is accumulated over all paths sharing (l1, l2) before it is contracted.
 // Paths whose CG is a signed permutation with a scalar operand (l1 = 0 or l2 = 0) skip the
 // products: acc[m3] += (w_p x0) (+-y[m2]).
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdlib>
@@ -1856,6 +1857,116 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S.ind--;
         S("}");
     }
+
+    // ------------------------------------------------------------------ fused radial forward
+    // Forward with the radial weights formed in registers: w[e,p,u] = sum_k h[e,k] W_last[k,p,u]
+    // for the NE edges a thread takes together, then the receiver-stationary contraction of each
+    // edge ("Receiver-streaming convolutions for channel-wise UVU tensor products", replies: the
+    // radial network fused into the convolution instead of its weights read from memory).
+    // One warp = one receiver x 32 channels x one register group; a block's warps share a slice of
+    // 32 channels, whose last-layer weights [H][P][32] sit in shared memory when they fit (else
+    // they are read through the read-only cache).  Forming NE edges' weights together reuses each
+    // last-layer weight NE times from a register.
+    void emit_radial_group(Src& S, int g, const std::vector<int>& paths, int NE) const {
+        const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
+        std::vector<int> outs;
+        for (int pi : paths)
+            for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
+        const bool f = !f64;
+        S(fmt("__device__ __forceinline__ void rad_group%d(int e0, int e1, const int* __restrict__ src, const %s* __restrict__ x,", g, T.c_str()));
+        S(fmt("    const %s* __restrict__ Y, const %s* __restrict__ h, const %s* __restrict__ wlb, int u, %s* __restrict__ orow) {",
+              T.c_str(), T.c_str(), T.c_str(), T.c_str()));
+        S.ind++;
+        for (int k : outs) S(fmt("%s acc_%d = 0;", T.c_str(), k));
+        S("#pragma unroll 1");
+        S("for (int eb = e0; eb < e1; eb += RD_NE) {");
+        S.ind++;
+        S("const int ne = min(RD_NE, e1 - eb);");
+        for (int j = 0; j < NE; ++j) {
+            S(fmt("const %s* __restrict__ hr%d = h + (size_t)(eb + min(%d, ne - 1)) * RD_H;", T.c_str(), j, j));
+            for (int pi : paths) S(fmt("%s w%d_%d = 0;", T.c_str(), j, pi));
+        }
+        S("#pragma unroll 2");
+        S("for (int k = 0; k < RD_H; k += 4) {");
+        S.ind++;
+        static const char* comp[4] = {"x", "y", "z", "w"};
+        for (int j = 0; j < NE; ++j) {
+            if (f) {
+                S(fmt("const float4 hq%d = __ldg(reinterpret_cast<const float4*>(hr%d + k));", j, j));
+            } else {
+                S(fmt("const double2 hqa%d = __ldg(reinterpret_cast<const double2*>(hr%d + k));", j, j));
+                S(fmt("const double2 hqb%d = __ldg(reinterpret_cast<const double2*>(hr%d + k) + 1);", j, j));
+            }
+        }
+        S(fmt("const %s* __restrict__ wk = wlb + (size_t)k * (UVU_P * RD_WSTR);", T.c_str()));
+        for (int kk = 0; kk < 4; ++kk) {
+            for (int pi : paths) {
+                S(fmt("{ const %s wl = wk[%d * RD_WSTR];", T.c_str(), kk * P->P + pi));
+                for (int j = 0; j < NE; ++j) {
+                    const std::string hv = f ? fmt("hq%d.%s", j, comp[kk]) : fmt("hq%c%d.%s", kk < 2 ? 'a' : 'b', j, comp[kk % 2]);
+                    S(fmt("  w%d_%d = fma(%s, wl, w%d_%d);", j, pi, hv.c_str(), j, pi));
+                }
+                S("}");
+            }
+        }
+        S.ind--;
+        S("}");
+        for (int j = 0; j < NE; ++j) {
+            S(fmt("if (%d < ne) {", j));
+            S.ind++;
+            S(fmt("const int e = eb + %d;", j));
+            S("const int s = __ldg(src + e);");
+            emit_row_loads(S, "xv", "x + ((size_t)s * UVU_U + u) * UVU_DX", P->Dx, xn);
+            emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
+            for (int pi : paths) S(fmt("const %s wv_%d = w%d_%d;", T.c_str(), pi, j, pi));
+            emit_fwd_edge(S, paths);
+            S.ind--;
+            S("}");
+        }
+        S.ind--;
+        S("}");
+        for (int k : outs) S(fmt("orow[%d] = acc_%d;", k, k));
+        S.ind--;
+        S("}");
+    }
+
+    void emit_fwd_radial(Src& S, const std::vector<std::vector<int>>& rg, int NE) const {
+        const int NG = int(rg.size());
+        for (int g = 0; g < NG; ++g) emit_radial_group(S, g, rg[g], NE);
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(RD_TPB, RD_MINB) uvu_fwd_radial(long long N, const int* __restrict__ off,"));
+        S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ h,",
+              T.c_str(), T.c_str(), T.c_str()));
+        S(fmt("    const %s* __restrict__ wlast, %s* __restrict__ out) {", T.c_str(), T.c_str()));
+        S.ind++;
+        S("const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;");
+        S("const int sl = blockIdx.x % RD_NSL;");
+        S("const long long rb = blockIdx.x / RD_NSL, nbs = gridDim.x / RD_NSL;");
+        S("const int u = sl * 32 + lane;");
+        S("#if RD_WSM");
+        S("extern __shared__ __align__(16) unsigned char smem[];");
+        S(fmt("%s* const wls = reinterpret_cast<%s*>(smem);", T.c_str(), T.c_str()));
+        S("for (int i = threadIdx.x; i < RD_H * UVU_P * 32; i += RD_TPB) {");
+        S("  const int l = i & 31, uu = sl * 32 + l;");
+        S("  wls[i] = uu < UVU_U ? __ldg(wlast + (size_t)(i >> 5) * UVU_U + uu) : 0;");
+        S("}");
+        S("__syncthreads();");
+        S(fmt("const %s* const wlb = wls + lane;", T.c_str()));
+        S("#else");
+        S(fmt("const %s* const wlb = wlast + u;", T.c_str()));
+        S("#endif");
+        S("if (u >= UVU_U || rb >= nbs) return;");
+        S("const int g = warp % RD_NG;");
+        S("for (long long r = rb * RD_RPB + warp / RD_NG; r < N; r += nbs * RD_RPB) {");
+        S.ind++;
+        S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+        S(fmt("%s* const orow = out + ((size_t)r * UVU_U + u) * UVU_DO;", T.c_str()));
+        for (int g = 0; g < NG; ++g)
+            S(fmt("%sif (g == %d) rad_group%d(e0, e1, src, x, Y, h, wlb, u, orow);", g ? "else " : "", g, g));
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+    }
 };
 
 }  // namespace
@@ -2043,7 +2154,69 @@ namespace uvu {
 // HVP call so that plans used only for the forward and the VJP do not pay for them.  They use
 // the direct-load structure and the plan's register groups.
 const char* const kAuxKernelNames[AUX_COUNT][2] = {
-    {"uvu_hvp_fwd", "uvu_hvp_edge"}, {"uvu_tp_fwd", "uvu_tp_edge"}, {"uvu_tp_fwd_sh", "uvu_tp_edge_sh"}};
+    {"uvu_hvp_fwd", "uvu_hvp_edge"}, {"uvu_tp_fwd", "uvu_tp_edge"}, {"uvu_tp_fwd_sh", "uvu_tp_edge_sh"},
+    {"uvu_fwd_radial", nullptr}};
+
+namespace {
+// Source of the fused-radial-weight forward for hidden width A.radial_h.  Register groups: runs
+// of consecutive paths whose accumulators plus the NE edges' weights fit one thread's budget
+// (UVU_RAD_BUDGET, a tuning switch, overrides it).  Warps per block: a multiple of the group
+// count near eight, sixteen when the last-layer slice leaves room for one block per SM only.
+std::string emit_radial_source(Plan* plan) {
+    Gen G{plan, plan->dtype == UVU_F64, plan->dtype == UVU_F64 ? "double" : "float"};
+    AuxBuild& A = plan->aux[AUX_RADIAL];
+    const int NE = A.radial_ne, H = A.radial_h;
+    int budget = G.f64 ? 48 : 96;
+    if (const char* e = std::getenv("UVU_RAD_BUDGET")) budget = std::max(8, std::atoi(e));
+    std::vector<std::vector<int>> rg(1);
+    int width = 0;
+    for (int p = 0; p < plan->P; ++p) {
+        const int c = 2 * plan->paths[p].l3 + 1 + NE;
+        if (!rg.back().empty() && width + c > budget) {
+            rg.emplace_back();
+            width = 0;
+        }
+        rg.back().push_back(p);
+        width += c;
+    }
+    const int NG = int(rg.size());
+    const size_t wsm_bytes = size_t(H) * plan->P * 32 * plan->elem();
+    A.radial_wsm = wsm_bytes <= 200 * 1024;
+    const size_t smem = A.radial_wsm ? wsm_bytes : 0;
+    const int fit = smem ? int(std::min<size_t>(4, (227 * 1024) / (smem + 1024))) : 4;
+    int rw = NG * std::max(1, (fit == 1 ? 16 : 8) / NG);
+    if (const char* e = std::getenv("UVU_RAD_RW")) rw = NG * std::max(1, std::atoi(e) / NG);
+    rw = std::min(rw, NG * std::max(1, 32 / NG));
+    if (rw * 32 > 1024) rw = NG;
+    const int minb = std::max(1, std::min({fit, A.minb[0], 2048 / (rw * 32)}));
+    A.minb_eff[0] = minb;
+    A.radial_nsl = (plan->U + 31) / 32;
+    A.radial_rpb = rw / NG;
+    A.g[0] = {rw * 32, 1, smem, true};
+    A.g[1] = {};
+    Src S;
+    S("// Generated by the UVU planner: forward with fused radial weights (last layer in registers).");
+    S(fmt("// irreps_x=%s irreps_sh=%s lmax_out=%d dtype=%s hidden=%d", plan->irreps_x.c_str(), plan->irreps_sh.c_str(),
+          plan->lmax_out, G.f64 ? "fp64" : "fp32", H));
+    S(fmt("#define UVU_U %d", plan->U));
+    S(fmt("#define UVU_P %d", plan->P));
+    S(fmt("#define UVU_DX %d", plan->Dx));
+    S(fmt("#define UVU_DY %d", plan->Dy));
+    S(fmt("#define UVU_DO %d", plan->Do));
+    S(fmt("#define RD_H %d", H));
+    S(fmt("#define RD_NE %d", NE));
+    S(fmt("#define RD_NG %d", NG));
+    S(fmt("#define RD_TPB %d", rw * 32));
+    S(fmt("#define RD_RPB %d", rw / NG));
+    S(fmt("#define RD_NSL %d", A.radial_nsl));
+    S(fmt("#define RD_WSM %d", A.radial_wsm ? 1 : 0));
+    S(fmt("#define RD_WSTR %s", A.radial_wsm ? "32" : "UVU_U"));
+    S(fmt("#define RD_MINB %d", minb));
+    S("__device__ unsigned int uvu_status_word;  // no bounded waits in this module: stays 0");
+    G.emit_fwd_radial(S, rg, NE);
+    return S.o.str();
+}
+}  // namespace
 
 // Source of an auxiliary module: the double backward (AUX_HVP) or the batched tensor product
 // with per-sample (AUX_TP) or batch-shared (AUX_TP_SHARED) weights.  For U >= 32 these are the
@@ -2051,6 +2224,7 @@ const char* const kAuxKernelNames[AUX_COUNT][2] = {
 // backward of smaller plans uses the direct-load kernels, and the batched tensor product needs
 // the pipelined plan (the C ABI refuses it otherwise).
 std::string emit_aux_source(Plan* plan, int kind) {
+    if (kind == AUX_RADIAL) return emit_radial_source(plan);
     Gen G{plan, plan->dtype == UVU_F64, plan->dtype == UVU_F64 ? "double" : "float"};
     AuxBuild& A = plan->aux[kind];
     const int U = plan->U, NG = int(plan->groups.size()), UP = plan->U_pad;

@@ -293,11 +293,22 @@ static uvu_status compile_aux_locked(Plan* plan, int kind, std::string* err) {
         uvu_status s = nvrtc_compile(A.source, &e, err);
         if (s != UVU_OK) return s;
         bool again = false;
-        for (int k = 0; k < 2 && attempt < 3; ++k)
-            if (plan->pipelined_recv && A.minb_eff[k] > 1 && spill_bytes(e.log, kAuxKernelNames[kind][k]) > 32) {
-                A.minb[k] = A.minb_eff[k] - 1;
-                again = true;
+        if (kind == AUX_RADIAL) {
+            // a spilling fused radial forward forms fewer edges' weights at a time, then gives
+            // up a resident block
+            if (attempt < 4 && spill_bytes(e.log, kAuxKernelNames[kind][0]) > 32) {
+                if (A.radial_ne > 1) A.radial_ne /= 2;
+                else if (A.minb_eff[0] > 1) A.minb[0] = A.minb_eff[0] - 1;
+                else attempt = 4;
+                again = attempt < 4;
             }
+        } else {
+            for (int k = 0; k < 2 && attempt < 3; ++k)
+                if (plan->pipelined_recv && A.minb_eff[k] > 1 && spill_bytes(e.log, kAuxKernelNames[kind][k]) > 32) {
+                    A.minb[k] = A.minb_eff[k] - 1;
+                    again = true;
+                }
+        }
         if (!again) {
             A.cubin = std::move(e.cubin);
             A.log = std::move(e.log);
@@ -323,6 +334,7 @@ uvu_status aux_module_for_current_device(Plan* plan, int kind, DeviceModule** ou
     if (!L.lib) {
         cudaError_t ce = cudaLibraryLoadData(&L.lib, A.cubin.data(), nullptr, nullptr, 0, nullptr, nullptr, 0);
         for (int k = 0; k < 2 && ce == cudaSuccess; ++k) {
+            if (!kAuxKernelNames[kind][k]) continue;  // one-kernel module
             ce = cudaLibraryGetKernel(&L.k[k], L.lib, kAuxKernelNames[kind][k]);
             const void* f = reinterpret_cast<const void*>(L.k[k]);
             if (ce == cudaSuccess && A.g[k].smem > 48 * 1024)

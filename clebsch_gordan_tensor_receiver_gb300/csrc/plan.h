@@ -46,7 +46,8 @@ struct KernelGeom {
 // Auxiliary modules of a plan, emitted and compiled on their first use, each with a
 // receiver-ordered "forward" kernel and an "edge" kernel: the double backward, and the batched
 // (non-convolution) tensor product with per-sample or batch-shared weights.
-enum AuxKind { AUX_HVP = 0, AUX_TP = 1, AUX_TP_SHARED = 2, AUX_COUNT = 3 };
+// The fused-radial-weight forward (AUX_RADIAL) has one kernel only.
+enum AuxKind { AUX_HVP = 0, AUX_TP = 1, AUX_TP_SHARED = 2, AUX_RADIAL = 3, AUX_COUNT = 4 };
 extern const char* const kAuxKernelNames[AUX_COUNT][2];
 
 struct AuxBuild {  // host side, per plan
@@ -55,6 +56,22 @@ struct AuxBuild {  // host side, per plan
     KernelGeom g[2];
     int minb[2] = {4, 4};      // register-budget caps (blocks per SM), lowered on spills
     int minb_eff[2] = {1, 1};  // value used by the last emission
+    // fused radial forward: hidden width the module is built for (0 = not yet), edges whose
+    // weights a thread forms together (lowered on spills), layout chosen at emission
+    int radial_h = 0;
+    int radial_ne = 4;
+    bool radial_wsm = false;   // last-layer slice staged in shared memory
+    int radial_nsl = 1;        // channel slices of 32
+    int radial_rpb = 1;        // receivers per block per round
+};
+
+// Radial network of the fused-weight forward (radial.cu): widths[0] = n_basis, then the hidden
+// layers' widths (multiples of 4), each layer followed by SiLU.
+constexpr int kRadialMaxLayers = 4;
+struct RadialNet {
+    int n_layers = 0;
+    int max_width = 0;
+    int widths[kRadialMaxLayers + 1] = {};
 };
 
 struct AuxLoaded {  // per device
@@ -136,6 +153,10 @@ cudaError_t launch_graph_validate(int64_t N, int64_t E, const int32_t* off, cons
                                   unsigned long long* bad, cudaStream_t st);
 // tp.cu
 cudaError_t launch_column_sum(const void* part, int64_t rows, int64_t cols, void* out, bool f64, cudaStream_t st);
+// radial.cu
+size_t radial_hidden_smem(const RadialNet& net, bool f64);
+cudaError_t launch_radial_hidden(int64_t E, const void* r, double r_cut, int p_env, const RadialNet& net, const void* W,
+                                 void* h, bool f64, int sm_count, cudaStream_t st);
 // mix.cu
 int mix_max_paths();
 size_t mix_workspace_bytes(const Plan& p, int64_t N, int W, bool bwd);

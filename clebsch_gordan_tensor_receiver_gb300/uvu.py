@@ -35,6 +35,7 @@ EXPORTS = (
     "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
     "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
     "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
+    "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source",
     "uvu_status_string", "uvu_last_error_message",
 )
 
@@ -82,6 +83,9 @@ def _load():
         "uvu_mix_bwd": [P, I64, I, P, P, P, P, P, P, SZ, P],
         "uvu_mix_workspace": [P, I64, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
         "uvu_conv_uvw_fwd": [P, I64, I64, P, P, P, P, P, P, I, P, P, P, SZ, P],
+        "uvu_radial_hidden": [P, I64, P, ctypes.c_double, I, I, ctypes.POINTER(I), P, P, P],
+        "uvu_conv_fwd_radial": [P, I64, I64, P, P, P, I, P, P, P, P, P],
+        "uvu_radial_module_source": [P, I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -120,7 +124,8 @@ for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source"
            "uvu_conv_bwd_dx", "uvu_conv_bwd_dx_reduce", "uvu_conv_bwd_workspace", "uvu_conv_bwd",
            "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
            "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
-           "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd"):
+           "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
+           "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source"):
     globals()[_n] = _wrap(_n)
 
 
@@ -209,6 +214,26 @@ class Plan:
 
     def hvp_source(self):
         return self.module_source(UVU_MODULE_HVP)
+
+    def radial_source(self, hidden: int):
+        """(source, NVRTC log) of the fused radial forward for `hidden` (fixes the plan's hidden
+        width); compiles it on the host if needed."""
+        s, l = ctypes.c_char_p(), ctypes.c_char_p()
+        uvu_radial_module_source(self.handle, int(hidden), ctypes.byref(s), ctypes.byref(l))
+        return s.value.decode(), l.value.decode()
+
+    def radial_hidden(self, r, r_cut, p_env, widths, weights, h, stream=None):
+        """Radial network h = silu(... silu(basis(r) W_1) ... W_L) (see uvu_radial_hidden);
+        `widths` = [n_basis, H_1, ..., H_L] (host ints), `weights` the layers back to back."""
+        wd = (ctypes.c_int * len(widths))(*[int(v) for v in widths])
+        uvu_radial_hidden(self.handle, r.numel(), _ptr(r), float(r_cut), int(p_env), len(widths) - 1, wd,
+                          _ptr(weights), _ptr(h), _stream(stream))
+
+    def fwd_radial(self, n_nodes, x, Y, h, w_last, recv_offsets, src, out, stream=None):
+        """Convolution with fused radial weights w = h W_last (see uvu_conv_fwd_radial)."""
+        uvu_conv_fwd_radial(self.handle, n_nodes, src.numel() if src is not None else 0, _ptr(x), _ptr(Y), _ptr(h),
+                            int(w_last.shape[0]), _ptr(w_last), _ptr(recv_offsets), _ptr(src), _ptr(out),
+                            _stream(stream))
 
     def tp_fwd(self, batch, x, y, w, out, w_shared=False, stream=None):
         """Batched tensor product (see uvu_tp_fwd)."""

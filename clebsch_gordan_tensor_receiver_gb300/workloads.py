@@ -251,3 +251,23 @@ def tp_inputs(spec: WorkloadSpec, batch: int, n_paths: int, dim_out: int, shared
     w = _normal(rng, (n_paths, spec.mul) if shared else (batch, n_paths, spec.mul), dtype)
     g = _normal(rng, (batch, spec.mul, dim_out), dtype)
     return np.ascontiguousarray(x), np.ascontiguousarray(y), np.ascontiguousarray(w), np.ascontiguousarray(g)
+
+
+def radial_inputs(spec: WorkloadSpec, n_edges: int, n_paths: int, n_basis: int = 8, hidden=(64, 64, 64),
+                  r_min: float = 0.75, r_cut: float = 5.0, seed: int = 0):
+    """Inputs of the convolution with fused radial weights on the irreps of `spec`:
+    edge lengths r [E] with density proportional to r^2 on [r_min, r_cut) (neighbours uniform in
+    space around each atom, none closer than r_min), the radial network's layers
+    W_i [H_(i-1)][H_i] ~ N(0, 1/H_(i-1)) with H_0 = n_basis, and its last layer
+    W_last [H][P][U] ~ N(0, 1/H) / sqrt(mean degree).  Seeded by (spec key, seed)."""
+    rng = np.random.default_rng(np.random.SeedSequence([SEED_BASE + spec.key, 11, seed]))
+    dtype = np.dtype(spec.dtype).type
+    a = (r_min / r_cut) ** 3
+    r = r_cut * np.cbrt(rng.uniform(a, 1.0, size=n_edges))
+    widths = [n_basis, *hidden]
+    layers = [(rng.standard_normal((widths[i], widths[i + 1])) / sqrt(widths[i])).astype(dtype)
+              for i in range(len(hidden))]
+    H = widths[-1]
+    w_last = rng.standard_normal((H, n_paths, spec.mul)) / sqrt(H) / sqrt(spec.w_scale_degree)
+    return (np.ascontiguousarray(r.astype(dtype)), [np.ascontiguousarray(W) for W in layers],
+            np.ascontiguousarray(w_last.astype(dtype)))

@@ -377,6 +377,47 @@ uvu_status uvu_tp_bwd(uvu_plan_t plan, int64_t batch, const void *x, const void 
 /* Bytes of device workspace uvu_tp_bwd needs (0 unless w_shared): min(B, 2048) * P * U * 8. */
 uvu_status uvu_tp_bwd_workspace(uvu_plan_t plan, int64_t batch, int w_shared, size_t *bytes);
 
+/* -------------------------------------------------------------- fused radial weights ---- */
+
+/* Radial network of the fused-weight convolution ("Receiver-streaming convolutions for
+ * channel-wise UVU tensor products", replies: the radial weights are materialised by a separate
+ * network before the convolution; fusing that network into it is named as the next step).  The
+ * page does not give the network; the one here is the radial network of MACE-style potentials.
+ * For each edge e with length r[e] > 0:
+ *     b_n   = sqrt(2 / r_cut) sin(n pi r / r_cut) / r * f(r / r_cut),   n = 1 .. widths[0]
+ *     f(s)  = 1 - (p+1)(p+2)/2 s^p + p(p+2) s^(p+1) - p(p+1)/2 s^(p+2) for s < 1, 0 otherwise
+ *     a_0 = b,  a_i = silu(a_(i-1) W_i) for i = 1 .. n_layers,  h[e] = a_(n_layers)
+ * with p = p_env and silu(v) = v / (1 + exp(-v)), no biases.  The last linear layer (hidden ->
+ * P x U) is not applied here: uvu_conv_fwd_radial applies it.
+ * r [E] and h [E][widths[n_layers]] are device memory of the plan's type; `weights` is device
+ * memory holding W_1 .. W_n_layers back to back, each row-major [widths[i-1]][widths[i]];
+ * `widths` is a host array of n_layers + 1 entries.  Limits: 1 <= n_layers <= 4,
+ * 1 <= widths[0] <= 64, later widths multiples of 4 in [4, 128], 1 <= p_env <= 16, r_cut > 0
+ * (UVU_ERR_INVALID_ARGUMENT otherwise).  Pointers 16-byte aligned; h is overwritten.
+ * Edges at or beyond r_cut get h = 0 (every layer maps 0 to 0).  Launches: 1 kernel. */
+uvu_status uvu_radial_hidden(uvu_plan_t plan, int64_t n_edges, const void *r, double r_cut, int p_env,
+                             int n_layers, const int *widths, const void *weights, void *h,
+                             uvu_stream_t stream);
+
+/* The convolution with fused radial weights: out = uvu_conv_fwd with
+ *     w[e,p,u] = sum_k h[e,k] w_last[k,p,u]
+ * formed in registers per (edge, channel) and never stored.  h [E][hidden] (uvu_radial_hidden's
+ * output), w_last [hidden][P][U]; the other arguments, layouts and the CSR are those of
+ * uvu_conv_fwd.  `hidden` is a multiple of 4 in [4, 256].  The kernel is generated for the
+ * plan's paths and for `hidden` on the first call (host, NVRTC); a plan serves one hidden width
+ * (a later call with another returns UVU_ERR_UNSUPPORTED).  Receivers without edges get zero
+ * rows.  Pointers 16-byte aligned (index arrays 4-byte); out is overwritten.
+ * Launches: 1 kernel. */
+uvu_status uvu_conv_fwd_radial(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges, const void *x,
+                               const void *Y, const void *h, int hidden, const void *w_last,
+                               const int32_t *recv_offsets, const int32_t *src, void *out,
+                               uvu_stream_t stream);
+
+/* Generated source and compile log of the fused radial forward for `hidden`, built on the host
+ * if it is not yet (this fixes the plan's hidden width, as a first uvu_conv_fwd_radial does).
+ * The strings stay valid for the plan's lifetime. */
+uvu_status uvu_radial_module_source(uvu_plan_t plan, int hidden, const char **source, const char **log);
+
 /* ---------------------------------------------------------------------------- errors ---- */
 
 const char *uvu_status_string(uvu_status s);

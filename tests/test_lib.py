@@ -149,3 +149,40 @@ def test_mixing_host_checks():
     for bad in (0, 5000):
         with pytest.raises(uvu.UVUError):
             p.mix_workspace_bytes(10, bad)
+
+
+def test_fused_radial_host_checks_and_module():
+    """The fused radial forward: its module compiles on the host for the plan's paths and the
+    hidden width (weights in registers, the last layer's channel slice in shared memory when it
+    fits, no spills on MACE-medium), a plan keeps one hidden width, and bad radial-network
+    arguments are refused before any device work."""
+    import numpy as np
+    import torch
+    from clebsch_gordan_tensor_receiver_gb300 import uvu
+    p = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3)
+    src, log = p.radial_source(64)
+    assert "uvu_fwd_radial" in src and "#define RD_H 64" in src and "#define RD_WSM 1" in src
+    assert "#define RD_NSL 4" in src
+    m = re.search(r"Function properties for uvu_fwd_radial\n.*?(\d+) bytes spill stores", log, re.S)
+    assert m and int(m.group(1)) == 0, log
+    with pytest.raises(uvu.UVUError) as ei:
+        p.radial_source(32)
+    assert ei.value.status == 2
+    big = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3)
+    assert "#define RD_WSM 0" in big.radial_source(128)[0]  # 128 x 13 x 32 fp32 > the shared-memory budget
+    q = uvu.Plan("16x0e+16x1o", "1x0e+1x1o+1x2e", 2)
+    for bad in (0, 6, 260):
+        with pytest.raises(uvu.UVUError) as ei:
+            q.radial_source(bad)
+        assert ei.value.status == 1
+    import types
+    r = torch.zeros(0)
+    h = torch.zeros(0, 8)
+    Wt = torch.zeros(64)
+    st = types.SimpleNamespace(cuda_stream=0)  # no device here: the calls return before any launch
+    for widths, pe, rc in (([8, 6], 5, 5.0), ([0, 8], 5, 5.0), ([8, 8], 0, 5.0), ([8, 8], 5, 0.0),
+                           ([8, 8, 8, 8, 8, 8], 5, 5.0), ([65, 8], 5, 5.0), ([8, 132], 5, 5.0)):
+        with pytest.raises(uvu.UVUError) as ei:
+            q.radial_hidden(r, rc, pe, widths, Wt, h, stream=st)
+        assert ei.value.status == 1, widths
+    q.radial_hidden(r, 5.0, 5, [8, 8], Wt, h, stream=st)  # no edges: nothing to do
