@@ -1867,11 +1867,15 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     // 32 channels, whose last-layer weights [H][P][32] sit in shared memory when they fit (else
     // they are read through the read-only cache).  Forming NE edges' weights together reuses each
     // last-layer weight NE times from a register.
-    void emit_radial_group(Src& S, int g, const std::vector<int>& paths, int NE) const {
+    // packed: fp32 weights formed two paths at a time with the paired FMA (fma.rn.f32x2), the
+    // last layer staged as (even, odd) path pairs per lane; each half rounds as a scalar FMA.
+    void emit_radial_group(Src& S, int g, const std::vector<int>& paths, int NE, bool packed) const {
         const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
         std::vector<int> outs;
         for (int pi : paths)
             for (int m = 0; m < 2 * P->paths[pi].l3 + 1; ++m) outs.push_back(P->paths[pi].ooff + m);
+        std::set<int> pairs;
+        for (int pi : paths) pairs.insert(pi / 2);
         const bool f = !f64;
         S(fmt("__device__ __forceinline__ void rad_group%d(int e0, int e1, const int* __restrict__ src, const %s* __restrict__ x,", g, T.c_str()));
         S(fmt("    const %s* __restrict__ Y, const %s* __restrict__ h, const %s* __restrict__ wlb, int u, %s* __restrict__ orow) {",
@@ -1882,9 +1886,21 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("for (int eb = e0; eb < e1; eb += RD_NE) {");
         S.ind++;
         S("const int ne = min(RD_NE, e1 - eb);");
+        // the batch's sender ids, and its x and Y rows asked into L1 before the weights are
+        // formed (UVU_RAD_PREFETCH=0, a tuning switch, leaves them to the loads after)
+        const bool pf = !(std::getenv("UVU_RAD_PREFETCH") && std::atoi(std::getenv("UVU_RAD_PREFETCH")) == 0);
+        for (int j = 0; j < NE; ++j) S(fmt("const int s%d = __ldg(src + eb + min(%d, ne - 1));", j, j));
+        if (pf)
+            for (int j = 0; j < NE; ++j) {
+                S(fmt("prefetch_l1(x + ((size_t)s%d * UVU_U + u) * UVU_DX);", j));
+                S(fmt("prefetch_l1(Y + (size_t)(eb + min(%d, ne - 1)) * UVU_DY);", j));
+            }
         for (int j = 0; j < NE; ++j) {
             S(fmt("const %s* __restrict__ hr%d = h + (size_t)(eb + min(%d, ne - 1)) * RD_H;", T.c_str(), j, j));
-            for (int pi : paths) S(fmt("%s w%d_%d = 0;", T.c_str(), j, pi));
+            if (packed)
+                for (int q : pairs) S(fmt("unsigned long long w%d_q%d = 0;", j, q));
+            else
+                for (int pi : paths) S(fmt("%s w%d_%d = 0;", T.c_str(), j, pi));
         }
         S("#pragma unroll 2");
         S("for (int k = 0; k < RD_H; k += 4) {");
@@ -1898,15 +1914,27 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 S(fmt("const double2 hqb%d = __ldg(reinterpret_cast<const double2*>(hr%d + k) + 1);", j, j));
             }
         }
-        S(fmt("const %s* __restrict__ wk = wlb + (size_t)k * (UVU_P * RD_WSTR);", T.c_str()));
-        for (int kk = 0; kk < 4; ++kk) {
-            for (int pi : paths) {
-                S(fmt("{ const %s wl = wk[%d * RD_WSTR];", T.c_str(), kk * P->P + pi));
-                for (int j = 0; j < NE; ++j) {
-                    const std::string hv = f ? fmt("hq%d.%s", j, comp[kk]) : fmt("hq%c%d.%s", kk < 2 ? 'a' : 'b', j, comp[kk % 2]);
-                    S(fmt("  w%d_%d = fma(%s, wl, w%d_%d);", j, pi, hv.c_str(), j, pi));
+        if (packed) {
+            S("const unsigned long long* __restrict__ wk = reinterpret_cast<const unsigned long long*>(wlb) + (size_t)k * (RD_P2 * 32);");
+            for (int kk = 0; kk < 4; ++kk) {
+                for (int j = 0; j < NE; ++j) S(fmt("const unsigned long long hp%d_%d = f2pack(hq%d.%s, hq%d.%s);", j, kk, j, comp[kk], j, comp[kk]));
+                for (int q : pairs) {
+                    S(fmt("{ const unsigned long long wl = wk[%d * 32];", kk * ((P->P + 1) / 2) + q));
+                    for (int j = 0; j < NE; ++j) S(fmt("  w%d_q%d = ffma2(hp%d_%d, wl, w%d_q%d);", j, q, j, kk, j, q));
+                    S("}");
                 }
-                S("}");
+            }
+        } else {
+            S(fmt("const %s* __restrict__ wk = wlb + (size_t)k * (UVU_P * RD_WSTR);", T.c_str()));
+            for (int kk = 0; kk < 4; ++kk) {
+                for (int pi : paths) {
+                    S(fmt("{ const %s wl = wk[%d * RD_WSTR];", T.c_str(), kk * P->P + pi));
+                    for (int j = 0; j < NE; ++j) {
+                        const std::string hv = f ? fmt("hq%d.%s", j, comp[kk]) : fmt("hq%c%d.%s", kk < 2 ? 'a' : 'b', j, comp[kk % 2]);
+                        S(fmt("  w%d_%d = fma(%s, wl, w%d_%d);", j, pi, hv.c_str(), j, pi));
+                    }
+                    S("}");
+                }
             }
         }
         S.ind--;
@@ -1915,10 +1943,14 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S(fmt("if (%d < ne) {", j));
             S.ind++;
             S(fmt("const int e = eb + %d;", j));
-            S("const int s = __ldg(src + e);");
-            emit_row_loads(S, "xv", "x + ((size_t)s * UVU_U + u) * UVU_DX", P->Dx, xn);
+            emit_row_loads(S, "xv", fmt("x + ((size_t)s%d * UVU_U + u) * UVU_DX", j), P->Dx, xn);
             emit_row_loads(S, "yv", "Y + (size_t)e * UVU_DY", P->Dy, yn);
-            for (int pi : paths) S(fmt("const %s wv_%d = w%d_%d;", T.c_str(), pi, j, pi));
+            if (packed) {
+                for (int q : pairs) S(fmt("float wq%d_a, wq%d_b; f2unpack(w%d_q%d, wq%d_a, wq%d_b);", q, q, j, q, q, q));
+                for (int pi : paths) S(fmt("const float wv_%d = wq%d_%c;", pi, pi / 2, pi % 2 ? 'b' : 'a'));
+            } else {
+                for (int pi : paths) S(fmt("const %s wv_%d = w%d_%d;", T.c_str(), pi, j, pi));
+            }
             emit_fwd_edge(S, paths);
             S.ind--;
             S("}");
@@ -1930,9 +1962,19 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("}");
     }
 
-    void emit_fwd_radial(Src& S, const std::vector<std::vector<int>>& rg, int NE) const {
+    void emit_fwd_radial(Src& S, const std::vector<std::vector<int>>& rg, int NE, bool packed) const {
         const int NG = int(rg.size());
-        for (int g = 0; g < NG; ++g) emit_radial_group(S, g, rg[g], NE);
+        S("__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile(\"prefetch.global.L1 [%0];\" :: \"l\"(p)); }");
+        if (packed) {
+            S("__device__ __forceinline__ unsigned long long f2pack(float a, float b) {");
+            S("  unsigned long long r; asm(\"mov.b64 %0, {%1, %2};\" : \"=l\"(r) : \"f\"(a), \"f\"(b)); return r; }");
+            S("__device__ __forceinline__ void f2unpack(unsigned long long v, float& a, float& b) {");
+            S("  asm(\"mov.b64 {%0, %1}, %2;\" : \"=f\"(a), \"=f\"(b) : \"l\"(v)); }");
+            S("// two fp32 FMAs in one instruction, each rounded as fmaf");
+            S("__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {");
+            S("  unsigned long long d; asm(\"fma.rn.f32x2 %0, %1, %2, %3;\" : \"=l\"(d) : \"l\"(a), \"l\"(b), \"l\"(c)); return d; }");
+        }
+        for (int g = 0; g < NG; ++g) emit_radial_group(S, g, rg[g], NE, packed);
         S(fmt("extern \"C\" __global__ void __launch_bounds__(RD_TPB, RD_MINB) uvu_fwd_radial(long long N, const int* __restrict__ off,"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ h,",
               T.c_str(), T.c_str(), T.c_str()));
@@ -1945,12 +1987,19 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("#if RD_WSM");
         S("extern __shared__ __align__(16) unsigned char smem[];");
         S(fmt("%s* const wls = reinterpret_cast<%s*>(smem);", T.c_str(), T.c_str()));
-        S("for (int i = threadIdx.x; i < RD_H * UVU_P * 32; i += RD_TPB) {");
-        S("  const int l = i & 31, uu = sl * 32 + l;");
-        S("  wls[i] = uu < UVU_U ? __ldg(wlast + (size_t)(i >> 5) * UVU_U + uu) : 0;");
-        S("}");
+        if (packed) {  // [k][path pair][lane][2]; the odd path past the last is zero
+            S("for (int i = threadIdx.x; i < RD_H * RD_P2 * 64; i += RD_TPB) {");
+            S("  const int l = (i >> 1) & 31, uu = sl * 32 + l, kq = i >> 6, k = kq / RD_P2, p = 2 * (kq - k * RD_P2) + (i & 1);");
+            S("  wls[i] = (uu < UVU_U && p < UVU_P) ? __ldg(wlast + ((size_t)k * UVU_P + p) * UVU_U + uu) : 0;");
+            S("}");
+        } else {  // [k][path][lane]
+            S("for (int i = threadIdx.x; i < RD_H * UVU_P * 32; i += RD_TPB) {");
+            S("  const int l = i & 31, uu = sl * 32 + l;");
+            S("  wls[i] = uu < UVU_U ? __ldg(wlast + (size_t)(i >> 5) * UVU_U + uu) : 0;");
+            S("}");
+        }
         S("__syncthreads();");
-        S(fmt("const %s* const wlb = wls + lane;", T.c_str()));
+        S(fmt("const %s* const wlb = wls + %s;", T.c_str(), packed ? "2 * lane" : "lane"));
         S("#else");
         S(fmt("const %s* const wlb = wlast + u;", T.c_str()));
         S("#endif");
@@ -2161,12 +2210,16 @@ namespace {
 // Source of the fused-radial-weight forward for hidden width A.radial_h.  Register groups: runs
 // of consecutive paths whose accumulators plus the NE edges' weights fit one thread's budget
 // (UVU_RAD_BUDGET, a tuning switch, overrides it).  Warps per block: a multiple of the group
-// count near eight, sixteen when the last-layer slice leaves room for one block per SM only.
+// count near six (two blocks per SM: twelve warps of up to 168 registers), twelve when the
+// last-layer slice leaves room for one block per SM only.  Measured on MACE-medium (hidden 64):
+// three edges per thread with twelve warps per SM ran 1.89 ms, against 2.22 ms for two edges
+// with sixteen warps (128 registers) and 1.96 ms for four edges with twelve warps; the
+// shared-memory reads of the last layer (one per FMA / NE) bound the two-edge form.
 std::string emit_radial_source(Plan* plan) {
     Gen G{plan, plan->dtype == UVU_F64, plan->dtype == UVU_F64 ? "double" : "float"};
     AuxBuild& A = plan->aux[AUX_RADIAL];
     const int NE = A.radial_ne, H = A.radial_h;
-    int budget = G.f64 ? 48 : 96;
+    int budget = G.f64 ? 64 : 128;
     if (const char* e = std::getenv("UVU_RAD_BUDGET")) budget = std::max(8, std::atoi(e));
     std::vector<std::vector<int>> rg(1);
     int width = 0;
@@ -2180,11 +2233,17 @@ std::string emit_radial_source(Plan* plan) {
         width += c;
     }
     const int NG = int(rg.size());
-    const size_t wsm_bytes = size_t(H) * plan->P * 32 * plan->elem();
-    A.radial_wsm = wsm_bytes <= 200 * 1024;
+    // fp32 plans pair the paths (UVU_RAD_PACK=0, a tuning switch, keeps one path per FMA)
+    const int P2 = (plan->P + 1) / 2;
+    const bool pack_ok = !G.f64 && !(std::getenv("UVU_RAD_PACK") && std::atoi(std::getenv("UVU_RAD_PACK")) == 0);
+    const size_t wsm_packed = size_t(H) * P2 * 64 * plan->elem();
+    const size_t wsm_plain = size_t(H) * plan->P * 32 * plan->elem();
+    const bool packed = pack_ok && wsm_packed <= 200 * 1024 + 16 * 1024;
+    const size_t wsm_bytes = packed ? wsm_packed : wsm_plain;
+    A.radial_wsm = packed || wsm_bytes <= 200 * 1024;
     const size_t smem = A.radial_wsm ? wsm_bytes : 0;
     const int fit = smem ? int(std::min<size_t>(4, (227 * 1024) / (smem + 1024))) : 4;
-    int rw = NG * std::max(1, (fit == 1 ? 16 : 8) / NG);
+    int rw = NG * std::max(1, (fit == 1 ? 12 : 6) / NG);
     if (const char* e = std::getenv("UVU_RAD_RW")) rw = NG * std::max(1, std::atoi(e) / NG);
     rw = std::min(rw, NG * std::max(1, 32 / NG));
     if (rw * 32 > 1024) rw = NG;
@@ -2211,9 +2270,11 @@ std::string emit_radial_source(Plan* plan) {
     S(fmt("#define RD_NSL %d", A.radial_nsl));
     S(fmt("#define RD_WSM %d", A.radial_wsm ? 1 : 0));
     S(fmt("#define RD_WSTR %s", A.radial_wsm ? "32" : "UVU_U"));
+    S(fmt("#define RD_P2 %d", P2));
+    S(fmt("#define RD_PACKED %d", packed ? 1 : 0));
     S(fmt("#define RD_MINB %d", minb));
     S("__device__ unsigned int uvu_status_word;  // no bounded waits in this module: stays 0");
-    G.emit_fwd_radial(S, rg, NE);
+    G.emit_fwd_radial(S, rg, NE, packed);
     return S.o.str();
 }
 }  // namespace

@@ -59,7 +59,7 @@ struct AuxBuild {  // host side, per plan
     // fused radial forward: hidden width the module is built for (0 = not yet), edges whose
     // weights a thread forms together (lowered on spills), layout chosen at emission
     int radial_h = 0;
-    int radial_ne = 4;
+    int radial_ne = 3;
     bool radial_wsm = false;   // last-layer slice staged in shared memory
     int radial_nsl = 1;        // channel slices of 32
     int radial_rpb = 1;        // receivers per block per round
