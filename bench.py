@@ -651,10 +651,15 @@ def main(argv=None):
         s_in, s_cmp, s_out = torch.cuda.Stream(dev), stream, torch.cuda.Stream(dev)
         mode_e2e = args.dx_mode
 
-        def e2e_step():
+        def e2e_step(s_cmp=s_cmp, capture=False):
+            # s_cmp: the compute stream (the capturing stream when recorded into a CUDA graph);
+            # the copy streams fork from it and join it again at the end
             ev_in, ev_cmp = [], []
             with torch.cuda.stream(s_in):
-                s_in.wait_stream(s_out)  # previous step's results are out before buffers are reused
+                if capture:
+                    s_in.wait_stream(s_cmp)  # fork; replays of the graph run one after another
+                else:
+                    s_in.wait_stream(s_out)  # previous step's results are out before buffers are reused
                 for k in ("x", "roff", "src", "soff", "seid", "srecv"):
                     dbuf[k].copy_(hin[k], non_blocking=True)
                 for a, b in zip(cuts[:-1], cuts[1:]):
@@ -692,6 +697,7 @@ def main(argv=None):
                     hout["dw"][e0:e1].copy_(dw[e0:e1], non_blocking=True)
                 s_out.wait_event(ev_dx)
                 hout["dx"].copy_(dx, non_blocking=True)
+            s_cmp.wait_stream(s_out)
 
         # device-resident results of one ordinary step, to check the chunked host path against
         step(args.dx_mode)
@@ -701,17 +707,53 @@ def main(argv=None):
             e2e_step()
         torch.cuda.synchronize()
         same = all(torch.equal(hout[k], ref[k].cpu()) for k in ref) if args.dx_mode != "atomic" else None
-        del ref
         barrier(world)
         tw = time.perf_counter()
+        issue = 0.0
         for _ in range(args.e2e_steps):
+            ti = time.perf_counter()
             e2e_step()
+            issue += time.perf_counter() - ti
         torch.cuda.synchronize()
-        e_ms = max_over_ranks((time.perf_counter() - tw) * 1000 / args.e2e_steps, world, dev)
+        eager_ms = (time.perf_counter() - tw) * 1000 / args.e2e_steps
+        issue_ms = issue * 1000 / args.e2e_steps
+        # The same step recorded once into a CUDA graph (copies, the library's kernels and the
+        # stream fork/join) and replayed: the host then issues one launch per step instead of
+        # about a hundred, so a slow or busy host CPU no longer sets the step time.
+        graph_ms, graph_err, graph_same = None, None, None
+        try:
+            cg = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(cg, stream=cap):
+                e2e_step(s_cmp=cap, capture=True)
+            torch.cuda.synchronize()
+            for v in hout.values():
+                v.zero_()
+            cg.replay()
+            torch.cuda.synchronize()
+            graph_same = all(torch.equal(hout[k], ref[k].cpu()) for k in ref) if args.dx_mode != "atomic" else None
+            barrier(world)
+            tw = time.perf_counter()
+            for _ in range(args.e2e_steps):
+                cg.replay()
+            torch.cuda.synchronize()
+            graph_ms = (time.perf_counter() - tw) * 1000 / args.e2e_steps
+            del cg
+        except Exception as ex:  # capture unsupported here: the eager step stands
+            graph_err = f"{type(ex).__name__}: {ex}"[:200]
+            torch.cuda.synchronize()
+        del ref
+        use_graph = graph_ms is not None and graph_same is not False
+        e_ms = max_over_ranks(graph_ms if use_graph else eager_ms, world, dev)
         # the results that came back are the full outputs of the step
         line["e2e"] = {"value": world * E / (e_ms / 1000), "unit": "edges/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+                       "launch": "cuda_graph" if use_graph else "eager",
+                       "eager_ms_per_step": eager_ms, "eager_host_issue_ms_per_step": issue_ms,
+                       "graph_ms_per_step": graph_ms, "graph_error": graph_err,
                        "chunks": len(cuts) - 1, "dx_mode": mode_e2e, "bitwise_equal_to_resident": same,
+                       "graph_bitwise_equal_to_resident": graph_same,
                        "h2d_GB_s": h2d / (e_ms / 1000) / 1e9, "d2h_GB_s": d2h / (e_ms / 1000) / 1e9}
 
         # this machine's host link, measured the same way (pinned buffers, one large copy each way,
