@@ -11,7 +11,9 @@
 // One block takes tiles of 64 edges.  The activations of a tile live in shared memory, feature-
 // major ([feature][edge]), so that a thread reads four consecutive edges with one vector load;
 // each thread computes a 4 x 4 block (edges x output features) of a layer from four edges'
-// inputs and four features' weights per input feature (weights read through the read-only cache).
+// inputs and four features' weights per input feature.  The weights of all layers are copied
+// into shared memory once per block when they fit in 64 KB (8-64-64-64: 35 KB), else read
+// through the read-only cache.
 #include <algorithm>
 #include <cmath>
 
@@ -54,13 +56,22 @@ __device__ __forceinline__ double sin_t(double v) { return sin(v); }
 __device__ __forceinline__ float sqrt_t(float v) { return sqrtf(v); }
 __device__ __forceinline__ double sqrt_t(double v) { return sqrt(v); }
 
-template <typename T>
+// W_SM: the layers' weights (n_w values) are copied into shared memory once per block, ahead of
+// the activation buffers; otherwise they are read through the read-only cache.
+template <typename T, bool W_SM>
 __global__ void __launch_bounds__(kThreads) radial_hidden_kernel(long long E, const T* __restrict__ r, T r_cut, int p_env,
-                                                                 RadialNet net, const T* __restrict__ W, T* __restrict__ h) {
+                                                                 RadialNet net, const T* __restrict__ Wg, int n_w,
+                                                                 T* __restrict__ h) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    T* const bufA = reinterpret_cast<T*>(smem_raw);
+    T* const wsm = reinterpret_cast<T*>(smem_raw);
+    T* const bufA = wsm + (W_SM ? (n_w + 3) / 4 * 4 : 0);
     T* const bufB = bufA + size_t(net.max_width) * kTE;
     const int tid = threadIdx.x;
+    if (W_SM) {
+        for (int i = tid; i < n_w; i += kThreads) wsm[i] = Wg[i];
+        __syncthreads();
+    }
+    const T* const W = W_SM ? wsm : Wg;
     const int nb = net.widths[0], H = net.widths[net.n_layers];
     const T pi_over_rc = T(3.14159265358979323846) / r_cut;
     const T norm = sqrt_t(T(2) / r_cut);
@@ -97,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) radial_hidden_kernel(long long E, co
 #pragma unroll 2
                 for (int k = 0; k < hin; ++k) {
                     const Q4<T> a = lds4(in + k * kTE + 4 * eq);
-                    const Q4<T> w = ldg4(Wl + size_t(k) * hout + 4 * q);
+                    const Q4<T> w = W_SM ? lds4(Wl + size_t(k) * hout + 4 * q) : ldg4(Wl + size_t(k) * hout + 4 * q);
                     const T av[4] = {a.a, a.b, a.c, a.d}, wv[4] = {w.a, w.b, w.c, w.d};
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
@@ -127,29 +138,50 @@ __global__ void __launch_bounds__(kThreads) radial_hidden_kernel(long long E, co
 
 }  // namespace
 
+namespace {
+int weight_count(const RadialNet& net) {
+    int n = 0;
+    for (int l = 0; l < net.n_layers; ++l) n += net.widths[l] * net.widths[l + 1];
+    return n;
+}
+// weights staged in shared memory when they take at most this many bytes
+constexpr size_t kWeightSmemMax = 64 * 1024;
+
+// Persistent grid: the blocks that are resident at once (a whole number per SM), each looping
+// over tiles.
+template <typename T, bool W_SM>
+cudaError_t launch_t(int64_t E, const void* r, double r_cut, int p_env, const RadialNet& net, const void* W, void* h,
+                     size_t smem, int sm_count, cudaStream_t st) {
+    auto k = radial_hidden_kernel<T, W_SM>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    int per_sm = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t tiles = (E + kTE - 1) / kTE;
+    const unsigned blocks = unsigned(std::min<int64_t>(tiles, int64_t(std::max(1, sm_count)) * std::max(1, per_sm)));
+    k<<<blocks, kThreads, smem, st>>>(E, static_cast<const T*>(r), T(r_cut), p_env, net, static_cast<const T*>(W),
+                                      weight_count(net), static_cast<T*>(h));
+    return cudaGetLastError();
+}
+}  // namespace
+
 size_t radial_hidden_smem(const RadialNet& net, bool f64) {
-    return 2 * size_t(net.max_width) * kTE * (f64 ? 8 : 4);
+    const size_t es = f64 ? 8 : 4;
+    const size_t wb = size_t(weight_count(net) + 3) / 4 * 4 * es;
+    return 2 * size_t(net.max_width) * kTE * es + (wb <= kWeightSmemMax ? wb : 0);
 }
 
 cudaError_t launch_radial_hidden(int64_t E, const void* r, double r_cut, int p_env, const RadialNet& net, const void* W,
                                  void* h, bool f64, int sm_count, cudaStream_t st) {
     if (E <= 0) return cudaSuccess;
+    const size_t es = f64 ? 8 : 4;
+    const bool wsm = size_t(weight_count(net) + 3) / 4 * 4 * es <= kWeightSmemMax;
     const size_t smem = radial_hidden_smem(net, f64);
-    const int64_t tiles = (E + kTE - 1) / kTE;
-    const unsigned blocks = unsigned(std::min<int64_t>(tiles, int64_t(std::max(1, sm_count)) * 4));
-    cudaError_t e;
-    if (f64) {
-        e = cudaFuncSetAttribute(radial_hidden_kernel<double>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return e;
-        radial_hidden_kernel<double><<<blocks, kThreads, smem, st>>>(E, static_cast<const double*>(r), r_cut, p_env, net,
-                                                                      static_cast<const double*>(W), static_cast<double*>(h));
-    } else {
-        e = cudaFuncSetAttribute(radial_hidden_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e != cudaSuccess) return e;
-        radial_hidden_kernel<float><<<blocks, kThreads, smem, st>>>(E, static_cast<const float*>(r), float(r_cut), p_env, net,
-                                                                     static_cast<const float*>(W), static_cast<float*>(h));
-    }
-    return cudaGetLastError();
+    if (f64)
+        return wsm ? launch_t<double, true>(E, r, r_cut, p_env, net, W, h, smem, sm_count, st)
+                   : launch_t<double, false>(E, r, r_cut, p_env, net, W, h, smem, sm_count, st);
+    return wsm ? launch_t<float, true>(E, r, r_cut, p_env, net, W, h, smem, sm_count, st)
+               : launch_t<float, false>(E, r, r_cut, p_env, net, W, h, smem, sm_count, st);
 }
 
 }  // namespace uvu

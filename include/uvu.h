@@ -32,6 +32,10 @@
  * recv_offsets + r0 with n_nodes = r1 - r0 and the matching rows of out / d_out (the edge-indexed
  * tensors keep their base pointers).  No entry point allocates device memory; the transpose takes a caller workspace.
  * Streams: work is enqueued on `stream` (0 = legacy default) and returns before it completes.
+ * Once a plan's kernels for a call are loaded on the device (its first such call, which compiles
+ * and loads the module), a call only enqueues kernel launches (and, for some, an asynchronous
+ * memset) with no host synchronisation, so a sequence of calls can be recorded into a CUDA graph
+ * by stream capture and replayed.
  * Outputs are overwritten, never accumulated: receivers without edges get out = 0, senders
  * without edges get dx = 0, n_edges == 0 writes zeros.
  * Errors: argument errors are detected on the host before anything is enqueued and return
