@@ -236,6 +236,11 @@ def main(argv=None):
     if args.impl == "reference":
         return run_reference(args)
 
+    # More hardware work queues than the default eight, set before the CUDA context exists: the
+    # e2e leg's copy-in and copy-out streams otherwise can share a queue with each other or with
+    # streams created earlier in the run, and then the two copy directions run one after the
+    # other (measured: 26 ms per step instead of 13 on the same box and buffers).
+    os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
     import numpy as np
     import torch
 
