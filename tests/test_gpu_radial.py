@@ -109,16 +109,19 @@ def test_one_hidden_width_per_plan():
         plan.radial_source(32)
 
 
-def test_mace_medium_sampled_receivers():
-    """The MACE-medium workload (5,000 receivers, 280,000 edges) in the launch configuration the
-    benchmark times, checked on sampled receivers (and every receiver against non-NaN)."""
-    wl = workloads.make_workload(1)
-    rng = np.random.default_rng(1234)
+@pytest.mark.parametrize("key", [1, 2, 3, 4])
+def test_full_size_sampled_receivers(key):
+    """The full-size workloads (MACE-medium in the launch configuration the benchmark times;
+    MACE-large; the wide proxy with U = 256, 24 paths and eight channel slices; the irregular fp64
+    graph with the last layer read through the cache), checked on sampled receivers (and every
+    receiver against non-NaN)."""
+    wl = workloads.make_workload(key)
+    rng = np.random.default_rng(1234 + key)
     rs = np.unique(np.concatenate([rng.choice(wl.n_nodes, 40, replace=False), [0, wl.n_nodes - 1]]))
     h, out, h_ref, ref, f64, _ = _run(wl.spec, wl.recv, wl.src, wl.x, wl.Y, wl.n_nodes, receivers=rs)
     es = rng.choice(wl.n_edges, 2000, replace=False)
-    check(h[torch.from_numpy(es).cuda()].cpu().numpy(), h_ref[es], False, "h")
-    check(out[torch.from_numpy(rs).cuda()].cpu().numpy(), ref, False, "out")
+    check(h[torch.from_numpy(es).cuda()].cpu().numpy(), h_ref[es], f64, "h")
+    check(out[torch.from_numpy(rs).cuda()].cpu().numpy(), ref, f64, "out")
     assert not torch.isnan(out).any()
 
 
