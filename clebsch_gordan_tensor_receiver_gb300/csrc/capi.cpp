@@ -756,8 +756,10 @@ uvu_status radial_prepare(Plan* p, int hidden) {
     AuxBuild& A = p->aux[AUX_RADIAL];
     if (A.radial_h == 0) {
         A.radial_h = hidden;
-        // UVU_RAD_NE (a tuning switch): edges whose weights a thread forms together
+        // UVU_RAD_NE / UVU_RAD_MINB (tuning switches): edges whose weights a thread forms
+        // together; cap on resident blocks per SM the register budget is sized for
         if (const char* e = std::getenv("UVU_RAD_NE")) A.radial_ne = std::max(1, std::min(8, std::atoi(e)));
+        if (const char* e = std::getenv("UVU_RAD_MINB")) A.minb[0] = std::max(1, std::min(8, std::atoi(e)));
     } else if (A.radial_h != hidden) {
         return fail(UVU_ERR_UNSUPPORTED, "this plan's fused radial forward was built for hidden width " +
                                              std::to_string(A.radial_h));
@@ -841,7 +843,7 @@ extern "C" uvu_status uvu_conv_fwd_radial(uvu_plan_t plan, int64_t n_nodes, int6
     const AuxBuild& A = p->aux[AUX_RADIAL];
     // grid: whole channel slices, each with the resident blocks' share (at most one block per
     // A.radial_rpb receivers)
-    const int64_t nsl = A.radial_nsl;
+    const int64_t nsl = int64_t(A.radial_nsl) * A.radial_gblk;
     const int64_t want = (n_nodes + A.radial_rpb - 1) / A.radial_rpb;
     const int64_t per_slice = std::max<int64_t>(1, std::min<int64_t>(want, int64_t(L.occ[0]) * m->sm_count / nsl));
     long long N = n_nodes;

@@ -1869,7 +1869,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     // last-layer weight NE times from a register.
     // packed: fp32 weights formed two paths at a time with the paired FMA (fma.rn.f32x2), the
     // last layer staged as (even, odd) path pairs per lane; each half rounds as a scalar FMA.
-    void emit_radial_group(Src& S, int g, const std::vector<int>& paths, int NE, bool packed) const {
+    // split: the block holds only this group's path pairs [q0, q0 + gp) of the last layer
+    void emit_radial_group(Src& S, int g, const std::vector<int>& paths, int NE, bool packed, bool split = false) const {
         const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
         std::vector<int> outs;
         for (int pi : paths)
@@ -1915,11 +1916,13 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             }
         }
         if (packed) {
-            S("const unsigned long long* __restrict__ wk = reinterpret_cast<const unsigned long long*>(wlb) + (size_t)k * (RD_P2 * 32);");
+            const int q0 = split ? *pairs.begin() : 0;
+            const int gp = split ? int(pairs.size()) : (P->P + 1) / 2;
+            S(fmt("const unsigned long long* __restrict__ wk = reinterpret_cast<const unsigned long long*>(wlb) + (size_t)k * (%d * 32);", gp));
             for (int kk = 0; kk < 4; ++kk) {
                 for (int j = 0; j < NE; ++j) S(fmt("const unsigned long long hp%d_%d = f2pack(hq%d.%s, hq%d.%s);", j, kk, j, comp[kk], j, comp[kk]));
                 for (int q : pairs) {
-                    S(fmt("{ const unsigned long long wl = wk[%d * 32];", kk * ((P->P + 1) / 2) + q));
+                    S(fmt("{ const unsigned long long wl = wk[%d * 32];", kk * gp + (q - q0)));
                     for (int j = 0; j < NE; ++j) S(fmt("  w%d_q%d = ffma2(hp%d_%d, wl, w%d_q%d);", j, q, j, kk, j, q));
                     S("}");
                 }
@@ -1962,7 +1965,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("}");
     }
 
-    void emit_fwd_radial(Src& S, const std::vector<std::vector<int>>& rg, int NE, bool packed) const {
+    // split: one block per (channel slice, register group), holding that group's pairs only
+    void emit_fwd_radial(Src& S, const std::vector<std::vector<int>>& rg, int NE, bool packed, bool split = false) const {
         const int NG = int(rg.size());
         S("__device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile(\"prefetch.global.L1 [%0];\" :: \"l\"(p)); }");
         if (packed) {
@@ -1974,7 +1978,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {");
             S("  unsigned long long d; asm(\"fma.rn.f32x2 %0, %1, %2, %3;\" : \"=l\"(d) : \"l\"(a), \"l\"(b), \"l\"(c)); return d; }");
         }
-        for (int g = 0; g < NG; ++g) emit_radial_group(S, g, rg[g], NE, packed);
+        for (int g = 0; g < NG; ++g) emit_radial_group(S, g, rg[g], NE, packed, split);
+        if (split) {
+            emit_fwd_radial_split(S, rg);
+            return;
+        }
         S(fmt("extern \"C\" __global__ void __launch_bounds__(RD_TPB, RD_MINB) uvu_fwd_radial(long long N, const int* __restrict__ off,"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y, const %s* __restrict__ h,",
               T.c_str(), T.c_str(), T.c_str()));
@@ -2009,6 +2017,46 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S.ind++;
         S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
         S(fmt("%s* const orow = out + ((size_t)r * UVU_U + u) * UVU_DO;", T.c_str()));
+        for (int g = 0; g < NG; ++g)
+            S(fmt("%sif (g == %d) rad_group%d(e0, e1, src, x, Y, h, wlb, u, orow);", g ? "else " : "", g, g));
+        S.ind--;
+        S("}");
+        S.ind--;
+        S("}");
+    }
+    void emit_fwd_radial_split(Src& S, const std::vector<std::vector<int>>& rg) const {
+        const int NG = int(rg.size());
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(RD_TPB, RD_MINB) uvu_fwd_radial(long long N, const int* __restrict__ off,"));
+        S("    const int* __restrict__ src, const float* __restrict__ x, const float* __restrict__ Y, const float* __restrict__ h,");
+        S("    const float* __restrict__ wlast, float* __restrict__ out) {");
+        S.ind++;
+        S("const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;");
+        S("const int sl = blockIdx.x % RD_NSL, g = (blockIdx.x / RD_NSL) % RD_NG;");
+        S("const long long rb = blockIdx.x / (RD_NSL * RD_NG), nbs = gridDim.x / (RD_NSL * RD_NG);");
+        S("const int u = sl * 32 + lane;");
+        S("extern __shared__ __align__(16) unsigned char smem[];");
+        S("float* const wls = reinterpret_cast<float*>(smem);");
+        std::string q0s = "{", gps = "{";
+        for (int g = 0; g < NG; ++g) {
+            std::set<int> pr;
+            for (int pi : rg[g]) pr.insert(pi / 2);
+            q0s += fmt("%s%d", g ? ", " : "", *pr.begin());
+            gps += fmt("%s%d", g ? ", " : "", int(pr.size()));
+        }
+        S(fmt("const int q0s[RD_NG] = %s}, gps[RD_NG] = %s};", q0s.c_str(), gps.c_str()));
+        S("const int q0 = q0s[g], gp = gps[g];");
+        S("// [k][pair of this group][lane][2]; a path past the last is zero");
+        S("for (int i = threadIdx.x; i < RD_H * gp * 64; i += RD_TPB) {");
+        S("  const int l = (i >> 1) & 31, uu = sl * 32 + l, kq = i >> 6, k = kq / gp, p = 2 * (q0 + kq - k * gp) + (i & 1);");
+        S("  wls[i] = (uu < UVU_U && p < UVU_P) ? __ldg(wlast + ((size_t)k * UVU_P + p) * UVU_U + uu) : 0.f;");
+        S("}");
+        S("__syncthreads();");
+        S("const float* const wlb = wls + 2 * lane;");
+        S("if (u >= UVU_U || rb >= nbs) return;");
+        S("for (long long r = rb * RD_RPB + warp; r < N; r += nbs * RD_RPB) {");
+        S.ind++;
+        S("const int e0 = __ldg(off + r), e1 = __ldg(off + r + 1);");
+        S("float* const orow = out + ((size_t)r * UVU_U + u) * UVU_DO;");
         for (int g = 0; g < NG; ++g)
             S(fmt("%sif (g == %d) rad_group%d(e0, e1, src, x, Y, h, wlb, u, orow);", g ? "else " : "", g, g));
         S.ind--;
@@ -2232,13 +2280,59 @@ std::string emit_radial_source(Plan* plan) {
         rg.back().push_back(p);
         width += c;
     }
-    const int NG = int(rg.size());
     // fp32 plans pair the paths (UVU_RAD_PACK=0, a tuning switch, keeps one path per FMA)
     const int P2 = (plan->P + 1) / 2;
     const bool pack_ok = !G.f64 && !(std::getenv("UVU_RAD_PACK") && std::atoi(std::getenv("UVU_RAD_PACK")) == 0);
     const size_t wsm_packed = size_t(H) * P2 * 64 * plan->elem();
     const size_t wsm_plain = size_t(H) * plan->P * 32 * plan->elem();
     const bool packed = pack_ok && wsm_packed <= 200 * 1024 + 16 * 1024;
+    // UVU_RAD_SPLIT=n (a tuning switch): the paths in n runs of whole pairs, one block per (channel
+    // slice, run), each block holding its run's part of the last layer only
+    const int split_n = (packed && std::getenv("UVU_RAD_SPLIT")) ? std::min(P2, std::atoi(std::getenv("UVU_RAD_SPLIT"))) : 0;
+    if (split_n >= 2) {
+        rg.assign(split_n, {});
+        for (int p = 0; p < plan->P; ++p) rg[std::min(split_n - 1, ((p / 2) * 2 + 1) * split_n / (2 * P2))].push_back(p);
+        size_t gpmax = 0;
+        for (auto& v : rg) gpmax = std::max<size_t>(gpmax, (v.back() / 2) - (v.front() / 2) + 1);
+        const size_t smem = size_t(H) * gpmax * 64 * plan->elem();
+        const int fit = int(std::min<size_t>(8, (227 * 1024) / (smem + 1024)));
+        int rw = 6;
+        if (const char* e = std::getenv("UVU_RAD_RW")) rw = std::max(1, std::min(32, std::atoi(e)));
+        const int minb = std::max(1, std::min({fit, A.minb[0], 2048 / (rw * 32)}));
+        A.minb_eff[0] = minb;
+        A.radial_wsm = true;
+        A.radial_nsl = (plan->U + 31) / 32;
+        A.radial_rpb = rw;
+        A.radial_gblk = split_n;
+        A.g[0] = {rw * 32, 1, smem, true};
+        A.g[1] = {};
+        Src S;
+        S("// Generated by the UVU planner: forward with fused radial weights (last layer in registers),");
+        S("// one block per (channel slice, run of path pairs).");
+        S(fmt("// irreps_x=%s irreps_sh=%s lmax_out=%d dtype=fp32 hidden=%d", plan->irreps_x.c_str(), plan->irreps_sh.c_str(),
+              plan->lmax_out, H));
+        S(fmt("#define UVU_U %d", plan->U));
+        S(fmt("#define UVU_P %d", plan->P));
+        S(fmt("#define UVU_DX %d", plan->Dx));
+        S(fmt("#define UVU_DY %d", plan->Dy));
+        S(fmt("#define UVU_DO %d", plan->Do));
+        S(fmt("#define RD_H %d", H));
+        S(fmt("#define RD_NE %d", NE));
+        S(fmt("#define RD_NG %d", split_n));
+        S(fmt("#define RD_TPB %d", rw * 32));
+        S(fmt("#define RD_RPB %d", rw));
+        S(fmt("#define RD_NSL %d", A.radial_nsl));
+        S("#define RD_WSM 1");
+        S("#define RD_WSTR 32");
+        S(fmt("#define RD_P2 %d", P2));
+        S("#define RD_PACKED 1");
+        S(fmt("#define RD_MINB %d", minb));
+        S("__device__ unsigned int uvu_status_word;  // no bounded waits in this module: stays 0");
+        G.emit_fwd_radial(S, rg, NE, true, true);
+        return S.o.str();
+    }
+    A.radial_gblk = 1;
+    const int NG = int(rg.size());
     const size_t wsm_bytes = packed ? wsm_packed : wsm_plain;
     A.radial_wsm = packed || wsm_bytes <= 200 * 1024;
     const size_t smem = A.radial_wsm ? wsm_bytes : 0;

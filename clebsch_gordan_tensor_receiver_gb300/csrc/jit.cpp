@@ -297,7 +297,7 @@ static uvu_status compile_aux_locked(Plan* plan, int kind, std::string* err) {
             // a spilling fused radial forward forms fewer edges' weights at a time, then gives
             // up a resident block
             if (attempt < 4 && spill_bytes(e.log, kAuxKernelNames[kind][0]) > 32) {
-                if (A.radial_ne > 1) A.radial_ne /= 2;
+                if (A.radial_ne > 1) A.radial_ne -= 1;
                 else if (A.minb_eff[0] > 1) A.minb[0] = A.minb_eff[0] - 1;
                 else attempt = 4;
                 again = attempt < 4;

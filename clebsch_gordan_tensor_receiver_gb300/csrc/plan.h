@@ -63,6 +63,7 @@ struct AuxBuild {  // host side, per plan
     bool radial_wsm = false;   // last-layer slice staged in shared memory
     int radial_nsl = 1;        // channel slices of 32
     int radial_rpb = 1;        // receivers per block per round
+    int radial_gblk = 1;       // blocks per channel slice and receiver set (path runs, split form)
 };
 
 // Radial network of the fused-weight forward (radial.cu): widths[0] = n_basis, then the hidden
