@@ -1867,6 +1867,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     // 32 channels, whose last-layer weights [H][P][32] sit in shared memory when they fit (else
     // they are read through the read-only cache).  Forming NE edges' weights together reuses each
     // last-layer weight NE times from a register.
+    mutable int radial_h_ = 0;  // hidden width of the radial module being emitted
+    int H_bytes_lines() const { return int((size_t(radial_h_) * P->elem() + 127) / 128); }
     // packed: fp32 weights formed two paths at a time with the paired FMA (fma.rn.f32x2), the
     // last layer staged as (even, odd) path pairs per lane; each half rounds as a scalar FMA.
     // split: the block holds only this group's path pairs [q0, q0 + gp) of the last layer
@@ -1889,13 +1891,22 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("const int ne = min(RD_NE, e1 - eb);");
         // the batch's sender ids, and its x and Y rows asked into L1 before the weights are
         // formed (UVU_RAD_PREFETCH=0, a tuning switch, leaves them to the loads after)
-        const bool pf = !(std::getenv("UVU_RAD_PREFETCH") && std::atoi(std::getenv("UVU_RAD_PREFETCH")) == 0);
+        // (UVU_RAD_PREFETCH=2 also asks for the next batch's h rows)
+        const int pfm = std::getenv("UVU_RAD_PREFETCH") ? std::atoi(std::getenv("UVU_RAD_PREFETCH")) : 1;
+        const bool pf = pfm != 0;
         for (int j = 0; j < NE; ++j) S(fmt("const int s%d = __ldg(src + eb + min(%d, ne - 1));", j, j));
         if (pf)
             for (int j = 0; j < NE; ++j) {
                 S(fmt("prefetch_l1(x + ((size_t)s%d * UVU_U + u) * UVU_DX);", j));
                 S(fmt("prefetch_l1(Y + (size_t)(eb + min(%d, ne - 1)) * UVU_DY);", j));
             }
+        if (pfm == 2) {
+            S("if (eb + RD_NE < e1) {");
+            for (int j = 0; j < NE; ++j)
+                for (int b = 0; b < H_bytes_lines(); ++b)
+                    S(fmt("  prefetch_l1(reinterpret_cast<const char*>(h + (size_t)min(eb + RD_NE + %d, e1 - 1) * RD_H) + %d);", j, b * 128));
+            S("}");
+        }
         for (int j = 0; j < NE; ++j) {
             S(fmt("const %s* __restrict__ hr%d = h + (size_t)(eb + min(%d, ne - 1)) * RD_H;", T.c_str(), j, j));
             if (packed)
@@ -2328,6 +2339,7 @@ std::string emit_radial_source(Plan* plan) {
         S("#define RD_PACKED 1");
         S(fmt("#define RD_MINB %d", minb));
         S("__device__ unsigned int uvu_status_word;  // no bounded waits in this module: stays 0");
+        G.radial_h_ = H;
         G.emit_fwd_radial(S, rg, NE, true, true);
         return S.o.str();
     }
@@ -2368,6 +2380,7 @@ std::string emit_radial_source(Plan* plan) {
     S(fmt("#define RD_PACKED %d", packed ? 1 : 0));
     S(fmt("#define RD_MINB %d", minb));
     S("__device__ unsigned int uvu_status_word;  // no bounded waits in this module: stays 0");
+    G.radial_h_ = H;
     G.emit_fwd_radial(S, rg, NE, packed);
     return S.o.str();
 }
