@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-hvp", action="store_true", help="skip the double-backward measurement")
     ap.add_argument("--no-tp", action="store_true", help="skip the batched tensor-product measurement")
     ap.add_argument("--no-radial", action="store_true", help="skip the fused-radial-weight measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the fwd and fwd+VJP measurement of the other four workloads")
     ap.add_argument("--tp-batch", type=int, default=100000, help="samples of the batched tensor product")
     ap.add_argument("--no-clocks", action="store_true", help="do not sample nvidia-smi clocks")
     ap.add_argument("--single-mode", action="store_true",
@@ -541,6 +543,57 @@ def main(argv=None):
                     "the materialised GEMMs are cuBLAS (library), shown for comparison only"}
         assert plan.device_status() == 0
         del rr, Wn, Wlast, hbuf, rout, wmat
+
+    # fwd and fwd+VJP (staged dx) of the other four workloads, each on its own plan and graph:
+    # edges/s, GB/s of the compulsory bytes and the fraction of the HBM peak; for the fp64
+    # workload also the FP64 arithmetic rate against the nominal FP64 peak.  w and d_out are
+    # drawn on the device (seeded); inputs of workloads 2-4 exceed L2, workload 0 fits in it.
+    if not args.no_configs and world == 1 and not args.single_mode and args.nodes is None:
+        cfg_line = {}
+        for key in [k for k in sorted(workloads.SPECS) if k != args.config]:
+            sp = workloads.SPECS[key]
+            wk = workloads.make_workload(key)
+            pk = uvu.Plan(sp.irreps_x, sp.irreps_sh, sp.lmax_out, sp.dtype)
+            ik = pk.info
+            Nk, Ek, Uk, Pk = wk.n_nodes, wk.n_edges, ik.mul, ik.n_paths
+            dtk = torch.float64 if sp.dtype == "float64" else torch.float32
+            sk = 8 if sp.dtype == "float64" else 4
+            cgen = torch.Generator(device=dev).manual_seed(600 + key)
+            xk, Yk = to_dev(wk.x), to_dev(wk.Y)
+            srck = to_dev(wk.src)
+            Gk = uvu.Graph(Nk, to_dev(wk.recv), srck)
+            wkd = torch.randn((Ek, Pk, Uk), generator=cgen, device=dev, dtype=dtk) / sp.w_scale_degree ** 0.5
+            gk = torch.randn((Nk, Uk, ik.dim_out), generator=cgen, device=dev, dtype=dtk)
+            ok_, dxk = torch.empty((Nk, Uk, ik.dim_out), device=dev, dtype=dtk), torch.empty((Nk, Uk, ik.dim_x), device=dev, dtype=dtk)
+            dYk, dwk = torch.empty((Ek, ik.dim_sh), device=dev, dtype=dtk), torch.empty_like(wkd)
+            wsk = torch.empty(max(16, pk.workspace_bytes(Nk, Ek, uvu.UVU_DX_STAGED)), dtype=torch.uint8, device=dev)
+            f_ms = ev_mix(lambda: pk.fwd(Nk, xk, Yk, wkd, Gk.recv_offsets, srck, ok_, stream), 10)
+
+            def vjp_k():
+                pk.bwd_edge(Nk, xk, Yk, wkd, Gk.recv_offsets, srck, gk, dY=dYk, dw=dwk, dx_edge=wsk, stream=stream)
+                pk.bwd_dx_reduce(Nk, Ek, Gk.send_offsets, Gk.send_eids, wsk, dxk, stream)
+            v_ms = ev_mix(vjp_k, 10)
+            assert pk.device_status() == 0
+            Bk = algorithmic_bytes(Nk, Ek, Uk, Pk, ik.dim_x, ik.dim_sh, ik.dim_out, sk)
+            ent = {"workload": describe(sp, ik, Ek, Nk), "n_edges": Ek,
+                   "fwd_ms": f_ms, "fwd_edges_per_s": Ek / (f_ms / 1000), "fwd_GB_s": frac(Bk["fwd"], f_ms)[0],
+                   "fwd_hbm_frac": frac(Bk["fwd"], f_ms)[1], "vjp_ms": v_ms, "vjp_edges_per_s": Ek / (v_ms / 1000),
+                   "vjp_GB_s": frac(Bk["vjp"], v_ms)[0], "vjp_hbm_frac": frac(Bk["vjp"], v_ms)[1],
+                   "fwd_vjp_edges_per_s": Ek / ((f_ms + v_ms) / 1000), "fwd_bytes": Bk["fwd"], "vjp_bytes": Bk["vjp"],
+                   "l2_resident": Bk["fwd"] < 129e6}
+            if sp.dtype == "float64":
+                # forward arithmetic from the plan's own CG: 2 flop per non-zero and per output component
+                nnz = 0
+                for pth in range(Pk):
+                    nnz += int((pk.cg(pth) != 0).sum())
+                ffl = 2.0 * Ek * Uk * (nnz + ik.dim_out)
+                ent["fwd_fp64_tflops"] = ffl / (f_ms / 1000) / 1e12
+                ent["fwd_fp64_frac_of_nominal"] = ent["fwd_fp64_tflops"] / 1.25
+                ent["fp64_note"] = "nominal GB300 FP64 peak 1.25 TFLOP/s"
+            cfg_line[sp.name] = ent
+            del xk, Yk, srck, Gk, wkd, gk, ok_, dxk, dYk, dwk, wsk, pk
+            torch.cuda.empty_cache()
+        line["configs"] = cfg_line
 
     # batched (non-convolution) tensor product on the same irreps: B samples, per-sample and
     # batch-shared weights, forward and VJP (dx, dy, dw); inputs drawn on the device (seeded)
