@@ -118,9 +118,13 @@ extern "C" uvu_status uvu_plan_create(const char* irreps_x, const char* irreps_s
             s = compile_plan(&p, &err);
             if (s != UVU_OK) return fail(s, err);
             const char* names[3] = {"uvu_fwd", "uvu_bwd_edge", "uvu_bwd_dx"};
+            // UVU_PIPE_SPILL_OK=n (a tuning switch): spill bytes accepted before a kernel gives up
+            // a resident block (default 32, about one call-site save)
+            size_t spill_ok = 32;
+            if (const char* e2 = std::getenv("UVU_PIPE_SPILL_OK")) spill_ok = size_t(std::max(0, std::atoi(e2)));
             bool again = false;
             for (int k = 0; k < 3; ++k)
-                if (p.minb_eff[k] > 1 && spill_bytes(p.log, names[k]) > 32) {
+                if (p.minb_eff[k] > 1 && spill_bytes(p.log, names[k]) > spill_ok) {
                     p.minb[k] = p.minb_eff[k] - 1;
                     again = true;
                 }
