@@ -1941,7 +1941,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         if (packed) {
             const int q0 = split ? *pairs.begin() : 0;
             const int gp = split ? int(pairs.size()) : (P->P + 1) / 2;
-            S(fmt("const unsigned long long* __restrict__ wk = reinterpret_cast<const unsigned long long*>(wlb) + (size_t)k * (%d * 32);", gp));
+            S(fmt("const unsigned long long* __restrict__ wk = reinterpret_cast<const unsigned long long*>(wlb) + (size_t)k * (%s * 32);",
+                  split ? fmt("%d", gp).c_str() : "RD_P2"));
             for (int kk = 0; kk < 4; ++kk) {
                 for (int j = 0; j < NE; ++j) S(fmt("const unsigned long long hp%d_%d = f2pack(hq%d.%s, hq%d.%s);", j, kk, j, comp[kk], j, comp[kk]));
                 for (int q : pairs) {
