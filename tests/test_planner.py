@@ -132,3 +132,35 @@ def test_unwritable_cache_dir_is_harmless(tmp_path):
     blocker.write_text("x")
     r = _run_child(_CHILD, {"UVU_CACHE_DIR": str(blocker / "sub")})
     assert r.returncode == 0 and r.stdout.startswith("OK"), r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("env", [
+    {"UVU_RAD_SPLIT": "2", "UVU_RAD_RW": "8", "UVU_RAD_MINB": "2"},
+    {"UVU_RAD_PACK": "0"},
+    {"UVU_RAD_PREFETCH": "2"},
+    {"UVU_PACK_PRODUCTS": "1"},
+], ids=["radial-split", "radial-unpaired", "radial-prefetch-h", "paired-products"])
+def test_tuning_variants_build_on_the_host(env, monkeypatch):
+    """The opt-in emission variants (measured, off by default) still generate code that compiles
+    for sm_103a without spills on MACE-medium, and differ from the default source."""
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    p = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3)
+    for monkey_k in env:
+        monkeypatch.delenv(monkey_k)
+    base = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3)
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    if "UVU_PACK_PRODUCTS" in env:
+        src, log = p.source()
+        assert "mul.rn.f32x2" in src and src != base.source()[0]
+        names = ("uvu_fwd", "uvu_bwd_edge")
+    else:
+        src, log = p.radial_source(64)
+        for k in env:
+            monkeypatch.delenv(k)
+        assert src != base.radial_source(64)[0]
+        names = ("uvu_fwd_radial",)
+    for k in names:
+        m = re.search(rf"Function properties for {k}\n.*?(\d+) bytes spill stores", log, re.S)
+        assert m and int(m.group(1)) == 0, (k, log)
