@@ -40,3 +40,22 @@ def test_unit_vector_sh_normalisation():
     Y = workloads.sh_inputs(v, 3)
     for l in range(4):
         np.testing.assert_allclose((Y[:, l * l:(l + 1) ** 2] ** 2).sum(1), 2 * l + 1, atol=1e-12)
+
+
+def test_radial_inputs_recipe():
+    """Edge lengths of the fused-radial-weight inputs: density proportional to r^2 on
+    [0.75, 5) (a Kolmogorov-Smirnov test against that law's CDF), seeded and reproducible;
+    layer shapes [H_(i-1)][H_i] with variance 1/H_(i-1); the last layer [H][P][U]."""
+    import scipy.stats
+    from clebsch_gordan_tensor_receiver_gb300 import workloads
+    spec = workloads.SPECS[1]
+    r, layers, wl = workloads.radial_inputs(spec, 20000, 13)
+    r2, layers2, wl2 = workloads.radial_inputs(spec, 20000, 13)
+    assert np.array_equal(r, r2) and np.array_equal(wl, wl2) and all(np.array_equal(a, b) for a, b in zip(layers, layers2))
+    assert r.dtype == np.float32 and r.min() >= 0.75 and r.max() < 5.0
+    a3, c3 = 0.75 ** 3, 5.0 ** 3
+    cdf = lambda t: np.clip((np.asarray(t, dtype=np.float64) ** 3 - a3) / (c3 - a3), 0.0, 1.0)
+    assert scipy.stats.kstest(r.astype(np.float64), cdf).pvalue > 1e-3
+    assert [W.shape for W in layers] == [(8, 64), (64, 64), (64, 64)] and wl.shape == (64, 13, 128)
+    assert abs(layers[1].astype(np.float64).var() * 64 - 1.0) < 0.1
+    assert abs(wl.astype(np.float64).var() * 64 * 56 - 1.0) < 0.05
