@@ -186,3 +186,34 @@ def test_fused_radial_host_checks_and_module():
             q.radial_hidden(r, rc, pe, widths, Wt, h, stream=st)
         assert ei.value.status == 1, widths
     q.radial_hidden(r, 5.0, 5, [8, 8], Wt, h, stream=st)  # no edges: nothing to do
+
+
+def test_fused_radial_forward_argument_errors():
+    """uvu_conv_fwd_radial refuses bad arguments on the host, before any device work: a hidden
+    width that is not a multiple of 4, NULL or misaligned tensors, negative sizes."""
+    import ctypes
+    import types
+    import torch
+    from clebsch_gordan_tensor_receiver_gb300 import uvu
+    p = uvu.Plan("32x0e+32x1o", "1x0e+1x1o+1x2e+1x3o", 3)
+    i = p.info
+    st = types.SimpleNamespace(cuda_stream=0)
+    x = torch.zeros(4, 32, i.dim_x)
+    Y = torch.zeros(6, i.dim_sh)
+    h = torch.zeros(6, 8)
+    wl = torch.zeros(8, i.n_paths, 32)
+    off = torch.zeros(5, dtype=torch.int32)
+    src = torch.zeros(6, dtype=torch.int32)
+    out = torch.zeros(4, 32, i.dim_out)
+    vp = lambda t, k=0: ctypes.c_void_p(t.data_ptr() + k)
+
+    def call(n_nodes=4, n_edges=6, xx=None, hidden=8, oo=None, ww=None):
+        pick = lambda a, b: b if a is None else a
+        uvu.uvu_conv_fwd_radial(p.handle, n_nodes, n_edges, pick(xx, vp(x)), vp(Y), vp(h), hidden, pick(ww, vp(wl)),
+                                vp(off), vp(src), pick(oo, vp(out)), ctypes.c_void_p(st.cuda_stream))
+    for kw, status in ((dict(hidden=6), 1), (dict(n_nodes=-1), 1), (dict(oo=ctypes.c_void_p(0)), 1),
+                       (dict(xx=vp(x, 4)), 1), (dict(ww=vp(wl, 8)), 1)):
+        with pytest.raises(uvu.UVUError) as ei:
+            call(**kw)
+        assert ei.value.status == status, kw
+    call(n_nodes=0, n_edges=0)  # nothing to do: no device work
