@@ -154,7 +154,7 @@ struct Gen {
     // UVU_PACK_PRODUCTS=1 (a tuning switch): fp32 products of an x value with two y values at
     // even/odd index pairs use one paired multiply (mul.rn.f32x2, each half rounded as a scalar
     // multiply, so the results are the same bits).  Measured on MACE-medium: forward 0.356 ->
-    // 0.340-0.346 ms, edge kernel within its spread, MACE-large unchanged.
+    // 0.340-0.348 ms, edge kernel within its spread, MACE-large unchanged.
     bool pack_products() const {
         return !f64 && std::getenv("UVU_PACK_PRODUCTS") && std::atoi(std::getenv("UVU_PACK_PRODUCTS")) == 1;
     }
