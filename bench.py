@@ -65,7 +65,10 @@ def parse_args(argv=None):
 # ------------------------------------------------------------------------- bytes and units
 
 def algorithmic_bytes(N, E, U, P, Dx, Dy, Do, s):
-    """Compulsory bytes per launch of each kernel (every tensor read or written once)."""
+    """Compulsory bytes per launch of each kernel: its share of the operation's inputs read once
+    and outputs written once (x, Y, w, out or d_out, the indices; dx, dY, dw).  Intermediates a
+    design chooses to keep in memory (the staged per-edge dx partials, an atomic dx
+    read-modify-write) are not algorithmic bytes: ``overhead_bytes`` lists them."""
     idx_r = 4 * (N + 1) + 4 * E          # recv_offsets + src
     idx_s = 4 * (N + 1) + 8 * E          # send_offsets + send_eids + send_recv
     x, Y, w, out = N * U * Dx * s, E * Dy * s, E * P * U * s, N * U * Do * s
@@ -74,16 +77,66 @@ def algorithmic_bytes(N, E, U, P, Dx, Dy, Do, s):
         "uvu_bwd_edge": x + Y + w + out + idx_r + Y + w,        # reads x,Y,w,d_out; writes dY,dw
         "uvu_bwd_edge+atomic_dx": x + Y + w + out + idx_r + Y + w + x,
         "uvu_bwd_dx": Y + w + out + idx_s + x,                  # reads Y,w,d_out; writes dx
-        "uvu_bwd_edge+dx_edge": x + Y + w + out + idx_r + Y + w + E * U * Dx * s,
-        "uvu_bwd_dx_reduce": E * U * Dx * s + 4 * (N + 1) + 4 * E + x,  # reads partials; writes dx
+        "uvu_bwd_dx_reduce": 4 * (N + 1) + 4 * E + x,           # reads the send CSR; writes dx
         "fwd": x + Y + w + out + idx_r,
         "vjp": (x + Y + w + out + idx_r + idx_s) + (x + Y + w),
     }
 
 
+def overhead_bytes(N, E, U, Dx, s):
+    """Bytes a kernel moves beyond its compulsory share, by dx mode: the staged mode writes and
+    reads back one dx partial row per (edge, channel)."""
+    part = E * U * Dx * s
+    return {"staged": {"uvu_bwd_edge": part, "uvu_bwd_dx_reduce": part},
+            "atomic": {}, "sender": {}}
+
+
 def describe(spec, info, E, N=None):
     return (f"{spec.name}: {N or spec.n_nodes} nodes, {E} edges, x {spec.irreps_x}, "
             f"SH {spec.irreps_sh}, l3<={spec.lmax_out} ({info.n_paths} paths), {spec.dtype}")
+
+
+def fp64_ops_per_edge_channel(plan):
+    """FP64 instructions the plan's generated forward executed per (edge, channel), from an ncu
+    count committed under profiles/ for this exact generated source (None when the source has
+    changed since the count was taken)."""
+    path = os.path.join(ROOT, "profiles", "fp64_ops.json")
+    if not os.path.exists(path):
+        return None
+    import hashlib
+    tab = json.load(open(path))
+    h = hashlib.sha256(plan.source()[0].encode()).hexdigest()[:16]
+    ent = tab.get("uvu_fwd")
+    if not ent or ent.get("source_sha") != h:
+        return None
+    return ent
+
+
+def measure_alu_peaks(uvu, torch, dev, stream):
+    """FP32 and FP64 FMA rates of this GPU, measured now with the library's FMA-chain probe
+    (8 independent chains per thread, 8 blocks of 256 threads per SM): the best of five launches,
+    timed with CUDA events on the launching stream.  TFLOP/s at 2 flop per FMA."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks = sms * 8
+    res = {}
+    for name, f64, iters in (("fp32", False, 1024), ("fp64", True, 64)):
+        buf = torch.empty(blocks * 256, dtype=torch.float64 if f64 else torch.float32, device=dev)
+        uvu.fma_rate_probe(buf, f64, blocks, iters, stream)
+        best = None
+        fmas = 0.0
+        for _ in range(5):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fmas = uvu.fma_rate_probe(buf, f64, blocks, iters, stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        res[name + "_tflops"] = 2.0 * fmas / (best / 1000.0) / 1e12
+        res[name + "_probe_ms"] = best
+    res["method"] = ("library FMA-chain probe (uvu_fma_rate_probe): %d blocks x 256 threads x 8 chains, "
+                     "best of 5 launches, CUDA events; 2 flop per FMA" % blocks)
+    return res
 
 
 # ------------------------------------------------------------------------- clocks sampling
@@ -169,62 +222,179 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------------- CPU oracle leg
 
-def oracle_sample(wl, w, g, lay, n_recv, seed):
-    """Time the oracle's fwd + VJP on a sample of receivers (fwd, dw, dY over their edges) and
-    senders (dx).  Returns (edges/s, description, threads)."""
-    import numpy as np
-    from oracle import conv, graph
-    rng = np.random.default_rng(seed)
-    N = wl.n_nodes
-    off = graph.recv_offsets(wl.recv, N)
-    rs = np.sort(rng.choice(N, size=min(n_recv, N), replace=False))
-    ss = np.sort(rng.choice(N, size=min(n_recv, N), replace=False))
-    edges = np.concatenate([np.arange(off[r], off[r + 1]) for r in rs])
-    n_send_edges = int(np.isin(wl.src, ss).sum())
-    t0 = time.perf_counter()
-    conv.fwd(lay, off, wl.src, wl.x, wl.Y, w, receivers=rs)
-    t1 = time.perf_counter()
-    conv.bwd_edges(lay, off, wl.src, wl.x, wl.Y, w, g, edges=edges)
-    t2 = time.perf_counter()
-    conv.bwd_dx(lay, off, wl.src, wl.Y, w, g, N, senders=ss)
-    t3 = time.perf_counter()
-    per_edge = (t1 - t0) / edges.size + (t2 - t1) / edges.size + (t3 - t2) / max(n_send_edges, 1)
-    desc = (f"oracle fwd+VJP: fwd and dw/dY over {rs.size} receivers ({edges.size} edges), dx over "
-            f"{ss.size} senders ({n_send_edges} edges); {t3 - t0:.1f} s wall")
-    return 1.0 / per_edge, desc, conv.default_threads()
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+class OracleSampler:
+    """Times the fp64 CPU oracle (oracle.conv, as it stands) on bounded samples of one workload.
+
+    fwd: the oracle's receiver-stationary loops over the edges of a random set of receivers;
+    VJP: dY and dw over the same receivers' edges, plus dx over a random set of senders, which
+    covers each of their out-edges.  A sample is a compact sub-problem: the sampled receivers
+    with their incoming edges (global sender ids, the full x), or the sampled senders with their
+    out-edges and the d_out rows those edges reach, so every edge is computed exactly as in the
+    full problem.  w and d_out values of the sampled rows are drawn here (the oracle's time does
+    not depend on them).  Each measurement repeats samples until at least `min_s` seconds of wall
+    time have passed and reports edges per second over that time."""
+
+    def __init__(self, key, wl=None, seed=0):
+        import numpy as np
+        from clebsch_gordan_tensor_receiver_gb300 import workloads
+        from oracle import graph, paths
+        self.np = np
+        self.spec = workloads.SPECS[key]
+        self.wl = wl if wl is not None else workloads.make_workload(key)
+        self.lay = paths.layout(self.spec.irreps_x, self.spec.irreps_sh, self.spec.lmax_out)
+        self.N, self.E = self.wl.n_nodes, self.wl.n_edges
+        self.off = graph.recv_offsets(self.wl.recv, self.N).astype(np.int64)
+        self.dt = np.float64 if self.spec.dtype == "float64" else np.float32
+        self.rng = np.random.default_rng(seed)
+        self.P, self.U = len(self.lay.paths), self.lay.mul
+        self.nr = max(1, min(self.N, 8))
+        self.ns = max(1, min(self.N, 8))
+
+    def _normal(self, shape, scale=1.0):
+        return (self.rng.standard_normal(shape) * scale).astype(self.dt)
+
+    def _recv_sample(self, n):
+        np = self.np
+        rs = np.sort(self.rng.choice(self.N, size=min(n, self.N), replace=False))
+        segs = [np.arange(self.off[r], self.off[r + 1]) for r in rs]
+        eidx = np.concatenate(segs) if segs else np.zeros(0, np.int64)
+        loff = np.zeros(rs.size + 1, np.int64)
+        np.cumsum([a.size for a in segs], out=loff[1:])
+        w = self._normal((eidx.size, self.P, self.U), 1.0 / self.spec.w_scale_degree ** 0.5)
+        g = self._normal((rs.size, self.U, self.lay.dim_out))
+        return loff, self.wl.src[eidx], self.wl.Y[eidx], w, g, eidx.size
+
+    def _send_sample(self, n):
+        np = self.np
+        from oracle import graph
+        ss = np.sort(self.rng.choice(self.N, size=min(n, self.N), replace=False))
+        eidx = np.nonzero(np.isin(self.wl.src, ss))[0]
+        recv = graph.recv_of_edges(self.off)[eidx]
+        # compact node ids: the sampled senders and the receivers their edges reach
+        nodes, inv = np.unique(np.concatenate([ss, recv, self.wl.src[eidx]]), return_inverse=True)
+        crecv = inv[ss.size:ss.size + eidx.size]
+        csrc = inv[ss.size + eidx.size:]
+        csend = inv[:ss.size]
+        coff = graph.recv_offsets(crecv, nodes.size)  # edges stay receiver-sorted
+        w = self._normal((eidx.size, self.P, self.U), 1.0 / self.spec.w_scale_degree ** 0.5)
+        g = self._normal((nodes.size, self.U, self.lay.dim_out))
+        return coff, csrc, self.wl.Y[eidx], w, g, nodes.size, csend, eidx.size
+
+    def _rate(self, kind, min_s, threads):
+        """edges/s of one measurement of `kind` ("fwd" or "vjp") lasting >= min_s seconds."""
+        from oracle import conv
+        done_e, spent = 0.0, 0.0
+        per_edge_vjp = []
+        while spent < min_s:
+            loff, src, Y, w, g, ne = self._recv_sample(self.nr)
+            if kind == "fwd":
+                t0 = time.perf_counter()
+                conv.fwd(self.lay, loff, src, self.wl.x, Y, w, nthreads=threads)
+                dt = time.perf_counter() - t0
+                done_e += ne
+                spent += dt
+                if dt < 0.5 and self.nr < self.N:  # grow the sample towards ~0.5 s per call
+                    self.nr = min(self.N, max(self.nr + 1, int(self.nr * 0.6 / max(dt, 1e-3))))
+                continue
+            t0 = time.perf_counter()
+            conv.bwd_edges(self.lay, loff, src, self.wl.x, Y, w, g, nthreads=threads)
+            t1 = time.perf_counter()
+            coff, csrc, Ys, ws, gs, nn, csend, nse = self._send_sample(self.ns)
+            t2 = time.perf_counter()
+            conv.bwd_dx(self.lay, coff, csrc, Ys, ws, gs, nn, senders=csend, nthreads=threads)
+            t3 = time.perf_counter()
+            spent += (t1 - t0) + (t3 - t2)
+            per_edge_vjp.append(((t1 - t0) / max(ne, 1) + (t3 - t2) / max(nse, 1), (t1 - t0) + (t3 - t2)))
+            if t1 - t0 < 0.3 and self.nr < self.N:
+                self.nr = min(self.N, max(self.nr + 1, int(self.nr * 0.4 / max(t1 - t0, 1e-3))))
+            if t3 - t2 < 0.3 and self.ns < self.N:
+                self.ns = min(self.N, max(self.ns + 1, int(self.ns * 0.4 / max(t3 - t2, 1e-3))))
+        if kind == "fwd":
+            return done_e / spent
+        # time-weighted mean of the per-edge VJP cost over the samples of this measurement
+        tot = sum(t for _, t in per_edge_vjp)
+        return 1.0 / (sum(c * t for c, t in per_edge_vjp) / tot)
+
+    def measure(self, threads, min_s=2.0, reps=3):
+        """Median of `reps` measurements: fwd edges/s, VJP edges/s and fwd+VJP edges/s."""
+        import statistics as st
+        self._rate("fwd", 0.3, threads)   # calibrate the sample sizes (untimed)
+        self._rate("vjp", 0.3, threads)
+        f = [self._rate("fwd", min_s, threads) for _ in range(reps)]
+        v = [self._rate("vjp", min_s, threads) for _ in range(reps)]
+        fm, vm = st.median(f), st.median(v)
+        return {"fwd_edges_per_s": fm, "vjp_edges_per_s": vm, "fwd_vjp_edges_per_s": 1.0 / (1.0 / fm + 1.0 / vm),
+                "fwd_runs": f, "vjp_runs": v, "threads": threads,
+                "sample": f"fwd: {self.nr} random receivers with their in-edges per call; VJP: dY, dw over "
+                          f"{self.nr} receivers' in-edges and dx over {self.ns} random senders' out-edges per call; "
+                          f"each run repeats calls for >= {min_s:.1f} s wall; median of {reps} runs"}
+
+
+def cpu_baseline_protocol(keys_wl, threads):
+    """The oracle on the host cores for every workload (fwd, VJP and fwd+VJP edges/s, median of
+    three runs of >= 2 s), plus single-threaded runs of the tiny and MACE-medium workloads."""
+    per = {}
+    for key, wl in keys_wl:
+        smp = OracleSampler(key, wl, seed=31 + key)
+        ent = {"workload": smp.spec.name, "all_cores": smp.measure(threads)}
+        if key in (0, 1):
+            ent["single_thread"] = OracleSampler(key, wl, seed=41 + key).measure(1)
+        per[smp.spec.name] = ent
+    return per
 
 
 def run_reference(args):
     rank, local_rank, world = dist_env()
     if world > 1 and rank != 0:
         return 0
-    from clebsch_gordan_tensor_receiver_gb300 import workloads
-    from oracle import paths
-    spec = workloads.SPECS[args.config]
-    wl = workloads.make_workload(spec)
-    lay = paths.layout(spec.irreps_x, spec.irreps_sh, spec.lmax_out)
-    w = workloads.make_weights(spec, wl.n_edges, len(lay.paths))
-    g = workloads.make_cotangent(spec, wl.n_nodes, lay.dim_out)
-    n_recv = 40
-    for i in range(args.warmup):
-        oracle_sample(wl, w, g, lay, n_recv, 500 + i)
-    rates, descs = [], []
+    from oracle import conv
+    smp = OracleSampler(args.config, seed=900)
+    thr = conv.default_threads()
+    smp._rate("fwd", 0.3, thr)
+    smp._rate("vjp", 0.3, thr)
+    for _ in range(args.warmup):
+        smp._rate("fwd", 0.5, thr)
+    rates, fw, vj = [], [], []
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        r, d, thr = oracle_sample(wl, w, g, lay, n_recv, 900 + i)
-        rates.append(r)
-        descs.append(d)
+    for _ in range(args.steps):
+        f = smp._rate("fwd", 1.0, thr)
+        v = smp._rate("vjp", 1.0, thr)
+        fw.append(f)
+        vj.append(v)
+        rates.append(1.0 / (1.0 / f + 1.0 / v))
     wall = time.perf_counter() - t0
     value = statistics.median(rates)
+    sample = ("each step: the oracle's fwd, then its VJP (dY, dw over sampled receivers' in-edges; dx over "
+              "sampled senders' out-edges), each repeated for >= 1 s wall on samples of %d receivers / %d senders; "
+              "value = median over steps of fwd+VJP edges/s" % (smp.nr, smp.ns))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "edges/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000 * wall / max(args.steps, 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": describe(spec, type("I", (), {"n_paths": len(lay.paths)}), wl.n_edges),
+        "config": {"workload": describe(smp.spec, type("I", (), {"n_paths": smp.P}), smp.E),
                    "parallelism": "replicas"},
+        "fwd_edges_per_s": statistics.median(fw), "vjp_edges_per_s": statistics.median(vj),
         "cpu_baseline": {"value": value, "unit": "edges/s", "cores": thr, "kind": "oracle",
-                         "sample": descs[0]},
+                         "cpu_model": cpu_model(), "sample": sample},
         "e2e": {"value": value, "unit": "edges/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -256,6 +426,7 @@ def main(argv=None):
     from clebsch_gordan_tensor_receiver_gb300 import uvu, workloads
     spec = workloads.SPECS[args.config]
     wl = workloads.make_workload(spec, args.nodes)
+    wl_cache = {args.config: wl} if args.nodes is None else {}
     plan = uvu.Plan(spec.irreps_x, spec.irreps_sh, spec.lmax_out, spec.dtype)
     info = plan.info
     N, E, U, P = wl.n_nodes, wl.n_edges, info.mul, info.n_paths
@@ -349,6 +520,8 @@ def main(argv=None):
     results = {m: timed(m, args.steps) for m in modes}
     clk = clocks.stop()
     assert plan.device_status() == 0, "a kernel reported a bounded-wait timeout"
+    alu = measure_alu_peaks(uvu, torch, dev, stream)
+    alu_peak = alu["fp32_tflops"]
 
     total_ms, kern_ms = results[args.dx_mode]
     total_ms = max_over_ranks(total_ms, world, dev)
@@ -368,8 +541,8 @@ def main(argv=None):
         gbs = bytes_ / (ms / 1000.0) / 1e9
         return gbs, gbs / hbm_peak
 
-    edge_key = {"atomic": "uvu_bwd_edge+atomic_dx", "staged": "uvu_bwd_edge+dx_edge",
-                "sender": "uvu_bwd_edge"}
+    edge_key = {"atomic": "uvu_bwd_edge+atomic_dx", "staged": "uvu_bwd_edge", "sender": "uvu_bwd_edge"}
+    OV = overhead_bytes(N, E, U, Dx, s)
 
     def mode_summary(mode):
         tot, km = results[mode]
@@ -377,14 +550,18 @@ def main(argv=None):
         gbs, fr = frac(B["vjp"], vjp)
         return {"vjp_ms": vjp, "vjp_edges_per_s": world * E / (vjp / 1000), "vjp_GB_s": gbs,
                 "vjp_hbm_frac": fr, "fwd_vjp_edges_per_s": world * E / (tot / args.steps / 1000),
-                "deterministic": mode != "atomic",
+                "deterministic": mode != "atomic", "overhead_bytes": sum(OV[mode].values()),
                 "kernels_ms": km}
 
+    # per kernel: compulsory bytes (its share of the operation's inputs and outputs) over its
+    # time against the HBM peak; the intermediates the design adds are listed beside them
     kernels = {}
     for k, ms in kern_ms.items():
         key = edge_key[args.dx_mode] if k == "uvu_bwd_edge" else k
         gbs, fr = frac(B[key], ms)
-        kernels[k] = {"ms": ms, "bytes": B[key], "GB_s": gbs, "frac": fr}
+        ov = OV[args.dx_mode].get(k, 0)
+        kernels[k] = {"ms": ms, "bytes": B[key], "GB_s": gbs, "frac": fr, "overhead_bytes": ov,
+                      "moved_GB_s": (B[key] + ov) / (ms / 1000.0) / 1e9}
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
@@ -415,9 +592,15 @@ def main(argv=None):
         "kernels": kernels,
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["GB_s"],
                      "peak": hbm_peak, "unit": "GB/s", "frac": kernels[dom]["frac"],
-                     "traffic": traffic, "peak_source": peak_src + " hbm_gbs (copy)"},
+                     "traffic": traffic, "algorithmic_bytes": kernels[dom]["bytes"],
+                     "overhead_bytes": kernels[dom]["overhead_bytes"],
+                     "traffic_over_algorithmic": (traffic / kernels[dom]["bytes"]) if traffic else None,
+                     "peak_source": peak_src + " hbm_gbs (copy)",
+                     "note": "achieved = compulsory bytes of the kernel (x, Y, w, d_out, indices read; dY, dw "
+                             "written) / its CUDA-event time; traffic = ncu DRAM read+write per launch"},
         "kernel_ms_spread": spread,
         "csr_build_ms": csr_ms,
+        "alu_peaks": alu,
         "clocks": clk,
         "gpu_launches": args.steps * (2 if args.dx_mode == "atomic" else 3),
     }
@@ -480,15 +663,12 @@ def main(argv=None):
         mi = ev_mix(lambda: plan.mix_bwd(N, Wm, out, Mm, mg, d_in=md_in, workspace=mws, stream=stream))
         mM = ev_mix(lambda: plan.mix_bwd(N, Wm, out, Mm, mg, dM=mdM, workspace=mws, stream=stream))
         flops = 2.0 * N * U * Wm * Do
-        # FP32 peak from the unit counts and clocks: 128 FMA lanes per SM x 2 flop x SMs x max SM clock
-        sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
-        alu_peak = 128 * 2 * sm_count * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
         line["mix"] = {"w_out": Wm, "flops_per_launch": flops,
                        "fwd_ms": mf, "bwd_d_in_ms": mi, "bwd_dM_ms": mM,
                        "fwd_tflops": flops / (mf / 1000) / 1e12, "bwd_d_in_tflops": flops / (mi / 1000) / 1e12,
                        "bwd_dM_tflops": flops / (mM / 1000) / 1e12,
                        "alu_peak_tflops": alu_peak, "fwd_alu_frac": flops / (mf / 1000) / 1e12 / alu_peak,
-                       "note": "bound alu: fp32 FMA peak = 128 lanes x 2 flop x SMs x max SM clock"}
+                       "note": "bound alu: fraction of the FP32 FMA rate measured in this run (alu_peaks)"}
         assert plan.device_status() == 0
         del Mm, mo, mg, md_in, mdM, mws
 
@@ -539,7 +719,7 @@ def main(argv=None):
                              "total_tf32_ms": hid_ms + gemm["tf32"] + conv_ms},
             "fused_total_ms": hid_ms + fus_ms,
             "rel_frobenius_vs_materialised_fp32": rel,
-            "note": "alu bound: last-layer FMAs (2 E U P H flop) over the fp32 peak from unit counts; "
+            "note": "alu bound: last-layer FMAs (2 E U P H flop) over the FP32 rate measured in this run; "
                     "the materialised GEMMs are cuBLAS (library), shown for comparison only"}
         assert plan.device_status() == 0
         del rr, Wn, Wlast, hbuf, rout, wmat
@@ -553,6 +733,7 @@ def main(argv=None):
         for key in [k for k in sorted(workloads.SPECS) if k != args.config]:
             sp = workloads.SPECS[key]
             wk = workloads.make_workload(key)
+            wl_cache[key] = wk
             pk = uvu.Plan(sp.irreps_x, sp.irreps_sh, sp.lmax_out, sp.dtype)
             ik = pk.info
             Nk, Ek, Uk, Pk = wk.n_nodes, wk.n_edges, ik.mul, ik.n_paths
@@ -582,14 +763,26 @@ def main(argv=None):
                    "fwd_vjp_edges_per_s": Ek / ((f_ms + v_ms) / 1000), "fwd_bytes": Bk["fwd"], "vjp_bytes": Bk["vjp"],
                    "l2_resident": Bk["fwd"] < 129e6}
             if sp.dtype == "float64":
-                # forward arithmetic from the plan's own CG: 2 flop per non-zero and per output component
+                # forward arithmetic from the plan's own CG: 2 flop per non-zero and per output
+                # component (the survey's estimate), and the FP64 operations the generated
+                # forward executes per (edge, channel) when an ncu count for this source exists
                 nnz = 0
                 for pth in range(Pk):
                     nnz += int((pk.cg(pth) != 0).sum())
                 ffl = 2.0 * Ek * Uk * (nnz + ik.dim_out)
-                ent["fwd_fp64_tflops"] = ffl / (f_ms / 1000) / 1e12
-                ent["fwd_fp64_frac_of_nominal"] = ent["fwd_fp64_tflops"] / 1.25
-                ent["fp64_note"] = "nominal GB300 FP64 peak 1.25 TFLOP/s"
+                ent["fwd_fp64_tflops_estimate"] = ffl / (f_ms / 1000) / 1e12
+                ent["fwd_fp64_frac_of_measured"] = ent["fwd_fp64_tflops_estimate"] / alu["fp64_tflops"]
+                ent["fp64_peak_tflops_measured"] = alu["fp64_tflops"]
+                ops = fp64_ops_per_edge_channel(pk)
+                if ops:
+                    ent["fwd_fp64_executed"] = {
+                        "dfma_per_edge_channel": ops["dfma"], "dmul_dadd_per_edge_channel": ops["dmul"] + ops["dadd"],
+                        "tflops": Ek * Uk * (2 * ops["dfma"] + ops["dmul"] + ops["dadd"]) / (f_ms / 1000) / 1e12,
+                        "pipe_frac_of_measured": Ek * Uk * (ops["dfma"] + ops["dmul"] + ops["dadd"]) /
+                                                 (f_ms / 1000) / (alu["fp64_tflops"] / 2 * 1e12),
+                        "source": ops["source"]}
+                ent["fp64_note"] = ("estimate = 2 E U (nnz + D_out) flop; fraction of the FP64 FMA rate measured "
+                                    "in this run (alu_peaks)")
             cfg_line[sp.name] = ent
             del xk, Yk, srck, Gk, wkd, gk, ok_, dxk, dYk, dwk, wsk, pk
             torch.cuda.empty_cache()
@@ -802,7 +995,10 @@ def main(argv=None):
             graph_err = f"{type(ex).__name__}: {ex}"[:200]
             torch.cuda.synchronize()
         del ref
-        use_graph = graph_ms is not None and graph_same is not False
+        # The faster of the two launch modes is the step time (both are reported): on some boxes
+        # the replayed graph's copy nodes ran the two copy directions one after the other
+        # (20.6 ms against 13.1 ms eager in one driver run), on others replay was the faster.
+        use_graph = graph_ms is not None and graph_same is not False and graph_ms <= eager_ms
         e_ms = max_over_ranks(graph_ms if use_graph else eager_ms, world, dev)
         # the results that came back are the full outputs of the step
         line["e2e"] = {"value": world * E / (e_ms / 1000), "unit": "edges/s",
@@ -846,11 +1042,17 @@ def main(argv=None):
         assert plan.device_status() == 0
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        from oracle import paths
-        lay = paths.layout(spec.irreps_x, spec.irreps_sh, spec.lmax_out)
-        rate, desc, thr = oracle_sample(wl, w_h, g_h, lay, 120, 7)
-        line["cpu_baseline"] = {"value": rate, "unit": "edges/s", "cores": thr, "kind": "oracle",
-                                "sample": desc}
+        # the fp64 CPU oracle on this host's cores, per workload (fwd, VJP, fwd+VJP; median of
+        # three runs of >= 2 s each), single-threaded too for the tiny and MACE-medium workloads
+        from oracle import conv
+        thr = conv.default_threads()
+        keys = [args.config] + [k for k in sorted(workloads.SPECS) if k != args.config]
+        per = cpu_baseline_protocol([(k, wl_cache.get(k)) for k in keys], thr)
+        main = per[spec.name]["all_cores"]
+        line["cpu_baseline"] = {"value": main["fwd_vjp_edges_per_s"], "unit": "edges/s", "cores": thr,
+                                "kind": "oracle", "cpu_model": cpu_model(),
+                                "sample": f"{spec.name}: " + main["sample"],
+                                "per_workload": per}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

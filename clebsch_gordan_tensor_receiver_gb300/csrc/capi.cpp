@@ -857,3 +857,15 @@ extern "C" uvu_status uvu_conv_fwd_radial(uvu_plan_t plan, int64_t n_nodes, int6
     if (e != cudaSuccess) return cuda_fail(e, "uvu_fwd_radial launch");
     return ok();
 }
+
+extern "C" uvu_status uvu_fma_rate_probe(uvu_dtype dtype, int blocks, int iters, void* out, double* fmas,
+                                         uvu_stream_t stream) {
+    UVU_RANGE("uvu_fma_rate_probe");
+    if (dtype != UVU_F32 && dtype != UVU_F64) return fail(UVU_ERR_INVALID_ARGUMENT, "unknown dtype");
+    if (blocks < 1 || blocks > (1 << 20) || iters < 1 || iters > (1 << 24))
+        return fail(UVU_ERR_INVALID_ARGUMENT, "blocks must be in [1, 2^20] and iters in [1, 2^24]");
+    UVU_TRY(need(out, "out"));
+    cudaError_t e = launch_fma_probe(dtype == UVU_F64, blocks, iters, out, static_cast<cudaStream_t>(stream), fmas);
+    if (e != cudaSuccess) return cuda_fail(e, "fma probe launch");
+    return ok();
+}

@@ -29,16 +29,18 @@ int grid_for(int64_t n) {
 }
 
 // offsets[r] = #{e : recv[e] < r}.  The thread owning edge e writes every offset in
-// (recv[e-1], recv[e]]; the last edge also writes (recv[E-1], N].
+// (recv[e-1], recv[e]]; the last edge also writes (recv[E-1], N].  Every write is clamped to
+// [0, N], so a receiver id outside [0, N) or a decreasing recv (a broken precondition) leaves an
+// invalid CSR, which uvu_graph_validate reports, and never a write outside recv_offsets.
 __global__ void csr_offsets_kernel(int64_t N, int64_t E, const int32_t* __restrict__ recv,
                                    int32_t* __restrict__ off) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < E; e += stride) {
-        const int64_t r = recv[e];
-        const int64_t prev = e == 0 ? -1 : recv[e - 1];
-        for (int64_t k = prev + 1; k <= r; ++k) off[k] = int32_t(e);
+        const int64_t r = recv[e] < N ? int64_t(recv[e]) : N;
+        const int64_t prev = e == 0 ? -1 : int64_t(recv[e - 1]);
+        for (int64_t k = (prev + 1 > 0 ? prev + 1 : 0); k <= r; ++k) off[k] = int32_t(e);
         if (e == E - 1)
-            for (int64_t k = r + 1; k <= N; ++k) off[k] = int32_t(E);
+            for (int64_t k = (r + 1 > 0 ? r + 1 : 0); k <= N; ++k) off[k] = int32_t(E);
     }
 }
 
@@ -102,22 +104,70 @@ __device__ __forceinline__ int32_t receiver_of(int64_t N, const int32_t* __restr
     return int32_t(lo);
 }
 
-// Place each unordered entry at its rank inside its sender segment (edge ids are distinct, so
-// the rank is unique): the result lists each sender's edges in ascending edge id.
-__global__ void rank_place_kernel(int64_t N, int64_t E, const int32_t* __restrict__ src,
-                                  const int32_t* __restrict__ soff, const int32_t* __restrict__ roff,
-                                  const int32_t* __restrict__ tmp, int32_t* __restrict__ eids,
-                                  int32_t* __restrict__ srecv) {
+// Sender segments up to this many edges are ordered by rank counting (each entry counts the
+// smaller ids of its segment: d^2 comparisons, cheap for the usual degrees); longer segments
+// (hub senders) are sorted in place by sort_segments_kernel instead, O(d log^2 d).
+constexpr int32_t kRankMax = 64;
+
+// Place each unordered entry of a short segment at its rank (edge ids are distinct, so the rank
+// is unique): the result lists each sender's edges in ascending edge id.  Entries of long
+// segments are copied unordered, to be sorted next.
+__global__ void rank_place_kernel(int64_t E, const int32_t* __restrict__ src, const int32_t* __restrict__ soff,
+                                  const int32_t* __restrict__ tmp, int32_t* __restrict__ eids) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < E; k += stride) {
         const int32_t e = tmp[k];
         const int32_t s = src[e];
         const int32_t b = soff[s], t = soff[s + 1];
+        if (t - b > kRankMax) {
+            eids[k] = e;
+            continue;
+        }
         int32_t rank = 0;
         for (int32_t j = b; j < t; ++j) rank += tmp[j] < e;
         eids[b + rank] = e;
-        srecv[b + rank] = receiver_of(N, roff, e);
     }
+}
+
+// Ascending sort of every segment longer than kRankMax, one block per segment (blocks stride
+// over the senders).  Bitonic network in the form whose comparators all put the smaller value
+// at the lower index (the first step of each merge compares i with its mirror in the block of
+// size k), so the segment behaves as if padded with +infinity up to the next power of two and
+// comparators that reach past its end do nothing.
+__global__ void sort_segments_kernel(int64_t N, const int32_t* __restrict__ soff, int32_t* __restrict__ eids) {
+    for (int64_t s = blockIdx.x; s < N; s += gridDim.x) {
+        const int32_t b = soff[s], d = soff[s + 1] - b;
+        if (d <= kRankMax) continue;
+        int32_t* a = eids + b;
+        int32_t n2 = 1;
+        while (n2 < d) n2 <<= 1;
+        for (int32_t k = 2; k <= n2; k <<= 1) {
+            for (int32_t j = k >> 1; j > 0; j >>= 1) {
+                __syncthreads();
+                // n2 / 2 comparators per step, each on one pair (lo < hi)
+                for (int32_t t = threadIdx.x; t < (n2 >> 1); t += blockDim.x) {
+                    const int32_t lo = (t / j) * (2 * j) + (t % j);
+                    const int32_t hi = (j == (k >> 1)) ? ((lo / k) * k + (k - 1 - (lo % k))) : lo + j;
+                    if (hi < d) {
+                        const int32_t x = a[lo], y = a[hi];
+                        if (y < x) {
+                            a[lo] = y;
+                            a[hi] = x;
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// send_recv[k] = receiver of send_eids[k], by binary search in the receiver CSR.
+__global__ void send_recv_kernel(int64_t N, int64_t E, const int32_t* __restrict__ roff,
+                                 const int32_t* __restrict__ eids, int32_t* __restrict__ srecv) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; k < E; k += stride)
+        srecv[k] = receiver_of(N, roff, eids[k]);
 }
 
 __global__ void validate_kernel(int64_t N, int64_t E, const int32_t* __restrict__ off,
@@ -163,7 +213,9 @@ cudaError_t launch_csr_transpose(int64_t N, int64_t E, const int32_t* roff, cons
     if (E > 0) {
         fill_kernel<<<grid_for(N + 1), kThreads, 0, st>>>(cnt, N + 1, 0);
         scatter_kernel<<<grid_for(E), kThreads, 0, st>>>(E, src, soff, cnt, tmp);
-        rank_place_kernel<<<grid_for(E), kThreads, 0, st>>>(N, E, src, soff, roff, tmp, eids, srecv);
+        rank_place_kernel<<<grid_for(E), kThreads, 0, st>>>(E, src, soff, tmp, eids);
+        sort_segments_kernel<<<152 * 4, 512, 0, st>>>(N, soff, eids);
+        send_recv_kernel<<<grid_for(E), kThreads, 0, st>>>(N, E, roff, eids, srecv);
     }
     return cudaGetLastError();
 }
@@ -196,23 +248,36 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char uvu_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mu;
-std::map<int, void*> g_noalloc_ptr;  // device ordinal -> device address of the array
+std::map<int, void*> g_noalloc_ptr;  // device ordinal -> address found by the last lookup there
 
-// The array's device address on the current device, looked up once per device.  In host code
-// `uvu_noalloc_scratch` names a host-side stand-in, so the address must come from the runtime.
-uvu_status noalloc_scratch(void** out) {
+// The array's device address on the current device.  In host code `uvu_noalloc_scratch` names a
+// host-side stand-in, so the address must come from the runtime (cudaGetSymbolAddress, with that
+// device current, its return code checked).  The lookup is repeated on every call made outside
+// stream capture, so a context torn down and recreated in between (cudaDeviceReset, a new primary
+// context) never leaves a stale address behind.  While `stream` is capturing, the lookup (which
+// may load the library's module) is not made: the address found by the last call on this device
+// is used, and a capture before any call on the device is refused.
+uvu_status noalloc_scratch(cudaStream_t stream, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
     std::lock_guard<std::mutex> g(g_noalloc_mu);
-    auto it = g_noalloc_ptr.find(dev);
-    if (it == g_noalloc_ptr.end()) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, uvu_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(uvu_noalloc_scratch)");
-        it = g_noalloc_ptr.emplace(dev, p).first;
+    if (cap != cudaStreamCaptureStatusNone) {
+        auto it = g_noalloc_ptr.find(dev);
+        if (it == g_noalloc_ptr.end())
+            return fail(UVU_ERR_INVALID_ARGUMENT,
+                        "uvu_csr_transpose_noalloc: the first call on a device must come before stream capture");
+        *out = it->second;
+        return UVU_OK;
     }
-    *out = it->second;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, uvu_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(uvu_noalloc_scratch)");
+    g_noalloc_ptr[dev] = p;
+    *out = p;
     return UVU_OK;
 }
 
@@ -235,7 +300,7 @@ extern "C" uvu_status uvu_csr_transpose_noalloc(int64_t n_nodes, int64_t n_edges
                         std::to_string(kNoAllocScratchBytes) + " bytes (4(N+1) + 4E rounded up); use uvu_csr_transpose "
                         "with a caller workspace");
     void* ws = nullptr;
-    uvu_status s = noalloc_scratch(&ws);
+    uvu_status s = noalloc_scratch(reinterpret_cast<cudaStream_t>(stream), &ws);
     if (s != UVU_OK) return s;
     cudaError_t e = launch_csr_transpose(n_nodes, n_edges, recv_offsets, src, send_offsets, send_eids, send_recv,
                                          ws, stream);

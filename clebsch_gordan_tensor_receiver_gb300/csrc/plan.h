@@ -147,6 +147,7 @@ const char* g_last_message_cstr();
 namespace uvu {
 // graph.cu
 size_t transpose_workspace_bytes(int64_t N, int64_t E);
+cudaError_t launch_fma_probe(bool f64, int blocks, int iters, void* out, cudaStream_t st, double* fmas);
 cudaError_t launch_csr_offsets(int64_t N, int64_t E, const int32_t* recv, int32_t* off, cudaStream_t st);
 cudaError_t launch_csr_transpose(int64_t N, int64_t E, const int32_t* roff, const int32_t* src,
                                  int32_t* soff, int32_t* eids, int32_t* srecv, void* ws, cudaStream_t st);

@@ -36,7 +36,7 @@ EXPORTS = (
     "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
     "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
     "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source",
-    "uvu_status_string", "uvu_last_error_message",
+    "uvu_fma_rate_probe", "uvu_status_string", "uvu_last_error_message",
 )
 
 
@@ -86,6 +86,7 @@ def _load():
         "uvu_radial_hidden": [P, I64, P, ctypes.c_double, I, I, ctypes.POINTER(I), P, P, P],
         "uvu_conv_fwd_radial": [P, I64, I64, P, P, P, I, P, P, P, P, P],
         "uvu_radial_module_source": [P, I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
+        "uvu_fma_rate_probe": [I, I, I, P, ctypes.POINTER(ctypes.c_double), P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -125,8 +126,16 @@ for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source"
            "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
            "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
            "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
-           "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source"):
+           "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source", "uvu_fma_rate_probe"):
     globals()[_n] = _wrap(_n)
+
+
+def fma_rate_probe(out, f64: bool, blocks: int, iters: int, stream=None) -> float:
+    """Enqueue one launch of the FMA-chain probe into `out` (a device tensor of at least
+    blocks * 256 elements of the dtype); returns the FMAs that launch performs."""
+    n = ctypes.c_double()
+    uvu_fma_rate_probe(UVU_F64 if f64 else UVU_F32, blocks, iters, _ptr(out), ctypes.byref(n), _stream(stream))
+    return n.value
 
 
 def uvu_plan_create(irreps_x: str, irreps_sh: str, lmax_out: int, dtype: int) -> int:

@@ -148,7 +148,9 @@ uvu_status uvu_plan_device_status(uvu_plan_t plan, unsigned *word, int reset);
  * the timed convolution).  recv_offsets[r] = #{e : recv[e] < r}.
  *   recv          device int32 [n_edges], non-decreasing, values in [0, n_nodes)
  *   recv_offsets  device int32 [n_nodes + 1], written
- * Bit-exact and deterministic. */
+ * Bit-exact and deterministic.  A recv that breaks its precondition (a value outside [0, N) or
+ * a decrease) gives an invalid CSR that uvu_graph_validate reports; no write leaves
+ * recv_offsets. */
 uvu_status uvu_csr_from_sorted_recv(int64_t n_nodes, int64_t n_edges, const int32_t *recv,
                                     int32_t *recv_offsets, uvu_stream_t stream);
 
@@ -158,7 +160,9 @@ uvu_status uvu_csr_transpose_workspace(int64_t n_nodes, int64_t n_edges, size_t 
 /* Transposed (sender) CSR: send_offsets [N+1]; send_eids [E] lists, per sender, the ids of
  * its edges in ascending edge-id order; send_recv[k] = receiver of edge send_eids[k].
  * Deterministic and bit-exact (the ordering is unique).  `workspace` is caller-owned device
- * memory of at least uvu_csr_transpose_workspace() bytes; its contents on entry do not matter. */
+ * memory of at least uvu_csr_transpose_workspace() bytes; its contents on entry do not matter.
+ * Senders with up to 64 edges are ordered by rank counting, longer segments (hub senders) by an
+ * in-place sort, O(d log^2 d) per segment of d edges. */
 uvu_status uvu_csr_transpose(int64_t n_nodes, int64_t n_edges, const int32_t *recv_offsets,
                              const int32_t *src, int32_t *send_offsets, int32_t *send_eids,
                              int32_t *send_recv, void *workspace, size_t workspace_bytes,
@@ -173,10 +177,14 @@ uvu_status uvu_csr_transpose(int64_t n_nodes, int64_t n_edges, const int32_t *re
  * GPU that loads it until the process exits.  Graphs needing more than that
  * (uvu_csr_transpose_workspace() > 16 MiB, i.e. roughly 4(N+1) + 4E > 16 MiB) are rejected with
  * UVU_ERR_UNSUPPORTED before anything is enqueued.  This function allocates nothing (no
- * cudaMalloc, no cudaFree, no allocating library call).  Its first call on a device looks up the
- * array's device address there (cudaGetSymbolAddress); make that first call before any stream
- * capture.  Every call re-initialises the scratch it reads, so the previous call's leftovers do
- * not matter, but all calls share one array: calls whose work overlaps on the GPU race. */
+ * cudaMalloc, no cudaFree, no allocating library call).  Each call made outside stream capture
+ * looks up the array's device address on the current device (cudaGetSymbolAddress; the first
+ * such call on a device also loads the array there), so a device reset in between leaves no
+ * stale address.  A call on a capturing stream reuses the address found by the last call on that
+ * device: make one call on each device before any stream capture (a capture before it returns
+ * UVU_ERR_INVALID_ARGUMENT).  Every call re-initialises the scratch it reads, so the previous
+ * call's leftovers do not matter, but all calls share one array: calls whose work overlaps on the
+ * GPU race. */
 uvu_status uvu_csr_transpose_noalloc(int64_t n_nodes, int64_t n_edges, const int32_t *recv_offsets,
                                      const int32_t *src, int32_t *send_offsets, int32_t *send_eids,
                                      int32_t *send_recv, uvu_stream_t stream);
@@ -421,6 +429,18 @@ uvu_status uvu_conv_fwd_radial(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges
  * if it is not yet (this fixes the plan's hidden width, as a first uvu_conv_fwd_radial does).
  * The strings stay valid for the plan's lifetime. */
 uvu_status uvu_radial_module_source(uvu_plan_t plan, int hidden, const char **source, const char **log);
+
+/* ------------------------------------------------------------------------ measurement ---- */
+
+/* Arithmetic-rate probe, the denominator of the FP32 / FP64 pipe fractions that the benchmark
+ * reports beside the HBM fractions (the pages give no peak for the hardware used here; the
+ * fraction of a pipe's peak is this library's own measurement): blocks x 256 threads, each
+ * running 8 independent FMA chains of `iters` steps (rounded up to a multiple of 4) in the
+ * dtype.  out: device memory of at least blocks * 256 elements of the dtype (16-byte aligned),
+ * overwritten with each thread's chain sum.  *fmas (host, may be NULL) receives the number of
+ * FMAs one launch performs (2 flop each).  Launches: 1 kernel. */
+uvu_status uvu_fma_rate_probe(uvu_dtype dtype, int blocks, int iters, void *out, double *fmas,
+                              uvu_stream_t stream);
 
 /* ---------------------------------------------------------------------------- errors ---- */
 

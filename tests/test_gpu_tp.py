@@ -1,7 +1,7 @@
 """GPU parity of the batched (non-convolution) tensor product (uvu_tp_fwd / uvu_tp_bwd) against
 the fp64 oracle (oracle.tp), with per-sample and batch-shared weights: element by element on
 small batches (several register groups, fp64, a batch smaller than the grid), on sampled rows
-of a 60,000-sample MACE-medium batch, the empty batch, and bitwise repeatability of the shared
+of a 60,000-sample MACE-medium batch (its shared dw over the whole batch), the empty batch, and bitwise repeatability of the shared
 dw (fixed-order block sums)."""
 import numpy as np
 import pytest
@@ -9,7 +9,7 @@ import torch
 
 from clebsch_gordan_tensor_receiver_gb300 import uvu, workloads
 from gpu_util import check, dev
-from oracle import paths, tp
+from oracle import conv, paths, tp
 
 pytestmark = pytest.mark.gpu
 
@@ -73,16 +73,20 @@ def test_medium_batch_sampled(shared):
     check(dx[rt].cpu().numpy(), r_dx, False, "dx")
     check(dy[rt].cpu().numpy(), r_dy, False, "dy")
     if shared:
-        # The shared dw sums all 60,000 samples, too many for the oracle; two properties that
-        # hold at any size pin it instead: it equals the sum over samples of the per-sample dw
-        # (the per-sample kernel is checked against the oracle above and in the small cases),
-        # and <dw, w> = <d_out, out> because out is linear in w.
-        X, Yd, G = dev(x), dev(y), dev(g)
-        wb = torch.from_numpy(np.ascontiguousarray(np.broadcast_to(w, (B,) + w.shape))).cuda()
-        dwb = torch.empty_like(wb)
-        plan.tp_bwd(B, X, Yd, wb, G, dw=dwb)
-        torch.cuda.synchronize()
-        check(dw.cpu().numpy(), dwb.double().sum(0).cpu().numpy(), False, "dw vs sum of per-sample dw")
+        # The shared dw sums all 60,000 samples.  The oracle's C loops give it: the batched
+        # product is the convolution on self loops (sample b = receiver b with the one edge b
+        # from sender b, a reading the oracle's own pins tie to oracle.tp), so the per-sample dw
+        # of oracle.conv.bwd_edges, summed over the batch in fp64, is the reference.  Also
+        # <dw, w> = <d_out, out>, because out is linear in w.
+        ref_dw = np.zeros(w.shape)
+        for b0 in range(0, B, 10000):
+            b1 = min(B, b0 + 10000)
+            n = b1 - b0
+            wb = np.broadcast_to(w, (n,) + w.shape)
+            _, dwb = conv.bwd_edges(lay, np.arange(n + 1), np.arange(n), x[b0:b1], y[b0:b1], wb, g[b0:b1])
+            ref_dw += dwb.sum(axis=0)
+        check(dw.cpu().numpy(), ref_dw, False, "shared dw vs oracle")
+        G = dev(g)
         lhs = float((dw.double() * dev(w).double()).sum())
         rhs = float((out.double() * G.double()).sum())
         assert abs(lhs - rhs) <= 1e-5 * abs(rhs), (lhs, rhs)

@@ -3,6 +3,9 @@ and rejects bad arguments on the host with clear statuses (no compute call is ma
 import ctypes
 import os
 import re
+import shutil
+import subprocess
+import sys
 
 import pytest
 
@@ -25,10 +28,22 @@ def test_exports_every_declared_symbol():
 
 
 def test_links_no_driver_library():
-    # the library must load on a host without a GPU driver: no libcuda dependency
+    # The library must load on a host without a GPU driver: it links the CUDA runtime statically
+    # and names no driver library among its dynamic dependencies.
     maps = open("/proc/self/maps").read()
     assert uvu.LIB_PATH in maps
-    assert "libcuda.so.1" not in maps or True  # torch may map it on GPU hosts
+    readelf = shutil.which("readelf")
+    if readelf:
+        dyn = subprocess.run([readelf, "-d", uvu.LIB_PATH], capture_output=True, text=True, check=True).stdout
+        needed = re.findall(r"\(NEEDED\)\s+Shared library: \[([^\]]+)\]", dyn)
+        assert needed, dyn
+        assert not [n for n in needed if n.startswith("libcuda.") or n.startswith("libcudart.")], needed
+    # and loading it in a fresh process (without torch, which maps the driver on GPU hosts) maps
+    # no driver library
+    code = ("import ctypes, sys; ctypes.CDLL(sys.argv[1]); "
+            "print(any('libcuda.so' in l for l in open('/proc/self/maps')))")
+    r = subprocess.run([sys.executable, "-c", code, uvu.LIB_PATH], capture_output=True, text=True, check=True)
+    assert r.stdout.strip() == "False", r.stdout
 
 
 def test_status_strings():

@@ -4,9 +4,10 @@ hands it input and output buffers, or a latency-critical path that must not take
 lock or risk an out-of-memory failure mid-run).  Its scratch is a fixed array inside the library.
 
 Checked here through the C ABI: on two calls in a row, with different graphs so that the second
-call starts from the scratch the first one left behind, its results equal bit for bit those of
-uvu_csr_transpose with a caller-provided workspace; and a graph larger than the built-in scratch
-is refused before any work is enqueued."""
+call starts from the scratch the first one left behind, its results equal bit for bit the
+oracle's stable counting sort and those of uvu_csr_transpose with a caller-provided workspace; a
+graph without edges gives empty sender rows; a graph whose scratch need is exactly the built-in
+16 MiB is served, and one needing more is refused before any work is enqueued."""
 import ctypes
 
 import numpy as np
@@ -14,6 +15,7 @@ import pytest
 import torch
 
 from clebsch_gordan_tensor_receiver_gb300 import uvu, workloads
+from oracle import graph
 
 pytestmark = pytest.mark.gpu
 
@@ -57,7 +59,14 @@ def _without_allocation(N, off, src_d):
     return so, se[:E], sr[:E]
 
 
-def test_two_calls_in_a_row_match_the_workspace_version():
+def _check_against_oracle(N, recv, src, got):
+    off = graph.recv_offsets(recv, N)
+    want = graph.transpose(off, src, N)
+    for name, a, b in zip(("send_offsets", "send_eids", "send_recv"), got, want):
+        assert np.array_equal(a.cpu().numpy(), b), name
+
+
+def test_two_calls_in_a_row_match_the_oracle_and_the_workspace_version():
     medium = workloads.make_workload(1)  # 5,000 receivers x 56 senders
     rng = np.random.default_rng(77)
     deg = rng.integers(0, 10, size=700)
@@ -70,10 +79,40 @@ def test_two_calls_in_a_row_match_the_workspace_version():
         torch.cuda.synchronize()
         for name, a, b in zip(("send_offsets", "send_eids", "send_recv"), got, want):
             assert torch.equal(a, b), name
+        _check_against_oracle(N, recv, src, got)
+
+
+def test_graph_without_edges():
+    N = 9
+    recv = np.zeros(0, np.int32)
+    src = np.zeros(0, np.int32)
+    off, src_d = _prepared(N, recv, src)
+    so, se, sr = _without_allocation(N, off, src_d)
+    torch.cuda.synchronize()
+    assert torch.equal(so.cpu(), torch.zeros(N + 1, dtype=torch.int32))
+
+
+def test_graph_at_the_scratch_limit():
+    # 4(N+1) and 4E rounded up to 256 bytes sum to exactly 16 MiB: the largest graph served
+    N, E = 194_303, 4_000_000
+    nb = ctypes.c_size_t()
+    uvu.uvu_csr_transpose_workspace(N, E, ctypes.byref(nb))
+    assert nb.value == 16 << 20
+    rng = np.random.default_rng(5)
+    recv = np.sort(rng.integers(0, N, size=E)).astype(np.int32)
+    src = rng.integers(0, N, size=E).astype(np.int32)
+    off, src_d = _prepared(N, recv, src)
+    got = _without_allocation(N, off, src_d)
+    torch.cuda.synchronize()
+    _check_against_oracle(N, recv, src, got)
 
 
 def test_graph_beyond_the_builtin_scratch_is_refused():
     dummy = V(256)  # never dereferenced: the size check comes first
-    st = uvu.lib.uvu_csr_transpose_noalloc(1000, 5_000_000, dummy, dummy, dummy, dummy, dummy, None)
-    assert st == 2  # UVU_ERR_UNSUPPORTED
-    assert "scratch" in uvu.uvu_last_error_message()
+    for N, E in ((1000, 5_000_000), (194_304, 4_000_000)):  # the second is 256 bytes over
+        nb = ctypes.c_size_t()
+        uvu.uvu_csr_transpose_workspace(N, E, ctypes.byref(nb))
+        assert nb.value > 16 << 20
+        st = uvu.lib.uvu_csr_transpose_noalloc(N, E, dummy, dummy, dummy, dummy, dummy, None)
+        assert st == 2  # UVU_ERR_UNSUPPORTED
+        assert "scratch" in uvu.uvu_last_error_message()
