@@ -28,8 +28,9 @@ wigner   real Wigner-D matrices fitted from SH samples (used only by equivarianc
 hvp      double backward (Hessian-vector product) through substituted forward / VJP calls.
 tp       batched (non-convolution) tensor product and its VJP, per-sample or shared weights.
 mix      per-path channel mixing that reduces a factorised UVW convolution to the UVU one.
-radial   radial weights from edge lengths (Bessel basis, polynomial envelope, SiLU network) and
-         the convolution that uses them.
+radial   radial weights from edge lengths (Bessel basis, polynomial envelope, SiLU network), the
+         convolution that uses them, and the reverse pass (edge-length and layer gradients,
+         gradients of the last linear layer).
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py`` against properties
 that the mathematics fixes (orthogonality, completeness, closed forms for l <= 1, intertwining

@@ -145,3 +145,83 @@ def test_linear_in_the_last_layer():
     lhs = radial.conv_fwd(lay, off, src, x, Y, h, Wl + 2.0 * W2)
     rhs = radial.conv_fwd(lay, off, src, x, Y, h, Wl) + 2.0 * radial.conv_fwd(lay, off, src, x, Y, h, W2)
     np.testing.assert_allclose(lhs, rhs, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- gradient pins
+# The reverse pass (radial.hidden_vjp, radial.weights_vjp) is pinned by central finite
+# differences of the forward definition (independent of the chain rule written out in the
+# oracle), by closed-form derivative values, and by the adjoint identity of a bilinear map.
+
+def _net(seed, widths=(8, 16, 12, 8)):
+    rng = np.random.default_rng(seed)
+    layers = [rng.standard_normal((widths[i], widths[i + 1])) / np.sqrt(widths[i]) for i in range(len(widths) - 1)]
+    return rng, layers
+
+
+def _fd(f, x, eps):
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        xp, xm = x.copy(), x.copy()
+        xp[i] += eps
+        xm[i] -= eps
+        g[i] = (f(xp) - f(xm)) / (2 * eps)
+    return g
+
+
+def test_envelope_and_basis_derivatives():
+    s = np.linspace(0.05, 0.95, 19)
+    for p in (3, 5, 6):
+        fd = (radial.envelope(s + 1e-7, p) - radial.envelope(s - 1e-7, p)) / 2e-7
+        np.testing.assert_allclose(radial.envelope_deriv(s, p), fd, atol=1e-7)
+        # value and slope vanish at the cutoff, the slope at 0 too (p > 1); zero beyond
+        assert abs(radial.envelope_deriv(np.array([1.0 - 1e-12]), p)[0]) < 1e-8
+        assert radial.envelope_deriv(np.array([0.0]), p)[0] == 0.0
+        assert radial.envelope_deriv(np.array([1.3]), p)[0] == 0.0
+    r = np.linspace(0.3, 4.9, 23)
+    fd = (radial.bessel_basis(r + 1e-7, 5.0, 8) - radial.bessel_basis(r - 1e-7, 5.0, 8)) / 2e-7
+    np.testing.assert_allclose(radial.bessel_basis_deriv(r, 5.0, 8), fd, atol=1e-6)
+    v = np.linspace(-6, 6, 25)
+    np.testing.assert_allclose(radial.silu_deriv(v), (radial.silu(v + 1e-7) - radial.silu(v - 1e-7)) / 2e-7, atol=1e-7)
+    # closed forms: silu'(0) = 1/2, d/dr b_n at r -> 0 tends to 0 (b_n is even in r about 0)
+    assert radial.silu_deriv(np.array([0.0]))[0] == 0.5
+    assert abs(radial.bessel_basis_deriv(np.array([1e-4]), 5.0, 3)).max() < 1e-3
+
+
+def test_hidden_vjp_matches_finite_differences():
+    rng, layers = _net(1)
+    E = 6
+    r = np.concatenate([rng.uniform(0.8, 4.9, size=E - 2), [4.999, 6.0]])  # one just inside, one beyond
+    dh = rng.standard_normal((E, 8))
+    dr, dWs = radial.hidden_vjp(r, 5.0, 5, layers, dh)
+
+    def L(rr, ls):
+        return float((dh * radial.hidden(rr, 5.0, 5, ls)).sum())
+
+    np.testing.assert_allclose(dr, _fd(lambda rr: L(rr, layers), r, 1e-6), atol=1e-8)
+    assert dr[-1] == 0.0  # beyond the cutoff: h = 0 around it
+    for i in range(len(layers)):
+        def Li(Wi, i=i):
+            ls = list(layers)
+            ls[i] = Wi
+            return L(r, ls)
+        np.testing.assert_allclose(dWs[i], _fd(Li, layers[i].copy(), 1e-6), atol=1e-8)
+
+
+def test_weights_vjp_adjoint_and_finite_differences():
+    rng = np.random.default_rng(9)
+    E, H, P, U = 7, 5, 3, 4
+    h = rng.standard_normal((E, H))
+    Wl = rng.standard_normal((H, P, U))
+    dw = rng.standard_normal((E, P, U))
+    dh, dWl = radial.weights_vjp(h, Wl, dw)
+    # w is bilinear in (h, W_last): <dw, w> = <dh, h> = <dW_last, W_last>
+    s = float((dw * radial.weights(h, Wl)).sum())
+    assert abs(float((dh * h).sum()) - s) < 1e-12 * max(1.0, abs(s))
+    assert abs(float((dWl * Wl).sum()) - s) < 1e-12 * max(1.0, abs(s))
+    np.testing.assert_allclose(dh, _fd(lambda hh: float((dw * radial.weights(hh, Wl)).sum()), h.copy(), 1e-6), atol=1e-8)
+    np.testing.assert_allclose(dWl, _fd(lambda ww: float((dw * radial.weights(h, ww)).sum()), Wl.copy(), 1e-6), atol=1e-8)
+    # brute force of one entry of each
+    assert abs(dh[2, 3] - sum(dw[2, p, u] * Wl[3, p, u] for p in range(P) for u in range(U))) < 1e-12
+    assert abs(dWl[1, 2, 0] - sum(h[e, 1] * dw[e, 2, 0] for e in range(E))) < 1e-12
