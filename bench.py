@@ -703,7 +703,51 @@ def main(argv=None):
         conv_ms = ev_mix(lambda: plan.fwd(N, x, Y, wmat.view(E, P, U), G.recv_offsets, src, out, stream), reps)
         torch.cuda.synchronize()
         rel = float(torch.linalg.vector_norm((rout - out).double()) / torch.linalg.vector_norm(out.double()))
+        # the tensor-core path: the last layer materialised by uvu_radial_weights (3xTF32), then the
+        # convolution; its VJP: uvu_conv_bwd's kernels with w, then the last layer's gradients (dh on
+        # the tensor cores, dW_last on CUDA cores) and the network's reverse pass (dr, dW_i)
+        tc_w_ms = ev_mix(lambda: plan.radial_weights(hbuf, Wlast, wmat.view(E, P, U), stream=stream), reps)
+        wv = wmat.view(E, P, U)
+        plan.radial_weights(hbuf, Wlast, wv, stream=stream)
+        tc_conv_ms = ev_mix(lambda: plan.fwd(N, x, Y, wv, G.recv_offsets, src, out, stream), reps)
+        rdw = torch.empty_like(wv)
+        rdh = torch.empty_like(hbuf)
+        rdWl = torch.empty_like(Wlast)
+        rdr = torch.empty_like(rr)
+        rdW = torch.empty_like(Wn)
+        rws = torch.empty(max(16, plan.radial_weights_bwd_workspace(E, Hr)), dtype=torch.uint8, device=dev)
+        rhws = torch.empty(max(16, plan.radial_hidden_bwd_workspace(E, widths)), dtype=torch.uint8, device=dev)
+
+        def conv_vjp():
+            plan.bwd_edge(N, x, Y, wv, G.recv_offsets, src, g, dY=dY, dw=rdw, dx_edge=ws, stream=stream)
+            plan.bwd_dx_reduce(N, E, G.send_offsets, G.send_eids, ws, dx, stream)
+        vjp_conv_ms = ev_mix(conv_vjp, reps)
+        dh_ms = ev_mix(lambda: plan.radial_weights_bwd(hbuf, Wlast, rdw, dh=rdh, workspace=rws, stream=stream), reps)
+        dWl_ms = ev_mix(lambda: plan.radial_weights_bwd(hbuf, Wlast, rdw, dw_last=rdWl, workspace=rws, stream=stream), reps)
+        hb_ms = ev_mix(lambda: plan.radial_hidden_bwd(rr, 5.0, 5, widths, Wn, rdh, rdr, rdW, workspace=rhws,
+                                                      stream=stream), reps)
+        torch.backends.cuda.matmul.allow_tf32 = False
+        cb_dh = ev_mix(lambda: torch.matmul(rdw.view(E, P * U), Wlast.view(Hr, P * U).t(), out=rdh), reps)
+        cb_dWl = ev_mix(lambda: torch.matmul(hbuf.t(), rdw.view(E, P * U), out=rdWl.view(Hr, P * U)), reps)
+        torch.backends.cuda.matmul.allow_tf32 = tf32_prev
+        assert plan.device_status() == 0
         flops_last = 2.0 * E * U * P * Hr
+        tf32_peak = float(peaks.get("bf16_tflops", 0.0)) / 2.0 if peaks.get("bf16_tflops") else None
+        tc = {
+            "weights_ms": tc_w_ms, "weights_GB_s": (E * P * U * s + E * Hr * s) / (tc_w_ms / 1000) / 1e9,
+            "weights_hbm_frac": (E * P * U * s + E * Hr * s) / (tc_w_ms / 1000) / 1e9 / hbm_peak,
+            "weights_tensor_tflops": 3 * flops_last / (tc_w_ms / 1000) / 1e12,
+            "tf32_peak_tflops": tf32_peak,
+            "conv_fwd_ms": tc_conv_ms, "fwd_total_ms": hid_ms + tc_w_ms + tc_conv_ms,
+            "conv_vjp_ms": vjp_conv_ms, "dh_ms": dh_ms, "dw_last_ms": dWl_ms, "hidden_bwd_ms": hb_ms,
+            "vjp_total_ms": vjp_conv_ms + dh_ms + dWl_ms + hb_ms,
+            "fwd_vjp_total_ms": hid_ms + tc_w_ms + tc_conv_ms + vjp_conv_ms + dh_ms + dWl_ms + hb_ms,
+            "cublas_fp32": {"weights_ms": gemm["fp32"], "dh_ms": cb_dh, "dw_last_ms": cb_dWl,
+                            "fwd_vjp_total_ms": hid_ms + gemm["fp32"] + conv_ms + vjp_conv_ms + cb_dh + cb_dWl + hb_ms},
+            "note": ("weights and dh on the tensor cores (tcgen05 kind::tf32, operands split hi + lo, three products "
+                     "per term: fp32 accuracy; tensor flops = 3 x 2 E H P U); dW_last and the network's reverse pass "
+                     "on CUDA cores (compensated sums over all edges); tf32 peak = measured bf16 dense / 2 (nominal "
+                     "ratio); cublas_fp32 replaces the three products with cuBLAS FP32 GEMMs (library, comparison only)")}
         hid_flops = 2.0 * E * sum(widths[i] * widths[i + 1] for i in range(3))
         fused_bytes = E * U * Dx * s + E * Dy * s + E * Hr * s + N * U * Do * s + 4 * (N + 1) + 4 * E
         line["radial"] = {
@@ -718,11 +762,12 @@ def main(argv=None):
                              "total_fp32_ms": hid_ms + gemm["fp32"] + conv_ms,
                              "total_tf32_ms": hid_ms + gemm["tf32"] + conv_ms},
             "fused_total_ms": hid_ms + fus_ms,
+            "tensor_core_path": tc,
             "rel_frobenius_vs_materialised_fp32": rel,
             "note": "alu bound: last-layer FMAs (2 E U P H flop) over the FP32 rate measured in this run; "
                     "the materialised GEMMs are cuBLAS (library), shown for comparison only"}
         assert plan.device_status() == 0
-        del rr, Wn, Wlast, hbuf, rout, wmat
+        del rr, Wn, Wlast, hbuf, rout, wmat, rdw, rdh, rdWl, rdr, rdW, rws, rhws
 
     # fwd and fwd+VJP (staged dx) of the other four workloads, each on its own plan and graph:
     # edges/s, GB/s of the compulsory bytes and the fraction of the HBM peak; for the fp64

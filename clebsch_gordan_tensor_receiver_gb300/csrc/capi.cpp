@@ -427,6 +427,11 @@ extern "C" uvu_status uvu_plan_device_status(uvu_plan_t plan, unsigned* word, in
         e = cudaMemcpy(&w2, a.status_word, sizeof(unsigned), cudaMemcpyDeviceToHost);
         *word |= w2;
     }
+    if (e == cudaSuccess) {  // the tensor-core product kernels' word (shared by all plans)
+        unsigned w3 = 0;
+        e = tc_status(&w3, reset != 0);
+        *word |= w3;
+    }
     if (e == cudaSuccess && reset) {
         const unsigned zero = 0;
         e = cudaMemcpy(m->status_word, &zero, sizeof(unsigned), cudaMemcpyHostToDevice);
@@ -867,5 +872,141 @@ extern "C" uvu_status uvu_fma_rate_probe(uvu_dtype dtype, int blocks, int iters,
     UVU_TRY(need(out, "out"));
     cudaError_t e = launch_fma_probe(dtype == UVU_F64, blocks, iters, out, static_cast<cudaStream_t>(stream), fmas);
     if (e != cudaSuccess) return cuda_fail(e, "fma probe launch");
+    return ok();
+}
+
+// ------------------------------------------------------- radial network: last layer, gradients
+namespace uvu {
+namespace {
+uvu_status radial_net(int n_layers, const int* widths, RadialNet* net) {
+    if (n_layers < 1 || n_layers > kRadialMaxLayers) return fail(UVU_ERR_INVALID_ARGUMENT, "n_layers must be in [1, 4]");
+    if (!widths) return fail(UVU_ERR_INVALID_ARGUMENT, "widths is NULL");
+    net->n_layers = n_layers;
+    if (widths[0] < 1 || widths[0] > 64) return fail(UVU_ERR_INVALID_ARGUMENT, "widths[0] (n_basis) must be in [1, 64]");
+    for (int i = 0; i <= n_layers; ++i) {
+        if (i > 0 && (widths[i] < 4 || widths[i] > 128 || widths[i] % 4))
+            return fail(UVU_ERR_INVALID_ARGUMENT, "hidden widths must be multiples of 4 in [4, 128]");
+        net->widths[i] = widths[i];
+        net->max_width = std::max(net->max_width, widths[i]);
+    }
+    return UVU_OK;
+}
+int sm_count_now() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return sms;
+}
+}  // namespace
+}  // namespace uvu
+
+extern "C" uvu_status uvu_radial_weights(uvu_plan_t plan, int64_t n_edges, const void* h, int hidden,
+                                         const void* w_last, void* w, uvu_stream_t stream) {
+    UVU_RANGE("uvu_radial_weights");
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(0, n_edges));
+    if (hidden < 4 || hidden > 256 || hidden % 4) return fail(UVU_ERR_INVALID_ARGUMENT, "hidden must be a multiple of 4 in [4, 256]");
+    if (n_edges == 0) return ok();
+    UVU_TRY(need(h, "h"));
+    UVU_TRY(need(w_last, "w_last"));
+    UVU_TRY(need(w, "w"));
+    const int PU = p->P * p->U;
+    cudaError_t e = launch_dense_product(p->dtype == UVU_F64, n_edges, hidden, PU, h, w_last, false, w, nullptr,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "radial last layer launch");
+    return ok();
+}
+
+extern "C" uvu_status uvu_radial_weights_bwd_workspace(uvu_plan_t plan, int64_t n_edges, int hidden, size_t* bytes) {
+    Plan* p = get(plan);
+    if (!p || !bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or bytes is NULL");
+    UVU_TRY(check_sizes(0, n_edges));
+    if (hidden < 4 || hidden > 256 || hidden % 4) return fail(UVU_ERR_INVALID_ARGUMENT, "hidden must be a multiple of 4 in [4, 256]");
+    const int PU = p->P * p->U;
+    const size_t a = (dense_product_workspace(hidden, PU, p->dtype == UVU_F64) + 255) / 256 * 256;
+    *bytes = a + dense_reduction_workspace(n_edges, hidden, PU);
+    return ok();
+}
+
+extern "C" uvu_status uvu_radial_weights_bwd(uvu_plan_t plan, int64_t n_edges, const void* h, int hidden,
+                                             const void* w_last, const void* dw, void* dh, void* dw_last,
+                                             void* workspace, size_t workspace_bytes, uvu_stream_t stream) {
+    UVU_RANGE("uvu_radial_weights_bwd");
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(0, n_edges));
+    if (hidden < 4 || hidden > 256 || hidden % 4) return fail(UVU_ERR_INVALID_ARGUMENT, "hidden must be a multiple of 4 in [4, 256]");
+    UVU_TRY(opt(dh, "dh"));
+    UVU_TRY(opt(dw_last, "dw_last"));
+    const bool f64 = p->dtype == UVU_F64;
+    const int PU = p->P * p->U;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n_edges == 0) {
+        if (dw_last) {
+            cudaError_t e = cudaMemsetAsync(dw_last, 0, size_t(hidden) * PU * p->elem(), st);
+            if (e != cudaSuccess) return cuda_fail(e, "memset");
+        }
+        return ok();
+    }
+    if (!dh && !dw_last) return ok();
+    UVU_TRY(need(dw, "dw"));
+    UVU_TRY(need(w_last, "w_last"));
+    if (dw_last) UVU_TRY(need(h, "h"));
+    size_t need_bytes = 0;
+    UVU_TRY(uvu_radial_weights_bwd_workspace(plan, n_edges, hidden, &need_bytes));
+    if (!workspace || workspace_bytes < need_bytes || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return fail(UVU_ERR_INVALID_ARGUMENT, "workspace is NULL, misaligned or smaller than uvu_radial_weights_bwd_workspace()");
+    char* ws = static_cast<char*>(workspace);
+    const size_t a = (dense_product_workspace(hidden, PU, f64) + 255) / 256 * 256;
+    cudaError_t e = cudaSuccess;
+    if (dh) e = launch_dense_product(f64, n_edges, PU, hidden, dw, w_last, true, dh, ws, st);
+    if (e == cudaSuccess && dw_last) e = launch_dense_reduction(f64, n_edges, hidden, PU, h, dw, dw_last, ws + a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "radial last-layer gradient launch");
+    return ok();
+}
+
+extern "C" uvu_status uvu_radial_hidden_bwd_workspace(uvu_plan_t plan, int64_t n_edges, int n_layers, const int* widths,
+                                                      size_t* bytes) {
+    Plan* p = get(plan);
+    if (!p || !bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or bytes is NULL");
+    UVU_TRY(check_sizes(0, n_edges));
+    RadialNet net;
+    UVU_TRY(radial_net(n_layers, widths, &net));
+    if (!radial_hidden_bwd_supported(net, p->dtype == UVU_F64))
+        return fail(UVU_ERR_UNSUPPORTED, "the radial network is too wide for the reverse pass's shared memory");
+    *bytes = radial_hidden_bwd_workspace(n_edges, net, p->dtype == UVU_F64, std::max(1, sm_count_now()));
+    return ok();
+}
+
+extern "C" uvu_status uvu_radial_hidden_bwd(uvu_plan_t plan, int64_t n_edges, const void* r, double r_cut, int p_env,
+                                            int n_layers, const int* widths, const void* weights, const void* dh,
+                                            void* dr, void* dweights, void* workspace, size_t workspace_bytes,
+                                            uvu_stream_t stream) {
+    UVU_RANGE("uvu_radial_hidden_bwd");
+    Plan* p = get(plan);
+    if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
+    UVU_TRY(check_sizes(0, n_edges));
+    if (!(r_cut > 0) || !std::isfinite(r_cut)) return fail(UVU_ERR_INVALID_ARGUMENT, "r_cut must be positive and finite");
+    if (p_env < 1 || p_env > 16) return fail(UVU_ERR_INVALID_ARGUMENT, "p_env must be in [1, 16]");
+    RadialNet net;
+    UVU_TRY(radial_net(n_layers, widths, &net));
+    const bool f64 = p->dtype == UVU_F64;
+    if (!radial_hidden_bwd_supported(net, f64))
+        return fail(UVU_ERR_UNSUPPORTED, "the radial network is too wide for the reverse pass's shared memory");
+    UVU_TRY(need(weights, "weights"));
+    UVU_TRY(need(dweights, "dweights"));
+    const int sms = std::max(1, sm_count_now());
+    if (n_edges > 0) {
+        UVU_TRY(need(r, "r"));
+        UVU_TRY(need(dh, "dh"));
+        UVU_TRY(need(dr, "dr"));
+        const size_t nb = radial_hidden_bwd_workspace(n_edges, net, f64, sms);
+        if (!workspace || workspace_bytes < nb || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+            return fail(UVU_ERR_INVALID_ARGUMENT, "workspace is NULL, misaligned or smaller than uvu_radial_hidden_bwd_workspace()");
+    }
+    cudaError_t e = launch_radial_hidden_bwd(n_edges, r, r_cut, p_env, net, weights, dh, dr, dweights, workspace, f64, sms,
+                                             static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "radial network reverse pass launch");
     return ok();
 }

@@ -151,12 +151,13 @@ struct Gen {
         }
     }
 
-    // UVU_PACK_PRODUCTS=1 (a tuning switch): fp32 products of an x value with two y values at
-    // even/odd index pairs use one paired multiply (mul.rn.f32x2, each half rounded as a scalar
-    // multiply, so the results are the same bits).  Measured on MACE-medium: forward 0.356 ->
-    // 0.340-0.348 ms, edge kernel within its spread, MACE-large unchanged.
+    // fp32 products of an x value with two y values at even/odd index pairs use one paired
+    // multiply (mul.rn.f32x2, each half rounded as a scalar multiply, so the results are the same
+    // bits).  Measured on MACE-medium: forward 0.356 -> 0.339 ms, edge kernel 0.862 -> 0.820 ms
+    // (fewer issue slots in issue-bound kernels); MACE-large unchanged.  UVU_PACK_PRODUCTS=0 (a
+    // tuning switch) emits scalar multiplies.
     bool pack_products() const {
-        return !f64 && std::getenv("UVU_PACK_PRODUCTS") && std::atoi(std::getenv("UVU_PACK_PRODUCTS")) == 1;
+        return !f64 && !(std::getenv("UVU_PACK_PRODUCTS") && std::atoi(std::getenv("UVU_PACK_PRODUCTS")) == 0);
     }
     // Device helpers of the paired fp32 products (emitted when they are used).
     void emit_pair_helpers(Src& S) const {

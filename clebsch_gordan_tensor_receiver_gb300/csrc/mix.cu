@@ -9,10 +9,15 @@
 // the operand to a component-major layout [D_out][N][U] (one pass, coalesced both ways through a
 // shared-memory tile); a path p is then the contiguous matrix of rows (ooff(p)+m, r), and the
 // mixing is one dense product per path, A_p [d3*N x U] times M[p] [U x W], written component-major
-// and copied back.  The input gradient is the same product with M[p] transposed (copied once per
-// call), and dM[p] = A_p^T G_p is a product over the rows, split into fixed row chunks summed in
-// fp64 (fp32 within 16 rows) and added in chunk order (deterministic).
+// and copied back.  The input gradient is the same product with M[p] transposed, and
+// dM[p] = A_p^T G_p is a product over the rows, split into fixed row chunks summed in fp64 (fp32
+// within 16 rows) and added in chunk order (deterministic).  In fp32 plans the two products with
+// K = U or W run on the tensor cores (tcgemm.cu: 3xTF32, fp32 accuracy), reading M directly as the
+// k-contiguous operand for the input gradient; dM, a sum over d3 N rows, stays on the compensated
+// CUDA-core kernel, whose fp32 steps of 16 rows keep the elementwise tolerance that the tensor
+// memory's accumulation did not.
 #include "plan.h"
+#include "tcgemm.h"
 
 namespace uvu {
 namespace {
@@ -277,6 +282,30 @@ cudaError_t relayout_launch(int64_t N, int A, int B, bool inv, const void* in, v
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// The per-path products as tensor-core jobs: segment p = the rows of path p in the
+// component-major operand A [Do N][K]; B_p [K][Nc] n-contiguous, or, with b_kcont, the product
+// with B_p^T of a [Nc][K] block (k contiguous) so that M needs no transposed copy.
+TcJobs tc_product_jobs(const Plan& p, int64_t N, int K, int Nc, const float* A, const float* B, bool b_kcont, float* C) {
+    TcJobs J{};
+    J.nseg = p.P;
+    for (int i = 0; i < p.P && i < kTcMaxSeg; ++i) {
+        J.row0[i] = int64_t(p.paths[i].ooff) * N;
+        J.rows[i] = int64_t(2 * p.paths[i].l3 + 1) * N;
+    }
+    J.K = K;
+    J.N = Nc;
+    J.b_kcont = b_kcont ? 1 : 0;
+    J.A = A;
+    J.lda = K;
+    J.B = B;
+    J.sbk = b_kcont ? 1 : Nc;
+    J.sbn = b_kcont ? K : 1;
+    J.b_seg_stride = int64_t(K) * Nc;
+    J.C = C;
+    J.ldc = Nc;
+    return J;
+}
+
 // in [N][K][Do] -> out [N][Nc][Do] through component-major copies in ws: [Do N K] then [Do N Nc]
 template <typename T>
 cudaError_t mix_product(const Plan& p, int64_t N, int K, int Nc, const void* in, const void* Bmat, void* out,
@@ -288,15 +317,109 @@ cudaError_t mix_product(const Plan& p, int64_t N, int K, int Nc, const void* in,
     int64_t tiles = 0;
     const SegTab tab = make_seg(p, N, &tiles);
     if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
-    seg_gemm<T><<<dim3(unsigned(tiles), unsigned((Nc + kTN - 1) / kTN)), 256, 0, st>>>(
-        K, Nc, tab, inT, static_cast<const T*>(Bmat), outT);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bool done = false;
+    if (sizeof(T) == 4) {
+        // fp32: the per-path products on the tensor cores (3xTF32), B_p = Bmat + p K Nc
+        TcJobs J = tc_product_jobs(p, N, K, Nc, reinterpret_cast<const float*>(inT),
+                                   reinterpret_cast<const float*>(Bmat), false, reinterpret_cast<float*>(outT));
+        if (tc_gemm_supported(J)) {
+            if ((e = launch_tc_gemm(J, st)) != cudaSuccess) return e;
+            done = true;
+        }
+    }
+    if (!done) {
+        seg_gemm<T><<<dim3(unsigned(tiles), unsigned((Nc + kTN - 1) / kTN)), 256, 0, st>>>(
+            K, Nc, tab, inT, static_cast<const T*>(Bmat), outT);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     return relayout_launch<T>(N, Nc, p.Do, true, outT, out, st);
 }
 
 }  // namespace
 
 int mix_max_paths() { return kMaxPaths; }
+
+// ------------------------------------------------- single dense products (radial last layer)
+
+// C[rows][Nc] = A[rows][K] B, with B [K][Nc] (b_kcont = 0) or given as the [Nc][K] block B^T
+// (b_kcont = 1).  fp32: the tensor cores when the shapes allow; otherwise (fp64, other shapes) the
+// register-tiled CUDA-core product, which needs B as [K][Nc] (a transposed copy in `ws`,
+// K * Nc elements, for b_kcont).
+cudaError_t launch_dense_product(bool f64, int64_t rows, int K, int Nc, const void* A, const void* B, bool b_kcont,
+                                 void* C, void* ws, cudaStream_t st) {
+    if (rows <= 0 || Nc <= 0) return cudaSuccess;
+    if (!f64) {
+        TcJobs J{};
+        J.nseg = 1;
+        J.row0[0] = 0;
+        J.rows[0] = rows;
+        J.K = K;
+        J.N = Nc;
+        J.b_kcont = b_kcont ? 1 : 0;
+        J.A = static_cast<const float*>(A);
+        J.lda = K;
+        J.B = static_cast<const float*>(B);
+        J.sbk = b_kcont ? 1 : Nc;
+        J.sbn = b_kcont ? K : 1;
+        J.b_seg_stride = 0;
+        J.C = static_cast<float*>(C);
+        J.ldc = Nc;
+        if (tc_gemm_supported(J)) return launch_tc_gemm(J, st);
+    }
+    const void* Bn = B;
+    cudaError_t e;
+    if (b_kcont) {  // [Nc][K] -> [K][Nc]
+        const int64_t n = int64_t(K) * Nc;
+        const unsigned nb = unsigned((n + 255) / 256);
+        if (f64) transpose_M<double><<<nb, 256, 0, st>>>(1, Nc, K, static_cast<const double*>(B), static_cast<double*>(ws));
+        else transpose_M<float><<<nb, 256, 0, st>>>(1, Nc, K, static_cast<const float*>(B), static_cast<float*>(ws));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        Bn = ws;
+    }
+    SegTab tab{};
+    tab.n = 1;
+    tab.row0[0] = 0;
+    tab.rows[0] = rows;
+    tab.tile0[0] = 0;
+    const int64_t tiles = (rows + kTM - 1) / kTM;
+    if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
+    tab.tile0[1] = int(tiles);
+    const dim3 grid(unsigned(tiles), unsigned((Nc + kTN - 1) / kTN));
+    if (f64) seg_gemm<double><<<grid, 256, 0, st>>>(K, Nc, tab, static_cast<const double*>(A), static_cast<const double*>(Bn), static_cast<double*>(C));
+    else seg_gemm<float><<<grid, 256, 0, st>>>(K, Nc, tab, static_cast<const float*>(A), static_cast<const float*>(Bn), static_cast<float*>(C));
+    return cudaGetLastError();
+}
+
+size_t dense_product_workspace(int K, int Nc, bool f64) { return size_t(K) * Nc * (f64 ? 8 : 4); }
+
+// C[Mr][Nc] = sum over rows of A[row][m] G[row][n]: fp32 steps of 16 rows, Kahan-compensated,
+// fp64 partials per chunk of kRowChunk rows (in `ws`) added in chunk order -- deterministic.
+size_t dense_reduction_workspace(int64_t rows, int Mr, int Nc) {
+    const int64_t C = std::max<int64_t>(1, (rows + kRowChunk - 1) / kRowChunk);
+    return size_t(C) * Mr * Nc * sizeof(double);
+}
+
+cudaError_t launch_dense_reduction(bool f64, int64_t rows, int Mr, int Nc, const void* A, const void* G, void* C, void* ws,
+                                   cudaStream_t st) {
+    if (Mr <= 0 || Nc <= 0) return cudaSuccess;
+    if (rows <= 0) return cudaMemsetAsync(C, 0, size_t(Mr) * Nc * (f64 ? 8 : 4), st);
+    SegTab tab{};
+    tab.n = 1;
+    tab.row0[0] = 0;
+    tab.rows[0] = rows;
+    const int64_t nch = (rows + kRowChunk - 1) / kRowChunk;
+    const unsigned tiles = unsigned(((Mr + kDT - 1) / kDT) * ((Nc + kDT - 1) / kDT));
+    const dim3 grid(tiles, 1u, unsigned(nch));
+    if (f64)
+        seg_dM<double><<<grid, 256, 0, st>>>(Mr, Nc, tab, static_cast<const double*>(A), static_cast<const double*>(G),
+                                              static_cast<double*>(ws));
+    else
+        seg_dM<float><<<grid, 256, 0, st>>>(Mr, Nc, tab, static_cast<const float*>(A), static_cast<const float*>(G),
+                                             static_cast<double*>(ws));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_column_sum(ws, nch, int64_t(Mr) * Nc, C, f64, st);
+}
 
 namespace {
 size_t r256(size_t b) { return (b + 255) / 256 * 256; }
@@ -332,7 +455,20 @@ cudaError_t launch_mix_bwd(const Plan& p, int64_t N, int W, const void* in, cons
     void* part = static_cast<char*>(Mt) + r256(PUW * s);
     const bool f64 = p.dtype == UVU_F64;
     cudaError_t e = cudaSuccess;
-    if (d_in) {
+    bool d_in_done = false;
+    if (d_in && !f64) {
+        // tensor cores: d_in_p = g_p M_p^T with M read as the k-contiguous operand (no transposed copy)
+        float* gT = static_cast<float*>(prod_ws);
+        float* dT = reinterpret_cast<float*>(base + r256(ND * W * s));
+        TcJobs J = tc_product_jobs(p, N, W, p.U, gT, static_cast<const float*>(M), true, dT);
+        if (tc_gemm_supported(J)) {
+            if ((e = relayout_launch<float>(N, W, p.Do, false, g, gT, st)) != cudaSuccess) return e;
+            if ((e = launch_tc_gemm(J, st)) != cudaSuccess) return e;
+            if ((e = relayout_launch<float>(N, p.U, p.Do, true, dT, d_in, st)) != cudaSuccess) return e;
+            d_in_done = true;
+        }
+    }
+    if (d_in && !d_in_done) {
         const unsigned nb = unsigned((PUW + 255) / 256);
         if (f64) transpose_M<double><<<nb, 256, 0, st>>>(p.P, p.U, W, static_cast<const double*>(M), static_cast<double*>(Mt));
         else transpose_M<float><<<nb, 256, 0, st>>>(p.P, p.U, W, static_cast<const float*>(M), static_cast<float*>(Mt));

@@ -159,7 +159,24 @@ cudaError_t launch_column_sum(const void* part, int64_t rows, int64_t cols, void
 size_t radial_hidden_smem(const RadialNet& net, bool f64);
 cudaError_t launch_radial_hidden(int64_t E, const void* r, double r_cut, int p_env, const RadialNet& net, const void* W,
                                  void* h, bool f64, int sm_count, cudaStream_t st);
+size_t radial_hidden_bwd_workspace(int64_t E, const RadialNet& net, bool f64, int sm_count);
+bool radial_hidden_bwd_supported(const RadialNet& net, bool f64);
+cudaError_t launch_radial_hidden_bwd(int64_t E, const void* r, double r_cut, int p_env, const RadialNet& net,
+                                     const void* W, const void* dh, void* dr, void* dW, void* ws, bool f64,
+                                     int sm_count, cudaStream_t st);
+// tcgemm.cu: fp32 products on the tensor cores (3xTF32, see tcgemm.cu)
+constexpr int kTcMaxSeg = 128;
+struct TcJobs;
+bool tc_gemm_supported(const TcJobs& J);
+cudaError_t launch_tc_gemm(TcJobs& J, cudaStream_t st);
+cudaError_t tc_status(unsigned* word, bool reset);
 // mix.cu
+cudaError_t launch_dense_product(bool f64, int64_t rows, int K, int Nc, const void* A, const void* B, bool b_kcont,
+                                 void* C, void* ws, cudaStream_t st);
+size_t dense_product_workspace(int K, int Nc, bool f64);
+size_t dense_reduction_workspace(int64_t rows, int Mr, int Nc);
+cudaError_t launch_dense_reduction(bool f64, int64_t rows, int Mr, int Nc, const void* A, const void* G, void* C, void* ws,
+                                   cudaStream_t st);
 int mix_max_paths();
 size_t mix_workspace_bytes(const Plan& p, int64_t N, int W, bool bwd);
 cudaError_t launch_mix_fwd(const Plan& p, int64_t N, int W, const void* in, const void* M, void* out, void* ws,

@@ -1,0 +1,29 @@
+// Job tables of the tensor-core product kernel (tcgemm.cu); shared by its callers.
+#pragma once
+
+#include "plan.h"
+
+namespace uvu {
+
+struct TcJobs {
+    int nseg;
+    long long row0[kTcMaxSeg];
+    long long rows[kTcMaxSeg];
+    int tile0[kTcMaxSeg + 1];  // prefix of 128-row tiles over the segments (set by the launcher)
+    int K;                   // reduction length (columns of A)
+    int N;                   // columns of C
+    int b_kcont;             // B[k][n] has k contiguous (else n contiguous)
+    const float* A;
+    long long lda;           // elements between rows of A
+    const float* B;
+    long long sbk, sbn;      // B strides for k and n
+    long long b_seg_stride;  // offset of B_s
+    float* C;
+    long long ldc;           // elements between rows of C
+    // set by the launcher
+    int bn;                  // columns per tile
+    int kacc;                // K per accumulator
+    int tmem_cols;           // tensor-memory columns allocated per CTA
+};
+
+}  // namespace uvu

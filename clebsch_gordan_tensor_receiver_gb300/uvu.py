@@ -36,6 +36,8 @@ EXPORTS = (
     "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
     "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
     "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source",
+    "uvu_radial_weights", "uvu_radial_weights_bwd", "uvu_radial_weights_bwd_workspace",
+    "uvu_radial_hidden_bwd", "uvu_radial_hidden_bwd_workspace",
     "uvu_fma_rate_probe", "uvu_status_string", "uvu_last_error_message",
 )
 
@@ -87,6 +89,11 @@ def _load():
         "uvu_conv_fwd_radial": [P, I64, I64, P, P, P, I, P, P, P, P, P],
         "uvu_radial_module_source": [P, I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
         "uvu_fma_rate_probe": [I, I, I, P, ctypes.POINTER(ctypes.c_double), P],
+        "uvu_radial_weights": [P, I64, P, I, P, P, P],
+        "uvu_radial_weights_bwd": [P, I64, P, I, P, P, P, P, P, SZ, P],
+        "uvu_radial_weights_bwd_workspace": [P, I64, I, ctypes.POINTER(SZ)],
+        "uvu_radial_hidden_bwd": [P, I64, P, ctypes.c_double, I, I, ctypes.POINTER(I), P, P, P, P, P, SZ, P],
+        "uvu_radial_hidden_bwd_workspace": [P, I64, I, ctypes.POINTER(I), ctypes.POINTER(SZ)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -126,7 +133,9 @@ for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source"
            "uvu_conv_hvp", "uvu_conv_hvp_workspace", "uvu_tp_fwd", "uvu_tp_bwd", "uvu_tp_bwd_workspace",
            "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
            "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
-           "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source", "uvu_fma_rate_probe"):
+           "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source", "uvu_fma_rate_probe",
+           "uvu_radial_weights", "uvu_radial_weights_bwd", "uvu_radial_weights_bwd_workspace",
+           "uvu_radial_hidden_bwd", "uvu_radial_hidden_bwd_workspace"):
     globals()[_n] = _wrap(_n)
 
 
@@ -243,6 +252,41 @@ class Plan:
         uvu_conv_fwd_radial(self.handle, n_nodes, src.numel() if src is not None else 0, _ptr(x), _ptr(Y), _ptr(h),
                             int(w_last.shape[0]), _ptr(w_last), _ptr(recv_offsets), _ptr(src), _ptr(out),
                             _stream(stream))
+
+    def radial_weights(self, h, w_last, w, stream=None):
+        """Materialised last layer w = h W_last (see uvu_radial_weights)."""
+        uvu_radial_weights(self.handle, h.shape[0], _ptr(h), int(h.shape[1]), _ptr(w_last), _ptr(w), _stream(stream))
+
+    def radial_weights_bwd_workspace(self, n_edges, hidden) -> int:
+        b = ctypes.c_size_t()
+        uvu_radial_weights_bwd_workspace(self.handle, n_edges, int(hidden), ctypes.byref(b))
+        return b.value
+
+    def radial_weights_bwd(self, h, w_last, dw, dh=None, dw_last=None, workspace=None, stream=None):
+        """dh = dw W_last^T and dW_last = h^T dw (see uvu_radial_weights_bwd)."""
+        import torch
+        E, H = h.shape
+        if workspace is None:
+            workspace = torch.empty(max(16, self.radial_weights_bwd_workspace(E, H)), dtype=torch.uint8, device=h.device)
+        uvu_radial_weights_bwd(self.handle, E, _ptr(h), int(H), _ptr(w_last), _ptr(dw), _ptr(dh), _ptr(dw_last),
+                               _ptr(workspace), workspace.numel(), _stream(stream))
+
+    def radial_hidden_bwd_workspace(self, n_edges, widths) -> int:
+        wd = (ctypes.c_int * len(widths))(*[int(v) for v in widths])
+        b = ctypes.c_size_t()
+        uvu_radial_hidden_bwd_workspace(self.handle, n_edges, len(widths) - 1, wd, ctypes.byref(b))
+        return b.value
+
+    def radial_hidden_bwd(self, r, r_cut, p_env, widths, weights, dh, dr, dweights, workspace=None, stream=None):
+        """Edge-length and layer gradients of <dh, h> (see uvu_radial_hidden_bwd)."""
+        import torch
+        wd = (ctypes.c_int * len(widths))(*[int(v) for v in widths])
+        if workspace is None:
+            workspace = torch.empty(max(16, self.radial_hidden_bwd_workspace(r.numel(), widths)), dtype=torch.uint8,
+                                    device=r.device)
+        uvu_radial_hidden_bwd(self.handle, r.numel(), _ptr(r), float(r_cut), int(p_env), len(widths) - 1, wd,
+                              _ptr(weights), _ptr(dh), _ptr(dr), _ptr(dweights), _ptr(workspace), workspace.numel(),
+                              _stream(stream))
 
     def tp_fwd(self, batch, x, y, w, out, w_shared=False, stream=None):
         """Batched tensor product (see uvu_tp_fwd)."""

@@ -134,8 +134,10 @@ uvu_status uvu_plan_module_source(uvu_plan_t plan, uvu_module module, const char
                                   const char **compile_log);
 
 /* Device-side status of the plan's kernels on the current device: bit 0 (UVU_DEV_TIMEOUT) is set
- * when a pipelined kernel gave up waiting for a shared-memory stage (about two seconds) and
- * skipped the rest of its work, so its outputs are not valid.  Synchronous: waits for all work
+ * when a pipelined kernel, or a tensor-core product kernel (channel mixing, radial last layer;
+ * their word is shared by all plans on the device), gave up waiting for a shared-memory stage or
+ * for its matrix-multiply completion (about two seconds) and skipped the rest of its work, so
+ * its outputs are not valid.  Synchronous: waits for all work
  * on the device, copies the word to *word and, if reset != 0, clears it.  Loads the plan's
  * module on the current device if needed. */
 #define UVU_DEV_TIMEOUT 1u
@@ -424,6 +426,53 @@ uvu_status uvu_conv_fwd_radial(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges
                                const void *Y, const void *h, int hidden, const void *w_last,
                                const int32_t *recv_offsets, const int32_t *src, void *out,
                                uvu_stream_t stream);
+
+/* The last linear layer of the radial network, materialised: w[e,p,u] = sum_k h[e,k] w_last[k,p,u]
+ * ("Receiver-streaming convolutions ...", replies: radial weights materialised by the network
+ * before the convolution).  h [E][hidden], w_last [hidden][P][U], w [E][P][U], device memory of the
+ * plan's type, 16-byte aligned; w is overwritten.  fp32 plans run it on the tensor cores
+ * (tcgen05, each operand split into two TF32 parts, three products per term: fp32 accuracy);
+ * fp64 plans on CUDA cores.  On GB300 this at HBM speed, followed by uvu_conv_fwd, is faster than
+ * the fused uvu_conv_fwd_radial, which forms every weight on CUDA cores; the fused form needs no
+ * memory for w.  `hidden` is a multiple of 4 in [4, 256].  Launches: 1 kernel. */
+uvu_status uvu_radial_weights(uvu_plan_t plan, int64_t n_edges, const void *h, int hidden, const void *w_last,
+                              void *w, uvu_stream_t stream);
+
+/* Gradients of the last layer for the cotangent dw [E][P][U] of w (uvu_conv_bwd's dw):
+ *     dh[e,k]         = sum_{p,u} dw[e,p,u] w_last[k,p,u]      [E][hidden]
+ *     dw_last[k,p,u]  = sum_e h[e,k] dw[e,p,u]                 [hidden][P][U]
+ * Either output may be NULL (not computed).  dh: tensor cores for fp32 plans (the K = P*U sum is
+ * split over several accumulators added in fp32 registers), CUDA cores for fp64.  dw_last, a sum
+ * over all edges, runs on CUDA cores: fp32 sums of 16 edges, Kahan-compensated, fp64 partials per
+ * 1024 edges added in order, so it is deterministic (the tensor memory's fp32 accumulation lost
+ * too much over such sums to keep the fp32 tolerance).  `workspace`: caller-owned device memory of
+ * at least uvu_radial_weights_bwd_workspace() bytes, 16-byte aligned.  n_edges == 0 sets dw_last
+ * to zero.  Launches: 1 kernel for dh (2 in fp64 plans), 2 for dw_last. */
+uvu_status uvu_radial_weights_bwd(uvu_plan_t plan, int64_t n_edges, const void *h, int hidden, const void *w_last,
+                                  const void *dw, void *dh, void *dw_last, void *workspace, size_t workspace_bytes,
+                                  uvu_stream_t stream);
+
+/* Bytes of device workspace uvu_radial_weights_bwd needs. */
+uvu_status uvu_radial_weights_bwd_workspace(uvu_plan_t plan, int64_t n_edges, int hidden, size_t *bytes);
+
+/* Reverse pass of the radial network of uvu_radial_hidden for the cotangent dh [E][widths[n]] of h:
+ *     dr[e]     = d/dr_e <dh, h>            (the edge-length gradient that forces need)
+ *     dweights  = d/dW_i <dh, h>, i = 1..n  (same layout as `weights`: W_1 .. W_n back to back)
+ * Each tile of edges recomputes the forward pass in shared memory, then applies the chain rule
+ * through the SiLU layers, the envelope and the Bessel basis.  dweights sums over all edges:
+ * compensated (Kahan) fp32 sums per block in `workspace`, added over the blocks in fp64 in block
+ * order (deterministic).  Arguments as uvu_radial_hidden; dr [E] and dweights are overwritten
+ * (edges at or beyond r_cut get dr = 0).  `workspace`: at least
+ * uvu_radial_hidden_bwd_workspace() bytes, 16-byte aligned.  UVU_ERR_UNSUPPORTED when the network's
+ * activations do not fit the block's shared memory even with 16-edge tiles.  n_edges == 0 sets
+ * dweights to zero.  Launches: 2 kernels. */
+uvu_status uvu_radial_hidden_bwd(uvu_plan_t plan, int64_t n_edges, const void *r, double r_cut, int p_env,
+                                 int n_layers, const int *widths, const void *weights, const void *dh, void *dr,
+                                 void *dweights, void *workspace, size_t workspace_bytes, uvu_stream_t stream);
+
+/* Bytes of device workspace uvu_radial_hidden_bwd needs on the current device. */
+uvu_status uvu_radial_hidden_bwd_workspace(uvu_plan_t plan, int64_t n_edges, int n_layers, const int *widths,
+                                           size_t *bytes);
 
 /* Generated source and compile log of the fused radial forward for `hidden`, built on the host
  * if it is not yet (this fixes the plan's hidden width, as a first uvu_conv_fwd_radial does).
