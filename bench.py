@@ -706,9 +706,10 @@ def main(argv=None):
         # the tensor-core path: the last layer materialised by uvu_radial_weights (3xTF32), then the
         # convolution; its VJP: uvu_conv_bwd's kernels with w, then the last layer's gradients (dh on
         # the tensor cores, dW_last on CUDA cores) and the network's reverse pass (dr, dW_i)
-        tc_w_ms = ev_mix(lambda: plan.radial_weights(hbuf, Wlast, wmat.view(E, P, U), stream=stream), reps)
+        rw_ws = torch.empty(max(16, plan.radial_weights_workspace(Hr)), dtype=torch.uint8, device=dev)
+        tc_w_ms = ev_mix(lambda: plan.radial_weights(hbuf, Wlast, wmat.view(E, P, U), workspace=rw_ws, stream=stream), reps)
         wv = wmat.view(E, P, U)
-        plan.radial_weights(hbuf, Wlast, wv, stream=stream)
+        plan.radial_weights(hbuf, Wlast, wv, workspace=rw_ws, stream=stream)
         tc_conv_ms = ev_mix(lambda: plan.fwd(N, x, Y, wv, G.recv_offsets, src, out, stream), reps)
         rdw = torch.empty_like(wv)
         rdh = torch.empty_like(hbuf)
@@ -767,7 +768,7 @@ def main(argv=None):
             "note": "alu bound: last-layer FMAs (2 E U P H flop) over the FP32 rate measured in this run; "
                     "the materialised GEMMs are cuBLAS (library), shown for comparison only"}
         assert plan.device_status() == 0
-        del rr, Wn, Wlast, hbuf, rout, wmat, rdw, rdh, rdWl, rdr, rdW, rws, rhws
+        del rr, Wn, Wlast, hbuf, rout, wmat, rdw, rdh, rdWl, rdr, rdW, rws, rhws, rw_ws
 
     # fwd and fwd+VJP (staged dx) of the other four workloads, each on its own plan and graph:
     # edges/s, GB/s of the compulsory bytes and the fraction of the HBM peak; for the fp64

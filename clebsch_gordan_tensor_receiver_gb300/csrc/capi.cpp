@@ -900,8 +900,17 @@ int sm_count_now() {
 }  // namespace
 }  // namespace uvu
 
+extern "C" uvu_status uvu_radial_weights_workspace(uvu_plan_t plan, int hidden, size_t* bytes) {
+    Plan* p = get(plan);
+    if (!p || !bytes) return fail(UVU_ERR_INVALID_ARGUMENT, "plan or bytes is NULL");
+    if (hidden < 4 || hidden > 256 || hidden % 4) return fail(UVU_ERR_INVALID_ARGUMENT, "hidden must be a multiple of 4 in [4, 256]");
+    *bytes = dense_product_workspace(hidden, p->P * p->U, p->dtype == UVU_F64);
+    return ok();
+}
+
 extern "C" uvu_status uvu_radial_weights(uvu_plan_t plan, int64_t n_edges, const void* h, int hidden,
-                                         const void* w_last, void* w, uvu_stream_t stream) {
+                                         const void* w_last, void* w, void* workspace, size_t workspace_bytes,
+                                         uvu_stream_t stream) {
     UVU_RANGE("uvu_radial_weights");
     Plan* p = get(plan);
     if (!p) return fail(UVU_ERR_INVALID_ARGUMENT, "plan is NULL");
@@ -912,7 +921,10 @@ extern "C" uvu_status uvu_radial_weights(uvu_plan_t plan, int64_t n_edges, const
     UVU_TRY(need(w_last, "w_last"));
     UVU_TRY(need(w, "w"));
     const int PU = p->P * p->U;
-    cudaError_t e = launch_dense_product(p->dtype == UVU_F64, n_edges, hidden, PU, h, w_last, false, w, nullptr,
+    if (!workspace || workspace_bytes < dense_product_workspace(hidden, PU, p->dtype == UVU_F64) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return fail(UVU_ERR_INVALID_ARGUMENT, "workspace is NULL, misaligned or smaller than uvu_radial_weights_workspace()");
+    cudaError_t e = launch_dense_product(p->dtype == UVU_F64, n_edges, hidden, PU, h, w_last, false, w, workspace,
                                          static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "radial last layer launch");
     return ok();

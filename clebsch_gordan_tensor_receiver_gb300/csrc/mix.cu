@@ -285,8 +285,10 @@ cudaError_t relayout_launch(int64_t N, int A, int B, bool inv, const void* in, v
 // The per-path products as tensor-core jobs: segment p = the rows of path p in the
 // component-major operand A [Do N][K]; B_p [K][Nc] n-contiguous, or, with b_kcont, the product
 // with B_p^T of a [Nc][K] block (k contiguous) so that M needs no transposed copy.
-TcJobs tc_product_jobs(const Plan& p, int64_t N, int K, int Nc, const float* A, const float* B, bool b_kcont, float* C) {
+TcJobs tc_product_jobs(const Plan& p, int64_t N, int K, int Nc, const float* A, const float* B, bool b_kcont, float* C,
+                       void* bpack) {
     TcJobs J{};
+    J.bpack = bpack;
     J.nseg = p.P;
     for (int i = 0; i < p.P && i < kTcMaxSeg; ++i) {
         J.row0[i] = int64_t(p.paths[i].ooff) * N;
@@ -319,9 +321,11 @@ cudaError_t mix_product(const Plan& p, int64_t N, int K, int Nc, const void* in,
     if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
     bool done = false;
     if (sizeof(T) == 4) {
-        // fp32: the per-path products on the tensor cores (3xTF32), B_p = Bmat + p K Nc
+        // fp32: the per-path products on the tensor cores (3xTF32), B_p = Bmat + p K Nc, its
+        // pre-split tiles after the two component-major copies in ws
+        void* bp = reinterpret_cast<char*>(outT) + (size_t(N) * p.Do * Nc * sizeof(T) + 255) / 256 * 256;
         TcJobs J = tc_product_jobs(p, N, K, Nc, reinterpret_cast<const float*>(inT),
-                                   reinterpret_cast<const float*>(Bmat), false, reinterpret_cast<float*>(outT));
+                                   reinterpret_cast<const float*>(Bmat), false, reinterpret_cast<float*>(outT), bp);
         if (tc_gemm_supported(J)) {
             if ((e = launch_tc_gemm(J, st)) != cudaSuccess) return e;
             done = true;
@@ -345,25 +349,33 @@ int mix_max_paths() { return kMaxPaths; }
 // (b_kcont = 1).  fp32: the tensor cores when the shapes allow; otherwise (fp64, other shapes) the
 // register-tiled CUDA-core product, which needs B as [K][Nc] (a transposed copy in `ws`,
 // K * Nc elements, for b_kcont).
+namespace {
+TcJobs dense_jobs(int64_t rows, int K, int Nc, const void* A, const void* B, bool b_kcont, void* C, void* ws) {
+    TcJobs J{};
+    J.nseg = 1;
+    J.row0[0] = 0;
+    J.rows[0] = rows;
+    J.K = K;
+    J.N = Nc;
+    J.b_kcont = b_kcont ? 1 : 0;
+    J.A = static_cast<const float*>(A);
+    J.lda = K;
+    J.B = static_cast<const float*>(B);
+    J.sbk = b_kcont ? 1 : Nc;
+    J.sbn = b_kcont ? K : 1;
+    J.b_seg_stride = 0;
+    J.C = static_cast<float*>(C);
+    J.ldc = Nc;
+    J.bpack = ws;
+    return J;
+}
+}  // namespace
+
 cudaError_t launch_dense_product(bool f64, int64_t rows, int K, int Nc, const void* A, const void* B, bool b_kcont,
                                  void* C, void* ws, cudaStream_t st) {
     if (rows <= 0 || Nc <= 0) return cudaSuccess;
     if (!f64) {
-        TcJobs J{};
-        J.nseg = 1;
-        J.row0[0] = 0;
-        J.rows[0] = rows;
-        J.K = K;
-        J.N = Nc;
-        J.b_kcont = b_kcont ? 1 : 0;
-        J.A = static_cast<const float*>(A);
-        J.lda = K;
-        J.B = static_cast<const float*>(B);
-        J.sbk = b_kcont ? 1 : Nc;
-        J.sbn = b_kcont ? K : 1;
-        J.b_seg_stride = 0;
-        J.C = static_cast<float*>(C);
-        J.ldc = Nc;
+        TcJobs J = dense_jobs(rows, K, Nc, A, B, b_kcont, C, ws);
         if (tc_gemm_supported(J)) return launch_tc_gemm(J, st);
     }
     const void* Bn = B;
@@ -390,7 +402,13 @@ cudaError_t launch_dense_product(bool f64, int64_t rows, int K, int Nc, const vo
     return cudaGetLastError();
 }
 
-size_t dense_product_workspace(int K, int Nc, bool f64) { return size_t(K) * Nc * (f64 ? 8 : 4); }
+// the tensor-core path's pre-split B tiles, or the CUDA-core path's transposed B
+size_t dense_product_workspace(int K, int Nc, bool f64) {
+    const size_t t = size_t(K) * Nc * (f64 ? 8 : 4);
+    if (f64) return t;
+    TcJobs J = dense_jobs(1, K, Nc, nullptr, nullptr, false, nullptr, nullptr);
+    return std::max(t, tc_gemm_workspace(J));
+}
 
 // C[Mr][Nc] = sum over rows of A[row][m] G[row][n]: fp32 steps of 16 rows, Kahan-compensated,
 // fp64 partials per chunk of kRowChunk rows (in `ws`) added in chunk order -- deterministic.
@@ -428,12 +446,20 @@ size_t r256(size_t b) { return (b + 255) / 256 * 256; }
 // Workspace regions (each starting on a 256-byte boundary).  Forward: [in | out] component-major.
 // Backward: [g | d_in] component-major (the input-gradient product; g alone for dM), in
 // component-major, M transposed, fp64 dM partials.
+// Pre-split M tiles of the tensor-core products (fp32 plans): forward (K = U, N = W) and input
+// gradient (K = W, N = U).
+size_t tc_pack_bytes(const Plan& p, int64_t N, int W, bool bwd) {
+    if (p.dtype != UVU_F32) return 0;
+    TcJobs J = tc_product_jobs(p, N, bwd ? W : p.U, bwd ? p.U : W, nullptr, nullptr, bwd, nullptr, nullptr);
+    return tc_gemm_workspace(J);
+}
+
 size_t mix_workspace_bytes(const Plan& p, int64_t N, int W, bool bwd) {
     const size_t s = p.elem(), ND = size_t(N) * p.Do;
     const size_t U = size_t(p.U);
-    if (!bwd) return r256(ND * U * s) + r256(ND * W * s);
+    if (!bwd) return r256(ND * U * s) + r256(ND * W * s) + r256(tc_pack_bytes(p, N, W, false));
     return r256(ND * W * s) + r256(ND * U * s) + r256(ND * U * s) + r256(size_t(p.P) * U * W * s) +
-           r256(size_t(max_chunks(p, N)) * p.P * U * W * sizeof(double));
+           r256(size_t(max_chunks(p, N)) * p.P * U * W * sizeof(double)) + r256(tc_pack_bytes(p, N, W, true));
 }
 
 cudaError_t launch_mix_fwd(const Plan& p, int64_t N, int W, const void* in, const void* M, void* out, void* ws,
@@ -460,7 +486,8 @@ cudaError_t launch_mix_bwd(const Plan& p, int64_t N, int W, const void* in, cons
         // tensor cores: d_in_p = g_p M_p^T with M read as the k-contiguous operand (no transposed copy)
         float* gT = static_cast<float*>(prod_ws);
         float* dT = reinterpret_cast<float*>(base + r256(ND * W * s));
-        TcJobs J = tc_product_jobs(p, N, W, p.U, gT, static_cast<const float*>(M), true, dT);
+        void* bp = static_cast<char*>(part) + r256(size_t(max_chunks(p, N)) * PUW * sizeof(double));
+        TcJobs J = tc_product_jobs(p, N, W, p.U, gT, static_cast<const float*>(M), true, dT, bp);
         if (tc_gemm_supported(J)) {
             if ((e = relayout_launch<float>(N, W, p.Do, false, g, gT, st)) != cudaSuccess) return e;
             if ((e = launch_tc_gemm(J, st)) != cudaSuccess) return e;

@@ -168,6 +168,7 @@ cudaError_t launch_radial_hidden_bwd(int64_t E, const void* r, double r_cut, int
 constexpr int kTcMaxSeg = 128;
 struct TcJobs;
 bool tc_gemm_supported(const TcJobs& J);
+size_t tc_gemm_workspace(const TcJobs& J);
 cudaError_t launch_tc_gemm(TcJobs& J, cudaStream_t st);
 cudaError_t tc_status(unsigned* word, bool reset);
 // mix.cu

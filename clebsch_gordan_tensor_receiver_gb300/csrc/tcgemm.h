@@ -20,6 +20,10 @@ struct TcJobs {
     long long b_seg_stride;  // offset of B_s
     float* C;
     long long ldc;           // elements between rows of C
+    // B pre-split into its hi and lo TF32 parts in the MMA's shared-memory layout, one 16-k chunk
+    // of one N tile per kTcBTile bytes: [segment][N tile][K chunk] (written by the launcher into
+    // caller workspace of tc_gemm_workspace() bytes)
+    void* bpack;
     // set by the launcher
     int bn;                  // columns per tile
     int kacc;                // K per accumulator

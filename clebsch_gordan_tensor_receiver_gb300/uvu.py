@@ -36,7 +36,7 @@ EXPORTS = (
     "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
     "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
     "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source",
-    "uvu_radial_weights", "uvu_radial_weights_bwd", "uvu_radial_weights_bwd_workspace",
+    "uvu_radial_weights", "uvu_radial_weights_workspace", "uvu_radial_weights_bwd", "uvu_radial_weights_bwd_workspace",
     "uvu_radial_hidden_bwd", "uvu_radial_hidden_bwd_workspace",
     "uvu_fma_rate_probe", "uvu_status_string", "uvu_last_error_message",
 )
@@ -89,7 +89,8 @@ def _load():
         "uvu_conv_fwd_radial": [P, I64, I64, P, P, P, I, P, P, P, P, P],
         "uvu_radial_module_source": [P, I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p)],
         "uvu_fma_rate_probe": [I, I, I, P, ctypes.POINTER(ctypes.c_double), P],
-        "uvu_radial_weights": [P, I64, P, I, P, P, P],
+        "uvu_radial_weights": [P, I64, P, I, P, P, P, SZ, P],
+        "uvu_radial_weights_workspace": [P, I, ctypes.POINTER(SZ)],
         "uvu_radial_weights_bwd": [P, I64, P, I, P, P, P, P, P, SZ, P],
         "uvu_radial_weights_bwd_workspace": [P, I64, I, ctypes.POINTER(SZ)],
         "uvu_radial_hidden_bwd": [P, I64, P, ctypes.c_double, I, I, ctypes.POINTER(I), P, P, P, P, P, SZ, P],
@@ -134,8 +135,8 @@ for _n in ("uvu_plan_destroy", "uvu_plan_info", "uvu_plan_cg", "uvu_plan_source"
            "uvu_conv_fwd_model", "uvu_conv_fwd_sender", "uvu_conv_fwd_mode",
            "uvu_mix_fwd", "uvu_mix_bwd", "uvu_mix_workspace", "uvu_conv_uvw_fwd",
            "uvu_radial_hidden", "uvu_conv_fwd_radial", "uvu_radial_module_source", "uvu_fma_rate_probe",
-           "uvu_radial_weights", "uvu_radial_weights_bwd", "uvu_radial_weights_bwd_workspace",
-           "uvu_radial_hidden_bwd", "uvu_radial_hidden_bwd_workspace"):
+           "uvu_radial_weights", "uvu_radial_weights_workspace", "uvu_radial_weights_bwd",
+           "uvu_radial_weights_bwd_workspace", "uvu_radial_hidden_bwd", "uvu_radial_hidden_bwd_workspace"):
     globals()[_n] = _wrap(_n)
 
 
@@ -253,9 +254,18 @@ class Plan:
                             int(w_last.shape[0]), _ptr(w_last), _ptr(recv_offsets), _ptr(src), _ptr(out),
                             _stream(stream))
 
-    def radial_weights(self, h, w_last, w, stream=None):
+    def radial_weights_workspace(self, hidden) -> int:
+        b = ctypes.c_size_t()
+        uvu_radial_weights_workspace(self.handle, int(hidden), ctypes.byref(b))
+        return b.value
+
+    def radial_weights(self, h, w_last, w, workspace=None, stream=None):
         """Materialised last layer w = h W_last (see uvu_radial_weights)."""
-        uvu_radial_weights(self.handle, h.shape[0], _ptr(h), int(h.shape[1]), _ptr(w_last), _ptr(w), _stream(stream))
+        import torch
+        if workspace is None:
+            workspace = torch.empty(max(16, self.radial_weights_workspace(h.shape[1])), dtype=torch.uint8, device=h.device)
+        uvu_radial_weights(self.handle, h.shape[0], _ptr(h), int(h.shape[1]), _ptr(w_last), _ptr(w), _ptr(workspace),
+                           workspace.numel(), _stream(stream))
 
     def radial_weights_bwd_workspace(self, n_edges, hidden) -> int:
         b = ctypes.c_size_t()

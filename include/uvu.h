@@ -434,9 +434,14 @@ uvu_status uvu_conv_fwd_radial(uvu_plan_t plan, int64_t n_nodes, int64_t n_edges
  * (tcgen05, each operand split into two TF32 parts, three products per term: fp32 accuracy);
  * fp64 plans on CUDA cores.  On GB300 this at HBM speed, followed by uvu_conv_fwd, is faster than
  * the fused uvu_conv_fwd_radial, which forms every weight on CUDA cores; the fused form needs no
- * memory for w.  `hidden` is a multiple of 4 in [4, 256].  Launches: 1 kernel. */
+ * memory for w.  `hidden` is a multiple of 4 in [4, 256].  `workspace`: caller-owned device
+ * memory of at least uvu_radial_weights_workspace() bytes, 16-byte aligned (w_last split into
+ * its tensor-core parts, about 4 bytes per element of w_last).  Launches: 2 kernels. */
 uvu_status uvu_radial_weights(uvu_plan_t plan, int64_t n_edges, const void *h, int hidden, const void *w_last,
-                              void *w, uvu_stream_t stream);
+                              void *w, void *workspace, size_t workspace_bytes, uvu_stream_t stream);
+
+/* Bytes of device workspace uvu_radial_weights needs. */
+uvu_status uvu_radial_weights_workspace(uvu_plan_t plan, int hidden, size_t *bytes);
 
 /* Gradients of the last layer for the cotangent dw [E][P][U] of w (uvu_conv_bwd's dw):
  *     dh[e,k]         = sum_{p,u} dw[e,p,u] w_last[k,p,u]      [E][hidden]
@@ -447,7 +452,7 @@ uvu_status uvu_radial_weights(uvu_plan_t plan, int64_t n_edges, const void *h, i
  * 1024 edges added in order, so it is deterministic (the tensor memory's fp32 accumulation lost
  * too much over such sums to keep the fp32 tolerance).  `workspace`: caller-owned device memory of
  * at least uvu_radial_weights_bwd_workspace() bytes, 16-byte aligned.  n_edges == 0 sets dw_last
- * to zero.  Launches: 1 kernel for dh (2 in fp64 plans), 2 for dw_last. */
+ * to zero.  Launches: 2 kernels for dh, 2 for dw_last. */
 uvu_status uvu_radial_weights_bwd(uvu_plan_t plan, int64_t n_edges, const void *h, int hidden, const void *w_last,
                                   const void *dw, void *dh, void *dw_last, void *workspace, size_t workspace_bytes,
                                   uvu_stream_t stream);

@@ -158,9 +158,13 @@ def test_mixing_host_checks():
     r = lambda b: (b + 255) // 256 * 256
     N, W, U, Do, P = 5000, 64, 128, 55, 13
     fwd, bwd = p.mix_workspace_bytes(N, W)
-    assert fwd == r(N * Do * U * 4) + r(N * Do * W * 4)
+    # the tensor-core products' pre-split M tiles: per path, N tile and 16-wide K chunk one
+    # 16,896-byte pair of 128 x 16 TF32 tiles (forward: K = U, N = W; input gradient: K = W, N = U)
+    tile = 2 * 16 * 528
+    assert fwd == r(N * Do * U * 4) + r(N * Do * W * 4) + r(P * 1 * (U // 16) * tile)
     chunks = (7 * N + 1023) // 1024  # widest path (l3 = 3) over 1024-row chunks
-    assert bwd == r(N * Do * W * 4) + 2 * r(N * Do * U * 4) + r(P * U * W * 4) + r(chunks * P * U * W * 8)
+    assert bwd == (r(N * Do * W * 4) + 2 * r(N * Do * U * 4) + r(P * U * W * 4) + r(chunks * P * U * W * 8) +
+                   r(P * 1 * (W // 16) * tile))
     for bad in (0, 5000):
         with pytest.raises(uvu.UVUError):
             p.mix_workspace_bytes(10, bad)
