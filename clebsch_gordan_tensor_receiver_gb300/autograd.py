@@ -79,3 +79,60 @@ def uvu_conv(x, Y, w, plan: "uvu.Plan", graph: "uvu.Graph", dx_mode: int = uvu.U
     """out = the UVU convolution of x [N][U][D_x], Y [E][D_Y], w [E][P][U] over `graph`, with
     autograd support up to second order (VJP and double backward run in the library)."""
     return _Conv.apply(_c(x), _c(Y), _c(w), plan, graph, dx_mode)
+
+
+class _RadialHidden(torch.autograd.Function):
+    """r [E] -> h [E][widths[-1]] (uvu_radial_hidden); backward = uvu_radial_hidden_bwd (dr and
+    the layers' gradients)."""
+
+    @staticmethod
+    def forward(ctx, r, weights, plan, r_cut, p_env, widths):
+        h = torch.empty(r.numel(), widths[-1], dtype=r.dtype, device=r.device)
+        plan.radial_hidden(r, r_cut, p_env, widths, weights, h)
+        ctx.save_for_backward(r, weights)
+        ctx.plan, ctx.r_cut, ctx.p_env, ctx.widths = plan, r_cut, p_env, widths
+        return h
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, dh):
+        r, weights = ctx.saved_tensors
+        dr = torch.empty_like(r)
+        dW = torch.empty_like(weights)
+        ctx.plan.radial_hidden_bwd(r, ctx.r_cut, ctx.p_env, ctx.widths, weights, _c(dh), dr, dW)
+        return dr, dW, None, None, None, None
+
+
+class _RadialWeights(torch.autograd.Function):
+    """(h, W_last) -> w = h W_last (uvu_radial_weights); backward = uvu_radial_weights_bwd."""
+
+    @staticmethod
+    def forward(ctx, h, w_last, plan):
+        i = plan.info
+        w = torch.empty(h.shape[0], i.n_paths, i.mul, dtype=h.dtype, device=h.device)
+        plan.radial_weights(h, w_last, w)
+        ctx.save_for_backward(h, w_last)
+        ctx.plan = plan
+        return w
+
+    @staticmethod
+    @once_differentiable
+    def backward(ctx, dw):
+        h, w_last = ctx.saved_tensors
+        need = ctx.needs_input_grad
+        dh = torch.empty_like(h) if need[0] else None
+        dwl = torch.empty_like(w_last) if need[1] else None
+        ctx.plan.radial_weights_bwd(h, w_last, _c(dw), dh=dh, dw_last=dwl)
+        return dh, dwl, None
+
+
+def radial_conv(r, x, Y, weights, w_last, plan: "uvu.Plan", graph: "uvu.Graph", r_cut: float, p_env: int,
+                widths, dx_mode: int = uvu.UVU_DX_STAGED):
+    """The convolution with radial weights from edge lengths r [E]: h = uvu_radial_hidden(r) (the
+    SiLU network, layers back to back in `weights`), w = h W_last (materialised on the tensor
+    cores), out = uvu_conv(x, Y, w).  First derivatives with respect to r (forces), x, Y, the
+    layers and W_last run in the library; second derivatives through the radial network are not
+    provided."""
+    h = _RadialHidden.apply(_c(r), _c(weights), plan, float(r_cut), int(p_env), [int(v) for v in widths])
+    w = _RadialWeights.apply(h, _c(w_last), plan)
+    return uvu_conv(x, Y, w, plan, graph, dx_mode)

@@ -83,8 +83,16 @@ struct Gen {
     // dw of a path: stored per edge (dwe[p * U]) or, for weights shared by a whole batch,
     // accumulated in the thread's registers (dwa_p) over the samples it processes
     mutable bool dw_accum = false;
+    // Set while emitting the plain edge kernel with a wide output row: the x (x) y products of an
+    // (x irrep, SH irrep) pair are formed inside that pair's block, just before its paths use
+    // them, instead of all at once before the paths (fewer values live at a time).
+    mutable bool local_products = false;
+    // guard_dw: the store is skipped when dw is NULL (the one-pass emission computes dw with the
+    // rest of the path instead of in a block of its own under that condition)
+    mutable bool guard_dw = false;
     std::string dw_store(int pi, const std::string& v) const {
-        return dw_accum ? fmt("dwa_%d += %s;", pi, v.c_str()) : fmt("dwe[%d * UVU_U] = %s;", pi, v.c_str());
+        if (dw_accum) return fmt("dwa_%d += %s;", pi, v.c_str());
+        return fmt("%sdwe[%d * UVU_U] = %s;", guard_dw ? "if (dw) " : "", pi, v.c_str());
     }
 
     bool is_identity(const PathInfo& p) const {
@@ -347,6 +355,7 @@ struct Gen {
             const int d1 = 2 * p0.l1 + 1, d2 = 2 * p0.l2 + 1;
             S("{");
             S.ind++;
+            if (local_products && want_dw) emit_products(S, pp);
             std::set<std::pair<int, int>> hdef;
             for (int pi : pp) {
                 const PathInfo& p = P->paths[pi];
@@ -900,6 +909,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         int odp = 0;  // row stride (elements) of the staged output block, 0 = not staged
         bool ovec = false;  // staged block copied out with 16-byte vectors
         bool gst = false;  // the receiver's d_out block is bulk-copied into shared memory
+        // gsm (with gst, plain edge kernel): each d_out value is read from the staged block where
+        // it is used, and the block is released when the receiver is done, instead of the row
+        // being copied into registers at the receiver start (frees D_out registers per thread)
+        bool gsm = false;
         bool dual = false;  // double backward: the stage also holds the cotangent rows aw, ax, aY
         bool tp = false;    // batched tensor product: sample b is receiver b with the one edge b, sender b
         bool wsh = false;   // weights [P][U] shared by the batch: not staged, read once per sample
@@ -1383,7 +1396,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 for (int pi : paths) dwa += fmt(", %s& dwa_%d", T.c_str(), pi);
             S(fmt("    %s* __restrict__ dxe, int g, const %s* __restrict__ w%s) {", T.c_str(), T.c_str(), dwa.c_str()));
             S.ind++;
-            if (R.gst) {
+            if (R.gst && R.gsm) {
+                // d_out row of this channel read from the receiver's staged block at each use
+                S(fmt("const %s* grow = reinterpret_cast<const %s*>(smem + EG_GBUF) + (uvalid ? u : 0) * UVU_DO;", T.c_str(), T.c_str()));
+                S("if (e1 > e0 && !dead) dead = !__all_sync(0xffffffffu, mbar_wait(sbase + EG_GBAR, kg & 1u));");
+            } else if (R.gst) {
                 // d_out row of this channel from the receiver's staged block; the block buffer
                 // is handed back to the producer as soon as the row is in registers
                 for (int k : outs) S(fmt("%s gv_%d = 0;", T.c_str(), k));
@@ -1428,7 +1445,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             emit_stage_edge_loads(S, R, "EG", xn, yn, paths);
             if (!R.wsh) S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
             for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
-            auto gval = [](int k) { return fmt("gv_%d", k); };
+            auto gval = [&R](int k) { return R.gsm ? fmt("grow[%d]", k) : fmt("gv_%d", k); };
             if (R.dual) {
                 // dw(x<-ax) + dw(Y<-aY) through the mixed products; dY(x<-ax) and dx(Y<-aY) with
                 // w; dY and dx with w<-aw
@@ -1440,6 +1457,15 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 S("}");
                 emit_bwd_pairs(S, paths, false, true, true, gval, "axv", "ayv", "wv");
                 emit_bwd_pairs(S, paths, false, true, true, gval, "xv", "yv", "awv");
+            } else if (R.gsm) {
+                // one pass per (x irrep, SH irrep) pair: its products, then per path dw, a = w g and
+                // h, then the pair's dY / dx contraction, so each d_out value is read and used within
+                // its path's block
+                local_products = true;
+                guard_dw = true;
+                emit_bwd_pairs(S, paths, true, true, true, gval);
+                local_products = false;
+                guard_dw = false;
             } else {
                 emit_products(S, paths);
                 S("if (dw) {");
@@ -1546,6 +1572,21 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("buf ^= 1;");
             S.ind--;
             S("}");
+            if (R.gst && R.gsm) {  // the receiver is done: its d_out block goes back to the producer
+                S("if (e1 > e0) {");
+                S.ind++;
+                S("if (!dead) {");
+                S.ind++;
+                if (release_mode() != 3) S("__threadfence_block();");
+                S("asm volatile(\"fence.proxy.async.shared::cta;\" ::: \"memory\");");
+                S("__syncwarp();");
+                S(std::string("if (") + (release_mode() == 1 ? "true" : "lane == 0") + ") mbar_arrive(sbase + EG_GBAR + 8u);");
+                S.ind--;
+                S("}");
+                S("++kg;");
+                S.ind--;
+                S("}");
+            }
             S.ind--;
             S("}");
             }
@@ -2191,6 +2232,16 @@ std::string emit_source(Plan* plan) {
     // UVU_PIPE_GSTAGE=0 (a tuning switch) reads the edge kernel's d_out rows straight from global memory.
     const bool gstage = !(std::getenv("UVU_PIPE_GSTAGE") && std::atoi(std::getenv("UVU_PIPE_GSTAGE")) == 0);
     Gen::RecvPipe RF = G.fwd_pipe(ncw, plan->minb[0], ostage), RE = G.recv_pipe(true, ncw, false, 0, gstage);
+    // Edge kernel: with a wide d_out row (fp32, D_out > 64) the row is read from the staged block
+    // at each use rather than held in registers, and each (x irrep, SH irrep) pair is emitted in
+    // one pass (MACE-large: 255 -> 168 registers, two resident blocks instead of one, edge kernel
+    // 2.64 -> 2.53 ms; wide: spills gone, 5.85 -> 5.66 ms; measured slower on MACE-medium, 0.82 ->
+    // 0.89 ms, and on the fp64 workload).  UVU_PIPE_GSMEM=1/0 (a tuning switch) forces it on or off.
+    {
+        bool gsm = plan->Do > 64 && plan->dtype == UVU_F32;
+        if (const char* e = std::getenv("UVU_PIPE_GSMEM")) gsm = std::atoi(e) != 0;
+        RE.gsm = RE.gst && !RE.lastwarp && gsm;
+    }
     Gen::SendPipe SD = G.send_pipe();
     const bool pipe_dx = !force_direct && U >= 32 && G.send_pipe_ok(SD);
     plan->pipelined_recv = pipe_recv;
