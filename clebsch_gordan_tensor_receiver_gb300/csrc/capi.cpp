@@ -925,7 +925,7 @@ extern "C" uvu_status uvu_radial_weights(uvu_plan_t plan, int64_t n_edges, const
         (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return fail(UVU_ERR_INVALID_ARGUMENT, "workspace is NULL, misaligned or smaller than uvu_radial_weights_workspace()");
     cudaError_t e = launch_dense_product(p->dtype == UVU_F64, n_edges, hidden, PU, h, w_last, false, w, workspace,
-                                         static_cast<cudaStream_t>(stream));
+                                         workspace_bytes, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "radial last layer launch");
     return ok();
 }
@@ -936,7 +936,8 @@ extern "C" uvu_status uvu_radial_weights_bwd_workspace(uvu_plan_t plan, int64_t 
     UVU_TRY(check_sizes(0, n_edges));
     if (hidden < 4 || hidden > 256 || hidden % 4) return fail(UVU_ERR_INVALID_ARGUMENT, "hidden must be a multiple of 4 in [4, 256]");
     const int PU = p->P * p->U;
-    const size_t a = (dense_product_workspace(hidden, PU, p->dtype == UVU_F64) + 255) / 256 * 256;
+    // dh = dw W_last^T is the product with K = P U and N = hidden (the forward's transpose)
+    const size_t a = (dense_product_workspace(PU, hidden, p->dtype == UVU_F64) + 255) / 256 * 256;
     *bytes = a + dense_reduction_workspace(n_edges, hidden, PU);
     return ok();
 }
@@ -970,9 +971,9 @@ extern "C" uvu_status uvu_radial_weights_bwd(uvu_plan_t plan, int64_t n_edges, c
     if (!workspace || workspace_bytes < need_bytes || (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return fail(UVU_ERR_INVALID_ARGUMENT, "workspace is NULL, misaligned or smaller than uvu_radial_weights_bwd_workspace()");
     char* ws = static_cast<char*>(workspace);
-    const size_t a = (dense_product_workspace(hidden, PU, f64) + 255) / 256 * 256;
+    const size_t a = (dense_product_workspace(PU, hidden, f64) + 255) / 256 * 256;
     cudaError_t e = cudaSuccess;
-    if (dh) e = launch_dense_product(f64, n_edges, PU, hidden, dw, w_last, true, dh, ws, st);
+    if (dh) e = launch_dense_product(f64, n_edges, PU, hidden, dw, w_last, true, dh, ws, a, st);
     if (e == cudaSuccess && dw_last) e = launch_dense_reduction(f64, n_edges, hidden, PU, h, dw, dw_last, ws + a, st);
     if (e != cudaSuccess) return cuda_fail(e, "radial last-layer gradient launch");
     return ok();

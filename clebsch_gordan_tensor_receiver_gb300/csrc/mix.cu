@@ -286,9 +286,10 @@ cudaError_t relayout_launch(int64_t N, int A, int B, bool inv, const void* in, v
 // component-major operand A [Do N][K]; B_p [K][Nc] n-contiguous, or, with b_kcont, the product
 // with B_p^T of a [Nc][K] block (k contiguous) so that M needs no transposed copy.
 TcJobs tc_product_jobs(const Plan& p, int64_t N, int K, int Nc, const float* A, const float* B, bool b_kcont, float* C,
-                       void* bpack) {
+                       void* bpack, size_t bpack_bytes) {
     TcJobs J{};
     J.bpack = bpack;
+    J.bpack_bytes = bpack_bytes;
     J.nseg = p.P;
     for (int i = 0; i < p.P && i < kTcMaxSeg; ++i) {
         J.row0[i] = int64_t(p.paths[i].ooff) * N;
@@ -308,10 +309,11 @@ TcJobs tc_product_jobs(const Plan& p, int64_t N, int K, int Nc, const float* A, 
     return J;
 }
 
-// in [N][K][Do] -> out [N][Nc][Do] through component-major copies in ws: [Do N K] then [Do N Nc]
+// in [N][K][Do] -> out [N][Nc][Do] through component-major copies in ws: [Do N K] then [Do N Nc],
+// then bp_bytes of room for the tensor-core path's pre-split B (0: CUDA cores only)
 template <typename T>
 cudaError_t mix_product(const Plan& p, int64_t N, int K, int Nc, const void* in, const void* Bmat, void* out,
-                        void* ws, cudaStream_t st) {
+                        void* ws, size_t bp_bytes, cudaStream_t st) {
     T* inT = static_cast<T*>(ws);
     T* outT = reinterpret_cast<T*>(static_cast<char*>(ws) + (size_t(N) * p.Do * K * sizeof(T) + 255) / 256 * 256);
     cudaError_t e = relayout_launch<T>(N, K, p.Do, false, in, inT, st);
@@ -320,12 +322,13 @@ cudaError_t mix_product(const Plan& p, int64_t N, int K, int Nc, const void* in,
     const SegTab tab = make_seg(p, N, &tiles);
     if (tiles > INT32_MAX) return cudaErrorInvalidConfiguration;
     bool done = false;
-    if (sizeof(T) == 4) {
+    if (sizeof(T) == 4 && bp_bytes) {
         // fp32: the per-path products on the tensor cores (3xTF32), B_p = Bmat + p K Nc, its
         // pre-split tiles after the two component-major copies in ws
         void* bp = reinterpret_cast<char*>(outT) + (size_t(N) * p.Do * Nc * sizeof(T) + 255) / 256 * 256;
         TcJobs J = tc_product_jobs(p, N, K, Nc, reinterpret_cast<const float*>(inT),
-                                   reinterpret_cast<const float*>(Bmat), false, reinterpret_cast<float*>(outT), bp);
+                                   reinterpret_cast<const float*>(Bmat), false, reinterpret_cast<float*>(outT), bp,
+                                   bp_bytes);
         if (tc_gemm_supported(J)) {
             if ((e = launch_tc_gemm(J, st)) != cudaSuccess) return e;
             done = true;
@@ -350,7 +353,8 @@ int mix_max_paths() { return kMaxPaths; }
 // register-tiled CUDA-core product, which needs B as [K][Nc] (a transposed copy in `ws`,
 // K * Nc elements, for b_kcont).
 namespace {
-TcJobs dense_jobs(int64_t rows, int K, int Nc, const void* A, const void* B, bool b_kcont, void* C, void* ws) {
+TcJobs dense_jobs(int64_t rows, int K, int Nc, const void* A, const void* B, bool b_kcont, void* C, void* ws,
+                  size_t ws_bytes) {
     TcJobs J{};
     J.nseg = 1;
     J.row0[0] = 0;
@@ -367,15 +371,17 @@ TcJobs dense_jobs(int64_t rows, int K, int Nc, const void* A, const void* B, boo
     J.C = static_cast<float*>(C);
     J.ldc = Nc;
     J.bpack = ws;
+    J.bpack_bytes = ws_bytes;
     return J;
 }
 }  // namespace
 
 cudaError_t launch_dense_product(bool f64, int64_t rows, int K, int Nc, const void* A, const void* B, bool b_kcont,
-                                 void* C, void* ws, cudaStream_t st) {
+                                 void* C, void* ws, size_t ws_bytes, cudaStream_t st) {
     if (rows <= 0 || Nc <= 0) return cudaSuccess;
+    if (ws_bytes < dense_product_workspace(K, Nc, f64)) return cudaErrorInvalidValue;
     if (!f64) {
-        TcJobs J = dense_jobs(rows, K, Nc, A, B, b_kcont, C, ws);
+        TcJobs J = dense_jobs(rows, K, Nc, A, B, b_kcont, C, ws, ws_bytes);
         if (tc_gemm_supported(J)) return launch_tc_gemm(J, st);
     }
     const void* Bn = B;
@@ -406,7 +412,7 @@ cudaError_t launch_dense_product(bool f64, int64_t rows, int K, int Nc, const vo
 size_t dense_product_workspace(int K, int Nc, bool f64) {
     const size_t t = size_t(K) * Nc * (f64 ? 8 : 4);
     if (f64) return t;
-    TcJobs J = dense_jobs(1, K, Nc, nullptr, nullptr, false, nullptr, nullptr);
+    TcJobs J = dense_jobs(1, K, Nc, nullptr, nullptr, false, nullptr, nullptr, 0);
     return std::max(t, tc_gemm_workspace(J));
 }
 
@@ -450,7 +456,7 @@ size_t r256(size_t b) { return (b + 255) / 256 * 256; }
 // gradient (K = W, N = U).
 size_t tc_pack_bytes(const Plan& p, int64_t N, int W, bool bwd) {
     if (p.dtype != UVU_F32) return 0;
-    TcJobs J = tc_product_jobs(p, N, bwd ? W : p.U, bwd ? p.U : W, nullptr, nullptr, bwd, nullptr, nullptr);
+    TcJobs J = tc_product_jobs(p, N, bwd ? W : p.U, bwd ? p.U : W, nullptr, nullptr, bwd, nullptr, nullptr, 0);
     return tc_gemm_workspace(J);
 }
 
@@ -465,8 +471,8 @@ size_t mix_workspace_bytes(const Plan& p, int64_t N, int W, bool bwd) {
 cudaError_t launch_mix_fwd(const Plan& p, int64_t N, int W, const void* in, const void* M, void* out, void* ws,
                            cudaStream_t st) {
     if (N == 0) return cudaSuccess;
-    return p.dtype == UVU_F64 ? mix_product<double>(p, N, p.U, W, in, M, out, ws, st)
-                              : mix_product<float>(p, N, p.U, W, in, M, out, ws, st);
+    return p.dtype == UVU_F64 ? mix_product<double>(p, N, p.U, W, in, M, out, ws, 0, st)
+                              : mix_product<float>(p, N, p.U, W, in, M, out, ws, tc_pack_bytes(p, N, W, false), st);
 }
 
 cudaError_t launch_mix_bwd(const Plan& p, int64_t N, int W, const void* in, const void* M, const void* g, void* d_in,
@@ -487,7 +493,7 @@ cudaError_t launch_mix_bwd(const Plan& p, int64_t N, int W, const void* in, cons
         float* gT = static_cast<float*>(prod_ws);
         float* dT = reinterpret_cast<float*>(base + r256(ND * W * s));
         void* bp = static_cast<char*>(part) + r256(size_t(max_chunks(p, N)) * PUW * sizeof(double));
-        TcJobs J = tc_product_jobs(p, N, W, p.U, gT, static_cast<const float*>(M), true, dT, bp);
+        TcJobs J = tc_product_jobs(p, N, W, p.U, gT, static_cast<const float*>(M), true, dT, bp, tc_pack_bytes(p, N, W, true));
         if (tc_gemm_supported(J)) {
             if ((e = relayout_launch<float>(N, W, p.Do, false, g, gT, st)) != cudaSuccess) return e;
             if ((e = launch_tc_gemm(J, st)) != cudaSuccess) return e;
@@ -500,8 +506,8 @@ cudaError_t launch_mix_bwd(const Plan& p, int64_t N, int W, const void* in, cons
         if (f64) transpose_M<double><<<nb, 256, 0, st>>>(p.P, p.U, W, static_cast<const double*>(M), static_cast<double*>(Mt));
         else transpose_M<float><<<nb, 256, 0, st>>>(p.P, p.U, W, static_cast<const float*>(M), static_cast<float*>(Mt));
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        e = f64 ? mix_product<double>(p, N, W, p.U, g, Mt, d_in, prod_ws, st)
-                : mix_product<float>(p, N, W, p.U, g, Mt, d_in, prod_ws, st);
+        e = f64 ? mix_product<double>(p, N, W, p.U, g, Mt, d_in, prod_ws, 0, st)
+                : mix_product<float>(p, N, W, p.U, g, Mt, d_in, prod_ws, 0, st);
         if (e != cudaSuccess) return e;
     }
     if (dM) {

@@ -173,7 +173,7 @@ cudaError_t launch_tc_gemm(TcJobs& J, cudaStream_t st);
 cudaError_t tc_status(unsigned* word, bool reset);
 // mix.cu
 cudaError_t launch_dense_product(bool f64, int64_t rows, int K, int Nc, const void* A, const void* B, bool b_kcont,
-                                 void* C, void* ws, cudaStream_t st);
+                                 void* C, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t dense_product_workspace(int K, int Nc, bool f64);
 size_t dense_reduction_workspace(int64_t rows, int Mr, int Nc);
 cudaError_t launch_dense_reduction(bool f64, int64_t rows, int Mr, int Nc, const void* A, const void* G, void* C, void* ws,

@@ -474,7 +474,7 @@ bool tc_gemm_supported(const TcJobs& J) {
         return false;
     if (J.K < 1 || J.K % 4 || J.lda % 4 || J.ldc % 4 || J.b_seg_stride % 4) return false;
     TcJobs T = J;
-    return tc_gemm_configure(T);
+    return tc_gemm_configure(T) && tc_gemm_workspace(T) <= J.bpack_bytes;
 }
 
 size_t tc_gemm_workspace(const TcJobs& J) {
@@ -493,7 +493,7 @@ cudaError_t launch_tc_gemm(TcJobs& J, cudaStream_t st) {
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    if (!tc_gemm_configure(J)) return cudaErrorInvalidValue;
+    if (!tc_gemm_configure(J) || tc_gemm_workspace(J) > J.bpack_bytes) return cudaErrorInvalidValue;
     long long t = 0;
     for (int s = 0; s < J.nseg; ++s) {
         J.tile0[s] = int(t);

@@ -24,6 +24,7 @@ struct TcJobs {
     // of one N tile per kTcBTile bytes: [segment][N tile][K chunk] (written by the launcher into
     // caller workspace of tc_gemm_workspace() bytes)
     void* bpack;
+    size_t bpack_bytes;      // room at bpack (the launcher refuses less than tc_gemm_workspace())
     // set by the launcher
     int bn;                  // columns per tile
     int kacc;                // K per accumulator

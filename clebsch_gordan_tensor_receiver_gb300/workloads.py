@@ -180,7 +180,7 @@ class Workload:
 
     @property
     def n_nodes(self) -> int:
-        return self.spec.n_nodes
+        return int(self.x.shape[0])
 
     @property
     def n_edges(self) -> int:

@@ -59,3 +59,12 @@ def test_radial_inputs_recipe():
     assert [W.shape for W in layers] == [(8, 64), (64, 64), (64, 64)] and wl.shape == (64, 13, 128)
     assert abs(layers[1].astype(np.float64).var() * 64 - 1.0) < 0.1
     assert abs(wl.astype(np.float64).var() * 64 * 56 - 1.0) < 0.05
+
+
+def test_reduced_node_count():
+    """A workload generated at fewer nodes than its recipe's default reports that count, and its
+    graph and inputs stay inside it (the reduced sizes used for small profiling runs)."""
+    from clebsch_gordan_tensor_receiver_gb300 import workloads
+    wl = workloads.make_workload(1, 300)
+    assert wl.n_nodes == 300 and wl.x.shape[0] == 300
+    assert wl.recv.max() < 300 and wl.src.max() < 300 and wl.n_edges == 300 * 56
