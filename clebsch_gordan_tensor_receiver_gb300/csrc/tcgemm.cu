@@ -1,35 +1,44 @@
 // Dense fp32 products on the 5th-generation tensor cores (tcgen05) with fp32 accuracy.
 //
 // The dense contractions next to the convolution -- the channel mixing that reduces a factorised
-// UVW convolution to the UVU one, and the last linear layer of the radial network (with its two
-// gradients) -- are ordinary matrix products.  A single TF32 product keeps 11 significant bits,
-// far outside the fp32 tolerance, so each operand is split as x = hi + lo with hi = x rounded to
-// TF32 and lo = (x - hi) rounded to TF32 (|lo| <= 2^-11 |x|, so hi + lo holds x to about 2^-22),
-// and the product is accumulated as hi*hi + hi*lo + lo*hi ("3xTF32"; the dropped lo*lo term is
-// below 2^-22 of each product).  Accumulation is fp32 in tensor memory.
+// UVW convolution to the UVU one, and the last linear layer of the radial network (with its
+// input gradient) -- are ordinary matrix products.  A single TF32 product keeps 11 significant
+// bits, far outside the fp32 tolerance, so each operand is split as x = hi + lo (hi = x rounded to
+// TF32, lo = x - hi rounded to TF32) and the product is accumulated as hi*hi + hi*lo + lo*hi
+// ("3xTF32"; the dropped lo*lo term and the rounding of lo are about 2^-22 of each product; a
+// split that truncated hi instead leaves a 13-bit lo whose truncation costs 2^-20 per product,
+// which long reductions visibly accumulate).  Accumulation is fp32 in tensor memory.
 //
-// Persistent kernel, one CTA per SM looping over 128 x BN tiles of C (BN = 128, or 64 when N <= 64
-// or K spans several ranges), with warp roles.  Eight producer warps load 16-wide K chunks of A
-// and B from global memory (three chunks in flight per thread), split them and store the hi and
-// lo parts into a ring of four shared-memory stages in the canonical K-major no-swizzle layout of
-// the MMA (8-row x 16-byte core matrices); one thread of a ninth warp issues the MMAs (M = 128,
-// N = BN, K = 8 per instruction) into one of two tensor-memory accumulators and commits each
-// stage back to its producers; four epilogue warps read the finished accumulator with
-// tcgen05.ld (one tile row per thread) and store it while the MMAs fill the other one.
+// Persistent kernel, one CTA per SM looping over 128 x BN tiles of C (BN = 128 for wide C, else 64),
+// with warp roles:
+//   warp 0      A producer: one TMA load per 32-wide K chunk of a 128-row tile (raw fp32, 128-byte
+//               swizzled K-major rows) into a ring of A stages;
+//   warp 1      B producer: B is pre-split once per call into hi and lo tiles in the MMA's layout
+//               (tc_pack_b); one bulk copy per chunk into a ring of B stages, skipped when the
+//               stage already holds that tile (a CTA keeps its N tile across row tiles, and a
+//               short K fits the ring, so small B stays resident);
+//   warp 2      MMA issue (one thread): M = 128, N = BN, K = 8 per instruction, three products per
+//               K step, into one of two tensor-memory accumulators;
+//   warps 4-7   epilogue: tcgen05.ld (one tile row per thread), fp32 sums of the K ranges in
+//               registers, rows staged in shared memory and stored 128 bytes at a time;
+//   warps 8-11  converters: thread = tile row; its 32 raw values of the chunk, split into hi and
+//               lo, written into tensor memory (tcgen05.st) as the A operand of the MMAs.
 // Measured on GB300: an accumulation in tensor memory loses more than a round-to-nearest fp32
 // add (a 35,000-term reduction was off by 3e-3 where fp32 sums in registers stay near 1e-4), so
 // long K is summed in ranges of at most 256, each accumulated afresh and added into fp32
-// registers by the epilogue, and sums over tens of thousands of rows are left to compensated
-// CUDA-core kernels.  Every mbarrier wait is bounded (about two seconds on the global timer); on
-// expiry the role sets a shared flag and the tc_status_word bit, every role leaves its loop, and
-// the CTA frees its tensor memory and returns.
+// registers by the epilogue.  Every mbarrier wait is bounded (about two seconds on the global
+// timer); on expiry the role sets a shared flag and the tc_status_word bit, every role leaves its
+// loop, the producers wait (bounded) for the copies they issued, the MMA thread for its issued
+// MMAs, and the CTA frees its tensor memory and returns.
 //
 //   C[row][n] = sum_k A[row][k] B_s[k][n] over the rows of each segment s (A row-major, K
 //   contiguous; B_s = B + s * b_seg_stride, either n- or k-contiguous).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "plan.h"
 #include "tcgemm.h"
@@ -37,11 +46,14 @@
 namespace uvu {
 namespace {
 
-constexpr int kBM = 128, kBNmax = 128, kBK = 16;
-constexpr int kSBO = 528;                       // bytes between 8-row core-matrix groups (512 + 16)
-constexpr int kTileBytes = 16 * kSBO;           // one 128-row x 16-k operand tile
-constexpr int kStageBytes = 4 * kTileBytes;     // A hi, A lo, B hi, B lo
-constexpr int kTcBTile = 2 * kTileBytes;        // a pre-split B chunk: hi tile, then lo tile
+constexpr int kBM = 128, kBNmax = 128, kBK = 32;
+constexpr int kRawBytes = kBM * kBK * 4;  // one raw A chunk: 128 rows x 128 bytes
+constexpr int kKacc = 256;                // longest K accumulated in tensor memory at once
+constexpr int kThreadsP = 12 * 32;
+constexpr int kStgPitch = 36;                      // floats per staged row (32 + 4 pad)
+constexpr int kStgBytes = 4 * 32 * kStgPitch * 4;  // four epilogue warps x 32 rows
+constexpr int kSmemMax = 232448;                   // 227 KB per CTA
+constexpr int kBarBytes = 512;  // up to 41 barriers (raw 8, A 6, B 4 stages), 8 bytes each
 
 __device__ unsigned int tc_status_word;
 
@@ -52,21 +64,20 @@ __device__ __forceinline__ uint32_t tf32_rna(float x) {
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return r;
 }
-// x = hi + lo, both representable in TF32
-__device__ __forceinline__ void split3(float x, uint32_t& hi, uint32_t& lo) {
-    hi = tf32_rna(x);
-    lo = tf32_rna(x - __uint_as_float(hi));
+
+// Byte offset of element (row, k), k < 32, in a 128-byte-swizzled K-major tile: 8-row groups of
+// 1024 bytes, 128 bytes per row, the 16-byte chunk index XORed with the row within the group
+// (the layout a TMA load with 128-byte swizzle writes, and the MMA's SWIZZLE_128B operand form).
+__device__ __forceinline__ uint32_t sw128(int row, int k) {
+    return uint32_t((row >> 3) * 1024 + (row & 7) * 128 + ((((k >> 2) ^ row) & 7) << 4) + (k & 3) * 4);
 }
 
-// byte offset of element (row, k) of an operand tile in the K-major no-swizzle layout
-__device__ __forceinline__ uint32_t toff(int row, int k) {
-    return uint32_t((row >> 3) * kSBO + (k >> 2) * 128 + (row & 7) * 16 + (k & 3) * 4);
-}
-
-// Shared-memory matrix descriptor: start address, leading (K-direction) core-matrix stride 128 B,
-// stride (8-row group) 528 B, fixed version bits 0b001 at 46, no swizzle.
+// Shared-memory matrix descriptor, K-major with 128-byte swizzle: start address, leading offset
+// unused (1), stride between 8-row groups 1024 bytes, fixed version bits 0b001 at 46, swizzle
+// mode 2 (128 bytes) at 61.  Advancing K by 8 TF32 values adds 32 bytes to the start address.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
-    return uint64_t((addr >> 4) & 0x3FFFu) | (uint64_t(128 >> 4) << 16) | (uint64_t(kSBO >> 4) << 32) | (1ull << 46);
+    return uint64_t((addr >> 4) & 0x3FFFu) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
 }
 
 // Instruction descriptor of kind::tf32: D fp32, A and B TF32, both K-major, M = 128, N = bn.
@@ -109,66 +120,21 @@ __device__ __noinline__ bool mbar_wait(uint32_t b, uint32_t parity) {
         }
     }
 }
-
-
-}  // namespace
-
-namespace {
-
-// Loads of one 16-wide K chunk of A into registers: two 16-byte vectors per thread (masked
-// entries read as zero).
-struct Chunk {
-    float4 a[2];
-};
-
-__device__ __forceinline__ float4 ld4(const float* p, bool ok) {
-    return ok ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-// four consecutive k of one row, as hi and lo TF32 parts, one 16-byte store each
-__device__ __forceinline__ void store_k4(unsigned char* tile_hi, unsigned char* tile_lo, int row, int k, float4 v) {
-    uint32_t h0, l0, h1, l1, h2, l2, h3, l3;
-    split3(v.x, h0, l0);
-    split3(v.y, h1, l1);
-    split3(v.z, h2, l2);
-    split3(v.w, h3, l3);
-    const uint32_t o = toff(row, k);
-    *reinterpret_cast<uint4*>(tile_hi + o) = make_uint4(h0, h1, h2, h3);
-    *reinterpret_cast<uint4*>(tile_lo + o) = make_uint4(l0, l1, l2, l3);
-}
-
-// Warp roles of the persistent kernel (13 warps): 0-7 load and split the operand chunks into the
-// stage ring; 8-11 drain the accumulators (warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. one
-// row of the tile per thread); 12 issues the MMAs (one thread).
-constexpr int kProdWarps = 8, kEpiWarp0 = 8, kMmaWarp = 12;
-constexpr int kThreadsP = 13 * 32;
-constexpr int kStages = 4;
-constexpr int kStagesBytes = kStages * kStageBytes;
-// barriers after the stages: full[kStages], empty[kStages], accfull[2], accempty[2], tmem slot
-constexpr int kBarFull = kStagesBytes, kBarEmpty = kBarFull + 8 * kStages, kBarAccF = kBarEmpty + 8 * kStages,
-              kBarAccE = kBarAccF + 16, kTslot = kBarAccE + 16;
-// output staging of the epilogue warps: 32 rows x (BN + 4) floats each (the pad keeps the rows'
-// 16-byte writes in distinct banks); rows leave as one bulk copy each
-constexpr int kStgPitch = kBNmax + 4;
-constexpr int kStage0 = (kTslot + 16 + 127) / 128 * 128;
-constexpr int kSmemP = kStage0 + 4 * 32 * kStgPitch * 4;
-
 __device__ __forceinline__ void mbar_init_n(uint32_t b, uint32_t n) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(n) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive1(uint32_t b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
 }
-__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void mbar_expect_tx_only(uint32_t b, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -178,35 +144,101 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 __device__ __forceinline__ void tc_commit(uint32_t b) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(b) : "memory");
 }
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__global__ void __maxnreg__(128) tc_gemm_kernel(TcJobs J) {  // 13 warps: 4 share one SM sub-partition's 16K registers
-    extern __shared__ __align__(1024) unsigned char smem[];
+// Shared-memory layout of one launch (offsets from the 1024-aligned base): nraw raw A stages (TMA
+// destinations), nb B stages (hi, lo), the epilogue staging rows, the barriers.  Tensor memory:
+// two accumulators of bn columns, then na A stages of 64 columns (hi in the first 32, lo in the
+// next 32; lane = tile row, column = k).
+struct Layout {
+    int bn, nraw, nb;
+    __host__ __device__ int b_bytes() const { return 2 * bn * 128; }
+    __host__ __device__ int b0() const { return nraw * kRawBytes; }
+    __host__ __device__ int stg0() const { return b0() + nb * b_bytes(); }
+    __host__ __device__ int bar0() const { return stg0() + kStgBytes; }
+    __host__ __device__ int total() const { return bar0() + kBarBytes + 1024; }  // + alignment slack
+};
+
+// Warp roles
+constexpr int kWarpA = 0, kWarpB = 1, kWarpMma = 2, kEpi0 = 4, kConv0 = 8;
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+// D (tensor memory) += A (tensor memory) B (shared memory descriptor)
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %3, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %4, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(b), "r"(accum), "r"(id)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kThreadsP, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, TcJobs J) {
+    extern __shared__ unsigned char smem_raw[];
     __shared__ int s_dead;
+    __shared__ uint32_t s_tmem;
+    unsigned char* smem =
+        reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const Layout L{J.bn, J.nraw, J.nb};
     const uint32_t sbase = smem_u32(smem);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kTslot);
-    const int bn = J.bn, K = J.K;
+    const int bn = J.bn, K = J.K, NA = J.na;
     const int nk = (K + kBK - 1) / kBK;   // K chunks per tile
     const int cpr = J.kacc / kBK;         // K chunks per accumulation range
     const int nr = (nk + cpr - 1) / cpr;  // ranges per tile
     const int ntn = (J.N + bn - 1) / bn;
-    const int T = J.tile0[J.nseg] * ntn;  // tiles (< 2^31, checked by the launcher)
+    const int nrt = J.tile0[J.nseg];      // row tiles
+    const int T = nrt * ntn;              // tiles (< 2^31, checked by the launcher)
     const int my_tiles = T > int(blockIdx.x) ? (T - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
+    const int C = my_tiles * nk;          // chunks of this CTA
+    const int nbu = nk <= L.nb ? nk : L.nb;  // B stages in use: chunk kc keeps stage kc when K fits
+    // barriers: raw_full[nraw], raw_empty[nraw], ta_full[na], ta_empty[na], b_full[nb], b_empty[nb],
+    // acc_full[2], acc_empty[2], fin
+    const uint32_t raw_full = sbase + L.bar0(), raw_empty = raw_full + 8 * L.nraw, ta_full = raw_empty + 8 * L.nraw,
+                   ta_empty = ta_full + 8 * NA, b_full = ta_empty + 8 * NA, b_empty = b_full + 8 * L.nb,
+                   acc_full = b_empty + 8 * L.nb, acc_empty = acc_full + 16, fin = acc_empty + 16;
 
     if (tid == 0) {
         s_dead = 0;
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init_n(sbase + kBarFull + 8 * i, kProdWarps);
-            mbar_init_n(sbase + kBarEmpty + 8 * i, 1);
+        for (int i = 0; i < L.nraw; ++i) {
+            mbar_init_n(raw_full + 8 * i, 1);
+            mbar_init_n(raw_empty + 8 * i, 4);
+        }
+        for (int i = 0; i < NA; ++i) {
+            mbar_init_n(ta_full + 8 * i, 4);
+            mbar_init_n(ta_empty + 8 * i, 1);
+        }
+        for (int i = 0; i < L.nb; ++i) {
+            mbar_init_n(b_full + 8 * i, 1);
+            mbar_init_n(b_empty + 8 * i, 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init_n(sbase + kBarAccF + 8 * i, 1);
-            mbar_init_n(sbase + kBarAccE + 8 * i, 4);
+            mbar_init_n(acc_full + 8 * i, 1);
+            mbar_init_n(acc_empty + 8 * i, 4);
         }
+        mbar_init_n(fin, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
                      "r"(J.tmem_cols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -214,211 +246,238 @@ __global__ void __maxnreg__(128) tc_gemm_kernel(TcJobs J) {  // 13 warps: 4 shar
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tslot);
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(&s_tmem);
+    const uint32_t ta0 = tmem + uint32_t(2 * bn);  // first A stage column
     volatile int* dead = &s_dead;
-    // the shared flag read warp-uniformly (every lane of the warp takes the same branch)
     auto wdead = [&]() { return __any_sync(0xffffffffu, *dead != 0); };
 
-    // tile number (within this CTA's sequence) -> segment, first row, row end, first column; tile
-    // counts fit 32 bits (the launcher checks), and the callers advance tile by tile
-    auto tile_of = [&](int lt, int& seg, long long& m0, long long& rend, int& n0) {
+    // tile number (within this CTA's sequence) -> segment, first row, row end, N tile.  With
+    // J.nmajor the row tiles of one N tile are consecutive (a CTA keeps its N tile, and so its B,
+    // over many row tiles); otherwise the N tiles of one row tile are.
+    auto tile_of = [&](int lt, int& seg, long long& m0, long long& rend, int& nt) {
         const int t = int(blockIdx.x) + lt * int(gridDim.x);
-        const int rt = t / ntn;
-        n0 = (t - rt * ntn) * bn;
+        int rt;
+        if (J.nmajor) {
+            nt = t / nrt;
+            rt = t - nt * nrt;
+        } else {
+            rt = t / ntn;
+            nt = t - rt * ntn;
+        }
         seg = 0;
         while (seg + 1 < J.nseg && rt >= J.tile0[seg + 1]) ++seg;
         m0 = J.row0[seg] + (long long)(rt - J.tile0[seg]) * kBM;
         rend = J.row0[seg] + J.rows[seg];
     };
 
-    if (warp < kProdWarps) {
-        // ---------------------------------------------------------------- producers
-        // Chunks in order (tile by tile, K chunks within a tile); the load cursor runs five chunks
-        // ahead of the store cursor (a ring of six register buffers), both advanced incrementally.
-        // Lane 0 of warp 0 also brings the chunk's pre-split B tile into the stage by one bulk
-        // copy, counted on the stage's "full" barrier with the eight warps' arrivals.
-        const int C = my_tiles * nk;  // chunks of this CTA
-        const int ptid = tid;         // 0 .. 255
-        int l_lt = 0, l_kc = 0, l_seg = 0, l_n0 = 0;
-        long long l_m0 = 0, l_rend = 0;
-        if (my_tiles > 0) tile_of(0, l_seg, l_m0, l_rend, l_n0);
-        auto load_next = [&](Chunk& ch) {
-            if (l_lt >= my_tiles) return;
-            const int k0 = l_kc * kBK;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                // a quarter-warp covers 8 rows at one k group: its 16-byte stores fill one core
-                // matrix (conflict-free), and each row's 64 bytes are read by 4 lanes of the warp
-                const int idx = ptid + 256 * j;
-                const int r = ((idx >> 5) << 3) | (idx & 7), kq = ((idx >> 3) & 3) * 4;
-                const long long row = l_m0 + r;
-                ch.a[j] = ld4(J.A + row * J.lda + (k0 + kq), row < l_rend && k0 + kq < K);
+    if (warp == kWarpA) {
+        // ---------------------------------------------------------------- A producer (TMA)
+        if (lane == 0) {
+            int q = 0;
+            for (int lt = 0; lt < my_tiles && !*dead; ++lt) {
+                int seg, nt;
+                long long m0, rend;
+                tile_of(lt, seg, m0, rend, nt);
+                for (int kc = 0; kc < nk; ++kc, ++q) {
+                    const int s = q % L.nraw;
+                    if (q >= L.nraw && !mbar_wait(raw_empty + 8 * s, uint32_t((q / L.nraw) - 1) & 1u)) {
+                        *dead = 1;
+                        break;
+                    }
+                    if (*dead) break;
+                    mbar_arrive_tx(raw_full + 8 * s, kRawBytes);
+                    tma_load_2d(sbase + s * kRawBytes, &tmA, kc * kBK, int(m0), raw_full + 8 * s);
+                }
             }
-            if (++l_kc == nk) {
-                l_kc = 0;
-                if (++l_lt < my_tiles) tile_of(l_lt, l_seg, l_m0, l_rend, l_n0);
-            }
-        };
-        // store cursor: the B tile of the chunk being stored
-        int s_lt = 0, s_kc = 0, s_seg = 0, s_n0 = 0;
-        long long s_m0 = 0, s_rend = 0;
-        if (my_tiles > 0) tile_of(0, s_seg, s_m0, s_rend, s_n0);
-        int s = 0;
-        uint32_t ph = 0;  // use count of stage s, mod 2 (the parity its "empty" barrier completes)
-        auto step = [&](int c, Chunk& cur, Chunk& fut) {
-            if (c >= C || wdead()) return;
-            load_next(fut);
-            if (c >= kStages && !__all_sync(0xffffffffu, mbar_wait(sbase + kBarEmpty + 8 * s, ph ^ 1u))) {
-                *dead = 1;
-                return;
-            }
-            const uint32_t full = sbase + kBarFull + 8 * s;
-            if (ptid == 0) {
-                const size_t bt = ((size_t(s_seg) * ntn + s_n0 / bn) * nk + s_kc) * size_t(kTcBTile);
-                mbar_expect_tx_only(full, kTcBTile);
-                bulk_g2s(sbase + s * kStageBytes + 2 * kTileBytes, static_cast<const unsigned char*>(J.bpack) + bt,
-                         kTcBTile, full);
-            }
-            unsigned char* st = smem + s * kStageBytes;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int idx = ptid + 256 * j;
-                const int r = ((idx >> 5) << 3) | (idx & 7), kq = ((idx >> 3) & 3) * 4;
-                store_k4(st, st + kTileBytes, r, kq, cur.a[j]);
-            }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive1(full);
-            if (++s == kStages) {
-                s = 0;
-                ph ^= 1u;
-            }
-            if (++s_kc == nk) {
-                s_kc = 0;
-                if (++s_lt < my_tiles) tile_of(s_lt, s_seg, s_m0, s_rend, s_n0);
-            }
-        };
-        Chunk b0, b1, b2, b3, b4, b5;
-        load_next(b0);
-        load_next(b1);
-        load_next(b2);
-        load_next(b3);
-        load_next(b4);
-        for (int c = 0; c < C && !wdead(); c += 6) {
-            step(c, b0, b5);
-            step(c + 1, b1, b0);
-            step(c + 2, b2, b1);
-            step(c + 3, b3, b2);
-            step(c + 4, b4, b3);
-            step(c + 5, b5, b4);
+            // copies still in flight land before the CTA can leave (only waits when a role gave up)
+            if (*dead)
+                for (int k = max(0, q - L.nraw); k < q; ++k)
+                    mbar_wait(raw_full + 8 * (k % L.nraw), uint32_t(k / L.nraw) & 1u);
         }
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kWarpB) {
+        // ---------------------------------------------------------------- B producer (bulk copy)
+        if (lane == 0) {
+            const uint32_t bb = uint32_t(L.b_bytes());
+            long long held[4] = {-1, -1, -1, -1};  // the tile each stage holds (-1: none)
+            int q = 0, issued = 0;
+            for (int lt = 0; lt < my_tiles && !*dead; ++lt) {
+                int seg, nt;
+                long long m0, rend;
+                tile_of(lt, seg, m0, rend, nt);
+                for (int kc = 0; kc < nk; ++kc, ++q) {
+                    const int s = q % nbu;
+                    if (q >= nbu && !mbar_wait(b_empty + 8 * s, uint32_t((q / nbu) - 1) & 1u)) {
+                        *dead = 1;
+                        break;
+                    }
+                    if (*dead) break;
+                    const long long id = ((long long)seg * ntn + nt) * nk + kc;
+                    if (held[s] == id) {
+                        mbar_arrive1(b_full + 8 * s);  // already in place
+                    } else {
+                        held[s] = id;
+                        mbar_arrive_tx(b_full + 8 * s, bb);
+                        bulk_g2s(sbase + L.b0() + s * bb, static_cast<const unsigned char*>(J.bpack) + size_t(id) * bb, bb,
+                                 b_full + 8 * s);
+                        issued = q + 1;
+                    }
+                }
+            }
+            if (*dead)
+                for (int k = max(0, issued - nbu); k < issued; ++k) mbar_wait(b_full + 8 * (k % nbu), uint32_t(k / nbu) & 1u);
+        }
+    } else if (warp >= kConv0) {
+        // ---------------------------------------------------------------- converters
+        // thread = tile row (its warp's TMEM lane quadrant); the row's 32 raw values are read from
+        // the swizzled stage, split, and written as 32 hi and 32 lo columns of the A stage
+        const int row = 32 * (warp & 3) + lane;
+        const uint32_t tq = uint32_t(32 * (warp & 3)) << 16;
+        const unsigned char* rbase = smem + (row >> 3) * 1024 + (row & 7) * 128;
+        for (int q = 0; q < C && !wdead(); ++q) {
+            const int r = q % L.nraw, a = q % NA;
+            bool ok = mbar_wait(raw_full + 8 * r, uint32_t(q / L.nraw) & 1u);
+            if (ok && q >= NA) ok = mbar_wait(ta_empty + 8 * a, uint32_t((q / NA) - 1) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) {
+                *dead = 1;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 v = *reinterpret_cast<const float4*>(rbase + r * kRawBytes + (((c ^ row) & 7) << 4));
+                const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t h = tf32_rna(x[j]);
+                    hi[4 * c + j] = h;
+                    lo[4 * c + j] = tf32_rna(x[j] - __uint_as_float(h));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(raw_empty + 8 * r);  // the raw stage has been read
+            const uint32_t col = ta0 + uint32_t(a * 64);
+            tmem_st32(tq + col, hi);
+            tmem_st32(tq + col + 32, lo);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(ta_full + 8 * a);
+        }
+    } else if (warp == kWarpMma) {
         // ---------------------------------------------------------------- MMA issue
         if (lane == 0) {
             const uint32_t id = idesc(bn);
-            int s = 0, q = 0;
-            uint32_t ph = 0;  // parity of the stage's current use
+            int q = 0, qa = 0;
             for (int lt = 0; lt < my_tiles && !*dead; ++lt) {
-                for (int r = 0; r < nr && !*dead; ++r, ++q) {
-                    const int b = q & 1;
-                    const int v = q >> 1;
-                    if (v > 0 && !mbar_wait(sbase + kBarAccE + 8 * b, uint32_t(v - 1) & 1u)) {
+                for (int rr = 0; rr < nr && !*dead; ++rr, ++qa) {
+                    const int b = qa & 1, v = qa >> 1;
+                    if (v > 0 && !mbar_wait(acc_empty + 8 * b, uint32_t(v - 1) & 1u)) {
                         *dead = 1;
                         break;
                     }
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t d = tmem + uint32_t(b * bn);
-                    const int k1 = min(nk, (r + 1) * cpr);
-                    for (int kc = r * cpr; kc < k1; ++kc) {
-                        if (!mbar_wait(sbase + kBarFull + 8 * s, ph)) {
+                    const int k1 = min(nk, (rr + 1) * cpr);
+                    for (int kc = rr * cpr; kc < k1; ++kc, ++q) {
+                        const int a = q % NA, sb = q % nbu;
+                        if (!mbar_wait(ta_full + 8 * a, uint32_t(q / NA) & 1u) ||
+                            !mbar_wait(b_full + 8 * sb, uint32_t(q / nbu) & 1u)) {
                             *dead = 1;
                             break;
                         }
                         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        const uint32_t st = sbase + s * kStageBytes;
+                        const uint32_t ah = ta0 + uint32_t(a * 64), al = ah + 32;
+                        const uint32_t bh = sbase + L.b0() + sb * L.b_bytes(), bl = bh + bn * 128;
 #pragma unroll
                         for (int ks = 0; ks < kBK / 8; ++ks) {
-                            const uint32_t ko = ks * 256;
-                            const uint64_t ah = sdesc(st + ko), al = sdesc(st + kTileBytes + ko);
-                            const uint64_t bh = sdesc(st + 2 * kTileBytes + ko), bl = sdesc(st + 3 * kTileBytes + ko);
-                            mma_tf32(d, al, bh, id, (kc == r * cpr && ks == 0) ? 0u : 1u);
-                            mma_tf32(d, ah, bl, id, 1u);
-                            mma_tf32(d, ah, bh, id, 1u);
+                            const uint32_t ko = ks * 32;
+                            mma_tf32_ta(d, al + ks * 8, sdesc(bh + ko), id, (kc == rr * cpr && ks == 0) ? 0u : 1u);
+                            mma_tf32_ta(d, ah + ks * 8, sdesc(bl + ko), id, 1u);
+                            mma_tf32_ta(d, ah + ks * 8, sdesc(bh + ko), id, 1u);
                         }
-                        tc_commit(sbase + kBarEmpty + 8 * s);  // the stage is free once these MMAs are done
-                        if (++s == kStages) {
-                            s = 0;
-                            ph ^= 1u;
-                        }
+                        // the stages are free once these MMAs are done
+                        tc_commit(ta_empty + 8 * a);
+                        tc_commit(b_empty + 8 * sb);
                     }
                     if (*dead) break;
-                    tc_commit(sbase + kBarAccF + 8 * b);  // the range's accumulator is complete
+                    tc_commit(acc_full + 8 * b);  // the range's accumulator is complete
                 }
             }
+            // every issued MMA has finished before the tensor memory is released
+            tc_commit(fin);
+            mbar_wait(fin, 0);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= kEpi0 && warp < kEpi0 + 4) {
         // ---------------------------------------------------------------- epilogue
-        // Each thread holds one tile row: 32 columns per TMEM read round (two loads, one wait),
-        // added to the running sums of earlier ranges when K spans several, then written into the
-        // warp's staging rows; after the last range the warp stores its rows row by row.
-        const int ew = warp - kEpiWarp0;  // 0..3 = TMEM lane quadrant
+        const int ew = warp & 3;  // TMEM lane quadrant: this warp may read lanes 32 ew .. + 31
         const uint32_t tl = tmem + (uint32_t(ew * 32) << 16);
-        float* stg = reinterpret_cast<float*>(smem + kStage0) + ew * 32 * kStgPitch;
-        float* myrow = stg + lane * kStgPitch;
-        int q = 0;
-        for (int lt = 0; lt < my_tiles && !wdead(); ++lt) {
-            int seg, n0;
-            long long m0, rend;
-            tile_of(lt, seg, m0, rend, n0);
-            for (int r = 0; r < nr && !wdead(); ++r, ++q) {
-                const int b = q & 1;
-                const bool ok = __all_sync(0xffffffffu, mbar_wait(sbase + kBarAccF + 8 * b, uint32_t(q >> 1) & 1u));
-                if (!ok) *dead = 1;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-#pragma unroll 1
-                for (int cc = 0; cc < bn; cc += 32) {
-                    uint32_t v0[16], v1[16];
-                    tmem_ld16_nw(tl + uint32_t(b * bn + cc), v0);
-                    tmem_ld16_nw(tl + uint32_t(b * bn + cc + 16), v1);
-                    tmem_wait();
-                    float4* dst = reinterpret_cast<float4*>(myrow + cc);
+        float* stg = reinterpret_cast<float*>(smem + L.stg0()) + (warp - kEpi0) * 32 * kStgPitch;
+        float sums[64];
+        int qa = 0;
+        // 32 columns of this warp's 32 rows, staged and stored 128 bytes per row segment
+        auto store32 = [&](const float* v, long long m0, long long rend, int col) {
+            float4* my = reinterpret_cast<float4*>(stg + lane * kStgPitch);
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        float4 a = make_float4(__uint_as_float(v0[4 * x]), __uint_as_float(v0[4 * x + 1]),
-                                               __uint_as_float(v0[4 * x + 2]), __uint_as_float(v0[4 * x + 3]));
-                        float4 c = make_float4(__uint_as_float(v1[4 * x]), __uint_as_float(v1[4 * x + 1]),
-                                               __uint_as_float(v1[4 * x + 2]), __uint_as_float(v1[4 * x + 3]));
-                        if (r > 0) {  // later ranges add onto the staged sums (fixed order)
-                            const float4 pa = dst[x], pc = dst[4 + x];
-                            a = make_float4(pa.x + a.x, pa.y + a.y, pa.z + a.z, pa.w + a.w);
-                            c = make_float4(pc.x + c.x, pc.y + c.y, pc.z + c.z, pc.w + c.w);
-                        }
-                        dst[x] = a;
-                        dst[4 + x] = c;
+            for (int x = 0; x < 8; ++x) my[x] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+            __syncwarp();
+            const int c4 = lane & 7;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int row = 4 * i + (lane >> 3);
+                const long long grow = m0 + ew * 32 + row;
+                if (grow < rend && col + 4 * c4 < J.N)
+                    *reinterpret_cast<float4*>(J.C + grow * J.ldc + col + 4 * c4) =
+                        *reinterpret_cast<const float4*>(stg + row * kStgPitch + 4 * c4);
+            }
+            __syncwarp();
+        };
+        for (int lt = 0; lt < my_tiles && !wdead(); ++lt) {
+            int seg, nt;
+            long long m0, rend;
+            tile_of(lt, seg, m0, rend, nt);
+            const int n0 = nt * bn;
+            for (int rr = 0; rr < nr && !wdead(); ++rr, ++qa) {
+                const int b = qa & 1;
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full + 8 * b, uint32_t(qa >> 1) & 1u));
+                if (!ok) {
+                    *dead = 1;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (nr == 1) {
+                    // one range: each 32-column block leaves as soon as it is read
+                    for (int cc = 0; cc < bn; cc += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tl + uint32_t(b * bn + cc), v);
+                        tmem_wait();
+                        float f[32];
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) f[x] = __uint_as_float(v[x]);
+                        store32(f, m0, rend, n0 + cc);
+                    }
+                } else {
+                    // several ranges (bn = 64): running fp32 sums in registers, in range order
+#pragma unroll
+                    for (int cc = 0; cc < 64; cc += 32) {
+                        uint32_t v[32];
+                        tmem_ld32(tl + uint32_t(b * bn + cc), v);
+                        tmem_wait();
+#pragma unroll
+                        for (int x = 0; x < 32; ++x)
+                            sums[cc + x] = rr == 0 ? __uint_as_float(v[x]) : sums[cc + x] + __uint_as_float(v[x]);
                     }
                 }
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive1(sbase + kBarAccE + 8 * b);  // the accumulator may be reused
-                if (r == nr - 1 && ok) {
-                    // the warp's 32 staged rows leave with coalesced 16-byte stores: one full row per
-                    // instruction for BN = 128, two rows for BN = 64
-                    __syncwarp();
-                    const int w4 = min(bn, J.N - n0) / 4;  // 16-byte groups per row
-                    const int lpr = bn / 4;                // lanes per row
-                    const int sub = lane / lpr, g = lane - sub * lpr;
-                    for (int i = sub; i < 32; i += 32 / lpr) {
-                        const long long row = m0 + ew * 32 + i;
-                        if (row < rend && g < w4)
-                            *reinterpret_cast<float4*>(J.C + row * J.ldc + n0 + 4 * g) =
-                                *reinterpret_cast<const float4*>(stg + i * kStgPitch + 4 * g);
-                    }
-                    __syncwarp();
+                if (lane == 0) mbar_arrive1(acc_empty + 8 * b);  // the accumulator may be reused
+                if (nr > 1 && rr == nr - 1) {
+                    store32(sums, m0, rend, n0);
+                    store32(sums + 32, m0, rend, n0 + 32);
                 }
             }
         }
-
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -426,53 +485,76 @@ __global__ void __maxnreg__(128) tc_gemm_kernel(TcJobs J) {  // 13 warps: 4 shar
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(J.tmem_cols) : "memory");
 }
 
-}  // namespace
-
-namespace {
 // B_s[k][n] (any strides) -> the pre-split tiles of J.bpack: one block per (segment, N tile,
-// K chunk), zeros outside [0, K) x [0, N) and beyond BN columns.
+// K chunk), hi tile then lo tile, each bn rows (n) x 32 k in the 128-byte-swizzled K-major layout;
+// zeros outside [0, K) x [0, N).
 __global__ void __launch_bounds__(256) tc_pack_b(TcJobs J, int ntn, int nk) {
     const int kc = blockIdx.x % nk, nt = (blockIdx.x / nk) % ntn, seg = blockIdx.x / (nk * ntn);
-    unsigned char* t = static_cast<unsigned char*>(J.bpack) + size_t(blockIdx.x) * kTcBTile;
+    const int bn = J.bn;
+    unsigned char* t = static_cast<unsigned char*>(J.bpack) + size_t(blockIdx.x) * (2 * bn * 128);
     const float* Bs = J.B + (long long)seg * J.b_seg_stride;
-    const int n0 = nt * J.bn, k0 = kc * kBK;
-    for (int e = threadIdx.x; e < 128 * kBK; e += 256) {
-        const int n = J.b_kcont ? (e >> 4) : (e & 127), k = J.b_kcont ? (e & 15) : (e >> 7);
+    const int n0 = nt * bn, k0 = kc * kBK;
+    for (int e = threadIdx.x; e < bn * kBK; e += 256) {
+        const int n = J.b_kcont ? (e / kBK) : (e % bn), k = J.b_kcont ? (e % kBK) : (e / bn);
         float v = 0.f;
-        if (n < J.bn && n0 + n < J.N && k0 + k < J.K) v = Bs[(long long)(k0 + k) * J.sbk + (long long)(n0 + n) * J.sbn];
-        uint32_t h, l;
-        split3(v, h, l);
-        const uint32_t o = toff(n, k);
+        if (n0 + n < J.N && k0 + k < J.K) v = Bs[(long long)(k0 + k) * J.sbk + (long long)(n0 + n) * J.sbn];
+        const uint32_t h = tf32_rna(v);
+        const uint32_t l = tf32_rna(v - __uint_as_float(h));
+        const uint32_t o = sw128(n, k);
         *reinterpret_cast<uint32_t*>(t + o) = h;
-        *reinterpret_cast<uint32_t*>(t + kTileBytes + o) = l;
+        *reinterpret_cast<uint32_t*>(t + bn * 128 + o) = l;
     }
 }
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime (the library does not link
+// the driver library).
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
 }  // namespace
 
-// Tile shape of a product: N tiles of 128 columns (64 when N <= 64, or when K spans several
-// ranges, whose sums then fit the registers), K summed in ranges of at most kKacc.
-namespace {
-constexpr int kKacc = 256;
-}  // namespace
-
+// Tile shape of a product: N tiles of 128 columns for wide C (N > 256, one K range), else 64
+// (whose several K-range sums then fit the registers); K summed in ranges of at most kKacc.
+// Tensor memory (512 columns): the two accumulators, then as many 64-column A stages as fit.
+// Shared memory: B stages enough to hold a short K, the rest raw A stages (up to 8).
 bool tc_gemm_configure(TcJobs& J) {
     const int nk = (J.K + kBK - 1) / kBK;
     const int nr = (J.K + kKacc - 1) / kKacc;  // ranges
     const int per = (nk + nr - 1) / nr;        // chunks per range
     J.kacc = per * kBK;
-    J.bn = (J.N <= 64 || nr > 1) ? 64 : kBNmax;
-    J.tmem_cols = 2 * J.bn;  // two accumulators: the MMAs fill one while the epilogue drains the other
-    return true;
+    J.bn = (J.N > 256 && nr == 1) ? kBNmax : 64;
+    J.tmem_cols = 512;
+    J.na = (512 - 2 * J.bn) / 64;
+    J.nb = J.bn == kBNmax ? 3 : 4;
+    const Layout none{J.bn, 0, J.nb};
+    const int room = kSmemMax - 1024 /* static shared memory */ - none.total();
+    J.nraw = std::min(8, room / kRawBytes);
+    return J.nraw >= 2;
 }
 
 // Requirements of the tensor-core path: 16-byte aligned base pointers and row strides that keep
-// every row 16-byte aligned (the loads are 4-vectors); widths that are multiples of 4; K small
-// enough that its accumulators fit the tensor memory.
+// every row 16-byte aligned (TMA and 16-byte stores); widths that are multiples of 4; room for
+// the pre-split B tiles.
 bool tc_gemm_supported(const TcJobs& J) {
     auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (!al(J.A) || !al(J.C) || !J.B || !J.bpack || !al(J.bpack) || J.nseg < 1 || J.nseg > kTcMaxSeg || J.N % 4 || J.N < 1)
         return false;
     if (J.K < 1 || J.K % 4 || J.lda % 4 || J.ldc % 4 || J.b_seg_stride % 4) return false;
+    if (!encoder()) return false;
     TcJobs T = J;
     return tc_gemm_configure(T) && tc_gemm_workspace(T) <= J.bpack_bytes;
 }
@@ -481,34 +563,57 @@ size_t tc_gemm_workspace(const TcJobs& J) {
     TcJobs T = J;
     tc_gemm_configure(T);
     const size_t ntn = size_t((T.N + T.bn - 1) / T.bn), nk = size_t((T.K + kBK - 1) / kBK);
-    return size_t(T.nseg) * ntn * nk * kTcBTile;
+    return size_t(T.nseg) * ntn * nk * size_t(2 * T.bn * 128);
 }
 
 cudaError_t launch_tc_gemm(TcJobs& J, cudaStream_t st) {
-    static int sms = 0;  // the attribute is per function, not per call; one resident CTA per SM
+    if (!tc_gemm_configure(J) || tc_gemm_workspace(J) > J.bpack_bytes) return cudaErrorInvalidValue;
+    const EncodeTiled enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const Layout L{J.bn, J.nraw, J.nb};
+    static int sms = 0;  // one resident CTA per SM; the attribute is per function
+    static int attr_bytes = 0;
     if (!sms) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemP);
         int dev = 0;
-        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    if (!tc_gemm_configure(J) || tc_gemm_workspace(J) > J.bpack_bytes) return cudaErrorInvalidValue;
-    long long t = 0;
+    if (L.total() > attr_bytes) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total());
+        if (e != cudaSuccess) return e;
+        attr_bytes = L.total();
+    }
+    long long t = 0, extent = 0;
     for (int s = 0; s < J.nseg; ++s) {
         J.tile0[s] = int(t);
         t += (J.rows[s] + kBM - 1) / kBM;
+        extent = std::max(extent, J.row0[s] + J.rows[s]);
     }
     J.tile0[J.nseg] = int(t);
     const long long tiles = t * ((J.N + J.bn - 1) / J.bn);
     if (tiles == 0) return cudaSuccess;
-    if (tiles > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    if (tiles > 0x7FFFFFFF || extent > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    // A as a 2-D tensor [extent rows][K] (row pitch lda), boxes of 128 rows x 32 values (128 bytes,
+    // the swizzle span); rows and K beyond the extent read as zeros
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {cuuint64_t(J.K), cuuint64_t(extent)};
+    const cuuint64_t strides[1] = {cuuint64_t(J.lda) * 4u};
+    const cuuint32_t box[2] = {uint32_t(kBK), uint32_t(kBM)};
+    const cuuint32_t es[2] = {1u, 1u};
+    if (enc(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(J.A), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     const int ntn = (J.N + J.bn - 1) / J.bn, nk = (J.K + kBK - 1) / kBK;
     tc_pack_b<<<unsigned(J.nseg * ntn * nk), 256, 0, st>>>(J, ntn, nk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned grid = unsigned(std::min<long long>(tiles, sms));
-    tc_gemm_kernel<<<grid, kThreadsP, kSmemP, st>>>(J);
+    // a CTA keeps one N tile in either order when the grid is a multiple of the N tiles (and then
+    // the CTAs on one row tile run together, sharing its A through L2); otherwise N-major order
+    J.nmajor = (grid % unsigned(ntn)) != 0 ? 1 : 0;
+    tc_gemm_kernel<<<grid, kThreadsP, L.total(), st>>>(tm, J);
     return cudaGetLastError();
 }
 
