@@ -242,11 +242,12 @@ __global__ void __launch_bounds__(256) seg_dM(int U, int W, SegTab tab, const T*
     }
 }
 
-// fp32 form of seg_dM for 4-aligned widths: block tile 64 u x 128 w, 256 threads with 4 x 8
-// outputs each read as 16-byte vectors (three shared-memory loads per 32 FMAs), rows in steps of 32
-// through a four-stage cp.async ring (one block per SM: the deep ring hides the HBM latency of
-// the G rows).  Each step's fp32 sums are added with Kahan compensation (the compensation carries
-// the chunk to fp32-round-off accuracy without fp64 registers), and the chunk's sum
+// fp32 form of seg_dM for 4-aligned widths.  Block tile 64 u x 128 w; warp tu (of 8) owns
+// u = u0 + 8 tu + i (i < 8), lane tw owns w = w0 + 4 tw + j (j < 4): per row the warp's lanes
+// share two 16-byte reads of A (broadcast) and read G as one contiguous 512-byte row (no bank
+// conflicts), 32 FMAs per three shared-memory reads.  Rows in steps of 32 through a four-stage
+// cp.async ring.  Each step's fp32 sums are added with Kahan compensation (which carries the
+// chunk to fp32-round-off accuracy without fp64 registers), and the chunk's sum
 // (sum - lost part) is stored as fp64, like seg_dM.
 constexpr int kFU = 64, kFW = 128, kFR = 32, kFS = 4;
 constexpr int kFStage = kFR * (kFU + kFW);  // floats per stage
@@ -263,16 +264,16 @@ __global__ void __launch_bounds__(256, 1) seg_dM_f32(int U, int W, SegTab tab, c
     const int pi = blockIdx.y, ch = blockIdx.z;
     const int64_t rbeg = tab.row0[pi] + int64_t(ch) * kRowChunk;
     const int64_t rend = min(tab.row0[pi] + tab.rows[pi], rbeg + kRowChunk);
-    const int tid = threadIdx.x, tu = tid >> 4, tw = tid & 15;  // outputs u0 + 4 tu + i, w0 + 8 tw + j
-    float ks[4][8], kc[4][8];
+    const int tid = threadIdx.x, tw = tid & 31, tu = tid >> 5;
+    float ks[8][4], kc[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ks[i][j] = kc[i][j] = 0.f;
+        for (int j = 0; j < 4; ++j) ks[i][j] = kc[i][j] = 0.f;
     const int nsteps = rbeg < rend ? int((rend - rbeg + kFR - 1) / kFR) : 0;
-    // step st: 32 rows of A (16 vectors per row) and of G (32 vectors per row) into its stage; rows
-    // past the chunk and columns past the width read as zeros.  Every thread commits one group per
-    // call, empty past the last step, so that the group count stays uniform.
+    // step st: 32 rows of A (16 vectors per row) and of G (32 vectors per row) into its stage;
+    // rows past the chunk and columns past the width read as zeros.  Every thread commits one
+    // group per call, empty past the last step, so that the group count stays uniform.
     auto load = [&](int st) {
         if (st < nsteps) {
             float* sa = fsm + (st % kFS) * kFStage;
@@ -301,31 +302,31 @@ __global__ void __launch_bounds__(256, 1) seg_dM_f32(int U, int W, SegTab tab, c
     for (int st = 0; st < kFS - 1; ++st) load(st);
     for (int st = 0; st < nsteps; ++st) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kFS - 2) : "memory");
-        __syncthreads();        // step st has landed for every thread; step st - 1's stage is free
-        load(st + kFS - 1);     // into the stage step st - 1 used
+        __syncthreads();     // step st has landed for every thread; step st - 1's stage is free
+        load(st + kFS - 1);  // into the stage step st - 1 used
         const float* sa = fsm + (st % kFS) * kFStage;
         const float* sg = sa + kFR * kFU;
-        float acc[4][8];
+        float acc[8][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
 #pragma unroll 8
         for (int k = 0; k < kFR; ++k) {
-            const float4 a = *reinterpret_cast<const float4*>(sa + k * kFU + 4 * tu);
-            const float4 b0 = *reinterpret_cast<const float4*>(sg + k * kFW + 8 * tw);
-            const float4 b1 = *reinterpret_cast<const float4*>(sg + k * kFW + 8 * tw + 4);
-            const float av[4] = {a.x, a.y, a.z, a.w};
-            const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            const float4 a0 = *reinterpret_cast<const float4*>(sa + k * kFU + 8 * tu);
+            const float4 a1 = *reinterpret_cast<const float4*>(sa + k * kFU + 8 * tu + 4);
+            const float4 b = *reinterpret_cast<const float4*>(sg + k * kFW + 4 * tw);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 const float y = acc[i][j] - kc[i][j];
                 const float t = ks[i][j] + y;
                 kc[i][j] = (t - ks[i][j]) - y;
@@ -335,21 +336,26 @@ __global__ void __launch_bounds__(256, 1) seg_dM_f32(int U, int W, SegTab tab, c
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     double* pr = part + (size_t(ch) * tab.n + pi) * size_t(U) * W;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int u = u0 + 4 * tu + i;
+    for (int i = 0; i < 8; ++i) {
+        const int u = u0 + 8 * tu + i;
         if (u >= U) continue;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int w = w0 + 8 * tw + j;
+        for (int j = 0; j < 4; ++j) {
+            const int w = w0 + 4 * tw + j;
             if (w < W) pr[size_t(u) * W + w] = double(ks[i][j]) - double(kc[i][j]);
         }
     }
 }
 
-// the dynamic shared memory of the fp32 form (above the 48 KB default), set once per process
-cudaError_t seg_dM_f32_attr() {
-    static cudaError_t e = cudaFuncSetAttribute(seg_dM_f32, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
-    return e;
+// Launch of the fp32 form; its dynamic shared memory (above the 48 KB default) is set once per
+// process.
+cudaError_t launch_dM_f32(int U, int W, const SegTab& tab, unsigned nseg, unsigned nch, const float* A, const float* G,
+                          double* part, cudaStream_t st) {
+    static const cudaError_t e0 = cudaFuncSetAttribute(seg_dM_f32, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+    if (e0 != cudaSuccess) return e0;
+    const unsigned t = unsigned(((U + kFU - 1) / kFU) * ((W + kFW - 1) / kFW));
+    seg_dM_f32<<<dim3(t, nseg, nch), 256, kFSmem, st>>>(U, W, tab, A, G, part);
+    return cudaGetLastError();
 }
 
 // the fp32 form takes 16-byte vectors of both operands
@@ -549,13 +555,9 @@ cudaError_t launch_dense_reduction(bool f64, int64_t rows, int Mr, int Nc, const
     tab.rows[0] = rows;
     const int64_t nch = (rows + kRowChunk - 1) / kRowChunk;
     if (!f64 && dM_f32_ok(Mr, Nc, A, G)) {
-        cudaError_t e0;
-        const unsigned t2 = unsigned(((Mr + kFU - 1) / kFU) * ((Nc + kFW - 1) / kFW));
-        if ((e0 = seg_dM_f32_attr()) != cudaSuccess) return e0;
-        seg_dM_f32<<<dim3(t2, 1u, unsigned(nch)), 256, kFSmem, st>>>(Mr, Nc, tab, static_cast<const float*>(A),
-                                                                static_cast<const float*>(G), static_cast<double*>(ws));
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        cudaError_t e0 = launch_dM_f32(Mr, Nc, tab, 1u, unsigned(nch), static_cast<const float*>(A),
+                                       static_cast<const float*>(G), static_cast<double*>(ws), st);
+        if (e0 != cudaSuccess) return e0;
         return launch_column_sum(ws, nch, int64_t(Mr) * Nc, C, f64, st);
     }
     const unsigned tiles = unsigned(((Mr + kDT - 1) / kDT) * ((Nc + kDT - 1) / kDT));
@@ -649,10 +651,9 @@ cudaError_t launch_mix_bwd(const Plan& p, int64_t N, int W, const void* in, cons
         const unsigned tiles = unsigned(((p.U + kDT - 1) / kDT) * ((W + kDT - 1) / kDT));
         dim3 grid(tiles, unsigned(p.P), unsigned(C));
         if (!f64 && dM_f32_ok(p.U, W, inT, gT)) {
-            const unsigned t2 = unsigned(((p.U + kFU - 1) / kFU) * ((W + kFW - 1) / kFW));
-            if ((e = seg_dM_f32_attr()) != cudaSuccess) return e;
-            seg_dM_f32<<<dim3(t2, unsigned(p.P), unsigned(C)), 256, kFSmem, st>>>(
-                p.U, W, tab, static_cast<const float*>(inT), static_cast<const float*>(gT), static_cast<double*>(part));
+            if ((e = launch_dM_f32(p.U, W, tab, unsigned(p.P), unsigned(C), static_cast<const float*>(inT),
+                                   static_cast<const float*>(gT), static_cast<double*>(part), st)) != cudaSuccess)
+                return e;
         } else if (f64)
             seg_dM<double><<<grid, 256, 0, st>>>(p.U, W, tab, static_cast<const double*>(inT),
                                                   static_cast<const double*>(gT), static_cast<double*>(part));
