@@ -9,8 +9,9 @@
 // split that truncated hi instead leaves a 13-bit lo whose truncation costs 2^-20 per product,
 // which long reductions visibly accumulate).  Accumulation is fp32 in tensor memory.
 //
-// Persistent kernel, one CTA per SM looping over 128 x BN tiles of C (BN = 128 for wide C, else 64),
-// with warp roles:
+// Persistent kernel, one CTA per SM looping over 128 x BN tiles of C (BN = 128, or 64 for narrow C
+// or long K), with warp roles (an MMA costs about 60 ns up to N = 128 and 66 ns at N = 256 on
+// GB300 when its operands change, so wide tiles pay):
 //   warp 0      A producer: one TMA load per 32-wide K chunk of a 128-row tile (raw fp32, 128-byte
 //               swizzled K-major rows) into a ring of A stages;
 //   warp 1      B producer: B is pre-split once per call into hi and lo tiles in the MMA's layout
@@ -527,7 +528,7 @@ EncodeTiled encoder() {
 
 }  // namespace
 
-// Tile shape of a product: N tiles of 128 columns for wide C (N > 256, one K range), else 64
+// Tile shape of a product: N tiles of 128 columns when N >= 128 and K is one range, else 64
 // (whose several K-range sums then fit the registers); K summed in ranges of at most kKacc.
 // Tensor memory (512 columns): the two accumulators, then as many 64-column A stages as fit.
 // Shared memory: B stages enough to hold a short K, the rest raw A stages (up to 8).
@@ -536,7 +537,7 @@ bool tc_gemm_configure(TcJobs& J) {
     const int nr = (J.K + kKacc - 1) / kKacc;  // ranges
     const int per = (nk + nr - 1) / nr;        // chunks per range
     J.kacc = per * kBK;
-    J.bn = (J.N > 256 && nr == 1) ? kBNmax : 64;
+    J.bn = (J.N >= 128 && nr == 1) ? kBNmax : 64;
     J.tmem_cols = 512;
     J.na = (512 - 2 * J.bn) / 64;
     J.nb = J.bn == kBNmax ? 3 : 4;
