@@ -226,7 +226,11 @@ struct BwdLayout {  // element offsets inside the block's shared memory
     int w_sm;        // W (as given) staged at offset 0 when nonzero
 };
 
-template <typename T, int TE>
+// REG: every layer has at most kThreads 4 x 4 blocks of dW and there are at most kRegLayers
+// layers, so each thread keeps its blocks' compensated sums in registers over all its tiles
+// (written once at the end) instead of reloading them from the block's scratch row per tile.
+constexpr int kRegLayers = 3;
+template <typename T, int TE, bool REG>
 __global__ void __launch_bounds__(kThreads, 1) radial_hidden_bwd_kernel(long long E, const T* __restrict__ r, T r_cut,
                                                                         int p_env, RadialNet net, BwdLayout L,
                                                                         const T* __restrict__ Wg, int n_w,
@@ -254,6 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1) radial_hidden_bwd_kernel(long lon
     const T d1 = p * (p + 1) * (p + 2) / 2;  // f'(s) = -d1 s^(p-1) + 2 d1 s^p - d1 s^(p+1)
     T* const accb = acc + (size_t)blockIdx.x * n_w * 2;
     bool first = true;
+    T rs[kRegLayers][4][4], rc[kRegLayers][4][4];  // REG: this thread's dW block per layer (sum, lost part)
+    if (REG) {
+#pragma unroll
+        for (int l = 0; l < kRegLayers; ++l)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) rs[l][i][j] = rc[l][i][j] = T(0);
+    }
     for (long long t0 = (long long)blockIdx.x * TE; t0 < E; t0 += (long long)gridDim.x * TE) {
         // ---- forward: a_0 = enveloped basis (rows padded to a multiple of 4 with zeros)
         const int nbp = (nb + 3) / 4 * 4;
@@ -318,50 +331,79 @@ __global__ void __launch_bounds__(kThreads, 1) radial_hidden_bwd_kernel(long lon
                 g[i] *= s + a * (T(1) - s);
             }
             __syncthreads();
-            // dW_l += a_(l-1)^T dz_l: 4 x 4 blocks (k, j) per thread, four edges per partial
+            // dW_l += a_(l-1)^T dz_l: 4 x 4 blocks (k, j) per thread, sixteen edges per partial.  The
+            // edge groups are visited starting at jb (mod TE/4) so that the lanes of a warp, which
+            // differ in jb, read different shared-memory banks (a fixed order per thread).
             const T* ain = S + L.act[l - 1];
-            for (int b = tid; b < (hinp / 4) * (hout / 4); b += kThreads) {
-                const int kb = b / (hout / 4), jb = b - kb * (hout / 4);
-                T s[4][4], c[4][4];
+            auto block = [&](int kb, int jb, T (&s)[4][4], T (&c)[4][4]) {
+                // groups of (up to) 16 edges summed in the working precision, each group's sum added
+                // with compensation
+                constexpr int G4 = TE / 4 < 4 ? TE / 4 : 4;
+                for (int e0 = 0; e0 < TE / 4; e0 += G4) {
+                    T v[4][4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                    for (int i = 0; i < 4; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int k = 4 * kb + i;
-                        const size_t o = (size_t(L.w_off[l]) + size_t(k) * hout + 4 * jb + j) * 2;
-                        const bool ok = k < hin && !first;
-                        s[i][j] = ok ? accb[o] : T(0);
-                        c[i][j] = ok ? accb[o + 1] : T(0);
-                    }
-                for (int e4 = 0; e4 < TE / 4; ++e4) {
-                    Q4<T> av[4], dv[4];
+                        for (int j = 0; j < 4; ++j) v[i][j] = T(0);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        av[i] = lds4(ain + (4 * kb + i) * TE + 4 * e4);
-                        dv[i] = lds4(g + (4 * jb + i) * TE + 4 * e4);
+                    for (int e = e0; e < e0 + G4; ++e) {
+                        const int e4 = (e + jb) & (TE / 4 - 1);
+                        Q4<T> av[4], dv[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            av[i] = lds4(ain + (4 * kb + i) * TE + 4 * e4);
+                            dv[i] = lds4(g + (4 * jb + i) * TE + 4 * e4);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                v[i][j] = fma(av[i].a, dv[j].a, v[i][j]);
+                                v[i][j] = fma(av[i].b, dv[j].b, v[i][j]);
+                                v[i][j] = fma(av[i].c, dv[j].c, v[i][j]);
+                                v[i][j] = fma(av[i].d, dv[j].d, v[i][j]);
+                            }
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
 #pragma unroll
+                        for (int j = 0; j < 4; ++j) kahan(s[i][j], c[i][j], v[i][j]);
+                }
+            };
+            if (REG) {
+                const int b = tid;
+                if (b < (hinp / 4) * (hout / 4)) {
+#pragma unroll
+                    for (int ll = 0; ll < kRegLayers; ++ll)
+                        if (ll == l - 1) block(b / (hout / 4), b % (hout / 4), rs[ll], rc[ll]);
+                }
+            } else {
+                for (int b = tid; b < (hinp / 4) * (hout / 4); b += kThreads) {
+                    const int kb = b / (hout / 4), jb = b - kb * (hout / 4);
+                    T s[4][4], c[4][4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            T v = av[i].a * dv[j].a;
-                            v = fma(av[i].b, dv[j].b, v);
-                            v = fma(av[i].c, dv[j].c, v);
-                            v = fma(av[i].d, dv[j].d, v);
-                            kahan(s[i][j], c[i][j], v);
+                            const int k = 4 * kb + i;
+                            const size_t o = (size_t(L.w_off[l]) + size_t(k) * hout + 4 * jb + j) * 2;
+                            const bool ok = k < hin && !first;
+                            s[i][j] = ok ? accb[o] : T(0);
+                            c[i][j] = ok ? accb[o + 1] : T(0);
+                        }
+                    block(kb, jb, s, c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int k = 4 * kb + i;
+                            if (k < hin) {
+                                const size_t o = (size_t(L.w_off[l]) + size_t(k) * hout + 4 * jb + j) * 2;
+                                accb[o] = s[i][j];
+                                accb[o + 1] = c[i][j];
+                            }
                         }
                 }
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int k = 4 * kb + i;
-                        if (k < hin) {
-                            const size_t o = (size_t(L.w_off[l]) + size_t(k) * hout + 4 * jb + j) * 2;
-                            accb[o] = s[i][j];
-                            accb[o + 1] = c[i][j];
-                        }
-                    }
             }
             // g_(l-1) = dz_l W_l^T: 4 edges x 4 inputs per thread
             const T* WT = S + L.wt + L.wt_off[l];
@@ -409,9 +451,31 @@ __global__ void __launch_bounds__(kThreads, 1) radial_hidden_bwd_kernel(long lon
         __syncthreads();
         first = false;
     }
-    // a block without any tile still owns its (zero) row of pairs
-    if (first)
+    if (REG) {  // this thread's blocks (zeros for a block without any tile)
+        for (int l = 1; l <= nl; ++l) {
+            const int hin = net.widths[l - 1], hout = net.widths[l], hinp = (hin + 3) / 4 * 4;
+            const int b = tid;
+            if (b >= (hinp / 4) * (hout / 4)) continue;
+            const int kb = b / (hout / 4), jb = b % (hout / 4);
+#pragma unroll
+            for (int ll = 0; ll < kRegLayers; ++ll) {
+                if (ll != l - 1) continue;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int k = 4 * kb + i;
+                        if (k < hin) {
+                            const size_t o = (size_t(L.w_off[l]) + size_t(k) * hout + 4 * jb + j) * 2;
+                            accb[o] = rs[ll][i][j];
+                            accb[o + 1] = rc[ll][i][j];
+                        }
+                    }
+            }
+        }
+    } else if (first) {  // a block without any tile still owns its (zero) row of pairs
         for (int i = tid; i < 2 * n_w; i += kThreads) accb[i] = T(0);
+    }
 }
 
 // out[i] = sum over blocks b, in order, of (sum - lost part) of entry i, in fp64
@@ -480,7 +544,10 @@ template <typename T, int TE>
 cudaError_t launch_bwd_t(int64_t E, const void* r, double r_cut, int p_env, const RadialNet& net, const BwdLayout& L,
                          const void* W, const void* dh, void* dr, void* dW, void* ws, size_t smem, int blocks,
                          cudaStream_t st) {
-    auto k = radial_hidden_bwd_kernel<T, TE>;
+    bool reg = net.n_layers <= kRegLayers;
+    for (int l = 1; l <= net.n_layers; ++l)
+        reg = reg && ((net.widths[l - 1] + 3) / 4) * (net.widths[l] / 4) <= kThreads;
+    auto k = reg ? radial_hidden_bwd_kernel<T, TE, true> : radial_hidden_bwd_kernel<T, TE, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     const int n_w = weight_count(net);
