@@ -245,13 +245,27 @@ __global__ void __launch_bounds__(256) seg_dM(int U, int W, SegTab tab, const T*
 // fp32 form of seg_dM for 4-aligned widths.  Block tile 64 u x 128 w; warp tu (of 8) owns
 // u = u0 + 8 tu + i (i < 8), lane tw owns w = w0 + 4 tw + j (j < 4): per row the warp's lanes
 // share two 16-byte reads of A (broadcast) and read G as one contiguous 512-byte row (no bank
-// conflicts), 32 FMAs per three shared-memory reads.  Rows in steps of 32 through a four-stage
+// conflicts), 32 FMAs (16 paired) per three shared-memory reads.  Rows in steps of 32 through a four-stage
 // cp.async ring.  Each step's fp32 sums are added with Kahan compensation (which carries the
 // chunk to fp32-round-off accuracy without fp64 registers), and the chunk's sum
 // (sum - lost part) is stored as fp64, like seg_dM.
 constexpr int kFU = 64, kFW = 128, kFR = 32, kFS = 4;
 constexpr int kFStage = kFR * (kFU + kFW);  // floats per stage
 constexpr int kFSmem = kFS * kFStage * 4;
+__device__ __forceinline__ unsigned long long f2pack(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(unsigned long long v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+// (a0, a1) * (b0, b1) + (c0, c1), each half rounded as a scalar fma
+__device__ __forceinline__ unsigned long long f2fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
     const unsigned d = unsigned(__cvta_generic_to_shared(dst));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
@@ -306,23 +320,31 @@ __global__ void __launch_bounds__(256, 1) seg_dM_f32(int U, int W, SegTab tab, c
         load(st + kFS - 1);  // into the stage step st - 1 used
         const float* sa = fsm + (st % kFS) * kFStage;
         const float* sg = sa + kFR * kFU;
-        float acc[8][4];
+        // step sums of (u 2i, u 2i + 1) pairs with paired FMAs (the same per-half rounding as
+        // scalar fmaf): half the FMA instructions
+        unsigned long long acc2[4][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+            for (int j = 0; j < 4; ++j) acc2[i][j] = 0ull;
 #pragma unroll 8
         for (int k = 0; k < kFR; ++k) {
             const float4 a0 = *reinterpret_cast<const float4*>(sa + k * kFU + 8 * tu);
             const float4 a1 = *reinterpret_cast<const float4*>(sa + k * kFU + 8 * tu + 4);
             const float4 b = *reinterpret_cast<const float4*>(sg + k * kFW + 4 * tw);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[4] = {b.x, b.y, b.z, b.w};
+            const unsigned long long ap[4] = {f2pack(a0.x, a0.y), f2pack(a0.z, a0.w), f2pack(a1.x, a1.y),
+                                              f2pack(a1.z, a1.w)};
+            const unsigned long long bp[4] = {f2pack(b.x, b.x), f2pack(b.y, b.y), f2pack(b.z, b.z), f2pack(b.w, b.w)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+                for (int j = 0; j < 4; ++j) acc2[i][j] = f2fma(ap[i], bp[j], acc2[i][j]);
         }
+        float acc[8][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) f2unpack(acc2[i][j], acc[2 * i][j], acc[2 * i + 1][j]);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
