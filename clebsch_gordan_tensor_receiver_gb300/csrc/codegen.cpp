@@ -108,6 +108,47 @@ struct Gen {
         return true;
     }
 
+    // Column scales of the d_out row: for each output index k = ooff + m3 of a general path, the
+    // magnitude shared by most CG entries of that (path, m3) column (1 for identity paths).  A
+    // kernel that keeps a receiver's d_out row in registers for all of its edges loads s_k g_k
+    // once per receiver and uses C / s_k, so the column's most common coefficient becomes +-1:
+    // the t row of dw starts without a multiply, and so do the h entries first reached through
+    // such a coefficient.  Set only while emitting such a kernel.
+    mutable const std::vector<double>* colscale = nullptr;
+    double cs(int k) const { return colscale ? (*colscale)[k] : 1.0; }
+    std::vector<double> column_scales() const {
+        std::vector<double> s(P->Do, 1.0);
+        for (const PathInfo& p : P->paths) {
+            if (is_identity(p)) continue;
+            for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3) {
+                std::vector<std::pair<double, int>> mags;  // (magnitude, count) in first-seen order
+                for (const Nz& z : p.nz) {
+                    if (z.m3 != m3) continue;
+                    const double a = std::abs(z.c);
+                    bool found = false;
+                    for (auto& mc : mags)
+                        if (std::abs(mc.first - a) <= 1e-13 * a) { mc.second++; found = true; break; }
+                    if (!found) mags.push_back({a, 1});
+                }
+                int best = -1;
+                for (size_t i = 0; i < mags.size(); ++i)
+                    if (best < 0 || mags[i].second > mags[size_t(best)].second) best = int(i);
+                if (best >= 0) s[size_t(p.ooff + m3)] = mags[size_t(best)].first;
+            }
+        }
+        return s;
+    }
+    // UVU_COL_SCALE=0 (a tuning switch) emits the unscaled form.
+    static bool col_scale_enabled() {
+        const char* e = std::getenv("UVU_COL_SCALE");
+        return !(e && std::atoi(e) == 0);
+    }
+    // d_out value k as loaded: scaled by its column scale when one is in force
+    std::string gload(int k, const std::string& v) const {
+        const double sk = cs(k);
+        return sk == 1.0 ? v : fmt("%s * %s", lit(sk).c_str(), v.c_str());
+    }
+
     std::set<int> x_needed(const std::vector<int>& paths) const {
         std::set<int> s;
         for (int pi : paths) {
@@ -214,18 +255,28 @@ struct Gen {
     void emit_t(Src& S, int pi, const char* qpre = "q", const char* tpre = "t") const {
         const PathInfo& p = P->paths[pi];
         for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3) {
-            bool first = true;
+            std::vector<std::pair<double, std::string>> terms;
             for (const Nz& z : p.nz) {
                 if (z.m3 != m3) continue;
-                const std::string q = fmt("%s_%d_%d", qpre, p.xoff + z.m1, p.yoff + z.m2);
+                terms.push_back({z.c / cs(p.ooff + m3), fmt("%s_%d_%d", qpre, p.xoff + z.m1, p.yoff + z.m2)});
+            }
+            if (colscale)  // a +-1 term first: the row then starts without a multiply
+                for (size_t i = 1; i < terms.size(); ++i)
+                    if (!is_one(terms[0].first) && is_one(terms[i].first)) std::swap(terms[0], terms[i]);
+            bool first = true;
+            for (const auto& tm : terms) {
+                const double c = tm.first;
+                const std::string& q = tm.second;
                 if (first) {
-                    if (is_one(z.c))
-                        S(fmt("%s %s_%d_%d = %s%s;", T.c_str(), tpre, pi, m3, z.c < 0 ? "-" : "", q.c_str()));
+                    if (is_one(c))
+                        S(fmt("%s %s_%d_%d = %s%s;", T.c_str(), tpre, pi, m3, c < 0 ? "-" : "", q.c_str()));
                     else
-                        S(fmt("%s %s_%d_%d = %s * %s;", T.c_str(), tpre, pi, m3, lit(z.c).c_str(), q.c_str()));
+                        S(fmt("%s %s_%d_%d = %s * %s;", T.c_str(), tpre, pi, m3, lit(c).c_str(), q.c_str()));
                     first = false;
+                } else if (colscale && is_one(c)) {
+                    S(fmt("%s_%d_%d %s= %s;", tpre, pi, m3, c < 0 ? "-" : "+", q.c_str()));
                 } else {
-                    S(fmt("%s_%d_%d = fma(%s, %s, %s_%d_%d);", tpre, pi, m3, lit(z.c).c_str(), q.c_str(), tpre, pi, m3));
+                    S(fmt("%s_%d_%d = fma(%s, %s, %s_%d_%d);", tpre, pi, m3, lit(c).c_str(), q.c_str(), tpre, pi, m3));
                 }
             }
             if (first) S(fmt("const %s %s_%d_%d = 0;", T.c_str(), tpre, pi, m3));
@@ -390,7 +441,38 @@ struct Gen {
                         S("}");
                     }
                 }
-                if (want_dy || want_dx) {
+                if ((want_dy || want_dx) && colscale) {
+                    for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3)
+                        S(fmt("const %s a_%d_%d = %s_%d * %s;", T.c_str(), pi, m3, wname, pi, gval(p.ooff + m3).c_str()));
+                    // this path's contributions per h entry; an entry not yet defined takes a +-1
+                    // contribution as its definition when it has one
+                    std::map<std::pair<int, int>, std::vector<std::pair<double, std::string>>> by;
+                    for (const Nz& z : p.nz)
+                        by[{p.xoff + z.m1, p.yoff + z.m2}].push_back({z.c / cs(p.ooff + z.m3), fmt("a_%d_%d", pi, z.m3)});
+                    for (auto& kv : by) {
+                        const int a = kv.first.first, b = kv.first.second;
+                        auto& L = kv.second;
+                        if (!hdef.count({a, b})) {
+                            for (size_t i = 1; i < L.size(); ++i)
+                                if (!is_one(L[0].first) && is_one(L[i].first)) std::swap(L[0], L[i]);
+                        }
+                        for (size_t i = 0; i < L.size(); ++i) {
+                            const double c = L[i].first;
+                            const std::string& av = L[i].second;
+                            if (!hdef.count({a, b})) {
+                                hdef.insert({a, b});
+                                if (is_one(c))
+                                    S(fmt("%s h_%d_%d = %s%s;", T.c_str(), a, b, c < 0 ? "-" : "", av.c_str()));
+                                else
+                                    S(fmt("%s h_%d_%d = %s * %s;", T.c_str(), a, b, lit(c).c_str(), av.c_str()));
+                            } else if (is_one(c)) {
+                                S(fmt("h_%d_%d %s= %s;", a, b, c < 0 ? "-" : "+", av.c_str()));
+                            } else {
+                                S(fmt("h_%d_%d = fma(%s, %s, h_%d_%d);", a, b, lit(c).c_str(), av.c_str(), a, b));
+                            }
+                        }
+                    }
+                } else if (want_dy || want_dx) {
                     for (int m3 = 0; m3 < 2 * p.l3 + 1; ++m3)
                         S(fmt("const %s a_%d_%d = %s_%d * %s;", T.c_str(), pi, m3, wname, pi, gval(p.ooff + m3).c_str()));
                     for (const Nz& z : p.nz) {
@@ -1379,6 +1461,9 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         const int NG = int(P->groups.size());
         dw_accum = R.wsh;
         emit_recv_producer(S, R, "EG", "edge_producer");
+        // d_out rows held in registers for the receiver's edges take column scales
+        const std::vector<double> scales = column_scales();
+        colscale = (!R.gsm && !R.tp && col_scale_enabled()) ? &scales : nullptr;
         for (int g = 0; g < NG; ++g) {
             const std::vector<int>& paths = P->groups[g];
             const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
@@ -1408,7 +1493,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 S.ind++;
                 S("if (!dead) dead = !__all_sync(0xffffffffu, mbar_wait(sbase + EG_GBAR, kg & 1u));");
                 S(fmt("const %s* grow = reinterpret_cast<const %s*>(smem + EG_GBUF) + (uvalid ? u : 0) * UVU_DO;", T.c_str(), T.c_str()));
-                for (int k : outs) S(fmt("gv_%d = grow[%d];", k, k));
+                for (int k : outs) S(fmt("gv_%d = %s;", k, gload(k, fmt("grow[%d]", k)).c_str()));
                 S("if (!dead) {");
                 S.ind++;
                 if (release_mode() != 3) S("__threadfence_block();");
@@ -1422,7 +1507,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 S("}");
             } else {
                 S(fmt("const %s* __restrict__ grow = gout + ((size_t)r * UVU_U + (uvalid ? u : 0)) * UVU_DO;", T.c_str()));
-                for (int k : outs) S(fmt("const %s gv_%d = __ldg(grow + %d);", T.c_str(), k, k));
+                for (int k : outs) S(fmt("const %s gv_%d = %s;", T.c_str(), k, gload(k, fmt("__ldg(grow + %d)", k)).c_str()));
             }
             S(fmt("%s* partbase = reinterpret_cast<%s*>(const_cast<unsigned char*>(smem) + EG_PART);", T.c_str(), T.c_str()));
             S("for (int eb = e0; eb < e1; eb += EG_CH, ++c) {");
@@ -1591,6 +1676,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("}");
             }
         }
+        colscale = nullptr;
         S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, EG_MINB) %s(long long N, const int* __restrict__ off,",
               R.dual ? "uvu_hvp_edge" : R.tp ? (R.wsh ? "uvu_tp_edge_sh" : "uvu_tp_edge") : "uvu_bwd_edge"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
