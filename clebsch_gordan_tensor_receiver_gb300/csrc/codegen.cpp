@@ -115,6 +115,10 @@ struct Gen {
     // the t row of dw starts without a multiply, and so do the h entries first reached through
     // such a coefficient.  Set only while emitting such a kernel.
     mutable const std::vector<double>* colscale = nullptr;
+    // Set while emitting an fp32 edge kernel whose dY and dx contractions use paired FMAs (h
+    // entries of adjacent SH components as one register pair; xb_a = {x_a, x_a}; dxq_a the even
+    // and odd partial sums of dx_a).
+    mutable bool pair_contract = false;
     double cs(int k) const { return colscale ? (*colscale)[k] : 1.0; }
     std::vector<double> column_scales() const {
         std::vector<double> s(P->Do, 1.0);
@@ -139,6 +143,10 @@ struct Gen {
         return s;
     }
     // UVU_COL_SCALE=0 (a tuning switch) emits the unscaled form.
+    static bool pair_contract_enabled() {
+        const char* e = std::getenv("UVU_PAIR_CONTRACT");
+        return !(e && std::atoi(e) == 0);
+    }
     static bool col_scale_enabled() {
         const char* e = std::getenv("UVU_COL_SCALE");
         return !(e && std::atoi(e) == 0);
@@ -217,6 +225,8 @@ struct Gen {
         S("  asm(\"mov.b64 {%0, %1}, %2;\" : \"=f\"(a), \"=f\"(b) : \"l\"(v)); }");
         S("__device__ __forceinline__ unsigned long long uvu_f2mul(unsigned long long a, unsigned long long b) {");
         S("  unsigned long long d; asm(\"mul.rn.f32x2 %0, %1, %2;\" : \"=l\"(d) : \"l\"(a), \"l\"(b)); return d; }");
+        S("__device__ __forceinline__ unsigned long long uvu_f2fma(unsigned long long a, unsigned long long b, unsigned long long c) {");
+        S("  unsigned long long d; asm(\"fma.rn.f32x2 %0, %1, %2, %3;\" : \"=l\"(d) : \"l\"(a), \"l\"(b), \"l\"(c)); return d; }");
     }
 
     // Products q_a_b = xv_a * yv_b used by the non-identity paths in `paths`.
@@ -493,7 +503,32 @@ struct Gen {
                     }
                 }
             }
-            if (want_dy) {
+            if (pair_contract && (want_dy || want_dx)) {
+                // h entries (a, b), (a, b+1) with b even as one register pair: dY's pair (b, b+1)
+                // and dx's even/odd partial sums each take one paired FMA per pair
+                for (int m1 = 0; m1 < d1; ++m1) {
+                    const int a = p0.xoff + m1;
+                    for (int m2 = 0; m2 < d2; ++m2) {
+                        const int b = p0.yoff + m2;
+                        if (!hdef.count({a, b})) continue;
+                        const bool pr = b % 2 == 0 && m2 + 1 < d2 && hdef.count({a, b + 1});
+                        const bool second = b % 2 == 1 && m2 > 0 && hdef.count({a, b - 1});
+                        if (second) continue;
+                        if (pr) {
+                            S(fmt("{ const unsigned long long hp = uvu_f2pack(h_%d_%d, h_%d_%d);", a, b, a, b + 1));
+                            if (want_dy)
+                                S(fmt("  { unsigned long long d = uvu_f2pack(dyp_%d, dyp_%d); d = uvu_f2fma(xb_%d, hp, d); "
+                                      "uvu_f2unpack(d, dyp_%d, dyp_%d); }", b, b + 1, a, b, b + 1));
+                            if (want_dx) S(fmt("  dxq_%d = uvu_f2fma(uvu_f2pack(%s_%d, %s_%d), hp, dxq_%d);", a, yname, b, yname, b + 1, a));
+                            S("}");
+                        } else {
+                            if (want_dy) S(fmt("dyp_%d = fma(%s_%d, h_%d_%d, dyp_%d);", b, xname, a, a, b, b));
+                            if (want_dx) S(fmt("dxp_%d = fma(%s_%d, h_%d_%d, dxp_%d);", a, yname, b, a, b, a));
+                        }
+                    }
+                }
+            }
+            if (want_dy && !pair_contract) {
                 for (int m2 = 0; m2 < d2; ++m2) {
                     const int b = p0.yoff + m2;
                     for (int m1 = 0; m1 < d1; ++m1) {
@@ -502,7 +537,7 @@ struct Gen {
                     }
                 }
             }
-            if (want_dx) {
+            if (want_dx && !pair_contract) {
                 for (int m1 = 0; m1 < d1; ++m1) {
                     const int a = p0.xoff + m1;
                     for (int m2 = 0; m2 < d2; ++m2) {
@@ -1285,6 +1320,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     void emit_fwd_v2(Src& S, const RecvPipe& R) const {
         const int NG = int(P->groups.size());
         emit_recv_producer(S, R, "FW", "fwd_producer");
+        // fp64 plans (bound by the FP64 pipe): the receiver's out row accumulates in column-scaled
+        // form (acc_k = out_k / s_k), written back scaled once per receiver.  The fp32 forwards are
+        // bound by memory, and ptxas gives the larger fp32 ones (MACE-large, wide) more registers
+        // or spills in the scaled form, so they keep the unscaled one.
+        const std::vector<double> scales = column_scales();
+        colscale = (f64 && !R.tp && col_scale_enabled()) ? &scales : nullptr;
         for (int g = 0; g < NG; ++g) {
             const std::vector<int>& paths = P->groups[g];
             const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
@@ -1324,11 +1365,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S.ind--;
             S("}");
             S("if (uvalid) {");
-            for (int k : outs) S(fmt("  orow[%d] = acc_%d;", k, k));
+            for (int k : outs) S(fmt("  orow[%d] = %s;", k, gload(k, fmt("acc_%d", k)).c_str()));
             S("}");
             S.ind--;
             S("}");
         }
+        colscale = nullptr;
         S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, FW_MINB) %s(long long N, const int* __restrict__ off,",
               R.dual ? "uvu_hvp_fwd" : R.tp ? (R.wsh ? "uvu_tp_fwd_sh" : "uvu_tp_fwd") : "uvu_fwd"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
@@ -1463,7 +1505,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         emit_recv_producer(S, R, "EG", "edge_producer");
         // d_out rows held in registers for the receiver's edges take column scales
         const std::vector<double> scales = column_scales();
-        colscale = (!R.gsm && !R.tp && col_scale_enabled()) ? &scales : nullptr;
+        colscale = (!R.tp && col_scale_enabled() && (!R.gsm || R.gst)) ? &scales : nullptr;
         for (int g = 0; g < NG; ++g) {
             const std::vector<int>& paths = P->groups[g];
             const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
@@ -1485,6 +1527,17 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 // d_out row of this channel read from the receiver's staged block at each use
                 S(fmt("const %s* grow = reinterpret_cast<const %s*>(smem + EG_GBUF) + (uvalid ? u : 0) * UVU_DO;", T.c_str(), T.c_str()));
                 S("if (e1 > e0 && !dead) dead = !__all_sync(0xffffffffu, mbar_wait(sbase + EG_GBAR, kg & 1u));");
+                if (colscale) {
+                    // the thread's own row of the block, scaled in place once per receiver (the
+                    // consumers hold the block until the receiver is done)
+                    S("if (e1 > e0 && !dead && uvalid) {");
+                    S.ind++;
+                    S(fmt("%s* gw = const_cast<%s*>(grow);", T.c_str(), T.c_str()));
+                    for (int k : outs)
+                        if (cs(k) != 1.0) S(fmt("gw[%d] = %s;", k, gload(k, fmt("gw[%d]", k)).c_str()));
+                    S.ind--;
+                    S("}");
+                }
             } else if (R.gst) {
                 // d_out row of this channel from the receiver's staged block; the block buffer
                 // is handed back to the producer as soon as the row is in registers
@@ -1530,6 +1583,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             emit_stage_edge_loads(S, R, "EG", xn, yn, paths);
             if (!R.wsh) S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
             for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
+            pair_contract = colscale && !R.dual && !R.gsm && pack_products() && pair_contract_enabled();
+            if (pair_contract)
+                for (int k : xn) {
+                    S(fmt("const unsigned long long xb_%d = uvu_f2pack(xv_%d, xv_%d);", k, k, k));
+                    S(fmt("unsigned long long dxq_%d = 0ull;", k));
+                }
             auto gval = [&R](int k) { return R.gsm ? fmt("grow[%d]", k) : fmt("gv_%d", k); };
             if (R.dual) {
                 // dw(x<-ax) + dw(Y<-aY) through the mixed products; dY(x<-ax) and dx(Y<-aY) with
@@ -1559,6 +1618,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 S.ind--;
                 S("}");
                 emit_bwd_pairs(S, paths, false, true, true, gval);
+            }
+            if (pair_contract) {
+                for (int k : xn) S(fmt("{ float lo, hi; uvu_f2unpack(dxq_%d, lo, hi); dxp_%d += lo + hi; }", k, k));
+                pair_contract = false;
             }
             S("if (dx) {");
             S.ind++;
