@@ -143,6 +143,18 @@ struct Gen {
         return s;
     }
     // UVU_COL_SCALE=0 (a tuning switch) emits the unscaled form.
+    // The plain edge kernel with one-edge stages writes dw and the per-edge dx partials into the
+    // stage it read w and x from (same shapes: [P][U] and [U][D_x]) and one thread moves them to
+    // global memory with two bulk copies per stage: no per-thread global stores (whose register
+    // operands the warps otherwise wait on) and full-line writes.  Measured: wide (U = 256) VJP
+    // 5.89 -> 5.33 ms, MACE-large and fp64 unchanged; MACE-medium (two-edge stages, released
+    // per warp otherwise) 0.777 -> 0.818 ms, so two-edge stages keep the per-thread stores.
+    // UVU_EDGE_BULK_OUT=0 (a tuning switch) keeps them everywhere.
+    static bool edge_bulk_out_enabled() {
+        const char* e = std::getenv("UVU_EDGE_BULK_OUT");
+        return !(e && std::atoi(e) == 0);
+    }
+    mutable bool obulk = false;
     static bool pair_contract_enabled() {
         const char* e = std::getenv("UVU_PAIR_CONTRACT");
         return !(e && std::atoi(e) == 0);
@@ -1009,6 +1021,16 @@ __device__ __forceinline__ void bulk_g2s(unsigned dst, const void* src, unsigned
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+// Bulk copy shared -> global (the async proxy reads [src, src + bytes) of this CTA's shared
+// memory); completion tracked per thread by bulk async-groups.
+__device__ __forceinline__ void bulk_s2g(void* dst, unsigned src, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" :: "l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the source reads of every committed group are done (the shared memory may be reused)
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed group is complete (its global writes performed)
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Asks the memory system to bring [src, src + bytes) into L2 ahead of its use (no completion
 // to wait for; the later bulk copy to shared memory then hits in L2).
 __device__ __forceinline__ void prefetch_l2(const void* src, unsigned bytes) {
@@ -1506,6 +1528,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         // d_out rows held in registers for the receiver's edges take column scales
         const std::vector<double> scales = column_scales();
         colscale = (!R.tp && col_scale_enabled() && (!R.gsm || R.gst)) ? &scales : nullptr;
+        obulk = edge_bulk_out_enabled() && R.ch == 1 && !R.dual && !R.tp && !R.wsh && !R.lastwarp && NG == 1 &&
+                R.xbulk && wbytes() % 16 == 0 && release_mode() != 1;
         for (int g = 0; g < NG; ++g) {
             const std::vector<int>& paths = P->groups[g];
             const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
@@ -1581,7 +1605,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("if (uvalid) {");
             S.ind++;
             emit_stage_edge_loads(S, R, "EG", xn, yn, paths);
-            if (!R.wsh) S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
+            if (obulk)  // dw goes where this thread read its w values, then out with the stage
+                S(fmt("%s* dwe = reinterpret_cast<%s*>(const_cast<unsigned char*>(stg)) + j * (UVU_P * UVU_U) + u;", T.c_str(), T.c_str()));
+            else if (!R.wsh)
+                S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
             for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
             pair_contract = colscale && !R.dual && !R.gsm && pack_products() && pair_contract_enabled();
             if (pair_contract)
@@ -1647,7 +1674,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("}");  // j < ne
             S.ind--;
             S("}");  // j
-            emit_release(S, "EG");
+            if (obulk) {  // the stage goes back to the producer after its outputs have left it
+                if (release_mode() != 3) S("__threadfence_block();");
+                S("asm volatile(\"fence.proxy.async.shared::cta;\" ::: \"memory\");");
+            } else {
+                emit_release(S, "EG");
+            }
             S.ind--;
             S("}");  // !dead
             if (R.lastwarp) {
@@ -1684,6 +1716,18 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 S("}");
             } else {
             S("consumer_sync();");
+            if (obulk) {
+                S("if (tid == 0 && !dead) {");
+                S.ind++;
+                S("const unsigned sst = sbase + st * EG_STAGE;");
+                S(fmt("if (dw) bulk_s2g(dw + (size_t)eb * (UVU_P * UVU_U), sst, (unsigned)ne * %zuu);", wbytes()));
+                S(fmt("if (dxe) bulk_s2g(dxe + (size_t)eb * (UVU_U * UVU_DX), sst + EG_XOFF, (unsigned)ne * %zuu);", xbytes()));
+                S("bulk_commit();");
+                S("bulk_wait_read();");
+                S("mbar_arrive(sbase + EG_BAR + 8u * (EG_NST + st));");
+                S.ind--;
+                S("}");
+            }
             if (NG > 1) {
                 S("if (!dead && dxe) {");
                 S.ind++;
@@ -1756,7 +1800,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("const unsigned sbase = smem_addr(smem);");
         S("const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;");
         S("if (tid == 0) {");
-        S("  for (int i = 0; i < EG_NST; ++i) { mbar_init(sbase + EG_BAR + 8u * i, 1u); mbar_init(sbase + EG_BAR + 8u * (EG_NST + i), " + std::string(empty_count("UVU_NCW", "UVU_NCT")) + "); }");
+        S("  for (int i = 0; i < EG_NST; ++i) { mbar_init(sbase + EG_BAR + 8u * i, 1u); mbar_init(sbase + EG_BAR + 8u * (EG_NST + i), " + std::string(obulk ? "1u" : empty_count("UVU_NCW", "UVU_NCT")) + "); }");
         if (R.gst) S("  mbar_init(sbase + EG_GBAR, 1u); mbar_init(sbase + EG_GBAR + 8u, " + std::string(empty_count("UVU_NCW", "UVU_NCT")) + ");");
         if (R.lastwarp) S("  for (int i = 0; i < EG_NBUF; ++i) reinterpret_cast<unsigned*>(smem + EG_CNT)[i] = 0u;");
         S("  asm volatile(\"fence.mbarrier_init.release.cluster;\" ::: \"memory\");");
@@ -1811,6 +1855,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         if (dacc) flush("++nacc == 16 && (nacc = 0, true)");
         S.ind--;
         S("}");
+        if (obulk) S("if (tid == 0) bulk_wait_all();  // the last stages' outputs are written");
+        obulk = false;
         if (dacc) flush("true");
         if (R.wsh) {  // the block's partial dw [P][U] in fp64 (row blockIdx.x of the caller's workspace)
             S("if (dw && uvalid) {");
@@ -1836,7 +1882,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S("if (dxe) {");
         S.ind++;
         if (NG == 1) {
-            S(T + "* __restrict__ dxer = dxe + ((size_t)e * UVU_U + u) * UVU_DX;");
+            if (obulk)  // where this thread read its x row, then out with the stage
+                S(fmt("%s* dxer = reinterpret_cast<%s*>(const_cast<unsigned char*>(stg) + EG_XOFF) + (j * UVU_U + u) * UVU_DX;",
+                      T.c_str(), T.c_str()));
+            else
+                S(T + "* __restrict__ dxer = dxe + ((size_t)e * UVU_U + u) * UVU_DX;");
             if (!f64 && P->Dx % 4 == 0) {
                 for (int c = 0; c < P->Dx / 4; ++c) {
                     std::string v[4];
