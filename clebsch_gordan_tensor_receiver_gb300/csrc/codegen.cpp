@@ -155,6 +155,16 @@ struct Gen {
         return !(e && std::atoi(e) == 0);
     }
     mutable bool obulk = false;
+    // Set while emitting the one-pass edge kernel that reads d_out from the staged block: each
+    // path's d_out values are read once at the top of its block, two at a time (8- or 16-byte
+    // shared-memory loads at even columns, so only for an even D_out, where every row starts
+    // at an even element offset), into gq_k.  UVU_GSM_VEC=0 (a tuning switch) reads each value
+    // where it is used.
+    mutable bool gsm_vec = false;
+    static bool gsm_vec_enabled() {
+        const char* e = std::getenv("UVU_GSM_VEC");
+        return !(e && std::atoi(e) == 0);
+    }
     static bool pair_contract_enabled() {
         const char* e = std::getenv("UVU_PAIR_CONTRACT");
         return !(e && std::atoi(e) == 0);
@@ -433,6 +443,20 @@ struct Gen {
             for (int pi : pp) {
                 const PathInfo& p = P->paths[pi];
                 S(fmt("// path %d: (%d,%d,%d)", pi, p.l1, p.l2, p.l3));
+                if (gsm_vec) {
+                    const int d3 = 2 * p.l3 + 1;
+                    const std::string T2 = f64 ? "double2" : "float2";
+                    for (int m3 = 0; m3 < d3; ++m3) {
+                        const int k = p.ooff + m3;
+                        if (k % 2 == 0 && m3 + 1 < d3) {
+                            S(fmt("const %s gq2_%d = *reinterpret_cast<const %s*>(grow + %d);", T2.c_str(), k, T2.c_str(), k));
+                            S(fmt("const %s gq_%d = gq2_%d.x, gq_%d = gq2_%d.y;", T.c_str(), k, k, k + 1, k));
+                            ++m3;
+                        } else {
+                            S(fmt("const %s gq_%d = grow[%d];", T.c_str(), k, k));
+                        }
+                    }
+                }
                 if (want_dw) {
                     if (is_identity(p)) {
                         const bool scal_x = (p.l1 == 0);
@@ -1616,7 +1640,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                     S(fmt("const unsigned long long xb_%d = uvu_f2pack(xv_%d, xv_%d);", k, k, k));
                     S(fmt("unsigned long long dxq_%d = 0ull;", k));
                 }
-            auto gval = [&R](int k) { return R.gsm ? fmt("grow[%d]", k) : fmt("gv_%d", k); };
+            // pair loads need every row of the staged block to start 8-byte (fp64: 16-byte)
+            // aligned: an even D_out (the block itself starts 16-byte aligned)
+            const bool gq = R.gsm && !R.dual && P->Do % 2 == 0 && R.g_off % 16 == 0 && gsm_vec_enabled();
+            auto gval = [&R, gq](int k) { return R.gsm ? (gq ? fmt("gq_%d", k) : fmt("grow[%d]", k)) : fmt("gv_%d", k); };
             if (R.dual) {
                 // dw(x<-ax) + dw(Y<-aY) through the mixed products; dY(x<-ax) and dx(Y<-aY) with
                 // w; dY and dx with w<-aw
@@ -1634,7 +1661,9 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 // its path's block
                 local_products = true;
                 guard_dw = true;
+                gsm_vec = gq;
                 emit_bwd_pairs(S, paths, true, true, true, gval);
+                gsm_vec = false;
                 local_products = false;
                 guard_dw = false;
             } else {
