@@ -16,6 +16,9 @@
 // k-contiguous operand for the input gradient; dM, a sum over d3 N rows, stays on the compensated
 // CUDA-core kernel, whose fp32 steps of 16 rows keep the elementwise tolerance that the tensor
 // memory's accumulation did not.
+#include <algorithm>
+#include <cstdint>
+
 #include "plan.h"
 #include "tcgemm.h"
 
@@ -27,30 +30,63 @@ constexpr int kMaxPaths = 128;
 // ----------------------------------------------------------------------------- layout copies
 
 // out[b][n][a] = in[n][a][b]  (to component-major: a = channel, b = component), or the inverse
-// out[n][a][b] = in[b][n][a] when INV.  Block = (n, 32 consecutive a); the tile [32][B] passes
-// through shared memory with an odd row pitch.
+// out[n][a][b] = in[b][n][a] when INV.  Block = (node n, TA consecutive channels a0..): the
+// node's [TA][B] slab (contiguous in the node-major layout) passes through shared memory with
+// an odd row pitch, so that the component-major side's accesses (lane = channel, stride pitch)
+// hit distinct banks.  The node-major side is one contiguous run: copied linearly (16-byte
+// vectors when aligned) when B is odd (pitch == B), else row by row (lane = component).
 template <typename T, bool INV>
-__global__ void __launch_bounds__(256) relayout(int64_t N, int A, int B, const T* __restrict__ in, T* __restrict__ out) {
+__global__ void __launch_bounds__(256) relayout(int64_t N, int A, int B, int TA, const T* __restrict__ in,
+                                                T* __restrict__ out) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     T* s = reinterpret_cast<T*>(smem_raw);
     const int pitch = B | 1;
     const int64_t n = blockIdx.x;
-    const int a0 = blockIdx.y * 32;
-    const int na = min(32, A - a0);
+    const int a0 = blockIdx.y * TA;
+    const int na = min(TA, A - a0);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t nm = (n * A + a0) * B;  // node-major start of the slab
+    const int cnt = na * B;
+    constexpr int V = 16 / int(sizeof(T));
+    const bool vec = pitch == B && ((reinterpret_cast<uintptr_t>(INV ? static_cast<const void*>(out + nm)
+                                                                     : static_cast<const void*>(in + nm)) & 15) == 0);
     if (!INV) {
-        for (int e = threadIdx.x; e < na * B; e += 256) s[(e / B) * pitch + e % B] = in[(n * A + a0) * B + e];
+        if (pitch == B) {
+            if (vec) {
+                const int nv = cnt / V;
+                for (int i = tid; i < nv; i += 256)
+                    reinterpret_cast<uint4*>(s)[i] = __ldg(reinterpret_cast<const uint4*>(in + nm) + i);
+                for (int e = nv * V + tid; e < cnt; e += 256) s[e] = in[nm + e];
+            } else {
+                for (int e = tid; e < cnt; e += 256) s[e] = in[nm + e];
+            }
+        } else {
+            for (int a = warp; a < na; a += 8)
+                for (int b = lane; b < B; b += 32) s[a * pitch + b] = in[nm + int64_t(a) * B + b];
+        }
         __syncthreads();
-        for (int e = threadIdx.x; e < B * 32; e += 256) {
-            const int b = e / 32, al = e % 32;
-            if (al < na) out[(int64_t(b) * N + n) * A + a0 + al] = s[al * pitch + b];
+        for (int b = warp; b < B; b += 8) {
+            T* o = out + (int64_t(b) * N + n) * A + a0;
+            for (int a = lane; a < na; a += 32) o[a] = s[a * pitch + b];
         }
     } else {
-        for (int e = threadIdx.x; e < B * 32; e += 256) {
-            const int b = e / 32, al = e % 32;
-            if (al < na) s[al * pitch + b] = in[(int64_t(b) * N + n) * A + a0 + al];
+        for (int b = warp; b < B; b += 8) {
+            const T* q = in + (int64_t(b) * N + n) * A + a0;
+            for (int a = lane; a < na; a += 32) s[a * pitch + b] = q[a];
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < na * B; e += 256) out[(n * A + a0) * B + e] = s[(e / B) * pitch + e % B];
+        if (pitch == B) {
+            if (vec) {
+                const int nv = cnt / V;
+                for (int i = tid; i < nv; i += 256) reinterpret_cast<uint4*>(out + nm)[i] = reinterpret_cast<const uint4*>(s)[i];
+                for (int e = nv * V + tid; e < cnt; e += 256) out[nm + e] = s[e];
+            } else {
+                for (int e = tid; e < cnt; e += 256) out[nm + e] = s[e];
+            }
+        } else {
+            for (int a = warp; a < na; a += 8)
+                for (int b = lane; b < B; b += 32) out[nm + int64_t(a) * B + b] = s[a * pitch + b];
+        }
     }
 }
 
@@ -411,17 +447,22 @@ int64_t max_chunks(const Plan& p, int64_t N) {
 
 template <typename T>
 cudaError_t relayout_launch(int64_t N, int A, int B, bool inv, const void* in, void* out, cudaStream_t st) {
-    const size_t smem = size_t(32) * (B | 1) * sizeof(T);
-    dim3 grid(unsigned(N), unsigned((A + 31) / 32));
+    // channel tile: the whole row of channels when its slab fits 32 KB of shared memory (one
+    // contiguous node-major run per block), else a multiple of 32 channels that does
+    const size_t row = size_t(B | 1) * sizeof(T);
+    int TA = int(std::min<size_t>(size_t(A), std::max<size_t>(32, (32768 / row) / 32 * 32)));
+    if (TA < A) TA = std::max(32, TA / 32 * 32);
+    const size_t smem = size_t(TA) * row;
+    dim3 grid(unsigned(N), unsigned((A + TA - 1) / TA));
     cudaError_t e;
     if (inv) {
         auto k = relayout<T, true>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e == cudaSuccess) k<<<grid, 256, smem, st>>>(N, A, B, static_cast<const T*>(in), static_cast<T*>(out));
+        if (e == cudaSuccess) k<<<grid, 256, smem, st>>>(N, A, B, TA, static_cast<const T*>(in), static_cast<T*>(out));
     } else {
         auto k = relayout<T, false>;
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
-        if (e == cudaSuccess) k<<<grid, 256, smem, st>>>(N, A, B, static_cast<const T*>(in), static_cast<T*>(out));
+        if (e == cudaSuccess) k<<<grid, 256, smem, st>>>(N, A, B, TA, static_cast<const T*>(in), static_cast<T*>(out));
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }

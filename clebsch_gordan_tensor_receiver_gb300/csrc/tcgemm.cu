@@ -489,13 +489,15 @@ __global__ void __launch_bounds__(kThreadsP, 1) tc_gemm_kernel(const __grid_cons
 // B_s[k][n] (any strides) -> the pre-split tiles of J.bpack: one block per (segment, N tile,
 // K chunk), hi tile then lo tile, each bn rows (n) x 32 k in the 128-byte-swizzled K-major layout;
 // zeros outside [0, K) x [0, N).
+// One tile (segment, N tile, K chunk) per blockIdx.x, its bn x 32 elements spread over
+// gridDim.y blocks (a few elements per thread: the tiles are small and latency-bound).
 __global__ void __launch_bounds__(256) tc_pack_b(TcJobs J, int ntn, int nk) {
     const int kc = blockIdx.x % nk, nt = (blockIdx.x / nk) % ntn, seg = blockIdx.x / (nk * ntn);
     const int bn = J.bn;
     unsigned char* t = static_cast<unsigned char*>(J.bpack) + size_t(blockIdx.x) * (2 * bn * 128);
     const float* Bs = J.B + (long long)seg * J.b_seg_stride;
     const int n0 = nt * bn, k0 = kc * kBK;
-    for (int e = threadIdx.x; e < bn * kBK; e += 256) {
+    for (int e = blockIdx.y * 256 + threadIdx.x; e < bn * kBK; e += 256 * gridDim.y) {
         const int n = J.b_kcont ? (e / kBK) : (e % bn), k = J.b_kcont ? (e % kBK) : (e / bn);
         float v = 0.f;
         if (n0 + n < J.N && k0 + k < J.K) v = Bs[(long long)(k0 + k) * J.sbk + (long long)(n0 + n) * J.sbn];
@@ -607,7 +609,7 @@ cudaError_t launch_tc_gemm(TcJobs& J, cudaStream_t st) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int ntn = (J.N + J.bn - 1) / J.bn, nk = (J.K + kBK - 1) / kBK;
-    tc_pack_b<<<unsigned(J.nseg * ntn * nk), 256, 0, st>>>(J, ntn, nk);
+    tc_pack_b<<<dim3(unsigned(J.nseg * ntn * nk), unsigned((J.bn * kBK + 1023) / 1024)), 256, 0, st>>>(J, ntn, nk);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned grid = unsigned(std::min<long long>(tiles, sms));
