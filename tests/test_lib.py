@@ -158,13 +158,14 @@ def test_mixing_host_checks():
     r = lambda b: (b + 255) // 256 * 256
     N, W, U, Do, P = 5000, 64, 128, 55, 13
     fwd, bwd = p.mix_workspace_bytes(N, W)
-    # the tensor-core products' pre-split M tiles: per path, N tile and 16-wide K chunk one
-    # 16,896-byte pair of 128 x 16 TF32 tiles (forward: K = U, N = W; input gradient: K = W, N = U)
-    tile = 2 * 16 * 528
-    assert fwd == r(N * Do * U * 4) + r(N * Do * W * 4) + r(P * 1 * (U // 16) * tile)
+    # the tensor-core products' pre-split M tiles: per path, N tile and 32-wide K chunk one hi and
+    # one lo tile of BN rows x 128 bytes (BN = 128 columns when N >= 128, else 64; forward: K = U,
+    # N = W = 64; input gradient: K = W, N = U = 128)
+    tile = lambda bn: 2 * bn * 128
+    assert fwd == r(N * Do * U * 4) + r(N * Do * W * 4) + r(P * 1 * (U // 32) * tile(64))
     chunks = (7 * N + 1023) // 1024  # widest path (l3 = 3) over 1024-row chunks
     assert bwd == (r(N * Do * W * 4) + 2 * r(N * Do * U * 4) + r(P * U * W * 4) + r(chunks * P * U * W * 8) +
-                   r(P * 1 * (W // 16) * tile))
+                   r(P * 1 * (W // 32) * tile(128)))
     for bad in (0, 5000):
         with pytest.raises(uvu.UVUError):
             p.mix_workspace_bytes(10, bad)
