@@ -1951,9 +1951,15 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
 
     // Sender-stationary sum of the per-edge dx partials over the transposed CSR: one thread per
     // (sender, channel) adds its edges' rows in ascending edge-id order and writes dx once.
+    // UVU_REDUCE_GROUP=n (a tuning switch, 1..16): edges per group of the dx reduction
+    static int reduce_group() {
+        const char* e = std::getenv("UVU_REDUCE_GROUP");
+        const int g = e ? std::atoi(e) : 8;
+        return std::max(1, std::min(16, g));
+    }
     void emit_dx_reduce(Src& S) const {
         const bool vec = !f64 && P->Dx % 4 == 0;
-        S(fmt("extern \"C\" __global__ void __launch_bounds__(256) uvu_bwd_dx_reduce(long long N, const int* __restrict__ soff,"));
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(256, 4) uvu_bwd_dx_reduce(long long N, const int* __restrict__ soff,"));
         S(fmt("    const int* __restrict__ seid, const %s* __restrict__ dxe, %s* __restrict__ dx) {", T.c_str(), T.c_str()));
         S.ind++;
         S("const long long t = (long long)blockIdx.x * 256 + threadIdx.x;");
@@ -1975,15 +1981,26 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             }
             S("}");
         };
+        // groups of kG edges, the next group's edge ids loaded while the current group's rows
+        // are read (one dependent round trip per group instead of two); the rows are added in
+        // ascending edge order, so the sum is the same for any grouping
+        const int kG = reduce_group();
         S("int k = k0;");
+        {
+            std::string ld;
+            for (int i = 0; i < kG; ++i) ld += fmt("%sn%d = (k + %d < k1) ? __ldg(seid + k + %d) : 0", i ? ", " : "int ", i, i, i);
+            S(ld + ";");
+        }
         S("#pragma unroll 1");
-        S("for (; k + 4 <= k1; k += 4) {");
+        S(fmt("for (; k + %d <= k1; k += %d) {", kG, kG));
         S.ind++;
-        S("const int e0 = __ldg(seid + k), e1 = __ldg(seid + k + 1), e2 = __ldg(seid + k + 2), e3 = __ldg(seid + k + 3);");
-        add_row("e0");
-        add_row("e1");
-        add_row("e2");
-        add_row("e3");
+        {
+            std::string cur;
+            for (int i = 0; i < kG; ++i) cur += fmt("%se%d = n%d", i ? ", " : "const int ", i, i);
+            S(cur + ";");
+            for (int i = 0; i < kG; ++i) S(fmt("n%d = (k + %d < k1) ? __ldg(seid + k + %d) : 0;", i, kG + i, kG + i));
+        }
+        for (int i = 0; i < kG; ++i) add_row(fmt("e%d", i));
         S.ind--;
         S("}");
         S("for (; k < k1; ++k) {");
