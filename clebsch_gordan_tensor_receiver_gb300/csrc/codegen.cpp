@@ -119,6 +119,9 @@ struct Gen {
     // entries of adjacent SH components as one register pair; xb_a = {x_a, x_a}; dxq_a the even
     // and odd partial sums of dx_a).
     mutable bool pair_contract = false;
+    // with pair_contract: only dY's contraction paired, {x_a, x_a} formed at each use (no
+    // per-edge pair registers), dx's contraction scalar (the staged-row kernels' register budget)
+    mutable bool pair_dy_only = false;
     double cs(int k) const { return colscale ? (*colscale)[k] : 1.0; }
     std::vector<double> column_scales() const {
         std::vector<double> s(P->Do, 1.0);
@@ -550,7 +553,16 @@ struct Gen {
                         const bool pr = b % 2 == 0 && m2 + 1 < d2 && hdef.count({a, b + 1});
                         const bool second = b % 2 == 1 && m2 > 0 && hdef.count({a, b - 1});
                         if (second) continue;
-                        if (pr) {
+                        if (pr && pair_dy_only) {
+                            if (want_dy)
+                                S(fmt("{ unsigned long long d = uvu_f2pack(dyp_%d, dyp_%d); d = uvu_f2fma(uvu_f2pack(%s_%d, %s_%d), "
+                                      "uvu_f2pack(h_%d_%d, h_%d_%d), d); uvu_f2unpack(d, dyp_%d, dyp_%d); }",
+                                      b, b + 1, xname, a, xname, a, a, b, a, b + 1, b, b + 1));
+                            if (want_dx) {
+                                S(fmt("dxp_%d = fma(%s_%d, h_%d_%d, dxp_%d);", a, yname, b, a, b, a));
+                                S(fmt("dxp_%d = fma(%s_%d, h_%d_%d, dxp_%d);", a, yname, b + 1, a, b + 1, a));
+                            }
+                        } else if (pr) {
                             S(fmt("{ const unsigned long long hp = uvu_f2pack(h_%d_%d, h_%d_%d);", a, b, a, b + 1));
                             if (want_dy)
                                 S(fmt("  { unsigned long long d = uvu_f2pack(dyp_%d, dyp_%d); d = uvu_f2fma(xb_%d, hp, d); "
@@ -1634,8 +1646,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             else if (!R.wsh)
                 S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
             for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
-            pair_contract = colscale && !R.dual && !R.gsm && pack_products() && pair_contract_enabled();
-            if (pair_contract)
+            // staged-row kernels pair only dY's contraction (the full pairing spilled there);
+            // measured: MACE-large VJP 2.560 -> 2.515 ms, wide 5.287 -> 5.185 ms
+            pair_dy_only = R.gsm;
+            pair_contract = colscale && !R.dual && pack_products() && pair_contract_enabled();
+            if (pair_contract && !pair_dy_only)
                 for (int k : xn) {
                     S(fmt("const unsigned long long xb_%d = uvu_f2pack(xv_%d, xv_%d);", k, k, k));
                     S(fmt("unsigned long long dxq_%d = 0ull;", k));
@@ -1675,10 +1690,9 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 S("}");
                 emit_bwd_pairs(S, paths, false, true, true, gval);
             }
-            if (pair_contract) {
+            if (pair_contract && !pair_dy_only)
                 for (int k : xn) S(fmt("{ float lo, hi; uvu_f2unpack(dxq_%d, lo, hi); dxp_%d += lo + hi; }", k, k));
-                pair_contract = false;
-            }
+            pair_contract = pair_dy_only = false;
             S("if (dx) {");
             S.ind++;
             if (!R.xbulk) {
