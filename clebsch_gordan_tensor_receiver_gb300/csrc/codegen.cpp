@@ -1647,9 +1647,11 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 S(T + "* __restrict__ dwe = dw + (size_t)e * (UVU_P * UVU_U) + u;");
             for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
             // staged-row kernels pair only dY's contraction (the full pairing spilled there);
-            // measured: MACE-large VJP 2.560 -> 2.515 ms, wide 5.287 -> 5.185 ms
-            pair_dy_only = R.gsm;
-            pair_contract = colscale && !R.dual && pack_products() && pair_contract_enabled();
+            // measured: MACE-large VJP 2.560 -> 2.515 ms, wide 5.287 -> 5.185 ms.  So do the
+            // double-backward kernels with register-resident rows, in both of their contractions
+            // (MACE-medium 1.487 -> 1.454 ms); with staged rows it spilled there.
+            pair_dy_only = R.gsm || R.dual;
+            pair_contract = colscale && !(R.dual && R.gsm) && pack_products() && pair_contract_enabled();
             if (pair_contract && !pair_dy_only)
                 for (int k : xn) {
                     S(fmt("const unsigned long long xb_%d = uvu_f2pack(xv_%d, xv_%d);", k, k, k));
