@@ -1648,10 +1648,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             for (int k : xn) S(fmt("%s dxp_%d = 0;", T.c_str(), k));
             // staged-row kernels pair only dY's contraction (the full pairing spilled there);
             // measured: MACE-large VJP 2.560 -> 2.515 ms, wide 5.287 -> 5.185 ms.  So do the
-            // double-backward kernels with register-resident rows, in both of their contractions
-            // (MACE-medium 1.487 -> 1.454 ms); with staged rows it spilled there.
+            // double-backward kernels with rows of at most 64 values, in both of their contractions
+            // (MACE-medium 1.487 -> 1.454 ms); with wider rows (MACE-large, wide) it added spills.
             pair_dy_only = R.gsm || R.dual;
-            pair_contract = colscale && !(R.dual && R.gsm) && pack_products() && pair_contract_enabled();
+            pair_contract = colscale && !(R.dual && (R.gsm || P->Do > 64)) && pack_products() && pair_contract_enabled();
             if (pair_contract && !pair_dy_only)
                 for (int k : xn) {
                     S(fmt("const unsigned long long xb_%d = uvu_f2pack(xv_%d, xv_%d);", k, k, k));
