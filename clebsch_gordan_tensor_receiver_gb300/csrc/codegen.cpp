@@ -168,6 +168,14 @@ struct Gen {
         const char* e = std::getenv("UVU_GSM_VEC");
         return !(e && std::atoi(e) == 0);
     }
+    // Words per warp of the dY tile: 32 rows of 16, rows 16..31 shifted by 16 words so that the
+    // two half-warps' column reads fall in opposite bank halves.
+    static constexpr int kDytWords = 528;
+    // UVU_DY_SMEM=0 (a tuning switch) keeps the shuffle transpose-reduce for dY.
+    static bool dy_smem_enabled() {
+        const char* e = std::getenv("UVU_DY_SMEM");
+        return !(e && std::atoi(e) == 0);
+    }
     static bool pair_contract_enabled() {
         const char* e = std::getenv("UVU_PAIR_CONTRACT");
         return !(e && std::atoi(e) == 0);
@@ -1101,6 +1109,10 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         // measured slower (MACE-medium edge kernel 0.897 vs 0.862 ms); the barrier keeps the warps
         // in step over the shared stages.
         bool lastwarp = false;
+        // dY's cross-lane sum through a per-warp shared-memory tile (fp32, 9..16 SH components)
+        // instead of the shuffle transpose-reduce
+        bool dyt = false;
+        size_t dyt_off = 0;
         int nbuf = 2;
         size_t cnt_off = 0;
         size_t tx_per_edge = 0;
@@ -1176,6 +1188,14 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         if (R.gst) R.total += a16(R.gbytes);
         R.dacc_off = R.total;
         if (wsh && with_partials && !f64) R.total += a16(size_t(P->P) * P->U_pad * 8);
+        // measured: MACE-large VJP 2.514 -> 2.442 ms, wide 5.183 -> 5.061 ms; slower on MACE-medium
+        // (edge kernel 0.776 -> 0.790 ms) and in the double backward (1.455 -> 1.527 ms), so only the
+        // plain edge kernels with wide output rows (fp32, D_out > 64) take it
+        R.dyt = with_partials && !f64 && !dual && !tp && P->Do > 64 && P->Dy > 8 && P->Dy <= 16 && dy_smem_enabled();
+        if (R.dyt) {
+            R.dyt_off = R.total;
+            R.total += a16(size_t(ncw) * kDytWords * 4);
+        }
         R.tx_per_edge = wb + (R.xbulk ? xbytes() : 0) + (R.ybulk ? ybytes() : 0);
         // With a receiver block staged, shorter stages keep three blocks resident per SM where
         // the default chunk would leave fewer (more warps beat a longer look-ahead per block).
@@ -1203,6 +1223,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         S(fmt("#define %s_GBAR %zu", pre, R.bar_off + 16 * R.nst));
         S(fmt("#define %s_GBYTES %zu", pre, R.gbytes));
         S(fmt("#define %s_DACC %zu", pre, R.dacc_off));
+        if (R.dyt) S(fmt("#define %s_DYT %zu", pre, R.dyt_off));
         if (R.lastwarp) {
             S(fmt("#define %s_CNT %zu", pre, R.cnt_off));
             S(fmt("#define %s_NBUF %d", pre, R.nbuf));
@@ -1507,6 +1528,52 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     // then one lane per component stores the warp sum into the stage's partial buffer.
     // Values are halved level by level (each lane keeps one half and receives the other half of
     // its xor partner), so D values over 32 lanes take about D shuffles instead of 5 D.
+    // dY's sum over the warp's 32 channels through a shared-memory tile: lane l writes its D
+    // (<= 16) values as row l (four 16-byte stores, the 16-byte groups rotated by (l >> 1) & 3 so
+    // that each quarter-warp's stores hit 32 distinct banks), then lane l sums column l & 15 over
+    // the rows of its half-warp in ascending order (16 loads, conflict-free: the halves' rows
+    // start in opposite bank halves) and the two halves are added by one shuffle.  The order of
+    // the additions is fixed, so dY stays bitwise repeatable.
+    void emit_dy_tile_reduce(Src& S, const std::vector<int>& K, const char* pre) const {
+        const int D = int(K.size());
+        S("{");
+        S.ind++;
+        S(fmt("float* const dyt = reinterpret_cast<float*>(const_cast<unsigned char*>(smem) + %s_DYT) + warp * %d;", pre, kDytWords));
+        S("float4* const trow = reinterpret_cast<float4*>(dyt + lane * 16 + ((lane & 16) ? 16 : 0));");
+        S("const int tsw = (lane >> 1) & 3;");
+        for (int c = 0; c < 4; ++c) {
+            std::string v[4];
+            for (int i = 0; i < 4; ++i) v[i] = (4 * c + i < D) ? fmt("dyp_%d", K[4 * c + i]) : "0.0f";
+            S(fmt("trow[%d ^ tsw] = make_float4(%s, %s, %s, %s);", c, v[0].c_str(), v[1].c_str(), v[2].c_str(), v[3].c_str()));
+        }
+        S("__syncwarp();");
+        S("const int tm = lane & 15, tg = tm >> 2;");
+        S("const float* const tcol = dyt + ((lane & 16) ? 272 : 0) + (tm & 3);");
+        S("const int to0 = (tg ^ 0) << 2, to1 = (tg ^ 1) << 2, to2 = (tg ^ 2) << 2, to3 = (tg ^ 3) << 2;");
+        for (int r = 0; r < 16; ++r) {
+            const int c = (r >> 1) & 3;
+            if (r == 0) S(fmt("float ts = tcol[%d + to%d];", r * 16, c));
+            else S(fmt("ts += tcol[%d + to%d];", r * 16, c));
+        }
+        S("ts += __shfl_xor_sync(0xffffffffu, ts, 16);");
+        S("__syncwarp();");
+        bool contiguous = true;
+        for (int i = 1; i < D; ++i) contiguous = contiguous && K[i] == K[0] + i;
+        std::string comp;
+        if (contiguous) {
+            comp = fmt("%d + tm", K[0]);
+        } else {
+            comp = "-1";
+            for (int i = D - 1; i >= 0; --i) comp = fmt("(tm == %d ? %d : %s)", i, K[i], comp.c_str());
+        }
+        S(fmt("if (lane < %d) part[j * UVU_DY + (%s)] = ts;", D, comp.c_str()));
+        std::set<int> ks(K.begin(), K.end());
+        for (int k = 0; k < P->Dy; ++k)
+            if (!ks.count(k)) S(fmt("if (lane == 0) part[j * UVU_DY + %d] = 0;", k));
+        S.ind--;
+        S("}");
+    }
+
     void emit_dy_warp_reduce(Src& S, const std::vector<int>& K) const {
         const int D = int(K.size());
         int P2 = 1;
@@ -1712,7 +1779,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             S("if (dY) {");
             S.ind++;
             std::vector<int> K(yn.begin(), yn.end());
-            emit_dy_warp_reduce(S, K);
+            if (R.dyt && K.size() > 8) emit_dy_tile_reduce(S, K, "EG");
+            else emit_dy_warp_reduce(S, K);
             S.ind--;
             S("}");
             S.ind--;
