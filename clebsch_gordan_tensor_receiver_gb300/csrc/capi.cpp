@@ -340,7 +340,7 @@ extern "C" uvu_status uvu_conv_bwd_dx_reduce(uvu_plan_t plan, int64_t n_nodes, i
     if (s != UVU_OK) return fail(s, err);
     long long N = n_nodes;
     void* args[] = {&N, &send_offsets, &send_eids, &dx_edge, &dx};
-    const int64_t threads = n_nodes * p->U_pad;
+    const int64_t threads = n_nodes * (p->reduce_per_sender > 0 ? p->reduce_per_sender : p->U_pad);
     const KernelGeom g{256, 256, 0, false, 1};
     UVU_TRY(launch(m->bwd_dx_reduce, 1, m->sm_count, threads, g, args, stream, "uvu_bwd_dx_reduce launch"));
     return ok();

@@ -2041,24 +2041,42 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         const int g = e ? std::atoi(e) : 8;
         return std::max(1, std::min(16, g));
     }
+    // dx[s] = sum over the out-edges e of s, in ascending edge id, of the per-edge partials
+    // dxe[e] (each a row of U x D_x values).  When a row is a whole number of 16-byte vectors
+    // the row is summed as flat vectors, one thread per (sender, vector) (D_x = 9 rows: one
+    // 16-byte load per edge instead of nine scalar ones); otherwise one thread per (sender,
+    // channel) sums its D_x values.  Either way every output value is the same ordered sum.
     void emit_dx_reduce(Src& S) const {
-        const bool vec = !f64 && P->Dx % 4 == 0;
+        const int V = f64 ? 2 : 4;
+        const bool flat = (P->U * P->Dx) % V == 0;
+        const int per = flat ? P->U * P->Dx / V : P->U_pad;
+        P->reduce_per_sender = per;
+        const std::string TV = f64 ? "double2" : "float4";
         S(fmt("extern \"C\" __global__ void __launch_bounds__(256, 4) uvu_bwd_dx_reduce(long long N, const int* __restrict__ soff,"));
         S(fmt("    const int* __restrict__ seid, const %s* __restrict__ dxe, %s* __restrict__ dx) {", T.c_str(), T.c_str()));
         S.ind++;
         S("const long long t = (long long)blockIdx.x * 256 + threadIdx.x;");
-        S("const long long sn = t / UVU_UP;");
-        S("const int u = (int)(t - sn * UVU_UP);");
-        S("if (sn >= N || u >= UVU_U) return;");
+        S(fmt("const long long sn = t / %d;", per));
+        S(fmt("const int c = (int)(t - sn * %d);", per));
+        S(flat ? "if (sn >= N) return;" : "if (sn >= N || c >= UVU_U) return;");
         S("const int k0 = __ldg(soff + sn), k1 = __ldg(soff + sn + 1);");
-        for (int k = 0; k < P->Dx; ++k) S(fmt("%s a_%d = 0;", T.c_str(), k));
+        const int nacc = flat ? V : P->Dx;
+        for (int k = 0; k < nacc; ++k) S(fmt("%s a_%d = 0;", T.c_str(), k));
+        const bool vec = !flat && !f64 && P->Dx % 4 == 0;
         auto add_row = [&](const std::string& e) {
-            S(fmt("{ const %s* __restrict__ row = dxe + ((size_t)(%s) * UVU_U + u) * UVU_DX;", T.c_str(), e.c_str()));
+            if (flat) {
+                S(fmt("{ const %s v = __ldg(reinterpret_cast<const %s*>(dxe + (size_t)(%s) * (UVU_U * UVU_DX)) + c);", TV.c_str(),
+                      TV.c_str(), e.c_str()));
+                if (f64) S("  a_0 += v.x; a_1 += v.y; }");
+                else S("  a_0 += v.x; a_1 += v.y; a_2 += v.z; a_3 += v.w; }");
+                return;
+            }
+            S(fmt("{ const %s* __restrict__ row = dxe + ((size_t)(%s) * UVU_U + c) * UVU_DX;", T.c_str(), e.c_str()));
             if (vec) {
-                for (int c = 0; c < P->Dx / 4; ++c) {
-                    S(fmt("  const float4 v%d = __ldg(reinterpret_cast<const float4*>(row) + %d);", c, c));
-                    S(fmt("  a_%d += v%d.x; a_%d += v%d.y; a_%d += v%d.z; a_%d += v%d.w;", 4 * c, c, 4 * c + 1, c, 4 * c + 2, c,
-                          4 * c + 3, c));
+                for (int q = 0; q < P->Dx / 4; ++q) {
+                    S(fmt("  const float4 v%d = __ldg(reinterpret_cast<const float4*>(row) + %d);", q, q));
+                    S(fmt("  a_%d += v%d.x; a_%d += v%d.y; a_%d += v%d.z; a_%d += v%d.w;", 4 * q, q, 4 * q + 1, q, 4 * q + 2, q,
+                          4 * q + 3, q));
                 }
             } else {
                 for (int k = 0; k < P->Dx; ++k) S(fmt("  a_%d += __ldg(row + %d);", k, k));
@@ -2093,8 +2111,13 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         add_row("e0");
         S.ind--;
         S("}");
-        S(T + "* __restrict__ dxr = dx + ((size_t)sn * UVU_U + u) * UVU_DX;");
-        for (int k = 0; k < P->Dx; ++k) S(fmt("dxr[%d] = a_%d;", k, k));
+        if (flat) {
+            if (f64) S("reinterpret_cast<double2*>(dx + (size_t)sn * (UVU_U * UVU_DX))[c] = make_double2(a_0, a_1);");
+            else S("reinterpret_cast<float4*>(dx + (size_t)sn * (UVU_U * UVU_DX))[c] = make_float4(a_0, a_1, a_2, a_3);");
+        } else {
+            S(T + "* __restrict__ dxr = dx + ((size_t)sn * UVU_U + c) * UVU_DX;");
+            for (int k = 0; k < P->Dx; ++k) S(fmt("dxr[%d] = a_%d;", k, k));
+        }
         S.ind--;
         S("}");
     }

@@ -101,6 +101,7 @@ struct Plan {
     std::vector<PathInfo> paths;
     std::vector<std::vector<int>> groups;  // path ids per register group
     KernelGeom g_fwd, g_edge, g_dx, g_fwd_sender;
+    int reduce_per_sender = 0;  // threads of uvu_bwd_dx_reduce per sender (set by the generator)
     int edge_chunk = 0;  // edges per dY reduction chunk in the edge kernel
     bool pipelined_recv = false, pipelined_dx = false;
     bool staged_ok = false;   // the edge kernel can write per-edge dx partials (staged dx)
