@@ -122,6 +122,31 @@ struct Gen {
     // with pair_contract: only dY's contraction paired, {x_a, x_a} formed at each use (no
     // per-edge pair registers), dx's contraction scalar (the staged-row kernels' register budget)
     mutable bool pair_dy_only = false;
+    // Identity paths (0,l,l) and (l,0,l) in the plain edge kernels: zi_p = sum of +-g x (or g y)
+    // over the path's pairs serves dw (zi_p times the width-1 operand), dY (l2 = 0: w zi_p) or dx
+    // (l1 = 0: w zi_p), and the other gradient takes (w times the width-1 operand) g directly:
+    // no h entries, no a = w g products.  zi_ready: paths whose zi_p is already in scope.
+    mutable bool id_fold = false;
+    mutable std::set<int> zi_ready;
+    static bool id_fold_enabled() {
+        const char* e = std::getenv("UVU_ID_FOLD");
+        return !(e && std::atoi(e) == 0);
+    }
+    template <class GV>
+    void emit_identity_z(Src& S, int pi, GV gval, const char* xname = "xv", const char* yname = "yv") const {
+        const PathInfo& p = P->paths[pi];
+        const bool scal_x = (p.l1 == 0);
+        bool first = true;
+        for (const Nz& z : p.nz) {
+            const std::string other = scal_x ? fmt("%s_%d", yname, p.yoff + z.m2) : fmt("%s_%d", xname, p.xoff + z.m1);
+            const std::string gv = gval(p.ooff + z.m3);
+            if (first)
+                S(fmt("%s zi_%d = %s%s * %s;", T.c_str(), pi, z.c < 0 ? "-" : "", gv.c_str(), other.c_str()));
+            else
+                S(fmt("zi_%d = fma(%s%s, %s, zi_%d);", pi, z.c < 0 ? "-" : "", gv.c_str(), other.c_str(), pi));
+            first = false;
+        }
+    }
     double cs(int k) const { return colscale ? (*colscale)[k] : 1.0; }
     std::vector<double> column_scales() const {
         std::vector<double> s(P->Do, 1.0);
@@ -467,6 +492,30 @@ struct Gen {
                             S(fmt("const %s gq_%d = grow[%d];", T.c_str(), k, k));
                         }
                     }
+                }
+                if (id_fold && is_identity(p)) {
+                    const bool scal_x = (p.l1 == 0);
+                    const std::string x0 = fmt("%s_%d", xname, p.xoff), y0 = fmt("%s_%d", yname, p.yoff);
+                    if (!zi_ready.count(pi)) emit_identity_z(S, pi, gval, xname, yname);
+                    if (want_dw) S(dw_store(pi, fmt("zi_%d * %s", pi, scal_x ? x0.c_str() : y0.c_str())));
+                    if (scal_x) {  // (0, l, l): dx_0 += w zi; dY_m2 += c (x_0 w) g_m3
+                        if (want_dx) S(fmt("dxp_%d = fma(%s_%d, zi_%d, dxp_%d);", p.xoff, wname, pi, pi, p.xoff));
+                        if (want_dy) {
+                            S(fmt("const %s xw_%d = %s * %s_%d;", T.c_str(), pi, x0.c_str(), wname, pi));
+                            for (const Nz& z : p.nz)
+                                S(fmt("dyp_%d = fma(%sxw_%d, %s, dyp_%d);", p.yoff + z.m2, z.c < 0 ? "-" : "", pi,
+                                      gval(p.ooff + z.m3).c_str(), p.yoff + z.m2));
+                        }
+                    } else {  // (l, 0, l): dY_0 += w zi; dx_m1 += c (y_0 w) g_m3
+                        if (want_dy) S(fmt("dyp_%d = fma(%s_%d, zi_%d, dyp_%d);", p.yoff, wname, pi, pi, p.yoff));
+                        if (want_dx) {
+                            S(fmt("const %s yw_%d = %s * %s_%d;", T.c_str(), pi, y0.c_str(), wname, pi));
+                            for (const Nz& z : p.nz)
+                                S(fmt("dxp_%d = fma(%syw_%d, %s, dxp_%d);", p.xoff + z.m1, z.c < 0 ? "-" : "", pi,
+                                      gval(p.ooff + z.m3).c_str(), p.xoff + z.m1));
+                        }
+                    }
+                    continue;
                 }
                 if (want_dw) {
                     if (is_identity(p)) {
@@ -1727,6 +1776,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             // pair loads need every row of the staged block to start 8-byte (fp64: 16-byte)
             // aligned: an even D_out (the block itself starts 16-byte aligned)
             const bool gq = R.gsm && !R.dual && P->Do % 2 == 0 && R.g_off % 16 == 0 && gsm_vec_enabled();
+            id_fold = !R.dual && id_fold_enabled();
             auto gval = [&R, gq](int k) { return R.gsm ? (gq ? fmt("gq_%d", k) : fmt("grow[%d]", k)) : fmt("gv_%d", k); };
             if (R.dual) {
                 // dw(x<-ax) + dw(Y<-aY) through the mixed products; dY(x<-ax) and dx(Y<-aY) with
@@ -1752,12 +1802,19 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
                 guard_dw = false;
             } else {
                 emit_products(S, paths);
+                if (id_fold)  // the identity paths' zi serve dw and the dY / dx below
+                    for (int pi : paths)
+                        if (is_identity(P->paths[pi])) {
+                            emit_identity_z(S, pi, gval);
+                            zi_ready.insert(pi);
+                        }
                 S("if (dw) {");
                 S.ind++;
                 emit_bwd_pairs(S, paths, true, false, false, gval);
                 S.ind--;
                 S("}");
                 emit_bwd_pairs(S, paths, false, true, true, gval);
+                zi_ready.clear();
             }
             if (pair_contract && !pair_dy_only)
                 for (int k : xn) S(fmt("{ float lo, hi; uvu_f2unpack(dxq_%d, lo, hi); dxp_%d += lo + hi; }", k, k));
@@ -1897,6 +1954,7 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
             }
         }
         colscale = nullptr;
+        id_fold = false;
         S(fmt("extern \"C\" __global__ void __launch_bounds__(UVU_NCT + 32, EG_MINB) %s(long long N, const int* __restrict__ off,",
               R.dual ? "uvu_hvp_edge" : R.tp ? (R.wsh ? "uvu_tp_edge_sh" : "uvu_tp_edge") : "uvu_bwd_edge"));
         S(fmt("    const int* __restrict__ src, const %s* __restrict__ x, const %s* __restrict__ Y,", T.c_str(), T.c_str()));
