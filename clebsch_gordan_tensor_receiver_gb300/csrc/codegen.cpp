@@ -1448,12 +1448,13 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     void emit_fwd_v2(Src& S, const RecvPipe& R) const {
         const int NG = int(P->groups.size());
         emit_recv_producer(S, R, "FW", "fwd_producer");
-        // fp64 plans (bound by the FP64 pipe): the receiver's out row accumulates in column-scaled
-        // form (acc_k = out_k / s_k), written back scaled once per receiver.  The fp32 forwards are
-        // bound by memory, and ptxas gives the larger fp32 ones (MACE-large, wide) more registers
-        // or spills in the scaled form, so they keep the unscaled one.
+        // The receiver's out row accumulates in column-scaled form (acc_k = out_k / s_k), written
+        // back scaled once per receiver: fp64 plans (bound by the FP64 pipe; 49.6 -> 37.7 ms) and
+        // fp32 plans with out rows of at most 64 values (MACE-medium 0.340 -> 0.329 ms).  ptxas
+        // gave the wider fp32 forwards (MACE-large, wide) and the double-backward forward more
+        // registers or spills in the scaled form, so they keep the unscaled one.
         const std::vector<double> scales = column_scales();
-        colscale = (f64 && !R.tp && col_scale_enabled()) ? &scales : nullptr;
+        colscale = ((f64 || (!R.dual && P->Do <= 64)) && !R.tp && col_scale_enabled()) ? &scales : nullptr;
         for (int g = 0; g < NG; ++g) {
             const std::vector<int>& paths = P->groups[g];
             const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
