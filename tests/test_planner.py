@@ -165,3 +165,35 @@ def test_tuning_variants_build_on_the_host(env, monkeypatch):
     for k in names:
         m = re.search(rf"Function properties for {k}\n.*?(\d+) bytes spill stores", log, re.S)
         assert m and int(m.group(1)) == 0, (k, log)
+
+
+_EDGE_SWITCHES = [("UVU_COL_SCALE", "0"), ("UVU_PAIR_CONTRACT", "0"), ("UVU_ID_FOLD", "0"),
+                  ("UVU_EDGE_BULK_OUT", "0"), ("UVU_GSM_VEC", "0"), ("UVU_DY_SMEM", "0"),
+                  ("UVU_REDUCE_GROUP", "4")]
+
+
+def test_edge_kernel_forms_present_by_default():
+    """The default emission carries the edge-kernel forms measured faster: on MACE-medium the
+    column-scaled d_out row, the folded identity paths and the paired dY/dx contractions; on
+    MACE-large (staged d_out rows) the paired staged reads, the shared-memory dY tile and the
+    dw / dx-partial bulk copies out of the stage; on both the flat-row dx reduction."""
+    med = uvu.Plan("128x0e+128x1o", "1x0e+1x1o+1x2e+1x3o", 3).source()[0]
+    assert "zi_1" in med and "uvu_f2fma(xb_" in med and "gv_19 = 5.773502" in med
+    assert "reinterpret_cast<float4*>(dx + (size_t)sn * (UVU_U * UVU_DX))[c]" in med
+    large = uvu.Plan("128x0e+128x1o+128x2e", "1x0e+1x1o+1x2e+1x3o", 3).source()[0]
+    assert "gq2_" in large and "EG_DYT" in large and "bulk_s2g(dw" in large and "gw[" in large
+
+
+@pytest.mark.parametrize("name,value", _EDGE_SWITCHES, ids=[n for n, _ in _EDGE_SWITCHES])
+def test_edge_kernel_switches_build_on_the_host(name, value, monkeypatch):
+    """Each edge-kernel tuning switch changes the emitted source of a plan it applies to, and the
+    result still compiles for sm_103a with at most a call-site register save of spill."""
+    irreps = "128x0e+128x1o+128x2e" if name in ("UVU_GSM_VEC", "UVU_DY_SMEM", "UVU_EDGE_BULK_OUT") else "128x0e+128x1o"
+    base = uvu.Plan(irreps, "1x0e+1x1o+1x2e+1x3o", 3).source()[0]
+    monkeypatch.setenv(name, value)
+    p = uvu.Plan(irreps, "1x0e+1x1o+1x2e+1x3o", 3)
+    src, log = p.source()
+    assert src != base
+    for k in ("uvu_bwd_edge", "uvu_bwd_dx_reduce"):
+        m = re.search(rf"Function properties for {k}\n.*?(\d+) bytes spill stores", log, re.S)
+        assert m and int(m.group(1)) <= 64, (k, log)
