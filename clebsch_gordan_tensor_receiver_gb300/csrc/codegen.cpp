@@ -1450,11 +1450,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         emit_recv_producer(S, R, "FW", "fwd_producer");
         // The receiver's out row accumulates in column-scaled form (acc_k = out_k / s_k), written
         // back scaled once per receiver: fp64 plans (bound by the FP64 pipe; 49.6 -> 37.7 ms) and
-        // fp32 plans with out rows of at most 64 values (MACE-medium 0.340 -> 0.329 ms).  ptxas
-        // gave the wider fp32 forwards (MACE-large, wide) and the double-backward forward more
-        // registers or spills in the scaled form, so they keep the unscaled one.
+        // fp32 plans with out rows of at most 64 values (MACE-medium 0.340 -> 0.329 ms; its
+        // double-backward forward 0.835 -> 0.797 ms with 8 bytes of spill).  ptxas gave the wider
+        // fp32 forwards (MACE-large, wide) more registers or spills in the scaled form, so they
+        // keep the unscaled one.
         const std::vector<double> scales = column_scales();
-        colscale = ((f64 || (!R.dual && P->Do <= 64)) && !R.tp && col_scale_enabled()) ? &scales : nullptr;
+        colscale = ((f64 || P->Do <= 64) && !R.tp && col_scale_enabled()) ? &scales : nullptr;
         for (int g = 0; g < NG; ++g) {
             const std::vector<int>& paths = P->groups[g];
             const std::set<int> xn = x_needed(paths), yn = y_needed(paths);
