@@ -2096,6 +2096,12 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
     // Sender-stationary sum of the per-edge dx partials over the transposed CSR: one thread per
     // (sender, channel) adds its edges' rows in ascending edge-id order and writes dx once.
     // UVU_REDUCE_GROUP=n (a tuning switch, 1..16): edges per group of the dx reduction
+    // UVU_REDUCE_MINB=n (a tuning switch): resident 256-thread blocks per SM the dx reduction's
+    // register budget is sized for
+    static int reduce_minb() {
+        const char* e = std::getenv("UVU_REDUCE_MINB");
+        return e ? std::max(1, std::min(8, std::atoi(e))) : 4;
+    }
     static int reduce_group() {
         const char* e = std::getenv("UVU_REDUCE_GROUP");
         const int g = e ? std::atoi(e) : 8;
@@ -2112,7 +2118,8 @@ __device__ __forceinline__ void consumer_sync() { asm volatile("barrier.sync 1, 
         const int per = flat ? P->U * P->Dx / V : P->U_pad;
         P->reduce_per_sender = per;
         const std::string TV = f64 ? "double2" : "float4";
-        S(fmt("extern \"C\" __global__ void __launch_bounds__(256, 4) uvu_bwd_dx_reduce(long long N, const int* __restrict__ soff,"));
+        S(fmt("extern \"C\" __global__ void __launch_bounds__(256, %d) uvu_bwd_dx_reduce(long long N, const int* __restrict__ soff,",
+              reduce_minb()));
         S(fmt("    const int* __restrict__ seid, const %s* __restrict__ dxe, %s* __restrict__ dx) {", T.c_str(), T.c_str()));
         S.ind++;
         S("const long long t = (long long)blockIdx.x * 256 + threadIdx.x;");
