@@ -810,8 +810,8 @@ def main(argv=None):
                    "l2_resident": Bk["fwd"] < 129e6}
             if sp.dtype == "float64":
                 # forward arithmetic from the plan's own CG: 2 flop per non-zero and per output
-                # component (the survey's estimate), and the FP64 operations the generated
-                # forward executes per (edge, channel) when an ncu count for this source exists
+                # component (a nominal count: the generated forward executes fewer operations
+                # where column scales turn coefficients into +-1)
                 nnz = 0
                 for pth in range(Pk):
                     nnz += int((pk.cg(pth) != 0).sum())
