@@ -306,7 +306,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
     const unsigned d = unsigned(__cvta_generic_to_shared(dst));
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
-__global__ void __launch_bounds__(256, 1) seg_dM_f32(int U, int W, SegTab tab, const float* __restrict__ A,
+// Two resident blocks per SM (a 128-register budget; ptxas spills 80 bytes of the 160 it would
+// use at one block): measured faster than one block at 160 registers (radial dW_last 1.61 ->
+// 1.41 ms, mixing dM 0.390 -> 0.365 ms on MACE-medium), the extra warps hiding the ring's waits.
+__global__ void __launch_bounds__(256, 2) seg_dM_f32(int U, int W, SegTab tab, const float* __restrict__ A,
                                                      const float* __restrict__ G, double* __restrict__ part) {
     extern __shared__ __align__(16) float fsm[];  // kFS stages of [kFR][kFU] A rows then [kFR][kFW] G rows
     const int ntw = (W + kFW - 1) / kFW;
